@@ -1,0 +1,392 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE FFN layer, forward + backward, on one GB300 per process.
+
+One step = moe_layer_fwd + moe_layer_bwd over one batch of the workload (default: the
+Mixtral-like layer, T = 8192 tokens = 2 x 4096, d_model 4096, 8 experts top-2, d_ff 14336,
+dropless), with seeded synthetic inputs and random-init weights of that shape resident in HBM.
+
+Prints one JSON line (rank 0):
+  value      tokens/s over all ranks (each rank runs an independent replica: the layer is
+             single-GPU by design, so N > 1 is replicas only, weak scaling)
+  e2e        the same through the C ABI with the step's inputs (x, dy) copied host->device from
+             pinned memory and its results (y, dx) copied back, inside the timed region
+  roofline   the dominant kernel: algorithmic work per launch / its CUDA-event duration, against the
+             measured peak (MEASURED_PEAKS.json)
+  cpu_baseline  the fp64 oracle on a bounded token sample, on this host's cores (rank 0, N = 1)
+
+--impl reference times the oracle alone (on the host cores) on the same workload and metric.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "MoE-layer tokens/s fwd+bwd"
+DESCR = {
+    "tiny": "tiny MoE layer: T=256, d=128, E=8 top-2, d_ff=256, SwiGLU, dropless",
+    "mixtral": "Mixtral-like MoE layer: T=8192 (2x4096), d=4096, E=8 top-2, d_ff=14336, SwiGLU, dropless",
+    "deepseek": "DeepSeek-like MoE layer: T=16384, d=2048, E=64 top-6 renormalised + 2 shared, d_ff=1408",
+    "qwen3": "Qwen3-like MoE layer: T=32768, d=2048, E=128 top-8, d_ff=768, Zipf(1.2)-biased router",
+    "gptoss": "GPT-OSS-like MoE layer: T=65536 (2x32768), d=2880, E=128 top-4, d_ff=2880, capacity 1.25",
+}
+GEMMS = {  # algorithmic FLOPs per launch in units of N*d*f (N = rows the experts see, no pads)
+    "gemm_gate_up_swiglu": 4, "gemm_down": 2, "gemm_bwd_recompute_dgrad_swiglu": 6,
+    "gemm_wgrad": 6, "gemm_dgrad_x": 4,
+}
+HBM_KERNELS = ("dispatch_gather", "combine", "combine_bwd")
+KERNEL_SOURCES = ("gemm.cu", "dispatch.cu", "combine.cu", "route.cu", "ptx.cuh", "common.cuh")
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="mixtral", choices=list(synth.CONFIGS))
+    ap.add_argument("--cpu-tokens", type=int, default=16, help="oracle sample size (tokens)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            p = json.load(fh)
+        return {"hbm": p["hbm_gbs"], "tensor": p["bf16_tflops_sustained"], "tensor_burst": p["bf16_tflops"],
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm": 6800.0, "tensor": 1700.0, "tensor_burst": 1900.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for n in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "mixture_experts_layer_10_gb300", "csrc", n), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on today's sources."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
+            t = json.load(fh)
+        e = t[workload][kernel]
+        if e.get("source_hash") != kernel_source_hash():
+            return None
+        return e["dram_bytes_per_launch"]
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        self.file.flush()
+        rows = []
+        with open(self.file.name) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.file.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(rows[0][2]),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
+
+
+def oracle_sample(inp, cfg, n_tokens, seed=1):
+    """The oracle as it stands on a seeded sample of tokens: routing, expert forward and
+    backward (weight-gradient products included) and the router backward of those tokens."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    toks = np.sort(rng.choice(cfg["T"], size=min(n_tokens, cfg["T"]), replace=False))
+    L = oracle.Layer(inp, cfg)
+    t0 = time.perf_counter()
+    L.token_outputs(toks)
+    return len(toks), time.perf_counter() - t0
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return
+    cfg = synth.CONFIGS[args.workload]
+    inp = synth.make_inputs(cfg, seed=0)
+    times = []
+    n = 0
+    for i in range(args.warmup + args.steps):
+        n, dt = oracle_sample(inp, cfg, args.cpu_tokens, seed=1 + i)
+        if i >= args.warmup:
+            times.append(dt)
+    ms = 1000.0 * sum(times) / len(times)
+    value = n / (ms / 1000.0)
+    cores = os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": DESCR[args.workload], "sample_tokens_per_step": n},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} seeded tokens of the {args.workload} workload per step "
+                                   f"(fwd + bwd incl. weight-gradient products), numpy/OpenBLAS threads"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import mixture_experts_layer_10_gb300 as moe
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    moe.load()
+    cfg = synth.CONFIGS[args.workload]
+    T, d, f, E, k, S = cfg["T"], cfg["d"], cfg["f"], cfg["E"], cfg["k"], cfg["S"]
+    G = E + S
+    inp = synth.make_inputs(cfg, seed=0)
+
+    def dev_bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
+
+    x, dy = dev_bf16(inp["x"]), dev_bf16(inp["dy"])
+    W_r = torch.from_numpy(inp["W_r"]).cuda()
+    b_r = torch.from_numpy(inp["b_r"]).cuda() if inp["b_r"] is not None else None
+    Wg, Wu, Wd = dev_bf16(inp["W_gate"]), dev_bf16(inp["W_up"]), dev_bf16(inp["W_down"])
+    mc = moe.config_from(cfg)
+    buf = moe.Buffers.allocate(mc)
+    y = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    dx = torch.empty_like(y)
+    dW_r = torch.empty(d, E, dtype=torch.float32, device="cuda")
+    db_r = torch.empty(E, dtype=torch.float32, device="cuda") if b_r is not None else None
+    dWg, dWu, dWd = torch.empty_like(Wg), torch.empty_like(Wu), torch.empty_like(Wd)
+
+    def step(xx=x, dyy=dy, yy=y, dxx=dx):
+        moe.moe_layer_fwd(mc, xx, W_r, b_r, Wg, Wu, Wd, yy, buf.saved, buf.ws)
+        moe.moe_layer_bwd(mc, xx, W_r, b_r, Wg, Wu, Wd, buf.saved, dyy, dxx, dW_r, db_r, dWg, dWu, dWd, buf.ws)
+
+    # rows the experts see (no pads): kept routed slots + shared tokens, from one dispatch
+    idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    gates = torch.empty(T, k, dtype=torch.float32, device="cuda")
+    moe.moe_route(mc, x, W_r, b_r, idx, gates)
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    scratch_rows = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    scratch_tok = torch.empty(T * k, dtype=torch.int32, device="cuda")
+    x_perm = torch.empty(buf.rows, d, dtype=torch.bfloat16, device="cuda")
+    moe.moe_dispatch(mc, idx, x, counts, offsets, scratch_rows, scratch_tok, x_perm, buf.ws)
+    status = moe.moe_check_error(buf.ws)
+    if status != 0:
+        raise RuntimeError(f"dispatch failed: {moe.moe_status_string(status)}")
+    counts_h = counts.cpu().numpy()
+    n_kept = int(offsets[-1].item())
+    N = n_kept + S * T
+    load_max_over_mean = float(counts_h.max() / counts_h.mean())
+    del x_perm, scratch_rows, scratch_tok
+
+    for _ in range(args.warmup):
+        step()
+    status = moe.moe_check_error(buf.ws)
+    if status != 0:
+        raise RuntimeError(f"layer failed: {moe.moe_status_string(status)}")
+
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clocks:
+        barrier()
+        torch.cuda.synchronize()
+        moe.moe_profile_enable(True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    prof = moe.moe_profile_read()
+    moe.moe_profile_enable(False)
+    clk = clocks.summary()
+    ms = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+    status = moe.moe_check_error(buf.ws)
+    if status != 0:
+        raise RuntimeError(f"layer failed in the timed region: {moe.moe_status_string(status)}")
+
+    # end to end through the C ABI with host buffers: H2D of x, dy and D2H of y, dx every step
+    x_h = torch.empty(T, d, dtype=torch.bfloat16, pin_memory=True).copy_(x.cpu())
+    dy_h = torch.empty_like(x_h).copy_(dy.cpu())
+    y_h, dx_h = torch.empty_like(x_h), torch.empty_like(x_h)
+    x2, dy2 = torch.empty_like(x), torch.empty_like(dy)
+
+    def e2e_step():
+        x2.copy_(x_h, non_blocking=True)
+        dy2.copy_(dy_h, non_blocking=True)
+        step(x2, dy2)
+        y_h.copy_(y, non_blocking=True)
+        dx_h.copy_(dx, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    barrier()
+    torch.cuda.synchronize()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms_e2e = ev0.elapsed_time(ev1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms_e2e], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+
+    pk = peaks()
+    kernels = {}
+    gemm_flops = gemm_ms = hbm_bytes = hbm_ms = 0.0
+    launches = 0
+    for name, (tot, n) in prof.items():
+        if n == 0:
+            continue
+        launches += n
+        ent = {"ms_per_step": tot / args.steps, "launches": n}
+        if name in GEMMS:
+            work = GEMMS[name] * N * d * f * n     # FLOPs over all launches
+            ent["tflops"] = work / (tot / 1000.0) / 1e12
+            ent["frac_of_measured_peak"] = ent["tflops"] / pk["tensor"]
+            gemm_flops += work
+            gemm_ms += tot
+        elif name in HBM_KERNELS:
+            if name == "dispatch_gather":   # fwd: x once + N rows; bwd: x and dy once + 2N rows
+                work = args.steps * ((T + N) * d * 2 + 2 * (T + N) * d * 2 + 3 * 12 * T * k)
+            elif name == "combine":
+                work = n * ((N + T) * d * 2 + 8 * T * k)
+            else:
+                work = n * ((N + T) * d * 2 + 4 * T * k + 4 * T * E + 4 * d * E)
+            ent["gbs"] = work / (tot / 1000.0) / 1e9
+            ent["frac_of_measured_peak"] = ent["gbs"] / pk["hbm"]
+            hbm_bytes += work
+            hbm_ms += tot
+        kernels[name] = ent
+    dom = max(kernels, key=lambda n: kernels[n]["ms_per_step"])
+    dom_n = kernels[dom]["launches"]
+    if dom in GEMMS:
+        per_launch = GEMMS[dom] * N * d * f
+        achieved = per_launch / (kernels[dom]["ms_per_step"] * args.steps / dom_n / 1000.0) / 1e12
+        roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": pk["tensor"],
+                "unit": "TFLOP/s", "frac": achieved / pk["tensor"],
+                "peak_kind": f"bf16_tflops_sustained ({pk['source']}): kernel timed inside a long step",
+                "work_per_launch": per_launch}
+    else:
+        roof = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom].get("gbs"), "peak": pk["hbm"],
+                "unit": "GB/s", "frac": kernels[dom].get("frac_of_measured_peak")}
+    roof["traffic"] = recorded_traffic(dom, args.workload)
+
+    value = world * T / (ms / 1000.0)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": DESCR[args.workload], "T": T, "d_model": d, "d_ff": f, "E": E, "k": k,
+                   "n_shared": S, "global_batch": world * T, "parallelism": f"replicas x{world}",
+                   "l2": "no flush: each step streams > L2 (expert weights alone %.2f GB)"
+                         % (3 * G * d * f * 2 / 1e9),
+                   "rows_per_step": N, "load_max_over_mean": load_max_over_mean},
+        "e2e": {"value": world * T / (ms_e2e / 1000.0), "unit": "tokens/s", "ms_per_step": ms_e2e,
+                "h2d_bytes_per_step": 2 * T * d * 2, "d2h_bytes_per_step": 2 * T * d * 2},
+        "roofline": roof,
+        "expert_gemm": {"tflops": gemm_flops / (gemm_ms / 1000.0) / 1e12 if gemm_ms else None,
+                        "frac_of_measured_peak": (gemm_flops / (gemm_ms / 1000.0) / 1e12 / pk["tensor"])
+                        if gemm_ms else None},
+        "dispatch_combine": {"gbs": hbm_bytes / (hbm_ms / 1000.0) / 1e9 if hbm_ms else None,
+                             "frac_of_measured_peak": (hbm_bytes / (hbm_ms / 1000.0) / 1e9 / pk["hbm"])
+                             if hbm_ms else None},
+        "kernels": kernels,
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n, dt = oracle_sample(inp, cfg, args.cpu_tokens)
+        line["cpu_baseline"] = {"value": n / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+                                "sample": f"{n} seeded tokens of the same workload, fp64 fwd + bwd "
+                                          f"(weight-gradient products included), {dt:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

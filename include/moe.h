@@ -1,0 +1,209 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) Mixture-of-Experts SwiGLU FFN layer, forward and backward.
+ *
+ * One GPU, one CUDA stream per call, no host synchronisation on the compute path.  Every entry
+ * point takes plain pointers and sizes; the caller owns and allocates every buffer (device
+ * memory unless stated otherwise).  The library never allocates device memory.
+ *
+ * The layer (the pages give the systems around it, not its formulas; see "readings" below):
+ *   logits = x W_r (+ b_r)                          [T,E] fp32
+ *   p      = softmax(logits) over the E routed experts
+ *   idx    = top-k experts by logit, larger first, a tie going to the lower expert index
+ *   gates  = p[idx]  (renormalised over the k selected when cfg.renorm != 0)
+ *   dispatch: per-expert queues in token order (histogram, exclusive prefix sum, stable
+ *             permutation); with a capacity C = ceil(cf*T*k/E) the positions >= C are dropped
+ *   expert e: h = silu(x_r W_gate[e]^T) * (x_r W_up[e]^T),  o = h W_down[e]^T
+ *   y_t    = sum over kept slots j of gates[t,j] * o_{t,j}  +  sum over shared experts s of o^s_t
+ *
+ * Sources on the pages:
+ *   - "MoEBlaze: Breaking the Memory Wall for Efficient MoE Training on Modern GPUs" (Korean
+ *     summary): Methodology item 1 (dispatch queues instead of a dense token-by-expert routing
+ *     matrix), item 2 (fused scatter/gather around the expert FFN; activation checkpointing that
+ *     keeps a minimum and recomputes the rest in backward), the training-loop figure (fused
+ *     expert kernels forward, checkpoint, fused expert kernels backward, gradient reduce) and
+ *     Limitations (static top-k routing).
+ *   - "Piper: Efficient Large-Scale MoE Training via Resource Modeling and Pipelined Hybrid
+ *     Parallelism" (Japanese explainer, "the problem"): the router picks a few experts per
+ *     token; loads can be heavily skewed; fine-grained experts give tall-and-skinny GEMMs.
+ *   - "DisagMoE" technical summary, section 2.2: dispatch and combine around the expert FFN.
+ *
+ * Readings where the pages are silent: softmax over all E then top-k; selection by logit with
+ * ties to the lower index; slot order = descending logit; capacity drops in token order (t, then
+ * slot); dropped slots contribute zero and get zero gate gradient; kept gates are not
+ * renormalised after drops; shared experts have weight 1 and sit outside softmax/top-k; SwiGLU
+ * without biases.
+ *
+ * Data types and layouts (all row-major, contiguous):
+ *   bf16 values are passed as raw 16-bit patterns (moe_bf16).
+ *   x, y, dy, dx          [T, d_model]          bf16
+ *   W_r                   [d_model, E]          fp32       b_r [E] fp32 (nullable)
+ *   W_gate, W_up          [E+S, d_ff, d_model]  bf16       (out x in, like torch Linear)
+ *   W_down                [E+S, d_model, d_ff]  bf16
+ *   experts E..E+S-1 are the S shared (always-on) experts.
+ *   idx                   [T, k] int32          gates, dgates [T, k] fp32
+ *   dW_r                  [d_model, E] fp32     db_r [E] fp32
+ *   dW_gate, dW_up, dW_down: same shapes as the weights, bf16, OVERWRITTEN (not accumulated).
+ *
+ * Expert-ordered ("permuted") rows.  moe_dispatch writes x_perm in a padded, expert-contiguous
+ * layout with room for moe_perm_rows() rows:
+ *   segment g (routed experts g < E first, then shared experts) starts at row P_g, a multiple of
+ *   128; P_0 = 0, P_{g+1} = P_g + roundup(n_g, 128), where n_g = min(counts[g], C) for routed
+ *   experts and n_g = T for shared ones.  Rows P_g + n_g .. P_{g+1}-1 are zero padding.
+ *   The kept assignment (t, j) of expert e with queue position q sits at row P_e + q; shared
+ *   expert s sees token t at row P_{E+s} + t.
+ * The exact (unpadded) numbering is reported as well: offsets[e] is the exclusive prefix sum of
+ * the kept counts and row_of_slot[t,j] = offsets[e] + q (or -1 when dropped).
+ *
+ * Workspace.  Size it with moe_workspace_size(), zero its header once with moe_workspace_init(),
+ * and pass the same workspace to every call of one layer instance.  moe_dispatch leaves the
+ * routing tables in it that moe_expert_ffn_fwd/bwd, moe_combine and moe_combine_bwd read; the
+ * fused moe_layer_fwd/bwd keep all their intermediates there.  Calls that share a workspace
+ * must be ordered on one stream.
+ *
+ * Errors.  Argument checks are synchronous: a call that returns anything but MOE_OK enqueued no
+ * work.  Errors found on the device (an expert id out of range, a bounded wait that ran out)
+ * are recorded in the workspace; moe_check_error() synchronises the stream, returns the first
+ * such error since the last check, and clears it.  Device waits never spin unboundedly.
+ *
+ * Requirements: 1 <= k <= E <= 256; 0 <= S <= 8; d_model and d_ff multiples of 64 and <= 16384;
+ * 1 <= T <= 1048576 and T*k <= 2^24; every pointer 16-byte aligned; sm_103a device.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* a null pointer, a misaligned pointer or a shape out of range */
+    MOE_ERR_UNSUPPORTED = 2,   /* a valid shape this build does not handle (or not an sm_103 device) */
+    MOE_ERR_WORKSPACE = 3,     /* workspace smaller than moe_workspace_size() */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
+    MOE_ERR_BAD_INDEX = 5,     /* (device) an expert id outside [0, E); that slot is dropped */
+    MOE_ERR_TIMEOUT = 6        /* (device) a bounded wait ran out; outputs of that call are invalid */
+} moe_status_t;
+
+typedef struct {
+    int32_t T;                 /* tokens */
+    int32_t d_model;           /* model width d */
+    int32_t d_ff;              /* expert hidden width f */
+    int32_t E;                 /* routed experts */
+    int32_t k;                 /* experts per token */
+    int32_t n_shared;          /* S always-on shared experts */
+    int32_t renorm;            /* 1: gates renormalised over the k selected */
+    float capacity_factor;     /* cf > 0: capacity ceil(cf*T*k/E) per expert; <= 0: dropless */
+} moe_config_t;
+
+typedef uint16_t moe_bf16;                 /* raw bf16 bit pattern */
+typedef struct CUstream_st* moe_stream_t;  /* a cudaStream_t; NULL is the legacy default stream */
+
+/* Workspace bytes for any call of this configuration, and bytes of the `saved` buffer that
+ * moe_layer_fwd fills and moe_layer_bwd reads (idx int32 [T,k] then gates fp32 [T,k]).
+ * Host only; touches no device. */
+moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* ws_bytes, size_t* saved_bytes);
+
+/* Rows (capacity) of x_perm / o_perm / dx_perm buffers: each is [rows, d_model] bf16.  Host only. */
+moe_status_t moe_perm_rows(const moe_config_t* cfg, int64_t* rows);
+
+/* Zero the workspace header (error word and device counters).  Call once after allocating. */
+moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Router: logits, softmax, top-k and gates for every token (warp per token for the selection).
+ * b_r and logits may be NULL.  Writes idx [T,k], gates [T,k], and logits [T,E] when non-NULL. */
+moe_status_t moe_route(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
+                       int32_t* idx, float* gates, float* logits, moe_stream_t stream);
+
+/* Dispatch queues (MoEBlaze, Methodology item 1): per-expert histogram, exclusive prefix sum with
+ * a decoupled look-back, stable (token-order) ranks, capacity, and the 16-byte gather of x rows into
+ * x_perm (padded layout above; pad rows are zeroed; shared-expert segments hold copies of x).
+ * Outputs: counts [E] (raw demand, sums to T*k), offsets [E+1] (exact), row_of_slot [T,k]
+ * (exact row or -1), token_of_row [T*k] (entries >= offsets[E] are left untouched),
+ * x_perm [moe_perm_rows(), d_model].  Leaves the padded tables in ws for the calls below.
+ * An id outside [0,E) in idx drops that slot and records MOE_ERR_BAD_INDEX. */
+moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* idx, const moe_bf16* x,
+                          int32_t* counts, int32_t* offsets, int32_t* row_of_slot, int32_t* token_of_row,
+                          moe_bf16* x_perm, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Grouped expert SwiGLU FFN on the rows moe_dispatch laid out in ws: tcgen05/TMEM tiles fed by
+ * TMA, a per-expert tile scheduler, SwiGLU fused into the first GEMM's epilogue.
+ * o_perm [moe_perm_rows(), d_model] bf16 receives every segment's rows (pad rows are zero). */
+moe_status_t moe_expert_ffn_fwd(const moe_config_t* cfg, const moe_bf16* x_perm,
+                                const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down,
+                                moe_bf16* o_perm, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Weighted combine back to token order, by token owner (no atomics, fixed slot order, fp32 sums,
+ * one rounding): y[t] = sum_kept gates[t,j] o_perm[row(t,j)] + sum_s o_perm[P_{E+s}+t]. */
+moe_status_t moe_combine(const moe_config_t* cfg, const moe_bf16* o_perm, const float* gates,
+                         moe_bf16* y, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Backward of the expert FFN and of the combine's gate weighting, recomputing the SwiGLU
+ * activations from x_perm (MoEBlaze, Methodology item 2: selective checkpointing).
+ * Reads dy [T,d] in token order; writes dx_perm [moe_perm_rows(), d_model] (gradient of x_perm,
+ * padded layout), dgates [T,k] (dy . o, zero for dropped slots), dW_gate, dW_up, dW_down. */
+moe_status_t moe_expert_ffn_bwd(const moe_config_t* cfg, const moe_bf16* x_perm, const moe_bf16* dy,
+                                const float* gates,
+                                const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down,
+                                moe_bf16* dx_perm, float* dgates,
+                                moe_bf16* dW_gate, moe_bf16* dW_up, moe_bf16* dW_down,
+                                void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Router backward with the selection held fixed: recompute logits from x, then
+ * dlogits [T,E] fp32 from dgates, dW_r = x^T dlogits, db_r = sum_t dlogits (db_r nullable).
+ * Without renorm: dl_e = p_e (dg_{slot(e)} [e selected] - sum_j dg_j g_j); with renorm:
+ * dl_{idx_j} = g_j (dg_j - sum_m dg_m g_m) and 0 elsewhere.  b_r nullable. */
+moe_status_t moe_router_bwd(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
+                            const int32_t* idx, const float* gates, const float* dgates,
+                            float* dlogits, float* dW_r, float* db_r,
+                            void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Input gradient, by token owner: dx[t] = sum_kept dx_perm[row(t,j)] + sum_s dx_perm[P_{E+s}+t]
+ * + dlogits[t] W_r^T.  dlogits may be NULL (no router term).  Uses the tables of moe_dispatch. */
+moe_status_t moe_combine_bwd(const moe_config_t* cfg, const moe_bf16* dx_perm, const float* dlogits,
+                             const float* W_r, moe_bf16* dx, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* The whole forward: route, dispatch, expert FFN, combine.  Fills `saved` (idx and gates only;
+ * activations are recomputed in backward). */
+moe_status_t moe_layer_fwd(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
+                           const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down,
+                           moe_bf16* y, void* saved, void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* The whole backward from x, the weights, `saved` and dy: rebuilds the dispatch queues from the
+ * saved idx, recomputes the expert activations, and writes dx, dW_r, db_r (nullable) and the
+ * expert weight gradients. */
+moe_status_t moe_layer_bwd(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
+                           const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down,
+                           const void* saved, const moe_bf16* dy,
+                           moe_bf16* dx, float* dW_r, float* db_r,
+                           moe_bf16* dW_gate, moe_bf16* dW_up, moe_bf16* dW_down,
+                           void* ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Synchronise `stream`, return the first device-side error recorded in ws since the last check
+ * (MOE_OK if none) and clear it.  Returns MOE_ERR_CUDA if the stream itself reports an error. */
+moe_status_t moe_check_error(void* ws, moe_stream_t stream);
+
+/* Test hook: make dispatch scan block `stall_block` never publish its counts (-1: off) and bound
+ * every device wait of later calls by `timeout_ns` (0: the default, 2 s).  Used to check that a
+ * wait that runs out returns MOE_ERR_TIMEOUT through moe_check_error instead of hanging. */
+moe_status_t moe_debug_inject(void* ws, int32_t stall_block, uint64_t timeout_ns, moe_stream_t stream);
+
+/* Kernel timing.  While enabled, every kernel launch of the library is bracketed by two CUDA
+ * events recorded on its launching stream.  moe_profile_enable(on) also clears the totals.
+ * moe_profile_read(kernel, ...) waits for the recorded events and returns, for kernel id
+ * 0..n-1, its name, summed milliseconds and launch count; MOE_ERR_INVALID_ARG past the last id.
+ * Host-side state shared by the whole process; not for concurrent use from several threads. */
+moe_status_t moe_profile_enable(int32_t on);
+moe_status_t moe_profile_read(int32_t kernel, const char** name, double* total_ms, int32_t* launches);
+
+/* Static text for a status code. */
+const char* moe_status_string(moe_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,570 @@
+// The C ABI (include/moe.h): argument validation, workspace layout and the composition of the
+// layer's forward and backward from the kernels of route.cu, dispatch.cu, gemm.cu and combine.cu.
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include "common.cuh"
+
+namespace moe {
+
+int route_block_tokens(int E);   // route.cu
+
+namespace {
+
+constexpr size_t kAlign = 1024;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status_t make_cfg(const moe_config_t* in, Cfg* c) {
+  if (in == nullptr) return MOE_ERR_INVALID_ARG;
+  const moe_config_t& m = *in;
+  if (m.T < 1 || m.T > (1 << 20) || m.E < 1 || m.E > kMaxE || m.k < 1 || m.k > m.E ||
+      m.n_shared < 0 || m.n_shared > kMaxS || m.d_model < 64 || m.d_ff < 64 ||
+      m.d_model > 16384 || m.d_ff > 16384 || (m.d_model % 64) != 0 || (m.d_ff % 64) != 0 ||
+      (int64_t)m.T * m.k > (int64_t)1 << 24 || !(m.capacity_factor == m.capacity_factor))
+    return MOE_ERR_INVALID_ARG;
+  c->T = m.T;
+  c->d = m.d_model;
+  c->f = m.d_ff;
+  c->E = m.E;
+  c->k = m.k;
+  c->S = m.n_shared;
+  c->G = m.E + m.n_shared;
+  c->renorm = m.renorm ? 1 : 0;
+  if (m.capacity_factor > 0.f) {
+    const double cap = std::ceil((double)m.capacity_factor * (double)m.T * (double)m.k / (double)m.E);
+    c->C = cap >= (double)INT_MAX ? INT_MAX : (int)cap;
+  } else {
+    c->C = INT_MAX;
+  }
+  return MOE_OK;
+}
+
+moe_status_t check_device() {
+  static int ok = -1;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+      (void)cudaGetLastError();
+      ok = 0;
+      return;
+    }
+    ok = (major == 10 && minor == 3) ? 1 : 0;
+  });
+  return ok == 1 ? MOE_OK : MOE_ERR_UNSUPPORTED;
+}
+
+struct Ws {
+  Layout L;
+  char* base;
+  Hdr* hdr() const { return reinterpret_cast<Hdr*>(base + L.hdr); }
+  Tables* tabs() const { return reinterpret_cast<Tables*>(base + L.tabs); }
+  template <class T> T* at(size_t off) const { return reinterpret_cast<T*>(base + off); }
+};
+
+moe_status_t get_ws(const Cfg& c, void* ws, size_t ws_bytes, Ws* w) {
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+  w->L = make_layout(c);
+  if (ws_bytes < w->L.total) return MOE_ERR_WORKSPACE;
+  w->base = static_cast<char*>(ws);
+  return MOE_OK;
+}
+
+DispatchArgs dispatch_args(const Ws& w) {
+  DispatchArgs a{};
+  a.hdr = w.hdr();
+  a.tabs = w.tabs();
+  a.scan_status = w.at<uint32_t>(w.L.scan_status);
+  a.rank = w.at<int32_t>(w.L.rank);
+  a.prow_of_slot = w.at<int32_t>(w.L.prow_of_slot);
+  a.slot_of_prow = w.at<int32_t>(w.L.slot_of_prow);
+  a.gate_of_prow = w.at<float>(w.L.gate_of_prow);
+  return a;
+}
+
+}  // namespace
+
+Layout make_layout(const Cfg& c) {
+  Layout L{};
+  const int64_t routed = ((int64_t)c.T * c.k + (int64_t)(kRowTile - 1) * c.E + kRowTile - 1) / kRowTile * kRowTile;
+  const int64_t shared = (int64_t)c.S * (((int64_t)c.T + kRowTile - 1) / kRowTile * kRowTile);
+  L.rows = routed + shared;
+  L.nscan = (int)(((int64_t)c.T * c.k + kScanChunk - 1) / kScanChunk);
+  L.ntf = (c.f + 127) / 128;
+  L.nblk_router = (c.T + route_block_tokens(c.E) - 1) / route_block_tokens(c.E);
+  const int dtiles = (c.d + 63) / 64;
+  L.nsplit_dwr = std::max(1, std::min((304 + dtiles - 1) / dtiles, (c.T + 255) / 256));
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, kAlign);
+    return o;
+  };
+  const size_t rows = (size_t)L.rows;
+  L.hdr = take(sizeof(Hdr));
+  L.tabs = take(sizeof(Tables));
+  L.scan_status = take((size_t)L.nscan * c.E * 4);
+  L.rank = take((size_t)c.T * c.k * 4);
+  L.prow_of_slot = take((size_t)c.T * c.k * 4);
+  L.slot_of_prow = take(rows * 4);
+  L.gate_of_prow = take(rows * 4);
+  L.dg_part = take(rows * L.ntf * 4);
+  L.dlogits = take((size_t)c.T * c.E * 4);
+  L.dwr_part = take((size_t)L.nsplit_dwr * c.d * c.E * 4);
+  L.db_part = take((size_t)L.nblk_router * c.E * 4);
+  L.dgates = take((size_t)c.T * c.k * 4);
+  L.xperm = take(rows * c.d * 2);
+  L.dy_perm = take(rows * c.d * 2);
+  L.buf_f0 = take(rows * c.f * 2);
+  L.buf_f1 = take(rows * c.f * 2);
+  L.buf_f2 = take(rows * c.f * 2);
+  L.buf_d1 = take(rows * c.d * 2);
+  L.total = off;
+  return L;
+}
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    (void)cudaGetLastError();
+    return 148;
+  }
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+      (void)cudaGetLastError();
+      n = 148;
+    }
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+moe_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  (void)cudaGetLastError();
+  return MOE_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------------------------
+// kernel event profiler
+// ---------------------------------------------------------------------------------------------
+
+namespace {
+
+const char* const kKernelNames[kKCount] = {
+    "route_fwd", "dispatch_scan", "dispatch_gather", "gemm_gate_up_swiglu", "gemm_down",
+    "combine", "gemm_bwd_recompute_dgrad_swiglu", "gemm_wgrad", "gemm_dgrad_x", "dgates_reduce",
+    "router_dlogits", "router_dwr", "router_reduce", "combine_bwd"};
+
+struct Profiler {
+  std::mutex mu;
+  bool on = false;
+  std::vector<cudaEvent_t> pool;           // events, reused across enables
+  size_t used = 0;
+  std::vector<std::pair<int, std::pair<size_t, size_t>>> marks;   // (kernel, (start, stop))
+  size_t open[kKCount];
+  double total_ms[kKCount];
+  int launches[kKCount];
+};
+
+Profiler& profiler() {
+  static Profiler p;
+  return p;
+}
+
+}  // namespace
+
+void prof_mark(int id, cudaStream_t s, bool begin) {
+  Profiler& p = profiler();
+  if (!p.on) return;
+  std::lock_guard<std::mutex> lock(p.mu);
+  if (p.used == p.pool.size()) {
+    cudaEvent_t ev;
+    if (cudaEventCreate(&ev) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return;
+    }
+    p.pool.push_back(ev);
+  }
+  const size_t e = p.used++;
+  if (cudaEventRecord(p.pool[e], s) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return;
+  }
+  if (begin) {
+    p.open[id] = e;
+  } else {
+    p.marks.push_back({id, {p.open[id], e}});
+  }
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+#define MOE_TRY(expr)                         \
+  do {                                        \
+    const moe_status_t _st = (expr);          \
+    if (_st != MOE_OK) return _st;            \
+  } while (0)
+#define MOE_CUDA(expr) MOE_TRY(cuda_status(expr))
+#define MOE_NEED(cond) \
+  do {                 \
+    if (!(cond)) return MOE_ERR_INVALID_ARG; \
+  } while (0)
+
+namespace {
+
+moe_status_t do_dispatch(const Cfg& c, const Ws& w, const int32_t* idx, const uint16_t* x,
+                         const uint16_t* dy, const float* gates, int32_t* counts, int32_t* offsets,
+                         int32_t* row_of_slot, int32_t* token_of_row, uint16_t* x_perm,
+                         uint16_t* dy_perm, cudaStream_t s) {
+  DispatchArgs a = dispatch_args(w);
+  a.idx = idx;
+  a.x = x;
+  a.dy = dy;
+  a.gates = gates;
+  a.counts = counts;
+  a.offsets = offsets;
+  a.row_of_slot = row_of_slot;
+  a.token_of_row = token_of_row;
+  a.x_perm = x_perm;
+  a.dy_perm = dy_perm;
+  MOE_CUDA(launch_dispatch_scan(c, w.L, a, s));
+  MOE_CUDA(launch_dispatch_gather(c, w.L, a, true, true, dy != nullptr, s));
+  return MOE_OK;
+}
+
+moe_status_t do_ffn_bwd(const Cfg& c, const Ws& w, const uint16_t* x_perm, const uint16_t* dy_perm,
+                        const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd,
+                        uint16_t* dx_perm, float* dgates, uint16_t* dWg, uint16_t* dWu,
+                        uint16_t* dWd, cudaStream_t s) {
+  FfnBwdArgs b{};
+  b.x_perm = x_perm;
+  b.dy_perm = dy_perm;
+  b.gate_of_prow = w.at<float>(w.L.gate_of_prow);
+  b.Wg = Wg;
+  b.Wu = Wu;
+  b.Wd = Wd;
+  b.dA = w.at<uint16_t>(w.L.buf_f0);
+  b.dB = w.at<uint16_t>(w.L.buf_f1);
+  b.Hg = w.at<uint16_t>(w.L.buf_f2);
+  b.dg_part = w.at<float>(w.L.dg_part);
+  b.dx_perm = dx_perm;
+  b.dWg = dWg;
+  b.dWu = dWu;
+  b.dWd = dWd;
+  b.hdr = w.hdr();
+  b.tabs = w.tabs();
+  MOE_CUDA(launch_ffn_bwd(c, w.L, b, s));
+  DgatesArgs g{};
+  g.dg_part = b.dg_part;
+  g.prow_of_slot = w.at<int32_t>(w.L.prow_of_slot);
+  g.dgates = dgates;
+  MOE_CUDA(launch_dgates(c, w.L, g, s));
+  return MOE_OK;
+}
+
+moe_status_t do_router_bwd(const Cfg& c, const Ws& w, const uint16_t* x, const float* W_r,
+                           const float* b_r, const int32_t* idx, const float* gates,
+                           const float* dgates, float* dlogits, float* dW_r, float* db_r,
+                           cudaStream_t s) {
+  RouterBwdArgs a{};
+  a.x = x;
+  a.W_r = W_r;
+  a.b_r = b_r;
+  a.idx = idx;
+  a.gates = gates;
+  a.dgates = dgates;
+  a.dlogits = dlogits;
+  a.dW_r = dW_r;
+  a.db_r = db_r;
+  a.dwr_part = w.at<float>(w.L.dwr_part);
+  a.db_part = w.at<float>(w.L.db_part);
+  MOE_CUDA(launch_router_bwd(c, w.L, a, s));
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_status_string(moe_status_t st) {
+  switch (st) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported configuration or device";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_BAD_INDEX: return "expert index out of range";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+  }
+  return "unknown status";
+}
+
+moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* ws_bytes, size_t* saved_bytes) {
+  Cfg c;
+  MOE_TRY(make_cfg(cfg, &c));
+  MOE_NEED(ws_bytes != nullptr);
+  *ws_bytes = make_layout(c).total;
+  if (saved_bytes) *saved_bytes = (size_t)c.T * c.k * 8;
+  return MOE_OK;
+}
+
+moe_status_t moe_perm_rows(const moe_config_t* cfg, int64_t* rows) {
+  Cfg c;
+  MOE_TRY(make_cfg(cfg, &c));
+  MOE_NEED(rows != nullptr);
+  *rows = make_layout(c).rows;
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  Cfg c;
+  MOE_TRY(make_cfg(cfg, &c));
+  Ws w;
+  MOE_TRY(get_ws(c, ws, ws_bytes, &w));
+  MOE_CUDA(cudaMemsetAsync(w.hdr(), 0, sizeof(Hdr), stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_route(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
+                       int32_t* idx, float* gates, float* logits, moe_stream_t stream) {
+  Cfg c;
+  MOE_TRY(make_cfg(cfg, &c));
+  MOE_NEED(x && W_r && idx && gates && aligned16(x) && aligned16(W_r) && aligned16(idx) &&
+           aligned16(gates) && (!b_r || aligned16(b_r)) && (!logits || aligned16(logits)));
+  MOE_TRY(check_device());
+  RouteArgs a{x, W_r, b_r, idx, gates, logits};
+  MOE_CUDA(launch_route(c, a, stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* idx, const moe_bf16* x,
+                          int32_t* counts, int32_t* offsets, int32_t* row_of_slot, int32_t* token_of_row,
+                          moe_bf16* x_perm, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  Cfg c;
+  MOE_TRY(make_cfg(cfg, &c));
+  MOE_NEED(idx && x && counts && offsets && row_of_slot && token_of_row && x_perm);
+  MOE_NEED(aligned16(idx) && aligned16(x) && aligned16(counts) && aligned16(offsets) &&
+           aligned16(row_of_slot) && aligned16(token_of_row) && aligned16(x_perm));
+  Ws w;
+  MOE_TRY(get_ws(c, ws, ws_bytes, &w));
+  MOE_TRY(check_device());
+  return do_dispatch(c, w, idx, x, nullptr, nullptr, counts, offsets, row_of_slot, token_of_row,
+                     x_perm, nullptr, stream);
+}
+
+moe_status_t moe_expert_ffn_fwd(const moe_config_t* cfg, const moe_bf16* x_perm,
+                                const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down,
+                                moe_bf16* o_perm, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  Cfg c;
+  MOE_TRY(make_cfg(cfg, &c));
+  MOE_NEED(x_perm && W_gate && W_up && W_down && o_perm);
+  MOE_NEED(aligned16(x_perm) && aligned16(W_gate) && aligned16(W_up) && aligned16(W_down) && aligned16(o_perm));
+  Ws w;
+  MOE_TRY(get_ws(c, ws, ws_bytes, &w));
+  MOE_TRY(check_device());
+  FfnFwdArgs a{x_perm, W_gate, W_up, W_down, w.at<uint16_t>(w.L.buf_f0), o_perm, w.hdr(), w.tabs()};
+  MOE_CUDA(launch_ffn_fwd(c, w.L, a, stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_combine(const moe_config_t* cfg, const moe_bf16* o_perm, const float* gates,
+                         moe_bf16* y, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  Cfg c;
+  MOE_TRY(make_cfg(cfg, &c));
+  MOE_NEED(o_perm && gates && y && aligned16(o_perm) && aligned16(gates) && aligned16(y));
+  Ws w;
+  MOE_TRY(get_ws(c, ws, ws_bytes, &w));
+  MOE_TRY(check_device());
+  CombineArgs a{o_perm, gates, y, w.tabs(), w.at<int32_t>(w.L.prow_of_slot)};
+  MOE_CUDA(launch_combine(c, a, stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_expert_ffn_bwd(const moe_config_t* cfg, const moe_bf16* x_perm, const moe_bf16* dy,
+                                const float* gates,
+                                const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down,
+                                moe_bf16* dx_perm, float* dgates,
+                                moe_bf16* dW_gate, moe_bf16* dW_up, moe_bf16* dW_down,
+                                void* ws, size_t ws_bytes, moe_stream_t stream) {
+  Cfg c;
+  MOE_TRY(make_cfg(cfg, &c));
+  MOE_NEED(x_perm && dy && gates && W_gate && W_up && W_down && dx_perm && dgates && dW_gate &&
+           dW_up && dW_down);
+  MOE_NEED(aligned16(x_perm) && aligned16(dy) && aligned16(gates) && aligned16(W_gate) &&
+           aligned16(W_up) && aligned16(W_down) && aligned16(dx_perm) && aligned16(dgates) &&
+           aligned16(dW_gate) && aligned16(dW_up) && aligned16(dW_down));
+  Ws w;
+  MOE_TRY(get_ws(c, ws, ws_bytes, &w));
+  MOE_TRY(check_device());
+  DispatchArgs a = dispatch_args(w);
+  a.dy = dy;
+  a.gates = gates;
+  a.dy_perm = w.at<uint16_t>(w.L.dy_perm);
+  MOE_CUDA(launch_dispatch_gather(c, w.L, a, false, false, true, stream));
+  return do_ffn_bwd(c, w, x_perm, a.dy_perm, W_gate, W_up, W_down, dx_perm, dgates, dW_gate, dW_up,
+                    dW_down, stream);
+}
+
+moe_status_t moe_router_bwd(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
+                            const int32_t* idx, const float* gates, const float* dgates,
+                            float* dlogits, float* dW_r, float* db_r,
+                            void* ws, size_t ws_bytes, moe_stream_t stream) {
+  Cfg c;
+  MOE_TRY(make_cfg(cfg, &c));
+  MOE_NEED(x && W_r && idx && gates && dgates && dlogits && dW_r);
+  MOE_NEED(aligned16(x) && aligned16(W_r) && aligned16(idx) && aligned16(gates) && aligned16(dgates) &&
+           aligned16(dlogits) && aligned16(dW_r) && (!b_r || aligned16(b_r)) && (!db_r || aligned16(db_r)));
+  Ws w;
+  MOE_TRY(get_ws(c, ws, ws_bytes, &w));
+  MOE_TRY(check_device());
+  return do_router_bwd(c, w, x, W_r, b_r, idx, gates, dgates, dlogits, dW_r, db_r, stream);
+}
+
+moe_status_t moe_combine_bwd(const moe_config_t* cfg, const moe_bf16* dx_perm, const float* dlogits,
+                             const float* W_r, moe_bf16* dx, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  Cfg c;
+  MOE_TRY(make_cfg(cfg, &c));
+  MOE_NEED(dx_perm && dx && aligned16(dx_perm) && aligned16(dx));
+  MOE_NEED(!dlogits || (W_r && aligned16(dlogits) && aligned16(W_r)));
+  Ws w;
+  MOE_TRY(get_ws(c, ws, ws_bytes, &w));
+  MOE_TRY(check_device());
+  CombineBwdArgs a{dx_perm, dlogits, W_r, dx, w.tabs(), w.at<int32_t>(w.L.prow_of_slot)};
+  MOE_CUDA(launch_combine_bwd(c, a, stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_fwd(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
+                           const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down,
+                           moe_bf16* y, void* saved, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  Cfg c;
+  MOE_TRY(make_cfg(cfg, &c));
+  MOE_NEED(x && W_r && W_gate && W_up && W_down && y && saved);
+  MOE_NEED(aligned16(x) && aligned16(W_r) && (!b_r || aligned16(b_r)) && aligned16(W_gate) &&
+           aligned16(W_up) && aligned16(W_down) && aligned16(y) && aligned16(saved));
+  Ws w;
+  MOE_TRY(get_ws(c, ws, ws_bytes, &w));
+  MOE_TRY(check_device());
+  int32_t* idx = static_cast<int32_t*>(saved);
+  float* gates = reinterpret_cast<float*>(idx + (size_t)c.T * c.k);
+  RouteArgs ra{x, W_r, b_r, idx, gates, nullptr};
+  MOE_CUDA(launch_route(c, ra, stream));
+  uint16_t* x_perm = w.at<uint16_t>(w.L.xperm);
+  MOE_TRY(do_dispatch(c, w, idx, x, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, x_perm,
+                      nullptr, stream));
+  uint16_t* o_perm = w.at<uint16_t>(w.L.buf_d1);
+  FfnFwdArgs fa{x_perm, W_gate, W_up, W_down, w.at<uint16_t>(w.L.buf_f0), o_perm, w.hdr(), w.tabs()};
+  MOE_CUDA(launch_ffn_fwd(c, w.L, fa, stream));
+  CombineArgs ca{o_perm, gates, y, w.tabs(), w.at<int32_t>(w.L.prow_of_slot)};
+  MOE_CUDA(launch_combine(c, ca, stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_bwd(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
+                           const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down,
+                           const void* saved, const moe_bf16* dy,
+                           moe_bf16* dx, float* dW_r, float* db_r,
+                           moe_bf16* dW_gate, moe_bf16* dW_up, moe_bf16* dW_down,
+                           void* ws, size_t ws_bytes, moe_stream_t stream) {
+  Cfg c;
+  MOE_TRY(make_cfg(cfg, &c));
+  MOE_NEED(x && W_r && W_gate && W_up && W_down && saved && dy && dx && dW_r && dW_gate && dW_up && dW_down);
+  MOE_NEED(aligned16(x) && aligned16(W_r) && (!b_r || aligned16(b_r)) && aligned16(W_gate) &&
+           aligned16(W_up) && aligned16(W_down) && aligned16(saved) && aligned16(dy) && aligned16(dx) &&
+           aligned16(dW_r) && (!db_r || aligned16(db_r)) && aligned16(dW_gate) && aligned16(dW_up) &&
+           aligned16(dW_down));
+  Ws w;
+  MOE_TRY(get_ws(c, ws, ws_bytes, &w));
+  MOE_TRY(check_device());
+  const int32_t* idx = static_cast<const int32_t*>(saved);
+  const float* gates = reinterpret_cast<const float*>(idx + (size_t)c.T * c.k);
+  uint16_t* x_perm = w.at<uint16_t>(w.L.xperm);
+  uint16_t* dy_perm = w.at<uint16_t>(w.L.dy_perm);
+  MOE_TRY(do_dispatch(c, w, idx, x, dy, gates, nullptr, nullptr, nullptr, nullptr, x_perm, dy_perm, stream));
+  uint16_t* dx_perm = w.at<uint16_t>(w.L.buf_d1);
+  float* dgates = w.at<float>(w.L.dgates);
+  MOE_TRY(do_ffn_bwd(c, w, x_perm, dy_perm, W_gate, W_up, W_down, dx_perm, dgates, dW_gate, dW_up,
+                     dW_down, stream));
+  float* dlogits = w.at<float>(w.L.dlogits);
+  MOE_TRY(do_router_bwd(c, w, x, W_r, b_r, idx, gates, dgates, dlogits, dW_r, db_r, stream));
+  CombineBwdArgs cb{dx_perm, dlogits, W_r, dx, w.tabs(), w.at<int32_t>(w.L.prow_of_slot)};
+  MOE_CUDA(launch_combine_bwd(c, cb, stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_check_error(void* ws, moe_stream_t stream) {
+  if (ws == nullptr) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  Hdr* h = static_cast<Hdr*>(ws);
+  int32_t st = 0;
+  MOE_CUDA(cudaMemcpy(&st, &h->status, sizeof(st), cudaMemcpyDeviceToHost));
+  MOE_CUDA(cudaMemset(&h->status, 0, 2 * sizeof(int32_t)));
+  return static_cast<moe_status_t>(st);
+}
+
+moe_status_t moe_profile_enable(int32_t on) {
+  Profiler& p = profiler();
+  std::lock_guard<std::mutex> lock(p.mu);
+  p.on = on != 0;
+  p.used = 0;
+  p.marks.clear();
+  for (int i = 0; i < kKCount; ++i) {
+    p.total_ms[i] = 0.0;
+    p.launches[i] = 0;
+  }
+  return MOE_OK;
+}
+
+moe_status_t moe_profile_read(int32_t kernel, const char** name, double* total_ms, int32_t* launches) {
+  if (kernel < 0 || kernel >= kKCount || name == nullptr || total_ms == nullptr || launches == nullptr)
+    return MOE_ERR_INVALID_ARG;
+  Profiler& p = profiler();
+  std::lock_guard<std::mutex> lock(p.mu);
+  if (!p.marks.empty()) {   // fold the recorded pairs into the totals (waits for them)
+    for (const auto& m : p.marks) {
+      float ms = 0.f;
+      if (cudaEventSynchronize(p.pool[m.second.second]) != cudaSuccess ||
+          cudaEventElapsedTime(&ms, p.pool[m.second.first], p.pool[m.second.second]) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return MOE_ERR_CUDA;
+      }
+      p.total_ms[m.first] += ms;
+      p.launches[m.first] += 1;
+    }
+    p.marks.clear();
+    p.used = 0;
+  }
+  *name = kKernelNames[kernel];
+  *total_ms = p.total_ms[kernel];
+  *launches = p.launches[kernel];
+  return MOE_OK;
+}
+
+moe_status_t moe_debug_inject(void* ws, int32_t stall_block, uint64_t timeout_ns, moe_stream_t stream) {
+  if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+  Hdr* h = static_cast<Hdr*>(ws);
+  const int32_t stall_p1 = stall_block < 0 ? 0 : stall_block + 1;
+  MOE_CUDA(cudaMemcpyAsync(&h->stall_block_p1, &stall_p1, sizeof(stall_p1), cudaMemcpyHostToDevice, stream));
+  MOE_CUDA(cudaMemcpyAsync(&h->timeout_ns, &timeout_ns, sizeof(timeout_ns), cudaMemcpyHostToDevice, stream));
+  MOE_CUDA(cudaStreamSynchronize(stream));
+  return MOE_OK;
+}
+
+}  // extern "C"

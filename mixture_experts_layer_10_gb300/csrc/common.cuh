@@ -1,0 +1,178 @@
+// Internal definitions shared by the layer's translation units: limits, the workspace layout,
+// device-side error recording and the bounded-wait clock.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "moe.h"
+
+namespace moe {
+
+constexpr int kMaxE = 256;
+constexpr int kMaxS = 8;
+constexpr int kMaxG = kMaxE + kMaxS;       // routed + shared segments
+constexpr int kRowTile = 128;              // GEMM M tile; segments are padded to it
+constexpr int kScanChunk = 4096;           // assignments per dispatch-scan block
+constexpr int kScanThreads = 512;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s bound on any device wait
+
+// Where a device error was raised (recorded beside the status code).
+enum Site : int32_t {
+  kSiteScanLookback = 1,
+  kSiteScanIndex = 2,
+  kSiteGemmProducer = 10,
+  kSiteGemmMma = 11,
+  kSiteGemmEpilogue = 12,
+};
+
+// Header at workspace offset 0.  `status`..`timeout_ns` persist across calls (cleared by
+// moe_workspace_init / moe_check_error); the dispatch counters are reset by every dispatch.
+struct Hdr {
+  int32_t status;
+  int32_t site;
+  int32_t stall_block_p1;   // test hook: scan block (value - 1) never publishes (0 off)
+  int32_t reserved0;
+  uint64_t timeout_ns;      // 0 = kDefaultTimeoutNs
+  uint32_t scan_ticket;     // dynamic block index of the dispatch scan
+  uint32_t scan_done;       // scan blocks finished; the last one builds the tables
+  uint32_t reserved[56];
+};
+static_assert(sizeof(Hdr) == 256, "header is 256 bytes");
+constexpr size_t kHdrResetOffset = offsetof(Hdr, scan_ticket);   // per-dispatch part
+constexpr size_t kHdrResetBytes = 8;
+
+// Routing tables written by the last dispatch-scan block.
+struct Tables {
+  int32_t G;                     // segments = E + S
+  int32_t n_mtiles;              // P_G / 128
+  int32_t total_rows;            // P_G
+  int32_t total_pad;             // pad rows over all segments
+  int32_t counts[kMaxE];         // raw demand per routed expert
+  int32_t kept[kMaxG];           // rows per segment
+  int32_t offsets[kMaxE + 1];    // exact exclusive scan of kept over routed experts
+  int32_t poff[kMaxG + 1];       // padded segment starts P_g
+  int32_t pad_start[kMaxG + 1];  // exclusive scan of pad rows per segment
+  int32_t seg_order[kMaxG];      // segments by padded rows, descending (ties: lower index)
+};
+
+// Byte offsets of every workspace region (host computed, passed to kernels as pointers).
+struct Layout {
+  int64_t rows;          // row capacity of the padded expert-ordered buffers
+  int nscan;             // dispatch-scan blocks
+  int ntf;               // 128-wide tiles over d_ff (per-row gate-gradient partials)
+  int nsplit_dwr;        // token splits of dW_r = x^T dlogits
+  int nblk_router;       // router backward blocks (db partials)
+  size_t hdr, tabs, scan_status, rank, prow_of_slot, slot_of_prow, gate_of_prow, dg_part,
+      dlogits, dwr_part, db_part, dgates, xperm, dy_perm, buf_f0, buf_f1, buf_f2, buf_d1;
+  size_t total;
+};
+
+struct Cfg {               // validated configuration with derived sizes
+  int T, d, f, E, k, S, G, renorm;
+  int C;                   // capacity (INT32_MAX when dropless)
+};
+
+// ---------------------------------------------------------------------------------------------
+// device-side error word and clock
+// ---------------------------------------------------------------------------------------------
+
+__device__ __forceinline__ void record_error(Hdr* h, int32_t code, int32_t site) {
+  if (atomicCAS(&h->status, 0, code) == 0) h->site = site;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint64_t wait_limit_ns(const Hdr* h) {
+  uint64_t t = *((volatile const uint64_t*)&h->timeout_ns);
+  return t ? t : kDefaultTimeoutNs;
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&p);
+}
+
+// ---------------------------------------------------------------------------------------------
+// host-side helpers shared by the launchers
+// ---------------------------------------------------------------------------------------------
+
+Layout make_layout(const Cfg& c);
+int num_sms();                                   // SMs of the current device (cached)
+moe_status_t cuda_status(cudaError_t e);          // MOE_OK or MOE_ERR_CUDA (clears the error)
+
+// Kernel event profiler (off unless moe_profile_enable(1)): every launch site brackets its kernel
+// with prof_mark(id, s, true/false), which records CUDA events on the launching stream.
+enum KernelId : int {
+  kKRoute = 0, kKScan, kKGather, kKGateUp, kKDown, kKCombine, kKBwdFused, kKWgrad, kKDgradX,
+  kKDgates, kKRouterDlogits, kKRouterDwr, kKRouterReduce, kKCombineBwd, kKCount
+};
+void prof_mark(int id, cudaStream_t s, bool begin);
+
+// Launchers implemented in the kernel translation units.  All enqueue on `s` and return the
+// launch status.
+struct RouteArgs {
+  const uint16_t* x; const float* W_r; const float* b_r;
+  int32_t* idx; float* gates; float* logits;
+};
+cudaError_t launch_route(const Cfg& c, const RouteArgs& a, cudaStream_t s);
+
+struct DispatchArgs {
+  const int32_t* idx; const uint16_t* x; const uint16_t* dy; const float* gates;
+  int32_t* counts; int32_t* offsets; int32_t* row_of_slot; int32_t* token_of_row;
+  uint16_t* x_perm; uint16_t* dy_perm;
+  Hdr* hdr; Tables* tabs; uint32_t* scan_status; int32_t* rank;
+  int32_t* prow_of_slot; int32_t* slot_of_prow; float* gate_of_prow;
+};
+cudaError_t launch_dispatch_scan(const Cfg& c, const Layout& L, const DispatchArgs& a, cudaStream_t s);
+cudaError_t launch_dispatch_gather(const Cfg& c, const Layout& L, const DispatchArgs& a,
+                                   bool write_meta, bool gather_x, bool gather_dy, cudaStream_t s);
+
+struct CombineArgs {
+  const uint16_t* o_perm; const float* gates; uint16_t* y;
+  const Tables* tabs; const int32_t* prow_of_slot;
+};
+cudaError_t launch_combine(const Cfg& c, const CombineArgs& a, cudaStream_t s);
+
+struct CombineBwdArgs {
+  const uint16_t* dx_perm; const float* dlogits; const float* W_r; uint16_t* dx;
+  const Tables* tabs; const int32_t* prow_of_slot;
+};
+cudaError_t launch_combine_bwd(const Cfg& c, const CombineBwdArgs& a, cudaStream_t s);
+
+struct RouterBwdArgs {
+  const uint16_t* x; const float* W_r; const float* b_r; const int32_t* idx; const float* gates;
+  const float* dgates; float* dlogits; float* dW_r; float* db_r;
+  float* dwr_part; float* db_part;
+};
+cudaError_t launch_router_bwd(const Cfg& c, const Layout& L, const RouterBwdArgs& a, cudaStream_t s);
+
+struct DgatesArgs {
+  const float* dg_part; const int32_t* prow_of_slot; float* dgates;
+};
+cudaError_t launch_dgates(const Cfg& c, const Layout& L, const DgatesArgs& a, cudaStream_t s);
+
+struct FfnFwdArgs {
+  const uint16_t* x_perm; const uint16_t* Wg; const uint16_t* Wu; const uint16_t* Wd;
+  uint16_t* h; uint16_t* o_perm; Hdr* hdr; const Tables* tabs;
+};
+cudaError_t launch_ffn_fwd(const Cfg& c, const Layout& L, const FfnFwdArgs& a, cudaStream_t s);
+
+struct FfnBwdArgs {
+  const uint16_t* x_perm; const uint16_t* dy_perm; const float* gate_of_prow;
+  const uint16_t* Wg; const uint16_t* Wu; const uint16_t* Wd;
+  uint16_t* dA; uint16_t* dB; uint16_t* Hg; float* dg_part; uint16_t* dx_perm;
+  uint16_t* dWg; uint16_t* dWu; uint16_t* dWd; Hdr* hdr; const Tables* tabs;
+};
+cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, cudaStream_t s);
+
+}  // namespace moe

@@ -1,0 +1,302 @@
+// Dispatch queues (MoEBlaze, Methodology item 1): tokens reach their experts through per-expert
+// queues built on the fly -- a histogram, an exclusive prefix sum and a stable permutation --
+// instead of a dense token-by-expert routing matrix.
+//
+// dispatch_scan_kernel: one pass over the T*k assignments in token order.  Each block ranks its
+//   4096 assignments per expert (warp match + shared-memory running counts, so ranks follow the
+//   (t, j) order), publishes its per-expert aggregate, and finds its per-expert exclusive prefix
+//   with a decoupled look-back over the preceding blocks (bounded spin).  The last block to
+//   finish builds the routing tables: counts, capacity, exact offsets, 128-row padded segment
+//   starts, pad-row prefix and the segment order by size.
+// dispatch_gather_kernel: token owner.  A warp reads each x (and dy) row once, 16 bytes per lane,
+//   and writes it to every kept slot's row (and every shared expert's row); then zeroes pad rows.
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kWarps = kScanThreads / 32;
+constexpr int kPerWarp = kScanChunk / kWarps;   // 256 assignments, 8 rounds of 32
+constexpr uint32_t kFlagAgg = 1u << 30;
+constexpr uint32_t kFlagIncl = 2u << 30;
+constexpr uint32_t kValueMask = (1u << 30) - 1;
+
+__device__ __forceinline__ void st_release(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(DispatchArgs a, int N, int T,
+                                                                     int E, int S, int C, int nblk,
+                                                                     long long row_cap) {
+  __shared__ int wcnt[kWarps][kMaxE];   // per-warp running counts, then warp exclusive prefix
+  __shared__ int blk_excl[kMaxE];
+  __shared__ int s_blk, s_last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) s_blk = (int)atomicAdd(&a.hdr->scan_ticket, 1u);
+  for (int i = threadIdx.x; i < kWarps * kMaxE; i += kScanThreads) (&wcnt[0][0])[i] = 0;
+  __syncthreads();
+  const int blk = s_blk;
+  const int base = blk * kScanChunk + warp * kPerWarp;
+
+  int my_e[kPerWarp / 32], my_r[kPerWarp / 32];
+#pragma unroll
+  for (int s = 0; s < kPerWarp / 32; ++s) {
+    const int i = base + s * 32 + lane;
+    int e = -1;
+    if (i < N) {
+      e = a.idx[i];
+      if (e < 0 || e >= E) {
+        record_error(a.hdr, MOE_ERR_BAD_INDEX, kSiteScanIndex);
+        e = -1;
+      }
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int before = (e >= 0) ? wcnt[warp][e] : 0;
+    __syncwarp();
+    if (e >= 0 && lane == __ffs(peers) - 1) wcnt[warp][e] = before + __popc(peers);
+    __syncwarp();
+    my_e[s] = e;
+    my_r[s] = before + __popc(peers & ((1u << lane) - 1u));
+  }
+  __syncthreads();
+
+  if (threadIdx.x < E) {
+    const int e = threadIdx.x;
+    int agg = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      const int c = wcnt[w][e];
+      wcnt[w][e] = agg;
+      agg += c;
+    }
+    uint32_t* st = a.scan_status + (size_t)blk * E + e;
+    const bool stall = (blk + 1 == a.hdr->stall_block_p1);
+    int excl = 0;
+    if (blk == 0) {
+      if (!stall) st_release(st, kFlagIncl | (uint32_t)agg);
+    } else {
+      if (!stall) st_release(st, kFlagAgg | (uint32_t)agg);
+      const uint64_t limit = wait_limit_ns(a.hdr);
+      const uint64_t t0 = global_ns();
+      int b = blk - 1;
+      while (b >= 0) {
+        const uint32_t v = ld_acquire(a.scan_status + (size_t)b * E + e);
+        if ((v & ~kValueMask) == 0) {
+          if (global_ns() - t0 > limit) {
+            record_error(a.hdr, MOE_ERR_TIMEOUT, kSiteScanLookback);
+            break;
+          }
+          continue;
+        }
+        excl += (int)(v & kValueMask);
+        if ((v & ~kValueMask) == kFlagIncl) break;
+        --b;
+      }
+      if (!stall) st_release(st, kFlagIncl | (uint32_t)((excl + agg) & (int)kValueMask));
+    }
+    blk_excl[e] = excl;
+  }
+  __syncthreads();
+
+#pragma unroll
+  for (int s = 0; s < kPerWarp / 32; ++s) {
+    const int i = base + s * 32 + lane;
+    const int e = my_e[s];
+    if (i < N && e >= 0) a.rank[i] = blk_excl[e] + wcnt[warp][e] + my_r[s];
+  }
+
+  // The last block to finish builds the tables.
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = (atomicAdd(&a.hdr->scan_done, 1u) == (unsigned)(nblk - 1));
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+
+  Tables* tb = a.tabs;
+  const int G = E + S;
+  if (threadIdx.x < E) {
+    const int e = threadIdx.x;
+    const uint32_t v = ld_acquire(a.scan_status + (size_t)(nblk - 1) * E + e);
+    const int total = (int)(v & kValueMask);
+    tb->counts[e] = total;
+    if (a.counts != nullptr) a.counts[e] = total;
+    tb->kept[e] = total < C ? total : C;
+  } else if (threadIdx.x < G) {
+    tb->kept[threadIdx.x] = T;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    // A pending device error means the ranks cannot be trusted: publish empty segments so that
+    // no later kernel touches rows on their account.
+    const bool bad = (*((volatile int*)&a.hdr->status)) != 0;
+    int off = 0;
+    long long poff = 0, pads = 0;
+    for (int g = 0; g < G; ++g) {
+      int kept = bad ? 0 : tb->kept[g];
+      tb->kept[g] = kept;
+      if (g < E) {
+        tb->offsets[g] = off;
+        if (a.offsets != nullptr) a.offsets[g] = off;
+        off += kept;
+      }
+      const long long padded = ((long long)kept + kRowTile - 1) / kRowTile * kRowTile;
+      tb->poff[g] = (int)poff;
+      tb->pad_start[g] = (int)pads;
+      poff += padded;
+      pads += padded - kept;
+    }
+    tb->offsets[E] = off;
+    if (a.offsets != nullptr) a.offsets[E] = off;
+    if (poff > row_cap) {   // cannot happen for valid ranks; guard the buffers regardless
+      record_error(a.hdr, MOE_ERR_BAD_INDEX, kSiteScanIndex);
+      for (int g = 0; g < G; ++g) {
+        tb->kept[g] = 0;
+        tb->poff[g] = 0;
+        tb->pad_start[g] = 0;
+      }
+      poff = 0;
+      pads = 0;
+    }
+    tb->poff[G] = (int)poff;
+    tb->pad_start[G] = (int)pads;
+    tb->G = G;
+    tb->total_rows = (int)poff;
+    tb->n_mtiles = (int)(poff / kRowTile);
+    tb->total_pad = (int)pads;
+  }
+  __syncthreads();
+  if (threadIdx.x < G) {
+    const int g = threadIdx.x;
+    const int pg = tb->poff[g + 1] - tb->poff[g];
+    int r = 0;
+    for (int h = 0; h < G; ++h) {
+      const int ph = tb->poff[h + 1] - tb->poff[h];
+      r += (ph > pg) || (ph == pg && h < g);
+    }
+    tb->seg_order[r] = g;
+  }
+}
+
+template <bool kMeta, bool kX, bool kDy>
+__global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a, int T, int k, int E,
+                                                              int S, int d) {
+  const Tables* tb = a.tabs;
+  const int lane = threadIdx.x & 31;
+  const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+  const int nw = (int)((gridDim.x * blockDim.x) >> 5);
+  const int nvec = d / 8;   // 16-byte pieces per row
+  for (int t = gw; t < T; t += nw) {
+    const uint4* xs = kX ? reinterpret_cast<const uint4*>(a.x + (size_t)t * d) : nullptr;
+    const uint4* dys = kDy ? reinterpret_cast<const uint4*>(a.dy + (size_t)t * d) : nullptr;
+    for (int jb = 0; jb < k; jb += 32) {
+      const int j = jb + lane;
+      int prow = -1;
+      if (j < k && !kMeta) {
+        // tables and rows were built by an earlier dispatch of the same workspace
+        const size_t slot = (size_t)t * k + j;
+        prow = a.prow_of_slot[slot];
+        if (kDy && prow >= 0) a.gate_of_prow[prow] = a.gates[slot];
+      } else if (j < k) {
+        const size_t slot = (size_t)t * k + j;
+        const int e = a.idx[slot];
+        const bool valid = e >= 0 && e < E;
+        const int r = valid ? a.rank[slot] : 0;
+        const bool kept = valid && r >= 0 && r < tb->kept[e];
+        prow = kept ? tb->poff[e] + r : -1;
+        {
+          const int row = kept ? tb->offsets[e] + r : -1;
+          if (a.row_of_slot != nullptr) a.row_of_slot[slot] = row;
+          a.prow_of_slot[slot] = prow;
+          if (kept) {
+            if (a.token_of_row != nullptr) a.token_of_row[row] = t;
+            a.slot_of_prow[prow] = (int)slot;
+          }
+        }
+        if (kDy && kept) a.gate_of_prow[prow] = a.gates[slot];
+      }
+      const int ng = min(32, k - jb);
+      for (int v = lane; v < nvec; v += 32) {
+        uint4 vx = make_uint4(0, 0, 0, 0), vd = make_uint4(0, 0, 0, 0);
+        if (kX) vx = xs[v];
+        if (kDy) vd = dys[v];
+        for (int q = 0; q < ng; ++q) {
+          const int p = __shfl_sync(0xffffffffu, prow, q);
+          if (p >= 0) {
+            if (kX) reinterpret_cast<uint4*>(a.x_perm + (size_t)p * d)[v] = vx;
+            if (kDy) reinterpret_cast<uint4*>(a.dy_perm + (size_t)p * d)[v] = vd;
+          }
+        }
+        if (jb == 0) {
+          for (int s = 0; s < S; ++s) {
+            if (t >= tb->kept[E + s]) continue;
+            const size_t p = (size_t)tb->poff[E + s] + t;
+            if (kX) reinterpret_cast<uint4*>(a.x_perm + p * d)[v] = vx;
+            if (kDy) reinterpret_cast<uint4*>(a.dy_perm + p * d)[v] = vd;
+          }
+        }
+      }
+    }
+    if (lane < S && t < tb->kept[E + lane]) {
+      const size_t p = (size_t)tb->poff[E + lane] + t;
+      if (kMeta) a.slot_of_prow[p] = -2;
+      if (kDy) a.gate_of_prow[p] = 1.f;
+    }
+  }
+  // zero the pad rows of every segment
+  const int G = tb->G;
+  const int total_pad = tb->total_pad;
+  for (int p = gw; p < total_pad; p += nw) {
+    int lo = 0, hi = G - 1;   // segment g with pad_start[g] <= p < pad_start[g+1]
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (tb->pad_start[mid] <= p) lo = mid; else hi = mid - 1;
+    }
+    const size_t row = (size_t)tb->poff[lo] + tb->kept[lo] + (p - tb->pad_start[lo]);
+    const uint4 z = make_uint4(0, 0, 0, 0);
+    for (int v = lane; v < nvec; v += 32) {
+      if (kX) reinterpret_cast<uint4*>(a.x_perm + row * d)[v] = z;
+      if (kDy) reinterpret_cast<uint4*>(a.dy_perm + row * d)[v] = z;
+    }
+    if (lane == 0) {
+      if (kMeta) a.slot_of_prow[row] = -1;
+      if (kDy) a.gate_of_prow[row] = 0.f;
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_dispatch_scan(const Cfg& c, const Layout& L, const DispatchArgs& a, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(reinterpret_cast<char*>(a.hdr) + kHdrResetOffset, 0, kHdrResetBytes, s);
+  if (e != cudaSuccess) return e;
+  e = cudaMemsetAsync(a.scan_status, 0, (size_t)L.nscan * c.E * sizeof(uint32_t), s);
+  if (e != cudaSuccess) return e;
+  const int N = c.T * c.k;
+  prof_mark(kKScan, s, true);
+  dispatch_scan_kernel<<<L.nscan, kScanThreads, 0, s>>>(a, N, c.T, c.E, c.S, c.C, L.nscan, L.rows);
+  prof_mark(kKScan, s, false);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dispatch_gather(const Cfg& c, const Layout& L, const DispatchArgs& a,
+                                   bool write_meta, bool gather_x, bool gather_dy, cudaStream_t s) {
+  (void)L;
+  const int blocks = num_sms() * 8;
+  if (!(write_meta && gather_x) && !(!write_meta && gather_dy && !gather_x)) return cudaErrorInvalidValue;
+  prof_mark(kKGather, s, true);
+  if (write_meta && gather_x && gather_dy)
+    dispatch_gather_kernel<true, true, true><<<blocks, 256, 0, s>>>(a, c.T, c.k, c.E, c.S, c.d);
+  else if (write_meta && gather_x)
+    dispatch_gather_kernel<true, true, false><<<blocks, 256, 0, s>>>(a, c.T, c.k, c.E, c.S, c.d);
+  else
+    dispatch_gather_kernel<false, false, true><<<blocks, 256, 0, s>>>(a, c.T, c.k, c.E, c.S, c.d);
+  prof_mark(kKGather, s, false);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

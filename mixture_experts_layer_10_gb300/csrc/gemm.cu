@@ -1,0 +1,725 @@
+// Grouped expert GEMMs on the 5th-generation tensor cores (tcgen05 + TMEM), fed by TMA.
+//
+// The pages' point (Piper explainer and technical summary: fine-grained experts turn the FFN into
+// many tall-and-skinny GEMMs that use the GPU poorly; MoEBlaze, Methodology item 2: fused expert
+// kernels with dispatch, and recompute instead of stored activations) is met here by one
+// persistent, warp-specialised kernel per GEMM family over all experts at once:
+//
+//   warp 0      TMA producer: loads operand tiles into a ring of shared-memory stages
+//   warp 1      MMA issuer: one thread issues tcgen05.mma into TMEM accumulators, commits each
+//               stage back to the producer and each finished tile to the epilogue
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (128 lanes = 128 rows), fused
+//               element-wise work, bf16 stores
+//
+// Rows are the dispatch's padded expert segments (multiples of 128), so every 128-row M tile
+// belongs to one expert and the per-expert tile scheduler is a table walk done identically by
+// the three roles.  Every wait is bounded (MOE_ERR_TIMEOUT instead of a hang).
+//
+// Problems (BM = 128, BK = 64, operands bf16, accumulators fp32):
+//   FwdGateUp  H    = silu(X Wg^T) * (X Wu^T)              A=X K-major, B=[Wg;Wu] K-major, N=256
+//   FwdDown    O    = H Wd^T                               A=H K-major, B=Wd K-major,      N=256
+//   BwdFused   a,b  = X [Wg;Wu]^T ; dh' = dY Wd  (recompute + dgrad of the down projection)
+//              epilogue: h = silu(a) b, dg += dh'.h, dh = g dh', dA = dh b silu'(a),
+//              dB = dh silu(a), Hg = g h                  N = 128 (a, b, dh': 384 TMEM columns)
+//   Wgrad      dWg = dA^T X, dWu = dB^T X, dWd = dY^T Hg   A and B MN-major, K = segment rows
+//   DgradX     dX   = dA Wg + dB Wu                        A K-major, B MN-major, K = 2 d_ff
+#include <algorithm>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kThreads = 192;
+constexpr uint32_t kTileA = kBM * kBK * 2;   // 16 KB: 128 rows x 64 bf16 (K-major)
+constexpr uint32_t kBox = 64 * kBK * 2;      // 8 KB: a 64 x 64 box (MN-major)
+constexpr int kChunkM = 32;                  // m-tiles per L2 reuse chunk of a segment
+
+struct Job {
+  int seg, m0, n0, kiters, kbase, sub;
+};
+
+struct SegSmem {
+  int G;
+  int n_mtiles;
+  int poff[kMaxG + 1];
+  int seg_order[kMaxG];
+};
+
+__device__ __forceinline__ void load_segs(SegSmem& s, const Tables* tb) {
+  if (threadIdx.x == 0) {
+    s.G = tb->G;
+    s.n_mtiles = tb->n_mtiles;
+  }
+  for (int i = threadIdx.x; i <= kMaxG; i += blockDim.x) {
+    s.poff[i] = tb->poff[i];
+    if (i < kMaxG) s.seg_order[i] = tb->seg_order[i];
+  }
+}
+
+// Row-tiled problems: tile t -> (segment, m-tile, n-tile).  Segments in index order; inside a
+// segment, chunks of up to 32 m-tiles x all n-tiles with the m-tile fastest, so the CTAs working
+// at the same time share one operand panel of each kind in L2.
+__device__ __forceinline__ Job row_job(const SegSmem& s, int t, int nt, int bn, int kiters) {
+  const int mt_of_t = t / nt;
+  int lo = 0, hi = s.G - 1;   // last segment whose first m-tile <= mt_of_t
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (s.poff[mid] / kBM <= mt_of_t) lo = mid; else hi = mid - 1;
+  }
+  const int seg = lo;
+  const int mstart = s.poff[seg] / kBM;
+  const int mt = (s.poff[seg + 1] - s.poff[seg]) / kBM;
+  const int local = t - mstart * nt;
+  const int c = local / (kChunkM * nt);
+  const int base = c * kChunkM;
+  const int cm = min(kChunkM, mt - base);
+  const int r = local - c * kChunkM * nt;
+  Job j;
+  j.seg = seg;
+  j.m0 = s.poff[seg] + (base + r % cm) * kBM;
+  j.n0 = (r / cm) * bn;
+  j.kiters = kiters;
+  j.kbase = 0;
+  j.sub = 0;
+  return j;
+}
+
+// ---------------------------------------------------------------------------------------------
+// Problem policies
+// ---------------------------------------------------------------------------------------------
+
+struct FwdGateUp {
+  static constexpr int kId = kKGateUp;
+  static constexpr int kStages = 4;
+  static constexpr uint32_t kStageBytes = kTileA + 2 * kTileA;   // X tile + Wg tile + Wu tile
+  static constexpr int kAccCols = 256;
+  static constexpr int kAccBufs = 2;
+  static constexpr int kTmemCols = 512;
+  static constexpr uint32_t kIdesc = idesc_bf16(128, 256, false, false);
+  struct Params {
+    CUtensorMap tmX, tmWg, tmWu;
+    uint16_t* H;
+    int f, d, nt;
+    Hdr* hdr;
+    const Tables* tabs;
+  };
+  __device__ static int num_tiles(const Params& p, const SegSmem& s) { return s.n_mtiles * p.nt; }
+  __device__ static Job job(const Params& p, const SegSmem& s, int t) {
+    return row_job(s, t, p.nt, 128, p.d / kBK);
+  }
+  __device__ static void prefetch(const Params& p) {
+    tma_prefetch(&p.tmX); tma_prefetch(&p.tmWg); tma_prefetch(&p.tmWu);
+  }
+  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint64_t* bar) {
+    tma_load_2d(st, &p.tmX, bar, kit * kBK, j.m0);
+    tma_load_3d(st + kTileA, &p.tmWg, bar, kit * kBK, j.n0, j.seg);
+    tma_load_3d(st + 2 * kTileA, &p.tmWu, bar, kit * kBK, j.n0, j.seg);
+  }
+  __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt) {
+#pragma unroll
+    for (int kk = 0; kk < kBK / 16; ++kk)
+      umma_bf16(dt, sdesc_kmajor(sa + kk * 32), sdesc_kmajor(sa + kTileA + kk * 32), kIdesc,
+                (kit | kk) != 0);
+  }
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row) {
+    uint16_t* out = p.H + (size_t)(j.m0 + row) * p.f + j.n0;
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 32) {
+      if (j.n0 + c >= p.f) break;
+      uint32_t ga[32], ub[32];
+      tmem_ld32(ta + c, ga);
+      tmem_ld32(ta + 128 + c, ub);
+      tmem_ld_wait();
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float a0 = __uint_as_float(ga[2 * i]), a1 = __uint_as_float(ga[2 * i + 1]);
+        const float h0 = a0 / (1.f + __expf(-a0)) * __uint_as_float(ub[2 * i]);
+        const float h1 = a1 / (1.f + __expf(-a1)) * __uint_as_float(ub[2 * i + 1]);
+        pk[i] = pack_bf16(h0, h1);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(out + c);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    }
+  }
+  __device__ static void epilogue_zero(const Params&, const Job&, int) {}
+};
+
+// Shared by FwdDown and DgradX: fp32 accumulator [128 x 256] -> bf16 rows of width `ncols`.
+__device__ __forceinline__ void store_acc_rows(uint16_t* base, int ld, int n0, int ncols,
+                                               uint32_t ta) {
+#pragma unroll 1
+  for (int c = 0; c < 256; c += 32) {
+    if (n0 + c >= ncols) break;
+    uint32_t v[32];
+    tmem_ld32(ta + c, v);
+    tmem_ld_wait();
+    uint32_t pk[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+    uint4* dst = reinterpret_cast<uint4*>(base + n0 + c);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+  }
+  (void)ld;
+}
+
+struct FwdDown {
+  static constexpr int kId = kKDown;
+  static constexpr int kStages = 4;
+  static constexpr uint32_t kStageBytes = kTileA + 2 * kTileA;   // H tile + Wd tile (256 rows)
+  static constexpr int kAccCols = 256;
+  static constexpr int kAccBufs = 2;
+  static constexpr int kTmemCols = 512;
+  static constexpr uint32_t kIdesc = idesc_bf16(128, 256, false, false);
+  struct Params {
+    CUtensorMap tmH, tmWd;
+    uint16_t* O;
+    int f, d, nt;
+    Hdr* hdr;
+    const Tables* tabs;
+  };
+  __device__ static int num_tiles(const Params& p, const SegSmem& s) { return s.n_mtiles * p.nt; }
+  __device__ static Job job(const Params& p, const SegSmem& s, int t) {
+    return row_job(s, t, p.nt, 256, p.f / kBK);
+  }
+  __device__ static void prefetch(const Params& p) { tma_prefetch(&p.tmH); tma_prefetch(&p.tmWd); }
+  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint64_t* bar) {
+    tma_load_2d(st, &p.tmH, bar, kit * kBK, j.m0);
+    tma_load_3d(st + kTileA, &p.tmWd, bar, kit * kBK, j.n0, j.seg);
+  }
+  __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt) {
+#pragma unroll
+    for (int kk = 0; kk < kBK / 16; ++kk)
+      umma_bf16(dt, sdesc_kmajor(sa + kk * 32), sdesc_kmajor(sa + kTileA + kk * 32), kIdesc,
+                (kit | kk) != 0);
+  }
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row) {
+    store_acc_rows(p.O + (size_t)(j.m0 + row) * p.d, p.d, j.n0, p.d, ta);
+  }
+  __device__ static void epilogue_zero(const Params&, const Job&, int) {}
+};
+
+struct BwdFused {
+  static constexpr int kId = kKBwdFused;
+  static constexpr int kStages = 2;
+  // X tile, dY tile, [Wg;Wu] tile (256 rows), Wd slice as two 64 x 64 MN-major boxes
+  static constexpr uint32_t kStageBytes = 4 * kTileA + 2 * kBox;
+  static constexpr int kAccCols = 384;
+  static constexpr int kAccBufs = 1;
+  static constexpr int kTmemCols = 512;
+  static constexpr uint32_t kIdescAB = idesc_bf16(128, 256, false, false);
+  static constexpr uint32_t kIdescDh = idesc_bf16(128, 128, false, true);
+  struct Params {
+    CUtensorMap tmX, tmDY, tmWg, tmWu, tmWdT;
+    const float* gate_of_prow;
+    uint16_t *dA, *dB, *Hg;
+    float* dg_part;
+    int f, d, nt;
+    Hdr* hdr;
+    const Tables* tabs;
+  };
+  __device__ static int num_tiles(const Params& p, const SegSmem& s) { return s.n_mtiles * p.nt; }
+  __device__ static Job job(const Params& p, const SegSmem& s, int t) {
+    return row_job(s, t, p.nt, 128, p.d / kBK);
+  }
+  __device__ static void prefetch(const Params& p) {
+    tma_prefetch(&p.tmX); tma_prefetch(&p.tmDY); tma_prefetch(&p.tmWg); tma_prefetch(&p.tmWu);
+    tma_prefetch(&p.tmWdT);
+  }
+  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint64_t* bar) {
+    tma_load_2d(st, &p.tmX, bar, kit * kBK, j.m0);
+    tma_load_2d(st + kTileA, &p.tmDY, bar, kit * kBK, j.m0);
+    tma_load_3d(st + 2 * kTileA, &p.tmWg, bar, kit * kBK, j.n0, j.seg);
+    tma_load_3d(st + 3 * kTileA, &p.tmWu, bar, kit * kBK, j.n0, j.seg);
+    tma_load_3d(st + 4 * kTileA, &p.tmWdT, bar, j.n0, kit * kBK, j.seg);
+    tma_load_3d(st + 4 * kTileA + kBox, &p.tmWdT, bar, j.n0 + 64, kit * kBK, j.seg);
+  }
+  __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt) {
+#pragma unroll
+    for (int kk = 0; kk < kBK / 16; ++kk) {
+      const uint32_t acc = (kit | kk) != 0;
+      umma_bf16(dt, sdesc_kmajor(sa + kk * 32), sdesc_kmajor(sa + 2 * kTileA + kk * 32), kIdescAB, acc);
+      umma_bf16(dt + 256, sdesc_kmajor(sa + kTileA + kk * 32),
+                sdesc_mnmajor(sa + 4 * kTileA + kk * 2048, kBox), kIdescDh, acc);
+    }
+  }
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row) {
+    const size_t r = (size_t)(j.m0 + row);
+    const float g = p.gate_of_prow[r];
+    float dg = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 32) {
+      if (j.n0 + c >= p.f) break;
+      uint32_t va[32], vb[32], vd[32];
+      tmem_ld32(ta + c, va);
+      tmem_ld32(ta + 128 + c, vb);
+      tmem_ld32(ta + 256 + c, vd);
+      tmem_ld_wait();
+      uint32_t pa[16], pb[16], ph[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float o_da[2], o_db[2], o_h[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float a = __uint_as_float(va[2 * i + h]);
+          const float b = __uint_as_float(vb[2 * i + h]);
+          const float dhp = __uint_as_float(vd[2 * i + h]);
+          const float sg = 1.f / (1.f + __expf(-a));
+          const float sa = a * sg;
+          const float hv = sa * b;
+          dg = fmaf(dhp, hv, dg);
+          const float dh = g * dhp;
+          o_da[h] = dh * b * sg * (1.f + a * (1.f - sg));
+          o_db[h] = dh * sa;
+          o_h[h] = g * hv;
+        }
+        pa[i] = pack_bf16(o_da[0], o_da[1]);
+        pb[i] = pack_bf16(o_db[0], o_db[1]);
+        ph[i] = pack_bf16(o_h[0], o_h[1]);
+      }
+      uint4* da = reinterpret_cast<uint4*>(p.dA + r * p.f + j.n0 + c);
+      uint4* db = reinterpret_cast<uint4*>(p.dB + r * p.f + j.n0 + c);
+      uint4* hg = reinterpret_cast<uint4*>(p.Hg + r * p.f + j.n0 + c);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        da[q] = make_uint4(pa[4 * q], pa[4 * q + 1], pa[4 * q + 2], pa[4 * q + 3]);
+        db[q] = make_uint4(pb[4 * q], pb[4 * q + 1], pb[4 * q + 2], pb[4 * q + 3]);
+        hg[q] = make_uint4(ph[4 * q], ph[4 * q + 1], ph[4 * q + 2], ph[4 * q + 3]);
+      }
+    }
+    p.dg_part[r * p.nt + j.n0 / 128] = dg;
+  }
+  __device__ static void epilogue_zero(const Params&, const Job&, int) {}
+};
+
+struct DgradX {
+  static constexpr int kId = kKDgradX;
+  static constexpr int kStages = 4;
+  static constexpr uint32_t kStageBytes = kTileA + 4 * kBox;   // dA/dB tile + 4 MN boxes of W
+  static constexpr int kAccCols = 256;
+  static constexpr int kAccBufs = 2;
+  static constexpr int kTmemCols = 512;
+  static constexpr uint32_t kIdesc = idesc_bf16(128, 256, false, true);
+  struct Params {
+    CUtensorMap tmDA, tmDB, tmWgT, tmWuT;
+    uint16_t* dX;
+    int f, d, nt;
+    Hdr* hdr;
+    const Tables* tabs;
+  };
+  __device__ static int num_tiles(const Params& p, const SegSmem& s) { return s.n_mtiles * p.nt; }
+  __device__ static Job job(const Params& p, const SegSmem& s, int t) {
+    return row_job(s, t, p.nt, 256, 2 * p.f / kBK);
+  }
+  __device__ static void prefetch(const Params& p) {
+    tma_prefetch(&p.tmDA); tma_prefetch(&p.tmDB); tma_prefetch(&p.tmWgT); tma_prefetch(&p.tmWuT);
+  }
+  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint64_t* bar) {
+    const int nk = p.f / kBK;
+    const bool up = kit >= nk;
+    const int k0 = (up ? kit - nk : kit) * kBK;
+    tma_load_2d(st, up ? &p.tmDB : &p.tmDA, bar, k0, j.m0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      tma_load_3d(st + kTileA + i * kBox, up ? &p.tmWuT : &p.tmWgT, bar, j.n0 + 64 * i, k0, j.seg);
+  }
+  __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt) {
+#pragma unroll
+    for (int kk = 0; kk < kBK / 16; ++kk)
+      umma_bf16(dt, sdesc_kmajor(sa + kk * 32), sdesc_mnmajor(sa + kTileA + kk * 2048, kBox), kIdesc,
+                (kit | kk) != 0);
+  }
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row) {
+    store_acc_rows(p.dX + (size_t)(j.m0 + row) * p.d, p.d, j.n0, p.d, ta);
+  }
+  __device__ static void epilogue_zero(const Params&, const Job&, int) {}
+};
+
+struct Wgrad {
+  static constexpr int kId = kKWgrad;
+  static constexpr int kStages = 4;
+  static constexpr uint32_t kStageBytes = 2 * kBox + 4 * kBox;   // A: 128 MN; B: 256 MN
+  static constexpr int kAccCols = 256;
+  static constexpr int kAccBufs = 2;
+  static constexpr int kTmemCols = 512;
+  static constexpr uint32_t kIdesc = idesc_bf16(128, 256, true, true);
+  struct Params {
+    CUtensorMap tmDA, tmDB, tmX, tmDY, tmHg;   // all [rows, width] with 64 x 64 boxes
+    uint16_t *dWg, *dWu, *dWd;
+    int f, d;
+    int mt_f, nt_d, mt_d, nt_f, tps;           // tiles: dWg/dWu (mt_f x nt_d), dWd (mt_d x nt_f)
+    Hdr* hdr;
+    const Tables* tabs;
+  };
+  __device__ static int num_tiles(const Params& p, const SegSmem& s) { return s.G * p.tps; }
+  __device__ static Job job(const Params& p, const SegSmem& s, int t) {
+    const int pos = t / p.tps;
+    int r = t - pos * p.tps;
+    Job j;
+    j.seg = s.seg_order[pos];
+    j.kbase = s.poff[j.seg];
+    j.kiters = (s.poff[j.seg + 1] - s.poff[j.seg]) / kBK;
+    const int gu = p.mt_f * p.nt_d;
+    if (r < 2 * gu) {
+      j.sub = r / gu;
+      r -= j.sub * gu;
+      j.m0 = (r / p.nt_d) * kBM;
+      j.n0 = (r % p.nt_d) * 256;
+    } else {
+      r -= 2 * gu;
+      j.sub = 2;
+      j.m0 = (r / p.nt_f) * kBM;
+      j.n0 = (r % p.nt_f) * 256;
+    }
+    return j;
+  }
+  __device__ static void prefetch(const Params& p) {
+    tma_prefetch(&p.tmDA); tma_prefetch(&p.tmDB); tma_prefetch(&p.tmX); tma_prefetch(&p.tmDY);
+    tma_prefetch(&p.tmHg);
+  }
+  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint64_t* bar) {
+    const int row = j.kbase + kit * kBK;
+    const CUtensorMap* ta = j.sub == 0 ? &p.tmDA : (j.sub == 1 ? &p.tmDB : &p.tmDY);
+    const CUtensorMap* tb = j.sub == 2 ? &p.tmHg : &p.tmX;
+    tma_load_2d(st, ta, bar, j.m0, row);
+    tma_load_2d(st + kBox, ta, bar, j.m0 + 64, row);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) tma_load_2d(st + (2 + i) * kBox, tb, bar, j.n0 + 64 * i, row);
+  }
+  __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt) {
+#pragma unroll
+    for (int kk = 0; kk < kBK / 16; ++kk)
+      umma_bf16(dt, sdesc_mnmajor(sa + kk * 2048, kBox), sdesc_mnmajor(sa + 2 * kBox + kk * 2048, kBox),
+                kIdesc, (kit | kk) != 0);
+  }
+  __device__ static uint16_t* out_row(const Params& p, const Job& j, int row, int& ncols, bool& ok) {
+    const int M = j.sub == 2 ? p.d : p.f;
+    ncols = j.sub == 2 ? p.f : p.d;
+    const int m = j.m0 + row;
+    ok = m < M;
+    uint16_t* W = j.sub == 0 ? p.dWg : (j.sub == 1 ? p.dWu : p.dWd);
+    return W + ((size_t)j.seg * M + (ok ? m : 0)) * ncols;
+  }
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row) {
+    int ncols;
+    bool ok;
+    uint16_t* base = out_row(p, j, row, ncols, ok);
+#pragma unroll 1
+    for (int c = 0; c < 256; c += 32) {
+      if (j.n0 + c >= ncols) break;
+      uint32_t v[32];
+      tmem_ld32(ta + c, v);
+      tmem_ld_wait();
+      if (!ok) continue;
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+      uint4* dst = reinterpret_cast<uint4*>(base + j.n0 + c);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    }
+  }
+  // An expert that received no rows has a zero gradient.
+  __device__ static void epilogue_zero(const Params& p, const Job& j, int row) {
+    int ncols;
+    bool ok;
+    uint16_t* base = out_row(p, j, row, ncols, ok);
+    if (!ok) return;
+    for (int c = 0; c < 256 && j.n0 + c < ncols; c += 8)
+      *reinterpret_cast<uint4*>(base + j.n0 + c) = make_uint4(0, 0, 0, 0);
+  }
+};
+
+// ---------------------------------------------------------------------------------------------
+// The persistent warp-specialised kernel
+// ---------------------------------------------------------------------------------------------
+
+template <class P>
+constexpr size_t smem_bytes() {
+  return 1024 + (size_t)P::kStages * P::kStageBytes + 256 + sizeof(SegSmem);
+}
+
+template <class P>
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ typename P::Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)P::kStages * P::kStageBytes);
+  uint64_t* empty = full + P::kStages;
+  uint64_t* tfull = empty + P::kStages;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  SegSmem& segs = *reinterpret_cast<SegSmem*>(smem + (size_t)P::kStages * P::kStageBytes + 256);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  load_segs(segs, p.tabs);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    P::prefetch(p);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, P::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int ntiles = P::num_tiles(p, segs);
+  const uint64_t limit = wait_limit_ns(p.hdr);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int t = blockIdx.x; t < ntiles && !*abort_flag; t += gridDim.x) {
+        const Job j = P::job(p, segs, t);
+        for (int kit = 0; kit < j.kiters; ++kit) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, limit, abort_flag)) {
+            record_error(p.hdr, MOE_ERR_TIMEOUT, kSiteGemmProducer);
+            *abort_flag = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], P::kStageBytes);
+          P::load(p, j, kit, stages + (size_t)stage * P::kStageBytes, &full[stage]);
+          if (++stage == P::kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int t = blockIdx.x; t < ntiles && !*abort_flag; t += gridDim.x) {
+        const Job j = P::job(p, segs, t);
+        if (j.kiters == 0) continue;
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, limit, abort_flag)) {
+          record_error(p.hdr, MOE_ERR_TIMEOUT, kSiteGemmMma);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t dt = tmem_base + (uint32_t)(acc * P::kAccCols);
+        bool ok = true;
+        for (int kit = 0; kit < j.kiters; ++kit) {
+          if (!mbar_wait(&full[stage], phase, limit, abort_flag)) {
+            record_error(p.hdr, MOE_ERR_TIMEOUT, kSiteGemmMma);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          P::mma(j, kit, smem_u32(stages + (size_t)stage * P::kStageBytes), dt);
+          umma_commit(&empty[stage]);
+          if (++stage == P::kStages) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        if (++acc == P::kAccBufs) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+    }
+  } else {
+    const int q = warp & 3;   // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+      const Job j = P::job(p, segs, t);
+      if (j.kiters == 0) {
+        P::epilogue_zero(p, j, row);
+        continue;
+      }
+      if (!mbar_wait(&tfull[acc], acc_phase, limit, abort_flag)) {
+        record_error(p.hdr, MOE_ERR_TIMEOUT, kSiteGemmEpilogue);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      P::epilogue(p, j, tmem_base + (uint32_t)(acc * P::kAccCols) + ((uint32_t)(q * 32) << 16), row);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (++acc == P::kAccBufs) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, P::kTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Host side: tensor maps and launches
+// ---------------------------------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2D bf16 tensor [rows, width] (width contiguous) with a box of box_w x box_r, 128-byte swizzle.
+bool map_2d(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows, uint32_t box_w,
+            uint32_t box_r) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {width, rows};
+  const cuuint64_t strides[1] = {width * 2};
+  const cuuint32_t box[2] = {box_w, box_r};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3D bf16 tensor [G, rows, width] with a box of box_w x box_r x 1, 128-byte swizzle.
+bool map_3d(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows, uint64_t G,
+            uint32_t box_w, uint32_t box_r) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {width, rows, G};
+  const cuuint64_t strides[2] = {width * 2, width * rows * 2};
+  const cuuint32_t box[3] = {box_w, box_r, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <class P>
+cudaError_t launch(const typename P::Params& p, cudaStream_t s) {
+  constexpr size_t smem = smem_bytes<P>();
+  static_assert(smem <= 232448, "shared memory per block");
+  cudaError_t e = cudaFuncSetAttribute(gemm_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  prof_mark(P::kId, s, true);
+  gemm_kernel<P><<<num_sms(), kThreads, smem, s>>>(p);
+  prof_mark(P::kId, s, false);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_fwd(const Cfg& c, const Layout& L, const FfnFwdArgs& a, cudaStream_t s) {
+  const uint64_t rows = (uint64_t)L.rows;
+  FwdGateUp::Params p1{};
+  if (!map_2d(&p1.tmX, a.x_perm, c.d, rows, 64, 128) ||
+      !map_3d(&p1.tmWg, a.Wg, c.d, c.f, c.G, 64, 128) || !map_3d(&p1.tmWu, a.Wu, c.d, c.f, c.G, 64, 128))
+    return cudaErrorInvalidValue;
+  p1.H = a.h;
+  p1.f = c.f;
+  p1.d = c.d;
+  p1.nt = (c.f + 127) / 128;
+  p1.hdr = a.hdr;
+  p1.tabs = a.tabs;
+  cudaError_t e = launch<FwdGateUp>(p1, s);
+  if (e != cudaSuccess) return e;
+  FwdDown::Params p2{};
+  if (!map_2d(&p2.tmH, a.h, c.f, rows, 64, 128) || !map_3d(&p2.tmWd, a.Wd, c.f, c.d, c.G, 64, 256))
+    return cudaErrorInvalidValue;
+  p2.O = a.o_perm;
+  p2.f = c.f;
+  p2.d = c.d;
+  p2.nt = (c.d + 255) / 256;
+  p2.hdr = a.hdr;
+  p2.tabs = a.tabs;
+  return launch<FwdDown>(p2, s);
+}
+
+cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, cudaStream_t s) {
+  const uint64_t rows = (uint64_t)L.rows;
+  BwdFused::Params p3{};
+  if (!map_2d(&p3.tmX, a.x_perm, c.d, rows, 64, 128) || !map_2d(&p3.tmDY, a.dy_perm, c.d, rows, 64, 128) ||
+      !map_3d(&p3.tmWg, a.Wg, c.d, c.f, c.G, 64, 128) || !map_3d(&p3.tmWu, a.Wu, c.d, c.f, c.G, 64, 128) ||
+      !map_3d(&p3.tmWdT, a.Wd, c.f, c.d, c.G, 64, 64))
+    return cudaErrorInvalidValue;
+  p3.gate_of_prow = a.gate_of_prow;
+  p3.dA = a.dA;
+  p3.dB = a.dB;
+  p3.Hg = a.Hg;
+  p3.dg_part = a.dg_part;
+  p3.f = c.f;
+  p3.d = c.d;
+  p3.nt = L.ntf;
+  p3.hdr = a.hdr;
+  p3.tabs = a.tabs;
+  cudaError_t e = launch<BwdFused>(p3, s);
+  if (e != cudaSuccess) return e;
+
+  Wgrad::Params p4{};
+  if (!map_2d(&p4.tmDA, a.dA, c.f, rows, 64, 64) || !map_2d(&p4.tmDB, a.dB, c.f, rows, 64, 64) ||
+      !map_2d(&p4.tmX, a.x_perm, c.d, rows, 64, 64) || !map_2d(&p4.tmDY, a.dy_perm, c.d, rows, 64, 64) ||
+      !map_2d(&p4.tmHg, a.Hg, c.f, rows, 64, 64))
+    return cudaErrorInvalidValue;
+  p4.dWg = a.dWg;
+  p4.dWu = a.dWu;
+  p4.dWd = a.dWd;
+  p4.f = c.f;
+  p4.d = c.d;
+  p4.mt_f = (c.f + 127) / 128;
+  p4.nt_d = (c.d + 255) / 256;
+  p4.mt_d = (c.d + 127) / 128;
+  p4.nt_f = (c.f + 255) / 256;
+  p4.tps = 2 * p4.mt_f * p4.nt_d + p4.mt_d * p4.nt_f;
+  p4.hdr = a.hdr;
+  p4.tabs = a.tabs;
+  e = launch<Wgrad>(p4, s);
+  if (e != cudaSuccess) return e;
+
+  DgradX::Params p5{};
+  if (!map_2d(&p5.tmDA, a.dA, c.f, rows, 64, 128) || !map_2d(&p5.tmDB, a.dB, c.f, rows, 64, 128) ||
+      !map_3d(&p5.tmWgT, a.Wg, c.d, c.f, c.G, 64, 64) || !map_3d(&p5.tmWuT, a.Wu, c.d, c.f, c.G, 64, 64))
+    return cudaErrorInvalidValue;
+  p5.dX = a.dx_perm;
+  p5.f = c.f;
+  p5.d = c.d;
+  p5.nt = (c.d + 255) / 256;
+  p5.hdr = a.hdr;
+  p5.tabs = a.tabs;
+  return launch<DgradX>(p5, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,468 @@
+// Router: logits = x W_r (+ b), softmax over the E routed experts, top-k by logit (ties to the
+// lower expert index), gates; and its backward with the selection held fixed.
+//
+// The logits are an fp32 SIMT tile product (x is bf16, W_r fp32, E <= 256 columns); selection,
+// softmax and the gate gradient run warp-per-token with shuffle reductions.  Sources: the Piper
+// explainer ("the problem": a router sends each token to a few experts) and the MoEBlaze summary
+// (Limitations: static top-k routing); the formulas are the plain softmax-then-top-k reading.
+#include <algorithm>
+#include <cfloat>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kKC = 32;   // k-chunk staged in shared memory
+
+// Tile shapes per expert bucket: BT tokens x EB experts per block; a thread owns TM tokens x TN
+// experts and a 1/KS share of each k-chunk.
+template <int EB> struct RouteShape;
+template <> struct RouteShape<8>   { static constexpr int BT = 32, TM = 1, TN = 8, KS = 8; };
+template <> struct RouteShape<16>  { static constexpr int BT = 32, TM = 2, TN = 8, KS = 8; };
+template <> struct RouteShape<32>  { static constexpr int BT = 32, TM = 2, TN = 8, KS = 4; };
+template <> struct RouteShape<64>  { static constexpr int BT = 64, TM = 4, TN = 4, KS = 1; };
+template <> struct RouteShape<128> { static constexpr int BT = 64, TM = 4, TN = 8, KS = 1; };
+template <> struct RouteShape<256> { static constexpr int BT = 32, TM = 4, TN = 8, KS = 1; };
+
+template <int EB>
+struct LogitSmem {
+  using S = RouteShape<EB>;
+  float xs[kKC][S::BT + 4];     // x chunk, k-major
+  float ws[kKC][EB];            // W_r chunk
+  float red[S::KS > 1 ? S::KS : 1][S::BT][EB + 1];   // k-split partials, then the logits tile
+};
+
+// logits tile [BT x EB] of tokens t0.. into sm.red[0] (bias added, experts >= E left at 0).
+template <int EB>
+__device__ void logits_tile(LogitSmem<EB>& sm, const uint16_t* __restrict__ x,
+                            const float* __restrict__ W_r, const float* __restrict__ b_r, int T,
+                            int d, int E, int t0) {
+  using S = RouteShape<EB>;
+  constexpr int TX = S::BT / S::TM, TY = EB / S::TN;
+  static_assert(TX * TY * S::KS == kThreads, "thread tiling");
+  const int tid = threadIdx.x;
+  const int ks = tid / (TX * TY);
+  const int ty = (tid / TX) % TY;
+  const int tx = tid % TX;
+  float acc[S::TM][S::TN];
+#pragma unroll
+  for (int i = 0; i < S::TM; ++i)
+#pragma unroll
+    for (int j = 0; j < S::TN; ++j) acc[i][j] = 0.f;
+
+  for (int k0 = 0; k0 < d; k0 += kKC) {
+    // x chunk: BT rows x 32 bf16 = 4 16-byte pieces per row
+    for (int p = tid; p < S::BT * 4; p += kThreads) {
+      const int t = p % S::BT, q = p / S::BT;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (t0 + t < T)
+        v = *reinterpret_cast<const uint4*>(x + (size_t)(t0 + t) * d + k0 + q * 8);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        sm.xs[q * 8 + 2 * m][t] = bf16_lo(w[m]);
+        sm.xs[q * 8 + 2 * m + 1][t] = bf16_hi(w[m]);
+      }
+    }
+    for (int p = tid; p < kKC * EB; p += kThreads) {
+      const int kk = p / EB, e = p % EB;
+      sm.ws[kk][e] = (e < E) ? W_r[(size_t)(k0 + kk) * E + e] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int kk = ks; kk < kKC; kk += S::KS) {
+      float xv[S::TM], wv[S::TN];
+#pragma unroll
+      for (int i = 0; i < S::TM; ++i) xv[i] = sm.xs[kk][tx * S::TM + i];
+#pragma unroll
+      for (int j = 0; j < S::TN; ++j) wv[j] = sm.ws[kk][ty * S::TN + j];
+#pragma unroll
+      for (int i = 0; i < S::TM; ++i)
+#pragma unroll
+        for (int j = 0; j < S::TN; ++j) acc[i][j] = fmaf(xv[i], wv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < S::TM; ++i)
+#pragma unroll
+    for (int j = 0; j < S::TN; ++j) sm.red[ks][tx * S::TM + i][ty * S::TN + j] = acc[i][j];
+  __syncthreads();
+  // fixed-order k-split reduction plus bias
+  for (int p = tid; p < S::BT * EB; p += kThreads) {
+    const int t = p / EB, e = p % EB;
+    float v = sm.red[0][t][e];
+#pragma unroll
+    for (int s = 1; s < S::KS; ++s) v += sm.red[s][t][e];
+    if (b_r != nullptr && e < E) v += b_r[e];
+    sm.red[0][t][e] = v;
+  }
+  __syncthreads();
+}
+
+constexpr int vals_per_lane(int EB) { return EB >= 32 ? EB / 32 : 1; }
+
+// Warp-wide (value, index) argmax: larger value wins, equal values go to the lower index.
+__device__ __forceinline__ void warp_argmax(float& v, int& i) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, off);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, off);
+    if (ov > v || (ov == v && oi < i)) {
+      v = ov;
+      i = oi;
+    }
+  }
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+  return v;
+}
+
+template <int EB>
+__global__ void __launch_bounds__(kThreads) route_fwd_kernel(RouteArgs a, int T, int d, int E,
+                                                             int k, int renorm) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  LogitSmem<EB>& sm = *reinterpret_cast<LogitSmem<EB>*>(smem_raw);
+  using S = RouteShape<EB>;
+  constexpr int NV = vals_per_lane(EB);
+  const int t0 = blockIdx.x * S::BT;
+  logits_tile<EB>(sm, a.x, a.W_r, a.b_r, T, d, E, t0);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int tt = warp; tt < S::BT; tt += kThreads / 32) {
+    const int t = t0 + tt;
+    if (t >= T) break;
+    float v[NV];
+    int slot[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int e = lane + 32 * i;
+      v[i] = (e < E) ? sm.red[0][tt][e] : -INFINITY;
+      slot[i] = -1;
+      if (a.logits != nullptr && e < E) a.logits[(size_t)t * E + e] = v[i];
+    }
+    float m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) m = fmaxf(m, v[i]);
+    m = warp_max(m);
+    float z = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) z += (lane + 32 * i < E) ? expf(v[i] - m) : 0.f;
+    z = warp_sum(z);
+    // top-k: k rounds of warp argmax over the not-yet-selected experts
+    for (int r = 0; r < k; ++r) {
+      float bv = -INFINITY;
+      int bi = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E && slot[i] < 0 && (v[i] > bv || (v[i] == bv && e < bi))) {
+          bv = v[i];
+          bi = e;
+        }
+      }
+      warp_argmax(bv, bi);
+#pragma unroll
+      for (int i = 0; i < NV; ++i)
+        if (lane + 32 * i == bi) slot[i] = r;
+    }
+    float zsel = 0.f;
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+      if (slot[i] >= 0) zsel += expf(v[i] - m);
+    zsel = warp_sum(zsel);
+    const float denom = renorm ? zsel : z;
+#pragma unroll
+    for (int i = 0; i < NV; ++i)
+      if (slot[i] >= 0) {
+        a.idx[(size_t)t * k + slot[i]] = lane + 32 * i;
+        a.gates[(size_t)t * k + slot[i]] = expf(v[i] - m) / denom;
+      }
+  }
+}
+
+// Router backward, part 1: per token dlogits (recomputing the softmax when not renormalised),
+// and per-block db partials.
+template <int EB>
+__global__ void __launch_bounds__(kThreads) router_dlogits_kernel(RouterBwdArgs a, int T, int d,
+                                                                  int E, int k, int renorm) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  LogitSmem<EB>& sm = *reinterpret_cast<LogitSmem<EB>*>(smem_raw);
+  using S = RouteShape<EB>;
+  constexpr int NV = vals_per_lane(EB);
+  __shared__ float dsel[kThreads / 32][EB];
+  __shared__ float dbw[kThreads / 32][EB];
+  const int t0 = blockIdx.x * S::BT;
+  if (!renorm) logits_tile<EB>(sm, a.x, a.W_r, a.b_r, T, d, E, t0);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  for (int e = lane; e < EB; e += 32) dbw[warp][e] = 0.f;
+  __syncwarp();
+  for (int tt = warp; tt < S::BT; tt += kThreads / 32) {
+    const int t = t0 + tt;
+    if (t >= T) break;
+    // s = sum_j dg_j g_j, and dsel[e] = dg of the slot that selected e
+    for (int e = lane; e < EB; e += 32) dsel[warp][e] = 0.f;
+    __syncwarp();
+    float s = 0.f;
+    for (int j = lane; j < k; j += 32) {
+      const float dg = a.dgates[(size_t)t * k + j];
+      const float g = a.gates[(size_t)t * k + j];
+      const int e = a.idx[(size_t)t * k + j];
+      s += dg * g;
+      if (e >= 0 && e < E) atomicAdd(&dsel[warp][e], renorm ? g * dg : dg);
+    }
+    s = warp_sum(s);
+    __syncwarp();
+    if (renorm) {
+      // dl_{idx_j} = g_j (dg_j - s); dsel holds g_j dg_j, so subtract g_j s per selected slot
+      for (int j = lane; j < k; j += 32) {
+        const int e = a.idx[(size_t)t * k + j];
+        if (e >= 0 && e < E) atomicAdd(&dsel[warp][e], -a.gates[(size_t)t * k + j] * s);
+      }
+      __syncwarp();
+      for (int e = lane; e < E; e += 32) {
+        const float dl = dsel[warp][e];
+        a.dlogits[(size_t)t * E + e] = dl;
+        dbw[warp][e] += dl;
+      }
+    } else {
+      float v[NV];
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = (e < E) ? sm.red[0][tt][e] : -INFINITY;
+      }
+      float m = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) m = fmaxf(m, v[i]);
+      m = warp_max(m);
+      float z = 0.f;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) z += (lane + 32 * i < E) ? expf(v[i] - m) : 0.f;
+      z = warp_sum(z);
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int e = lane + 32 * i;
+        if (e < E) {
+          const float p = expf(v[i] - m) / z;
+          const float dl = p * (dsel[warp][e] - s);
+          a.dlogits[(size_t)t * E + e] = dl;
+          dbw[warp][e] += dl;
+        }
+      }
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kThreads) {
+    float acc = 0.f;
+    for (int w = 0; w < kThreads / 32; ++w) acc += dbw[w][e];
+    a.db_part[(size_t)blockIdx.x * E + e] = acc;
+  }
+}
+
+// Router backward, part 2: dW_r partials over token splits, dW_r[i][e] = sum_t x[t][i] dl[t][e].
+template <int EB> struct DwrShape;
+template <> struct DwrShape<8>   { static constexpr int TM = 2, TN = 8, KS = 8; };
+template <> struct DwrShape<16>  { static constexpr int TM = 4, TN = 8, KS = 8; };
+template <> struct DwrShape<32>  { static constexpr int TM = 4, TN = 8, KS = 4; };
+template <> struct DwrShape<64>  { static constexpr int TM = 4, TN = 4, KS = 1; };
+template <> struct DwrShape<128> { static constexpr int TM = 4, TN = 8, KS = 1; };
+template <> struct DwrShape<256> { static constexpr int TM = 8, TN = 8, KS = 1; };
+
+constexpr int kDwrRows = 64;   // d-rows per block
+
+template <int EB>
+struct DwrSmem {
+  using S = DwrShape<EB>;
+  float xs[kKC][kDwrRows + 4];
+  float ls[kKC][EB];
+  float red[S::KS > 1 ? S::KS : 1][kDwrRows][EB + 1];
+};
+
+template <int EB>
+__global__ void __launch_bounds__(kThreads) router_dwr_kernel(RouterBwdArgs a, int T, int d, int E,
+                                                              int tokens_per_split) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  DwrSmem<EB>& sm = *reinterpret_cast<DwrSmem<EB>*>(smem_raw);
+  using S = DwrShape<EB>;
+  constexpr int TX = kDwrRows / S::TM, TY = EB / S::TN;
+  static_assert(TX * TY * S::KS == kThreads, "thread tiling");
+  const int tid = threadIdx.x;
+  const int ks = tid / (TX * TY), ty = (tid / TX) % TY, tx = tid % TX;
+  const int i0 = blockIdx.x * kDwrRows;
+  const int split = blockIdx.y;
+  const int tb = split * tokens_per_split;
+  const int te = min(T, tb + tokens_per_split);
+  float acc[S::TM][S::TN];
+#pragma unroll
+  for (int i = 0; i < S::TM; ++i)
+#pragma unroll
+    for (int j = 0; j < S::TN; ++j) acc[i][j] = 0.f;
+  for (int c0 = tb; c0 < te; c0 += kKC) {
+    // x rows c0..c0+31, columns i0..i0+63 (8 16-byte pieces per row)
+    for (int p = tid; p < kKC * 8; p += kThreads) {
+      const int r = p / 8, q = p % 8;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (c0 + r < te && i0 + q * 8 < d)
+        v = *reinterpret_cast<const uint4*>(a.x + (size_t)(c0 + r) * d + i0 + q * 8);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        sm.xs[r][q * 8 + 2 * m] = bf16_lo(w[m]);
+        sm.xs[r][q * 8 + 2 * m + 1] = bf16_hi(w[m]);
+      }
+    }
+    for (int p = tid; p < kKC * EB; p += kThreads) {
+      const int r = p / EB, e = p % EB;
+      sm.ls[r][e] = (c0 + r < te && e < E) ? a.dlogits[(size_t)(c0 + r) * E + e] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int kk = ks; kk < kKC; kk += S::KS) {
+      float xv[S::TM], lv[S::TN];
+#pragma unroll
+      for (int i = 0; i < S::TM; ++i) xv[i] = sm.xs[kk][tx * S::TM + i];
+#pragma unroll
+      for (int j = 0; j < S::TN; ++j) lv[j] = sm.ls[kk][ty * S::TN + j];
+#pragma unroll
+      for (int i = 0; i < S::TM; ++i)
+#pragma unroll
+        for (int j = 0; j < S::TN; ++j) acc[i][j] = fmaf(xv[i], lv[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < S::TM; ++i)
+#pragma unroll
+    for (int j = 0; j < S::TN; ++j) sm.red[ks][tx * S::TM + i][ty * S::TN + j] = acc[i][j];
+  __syncthreads();
+  for (int p = tid; p < kDwrRows * EB; p += kThreads) {
+    const int r = p / EB, e = p % EB;
+    if (i0 + r >= d || e >= E) continue;
+    float v = sm.red[0][r][e];
+#pragma unroll
+    for (int s = 1; s < S::KS; ++s) v += sm.red[s][r][e];
+    a.dwr_part[((size_t)split * d + i0 + r) * E + e] = v;
+  }
+}
+
+// Router backward, part 3: fixed-order sums of the dW_r and db partials.
+__global__ void router_reduce_kernel(RouterBwdArgs a, int d, int E, int nsplit, int nblk) {
+  const size_t n = (size_t)d * E;
+  for (size_t p = blockIdx.x * (size_t)blockDim.x + threadIdx.x; p < n + E;
+       p += (size_t)gridDim.x * blockDim.x) {
+    if (p < n) {
+      float v = 0.f;
+      for (int s = 0; s < nsplit; ++s) v += a.dwr_part[(size_t)s * n + p];
+      a.dW_r[p] = v;
+    } else if (a.db_r != nullptr) {
+      const int e = (int)(p - n);
+      float v = 0.f;
+      for (int b = 0; b < nblk; ++b) v += a.db_part[(size_t)b * E + e];
+      a.db_r[e] = v;
+    }
+  }
+}
+
+int bucket_of(int E) {
+  int b = 8;
+  while (b < E) b *= 2;
+  return b;
+}
+
+template <int EB>
+cudaError_t route_fwd_eb(const Cfg& c, const RouteArgs& a, cudaStream_t s) {
+  using S = RouteShape<EB>;
+  const size_t smem = sizeof(LogitSmem<EB>);
+  auto kern = route_fwd_kernel<EB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int grid = (c.T + S::BT - 1) / S::BT;
+  prof_mark(kKRoute, s, true);
+  kern<<<grid, kThreads, smem, s>>>(a, c.T, c.d, c.E, c.k, c.renorm);
+  prof_mark(kKRoute, s, false);
+  return cudaGetLastError();
+}
+
+template <int EB>
+cudaError_t router_bwd_eb(const Cfg& c, const Layout& L, const RouterBwdArgs& a, cudaStream_t s) {
+  using S = RouteShape<EB>;
+  {
+    const size_t smem = sizeof(LogitSmem<EB>);
+    auto kern = router_dlogits_kernel<EB>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    prof_mark(kKRouterDlogits, s, true);
+    kern<<<L.nblk_router, kThreads, smem, s>>>(a, c.T, c.d, c.E, c.k, c.renorm);
+    prof_mark(kKRouterDlogits, s, false);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    (void)S::BT;
+  }
+  {
+    const size_t smem = sizeof(DwrSmem<EB>);
+    auto kern = router_dwr_kernel<EB>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int per = (c.T + L.nsplit_dwr - 1) / L.nsplit_dwr;
+    dim3 grid((c.d + kDwrRows - 1) / kDwrRows, L.nsplit_dwr);
+    prof_mark(kKRouterDwr, s, true);
+    kern<<<grid, kThreads, smem, s>>>(a, c.T, c.d, c.E, per);
+    prof_mark(kKRouterDwr, s, false);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  const size_t n = (size_t)c.d * c.E + c.E;
+  const int blocks = (int)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 4);
+  prof_mark(kKRouterReduce, s, true);
+  router_reduce_kernel<<<blocks, 256, 0, s>>>(a, c.d, c.E, L.nsplit_dwr, L.nblk_router);
+  prof_mark(kKRouterReduce, s, false);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int route_block_tokens(int E) {
+  switch (bucket_of(E)) {
+    case 8: return RouteShape<8>::BT;
+    case 16: return RouteShape<16>::BT;
+    case 32: return RouteShape<32>::BT;
+    case 64: return RouteShape<64>::BT;
+    case 128: return RouteShape<128>::BT;
+    default: return RouteShape<256>::BT;
+  }
+}
+
+cudaError_t launch_route(const Cfg& c, const RouteArgs& a, cudaStream_t s) {
+  switch (bucket_of(c.E)) {
+    case 8: return route_fwd_eb<8>(c, a, s);
+    case 16: return route_fwd_eb<16>(c, a, s);
+    case 32: return route_fwd_eb<32>(c, a, s);
+    case 64: return route_fwd_eb<64>(c, a, s);
+    case 128: return route_fwd_eb<128>(c, a, s);
+    default: return route_fwd_eb<256>(c, a, s);
+  }
+}
+
+cudaError_t launch_router_bwd(const Cfg& c, const Layout& L, const RouterBwdArgs& a, cudaStream_t s) {
+  switch (bucket_of(c.E)) {
+    case 8: return router_bwd_eb<8>(c, L, a, s);
+    case 16: return router_bwd_eb<16>(c, L, a, s);
+    case 32: return router_bwd_eb<32>(c, L, a, s);
+    case 64: return router_bwd_eb<64>(c, L, a, s);
+    case 128: return router_bwd_eb<128>(c, L, a, s);
+    default: return router_bwd_eb<256>(c, L, a, s);
+  }
+}
+
+}  // namespace moe

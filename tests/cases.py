@@ -1,0 +1,32 @@
+"""Small and medium parity workloads (seconds for the oracle, several tiles and ragged tails).
+
+Each case is shaped like one of the pages' workload families (Mixtral-, DeepSeek-, Qwen3- and
+GPT-OSS-like layers) but small: segments of 1-3 M tiles with ragged ends, d_model and d_ff that are
+multiples of 64 but not of 128 or 256, shared experts with renormalised gates, a Zipf-skewed router
+with empty experts, and a capacity that drops slots.
+"""
+from __future__ import annotations
+
+import functools
+
+import oracle
+import synth
+
+CASES = {
+    "tiny": dict(synth.CONFIGS["tiny"]),
+    "ragged_mixtral": dict(T=1000, d=320, E=8, k=2, f=384, S=0, renorm=0, cf=0.0, zipf=False),
+    "deepseek_small": dict(T=512, d=256, E=16, k=4, f=192, S=2, renorm=1, cf=0.0, zipf=False),
+    "qwen_small": dict(T=777, d=128, E=32, k=4, f=128, S=0, renorm=0, cf=0.0, zipf=True),
+    "gptoss_small": dict(T=600, d=192, E=16, k=4, f=192, S=0, renorm=0, cf=1.25, zipf=True),
+    "single_expert": dict(T=100, d=64, E=1, k=1, f=64, S=0, renorm=0, cf=0.0, zipf=False),
+    "k_equals_E": dict(T=130, d=128, E=4, k=4, f=128, S=1, renorm=1, cf=0.0, zipf=False),
+}
+
+FAST = ["tiny", "ragged_mixtral", "deepseek_small", "qwen_small", "gptoss_small"]
+
+
+@functools.lru_cache(maxsize=None)
+def case(name: str, seed: int = 0):
+    cfg = dict(CASES[name])
+    inp = synth.make_inputs(cfg, seed=seed)
+    return cfg, inp, oracle.Layer(inp, cfg)

@@ -1,0 +1,78 @@
+"""The C-ABI library loads, exports every entry point include/moe.h declares, and its host-side
+argument checks answer without a GPU (CPU only: no compute call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import mixture_experts_layer_10_gb300 as moe
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "moe.h")).read()
+    return sorted(set(re.findall(r"^(?:moe_status_t|const char\*)\s+(moe_\w+)\s*\(", text, re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return moe.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(lib, n), f"libmoe.so does not export {n}"
+    assert sorted(moe.EXPORTS) == names, "binding and header disagree"
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert moe.moe_status_string(code)
+    assert moe.moe_status_string(3) == "workspace too small"
+
+
+def test_workspace_size_and_rows():
+    c = moe.config(T=8192, d=4096, f=14336, E=8, k=2)
+    ws, saved = moe.moe_workspace_size(c)
+    assert saved == 8192 * 2 * 8
+    rows = moe.moe_perm_rows(c)
+    # routed rows padded per expert to 128, all segment starts multiples of 128
+    assert rows % 128 == 0 and rows >= 8192 * 2 + 127 * 8
+    assert ws > 3 * rows * 14336 * 2
+    c2 = moe.config(T=16384, d=2048, f=1408, E=64, k=6, S=2, renorm=1)
+    assert moe.moe_perm_rows(c2) >= 16384 * 6 + 2 * 16384
+
+
+@pytest.mark.parametrize("bad", [
+    dict(T=0, d=128, f=256, E=8, k=2), dict(T=16, d=100, f=256, E=8, k=2),
+    dict(T=16, d=128, f=96, E=8, k=2), dict(T=16, d=128, f=256, E=8, k=9),
+    dict(T=16, d=128, f=256, E=300, k=2), dict(T=16, d=128, f=256, E=8, k=2, S=9),
+    dict(T=16, d=128, f=256, E=8, k=0),
+])
+def test_invalid_config_rejected(lib, bad):
+    c = moe.config(**bad)
+    ws, saved = ctypes.c_size_t(), ctypes.c_size_t()
+    assert lib.moe_workspace_size(ctypes.byref(c), ctypes.byref(ws), ctypes.byref(saved)) == 1
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    c = moe.config(T=64, d=128, f=256, E=8, k=2)
+    s = None
+    # null x
+    assert lib.moe_route(ctypes.byref(c), None, 0x10000, None, 0x20000, 0x30000, None, s) == 1
+    # misaligned W_r
+    assert lib.moe_route(ctypes.byref(c), 0x10000, 0x20004, None, 0x30000, 0x40000, None, s) == 1
+    # workspace pointer must be 256-byte aligned
+    assert lib.moe_combine(ctypes.byref(c), 0x10000, 0x20000, 0x30000, 0x40010, 1 << 30, s) == 1
+
+
+def test_small_workspace_rejected(lib):
+    c = moe.config(T=64, d=128, f=256, E=8, k=2)
+    ws, _ = moe.moe_workspace_size(c)
+    assert lib.moe_combine(ctypes.byref(c), 0x10000, 0x20000, 0x30000, 0x100000, ws - 1, None) == 3
+    assert lib.moe_dispatch(ctypes.byref(c), 0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000,
+                            0x70000, 0x100000, 16, None) == 3

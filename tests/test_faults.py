@@ -1,0 +1,84 @@
+"""Device-side error reporting without faulting the GPU (GPU).
+
+* An expert id outside [0, E) drops that slot and comes back as MOE_ERR_BAD_INDEX through
+  moe_check_error; the next clean call succeeds.
+* A bounded wait that runs out: the test hook makes one dispatch-scan block never publish its
+  counts, the look-back of the blocks after it gives up after a short limit, the call reports
+  MOE_ERR_TIMEOUT and downstream kernels see empty tables; the next clean call succeeds.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from harness import from_dev, to_dev, to_dev_bf16
+
+pytestmark = pytest.mark.gpu
+
+BAD_INDEX, TIMEOUT = 5, 6
+
+
+def _bufs(moe, T, d, E, k):
+    mc = moe.config(T=T, d=d, f=64, E=E, k=k)
+    buf = moe.Buffers.allocate(mc)
+    out = dict(counts=torch.empty(E, dtype=torch.int32, device="cuda"),
+               offsets=torch.empty(E + 1, dtype=torch.int32, device="cuda"),
+               row_of_slot=torch.empty(T * k, dtype=torch.int32, device="cuda"),
+               token_of_row=torch.empty(T * k, dtype=torch.int32, device="cuda"),
+               x_perm=torch.zeros(buf.rows, d, dtype=torch.bfloat16, device="cuda"))
+    return mc, buf, out
+
+
+def _dispatch(moe, mc, buf, o, idx, x):
+    moe.moe_dispatch(mc, idx, x, o["counts"], o["offsets"], o["row_of_slot"], o["token_of_row"],
+                     o["x_perm"], buf.ws)
+
+
+def test_bad_expert_index_is_reported(moe):
+    T, d, E, k = 300, 64, 8, 2
+    mc, buf, o = _bufs(moe, T, d, E, k)
+    idx_np = synth.random_assignments(3, T, E, k)
+    bad = idx_np.copy()
+    bad[5, 1] = E
+    bad[17, 0] = -3
+    x = to_dev_bf16(synth.normal_bf16(3, "x", (T, d), 1.0))
+    _dispatch(moe, mc, buf, o, to_dev(bad), x)
+    assert moe.moe_check_error(buf.ws) == BAD_INDEX
+    # the error is cleared by the check; a clean call then matches the oracle
+    _dispatch(moe, mc, buf, o, to_dev(idx_np), x)
+    assert moe.moe_check_error(buf.ws) == 0
+    D = oracle.dispatch(idx_np, E, None)
+    assert np.array_equal(from_dev(o["counts"]), D.counts)
+    assert np.array_equal(from_dev(o["row_of_slot"]).reshape(T, k), D.row_of_slot)
+
+
+def test_stalled_scan_block_times_out(moe):
+    T, d, E, k = 5000, 64, 16, 2          # 10000 assignments: three scan blocks
+    mc, buf, o = _bufs(moe, T, d, E, k)
+    idx_np = synth.random_assignments(4, T, E, k)
+    x = to_dev_bf16(synth.normal_bf16(4, "x", (T, d), 1.0))
+    moe.moe_debug_inject(buf.ws, 0, 20_000_000)      # block 0 never publishes; 20 ms limit
+    _dispatch(moe, mc, buf, o, to_dev(idx_np), x)
+    assert moe.moe_check_error(buf.ws) == TIMEOUT
+    moe.moe_debug_inject(buf.ws, -1, 0)
+    _dispatch(moe, mc, buf, o, to_dev(idx_np), x)
+    assert moe.moe_check_error(buf.ws) == 0
+    D = oracle.dispatch(idx_np, E, None)
+    assert np.array_equal(from_dev(o["counts"]), D.counts)
+    assert np.array_equal(from_dev(o["offsets"]), D.offsets)
+    assert np.array_equal(from_dev(o["row_of_slot"]).reshape(T, k), D.row_of_slot)
+
+
+def test_invalid_arguments_enqueue_nothing(moe):
+    mc = moe.config(T=64, d=128, f=128, E=4, k=2)
+    buf = moe.Buffers.allocate(mc)
+    y = torch.empty(64, 128, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(moe.MoEError) as e:
+        moe.moe_combine(mc, None, None, y, buf.ws)
+    assert e.value.code == 1
+    small = buf.ws[: buf.ws.numel() // 2]
+    with pytest.raises(moe.MoEError) as e:
+        moe.moe_combine(mc, y, y, y, small)
+    assert e.value.code == 3
+    assert moe.moe_check_error(buf.ws) == 0

@@ -1,0 +1,69 @@
+"""Parity of the fused moe_layer_fwd / moe_layer_bwd calls with the fp64 oracle (GPU)."""
+import numpy as np
+import pytest
+import torch
+
+from cases import CASES, case
+from harness import (check_close, check_gates, check_routing, check_weight_grad, decided_tokens,
+                     from_dev, from_dev_bf16, to_dev, to_dev_bf16)
+
+pytestmark = pytest.mark.gpu
+
+
+def run_layer(moe, c, inp, buf=None):
+    mc = moe.config_from(c)
+    buf = buf or moe.Buffers.allocate(mc)
+    T, d, f, E, S = c["T"], c["d"], c["f"], c["E"], c["S"]
+    G = E + S
+    dev = dict(x=to_dev_bf16(inp["x"]), W_r=to_dev(inp["W_r"]),
+               b_r=to_dev(inp["b_r"]) if inp["b_r"] is not None else None,
+               Wg=to_dev_bf16(inp["W_gate"]), Wu=to_dev_bf16(inp["W_up"]), Wd=to_dev_bf16(inp["W_down"]),
+               dy=to_dev_bf16(inp["dy"]))
+    y = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    moe.moe_layer_fwd(mc, dev["x"], dev["W_r"], dev["b_r"], dev["Wg"], dev["Wu"], dev["Wd"], y, buf.saved, buf.ws)
+    out = dict(y=y, dx=torch.empty(T, d, dtype=torch.bfloat16, device="cuda"),
+               dW_r=torch.empty(d, E, dtype=torch.float32, device="cuda"),
+               db_r=torch.empty(E, dtype=torch.float32, device="cuda"),
+               dWg=torch.empty(G, f, d, dtype=torch.bfloat16, device="cuda"),
+               dWu=torch.empty(G, f, d, dtype=torch.bfloat16, device="cuda"),
+               dWd=torch.empty(G, d, f, dtype=torch.bfloat16, device="cuda"))
+    moe.moe_layer_bwd(mc, dev["x"], dev["W_r"], dev["b_r"], dev["Wg"], dev["Wu"], dev["Wd"], buf.saved,
+                      dev["dy"], out["dx"], out["dW_r"], out["db_r"], out["dWg"], out["dWu"], out["dWd"], buf.ws)
+    status = moe.moe_check_error(buf.ws)
+    assert status == 0, moe.moe_status_string(status)
+    k = c["k"]
+    sv = buf.saved.view(torch.int32)
+    out["idx"] = sv[:T * k].view(T, k)
+    out["gates"] = buf.saved.view(torch.float32)[T * k:2 * T * k].view(T, k)
+    return out, buf
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_layer_fwd_bwd(moe, name):
+    c, inp, L = case(name)
+    out, _ = run_layer(moe, c, inp)
+    R = L.routing()
+    same = check_routing(from_dev(out["idx"]), from_dev(out["gates"]), R, c["k"])
+    y_ref, _ = L.forward()
+    g = L.backward()
+    if not same.all():
+        # a near-tie went the other way: each token's outputs depend only on its own routing when
+        # no capacity is set, so compare the tokens whose assignment agrees
+        assert c["cf"] <= 0, "capacity workloads must route identically"
+    rows = np.flatnonzero(same)
+    check_close("y", from_dev_bf16(out["y"])[rows], y_ref[rows], float(np.abs(y_ref).max()))
+    check_close("dx", from_dev_bf16(out["dx"])[rows], g["dx"][rows], float(np.abs(g["dx"]).max()))
+    check_close("dW_r", from_dev(out["dW_r"]), g["dW_r"])
+    check_close("db_r", from_dev(out["db_r"]), g["db_r"])
+    check_weight_grad("dW_gate", from_dev_bf16(out["dWg"]), g["dW_gate"])
+    check_weight_grad("dW_up", from_dev_bf16(out["dWu"]), g["dW_up"])
+    check_weight_grad("dW_down", from_dev_bf16(out["dWd"]), g["dW_down"])
+
+
+@pytest.mark.parametrize("name", ["tiny", "deepseek_small", "gptoss_small"])
+def test_layer_is_deterministic(moe, name):
+    c, inp, _ = case(name)
+    a, buf = run_layer(moe, c, inp)
+    b, _ = run_layer(moe, c, inp, buf)
+    for key in a:
+        assert torch.equal(a[key].view(torch.uint8), b[key].view(torch.uint8)), key
