@@ -21,6 +21,8 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+}  // namespace
+
 moe_status_t make_cfg(const moe_config_t* in, Cfg* c) {
   if (in == nullptr) return MOE_ERR_INVALID_ARG;
   const moe_config_t& m = *in;
@@ -63,6 +65,8 @@ moe_status_t check_device() {
   return ok == 1 ? MOE_OK : MOE_ERR_UNSUPPORTED;
 }
 
+namespace {
+
 struct Ws {
   Layout L;
   char* base;
@@ -100,6 +104,7 @@ Layout make_layout(const Cfg& c) {
   L.rows = routed + shared;
   L.nscan = (int)(((int64_t)c.T * c.k + kScanChunk - 1) / kScanChunk);
   L.ntf = (c.f + 127) / 128;
+  L.ndg = 2 * L.ntf;
   L.nblk_router = (c.T + route_block_tokens(c.E) - 1) / route_block_tokens(c.E);
   const int dtiles = (c.d + 63) / 64;
   L.nsplit_dwr = std::max(1, std::min((304 + dtiles - 1) / dtiles, (c.T + 255) / 256));
@@ -117,7 +122,7 @@ Layout make_layout(const Cfg& c) {
   L.prow_of_slot = take((size_t)c.T * c.k * 4);
   L.slot_of_prow = take(rows * 4);
   L.gate_of_prow = take(rows * 4);
-  L.dg_part = take(rows * L.ntf * 4);
+  L.dg_part = take(rows * L.ndg * 4);
   L.dlogits = take((size_t)c.T * c.E * 4);
   L.dwr_part = take((size_t)L.nsplit_dwr * c.d * c.E * 4);
   L.db_part = take((size_t)L.nblk_router * c.E * 4);

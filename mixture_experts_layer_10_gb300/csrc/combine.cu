@@ -62,17 +62,18 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 
   if (kBwd && dlogits != nullptr) {
     for (int e0 = 0; e0 < E; e0 += kEChunk) {
-      for (int p = threadIdx.x; p < kColTile * kEChunk; p += 256) {
-        const int i = p / kEChunk, ee = p % kEChunk;
-        wt[ee][i] = (c0 + i < d && e0 + ee < E) ? W_r[(size_t)(c0 + i) * E + e0 + ee] : 0.f;
+      const int ne = min(kEChunk, E - e0);   // experts in this chunk; loads run along W_r's rows
+      for (int p = threadIdx.x; p < kColTile * ne; p += 256) {
+        const int i = p / ne, ee = p % ne;
+        wt[ee][i] = (c0 + i < d) ? W_r[(size_t)(c0 + i) * E + e0 + ee] : 0.f;
       }
-      for (int p = threadIdx.x; p < kTokTile * kEChunk; p += 256) {
-        const int tt = p / kEChunk, ee = p % kEChunk;
-        dl[tt][ee] = (t0 + tt < T && e0 + ee < E) ? dlogits[(size_t)(t0 + tt) * E + e0 + ee] : 0.f;
+      for (int p = threadIdx.x; p < kTokTile * ne; p += 256) {
+        const int tt = p / ne, ee = p % ne;
+        dl[tt][ee] = (t0 + tt < T) ? dlogits[(size_t)(t0 + tt) * E + e0 + ee] : 0.f;
       }
       __syncthreads();
 #pragma unroll 4
-      for (int ee = 0; ee < kEChunk; ++ee) {
+      for (int ee = 0; ee < ne; ++ee) {
         const float4 w0 = *reinterpret_cast<const float4*>(&wt[ee][tx * 8]);
         const float4 w1 = *reinterpret_cast<const float4*>(&wt[ee][tx * 8 + 4]);
         const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
@@ -142,7 +143,7 @@ cudaError_t launch_dgates(const Cfg& c, const Layout& L, const DgatesArgs& a, cu
   const int n = c.T * c.k;
   const int blocks = std::max(1, std::min((n + 255) / 256, num_sms() * 4));
   prof_mark(kKDgates, s, true);
-  dgates_kernel<<<blocks, 256, 0, s>>>(a.dg_part, a.prow_of_slot, a.dgates, n, L.ntf);
+  dgates_kernel<<<blocks, 256, 0, s>>>(a.dg_part, a.prow_of_slot, a.dgates, n, L.ndg);
   prof_mark(kKDgates, s, false);
   return cudaGetLastError();
 }

@@ -63,7 +63,8 @@ struct Tables {
 struct Layout {
   int64_t rows;          // row capacity of the padded expert-ordered buffers
   int nscan;             // dispatch-scan blocks
-  int ntf;               // 128-wide tiles over d_ff (per-row gate-gradient partials)
+  int ntf;               // 128-wide tiles over d_ff
+  int ndg;               // per-row gate-gradient partials (two 64-column halves per d_ff tile)
   int nsplit_dwr;        // token splits of dW_r = x^T dlogits
   int nblk_router;       // router backward blocks (db partials)
   size_t hdr, tabs, scan_status, rank, prow_of_slot, slot_of_prow, gate_of_prow, dg_part,
@@ -107,6 +108,8 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 // ---------------------------------------------------------------------------------------------
 
 Layout make_layout(const Cfg& c);
+moe_status_t make_cfg(const moe_config_t* in, Cfg* c);   // validate a configuration
+moe_status_t check_device();                     // MOE_OK on an sm_103 device
 int num_sms();                                   // SMs of the current device (cached)
 moe_status_t cuda_status(cudaError_t e);          // MOE_OK or MOE_ERR_CUDA (clears the error)
 

@@ -220,18 +220,22 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a, in
         if (kDy && kept) a.gate_of_prow[prow] = a.gates[slot];
       }
       const int ng = min(32, k - jb);
-      for (int v = lane; v < nvec; v += 32) {
+      // warp-uniform trip count: every lane takes part in every shuffle, and the vector index is
+      // predicated instead (a row need not be a multiple of 32 vectors, e.g. d = 2880)
+      for (int v0 = 0; v0 < nvec; v0 += 32) {
+        const int v = v0 + lane;
+        const bool live = v < nvec;
         uint4 vx = make_uint4(0, 0, 0, 0), vd = make_uint4(0, 0, 0, 0);
-        if (kX) vx = xs[v];
-        if (kDy) vd = dys[v];
+        if (kX && live) vx = xs[v];
+        if (kDy && live) vd = dys[v];
         for (int q = 0; q < ng; ++q) {
           const int p = __shfl_sync(0xffffffffu, prow, q);
-          if (p >= 0) {
+          if (p >= 0 && live) {
             if (kX) reinterpret_cast<uint4*>(a.x_perm + (size_t)p * d)[v] = vx;
             if (kDy) reinterpret_cast<uint4*>(a.dy_perm + (size_t)p * d)[v] = vd;
           }
         }
-        if (jb == 0) {
+        if (jb == 0 && live) {
           for (int s = 0; s < S; ++s) {
             if (t >= tb->kept[E + s]) continue;
             const size_t p = (size_t)tb->poff[E + s] + t;

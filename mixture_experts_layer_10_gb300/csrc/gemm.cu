@@ -8,8 +8,8 @@
 //   warp 0      TMA producer: loads operand tiles into a ring of shared-memory stages
 //   warp 1      MMA issuer: one thread issues tcgen05.mma into TMEM accumulators, commits each
 //               stage back to the producer and each finished tile to the epilogue
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (128 lanes = 128 rows), fused
-//               element-wise work, bf16 stores
+//   warps 2..   epilogue (4 or 8 warps): tcgen05.ld of the accumulator (128 lanes = 128 rows),
+//               fused element-wise work, bf16 stores
 //
 // Rows are the dispatch's padded expert segments (multiples of 128), so every 128-row M tile
 // belongs to one expert and the per-expert tile scheduler is a table walk done identically by
@@ -18,9 +18,9 @@
 // Problems (BM = 128, BK = 64, operands bf16, accumulators fp32):
 //   FwdGateUp  H    = silu(X Wg^T) * (X Wu^T)              A=X K-major, B=[Wg;Wu] K-major, N=256
 //   FwdDown    O    = H Wd^T                               A=H K-major, B=Wd K-major,      N=256
-//   BwdFused   a,b  = X [Wg;Wu]^T ; dh' = dY Wd  (recompute + dgrad of the down projection)
+//   BwdFused   phase 1: dh' = dY Wd (B MN-major); phase 2: a|b = X [Wg;Wu]^T (recompute)
 //              epilogue: h = silu(a) b, dg += dh'.h, dh = g dh', dA = dh b silu'(a),
-//              dB = dh silu(a), Hg = g h                  N = 128 (a, b, dh': 384 TMEM columns)
+//              dB = dh silu(a), Hg = g h                  N = 128 (a, b, dh' slots in TMEM)
 //   Wgrad      dWg = dA^T X, dWu = dB^T X, dWd = dY^T Hg   A and B MN-major, K = segment rows
 //   DgradX     dX   = dA Wg + dB Wu                        A K-major, B MN-major, K = 2 d_ff
 #include <algorithm>
@@ -36,13 +36,20 @@ namespace {
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
-constexpr int kThreads = 192;
 constexpr uint32_t kTileA = kBM * kBK * 2;   // 16 KB: 128 rows x 64 bf16 (K-major)
 constexpr uint32_t kBox = 64 * kBK * 2;      // 8 KB: a 64 x 64 box (MN-major)
 constexpr int kChunkM = 32;                  // m-tiles per L2 reuse chunk of a segment
 
 struct Job {
   int seg, m0, n0, kiters, kbase, sub;
+};
+
+// Defaults of the per-problem hooks; a policy overrides what it needs.
+struct PolicyDefaults {
+  // k-iteration before which the MMA waits for the epilogue to release the accumulator
+  __device__ static int acc_wait_kit(const Job&) { return 0; }
+  // TMA bytes that complete one stage at k-iteration kit
+  __device__ static uint32_t tx_bytes(const Job&, int, uint32_t stage_bytes) { return stage_bytes; }
 };
 
 struct SegSmem {
@@ -95,8 +102,9 @@ __device__ __forceinline__ Job row_job(const SegSmem& s, int t, int nt, int bn, 
 // Problem policies
 // ---------------------------------------------------------------------------------------------
 
-struct FwdGateUp {
+struct FwdGateUp : PolicyDefaults {
   static constexpr int kId = kKGateUp;
+  static constexpr int kEpiWarps = 4;
   static constexpr int kStages = 4;
   static constexpr uint32_t kStageBytes = kTileA + 2 * kTileA;   // X tile + Wg tile + Wu tile
   static constexpr int kAccCols = 256;
@@ -122,13 +130,13 @@ struct FwdGateUp {
     tma_load_3d(st + kTileA, &p.tmWg, bar, kit * kBK, j.n0, j.seg);
     tma_load_3d(st + 2 * kTileA, &p.tmWu, bar, kit * kBK, j.n0, j.seg);
   }
-  __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt) {
+  __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
 #pragma unroll
     for (int kk = 0; kk < kBK / 16; ++kk)
       umma_bf16(dt, sdesc_kmajor(sa + kk * 32), sdesc_kmajor(sa + kTileA + kk * 32), kIdesc,
                 (kit | kk) != 0);
   }
-  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row) {
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int, int) {
     uint16_t* out = p.H + (size_t)(j.m0 + row) * p.f + j.n0;
 #pragma unroll 1
     for (int c = 0; c < 128; c += 32) {
@@ -150,7 +158,7 @@ struct FwdGateUp {
       for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
     }
   }
-  __device__ static void epilogue_zero(const Params&, const Job&, int) {}
+  __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
 };
 
 // Shared by FwdDown and DgradX: fp32 accumulator [128 x 256] -> bf16 rows of width `ncols`.
@@ -172,8 +180,9 @@ __device__ __forceinline__ void store_acc_rows(uint16_t* base, int ld, int n0, i
   (void)ld;
 }
 
-struct FwdDown {
+struct FwdDown : PolicyDefaults {
   static constexpr int kId = kKDown;
+  static constexpr int kEpiWarps = 4;
   static constexpr int kStages = 4;
   static constexpr uint32_t kStageBytes = kTileA + 2 * kTileA;   // H tile + Wd tile (256 rows)
   static constexpr int kAccCols = 256;
@@ -196,24 +205,31 @@ struct FwdDown {
     tma_load_2d(st, &p.tmH, bar, kit * kBK, j.m0);
     tma_load_3d(st + kTileA, &p.tmWd, bar, kit * kBK, j.n0, j.seg);
   }
-  __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt) {
+  __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
 #pragma unroll
     for (int kk = 0; kk < kBK / 16; ++kk)
       umma_bf16(dt, sdesc_kmajor(sa + kk * 32), sdesc_kmajor(sa + kTileA + kk * 32), kIdesc,
                 (kit | kk) != 0);
   }
-  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row) {
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int, int) {
     store_acc_rows(p.O + (size_t)(j.m0 + row) * p.d, p.d, j.n0, p.d, ta);
   }
-  __device__ static void epilogue_zero(const Params&, const Job&, int) {}
+  __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
 };
 
-struct BwdFused {
+// Two phases per tile over the same K (= d_model): phase 1 accumulates dh' = dY Wd into a
+// 128-column TMEM slot that alternates between consecutive tiles (columns 256-383 / 384-511);
+// phase 2 accumulates a | b = X [Wg;Wu]^T into columns 0-255.  Only phase 2 has to wait for the
+// previous tile's epilogue to release TMEM, so that epilogue runs under the next tile's phase 1.
+// (Phase 1 of tile i+1 overwrites the slot of tile i-1, whose epilogue finished before phase 2 of
+// tile i began.)  Eight epilogue warps: two per TMEM lane quarter, each owning 64 columns.
+struct BwdFused : PolicyDefaults {
   static constexpr int kId = kKBwdFused;
-  static constexpr int kStages = 2;
-  // X tile, dY tile, [Wg;Wu] tile (256 rows), Wd slice as two 64 x 64 MN-major boxes
-  static constexpr uint32_t kStageBytes = 4 * kTileA + 2 * kBox;
-  static constexpr int kAccCols = 384;
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kStages = 4;
+  static constexpr uint32_t kStageBytes = 3 * kTileA;            // phase 2: X tile + [Wg;Wu] (256 rows)
+  static constexpr uint32_t kPhase1Bytes = kTileA + 2 * kBox;    // phase 1: dY tile + Wd slice (2 MN boxes)
+  static constexpr int kAccCols = 0;     // one accumulator set with the layout above
   static constexpr int kAccBufs = 1;
   static constexpr int kTmemCols = 512;
   static constexpr uint32_t kIdescAB = idesc_bf16(128, 256, false, false);
@@ -223,46 +239,62 @@ struct BwdFused {
     const float* gate_of_prow;
     uint16_t *dA, *dB, *Hg;
     float* dg_part;
-    int f, d, nt;
+    int f, d, nt, ndg;
     Hdr* hdr;
     const Tables* tabs;
   };
+  __device__ static uint32_t dh_col(int seq) { return 256u + 128u * (uint32_t)(seq & 1); }
   __device__ static int num_tiles(const Params& p, const SegSmem& s) { return s.n_mtiles * p.nt; }
   __device__ static Job job(const Params& p, const SegSmem& s, int t) {
-    return row_job(s, t, p.nt, 128, p.d / kBK);
+    return row_job(s, t, p.nt, 128, 2 * (p.d / kBK));
+  }
+  __device__ static int acc_wait_kit(const Job& j) { return j.kiters / 2; }
+  __device__ static uint32_t tx_bytes(const Job& j, int kit, uint32_t) {
+    return kit < j.kiters / 2 ? kPhase1Bytes : kStageBytes;
   }
   __device__ static void prefetch(const Params& p) {
     tma_prefetch(&p.tmX); tma_prefetch(&p.tmDY); tma_prefetch(&p.tmWg); tma_prefetch(&p.tmWu);
     tma_prefetch(&p.tmWdT);
   }
   __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint64_t* bar) {
-    tma_load_2d(st, &p.tmX, bar, kit * kBK, j.m0);
-    tma_load_2d(st + kTileA, &p.tmDY, bar, kit * kBK, j.m0);
-    tma_load_3d(st + 2 * kTileA, &p.tmWg, bar, kit * kBK, j.n0, j.seg);
-    tma_load_3d(st + 3 * kTileA, &p.tmWu, bar, kit * kBK, j.n0, j.seg);
-    tma_load_3d(st + 4 * kTileA, &p.tmWdT, bar, j.n0, kit * kBK, j.seg);
-    tma_load_3d(st + 4 * kTileA + kBox, &p.tmWdT, bar, j.n0 + 64, kit * kBK, j.seg);
-  }
-  __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt) {
-#pragma unroll
-    for (int kk = 0; kk < kBK / 16; ++kk) {
-      const uint32_t acc = (kit | kk) != 0;
-      umma_bf16(dt, sdesc_kmajor(sa + kk * 32), sdesc_kmajor(sa + 2 * kTileA + kk * 32), kIdescAB, acc);
-      umma_bf16(dt + 256, sdesc_kmajor(sa + kTileA + kk * 32),
-                sdesc_mnmajor(sa + 4 * kTileA + kk * 2048, kBox), kIdescDh, acc);
+    const int nk = j.kiters / 2;
+    if (kit < nk) {
+      const int k0 = kit * kBK;
+      tma_load_2d(st, &p.tmDY, bar, k0, j.m0);
+      tma_load_3d(st + kTileA, &p.tmWdT, bar, j.n0, k0, j.seg);
+      tma_load_3d(st + kTileA + kBox, &p.tmWdT, bar, j.n0 + 64, k0, j.seg);
+    } else {
+      const int k0 = (kit - nk) * kBK;
+      tma_load_2d(st, &p.tmX, bar, k0, j.m0);
+      tma_load_3d(st + kTileA, &p.tmWg, bar, k0, j.n0, j.seg);
+      tma_load_3d(st + 2 * kTileA, &p.tmWu, bar, k0, j.n0, j.seg);
     }
   }
-  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row) {
+  __device__ static void mma(const Job& j, int kit, uint32_t sa, uint32_t dt, int seq) {
+    const int nk = j.kiters / 2;
+    if (kit < nk) {
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk)
+        umma_bf16(dt + dh_col(seq), sdesc_kmajor(sa + kk * 32), sdesc_mnmajor(sa + kTileA + kk * 2048, kBox),
+                  kIdescDh, (kit | kk) != 0);
+    } else {
+#pragma unroll
+      for (int kk = 0; kk < kBK / 16; ++kk)
+        umma_bf16(dt, sdesc_kmajor(sa + kk * 32), sdesc_kmajor(sa + kTileA + kk * 32), kIdescAB,
+                  ((kit - nk) | kk) != 0);
+    }
+  }
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int part, int seq) {
     const size_t r = (size_t)(j.m0 + row);
     const float g = p.gate_of_prow[r];
     float dg = 0.f;
 #pragma unroll 1
-    for (int c = 0; c < 128; c += 32) {
+    for (int c = part * 64; c < part * 64 + 64; c += 32) {
       if (j.n0 + c >= p.f) break;
       uint32_t va[32], vb[32], vd[32];
       tmem_ld32(ta + c, va);
       tmem_ld32(ta + 128 + c, vb);
-      tmem_ld32(ta + 256 + c, vd);
+      tmem_ld32(ta + dh_col(seq) + c, vd);
       tmem_ld_wait();
       uint32_t pa[16], pb[16], ph[16];
 #pragma unroll
@@ -296,13 +328,14 @@ struct BwdFused {
         hg[q] = make_uint4(ph[4 * q], ph[4 * q + 1], ph[4 * q + 2], ph[4 * q + 3]);
       }
     }
-    p.dg_part[r * p.nt + j.n0 / 128] = dg;
+    p.dg_part[r * p.ndg + (j.n0 / 128) * 2 + part] = dg;
   }
-  __device__ static void epilogue_zero(const Params&, const Job&, int) {}
+  __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
 };
 
-struct DgradX {
+struct DgradX : PolicyDefaults {
   static constexpr int kId = kKDgradX;
+  static constexpr int kEpiWarps = 4;
   static constexpr int kStages = 4;
   static constexpr uint32_t kStageBytes = kTileA + 4 * kBox;   // dA/dB tile + 4 MN boxes of W
   static constexpr int kAccCols = 256;
@@ -332,20 +365,21 @@ struct DgradX {
     for (int i = 0; i < 4; ++i)
       tma_load_3d(st + kTileA + i * kBox, up ? &p.tmWuT : &p.tmWgT, bar, j.n0 + 64 * i, k0, j.seg);
   }
-  __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt) {
+  __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
 #pragma unroll
     for (int kk = 0; kk < kBK / 16; ++kk)
       umma_bf16(dt, sdesc_kmajor(sa + kk * 32), sdesc_mnmajor(sa + kTileA + kk * 2048, kBox), kIdesc,
                 (kit | kk) != 0);
   }
-  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row) {
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int, int) {
     store_acc_rows(p.dX + (size_t)(j.m0 + row) * p.d, p.d, j.n0, p.d, ta);
   }
-  __device__ static void epilogue_zero(const Params&, const Job&, int) {}
+  __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
 };
 
-struct Wgrad {
+struct Wgrad : PolicyDefaults {
   static constexpr int kId = kKWgrad;
+  static constexpr int kEpiWarps = 8;
   static constexpr int kStages = 4;
   static constexpr uint32_t kStageBytes = 2 * kBox + 4 * kBox;   // A: 128 MN; B: 256 MN
   static constexpr int kAccCols = 256;
@@ -395,7 +429,7 @@ struct Wgrad {
 #pragma unroll
     for (int i = 0; i < 4; ++i) tma_load_2d(st + (2 + i) * kBox, tb, bar, j.n0 + 64 * i, row);
   }
-  __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt) {
+  __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
 #pragma unroll
     for (int kk = 0; kk < kBK / 16; ++kk)
       umma_bf16(dt, sdesc_mnmajor(sa + kk * 2048, kBox), sdesc_mnmajor(sa + 2 * kBox + kk * 2048, kBox),
@@ -409,12 +443,13 @@ struct Wgrad {
     uint16_t* W = j.sub == 0 ? p.dWg : (j.sub == 1 ? p.dWu : p.dWd);
     return W + ((size_t)j.seg * M + (ok ? m : 0)) * ncols;
   }
-  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row) {
+  // Eight epilogue warps: the two warps of a TMEM lane quarter take 128 columns each.
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int part, int) {
     int ncols;
     bool ok;
     uint16_t* base = out_row(p, j, row, ncols, ok);
 #pragma unroll 1
-    for (int c = 0; c < 256; c += 32) {
+    for (int c = part * 128; c < part * 128 + 128; c += 32) {
       if (j.n0 + c >= ncols) break;
       uint32_t v[32];
       tmem_ld32(ta + c, v);
@@ -429,7 +464,7 @@ struct Wgrad {
     }
   }
   // An expert that received no rows has a zero gradient.
-  __device__ static void epilogue_zero(const Params& p, const Job& j, int row) {
+  __device__ static void epilogue_zero(const Params& p, const Job& j, int row, int) {
     int ncols;
     bool ok;
     uint16_t* base = out_row(p, j, row, ncols, ok);
@@ -449,7 +484,12 @@ constexpr size_t smem_bytes() {
 }
 
 template <class P>
-__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ typename P::Params p) {
+constexpr int threads_of() {
+  return 64 + 32 * P::kEpiWarps;
+}
+
+template <class P>
+__global__ void __launch_bounds__(threads_of<P>(), 1) gemm_kernel(const __grid_constant__ typename P::Params p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
@@ -470,7 +510,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 4);
+      mbar_init(&tempty[a], P::kEpiWarps);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -499,7 +539,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             *abort_flag = 1;
             break;
           }
-          mbar_arrive_expect_tx(&full[stage], P::kStageBytes);
+          mbar_arrive_expect_tx(&full[stage], P::tx_bytes(j, kit, P::kStageBytes));
           P::load(p, j, kit, stages + (size_t)stage * P::kStageBytes, &full[stage]);
           if (++stage == P::kStages) {
             stage = 0;
@@ -514,18 +554,23 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
+      int seq = 0;   // tiles with work issued by this CTA (the epilogue counts the same way)
       for (int t = blockIdx.x; t < ntiles && !*abort_flag; t += gridDim.x) {
         const Job j = P::job(p, segs, t);
         if (j.kiters == 0) continue;
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, limit, abort_flag)) {
-          record_error(p.hdr, MOE_ERR_TIMEOUT, kSiteGemmMma);
-          *abort_flag = 1;
-          break;
-        }
-        tc_fence_after();
+        const int wait_at = P::acc_wait_kit(j);
         const uint32_t dt = tmem_base + (uint32_t)(acc * P::kAccCols);
         bool ok = true;
         for (int kit = 0; kit < j.kiters; ++kit) {
+          if (kit == wait_at) {   // the epilogue must have released this accumulator
+            if (!mbar_wait(&tempty[acc], acc_phase ^ 1, limit, abort_flag)) {
+              record_error(p.hdr, MOE_ERR_TIMEOUT, kSiteGemmMma);
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
           if (!mbar_wait(&full[stage], phase, limit, abort_flag)) {
             record_error(p.hdr, MOE_ERR_TIMEOUT, kSiteGemmMma);
             *abort_flag = 1;
@@ -533,7 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             break;
           }
           tc_fence_after();
-          P::mma(j, kit, smem_u32(stages + (size_t)stage * P::kStageBytes), dt);
+          P::mma(j, kit, smem_u32(stages + (size_t)stage * P::kStageBytes), dt, seq);
           umma_commit(&empty[stage]);
           if (++stage == P::kStages) {
             stage = 0;
@@ -542,6 +587,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
         if (!ok) break;
         umma_commit(&tfull[acc]);
+        ++seq;
         if (++acc == P::kAccBufs) {
           acc = 0;
           acc_phase ^= 1;
@@ -549,14 +595,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
       }
     }
   } else {
-    const int q = warp & 3;   // TMEM lane quarter this warp may access
+    const int q = warp & 3;            // TMEM lane quarter this warp may access
+    const int part = (warp - 2) >> 2;  // column share when two warps serve one quarter
     const int row = q * 32 + lane;
     int acc = 0;
     uint32_t acc_phase = 0;
+    int seq = 0;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const Job j = P::job(p, segs, t);
       if (j.kiters == 0) {
-        P::epilogue_zero(p, j, row);
+        if (part == 0) P::epilogue_zero(p, j, row, part);
         continue;
       }
       if (!mbar_wait(&tfull[acc], acc_phase, limit, abort_flag)) {
@@ -565,7 +613,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         break;
       }
       tc_fence_after();
-      P::epilogue(p, j, tmem_base + (uint32_t)(acc * P::kAccCols) + ((uint32_t)(q * 32) << 16), row);
+      P::epilogue(p, j, tmem_base + (uint32_t)(acc * P::kAccCols) + ((uint32_t)(q * 32) << 16), row, part,
+                  seq);
+      ++seq;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -601,7 +651,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2D bf16 tensor [rows, width] (width contiguous) with a box of box_w x box_r, 128-byte swizzle.
+// Swizzle of a box whose inner extent is box_w bf16 elements (64 -> 128 bytes, 32 -> 64 bytes).
+CUtensorMapSwizzle swizzle_for(uint32_t box_w) {
+  return box_w == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+}
+
+// 2D bf16 tensor [rows, width] (width contiguous) with a box of box_w x box_r.
 bool map_2d(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows, uint32_t box_w,
             uint32_t box_r) {
   auto fn = encode_fn();
@@ -611,11 +666,11 @@ bool map_2d(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows, uin
   const cuuint32_t box[2] = {box_w, box_r};
   const cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(box_w),
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3D bf16 tensor [G, rows, width] with a box of box_w x box_r x 1, 128-byte swizzle.
+// 3D bf16 tensor [G, rows, width] with a box of box_w x box_r x 1.
 bool map_3d(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows, uint64_t G,
             uint32_t box_w, uint32_t box_r) {
   auto fn = encode_fn();
@@ -625,7 +680,7 @@ bool map_3d(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows, uin
   const cuuint32_t box[3] = {box_w, box_r, 1};
   const cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_for(box_w),
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -636,7 +691,7 @@ cudaError_t launch(const typename P::Params& p, cudaStream_t s) {
   cudaError_t e = cudaFuncSetAttribute(gemm_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   prof_mark(P::kId, s, true);
-  gemm_kernel<P><<<num_sms(), kThreads, smem, s>>>(p);
+  gemm_kernel<P><<<num_sms(), threads_of<P>(), smem, s>>>(p);
   prof_mark(P::kId, s, false);
   return cudaGetLastError();
 }
@@ -684,6 +739,7 @@ cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, c
   p3.f = c.f;
   p3.d = c.d;
   p3.nt = L.ntf;
+  p3.ndg = L.ndg;
   p3.hdr = a.hdr;
   p3.tabs = a.tabs;
   cudaError_t e = launch<BwdFused>(p3, s);

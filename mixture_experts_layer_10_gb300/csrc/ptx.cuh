@@ -188,6 +188,18 @@ __device__ __forceinline__ uint64_t sdesc_kmajor(uint32_t saddr) {
   return d;
 }
 
+// K-major with the 64-byte swizzle (32-element K blocks): 64-byte rows, 8-row atoms of 512 bytes,
+// SBO = 512, swizzle mode 4.  K=16 steps advance the start address by 32 bytes.
+__device__ __forceinline__ uint64_t sdesc_kmajor_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(512 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;
+  return d;
+}
+
 __device__ __forceinline__ uint64_t sdesc_mnmajor(uint32_t saddr, uint32_t lbo_bytes) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);

@@ -14,7 +14,7 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kKC = 32;   // k-chunk staged in shared memory
+constexpr int kKC = 64;   // k-chunk staged in shared memory (double-buffered)
 
 // Tile shapes per expert bucket: BT tokens x EB experts per block; a thread owns TM tokens x TN
 // experts and a 1/KS share of each k-chunk.
@@ -29,12 +29,79 @@ template <> struct RouteShape<256> { static constexpr int BT = 32, TM = 4, TN = 
 template <int EB>
 struct LogitSmem {
   using S = RouteShape<EB>;
-  float xs[kKC][S::BT + 4];     // x chunk, k-major
-  float ws[kKC][EB];            // W_r chunk
+  float xs[2][kKC][S::BT + 4];  // x chunk, k-major, double-buffered
+  float ws[2][kKC][EB];         // W_r chunk, double-buffered
   float red[S::KS > 1 ? S::KS : 1][S::BT][EB + 1];   // k-split partials, then the logits tile
 };
 
+// One k-chunk of x (BT rows x 64 bf16, 8 16-byte pieces per row) and of W_r (64 rows x EB),
+// held in registers between its global loads and its shared-memory stores.
+template <int EB>
+struct ChunkRegs {
+  using S = RouteShape<EB>;
+  static constexpr int NX = (S::BT * kKC / 8 + kThreads - 1) / kThreads;
+  static constexpr int NW = (kKC * EB / 4 + kThreads - 1) / kThreads;
+  uint4 x[NX];
+  float4 w[NW];
+
+  __device__ void load(const uint16_t* __restrict__ xg, const float* __restrict__ W_r, int T, int d,
+                       int E, int t0, int k0) {
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int i = 0; i < NX; ++i) {
+      const int p = tid + i * kThreads;
+      const int t = p % S::BT, q = p / S::BT;
+      x[i] = make_uint4(0, 0, 0, 0);
+      if (p < S::BT * kKC / 8 && t0 + t < T)
+        x[i] = *reinterpret_cast<const uint4*>(xg + (size_t)(t0 + t) * d + k0 + q * 8);
+    }
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+      const int p = tid + i * kThreads;
+      const int kk = p / (EB / 4), e = (p % (EB / 4)) * 4;
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (p < kKC * EB / 4) {
+        const float* row = W_r + (size_t)(k0 + kk) * E;
+        if ((E & 3) == 0 && e + 3 < E) {
+          v = *reinterpret_cast<const float4*>(row + e);
+        } else {
+          if (e < E) v.x = row[e];
+          if (e + 1 < E) v.y = row[e + 1];
+          if (e + 2 < E) v.z = row[e + 2];
+          if (e + 3 < E) v.w = row[e + 3];
+        }
+      }
+      w[i] = v;
+    }
+  }
+
+  __device__ void store(LogitSmem<EB>& sm, int buf) const {
+    const int tid = threadIdx.x;
+#pragma unroll
+    for (int i = 0; i < NX; ++i) {
+      const int p = tid + i * kThreads;
+      if (p >= S::BT * kKC / 8) break;
+      const int t = p % S::BT, q = p / S::BT;
+      const uint32_t u[4] = {x[i].x, x[i].y, x[i].z, x[i].w};
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        sm.xs[buf][q * 8 + 2 * m][t] = bf16_lo(u[m]);
+        sm.xs[buf][q * 8 + 2 * m + 1][t] = bf16_hi(u[m]);
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < NW; ++i) {
+      const int p = tid + i * kThreads;
+      if (p >= kKC * EB / 4) break;
+      const int kk = p / (EB / 4), e = (p % (EB / 4)) * 4;
+      *reinterpret_cast<float4*>(&sm.ws[buf][kk][e]) = w[i];
+    }
+  }
+};
+
 // logits tile [BT x EB] of tokens t0.. into sm.red[0] (bias added, experts >= E left at 0).
+// The next chunk's global loads are issued before the current chunk's products, and the chunks
+// alternate between two shared-memory buffers (one barrier per chunk).
 template <int EB>
 __device__ void logits_tile(LogitSmem<EB>& sm, const uint16_t* __restrict__ x,
                             const float* __restrict__ W_r, const float* __restrict__ b_r, int T,
@@ -52,38 +119,40 @@ __device__ void logits_tile(LogitSmem<EB>& sm, const uint16_t* __restrict__ x,
 #pragma unroll
     for (int j = 0; j < S::TN; ++j) acc[i][j] = 0.f;
 
+  ChunkRegs<EB> regs;
+  regs.load(x, W_r, T, d, E, t0, 0);
+  regs.store(sm, 0);
+  __syncthreads();
+  int buf = 0;
   for (int k0 = 0; k0 < d; k0 += kKC) {
-    // x chunk: BT rows x 32 bf16 = 4 16-byte pieces per row
-    for (int p = tid; p < S::BT * 4; p += kThreads) {
-      const int t = p % S::BT, q = p / S::BT;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (t0 + t < T)
-        v = *reinterpret_cast<const uint4*>(x + (size_t)(t0 + t) * d + k0 + q * 8);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const bool more = k0 + kKC < d;
+    if (more) regs.load(x, W_r, T, d, E, t0, k0 + kKC);
+    // two-level sum: each 64-wide chunk is summed on its own, then added to the running total,
+    // which keeps the fp32 rounding of d-long dot products (the gates need 1e-5) several times smaller
+    float part[S::TM][S::TN];
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        sm.xs[q * 8 + 2 * m][t] = bf16_lo(w[m]);
-        sm.xs[q * 8 + 2 * m + 1][t] = bf16_hi(w[m]);
-      }
-    }
-    for (int p = tid; p < kKC * EB; p += kThreads) {
-      const int kk = p / EB, e = p % EB;
-      sm.ws[kk][e] = (e < E) ? W_r[(size_t)(k0 + kk) * E + e] : 0.f;
-    }
-    __syncthreads();
+    for (int i = 0; i < S::TM; ++i)
+#pragma unroll
+      for (int j = 0; j < S::TN; ++j) part[i][j] = 0.f;
 #pragma unroll 4
     for (int kk = ks; kk < kKC; kk += S::KS) {
       float xv[S::TM], wv[S::TN];
 #pragma unroll
-      for (int i = 0; i < S::TM; ++i) xv[i] = sm.xs[kk][tx * S::TM + i];
+      for (int i = 0; i < S::TM; ++i) xv[i] = sm.xs[buf][kk][tx * S::TM + i];
 #pragma unroll
-      for (int j = 0; j < S::TN; ++j) wv[j] = sm.ws[kk][ty * S::TN + j];
+      for (int j = 0; j < S::TN; ++j) wv[j] = sm.ws[buf][kk][ty * S::TN + j];
 #pragma unroll
       for (int i = 0; i < S::TM; ++i)
 #pragma unroll
-        for (int j = 0; j < S::TN; ++j) acc[i][j] = fmaf(xv[i], wv[j], acc[i][j]);
+        for (int j = 0; j < S::TN; ++j) part[i][j] = fmaf(xv[i], wv[j], part[i][j]);
     }
+#pragma unroll
+    for (int i = 0; i < S::TM; ++i)
+#pragma unroll
+      for (int j = 0; j < S::TN; ++j) acc[i][j] += part[i][j];
+    if (more) regs.store(sm, buf ^ 1);   // that buffer was last read before the previous barrier
     __syncthreads();
+    buf ^= 1;
   }
 #pragma unroll
   for (int i = 0; i < S::TM; ++i)

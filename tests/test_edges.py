@@ -127,6 +127,13 @@ def test_gptoss_ffn_width(moe):
     run_steps(moe, T, 192, 2880, E, k, 0, idx, np.full((T, k), 0.5))
 
 
+def test_many_tokens_per_warp_ragged_width(moe):
+    # more tokens than gather warps (each warp owns several tokens) and rows of 40 16-byte vectors
+    T, E, k = 24000, 8, 2
+    idx = synth.random_assignments(8, T, E, k)
+    run_steps(moe, T, 320, 64, E, k, 1, idx, np.full((T, k), 0.5))
+
+
 def test_capacity_one(moe):
     T, E, k = 200, 8, 2
     idx = synth.random_assignments(7, T, E, k, skew=1.5)

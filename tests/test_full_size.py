@@ -15,8 +15,8 @@ import torch
 
 import oracle
 import synth
-from harness import (check_close, check_routing, decided_tokens, from_dev, from_dev_bf16, to_dev,
-                     to_dev_bf16)
+from harness import (check_close, check_routing, decided_tokens, from_dev, from_dev_bf16, segment_rows,
+                     to_dev, to_dev_bf16)
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -82,6 +82,17 @@ def test_dispatch_every_slot(full, moe):
     assert np.array_equal(from_dev(tor)[:D.offsets[-1]], D.token_of_row)
     if cfg["cf"] > 0:
         assert D.kept.max() <= oracle.capacity_of(T, k, E, cfg["cf"])
+    # gathered rows: a seeded sample of kept slots (exact copies) and every pad row (zeros)
+    kept, P = segment_rows(D, T, cfg["S"])
+    rng = np.random.default_rng(7)
+    ts, js = np.nonzero(D.row_of_slot >= 0)
+    pick = rng.choice(ts.size, size=min(4096, ts.size), replace=False)
+    rows = np.array([P[L.routing().idx[t, j]] + D.position[t, j] for t, j in zip(ts[pick], js[pick])])
+    got = from_dev_bf16(x_perm[torch.from_numpy(rows).cuda()])
+    assert np.array_equal(got, L.x[ts[pick]]), "gathered rows differ from x"
+    pads = np.concatenate([np.arange(P[g] + kept[g], P[g + 1]) for g in range(len(kept))]).astype(np.int64)
+    if pads.size:
+        assert torch.count_nonzero(x_perm[torch.from_numpy(pads).cuda()]).item() == 0, "pad rows not zero"
 
 
 def _sample_tokens(cfg, L, out, seed):
