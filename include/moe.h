@@ -129,6 +129,27 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* idx, const moe
                           int32_t* counts, int32_t* offsets, int32_t* row_of_slot, int32_t* token_of_row,
                           moe_bf16* x_perm, void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* moe_dispatch for callers that cannot allocate device memory: no workspace argument.  (The
+ * pages have no counterpart; this exists for integration.)  Meant for code that runs where
+ * cudaMalloc is not available or not allowed: inside a memory arena or pool owned by a host
+ * framework that cannot grow at step time, or on a path that must not pay cudaMalloc's implicit
+ * synchronisation.  Outputs and their meaning are those of moe_dispatch (counts, offsets,
+ * row_of_slot, token_of_row, x_perm with room for moe_perm_rows() rows); the caller still
+ * provides every input and output buffer.
+ * Scratch: a fixed device array of about 3.6 MB inside the library, which every GPU that loads
+ * the library holds until the process exits.  Limits: T*k <= 262144 assignments and
+ * moe_perm_rows() <= 393216 rows; larger configurations return MOE_ERR_UNSUPPORTED and enqueue
+ * nothing.  The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call before any stream
+ * capture.  The call allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ * Every call shares the one array and leaves its contents behind (each call clears what must
+ * start at zero), so calls that may overlap on the GPU -- on different streams, or from several
+ * host threads -- race and must be serialised by the caller.  Device-side errors (an expert id
+ * out of range drops that slot) are not reported by this entry point. */
+moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, const int32_t* idx, const moe_bf16* x,
+                                  int32_t* counts, int32_t* offsets, int32_t* row_of_slot,
+                                  int32_t* token_of_row, moe_bf16* x_perm, moe_stream_t stream);
+
 /* Grouped expert SwiGLU FFN on the rows moe_dispatch laid out in ws: tcgen05/TMEM tiles fed by
  * TMA, a per-expert tile scheduler, SwiGLU fused into the first GEMM's epilogue.
  * o_perm [moe_perm_rows(), d_model] bf16 receives every segment's rows (pad rows are zero). */

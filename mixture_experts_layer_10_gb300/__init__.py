@@ -22,6 +22,7 @@ STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "M
 
 # Every entry point declared in include/moe.h.
 EXPORTS = ("moe_workspace_size", "moe_perm_rows", "moe_workspace_init", "moe_route", "moe_dispatch",
+           "moe_dispatch_noalloc",
            "moe_expert_ffn_fwd", "moe_combine", "moe_expert_ffn_bwd", "moe_router_bwd",
            "moe_combine_bwd", "moe_layer_fwd", "moe_layer_bwd", "moe_check_error",
            "moe_debug_inject", "moe_profile_enable", "moe_profile_read", "moe_status_string")
@@ -60,6 +61,7 @@ def load(path: str | None = None):
         "moe_workspace_init": [cfgp, _P, ctypes.c_size_t, _P],
         "moe_route": [cfgp, _P, _P, _P, _P, _P, _P, _P],
         "moe_dispatch": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+        "moe_dispatch_noalloc": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P],
         "moe_expert_ffn_fwd": [cfgp, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
         "moe_combine": [cfgp, _P, _P, _P, _P, ctypes.c_size_t, _P],
         "moe_expert_ffn_bwd": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
@@ -152,6 +154,12 @@ def moe_route(cfg, x, W_r, b_r, idx, gates, logits=None, stream=None):
 def moe_dispatch(cfg, idx, x, counts, offsets, row_of_slot, token_of_row, x_perm, ws, stream=None):
     _call("moe_dispatch", ctypes.byref(cfg), _ptr(idx), _ptr(x), _ptr(counts), _ptr(offsets),
           _ptr(row_of_slot), _ptr(token_of_row), _ptr(x_perm), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def moe_dispatch_noalloc(cfg, idx, x, counts, offsets, row_of_slot, token_of_row, x_perm, stream=None):
+    """moe_dispatch without a workspace (scratch in a fixed array inside the library)."""
+    _call("moe_dispatch_noalloc", ctypes.byref(cfg), _ptr(idx), _ptr(x), _ptr(counts), _ptr(offsets),
+          _ptr(row_of_slot), _ptr(token_of_row), _ptr(x_perm), _stream(stream))
 
 
 def moe_expert_ffn_fwd(cfg, x_perm, W_gate, W_up, W_down, o_perm, ws, stream=None):

@@ -10,6 +10,8 @@
 //   starts, pad-row prefix and the segment order by size.
 // dispatch_gather_kernel: token owner.  A warp reads each x (and dy) row once, 16 bytes per lane,
 //   and writes it to every kept slot's row (and every shared expert's row); then zeroes pad rows.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace moe {
@@ -304,3 +306,106 @@ cudaError_t launch_dispatch_gather(const Cfg& c, const Layout& L, const Dispatch
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------------------------
+// moe_dispatch_noalloc: the same dispatch with its scratch in a fixed, file-scope device array.
+// ---------------------------------------------------------------------------------------------
+//
+// Some callers cannot allocate device memory for a workspace: code that runs inside a memory
+// arena owned by a host framework, under a pool that forbids growth at step time, or on a path
+// where the implicit synchronisation of cudaMalloc is not allowed.  For them this entry point
+// keeps the dispatch's scratch (header, routing tables, look-back status words, per-slot ranks
+// and rows, per-row slots) in `g_noalloc_scratch`, which every device that loads the library
+// holds until the process exits.  The host side only ever passes the array's device address,
+// taken once per device with cudaGetSymbolAddress while that device is current.
+
+namespace moe {
+namespace {
+
+constexpr int kNoAllocMaxSlots = 1 << 18;                 // T*k assignments
+constexpr int kNoAllocMaxRows = 3 << 17;                  // padded expert-ordered rows
+constexpr int kNoAllocMaxScanBlocks = kNoAllocMaxSlots / kScanChunk;
+
+struct NoAllocScratch {
+  Hdr hdr;
+  Tables tabs;
+  uint32_t scan_status[kNoAllocMaxScanBlocks * kMaxE];
+  int32_t rank[kNoAllocMaxSlots];
+  int32_t prow_of_slot[kNoAllocMaxSlots];
+  int32_t slot_of_prow[kNoAllocMaxRows];
+};
+
+__device__ __align__(256) unsigned char g_noalloc_scratch[sizeof(NoAllocScratch)];
+
+// Device address of the scratch array on the current device (set up on first use per device).
+moe_status_t noalloc_scratch(NoAllocScratch** out) {
+  static std::mutex mu;
+  static void* addr[64] = {nullptr};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    (void)cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      (void)cudaGetLastError();
+      return MOE_ERR_CUDA;
+    }
+    addr[dev] = p;
+  }
+  *out = static_cast<NoAllocScratch*>(addr[dev]);
+  return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, const int32_t* idx,
+                                             const moe_bf16* x, int32_t* counts, int32_t* offsets,
+                                             int32_t* row_of_slot, int32_t* token_of_row,
+                                             moe_bf16* x_perm, moe_stream_t stream) {
+  using namespace moe;
+  Cfg c;
+  moe_status_t st = make_cfg(cfg, &c);
+  if (st != MOE_OK) return st;
+  const void* ptrs[] = {idx, x, counts, offsets, row_of_slot, token_of_row, x_perm};
+  for (const void* p : ptrs)
+    if (p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) != 0) return MOE_ERR_INVALID_ARG;
+  const Layout L = make_layout(c);
+  if ((int64_t)c.T * c.k > kNoAllocMaxSlots || L.rows > kNoAllocMaxRows || L.nscan > kNoAllocMaxScanBlocks)
+    return MOE_ERR_UNSUPPORTED;
+  if ((st = check_device()) != MOE_OK) return st;
+  NoAllocScratch* sc = nullptr;
+  if ((st = noalloc_scratch(&sc)) != MOE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // The array keeps the previous call's contents: start from a clean header (error word,
+  // look-back counters, test hooks); the scan clears its status words itself.
+  if (cudaMemsetAsync(&sc->hdr, 0, sizeof(Hdr), s) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  DispatchArgs a{};
+  a.idx = idx;
+  a.x = reinterpret_cast<const uint16_t*>(x);
+  a.counts = counts;
+  a.offsets = offsets;
+  a.row_of_slot = row_of_slot;
+  a.token_of_row = token_of_row;
+  a.x_perm = reinterpret_cast<uint16_t*>(x_perm);
+  a.hdr = &sc->hdr;
+  a.tabs = &sc->tabs;
+  a.scan_status = sc->scan_status;
+  a.rank = sc->rank;
+  a.prow_of_slot = sc->prow_of_slot;
+  a.slot_of_prow = sc->slot_of_prow;
+  cudaError_t e = launch_dispatch_scan(c, L, a, s);
+  if (e == cudaSuccess) e = launch_dispatch_gather(c, L, a, true, true, false, s);
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
+}
