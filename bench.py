@@ -45,7 +45,7 @@ DESCR = {
     "gptoss": "GPT-OSS-like MoE layer: T=65536 (2x32768), d=2880, E=128 top-4, d_ff=2880, capacity 1.25",
 }
 GEMMS = {  # algorithmic FLOPs per launch in units of N*d*f (N = rows the experts see, no pads)
-    "gemm_gate_up_swiglu": 4, "gemm_down": 2, "gemm_bwd_recompute_dgrad_swiglu": 6,
+    "gemm_gate_up_swiglu": 4, "gemm_down": 2, "gemm_bwd_dgrad_down": 2, "gemm_bwd_recompute_swiglu": 4,
     "gemm_wgrad": 6, "gemm_dgrad_x": 4,
 }
 HBM_KERNELS = ("dispatch_gather", "combine", "combine_bwd")
@@ -62,6 +62,8 @@ def parse():
     ap.add_argument("--cpu-tokens", type=int, default=16, help="oracle sample size (tokens)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override T (a smaller case of the same layer shape, for profiler captures)")
+    ap.add_argument("--experts", type=int, default=0, help="override E (profiler captures)")
+    ap.add_argument("--topk", type=int, default=0, help="override k (profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -151,6 +153,18 @@ class ClockSampler:
                 "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
 
 
+def max_over_ranks(value: float, world: int) -> float:
+    """The largest of every rank's value (the slowest replica sets the step time)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def oracle_sample(inp, cfg, n_tokens, seed=1):
     """The oracle as it stands on a seeded sample of tokens: routing, expert forward and
     backward (weight-gradient products included) and the router backward of those tokens."""
@@ -216,6 +230,10 @@ def main():
     cfg = dict(synth.CONFIGS[args.workload])
     if args.tokens:
         cfg["T"] = args.tokens
+    if args.experts:
+        cfg["E"] = args.experts
+    if args.topk:
+        cfg["k"] = args.topk
     T, d, f, E, k, S = cfg["T"], cfg["d"], cfg["f"], cfg["E"], cfg["k"], cfg["S"]
     G = E + S
     inp = synth.make_inputs(cfg, seed=0)
@@ -279,11 +297,7 @@ def main():
     prof = moe.moe_profile_read()
     moe.moe_profile_enable(False)
     clk = clocks.summary()
-    ms = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
     status = moe.moe_check_error(buf.ws)
     if status != 0:
         raise RuntimeError(f"layer failed in the timed region: {moe.moe_status_string(status)}")
@@ -333,11 +347,7 @@ def main():
     ev1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    ms_e2e = ev0.elapsed_time(ev1) / args.steps
-    if world > 1:
-        t = torch.tensor([ms_e2e], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t.item())
+    ms_e2e = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
 
     pk = peaks()
     # Denominator for the tensor-bound kernels: the burst cuBLAS figure when the SM clock held at
@@ -390,7 +400,8 @@ def main():
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": DESCR[args.workload] + (f" with T overridden to {T}" if args.tokens else ""),
+        "config": {"workload": DESCR[args.workload] + ("" if not (args.tokens or args.experts or args.topk)
+                                                       else f" with T={T}, E={E}, k={k} overridden"),
                    "T": T, "d_model": d, "d_ff": f, "E": E, "k": k,
                    "n_shared": S, "global_batch": world * T, "parallelism": f"replicas x{world}",
                    "l2": "no flush: each step streams > L2 (expert weights alone %.2f GB)"

@@ -132,6 +132,7 @@ Layout make_layout(const Cfg& c) {
   L.buf_f0 = take(rows * c.f * 2);
   L.buf_f1 = take(rows * c.f * 2);
   L.buf_f2 = take(rows * c.f * 2);
+  L.buf_f3 = take(rows * c.f * 2);
   L.buf_d1 = take(rows * c.d * 2);
   L.total = off;
   return L;
@@ -169,8 +170,8 @@ namespace {
 
 const char* const kKernelNames[kKCount] = {
     "route_fwd", "dispatch_scan", "dispatch_gather", "gemm_gate_up_swiglu", "gemm_down",
-    "combine", "gemm_bwd_recompute_dgrad_swiglu", "gemm_wgrad", "gemm_dgrad_x", "dgates_reduce",
-    "router_dlogits", "router_dwr", "router_reduce", "combine_bwd"};
+    "combine", "gemm_bwd_recompute_swiglu", "gemm_wgrad", "gemm_dgrad_x", "dgates_reduce",
+    "router_dlogits", "router_dwr", "router_reduce", "combine_bwd", "gemm_bwd_dgrad_down"};
 
 struct Profiler {
   std::mutex mu;
@@ -262,6 +263,7 @@ moe_status_t do_ffn_bwd(const Cfg& c, const Ws& w, const uint16_t* x_perm, const
   b.Wg = Wg;
   b.Wu = Wu;
   b.Wd = Wd;
+  b.dh = w.at<uint16_t>(w.L.buf_f3);
   b.dA = w.at<uint16_t>(w.L.buf_f0);
   b.dB = w.at<uint16_t>(w.L.buf_f1);
   b.Hg = w.at<uint16_t>(w.L.buf_f2);

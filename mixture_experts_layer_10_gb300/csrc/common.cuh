@@ -68,7 +68,7 @@ struct Layout {
   int nsplit_dwr;        // token splits of dW_r = x^T dlogits
   int nblk_router;       // router backward blocks (db partials)
   size_t hdr, tabs, scan_status, rank, prow_of_slot, slot_of_prow, gate_of_prow, dg_part,
-      dlogits, dwr_part, db_part, dgates, xperm, dy_perm, buf_f0, buf_f1, buf_f2, buf_d1;
+      dlogits, dwr_part, db_part, dgates, xperm, dy_perm, buf_f0, buf_f1, buf_f2, buf_f3, buf_d1;
   size_t total;
 };
 
@@ -117,7 +117,7 @@ moe_status_t cuda_status(cudaError_t e);          // MOE_OK or MOE_ERR_CUDA (cle
 // with prof_mark(id, s, true/false), which records CUDA events on the launching stream.
 enum KernelId : int {
   kKRoute = 0, kKScan, kKGather, kKGateUp, kKDown, kKCombine, kKBwdFused, kKWgrad, kKDgradX,
-  kKDgates, kKRouterDlogits, kKRouterDwr, kKRouterReduce, kKCombineBwd, kKCount
+  kKDgates, kKRouterDlogits, kKRouterDwr, kKRouterReduce, kKCombineBwd, kKBwdDh, kKCount
 };
 void prof_mark(int id, cudaStream_t s, bool begin);
 
@@ -173,7 +173,7 @@ cudaError_t launch_ffn_fwd(const Cfg& c, const Layout& L, const FfnFwdArgs& a, c
 struct FfnBwdArgs {
   const uint16_t* x_perm; const uint16_t* dy_perm; const float* gate_of_prow;
   const uint16_t* Wg; const uint16_t* Wu; const uint16_t* Wd;
-  uint16_t* dA; uint16_t* dB; uint16_t* Hg; float* dg_part; uint16_t* dx_perm;
+  uint16_t* dh; uint16_t* dA; uint16_t* dB; uint16_t* Hg; float* dg_part; uint16_t* dx_perm;
   uint16_t* dWg; uint16_t* dWu; uint16_t* dWd; Hdr* hdr; const Tables* tabs;
 };
 cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, cudaStream_t s);

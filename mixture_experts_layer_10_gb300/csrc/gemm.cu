@@ -217,25 +217,64 @@ struct FwdDown : PolicyDefaults {
   __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
 };
 
-// Two phases per tile over the same K (= d_model): phase 1 accumulates dh' = dY Wd into a
-// 128-column TMEM slot that alternates between consecutive tiles (columns 256-383 / 384-511);
-// phase 2 accumulates a | b = X [Wg;Wu]^T into columns 0-255.  Only phase 2 has to wait for the
-// previous tile's epilogue to release TMEM, so that epilogue runs under the next tile's phase 1.
-// (Phase 1 of tile i+1 overwrites the slot of tile i-1, whose epilogue finished before phase 2 of
-// tile i began.)  Eight epilogue warps: two per TMEM lane quarter, each owning 64 columns.
+// dh' = dY W_d for every row tile: M = rows, N = 256 columns of d_ff, K = d_model.  W_d[e] is
+// [d_model, d_ff], so it is the MN-major B operand (four 64-wide boxes per stage).  dh' is stored
+// in bf16 for the SwiGLU backward below.
+struct BwdDh : PolicyDefaults {
+  static constexpr int kId = kKBwdDh;
+  static constexpr int kEpiWarps = 4;
+  static constexpr int kStages = 4;
+  static constexpr uint32_t kStageBytes = kTileA + 4 * kBox;   // dY tile + Wd slice (4 MN boxes)
+  static constexpr int kAccCols = 256;
+  static constexpr int kAccBufs = 2;
+  static constexpr int kTmemCols = 512;
+  static constexpr uint32_t kIdesc = idesc_bf16(128, 256, false, true);
+  struct Params {
+    CUtensorMap tmDY, tmWdT;
+    uint16_t* DH;
+    int f, d, nt;
+    Hdr* hdr;
+    const Tables* tabs;
+  };
+  __device__ static int num_tiles(const Params& p, const SegSmem& s) { return s.n_mtiles * p.nt; }
+  __device__ static Job job(const Params& p, const SegSmem& s, int t) {
+    return row_job(s, t, p.nt, 256, p.d / kBK);
+  }
+  __device__ static void prefetch(const Params& p) { tma_prefetch(&p.tmDY); tma_prefetch(&p.tmWdT); }
+  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint64_t* bar) {
+    tma_load_2d(st, &p.tmDY, bar, kit * kBK, j.m0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      tma_load_3d(st + kTileA + i * kBox, &p.tmWdT, bar, j.n0 + 64 * i, kit * kBK, j.seg);
+  }
+  __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
+#pragma unroll
+    for (int kk = 0; kk < kBK / 16; ++kk)
+      umma_bf16(dt, sdesc_kmajor(sa + kk * 32), sdesc_mnmajor(sa + kTileA + kk * 2048, kBox), kIdesc,
+                (kit | kk) != 0);
+  }
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int, int) {
+    store_acc_rows(p.DH + (size_t)(j.m0 + row) * p.f, p.f, j.n0, p.f, ta);
+  }
+  __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
+};
+
+// The recompute a | b = X [Wg;Wu]^T (the forward's first GEMM shape, double-buffered TMEM) with the
+// SwiGLU backward in its epilogue, which reads this tile's dh' written by BwdDh:
+//   h = silu(a) b, dg += dh'.h, dh = g dh', dA = dh b silu'(a), dB = dh silu(a), Hg = g h.
+// Eight epilogue warps: two per TMEM lane quarter, each owning 64 of the 128 columns.
 struct BwdFused : PolicyDefaults {
   static constexpr int kId = kKBwdFused;
   static constexpr int kEpiWarps = 8;
   static constexpr int kStages = 4;
-  static constexpr uint32_t kStageBytes = 3 * kTileA;            // phase 2: X tile + [Wg;Wu] (256 rows)
-  static constexpr uint32_t kPhase1Bytes = kTileA + 2 * kBox;    // phase 1: dY tile + Wd slice (2 MN boxes)
-  static constexpr int kAccCols = 0;     // one accumulator set with the layout above
-  static constexpr int kAccBufs = 1;
+  static constexpr uint32_t kStageBytes = 3 * kTileA;   // X tile + [Wg;Wu] (256 rows)
+  static constexpr int kAccCols = 256;
+  static constexpr int kAccBufs = 2;
   static constexpr int kTmemCols = 512;
-  static constexpr uint32_t kIdescAB = idesc_bf16(128, 256, false, false);
-  static constexpr uint32_t kIdescDh = idesc_bf16(128, 128, false, true);
+  static constexpr uint32_t kIdesc = idesc_bf16(128, 256, false, false);
   struct Params {
-    CUtensorMap tmX, tmDY, tmWg, tmWu, tmWdT;
+    CUtensorMap tmX, tmWg, tmWu;
+    const uint16_t* DH;
     const float* gate_of_prow;
     uint16_t *dA, *dB, *Hg;
     float* dg_part;
@@ -243,59 +282,41 @@ struct BwdFused : PolicyDefaults {
     Hdr* hdr;
     const Tables* tabs;
   };
-  __device__ static uint32_t dh_col(int seq) { return 256u + 128u * (uint32_t)(seq & 1); }
   __device__ static int num_tiles(const Params& p, const SegSmem& s) { return s.n_mtiles * p.nt; }
   __device__ static Job job(const Params& p, const SegSmem& s, int t) {
-    return row_job(s, t, p.nt, 128, 2 * (p.d / kBK));
-  }
-  __device__ static int acc_wait_kit(const Job& j) { return j.kiters / 2; }
-  __device__ static uint32_t tx_bytes(const Job& j, int kit, uint32_t) {
-    return kit < j.kiters / 2 ? kPhase1Bytes : kStageBytes;
+    return row_job(s, t, p.nt, 128, p.d / kBK);
   }
   __device__ static void prefetch(const Params& p) {
-    tma_prefetch(&p.tmX); tma_prefetch(&p.tmDY); tma_prefetch(&p.tmWg); tma_prefetch(&p.tmWu);
-    tma_prefetch(&p.tmWdT);
+    tma_prefetch(&p.tmX); tma_prefetch(&p.tmWg); tma_prefetch(&p.tmWu);
   }
   __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint64_t* bar) {
-    const int nk = j.kiters / 2;
-    if (kit < nk) {
-      const int k0 = kit * kBK;
-      tma_load_2d(st, &p.tmDY, bar, k0, j.m0);
-      tma_load_3d(st + kTileA, &p.tmWdT, bar, j.n0, k0, j.seg);
-      tma_load_3d(st + kTileA + kBox, &p.tmWdT, bar, j.n0 + 64, k0, j.seg);
-    } else {
-      const int k0 = (kit - nk) * kBK;
-      tma_load_2d(st, &p.tmX, bar, k0, j.m0);
-      tma_load_3d(st + kTileA, &p.tmWg, bar, k0, j.n0, j.seg);
-      tma_load_3d(st + 2 * kTileA, &p.tmWu, bar, k0, j.n0, j.seg);
-    }
+    tma_load_2d(st, &p.tmX, bar, kit * kBK, j.m0);
+    tma_load_3d(st + kTileA, &p.tmWg, bar, kit * kBK, j.n0, j.seg);
+    tma_load_3d(st + 2 * kTileA, &p.tmWu, bar, kit * kBK, j.n0, j.seg);
   }
-  __device__ static void mma(const Job& j, int kit, uint32_t sa, uint32_t dt, int seq) {
-    const int nk = j.kiters / 2;
-    if (kit < nk) {
+  __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
 #pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk)
-        umma_bf16(dt + dh_col(seq), sdesc_kmajor(sa + kk * 32), sdesc_mnmajor(sa + kTileA + kk * 2048, kBox),
-                  kIdescDh, (kit | kk) != 0);
-    } else {
-#pragma unroll
-      for (int kk = 0; kk < kBK / 16; ++kk)
-        umma_bf16(dt, sdesc_kmajor(sa + kk * 32), sdesc_kmajor(sa + kTileA + kk * 32), kIdescAB,
-                  ((kit - nk) | kk) != 0);
-    }
+    for (int kk = 0; kk < kBK / 16; ++kk)
+      umma_bf16(dt, sdesc_kmajor(sa + kk * 32), sdesc_kmajor(sa + kTileA + kk * 32), kIdesc,
+                (kit | kk) != 0);
   }
-  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int part, int seq) {
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int part, int) {
     const size_t r = (size_t)(j.m0 + row);
     const float g = p.gate_of_prow[r];
     float dg = 0.f;
 #pragma unroll 1
     for (int c = part * 64; c < part * 64 + 64; c += 32) {
       if (j.n0 + c >= p.f) break;
-      uint32_t va[32], vb[32], vd[32];
+      const uint4* dsrc = reinterpret_cast<const uint4*>(p.DH + r * p.f + j.n0 + c);
+      uint4 dv[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) dv[q] = dsrc[q];
+      uint32_t va[32], vb[32];
       tmem_ld32(ta + c, va);
       tmem_ld32(ta + 128 + c, vb);
-      tmem_ld32(ta + dh_col(seq) + c, vd);
       tmem_ld_wait();
+      const uint32_t du[16] = {dv[0].x, dv[0].y, dv[0].z, dv[0].w, dv[1].x, dv[1].y, dv[1].z, dv[1].w,
+                               dv[2].x, dv[2].y, dv[2].z, dv[2].w, dv[3].x, dv[3].y, dv[3].z, dv[3].w};
       uint32_t pa[16], pb[16], ph[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
@@ -304,7 +325,7 @@ struct BwdFused : PolicyDefaults {
         for (int h = 0; h < 2; ++h) {
           const float a = __uint_as_float(va[2 * i + h]);
           const float b = __uint_as_float(vb[2 * i + h]);
-          const float dhp = __uint_as_float(vd[2 * i + h]);
+          const float dhp = h ? bf16_hi(du[i]) : bf16_lo(du[i]);
           const float sg = 1.f / (1.f + __expf(-a));
           const float sa = a * sg;
           const float hv = sa * b;
@@ -726,11 +747,23 @@ cudaError_t launch_ffn_fwd(const Cfg& c, const Layout& L, const FfnFwdArgs& a, c
 
 cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, cudaStream_t s) {
   const uint64_t rows = (uint64_t)L.rows;
-  BwdFused::Params p3{};
-  if (!map_2d(&p3.tmX, a.x_perm, c.d, rows, 64, 128) || !map_2d(&p3.tmDY, a.dy_perm, c.d, rows, 64, 128) ||
-      !map_3d(&p3.tmWg, a.Wg, c.d, c.f, c.G, 64, 128) || !map_3d(&p3.tmWu, a.Wu, c.d, c.f, c.G, 64, 128) ||
-      !map_3d(&p3.tmWdT, a.Wd, c.f, c.d, c.G, 64, 64))
+  BwdDh::Params p2{};
+  if (!map_2d(&p2.tmDY, a.dy_perm, c.d, rows, 64, 128) || !map_3d(&p2.tmWdT, a.Wd, c.f, c.d, c.G, 64, 64))
     return cudaErrorInvalidValue;
+  p2.DH = a.dh;
+  p2.f = c.f;
+  p2.d = c.d;
+  p2.nt = (c.f + 255) / 256;
+  p2.hdr = a.hdr;
+  p2.tabs = a.tabs;
+  cudaError_t e = launch<BwdDh>(p2, s);
+  if (e != cudaSuccess) return e;
+
+  BwdFused::Params p3{};
+  if (!map_2d(&p3.tmX, a.x_perm, c.d, rows, 64, 128) || !map_3d(&p3.tmWg, a.Wg, c.d, c.f, c.G, 64, 128) ||
+      !map_3d(&p3.tmWu, a.Wu, c.d, c.f, c.G, 64, 128))
+    return cudaErrorInvalidValue;
+  p3.DH = a.dh;
   p3.gate_of_prow = a.gate_of_prow;
   p3.dA = a.dA;
   p3.dB = a.dB;
@@ -742,7 +775,7 @@ cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, c
   p3.ndg = L.ndg;
   p3.hdr = a.hdr;
   p3.tabs = a.tabs;
-  cudaError_t e = launch<BwdFused>(p3, s);
+  e = launch<BwdFused>(p3, s);
   if (e != cudaSuccess) return e;
 
   Wgrad::Params p4{};
