@@ -106,8 +106,9 @@ Layout make_layout(const Cfg& c) {
   L.ntf = (c.f + 127) / 128;
   L.ndg = 2 * L.ntf;
   L.nblk_router = (c.T + route_block_tokens(c.E) - 1) / route_block_tokens(c.E);
-  const int dtiles = (c.d + 63) / 64;
-  L.nsplit_dwr = std::max(1, std::min((304 + dtiles - 1) / dtiles, (c.T + 255) / 256));
+  // token splits of the dW_r tensor-core GEMM: about two tiles per SM, at least 512 tokens each
+  const int mtiles = (c.d + 127) / 128;
+  L.nsplit_dwr = std::max(1, std::min((304 + mtiles - 1) / mtiles, (c.T + 511) / 512));
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -134,6 +135,9 @@ Layout make_layout(const Cfg& c) {
   L.buf_f2 = take(rows * c.f * 2);
   L.buf_f3 = take(rows * c.f * 2);
   L.buf_d1 = take(rows * c.d * 2);
+  L.Ep = (c.E + 63) / 64 * 64;
+  L.dl_bf16 = take((size_t)c.T * L.Ep * 2);
+  L.wr_bf16 = take((size_t)c.d * L.Ep * 2);
   L.total = off;
   return L;
 }
@@ -299,7 +303,29 @@ moe_status_t do_router_bwd(const Cfg& c, const Ws& w, const uint16_t* x, const f
   a.db_r = db_r;
   a.dwr_part = w.at<float>(w.L.dwr_part);
   a.db_part = w.at<float>(w.L.db_part);
-  MOE_CUDA(launch_router_bwd(c, w.L, a, s));
+  uint16_t* dl_bf16 = w.at<uint16_t>(w.L.dl_bf16);
+  MOE_CUDA(launch_router_dlogits(c, w.L, a, s));
+  MOE_CUDA(launch_to_bf16_rows(dlogits, c.T, c.E, w.L.Ep, dl_bf16, s));
+  MOE_CUDA(launch_router_dwr(c, w.L, x, dl_bf16, a.dwr_part, w.hdr(), w.tabs(), s));
+  MOE_CUDA(launch_router_reduce(c, w.L, a, s));
+  return MOE_OK;
+}
+
+// dx = dlogits W_r^T (when dlogits is given) + the token's expert rows of dx_perm, on the tensor
+// cores with bf16 copies of dlogits and W_r padded to Ep columns.
+moe_status_t do_combine_bwd(const Cfg& c, const Ws& w, const uint16_t* dx_perm, const float* dlogits,
+                            const float* W_r, uint16_t* dx, cudaStream_t s) {
+  uint16_t* dl_bf16 = w.at<uint16_t>(w.L.dl_bf16);
+  uint16_t* wr_bf16 = w.at<uint16_t>(w.L.wr_bf16);
+  if (dlogits != nullptr) {
+    MOE_CUDA(launch_to_bf16_rows(dlogits, c.T, c.E, w.L.Ep, dl_bf16, s));
+    MOE_CUDA(launch_to_bf16_rows(W_r, c.d, c.E, w.L.Ep, wr_bf16, s));
+  } else {   // no router term: a zero product
+    MOE_CUDA(cudaMemsetAsync(dl_bf16, 0, (size_t)c.T * w.L.Ep * 2, s));
+    MOE_CUDA(cudaMemsetAsync(wr_bf16, 0, (size_t)c.d * w.L.Ep * 2, s));
+  }
+  CombineBwdArgs a{dl_bf16, wr_bf16, dx_perm, dx, w.at<int32_t>(w.L.prow_of_slot), w.hdr(), w.tabs()};
+  MOE_CUDA(launch_combine_bwd(c, w.L, a, s));
   return MOE_OK;
 }
 
@@ -450,9 +476,7 @@ moe_status_t moe_combine_bwd(const moe_config_t* cfg, const moe_bf16* dx_perm, c
   Ws w;
   MOE_TRY(get_ws(c, ws, ws_bytes, &w));
   MOE_TRY(check_device());
-  CombineBwdArgs a{dx_perm, dlogits, W_r, dx, w.tabs(), w.at<int32_t>(w.L.prow_of_slot)};
-  MOE_CUDA(launch_combine_bwd(c, a, stream));
-  return MOE_OK;
+  return do_combine_bwd(c, w, dx_perm, dlogits, W_r, dx, stream);
 }
 
 moe_status_t moe_layer_fwd(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
@@ -508,9 +532,7 @@ moe_status_t moe_layer_bwd(const moe_config_t* cfg, const moe_bf16* x, const flo
                      dW_down, stream));
   float* dlogits = w.at<float>(w.L.dlogits);
   MOE_TRY(do_router_bwd(c, w, x, W_r, b_r, idx, gates, dgates, dlogits, dW_r, db_r, stream));
-  CombineBwdArgs cb{dx_perm, dlogits, W_r, dx, w.tabs(), w.at<int32_t>(w.L.prow_of_slot)};
-  MOE_CUDA(launch_combine_bwd(c, cb, stream));
-  return MOE_OK;
+  return do_combine_bwd(c, w, dx_perm, dlogits, W_r, dx, stream);
 }
 
 moe_status_t moe_check_error(void* ws, moe_stream_t stream) {

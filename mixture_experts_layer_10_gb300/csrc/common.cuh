@@ -67,8 +67,10 @@ struct Layout {
   int ndg;               // per-row gate-gradient partials (two 64-column halves per d_ff tile)
   int nsplit_dwr;        // token splits of dW_r = x^T dlogits
   int nblk_router;       // router backward blocks (db partials)
+  int Ep;                // E rounded up to 64: row length of the bf16 router operands
   size_t hdr, tabs, scan_status, rank, prow_of_slot, slot_of_prow, gate_of_prow, dg_part,
-      dlogits, dwr_part, db_part, dgates, xperm, dy_perm, buf_f0, buf_f1, buf_f2, buf_f3, buf_d1;
+      dlogits, dwr_part, db_part, dgates, xperm, dy_perm, buf_f0, buf_f1, buf_f2, buf_f3, buf_d1,
+      dl_bf16, wr_bf16;
   size_t total;
 };
 
@@ -146,18 +148,25 @@ struct CombineArgs {
 };
 cudaError_t launch_combine(const Cfg& c, const CombineArgs& a, cudaStream_t s);
 
+// dx = dl W_r^T + the token's expert rows of dx_perm (tensor cores; bf16 operands of E padded to Ep)
 struct CombineBwdArgs {
-  const uint16_t* dx_perm; const float* dlogits; const float* W_r; uint16_t* dx;
-  const Tables* tabs; const int32_t* prow_of_slot;
+  const uint16_t* dl_bf16; const uint16_t* wr_bf16; const uint16_t* dx_perm; uint16_t* dx;
+  const int32_t* prow_of_slot; Hdr* hdr; const Tables* tabs;
 };
-cudaError_t launch_combine_bwd(const Cfg& c, const CombineBwdArgs& a, cudaStream_t s);
+cudaError_t launch_combine_bwd(const Cfg& c, const Layout& L, const CombineBwdArgs& a, cudaStream_t s);
 
 struct RouterBwdArgs {
   const uint16_t* x; const float* W_r; const float* b_r; const int32_t* idx; const float* gates;
   const float* dgates; float* dlogits; float* dW_r; float* db_r;
   float* dwr_part; float* db_part;
 };
-cudaError_t launch_router_bwd(const Cfg& c, const Layout& L, const RouterBwdArgs& a, cudaStream_t s);
+cudaError_t launch_router_dlogits(const Cfg& c, const Layout& L, const RouterBwdArgs& a, cudaStream_t s);
+cudaError_t launch_router_reduce(const Cfg& c, const Layout& L, const RouterBwdArgs& a, cudaStream_t s);
+// dW_r partials over token splits on the tensor cores (x and the bf16 dlogits, both MN-major)
+cudaError_t launch_router_dwr(const Cfg& c, const Layout& L, const uint16_t* x, const uint16_t* dl_bf16,
+                              float* dwr_part, Hdr* hdr, const Tables* tabs, cudaStream_t s);
+// dst [rows, ld] bf16 = src [rows, cols] fp32, zero for cols <= c < ld
+cudaError_t launch_to_bf16_rows(const float* src, int rows, int cols, int ld, uint16_t* dst, cudaStream_t s);
 
 struct DgatesArgs {
   const float* dg_part; const int32_t* prow_of_slot; float* dgates;

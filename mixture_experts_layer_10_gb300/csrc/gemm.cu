@@ -18,11 +18,13 @@
 // Problems (BM = 128, BK = 64, operands bf16, accumulators fp32):
 //   FwdGateUp  H    = silu(X Wg^T) * (X Wu^T)              A=X K-major, B=[Wg;Wu] K-major, N=256
 //   FwdDown    O    = H Wd^T                               A=H K-major, B=Wd K-major,      N=256
-//   BwdFused   phase 1: dh' = dY Wd (B MN-major); phase 2: a|b = X [Wg;Wu]^T (recompute)
-//              epilogue: h = silu(a) b, dg += dh'.h, dh = g dh', dA = dh b silu'(a),
-//              dB = dh silu(a), Hg = g h                  N = 128 (a, b, dh' slots in TMEM)
+//   BwdDh      dh'  = dY Wd                                A K-major, B MN-major,      N=256
+//   BwdFused   a|b  = X [Wg;Wu]^T (recompute); epilogue: h = silu(a) b, dg += dh'.h, dh = g dh',
+//              dA = dh b silu'(a), dB = dh silu(a), Hg = g h                         N=256
 //   Wgrad      dWg = dA^T X, dWu = dB^T X, dWd = dY^T Hg   A and B MN-major, K = segment rows
 //   DgradX     dX   = dA Wg + dB Wu                        A K-major, B MN-major, K = 2 d_ff
+//   RouterDwr  dW_r partials = x^T dl over token splits    A and B MN-major, N = E padded to 64
+//   CombineBwd dx   = dl W_r^T + the token's rows of dX     A and B K-major, K = E padded to 64
 #include <algorithm>
 #include <mutex>
 
@@ -42,6 +44,7 @@ constexpr int kChunkM = 32;                  // m-tiles per L2 reuse chunk of a 
 
 struct Job {
   int seg, m0, n0, kiters, kbase, sub;
+  uint32_t idesc;   // instruction descriptor, for problems whose N is a runtime value
 };
 
 // Defaults of the per-problem hooks; a policy overrides what it needs.
@@ -495,6 +498,169 @@ struct Wgrad : PolicyDefaults {
   }
 };
 
+// Router weight gradient on the tensor cores: partial[split][i][e] = sum over the split's tokens of
+// x[t][i] dl[t][e].  M = d_model in 128-row tiles (A = x, MN-major), N = E padded to 64 (B = the
+// bf16 dlogits [T, Ep], MN-major), K = the split's tokens (tensor maps zero-fill past T).  Four B
+// boxes are always loaded; boxes past Ep are zero-filled and never read by the MMA.  The splits are
+// summed in a fixed order afterwards, so the result is deterministic.
+struct RouterDwr : PolicyDefaults {
+  static constexpr int kId = kKRouterDwr;
+  static constexpr int kEpiWarps = 4;
+  static constexpr int kStages = 4;
+  static constexpr uint32_t kStageBytes = 2 * kBox + 4 * kBox;
+  static constexpr int kAccCols = 256;
+  static constexpr int kAccBufs = 2;
+  static constexpr int kTmemCols = 512;
+  struct Params {
+    CUtensorMap tmX, tmDL;
+    float* part;
+    int d, E, Ep, T, mt, ksplit, nsplit;
+    Hdr* hdr;
+    const Tables* tabs;
+  };
+  __device__ static int num_tiles(const Params& p, const SegSmem&) { return p.mt * p.nsplit; }
+  __device__ static Job job(const Params& p, const SegSmem&, int t) {
+    Job j;
+    const int split = t / p.mt;
+    j.m0 = (t - split * p.mt) * kBM;
+    j.n0 = 0;
+    j.seg = 0;
+    j.sub = split;
+    j.kbase = split * p.ksplit;
+    const int rows = max(0, min(p.ksplit, p.T - j.kbase));
+    j.kiters = (rows + kBK - 1) / kBK;
+    j.idesc = idesc_bf16(128, p.Ep, true, true);
+    return j;
+  }
+  __device__ static void prefetch(const Params& p) { tma_prefetch(&p.tmX); tma_prefetch(&p.tmDL); }
+  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint64_t* bar) {
+    const int row = j.kbase + kit * kBK;
+    tma_load_2d(st, &p.tmX, bar, j.m0, row);
+    tma_load_2d(st + kBox, &p.tmX, bar, j.m0 + 64, row);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) tma_load_2d(st + (2 + i) * kBox, &p.tmDL, bar, 64 * i, row);
+  }
+  __device__ static void mma(const Job& j, int kit, uint32_t sa, uint32_t dt, int) {
+#pragma unroll
+    for (int kk = 0; kk < kBK / 16; ++kk)
+      umma_bf16(dt, sdesc_mnmajor(sa + kk * 2048, kBox), sdesc_mnmajor(sa + 2 * kBox + kk * 2048, kBox),
+                j.idesc, (kit | kk) != 0);
+  }
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int, int) {
+    const int m = j.m0 + row;
+    float* out = p.part + ((size_t)j.sub * p.d + (m < p.d ? m : 0)) * p.E;
+#pragma unroll 1
+    for (int c = 0; c < p.Ep; c += 32) {
+      uint32_t v[32];
+      tmem_ld32(ta + c, v);
+      tmem_ld_wait();
+      if (m >= p.d) continue;
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (c + i < p.E) out[c + i] = __uint_as_float(v[i]);
+    }
+  }
+  // a split with no tokens contributes zeros
+  __device__ static void epilogue_zero(const Params& p, const Job& j, int row, int) {
+    const int m = j.m0 + row;
+    if (m >= p.d) return;
+    float* out = p.part + ((size_t)j.sub * p.d + m) * p.E;
+    for (int e = 0; e < p.E; ++e) out[e] = 0.f;
+  }
+};
+
+// Input gradient of the layer on the tensor cores: dx[t] = dl[t] W_r^T (M = 128 tokens, N = 256
+// columns of d_model, K = E padded to 64, both operands bf16 K-major), with the epilogue adding, in
+// fixed order and fp32, the token's kept expert rows of dx_perm and its shared-expert rows, then
+// rounding once to bf16.  Token owner, no atomics.  Eight epilogue warps (128 columns each).
+struct CombineBwd : PolicyDefaults {
+  static constexpr int kId = kKCombineBwd;
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kStages = 4;
+  static constexpr uint32_t kStageBytes = kTileA + 2 * kTileA;   // dl tile + W_r tile (256 rows)
+  static constexpr int kAccCols = 256;
+  static constexpr int kAccBufs = 2;
+  static constexpr int kTmemCols = 512;
+  static constexpr uint32_t kIdesc = idesc_bf16(128, 256, false, false);
+  struct Params {
+    CUtensorMap tmDL, tmWR;
+    const uint16_t* dx_perm;
+    uint16_t* dx;
+    const int32_t* prow_of_slot;
+    int T, d, k, E, S, mt, nt, kiters;
+    Hdr* hdr;
+    const Tables* tabs;
+  };
+  __device__ static int num_tiles(const Params& p, const SegSmem&) { return p.mt * p.nt; }
+  __device__ static Job job(const Params& p, const SegSmem&, int t) {
+    Job j;
+    const int n = t / p.mt;
+    j.m0 = (t - n * p.mt) * kBM;
+    j.n0 = n * 256;
+    j.seg = 0;
+    j.sub = 0;
+    j.kbase = 0;
+    j.kiters = p.kiters;
+    j.idesc = kIdesc;
+    return j;
+  }
+  __device__ static void prefetch(const Params& p) { tma_prefetch(&p.tmDL); tma_prefetch(&p.tmWR); }
+  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint64_t* bar) {
+    tma_load_2d(st, &p.tmDL, bar, kit * kBK, j.m0);
+    tma_load_2d(st + kTileA, &p.tmWR, bar, kit * kBK, j.n0);
+  }
+  __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
+#pragma unroll
+    for (int kk = 0; kk < kBK / 16; ++kk)
+      umma_bf16(dt, sdesc_kmajor(sa + kk * 32), sdesc_kmajor(sa + kTileA + kk * 32), kIdesc,
+                (kit | kk) != 0);
+  }
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int part, int) {
+    const int t = j.m0 + row;
+#pragma unroll 1
+    for (int c = part * 128; c < part * 128 + 128; c += 32) {
+      const int col = j.n0 + c;
+      if (col >= p.d) break;
+      uint32_t v[32];
+      tmem_ld32(ta + c, v);
+      tmem_ld_wait();
+      if (t >= p.T) continue;
+      float acc[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(v[i]);
+      for (int jj = 0; jj < p.k + p.S; ++jj) {
+        size_t prow;
+        if (jj < p.k) {
+          const int pr = p.prow_of_slot[(size_t)t * p.k + jj];
+          if (pr < 0) continue;
+          prow = (size_t)pr;
+        } else {
+          const int s = p.E + (jj - p.k);
+          if (t >= p.tabs->kept[s]) continue;
+          prow = (size_t)p.tabs->poff[s] + t;
+        }
+        const uint4* src = reinterpret_cast<const uint4*>(p.dx_perm + prow * p.d + col);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint4 u = src[q];
+          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+          for (int m = 0; m < 4; ++m) {
+            acc[8 * q + 2 * m] += bf16_lo(w[m]);
+            acc[8 * q + 2 * m + 1] += bf16_hi(w[m]);
+          }
+        }
+      }
+      uint4* dst = reinterpret_cast<uint4*>(p.dx + (size_t)t * p.d + col);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        dst[q] = make_uint4(pack_bf16(acc[8 * q], acc[8 * q + 1]), pack_bf16(acc[8 * q + 2], acc[8 * q + 3]),
+                            pack_bf16(acc[8 * q + 4], acc[8 * q + 5]), pack_bf16(acc[8 * q + 6], acc[8 * q + 7]));
+    }
+  }
+  __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
+};
+
 // ---------------------------------------------------------------------------------------------
 // The persistent warp-specialised kernel
 // ---------------------------------------------------------------------------------------------
@@ -809,6 +975,44 @@ cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, c
   p5.hdr = a.hdr;
   p5.tabs = a.tabs;
   return launch<DgradX>(p5, s);
+}
+
+cudaError_t launch_router_dwr(const Cfg& c, const Layout& L, const uint16_t* x, const uint16_t* dl_bf16,
+                              float* dwr_part, Hdr* hdr, const Tables* tabs, cudaStream_t s) {
+  RouterDwr::Params p{};
+  if (!map_2d(&p.tmX, x, c.d, c.T, 64, 64) || !map_2d(&p.tmDL, dl_bf16, L.Ep, c.T, 64, 64))
+    return cudaErrorInvalidValue;
+  p.part = dwr_part;
+  p.d = c.d;
+  p.E = c.E;
+  p.Ep = L.Ep;
+  p.T = c.T;
+  p.mt = (c.d + kBM - 1) / kBM;
+  p.nsplit = L.nsplit_dwr;
+  p.ksplit = ((c.T + L.nsplit_dwr - 1) / L.nsplit_dwr + kBK - 1) / kBK * kBK;
+  p.hdr = hdr;
+  p.tabs = tabs;
+  return launch<RouterDwr>(p, s);
+}
+
+cudaError_t launch_combine_bwd(const Cfg& c, const Layout& L, const CombineBwdArgs& a, cudaStream_t s) {
+  CombineBwd::Params p{};
+  if (!map_2d(&p.tmDL, a.dl_bf16, L.Ep, c.T, 64, 128) || !map_2d(&p.tmWR, a.wr_bf16, L.Ep, c.d, 64, 256))
+    return cudaErrorInvalidValue;
+  p.dx_perm = a.dx_perm;
+  p.dx = a.dx;
+  p.prow_of_slot = a.prow_of_slot;
+  p.T = c.T;
+  p.d = c.d;
+  p.k = c.k;
+  p.E = c.E;
+  p.S = c.S;
+  p.mt = (c.T + kBM - 1) / kBM;
+  p.nt = (c.d + 255) / 256;
+  p.kiters = L.Ep / kBK;
+  p.hdr = a.hdr;
+  p.tabs = a.tabs;
+  return launch<CombineBwd>(p, s);
 }
 
 }  // namespace moe

@@ -341,92 +341,6 @@ __global__ void __launch_bounds__(kThreads) router_dlogits_kernel(RouterBwdArgs 
   }
 }
 
-// Router backward, part 2: dW_r partials over token splits, dW_r[i][e] = sum_t x[t][i] dl[t][e].
-template <int EB> struct DwrShape;
-template <> struct DwrShape<8>   { static constexpr int TM = 2, TN = 8, KS = 8; };
-template <> struct DwrShape<16>  { static constexpr int TM = 4, TN = 8, KS = 8; };
-template <> struct DwrShape<32>  { static constexpr int TM = 4, TN = 8, KS = 4; };
-template <> struct DwrShape<64>  { static constexpr int TM = 4, TN = 4, KS = 1; };
-template <> struct DwrShape<128> { static constexpr int TM = 4, TN = 8, KS = 1; };
-template <> struct DwrShape<256> { static constexpr int TM = 8, TN = 8, KS = 1; };
-
-constexpr int kDwrRows = 64;   // d-rows per block
-
-template <int EB>
-struct DwrSmem {
-  using S = DwrShape<EB>;
-  float xs[kKC][kDwrRows + 4];
-  float ls[kKC][EB];
-  float red[S::KS > 1 ? S::KS : 1][kDwrRows][EB + 1];
-};
-
-template <int EB>
-__global__ void __launch_bounds__(kThreads) router_dwr_kernel(RouterBwdArgs a, int T, int d, int E,
-                                                              int tokens_per_split) {
-  extern __shared__ __align__(16) uint8_t smem_raw[];
-  DwrSmem<EB>& sm = *reinterpret_cast<DwrSmem<EB>*>(smem_raw);
-  using S = DwrShape<EB>;
-  constexpr int TX = kDwrRows / S::TM, TY = EB / S::TN;
-  static_assert(TX * TY * S::KS == kThreads, "thread tiling");
-  const int tid = threadIdx.x;
-  const int ks = tid / (TX * TY), ty = (tid / TX) % TY, tx = tid % TX;
-  const int i0 = blockIdx.x * kDwrRows;
-  const int split = blockIdx.y;
-  const int tb = split * tokens_per_split;
-  const int te = min(T, tb + tokens_per_split);
-  float acc[S::TM][S::TN];
-#pragma unroll
-  for (int i = 0; i < S::TM; ++i)
-#pragma unroll
-    for (int j = 0; j < S::TN; ++j) acc[i][j] = 0.f;
-  for (int c0 = tb; c0 < te; c0 += kKC) {
-    // x rows c0..c0+31, columns i0..i0+63 (8 16-byte pieces per row)
-    for (int p = tid; p < kKC * 8; p += kThreads) {
-      const int r = p / 8, q = p % 8;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (c0 + r < te && i0 + q * 8 < d)
-        v = *reinterpret_cast<const uint4*>(a.x + (size_t)(c0 + r) * d + i0 + q * 8);
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        sm.xs[r][q * 8 + 2 * m] = bf16_lo(w[m]);
-        sm.xs[r][q * 8 + 2 * m + 1] = bf16_hi(w[m]);
-      }
-    }
-    for (int p = tid; p < kKC * EB; p += kThreads) {
-      const int r = p / EB, e = p % EB;
-      sm.ls[r][e] = (c0 + r < te && e < E) ? a.dlogits[(size_t)(c0 + r) * E + e] : 0.f;
-    }
-    __syncthreads();
-#pragma unroll 4
-    for (int kk = ks; kk < kKC; kk += S::KS) {
-      float xv[S::TM], lv[S::TN];
-#pragma unroll
-      for (int i = 0; i < S::TM; ++i) xv[i] = sm.xs[kk][tx * S::TM + i];
-#pragma unroll
-      for (int j = 0; j < S::TN; ++j) lv[j] = sm.ls[kk][ty * S::TN + j];
-#pragma unroll
-      for (int i = 0; i < S::TM; ++i)
-#pragma unroll
-        for (int j = 0; j < S::TN; ++j) acc[i][j] = fmaf(xv[i], lv[j], acc[i][j]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int i = 0; i < S::TM; ++i)
-#pragma unroll
-    for (int j = 0; j < S::TN; ++j) sm.red[ks][tx * S::TM + i][ty * S::TN + j] = acc[i][j];
-  __syncthreads();
-  for (int p = tid; p < kDwrRows * EB; p += kThreads) {
-    const int r = p / EB, e = p % EB;
-    if (i0 + r >= d || e >= E) continue;
-    float v = sm.red[0][r][e];
-#pragma unroll
-    for (int s = 1; s < S::KS; ++s) v += sm.red[s][r][e];
-    a.dwr_part[((size_t)split * d + i0 + r) * E + e] = v;
-  }
-}
-
 // Router backward, part 3: fixed-order sums of the dW_r and db partials.
 __global__ void router_reduce_kernel(RouterBwdArgs a, int d, int E, int nsplit, int nblk) {
   const size_t n = (size_t)d * E;
@@ -466,37 +380,27 @@ cudaError_t route_fwd_eb(const Cfg& c, const RouteArgs& a, cudaStream_t s) {
 }
 
 template <int EB>
-cudaError_t router_bwd_eb(const Cfg& c, const Layout& L, const RouterBwdArgs& a, cudaStream_t s) {
-  using S = RouteShape<EB>;
-  {
-    const size_t smem = sizeof(LogitSmem<EB>);
-    auto kern = router_dlogits_kernel<EB>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    prof_mark(kKRouterDlogits, s, true);
-    kern<<<L.nblk_router, kThreads, smem, s>>>(a, c.T, c.d, c.E, c.k, c.renorm);
-    prof_mark(kKRouterDlogits, s, false);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    (void)S::BT;
-  }
-  {
-    const size_t smem = sizeof(DwrSmem<EB>);
-    auto kern = router_dwr_kernel<EB>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    const int per = (c.T + L.nsplit_dwr - 1) / L.nsplit_dwr;
-    dim3 grid((c.d + kDwrRows - 1) / kDwrRows, L.nsplit_dwr);
-    prof_mark(kKRouterDwr, s, true);
-    kern<<<grid, kThreads, smem, s>>>(a, c.T, c.d, c.E, per);
-    prof_mark(kKRouterDwr, s, false);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  const size_t n = (size_t)c.d * c.E + c.E;
-  const int blocks = (int)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 4);
-  prof_mark(kKRouterReduce, s, true);
-  router_reduce_kernel<<<blocks, 256, 0, s>>>(a, c.d, c.E, L.nsplit_dwr, L.nblk_router);
-  prof_mark(kKRouterReduce, s, false);
+cudaError_t router_dlogits_eb(const Cfg& c, const Layout& L, const RouterBwdArgs& a, cudaStream_t s) {
+  const size_t smem = sizeof(LogitSmem<EB>);
+  auto kern = router_dlogits_kernel<EB>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  prof_mark(kKRouterDlogits, s, true);
+  kern<<<L.nblk_router, kThreads, smem, s>>>(a, c.T, c.d, c.E, c.k, c.renorm);
+  prof_mark(kKRouterDlogits, s, false);
   return cudaGetLastError();
+}
+
+// dst[r][c] = bf16(src[r][c]) for c < cols, 0 for cols <= c < ld (rows of the tensor-core operands)
+__global__ void to_bf16_rows_kernel(const float* __restrict__ src, int rows, int cols, int ld,
+                                    uint16_t* __restrict__ dst) {
+  const size_t n = (size_t)rows * ld;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = i / ld;
+    const int c = (int)(i - r * ld);
+    const float v = c < cols ? src[r * cols + c] : 0.f;
+    dst[i] = (uint16_t)(pack_bf16(v, 0.f) & 0xFFFFu);
+  }
 }
 
 }  // namespace
@@ -523,15 +427,31 @@ cudaError_t launch_route(const Cfg& c, const RouteArgs& a, cudaStream_t s) {
   }
 }
 
-cudaError_t launch_router_bwd(const Cfg& c, const Layout& L, const RouterBwdArgs& a, cudaStream_t s) {
+cudaError_t launch_router_dlogits(const Cfg& c, const Layout& L, const RouterBwdArgs& a, cudaStream_t s) {
   switch (bucket_of(c.E)) {
-    case 8: return router_bwd_eb<8>(c, L, a, s);
-    case 16: return router_bwd_eb<16>(c, L, a, s);
-    case 32: return router_bwd_eb<32>(c, L, a, s);
-    case 64: return router_bwd_eb<64>(c, L, a, s);
-    case 128: return router_bwd_eb<128>(c, L, a, s);
-    default: return router_bwd_eb<256>(c, L, a, s);
+    case 8: return router_dlogits_eb<8>(c, L, a, s);
+    case 16: return router_dlogits_eb<16>(c, L, a, s);
+    case 32: return router_dlogits_eb<32>(c, L, a, s);
+    case 64: return router_dlogits_eb<64>(c, L, a, s);
+    case 128: return router_dlogits_eb<128>(c, L, a, s);
+    default: return router_dlogits_eb<256>(c, L, a, s);
   }
+}
+
+cudaError_t launch_router_reduce(const Cfg& c, const Layout& L, const RouterBwdArgs& a, cudaStream_t s) {
+  const size_t n = (size_t)c.d * c.E + c.E;
+  const int blocks = (int)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 4);
+  prof_mark(kKRouterReduce, s, true);
+  router_reduce_kernel<<<blocks, 256, 0, s>>>(a, c.d, c.E, L.nsplit_dwr, L.nblk_router);
+  prof_mark(kKRouterReduce, s, false);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_to_bf16_rows(const float* src, int rows, int cols, int ld, uint16_t* dst, cudaStream_t s) {
+  const size_t n = (size_t)rows * ld;
+  const int blocks = (int)std::max<size_t>(1, std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 8));
+  to_bf16_rows_kernel<<<blocks, 256, 0, s>>>(src, rows, cols, ld, dst);
+  return cudaGetLastError();
 }
 
 }  // namespace moe
