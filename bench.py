@@ -260,7 +260,7 @@ def main():
     # rows the experts see (no pads): kept routed slots + shared tokens, from one dispatch
     idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
     gates = torch.empty(T, k, dtype=torch.float32, device="cuda")
-    moe.moe_route(mc, x, W_r, b_r, idx, gates)
+    moe.moe_route(mc, x, W_r, b_r, idx, gates, None, buf.ws)
     counts = torch.empty(E, dtype=torch.int32, device="cuda")
     offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
     scratch_rows = torch.empty(T * k, dtype=torch.int32, device="cuda")

@@ -113,10 +113,15 @@ moe_status_t moe_perm_rows(const moe_config_t* cfg, int64_t* rows);
 /* Zero the workspace header (error word and device counters).  Call once after allocating. */
 moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* Router: logits, softmax, top-k and gates for every token (warp per token for the selection).
- * b_r and logits may be NULL.  Writes idx [T,k], gates [T,k], and logits [T,E] when non-NULL. */
+/* Router: logits, softmax, top-k and gates for every token.  b_r and logits may be NULL.
+ * Writes idx [T,k], gates [T,k], and logits [T,E] when non-NULL.  ws is this configuration's
+ * workspace (moe_workspace_size).  For 32 <= E <= 128 and k <= 8 the logits run on the tensor
+ * cores: W_r is split in ws into three bf16 parts whose sum equals it within fp32 rounding, and the
+ * products are summed in fp32 over 256-wide slices of d_model; other shapes use an fp32 tile
+ * product with warp-per-token selection. */
 moe_status_t moe_route(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
-                       int32_t* idx, float* gates, float* logits, moe_stream_t stream);
+                       int32_t* idx, float* gates, float* logits, void* ws, size_t ws_bytes,
+                       moe_stream_t stream);
 
 /* Dispatch queues (MoEBlaze, Methodology item 1): per-expert histogram, exclusive prefix sum with
  * a decoupled look-back, stable (token-order) ranks, capacity, and the 16-byte gather of x rows into

@@ -59,7 +59,7 @@ def load(path: str | None = None):
         "moe_workspace_size": [cfgp, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)],
         "moe_perm_rows": [cfgp, ctypes.POINTER(ctypes.c_int64)],
         "moe_workspace_init": [cfgp, _P, ctypes.c_size_t, _P],
-        "moe_route": [cfgp, _P, _P, _P, _P, _P, _P, _P],
+        "moe_route": [cfgp, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
         "moe_dispatch": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
         "moe_dispatch_noalloc": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P],
         "moe_expert_ffn_fwd": [cfgp, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
@@ -146,9 +146,9 @@ def moe_workspace_init(cfg, ws, stream=None):
     _call("moe_workspace_init", ctypes.byref(cfg), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
 
 
-def moe_route(cfg, x, W_r, b_r, idx, gates, logits=None, stream=None):
+def moe_route(cfg, x, W_r, b_r, idx, gates, logits, ws, stream=None):
     _call("moe_route", ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(b_r), _ptr(idx), _ptr(gates),
-          _ptr(logits), _stream(stream))
+          _ptr(logits), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
 
 
 def moe_dispatch(cfg, idx, x, counts, offsets, row_of_slot, token_of_row, x_perm, ws, stream=None):

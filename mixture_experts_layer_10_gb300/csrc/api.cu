@@ -105,7 +105,9 @@ Layout make_layout(const Cfg& c) {
   L.nscan = (int)(((int64_t)c.T * c.k + kScanChunk - 1) / kScanChunk);
   L.ntf = (c.f + 127) / 128;
   L.ndg = 2 * L.ntf;
-  L.nblk_router = (c.T + route_block_tokens(c.E) - 1) / route_block_tokens(c.E);
+  // db partials: one per 32 tokens from the tensor-core backward, else one per SIMT router block
+  L.nblk_router = router_bwd_on_tensor_cores(c) ? 4 * ((c.T + kRowTile - 1) / kRowTile)
+                                                : (c.T + route_block_tokens(c.E) - 1) / route_block_tokens(c.E);
   // token splits of the dW_r tensor-core GEMM: about two tiles per SM, at least 512 tokens each
   const int mtiles = (c.d + 127) / 128;
   L.nsplit_dwr = std::max(1, std::min((304 + mtiles - 1) / mtiles, (c.T + 511) / 512));
@@ -138,6 +140,7 @@ Layout make_layout(const Cfg& c) {
   L.Ep = (c.E + 63) / 64 * 64;
   L.dl_bf16 = take((size_t)c.T * L.Ep * 2);
   L.wr_bf16 = take((size_t)c.d * L.Ep * 2);
+  L.wr3 = take((size_t)3 * L.Ep * c.d * 2);
   L.total = off;
   return L;
 }
@@ -304,10 +307,34 @@ moe_status_t do_router_bwd(const Cfg& c, const Ws& w, const uint16_t* x, const f
   a.dwr_part = w.at<float>(w.L.dwr_part);
   a.db_part = w.at<float>(w.L.db_part);
   uint16_t* dl_bf16 = w.at<uint16_t>(w.L.dl_bf16);
-  MOE_CUDA(launch_router_dlogits(c, w.L, a, s));
-  MOE_CUDA(launch_to_bf16_rows(dlogits, c.T, c.E, w.L.Ep, dl_bf16, s));
+  if (router_bwd_on_tensor_cores(c)) {   // logits recomputed on the tensor cores; dl in both types
+    uint16_t* wr3 = w.at<uint16_t>(w.L.wr3);
+    MOE_CUDA(launch_split_wr(W_r, c.d, c.E, w.L.Ep, wr3, s));
+    RouterTcArgs t{x, wr3, b_r, const_cast<int32_t*>(idx), const_cast<float*>(gates), nullptr,
+                   dgates, dlogits, dl_bf16, a.db_part, w.hdr(), w.tabs()};
+    MOE_CUDA(launch_router_dlogits_tc(c, w.L, t, s));
+  } else {
+    MOE_CUDA(launch_router_dlogits(c, w.L, a, s));
+    MOE_CUDA(launch_to_bf16_rows(dlogits, c.T, c.E, w.L.Ep, dl_bf16, s));
+  }
   MOE_CUDA(launch_router_dwr(c, w.L, x, dl_bf16, a.dwr_part, w.hdr(), w.tabs(), s));
   MOE_CUDA(launch_router_reduce(c, w.L, a, s));
+  return MOE_OK;
+}
+
+// Router forward: logits on the tensor cores when the shape allows (W_r split into bf16 parts
+// first), else the fp32 tile product.
+moe_status_t do_route(const Cfg& c, const Ws& w, const uint16_t* x, const float* W_r, const float* b_r,
+                      int32_t* idx, float* gates, float* logits, cudaStream_t s) {
+  if (router_on_tensor_cores(c)) {
+    uint16_t* wr3 = w.at<uint16_t>(w.L.wr3);
+    MOE_CUDA(launch_split_wr(W_r, c.d, c.E, w.L.Ep, wr3, s));
+    RouterTcArgs t{x, wr3, b_r, idx, gates, logits, nullptr, nullptr, nullptr, nullptr, w.hdr(), w.tabs()};
+    MOE_CUDA(launch_route_tc(c, w.L, t, s));
+  } else {
+    RouteArgs a{x, W_r, b_r, idx, gates, logits};
+    MOE_CUDA(launch_route(c, a, s));
+  }
   return MOE_OK;
 }
 
@@ -373,15 +400,16 @@ moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, size_t ws_byt
 }
 
 moe_status_t moe_route(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
-                       int32_t* idx, float* gates, float* logits, moe_stream_t stream) {
+                       int32_t* idx, float* gates, float* logits, void* ws, size_t ws_bytes,
+                       moe_stream_t stream) {
   Cfg c;
   MOE_TRY(make_cfg(cfg, &c));
   MOE_NEED(x && W_r && idx && gates && aligned16(x) && aligned16(W_r) && aligned16(idx) &&
            aligned16(gates) && (!b_r || aligned16(b_r)) && (!logits || aligned16(logits)));
+  Ws w;
+  MOE_TRY(get_ws(c, ws, ws_bytes, &w));
   MOE_TRY(check_device());
-  RouteArgs a{x, W_r, b_r, idx, gates, logits};
-  MOE_CUDA(launch_route(c, a, stream));
-  return MOE_OK;
+  return do_route(c, w, x, W_r, b_r, idx, gates, logits, stream);
 }
 
 moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* idx, const moe_bf16* x,
@@ -492,8 +520,7 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const moe_bf16* x, const flo
   MOE_TRY(check_device());
   int32_t* idx = static_cast<int32_t*>(saved);
   float* gates = reinterpret_cast<float*>(idx + (size_t)c.T * c.k);
-  RouteArgs ra{x, W_r, b_r, idx, gates, nullptr};
-  MOE_CUDA(launch_route(c, ra, stream));
+  MOE_TRY(do_route(c, w, x, W_r, b_r, idx, gates, nullptr, stream));
   uint16_t* x_perm = w.at<uint16_t>(w.L.xperm);
   MOE_TRY(do_dispatch(c, w, idx, x, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, x_perm,
                       nullptr, stream));

@@ -70,7 +70,7 @@ struct Layout {
   int Ep;                // E rounded up to 64: row length of the bf16 router operands
   size_t hdr, tabs, scan_status, rank, prow_of_slot, slot_of_prow, gate_of_prow, dg_part,
       dlogits, dwr_part, db_part, dgates, xperm, dy_perm, buf_f0, buf_f1, buf_f2, buf_f3, buf_d1,
-      dl_bf16, wr_bf16;
+      dl_bf16, wr_bf16, wr3;
   size_t total;
 };
 
@@ -167,6 +167,20 @@ cudaError_t launch_router_dwr(const Cfg& c, const Layout& L, const uint16_t* x, 
                               float* dwr_part, Hdr* hdr, const Tables* tabs, cudaStream_t s);
 // dst [rows, ld] bf16 = src [rows, cols] fp32, zero for cols <= c < ld
 cudaError_t launch_to_bf16_rows(const float* src, int rows, int cols, int ld, uint16_t* dst, cudaStream_t s);
+
+// Router logits on the tensor cores (32 <= E <= 128, k <= 8): W_r [d, E] fp32 is split into
+// hi + mid + lo bf16 parts stored K-major as wr3 [3][Ep][d].
+bool router_on_tensor_cores(const Cfg& c);
+bool router_bwd_on_tensor_cores(const Cfg& c);   // the backward too (gates not renormalised)
+cudaError_t launch_split_wr(const float* W_r, int d, int E, int Ep, uint16_t* wr3, cudaStream_t s);
+struct RouterTcArgs {
+  const uint16_t* x; const uint16_t* wr3; const float* b_r;
+  int32_t* idx; float* gates; float* logits;                               // forward (read in bwd)
+  const float* dgates; float* dlogits; uint16_t* dl_bf16; float* db_part;   // backward
+  Hdr* hdr; const Tables* tabs;
+};
+cudaError_t launch_route_tc(const Cfg& c, const Layout& L, const RouterTcArgs& a, cudaStream_t s);
+cudaError_t launch_router_dlogits_tc(const Cfg& c, const Layout& L, const RouterTcArgs& a, cudaStream_t s);
 
 struct DgatesArgs {
   const float* dg_part; const int32_t* prow_of_slot; float* dgates;

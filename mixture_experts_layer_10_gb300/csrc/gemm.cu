@@ -25,6 +25,8 @@
 //   DgradX     dX   = dA Wg + dB Wu                        A K-major, B MN-major, K = 2 d_ff
 //   RouterDwr  dW_r partials = x^T dl over token splits    A and B MN-major, N = E padded to 64
 //   CombineBwd dx   = dl W_r^T + the token's rows of dX     A and B K-major, K = E padded to 64
+//   RouterLogits  l = x W_r with W_r in three bf16 parts; epilogue: softmax, top-k, or the
+//              router's dlogits                          A and B K-major, N = E padded to 64
 #include <algorithm>
 #include <mutex>
 
@@ -53,6 +55,9 @@ struct PolicyDefaults {
   __device__ static int acc_wait_kit(const Job&) { return 0; }
   // TMA bytes that complete one stage at k-iteration kit
   __device__ static uint32_t tx_bytes(const Job&, int, uint32_t stage_bytes) { return stage_bytes; }
+  // a stateful policy keeps per-lane epilogue state across the jobs of one CTA (epilogue_s)
+  static constexpr bool kStateful = false;
+  struct EpiState {};
 };
 
 struct SegSmem {
@@ -661,6 +666,243 @@ struct CombineBwd : PolicyDefaults {
   __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
 };
 
+// Router logits on the tensor cores: l = x W_r with W_r split into three bf16 parts
+// (W = hi + mid + lo, equal to W within fp32 rounding) stored K-major as [3][Ep][d_model].  x is
+// exactly bf16, so every partial product is exact and only the accumulation rounds.  A tensor-core
+// accumulator can lose about one fp32 unit of its own size per MMA step, so a single accumulator
+// over all 3 d_model / 16 steps drifts by ~1e-5 of the logit at d_model = 2048.  K is therefore cut
+// into chunks of kChunkKits 64-wide blocks; each chunk starts two fresh accumulators, one for the hi
+// products (16 MMA steps) and one for the mid + lo products (2^8 smaller, so their rounding is
+// negligible), and the epilogue adds both into fp32 registers.  A job is one (128-token tile, K
+// chunk); the chunks of a tile run on one CTA, in order.  M = 128 tokens, N = Ep (64 or 128).
+// After the last chunk the epilogue stores each lane's sums into the hi columns of the accumulator
+// it still holds, then reads its logits back in 32-column pieces:
+//   forward (kBwd = false): online softmax (running max and rescaled sum of exp) and the top-k
+//     kept sorted while streaming, larger logit first and a tie keeping the lower expert index
+//     (k <= 8); gates are p of the selected experts, or renormalised over them; logits written when
+//     requested.
+//   backward: a second pass gives dl_e = p_e (dg_slot(e) [e selected] - sum_j dg_j g_j) in fp32
+//     and as the bf16 operand row (zero-padded to Ep), and for db one partial sum per warp of 32
+//     tokens (summed in a fixed order afterwards).
+constexpr int kRouterTopK = 8;
+
+template <bool kBwd>
+struct RouterLogits : PolicyDefaults {
+  static constexpr int kId = kBwd ? kKRouterDlogits : kKRoute;
+  static constexpr int kEpiWarps = 4;
+  static constexpr int kStages = 3;
+  static constexpr uint32_t kStageBytes = 4 * kTileA;   // x tile + three W_r parts (128 rows each)
+  static constexpr int kAccCols = 256;                   // hi products, then mid + lo at +128
+  static constexpr int kAccBufs = 2;
+  static constexpr int kTmemCols = 512;
+  static constexpr int kChunkKits = 4;                   // 256 of K per chunk
+  static constexpr bool kStateful = true;
+  struct Params {
+    CUtensorMap tmX, tmW;
+    const float* b_r;
+    int T, d, E, Ep, k, renorm, mt, nch;
+    int32_t* idx;            // forward output / backward input
+    float* gates;            // forward output / backward input
+    float* logits;           // forward, nullable
+    const float* dgates;     // backward
+    float* dlogits;          // backward
+    uint16_t* dl_bf16;       // backward [T, Ep]
+    float* db_part;          // backward [4 * mt, E]
+    Hdr* hdr;
+    const Tables* tabs;
+  };
+  // CTA b runs tiles b, b + grid, ... and each tile's nch chunks back to back
+  __device__ static int num_tiles(const Params& p, const SegSmem&) {
+    const int g = (int)gridDim.x;
+    return g * ((p.mt + g - 1) / g) * p.nch;
+  }
+  __device__ static Job job(const Params& p, const SegSmem&, int t) {
+    const int g = (int)gridDim.x;
+    const int i = t / g;
+    const int tile = (t - i * g) + (i / p.nch) * g;
+    const int ch = i % p.nch;
+    Job j;
+    j.m0 = tile * kBM;
+    j.n0 = 0;
+    j.seg = 0;
+    j.sub = ch;
+    j.kbase = ch * kChunkKits;
+    j.kiters = tile < p.mt ? min(kChunkKits, p.d / kBK - j.kbase) : 0;
+    j.idesc = idesc_bf16(128, p.Ep, false, false);
+    return j;
+  }
+  __device__ static void prefetch(const Params& p) { tma_prefetch(&p.tmX); tma_prefetch(&p.tmW); }
+  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint64_t* bar) {
+    const int kx = (j.kbase + kit) * kBK;
+    tma_load_2d(st, &p.tmX, bar, kx, j.m0);
+#pragma unroll
+    for (int q = 0; q < 3; ++q) tma_load_3d(st + (1 + q) * kTileA, &p.tmW, bar, kx, 0, q);
+  }
+  __device__ static void mma(const Job& j, int kit, uint32_t sa, uint32_t dt, int) {
+#pragma unroll
+    for (int kk = 0; kk < kBK / 16; ++kk) {
+      const uint64_t da = sdesc_kmajor(sa + kk * 32);
+      const bool acc = (kit | kk) != 0;
+      umma_bf16(dt, da, sdesc_kmajor(sa + kTileA + kk * 32), j.idesc, acc);
+      umma_bf16(dt + 128, da, sdesc_kmajor(sa + 2 * kTileA + kk * 32), j.idesc, acc);
+      umma_bf16(dt + 128, da, sdesc_kmajor(sa + 3 * kTileA + kk * 32), j.idesc, true);
+    }
+  }
+  struct EpiState { float l[128]; };   // this lane's running sums over the chunks so far
+  __device__ static void epilogue_s(const Params& p, const Job& j, uint32_t ta, int row, int, int,
+                                    EpiState& st, uint32_t) {
+    const bool first = j.sub == 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      if (c * 32 < p.Ep) {   // warp-uniform: tcgen05.ld is warp-wide
+        uint32_t h[32], r[32];
+        tmem_ld32(ta + c * 32, h);
+        tmem_ld32(ta + 128 + c * 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          st.l[c * 32 + i] = (first ? 0.f : st.l[c * 32 + i]) + (__uint_as_float(h[i]) + __uint_as_float(r[i]));
+      }
+    }
+    if (j.sub != p.nch - 1) return;
+    // last chunk: the sums go back into this accumulator's hi columns for the rolled passes below
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      if (c * 32 < p.Ep) {
+        uint32_t v[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(st.l[c * 32 + i]);
+        tmem_st32(ta + c * 32, v);
+      }
+    }
+    tmem_st_wait();
+    finish(p, j, ta, row);
+  }
+  // logits of columns [c, c + 32) for this lane's token from S (bias added, -inf past E)
+  __device__ static void chunk(const Params& p, uint32_t sum, int c, float (&l)[32]) {
+    uint32_t v[32];
+    tmem_ld32(sum + c, v);
+    tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const int e = c + i;
+      l[i] = e < p.E ? __uint_as_float(v[i]) + (p.b_r != nullptr ? p.b_r[e] : 0.f) : -INFINITY;
+    }
+  }
+  __device__ static void finish(const Params& p, const Job& j, uint32_t sum, int row) {
+    const int t = j.m0 + row;
+    const bool live = t < p.T;
+    // pass 1: running max and rescaled sum of exp (every lane loads: tcgen05.ld is warp-wide)
+    float m = -INFINITY, z = 0.f;
+    float tv[kRouterTopK];
+    int ti[kRouterTopK];
+#pragma unroll
+    for (int s = 0; s < kRouterTopK; ++s) {
+      tv[s] = -INFINITY;
+      ti[s] = 0x7fffffff;
+    }
+#pragma unroll 1
+    for (int c = 0; c < p.Ep; c += 32) {
+      float l[32];
+      chunk(p, sum, c, l);
+      float cm = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) cm = fmaxf(cm, l[i]);
+      if (cm > m) {
+        z = (m == -INFINITY) ? 0.f : z * expf(m - cm);
+        m = cm;
+      }
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z += (c + i < p.E) ? expf(l[i] - m) : 0.f;
+      if (!kBwd) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          if (live && p.logits != nullptr && c + i < p.E) p.logits[(size_t)t * p.E + c + i] = l[i];
+          float cv = l[i];
+          int ci = c + i;
+#pragma unroll
+          for (int s = 0; s < kRouterTopK; ++s)
+            if (cv > tv[s]) {
+              const float fv = tv[s];
+              const int fi = ti[s];
+              tv[s] = cv;
+              ti[s] = ci;
+              cv = fv;
+              ci = fi;
+            }
+        }
+      }
+    }
+    if (!kBwd) {
+      if (!live) return;
+      float zsel = 0.f;
+#pragma unroll
+      for (int s = 0; s < kRouterTopK; ++s)
+        if (s < p.k) zsel += expf(tv[s] - m);
+      const float denom = p.renorm ? zsel : z;
+#pragma unroll
+      for (int s = 0; s < kRouterTopK; ++s)
+        if (s < p.k) {
+          p.idx[(size_t)t * p.k + s] = ti[s];
+          p.gates[(size_t)t * p.k + s] = expf(tv[s] - m) / denom;
+        }
+      return;
+    }
+    // backward pass 2: dl for every expert of this token
+    float sdg = 0.f;
+    int sid[kRouterTopK];
+    float sgd[kRouterTopK];
+#pragma unroll
+    for (int s = 0; s < kRouterTopK; ++s) {
+      sid[s] = -1;
+      sgd[s] = 0.f;
+      if (live && s < p.k) {
+        sid[s] = p.idx[(size_t)t * p.k + s];
+        sgd[s] = p.dgates[(size_t)t * p.k + s];
+        sdg += sgd[s] * p.gates[(size_t)t * p.k + s];
+      }
+    }
+    const int lane = threadIdx.x & 31;
+    const int wq = row >> 5;   // TMEM lane quarter: one db partial per 32 tokens
+#pragma unroll 1
+    for (int c = 0; c < p.Ep; c += 32) {
+      float l[32];
+      chunk(p, sum, c, l);
+      float dl[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int e = c + i;
+        float dsel = 0.f;
+#pragma unroll
+        for (int s = 0; s < kRouterTopK; ++s) dsel += (sid[s] == e) ? sgd[s] : 0.f;
+        dl[i] = (live && e < p.E) ? expf(l[i] - m) / z * (dsel - sdg) : 0.f;
+      }
+      if (live) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(dl[2 * i], dl[2 * i + 1]);
+        uint4* db = reinterpret_cast<uint4*>(p.dl_bf16 + (size_t)t * p.Ep + c);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) db[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (c + i < p.E) p.dlogits[(size_t)t * p.E + c + i] = dl[i];
+      }
+      // db partial of these 32 tokens: a warp sum per expert, lane i keeps expert c + i
+      float mine = 0.f;
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        float v = dl[i];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        if (lane == i) mine = v;
+      }
+      if (c + lane < p.E) p.db_part[((size_t)(j.m0 / kBM) * 4 + wq) * p.E + c + lane] = mine;
+    }
+  }
+  __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
+};
+
 // ---------------------------------------------------------------------------------------------
 // The persistent warp-specialised kernel
 // ---------------------------------------------------------------------------------------------
@@ -788,6 +1030,7 @@ __global__ void __launch_bounds__(threads_of<P>(), 1) gemm_kernel(const __grid_c
     int acc = 0;
     uint32_t acc_phase = 0;
     int seq = 0;
+    typename P::EpiState es;
     for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
       const Job j = P::job(p, segs, t);
       if (j.kiters == 0) {
@@ -800,8 +1043,11 @@ __global__ void __launch_bounds__(threads_of<P>(), 1) gemm_kernel(const __grid_c
         break;
       }
       tc_fence_after();
-      P::epilogue(p, j, tmem_base + (uint32_t)(acc * P::kAccCols) + ((uint32_t)(q * 32) << 16), row, part,
-                  seq);
+      const uint32_t ta = tmem_base + (uint32_t)(acc * P::kAccCols) + ((uint32_t)(q * 32) << 16);
+      if constexpr (P::kStateful)
+        P::epilogue_s(p, j, ta, row, part, seq, es, tmem_base + ((uint32_t)(q * 32) << 16));
+      else
+        P::epilogue(p, j, ta, row, part, seq);
       ++seq;
       tc_fence_before();
       __syncwarp();
@@ -993,6 +1239,41 @@ cudaError_t launch_router_dwr(const Cfg& c, const Layout& L, const uint16_t* x, 
   p.hdr = hdr;
   p.tabs = tabs;
   return launch<RouterDwr>(p, s);
+}
+
+template <bool kBwd>
+cudaError_t launch_router_tc(const Cfg& c, const Layout& L, const RouterTcArgs& a, cudaStream_t s) {
+  using P = RouterLogits<kBwd>;
+  typename P::Params p{};
+  if (!map_2d(&p.tmX, a.x, c.d, c.T, 64, 128) || !map_3d(&p.tmW, a.wr3, c.d, L.Ep, 3, 64, 128))
+    return cudaErrorInvalidValue;
+  p.b_r = a.b_r;
+  p.T = c.T;
+  p.d = c.d;
+  p.E = c.E;
+  p.Ep = L.Ep;
+  p.k = c.k;
+  p.renorm = c.renorm;
+  p.mt = (c.T + kBM - 1) / kBM;
+  p.nch = (c.d / kBK + P::kChunkKits - 1) / P::kChunkKits;
+  p.idx = a.idx;
+  p.gates = a.gates;
+  p.logits = a.logits;
+  p.dgates = a.dgates;
+  p.dlogits = a.dlogits;
+  p.dl_bf16 = a.dl_bf16;
+  p.db_part = a.db_part;
+  p.hdr = a.hdr;
+  p.tabs = a.tabs;
+  return launch<P>(p, s);
+}
+
+cudaError_t launch_route_tc(const Cfg& c, const Layout& L, const RouterTcArgs& a, cudaStream_t s) {
+  return launch_router_tc<false>(c, L, a, s);
+}
+
+cudaError_t launch_router_dlogits_tc(const Cfg& c, const Layout& L, const RouterTcArgs& a, cudaStream_t s) {
+  return launch_router_tc<true>(c, L, a, s);
 }
 
 cudaError_t launch_combine_bwd(const Cfg& c, const Layout& L, const CombineBwdArgs& a, cudaStream_t s) {

@@ -391,6 +391,35 @@ cudaError_t router_dlogits_eb(const Cfg& c, const Layout& L, const RouterBwdArgs
   return cudaGetLastError();
 }
 
+// W_r [d, E] fp32 -> three bf16 parts, K-major [3][Ep][d]: hi = bf16(w), mid = bf16(w - hi),
+// lo = bf16(w - hi - mid) (each difference is exact in fp32), so hi + mid + lo equals w to within
+// fp32 rounding; experts E..Ep-1 are zero.  32 x 32 tiles transposed through shared memory.
+__global__ void split_wr_kernel(const float* __restrict__ W_r, int d, int E, int Ep, uint16_t* __restrict__ wr3) {
+  __shared__ float tile[32][33];
+  const int r0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;   // 32 x 8 threads
+  for (int i = ty; i < 32; i += 8) {
+    const int r = r0 + i, e = e0 + tx;
+    tile[i][tx] = (r < d && e < E) ? W_r[(size_t)r * E + e] : 0.f;
+  }
+  __syncthreads();
+  const size_t n = (size_t)Ep * d;
+  for (int i = ty; i < 32; i += 8) {
+    const int e = e0 + i, r = r0 + tx;
+    if (e >= Ep || r >= d) continue;
+    const float w = tile[tx][i];
+    const uint32_t hi = pack_bf16(w, 0.f) & 0xFFFFu;
+    const float r1 = w - bf16_lo(hi);
+    const uint32_t mid = pack_bf16(r1, 0.f) & 0xFFFFu;
+    const float r2 = r1 - bf16_lo(mid);
+    const uint32_t lo = pack_bf16(r2, 0.f) & 0xFFFFu;
+    const size_t o = (size_t)e * d + r;
+    wr3[o] = (uint16_t)hi;
+    wr3[n + o] = (uint16_t)mid;
+    wr3[2 * n + o] = (uint16_t)lo;
+  }
+}
+
 // dst[r][c] = bf16(src[r][c]) for c < cols, 0 for cols <= c < ld (rows of the tensor-core operands)
 __global__ void to_bf16_rows_kernel(const float* __restrict__ src, int rows, int cols, int ld,
                                     uint16_t* __restrict__ dst) {
@@ -444,6 +473,15 @@ cudaError_t launch_router_reduce(const Cfg& c, const Layout& L, const RouterBwdA
   prof_mark(kKRouterReduce, s, true);
   router_reduce_kernel<<<blocks, 256, 0, s>>>(a, c.d, c.E, L.nsplit_dwr, L.nblk_router);
   prof_mark(kKRouterReduce, s, false);
+  return cudaGetLastError();
+}
+
+bool router_on_tensor_cores(const Cfg& c) { return c.E >= 32 && c.E <= 128 && c.k <= 8; }
+bool router_bwd_on_tensor_cores(const Cfg& c) { return router_on_tensor_cores(c) && !c.renorm; }
+
+cudaError_t launch_split_wr(const float* W_r, int d, int E, int Ep, uint16_t* wr3, cudaStream_t s) {
+  const dim3 grid((d + 31) / 32, (Ep + 31) / 32);
+  split_wr_kernel<<<grid, 256, 0, s>>>(W_r, d, E, Ep, wr3);
   return cudaGetLastError();
 }
 

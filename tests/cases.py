@@ -20,6 +20,11 @@ CASES = {
     "gptoss_small": dict(T=600, d=192, E=16, k=4, f=192, S=0, renorm=0, cf=1.25, zipf=True),
     "single_expert": dict(T=100, d=64, E=1, k=1, f=64, S=0, renorm=0, cf=0.0, zipf=False),
     "k_equals_E": dict(T=130, d=128, E=4, k=4, f=128, S=1, renorm=1, cf=0.0, zipf=False),
+    # tensor-core router shapes: E not a multiple of 64 (padded logit columns), k = 8, a router
+    # bias, and d_model = 320 (five 64-wide K blocks: one full 256-wide K slice and a short one)
+    "router_e96_k8": dict(T=333, d=320, E=96, k=8, f=64, S=0, renorm=0, cf=0.0, zipf=True),
+    # tensor-core forward with renormalised gates (the backward then needs no logits)
+    "router_e64_renorm": dict(T=257, d=256, E=64, k=6, f=128, S=1, renorm=1, cf=0.0, zipf=False),
 }
 
 FAST = ["tiny", "ragged_mixtral", "deepseek_small", "qwen_small", "gptoss_small"]

@@ -63,9 +63,9 @@ def test_null_and_misaligned_pointers_rejected(lib):
     c = moe.config(T=64, d=128, f=256, E=8, k=2)
     s = None
     # null x
-    assert lib.moe_route(ctypes.byref(c), None, 0x10000, None, 0x20000, 0x30000, None, s) == 1
+    assert lib.moe_route(ctypes.byref(c), None, 0x10000, None, 0x20000, 0x30000, None, 0x40000, 1 << 30, s) == 1
     # misaligned W_r
-    assert lib.moe_route(ctypes.byref(c), 0x10000, 0x20004, None, 0x30000, 0x40000, None, s) == 1
+    assert lib.moe_route(ctypes.byref(c), 0x10000, 0x20004, None, 0x30000, 0x40000, None, 0x50000, 1 << 30, s) == 1
     # workspace pointer must be 256-byte aligned
     assert lib.moe_combine(ctypes.byref(c), 0x10000, 0x20000, 0x30000, 0x40010, 1 << 30, s) == 1
 

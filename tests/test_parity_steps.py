@@ -53,7 +53,9 @@ def test_route(moe, name):
     idx = torch.empty(T, k, dtype=torch.int32, device="cuda")
     gates = torch.empty(T, k, dtype=torch.float32, device="cuda")
     logits = torch.empty(T, E, dtype=torch.float32, device="cuda")
-    moe.moe_route(mc, x, W_r, b_r, idx, gates, logits)
+    buf = moe.Buffers.allocate(mc)
+    moe.moe_route(mc, x, W_r, b_r, idx, gates, logits, buf.ws)
+    assert moe.moe_check_error(buf.ws) == 0
     torch.cuda.synchronize()
     R = L.routing()
     lg = from_dev(logits).astype(np.float64)
