@@ -19,6 +19,7 @@ Prints one JSON line (rank 0):
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -100,8 +101,9 @@ def recorded_traffic(kernel: str, workload: str):
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons, sampled every 200 ms while running."""
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi clocks and throttle reasons, sampled every 50 ms; summary() keeps the samples
+    taken between mark_start() and mark_end() (the timed region)."""
+    Q = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -109,11 +111,18 @@ class ClockSampler:
         self.idx = gpu_index
         self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         self.proc = None
+        self.t0 = self.t1 = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.file, stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -145,11 +154,22 @@ class ClockSampler:
                 return float(v)
             except ValueError:
                 return None
+
+        def when(v):
+            try:
+                return datetime.datetime.strptime(v, "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                return None
+        if self.t0 is not None and self.t1 is not None:
+            inside = [r for r in rows if when(r[0]) is not None and self.t0 <= when(r[0]) <= self.t1]
+            if inside:
+                rows = inside
         sm = [num(r[1]) for r in rows if num(r[1]) is not None]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(rows[0][2]),
                 "reasons": reasons, "samples": len(rows),
+                "sm_mhz_min": min(sm) if sm else None,
                 "power_w_max": max((num(r[3]) or 0.0) for r in rows)}
 
 
@@ -288,11 +308,13 @@ def main():
         barrier()
         torch.cuda.synchronize()
         moe.moe_profile_enable(True)
+        clocks.mark_start()
         ev0.record(stream)
         for _ in range(args.steps):
             step()
         ev1.record(stream)
         torch.cuda.synchronize()
+        clocks.mark_end()
         barrier()
     prof = moe.moe_profile_read()
     moe.moe_profile_enable(False)

@@ -47,7 +47,7 @@
  * Expert-ordered ("permuted") rows.  moe_dispatch writes x_perm in a padded, expert-contiguous
  * layout with room for moe_perm_rows() rows:
  *   segment g (routed experts g < E first, then shared experts) starts at row P_g, a multiple of
- *   128; P_0 = 0, P_{g+1} = P_g + roundup(n_g, 128), where n_g = min(counts[g], C) for routed
+ *   256; P_0 = 0, P_{g+1} = P_g + roundup(n_g, 256), where n_g = min(counts[g], C) for routed
  *   experts and n_g = T for shared ones.  Rows P_g + n_g .. P_{g+1}-1 are zero padding.
  *   The kept assignment (t, j) of expert e with queue position q sits at row P_e + q; shared
  *   expert s sees token t at row P_{E+s} + t.

@@ -106,7 +106,7 @@ Layout make_layout(const Cfg& c) {
   L.ntf = (c.f + 127) / 128;
   L.ndg = 2 * L.ntf;
   // db partials: one per 32 tokens from the tensor-core backward, else one per SIMT router block
-  L.nblk_router = router_bwd_on_tensor_cores(c) ? 4 * ((c.T + kRowTile - 1) / kRowTile)
+  L.nblk_router = router_bwd_on_tensor_cores(c) ? 4 * ((c.T + kRouterTile - 1) / kRouterTile)
                                                 : (c.T + route_block_tokens(c.E) - 1) / route_block_tokens(c.E);
   // token splits of the dW_r tensor-core GEMM: about two tiles per SM, at least 512 tokens each
   const int mtiles = (c.d + 127) / 128;

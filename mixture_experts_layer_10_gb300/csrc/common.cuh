@@ -15,7 +15,8 @@ namespace moe {
 constexpr int kMaxE = 256;
 constexpr int kMaxS = 8;
 constexpr int kMaxG = kMaxE + kMaxS;       // routed + shared segments
-constexpr int kRowTile = 128;              // GEMM M tile; segments are padded to it
+constexpr int kRowTile = 256;              // CTA-pair GEMM M tile; segments are padded to it
+constexpr int kRouterTile = 128;           // tokens per router tensor-core tile
 constexpr int kScanChunk = 4096;           // assignments per dispatch-scan block
 constexpr int kScanThreads = 512;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;   // 2 s bound on any device wait
@@ -48,7 +49,7 @@ constexpr size_t kHdrResetBytes = 8;
 // Routing tables written by the last dispatch-scan block.
 struct Tables {
   int32_t G;                     // segments = E + S
-  int32_t n_mtiles;              // P_G / 128
+  int32_t n_mtiles;              // P_G / kRowTile
   int32_t total_rows;            // P_G
   int32_t total_pad;             // pad rows over all segments
   int32_t counts[kMaxE];         // raw demand per routed expert

@@ -6,7 +6,7 @@
 //   4096 assignments per expert (warp match + shared-memory running counts, so ranks follow the
 //   (t, j) order), publishes its per-expert aggregate, and finds its per-expert exclusive prefix
 //   with a decoupled look-back over the preceding blocks (bounded spin).  The last block to
-//   finish builds the routing tables: counts, capacity, exact offsets, 128-row padded segment
+//   finish builds the routing tables: counts, capacity, exact offsets, 256-row padded segment
 //   starts, pad-row prefix and the segment order by size.
 // dispatch_gather_kernel: token owner.  A warp reads each x (and dy) row once, 16 bytes per lane,
 //   and writes it to every kept slot's row (and every shared expert's row); then zeroes pad rows.

@@ -11,11 +11,16 @@
 //   warps 2..   epilogue (4 or 8 warps): tcgen05.ld of the accumulator (128 lanes = 128 rows),
 //               fused element-wise work, bf16 stores
 //
-// Rows are the dispatch's padded expert segments (multiples of 128), so every 128-row M tile
+// The six expert GEMMs run on CTA pairs (clusters of two): one 256 x 256 tile per pair, each CTA
+// loading its own 128 rows of A and its own 128-row half of B, and the even CTA issuing
+// tcgen05.mma.cta_group::2, which feeds both halves of B to both SMs.  Per FLOP this halves the
+// shared-memory traffic of B against one CTA doing a 128 x 256 tile, which otherwise saturates the
+// SM's shared-memory bandwidth (TMA writes plus tensor-core reads) before the tensor cores.
+// Rows are the dispatch's padded expert segments (multiples of 256), so every 256-row pair tile
 // belongs to one expert and the per-expert tile scheduler is a table walk done identically by
-// the three roles.  Every wait is bounded (MOE_ERR_TIMEOUT instead of a hang).
+// the three roles of both CTAs.  Every wait is bounded (MOE_ERR_TIMEOUT instead of a hang).
 //
-// Problems (BM = 128, BK = 64, operands bf16, accumulators fp32):
+// Problems (BK = 64, operands bf16, accumulators fp32; pair tiles M = 256 unless noted):
 //   FwdGateUp  H    = silu(X Wg^T) * (X Wu^T)              A=X K-major, B=[Wg;Wu] K-major, N=256
 //   FwdDown    O    = H Wd^T                               A=H K-major, B=Wd K-major,      N=256
 //   BwdDh      dh'  = dY Wd                                A K-major, B MN-major,      N=256
@@ -23,8 +28,10 @@
 //              dA = dh b silu'(a), dB = dh silu(a), Hg = g h                         N=256
 //   Wgrad      dWg = dA^T X, dWu = dB^T X, dWd = dY^T Hg   A and B MN-major, K = segment rows
 //   DgradX     dX   = dA Wg + dB Wu                        A K-major, B MN-major, K = 2 d_ff
-//   RouterDwr  dW_r partials = x^T dl over token splits    A and B MN-major, N = E padded to 64
-//   CombineBwd dx   = dl W_r^T + the token's rows of dX     A and B K-major, K = E padded to 64
+//   RouterDwr  dW_r partials = x^T dl over token splits    A and B MN-major, N = E padded to 64,
+//              one CTA, M = 128
+//   CombineBwd dx   = dl W_r^T + the token's rows of dX     A and B K-major, K = E padded to 64,
+//              one CTA, M = 128
 //   RouterLogits  l = x W_r with W_r in three bf16 parts; epilogue: softmax, top-k, or the
 //              router's dlogits                          A and B K-major, N = E padded to 64
 #include <algorithm>
@@ -42,7 +49,9 @@ constexpr int kBM = 128;
 constexpr int kBK = 64;
 constexpr uint32_t kTileA = kBM * kBK * 2;   // 16 KB: 128 rows x 64 bf16 (K-major)
 constexpr uint32_t kBox = 64 * kBK * 2;      // 8 KB: a 64 x 64 box (MN-major)
-constexpr int kChunkM = 32;                  // m-tiles per L2 reuse chunk of a segment
+constexpr int kPairM = 2 * kBM;              // rows of a CTA-pair tile (kRowTile)
+constexpr int kChunkM = 16;                  // pair m-tiles per L2 reuse chunk of a segment
+static_assert(kPairM == kRowTile, "segments are padded to the pair tile");
 
 struct Job {
   int seg, m0, n0, kiters, kbase, sub;
@@ -58,13 +67,14 @@ struct PolicyDefaults {
   // a stateful policy keeps per-lane epilogue state across the jobs of one CTA (epilogue_s)
   static constexpr bool kStateful = false;
   struct EpiState {};
+  static constexpr int kEpiBoxes = 0;   // TMA-store staging boxes per epilogue warp (pair kernel)
 };
 
 struct SegSmem {
   int G;
   int n_mtiles;
   int poff[kMaxG + 1];
-  int seg_order[kMaxG];
+  int16_t seg_order[kMaxG];
 };
 
 __device__ __forceinline__ void load_segs(SegSmem& s, const Tables* tb) {
@@ -74,23 +84,23 @@ __device__ __forceinline__ void load_segs(SegSmem& s, const Tables* tb) {
   }
   for (int i = threadIdx.x; i <= kMaxG; i += blockDim.x) {
     s.poff[i] = tb->poff[i];
-    if (i < kMaxG) s.seg_order[i] = tb->seg_order[i];
+    if (i < kMaxG) s.seg_order[i] = (int16_t)tb->seg_order[i];
   }
 }
 
-// Row-tiled problems: tile t -> (segment, m-tile, n-tile).  Segments in index order; inside a
-// segment, chunks of up to 32 m-tiles x all n-tiles with the m-tile fastest, so the CTAs working
-// at the same time share one operand panel of each kind in L2.
+// Row-tiled problems: tile t -> (segment, 256-row m-tile, n-tile).  Segments in index order;
+// inside a segment, chunks of up to 16 m-tiles x all n-tiles with the m-tile fastest, so the CTA
+// pairs working at the same time share one operand panel of each kind in L2.
 __device__ __forceinline__ Job row_job(const SegSmem& s, int t, int nt, int bn, int kiters) {
   const int mt_of_t = t / nt;
   int lo = 0, hi = s.G - 1;   // last segment whose first m-tile <= mt_of_t
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (s.poff[mid] / kBM <= mt_of_t) lo = mid; else hi = mid - 1;
+    if (s.poff[mid] / kPairM <= mt_of_t) lo = mid; else hi = mid - 1;
   }
   const int seg = lo;
-  const int mstart = s.poff[seg] / kBM;
-  const int mt = (s.poff[seg + 1] - s.poff[seg]) / kBM;
+  const int mstart = s.poff[seg] / kPairM;
+  const int mt = (s.poff[seg + 1] - s.poff[seg]) / kPairM;
   const int local = t - mstart * nt;
   const int c = local / (kChunkM * nt);
   const int base = c * kChunkM;
@@ -98,7 +108,7 @@ __device__ __forceinline__ Job row_job(const SegSmem& s, int t, int nt, int bn, 
   const int r = local - c * kChunkM * nt;
   Job j;
   j.seg = seg;
-  j.m0 = s.poff[seg] + (base + r % cm) * kBM;
+  j.m0 = s.poff[seg] + (base + r % cm) * kPairM;
   j.n0 = (r / cm) * bn;
   j.kiters = kiters;
   j.kbase = 0;
@@ -110,18 +120,98 @@ __device__ __forceinline__ Job row_job(const SegSmem& s, int t, int nt, int bn, 
 // Problem policies
 // ---------------------------------------------------------------------------------------------
 
-struct FwdGateUp : PolicyDefaults {
-  static constexpr int kId = kKGateUp;
-  static constexpr int kEpiWarps = 4;
-  static constexpr int kStages = 4;
-  static constexpr uint32_t kStageBytes = kTileA + 2 * kTileA;   // X tile + Wg tile + Wu tile
+// Hooks of the CTA-pair problems: per CTA a stage holds A (128 x 64) and half of B (128 x 64);
+// load() gets the pair's job, this CTA's rank and the even CTA's full barrier (cluster address).
+struct PairDefaults : PolicyDefaults {
+  static constexpr int kStages = 6;                 // 64-wide K blocks of storage
+  static constexpr int kSub = 1;                    // K blocks per pipeline slot (one barrier round)
+  static constexpr uint32_t kStageBytes = 2 * kTileA;   // one K block: A 128 x 64 + B half 128 x 64
   static constexpr int kAccCols = 256;
   static constexpr int kAccBufs = 2;
   static constexpr int kTmemCols = 512;
-  static constexpr uint32_t kIdesc = idesc_bf16(128, 256, false, false);
+  static constexpr uint32_t kIdesc = idesc_bf16(kPairM, 256, false, false);
+  static constexpr int kEpiBoxes = 2;
+};
+
+// Epilogue output goes through shared memory and TMA stores: each epilogue warp writes a [32 rows x
+// 32 bf16] box (its TMEM lane quarter x 32 columns, 2 KB) in the layout of a SWIZZLE_64B tensor map
+// -- 16-byte chunk q of row r at r * 64 + ((q ^ ((r >> 1) & 3)) * 16), so each 8-lane phase of a
+// chunk write hits distinct banks -- and lane 0 stores the box with one bulk tensor copy that
+// writes whole lines.  A thread's direct 16-byte stores would instead touch 32 rows per warp
+// instruction, with half-filled sectors, on the same L1 the operand loads pass through.
+constexpr uint32_t kEpiBox = 32 * 32 * 2;
+
+__device__ __forceinline__ void stage_box(uint8_t* box, int lane, const uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q)
+    *reinterpret_cast<uint4*>(box + lane * 64 + ((q ^ ((lane >> 1) & 3)) << 4)) =
+        make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+}
+
+// Box i of this warp's epilogue (i counts from 0 within one tile): the box used two stores ago is
+// free again once at most one bulk group is still reading.
+__device__ __forceinline__ uint8_t* claim_box(uint8_t* ebuf, int i, int lane) {
+  if (i >= 2) {
+    if (lane == 0) bulk_wait_read<1>();
+    __syncwarp();
+  }
+  return ebuf + (i & 1) * kEpiBox;
+}
+
+// After stage_box(): make the box visible to the TMA and store it at (x, y) [, z].
+__device__ __forceinline__ void store_box_2d(const CUtensorMap* map, const uint8_t* box, int lane, int x, int y) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_2d(map, box, x, y);
+    bulk_commit();
+  }
+}
+
+__device__ __forceinline__ void store_box_3d(const CUtensorMap* map, const uint8_t* box, int lane, int x, int y,
+                                             int z) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    tma_store_3d(map, box, x, y, z);
+    bulk_commit();
+  }
+}
+
+// Start of a tile's epilogue: every box of the previous tile has been read.
+__device__ __forceinline__ void epi_begin(int lane) {
+  if (lane == 0) bulk_wait_read<0>();
+  __syncwarp();
+}
+
+__device__ __forceinline__ void pack32(const uint32_t (&v)[32], uint32_t (&pk)[16]) {
+#pragma unroll
+  for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+}
+
+// K-major A and B: kk-th K=16 step of a 64-wide block
+__device__ __forceinline__ void mma_kk_kmajor(uint32_t sa, uint32_t dt, uint32_t idesc, int kit) {
+#pragma unroll
+  for (int kk = 0; kk < kBK / 16; ++kk)
+    umma_bf16_pair(dt, sdesc_kmajor(sa + kk * 32), sdesc_kmajor(sa + kTileA + kk * 32), idesc, (kit | kk) != 0);
+}
+
+// K-major A, MN-major B (two 64-wide boxes)
+__device__ __forceinline__ void mma_kk_bmn(uint32_t sa, uint32_t dt, uint32_t idesc, int kit) {
+#pragma unroll
+  for (int kk = 0; kk < kBK / 16; ++kk)
+    umma_bf16_pair(dt, sdesc_kmajor(sa + kk * 32), sdesc_mnmajor(sa + kTileA + kk * 2048, kBox), idesc,
+                   (kit | kk) != 0);
+}
+
+// H = silu(X Wg^T) * (X Wu^T).  B = [Wg rows n0..n0+127; Wu rows n0..n0+127]: the even CTA loads
+// the Wg half and the odd CTA the Wu half, so TMEM columns 0-127 hold the gate and 128-255 the up
+// projection of the same 128 hidden units.
+struct FwdGateUp : PairDefaults {
+  static constexpr int kId = kKGateUp;
+  static constexpr int kEpiWarps = 4;
   struct Params {
-    CUtensorMap tmX, tmWg, tmWu;
-    uint16_t* H;
+    CUtensorMap tmX, tmWg, tmWu, tmH;
     int f, d, nt;
     Hdr* hdr;
     const Tables* tabs;
@@ -133,19 +223,17 @@ struct FwdGateUp : PolicyDefaults {
   __device__ static void prefetch(const Params& p) {
     tma_prefetch(&p.tmX); tma_prefetch(&p.tmWg); tma_prefetch(&p.tmWu);
   }
-  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint64_t* bar) {
-    tma_load_2d(st, &p.tmX, bar, kit * kBK, j.m0);
-    tma_load_3d(st + kTileA, &p.tmWg, bar, kit * kBK, j.n0, j.seg);
-    tma_load_3d(st + 2 * kTileA, &p.tmWu, bar, kit * kBK, j.n0, j.seg);
+  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint32_t cbar, int rank) {
+    tma_load_2d_pair(st, &p.tmX, cbar, kit * kBK, j.m0 + kBM * rank);
+    tma_load_3d_pair(st + kTileA, rank ? &p.tmWu : &p.tmWg, cbar, kit * kBK, j.n0, j.seg);
   }
   __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
-#pragma unroll
-    for (int kk = 0; kk < kBK / 16; ++kk)
-      umma_bf16(dt, sdesc_kmajor(sa + kk * 32), sdesc_kmajor(sa + kTileA + kk * 32), kIdesc,
-                (kit | kk) != 0);
+    mma_kk_kmajor(sa, dt, kIdesc, kit);
   }
-  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int, int) {
-    uint16_t* out = p.H + (size_t)(j.m0 + row) * p.f + j.n0;
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int, int, uint8_t* ebuf) {
+    const int lane = row & 31;
+    const int y = j.m0 + (row & ~31);
+    epi_begin(lane);
 #pragma unroll 1
     for (int c = 0; c < 128; c += 32) {
       if (j.n0 + c >= p.f) break;
@@ -161,17 +249,19 @@ struct FwdGateUp : PolicyDefaults {
         const float h1 = a1 / (1.f + __expf(-a1)) * __uint_as_float(ub[2 * i + 1]);
         pk[i] = pack_bf16(h0, h1);
       }
-      uint4* dst = reinterpret_cast<uint4*>(out + c);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      uint8_t* box = claim_box(ebuf, c / 32, lane);
+      stage_box(box, lane, pk);
+      store_box_2d(&p.tmH, box, lane, j.n0 + c, y);
     }
   }
   __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
 };
 
-// Shared by FwdDown and DgradX: fp32 accumulator [128 x 256] -> bf16 rows of width `ncols`.
-__device__ __forceinline__ void store_acc_rows(uint16_t* base, int ld, int n0, int ncols,
-                                               uint32_t ta) {
+// Shared by FwdDown, BwdDh and DgradX: this warp's 32 rows of the fp32 accumulator [128 x 256] ->
+// bf16 boxes of the output [rows, ncols] at row y (the warp's first row) and columns n0 + c.
+__device__ __forceinline__ void store_acc_boxes(const CUtensorMap* map, int y, int n0, int ncols, uint32_t ta,
+                                                int lane, uint8_t* ebuf) {
+  epi_begin(lane);
 #pragma unroll 1
   for (int c = 0; c < 256; c += 32) {
     if (n0 + c >= ncols) break;
@@ -179,27 +269,19 @@ __device__ __forceinline__ void store_acc_rows(uint16_t* base, int ld, int n0, i
     tmem_ld32(ta + c, v);
     tmem_ld_wait();
     uint32_t pk[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-    uint4* dst = reinterpret_cast<uint4*>(base + n0 + c);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+    pack32(v, pk);
+    uint8_t* box = claim_box(ebuf, c / 32, lane);
+    stage_box(box, lane, pk);
+    store_box_2d(map, box, lane, n0 + c, y);
   }
-  (void)ld;
 }
 
-struct FwdDown : PolicyDefaults {
+// O = H Wd^T: N = 256 columns of d_model, each CTA loading 128 rows of Wd[e].
+struct FwdDown : PairDefaults {
   static constexpr int kId = kKDown;
   static constexpr int kEpiWarps = 4;
-  static constexpr int kStages = 4;
-  static constexpr uint32_t kStageBytes = kTileA + 2 * kTileA;   // H tile + Wd tile (256 rows)
-  static constexpr int kAccCols = 256;
-  static constexpr int kAccBufs = 2;
-  static constexpr int kTmemCols = 512;
-  static constexpr uint32_t kIdesc = idesc_bf16(128, 256, false, false);
   struct Params {
-    CUtensorMap tmH, tmWd;
-    uint16_t* O;
+    CUtensorMap tmH, tmWd, tmO;
     int f, d, nt;
     Hdr* hdr;
     const Tables* tabs;
@@ -209,37 +291,28 @@ struct FwdDown : PolicyDefaults {
     return row_job(s, t, p.nt, 256, p.f / kBK);
   }
   __device__ static void prefetch(const Params& p) { tma_prefetch(&p.tmH); tma_prefetch(&p.tmWd); }
-  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint64_t* bar) {
-    tma_load_2d(st, &p.tmH, bar, kit * kBK, j.m0);
-    tma_load_3d(st + kTileA, &p.tmWd, bar, kit * kBK, j.n0, j.seg);
+  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint32_t cbar, int rank) {
+    tma_load_2d_pair(st, &p.tmH, cbar, kit * kBK, j.m0 + kBM * rank);
+    tma_load_3d_pair(st + kTileA, &p.tmWd, cbar, kit * kBK, j.n0 + kBM * rank, j.seg);
   }
   __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
-#pragma unroll
-    for (int kk = 0; kk < kBK / 16; ++kk)
-      umma_bf16(dt, sdesc_kmajor(sa + kk * 32), sdesc_kmajor(sa + kTileA + kk * 32), kIdesc,
-                (kit | kk) != 0);
+    mma_kk_kmajor(sa, dt, kIdesc, kit);
   }
-  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int, int) {
-    store_acc_rows(p.O + (size_t)(j.m0 + row) * p.d, p.d, j.n0, p.d, ta);
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int, int, uint8_t* ebuf) {
+    store_acc_boxes(&p.tmO, j.m0 + (row & ~31), j.n0, p.d, ta, row & 31, ebuf);
   }
   __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
 };
 
-// dh' = dY W_d for every row tile: M = rows, N = 256 columns of d_ff, K = d_model.  W_d[e] is
-// [d_model, d_ff], so it is the MN-major B operand (four 64-wide boxes per stage).  dh' is stored
-// in bf16 for the SwiGLU backward below.
-struct BwdDh : PolicyDefaults {
+// dh' = dY W_d for every row tile: N = 256 columns of d_ff, K = d_model.  W_d[e] is
+// [d_model, d_ff], so it is the MN-major B operand (two 64-wide boxes per CTA and stage).  dh' is
+// stored in bf16 for the SwiGLU backward below.
+struct BwdDh : PairDefaults {
   static constexpr int kId = kKBwdDh;
   static constexpr int kEpiWarps = 4;
-  static constexpr int kStages = 4;
-  static constexpr uint32_t kStageBytes = kTileA + 4 * kBox;   // dY tile + Wd slice (4 MN boxes)
-  static constexpr int kAccCols = 256;
-  static constexpr int kAccBufs = 2;
-  static constexpr int kTmemCols = 512;
-  static constexpr uint32_t kIdesc = idesc_bf16(128, 256, false, true);
+  static constexpr uint32_t kIdesc = idesc_bf16(kPairM, 256, false, true);
   struct Params {
-    CUtensorMap tmDY, tmWdT;
-    uint16_t* DH;
+    CUtensorMap tmDY, tmWdT, tmDH;
     int f, d, nt;
     Hdr* hdr;
     const Tables* tabs;
@@ -249,20 +322,17 @@ struct BwdDh : PolicyDefaults {
     return row_job(s, t, p.nt, 256, p.d / kBK);
   }
   __device__ static void prefetch(const Params& p) { tma_prefetch(&p.tmDY); tma_prefetch(&p.tmWdT); }
-  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint64_t* bar) {
-    tma_load_2d(st, &p.tmDY, bar, kit * kBK, j.m0);
+  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint32_t cbar, int rank) {
+    tma_load_2d_pair(st, &p.tmDY, cbar, kit * kBK, j.m0 + kBM * rank);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      tma_load_3d(st + kTileA + i * kBox, &p.tmWdT, bar, j.n0 + 64 * i, kit * kBK, j.seg);
+    for (int i = 0; i < 2; ++i)
+      tma_load_3d_pair(st + kTileA + i * kBox, &p.tmWdT, cbar, j.n0 + kBM * rank + 64 * i, kit * kBK, j.seg);
   }
   __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
-#pragma unroll
-    for (int kk = 0; kk < kBK / 16; ++kk)
-      umma_bf16(dt, sdesc_kmajor(sa + kk * 32), sdesc_mnmajor(sa + kTileA + kk * 2048, kBox), kIdesc,
-                (kit | kk) != 0);
+    mma_kk_bmn(sa, dt, kIdesc, kit);
   }
-  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int, int) {
-    store_acc_rows(p.DH + (size_t)(j.m0 + row) * p.f, p.f, j.n0, p.f, ta);
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int, int, uint8_t* ebuf) {
+    store_acc_boxes(&p.tmDH, j.m0 + (row & ~31), j.n0, p.f, ta, row & 31, ebuf);
   }
   __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
 };
@@ -271,20 +341,15 @@ struct BwdDh : PolicyDefaults {
 // SwiGLU backward in its epilogue, which reads this tile's dh' written by BwdDh:
 //   h = silu(a) b, dg += dh'.h, dh = g dh', dA = dh b silu'(a), dB = dh silu(a), Hg = g h.
 // Eight epilogue warps: two per TMEM lane quarter, each owning 64 of the 128 columns.
-struct BwdFused : PolicyDefaults {
+struct BwdFused : PairDefaults {
   static constexpr int kId = kKBwdFused;
   static constexpr int kEpiWarps = 8;
-  static constexpr int kStages = 4;
-  static constexpr uint32_t kStageBytes = 3 * kTileA;   // X tile + [Wg;Wu] (256 rows)
-  static constexpr int kAccCols = 256;
-  static constexpr int kAccBufs = 2;
-  static constexpr int kTmemCols = 512;
-  static constexpr uint32_t kIdesc = idesc_bf16(128, 256, false, false);
+  static constexpr int kStages = 5;
+  static constexpr int kEpiBoxes = 3;   // dA, dB, Hg
   struct Params {
-    CUtensorMap tmX, tmWg, tmWu;
+    CUtensorMap tmX, tmWg, tmWu, tmDA, tmDB, tmHg;
     const uint16_t* DH;
     const float* gate_of_prow;
-    uint16_t *dA, *dB, *Hg;
     float* dg_part;
     int f, d, nt, ndg;
     Hdr* hdr;
@@ -297,18 +362,17 @@ struct BwdFused : PolicyDefaults {
   __device__ static void prefetch(const Params& p) {
     tma_prefetch(&p.tmX); tma_prefetch(&p.tmWg); tma_prefetch(&p.tmWu);
   }
-  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint64_t* bar) {
-    tma_load_2d(st, &p.tmX, bar, kit * kBK, j.m0);
-    tma_load_3d(st + kTileA, &p.tmWg, bar, kit * kBK, j.n0, j.seg);
-    tma_load_3d(st + 2 * kTileA, &p.tmWu, bar, kit * kBK, j.n0, j.seg);
+  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint32_t cbar, int rank) {
+    tma_load_2d_pair(st, &p.tmX, cbar, kit * kBK, j.m0 + kBM * rank);
+    tma_load_3d_pair(st + kTileA, rank ? &p.tmWu : &p.tmWg, cbar, kit * kBK, j.n0, j.seg);
   }
   __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
-#pragma unroll
-    for (int kk = 0; kk < kBK / 16; ++kk)
-      umma_bf16(dt, sdesc_kmajor(sa + kk * 32), sdesc_kmajor(sa + kTileA + kk * 32), kIdesc,
-                (kit | kk) != 0);
+    mma_kk_kmajor(sa, dt, kIdesc, kit);
   }
-  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int part, int) {
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int part, int,
+                                  uint8_t* ebuf) {
+    const int lane = row & 31;
+    const int y = j.m0 + (row & ~31);
     const size_t r = (size_t)(j.m0 + row);
     const float g = p.gate_of_prow[r];
     float dg = 0.f;
@@ -347,14 +411,18 @@ struct BwdFused : PolicyDefaults {
         pb[i] = pack_bf16(o_db[0], o_db[1]);
         ph[i] = pack_bf16(o_h[0], o_h[1]);
       }
-      uint4* da = reinterpret_cast<uint4*>(p.dA + r * p.f + j.n0 + c);
-      uint4* db = reinterpret_cast<uint4*>(p.dB + r * p.f + j.n0 + c);
-      uint4* hg = reinterpret_cast<uint4*>(p.Hg + r * p.f + j.n0 + c);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        da[q] = make_uint4(pa[4 * q], pa[4 * q + 1], pa[4 * q + 2], pa[4 * q + 3]);
-        db[q] = make_uint4(pb[4 * q], pb[4 * q + 1], pb[4 * q + 2], pb[4 * q + 3]);
-        hg[q] = make_uint4(ph[4 * q], ph[4 * q + 1], ph[4 * q + 2], ph[4 * q + 3]);
+      if (lane == 0) bulk_wait_read<0>();   // the previous boxes have been read
+      __syncwarp();
+      stage_box(ebuf, lane, pa);
+      stage_box(ebuf + kEpiBox, lane, pb);
+      stage_box(ebuf + 2 * kEpiBox, lane, ph);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&p.tmDA, ebuf, j.n0 + c, y);
+        tma_store_2d(&p.tmDB, ebuf + kEpiBox, j.n0 + c, y);
+        tma_store_2d(&p.tmHg, ebuf + 2 * kEpiBox, j.n0 + c, y);
+        bulk_commit();
       }
     }
     p.dg_part[r * p.ndg + (j.n0 / 128) * 2 + part] = dg;
@@ -362,18 +430,14 @@ struct BwdFused : PolicyDefaults {
   __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
 };
 
-struct DgradX : PolicyDefaults {
+// dX = dA Wg + dB Wu: K = 2 d_ff (the dA blocks, then the dB blocks), N = 256 columns of d_model;
+// Wg[e], Wu[e] are [d_ff, d_model], so B is MN-major (two 64-wide boxes per CTA and stage).
+struct DgradX : PairDefaults {
   static constexpr int kId = kKDgradX;
   static constexpr int kEpiWarps = 4;
-  static constexpr int kStages = 4;
-  static constexpr uint32_t kStageBytes = kTileA + 4 * kBox;   // dA/dB tile + 4 MN boxes of W
-  static constexpr int kAccCols = 256;
-  static constexpr int kAccBufs = 2;
-  static constexpr int kTmemCols = 512;
-  static constexpr uint32_t kIdesc = idesc_bf16(128, 256, false, true);
+  static constexpr uint32_t kIdesc = idesc_bf16(kPairM, 256, false, true);
   struct Params {
-    CUtensorMap tmDA, tmDB, tmWgT, tmWuT;
-    uint16_t* dX;
+    CUtensorMap tmDA, tmDB, tmWgT, tmWuT, tmDX;
     int f, d, nt;
     Hdr* hdr;
     const Tables* tabs;
@@ -385,41 +449,38 @@ struct DgradX : PolicyDefaults {
   __device__ static void prefetch(const Params& p) {
     tma_prefetch(&p.tmDA); tma_prefetch(&p.tmDB); tma_prefetch(&p.tmWgT); tma_prefetch(&p.tmWuT);
   }
-  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint64_t* bar) {
+  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint32_t cbar, int rank) {
     const int nk = p.f / kBK;
     const bool up = kit >= nk;
     const int k0 = (up ? kit - nk : kit) * kBK;
-    tma_load_2d(st, up ? &p.tmDB : &p.tmDA, bar, k0, j.m0);
+    tma_load_2d_pair(st, up ? &p.tmDB : &p.tmDA, cbar, k0, j.m0 + kBM * rank);
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      tma_load_3d(st + kTileA + i * kBox, up ? &p.tmWuT : &p.tmWgT, bar, j.n0 + 64 * i, k0, j.seg);
+    for (int i = 0; i < 2; ++i)
+      tma_load_3d_pair(st + kTileA + i * kBox, up ? &p.tmWuT : &p.tmWgT, cbar, j.n0 + kBM * rank + 64 * i, k0,
+                       j.seg);
   }
   __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
-#pragma unroll
-    for (int kk = 0; kk < kBK / 16; ++kk)
-      umma_bf16(dt, sdesc_kmajor(sa + kk * 32), sdesc_mnmajor(sa + kTileA + kk * 2048, kBox), kIdesc,
-                (kit | kk) != 0);
+    mma_kk_bmn(sa, dt, kIdesc, kit);
   }
-  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int, int) {
-    store_acc_rows(p.dX + (size_t)(j.m0 + row) * p.d, p.d, j.n0, p.d, ta);
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int, int, uint8_t* ebuf) {
+    store_acc_boxes(&p.tmDX, j.m0 + (row & ~31), j.n0, p.d, ta, row & 31, ebuf);
   }
   __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
 };
 
-struct Wgrad : PolicyDefaults {
+// Weight gradients, K = the expert's rows: dWg = dA^T X and dWu = dB^T X (M = d_ff, N = d_model),
+// dWd = dY^T Hg (M = d_model, N = d_ff).  A and B are row-major activations read MN-major, two
+// 64-wide boxes each per CTA and stage.  Tiles go expert by expert, largest first.
+struct Wgrad : PairDefaults {
   static constexpr int kId = kKWgrad;
   static constexpr int kEpiWarps = 8;
-  static constexpr int kStages = 4;
-  static constexpr uint32_t kStageBytes = 2 * kBox + 4 * kBox;   // A: 128 MN; B: 256 MN
-  static constexpr int kAccCols = 256;
-  static constexpr int kAccBufs = 2;
-  static constexpr int kTmemCols = 512;
-  static constexpr uint32_t kIdesc = idesc_bf16(128, 256, true, true);
+  static constexpr uint32_t kIdesc = idesc_bf16(kPairM, 256, true, true);
   struct Params {
     CUtensorMap tmDA, tmDB, tmX, tmDY, tmHg;   // all [rows, width] with 64 x 64 boxes
+    CUtensorMap tmdWg, tmdWu, tmdWd;           // [G, M, ncols] with 32 x 32 boxes (stores)
     uint16_t *dWg, *dWu, *dWd;
     int f, d;
-    int mt_f, nt_d, mt_d, nt_f, tps;           // tiles: dWg/dWu (mt_f x nt_d), dWd (mt_d x nt_f)
+    int mt_f, nt_d, mt_d, nt_f, tps;           // pair tiles: dWg/dWu (mt_f x nt_d), dWd (mt_d x nt_f)
     Hdr* hdr;
     const Tables* tabs;
   };
@@ -435,12 +496,12 @@ struct Wgrad : PolicyDefaults {
     if (r < 2 * gu) {
       j.sub = r / gu;
       r -= j.sub * gu;
-      j.m0 = (r / p.nt_d) * kBM;
+      j.m0 = (r / p.nt_d) * kPairM;
       j.n0 = (r % p.nt_d) * 256;
     } else {
       r -= 2 * gu;
       j.sub = 2;
-      j.m0 = (r / p.nt_f) * kBM;
+      j.m0 = (r / p.nt_f) * kPairM;
       j.n0 = (r % p.nt_f) * 256;
     }
     return j;
@@ -449,20 +510,21 @@ struct Wgrad : PolicyDefaults {
     tma_prefetch(&p.tmDA); tma_prefetch(&p.tmDB); tma_prefetch(&p.tmX); tma_prefetch(&p.tmDY);
     tma_prefetch(&p.tmHg);
   }
-  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint64_t* bar) {
+  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint32_t cbar, int rank) {
     const int row = j.kbase + kit * kBK;
     const CUtensorMap* ta = j.sub == 0 ? &p.tmDA : (j.sub == 1 ? &p.tmDB : &p.tmDY);
     const CUtensorMap* tb = j.sub == 2 ? &p.tmHg : &p.tmX;
-    tma_load_2d(st, ta, bar, j.m0, row);
-    tma_load_2d(st + kBox, ta, bar, j.m0 + 64, row);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) tma_load_2d(st + (2 + i) * kBox, tb, bar, j.n0 + 64 * i, row);
+    for (int i = 0; i < 2; ++i) {
+      tma_load_2d_pair(st + i * kBox, ta, cbar, j.m0 + kBM * rank + 64 * i, row);
+      tma_load_2d_pair(st + (2 + i) * kBox, tb, cbar, j.n0 + kBM * rank + 64 * i, row);
+    }
   }
   __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
 #pragma unroll
     for (int kk = 0; kk < kBK / 16; ++kk)
-      umma_bf16(dt, sdesc_mnmajor(sa + kk * 2048, kBox), sdesc_mnmajor(sa + 2 * kBox + kk * 2048, kBox),
-                kIdesc, (kit | kk) != 0);
+      umma_bf16_pair(dt, sdesc_mnmajor(sa + kk * 2048, kBox), sdesc_mnmajor(sa + 2 * kBox + kk * 2048, kBox),
+                     kIdesc, (kit | kk) != 0);
   }
   __device__ static uint16_t* out_row(const Params& p, const Job& j, int row, int& ncols, bool& ok) {
     const int M = j.sub == 2 ? p.d : p.f;
@@ -472,24 +534,29 @@ struct Wgrad : PolicyDefaults {
     uint16_t* W = j.sub == 0 ? p.dWg : (j.sub == 1 ? p.dWu : p.dWd);
     return W + ((size_t)j.seg * M + (ok ? m : 0)) * ncols;
   }
-  // Eight epilogue warps: the two warps of a TMEM lane quarter take 128 columns each.
-  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int part, int) {
-    int ncols;
-    bool ok;
-    uint16_t* base = out_row(p, j, row, ncols, ok);
+  // Eight epilogue warps: the two warps of a TMEM lane quarter take 128 columns each.  A warp whose
+  // 32 rows all lie past M (the last pair tile of a d_ff or d_model not a multiple of 256) stores
+  // nothing; boxes that reach past M are clipped by the tensor map.
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int part, int,
+                                  uint8_t* ebuf) {
+    const int lane = row & 31;
+    const int M = j.sub == 2 ? p.d : p.f;
+    const int ncols = j.sub == 2 ? p.f : p.d;
+    const int y = j.m0 + (row & ~31);
+    if (y >= M) return;
+    const CUtensorMap* map = j.sub == 0 ? &p.tmdWg : (j.sub == 1 ? &p.tmdWu : &p.tmdWd);
+    epi_begin(lane);
 #pragma unroll 1
     for (int c = part * 128; c < part * 128 + 128; c += 32) {
       if (j.n0 + c >= ncols) break;
       uint32_t v[32];
       tmem_ld32(ta + c, v);
       tmem_ld_wait();
-      if (!ok) continue;
       uint32_t pk[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) pk[i] = pack_bf16(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-      uint4* dst = reinterpret_cast<uint4*>(base + j.n0 + c);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) dst[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+      pack32(v, pk);
+      uint8_t* box = claim_box(ebuf, (c - part * 128) / 32, lane);
+      stage_box(box, lane, pk);
+      store_box_3d(map, box, lane, j.n0 + c, y, j.seg);
     }
   }
   // An expert that received no rows has a zero gradient.
@@ -908,8 +975,13 @@ struct RouterLogits : PolicyDefaults {
 // ---------------------------------------------------------------------------------------------
 
 template <class P>
+constexpr size_t epi_bytes() {
+  return (size_t)P::kEpiWarps * P::kEpiBoxes * kEpiBox;
+}
+
+template <class P>
 constexpr size_t smem_bytes() {
-  return 1024 + (size_t)P::kStages * P::kStageBytes + 256 + sizeof(SegSmem);
+  return 1024 + (size_t)P::kStages * P::kStageBytes + epi_bytes<P>() + 256 + sizeof(SegSmem);
 }
 
 template <class P>
@@ -1066,6 +1138,188 @@ __global__ void __launch_bounds__(threads_of<P>(), 1) gemm_kernel(const __grid_c
   }
 }
 
+// The CTA-pair version: a cluster of two CTAs shares every tile.  Both CTAs run the producer and
+// the epilogue for their own 128 rows; only the even CTA's MMA thread issues (cta_group::2):
+//   full[s]    even CTA: one expect_tx arrival, completed by both CTAs' TMA bytes
+//   empty[s]   even CTA: freed by a commit of the MMA thread once the slot's MMAs are done; odd
+//              CTA: freed by the even CTA's producer, which forwards that completion (a relaxed
+//              remote arrival, after its own loads) when it refills the slot.  One commit per
+//              slot: a second commit per 64-wide K block cost 6-8% of the MMA rate (measured in
+//              SM cycles), while slots of two K blocks, with half the slots, lost more to the
+//              shallower pipeline.
+//   tfull[a]   each CTA: the finished accumulator, committed by the MMA thread to both CTAs
+//   tempty[a]  even CTA: released by the epilogue warps of both CTAs (remote arrivals)
+// Both CTAs walk the same tile sequence (pair id, stride = number of pairs).  Every wait is
+// bounded; whatever happens, both CTAs meet at the final cluster barrier before TMEM is freed, so
+// neither exits while the other may still touch its shared memory.
+template <class P>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<P>(), 1)
+    gemm_pair_kernel(const __grid_constant__ typename P::Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stages = smem;
+  uint8_t* epi = smem + (size_t)P::kStages * P::kStageBytes;   // 1024-aligned staging boxes
+  uint64_t* full = reinterpret_cast<uint64_t*>(epi + epi_bytes<P>());
+  uint64_t* empty = full + P::kStages;
+  uint64_t* tfull = empty + P::kStages;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  SegSmem& segs = *reinterpret_cast<SegSmem*>(epi + epi_bytes<P>() + 256);
+
+  constexpr int kSub = P::kSub;
+  constexpr int kSlots = P::kStages / kSub;
+  constexpr size_t kSlotBytes = (size_t)kSub * P::kStageBytes;
+  static_assert(P::kStages % kSub == 0, "whole slots");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rank = (int)cluster_rank();
+  const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+  load_segs(segs, p.tabs);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < P::kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 2 * P::kEpiWarps);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+    P::prefetch(p);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, P::kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();   // both CTAs' barriers exist before any remote arrival
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int ntiles = P::num_tiles(p, segs);
+  const uint64_t limit = wait_limit_ns(p.hdr);
+
+  if (warp == 0) {
+    if (lane == 0) {
+      int slot = 0;
+      uint32_t phase = 0;
+      int uses = 0;   // slots filled so far; from kSlots on, every fill follows a completed use
+      for (int t = pair; t < ntiles && !*abort_flag; t += npairs) {
+        const Job j = P::job(p, segs, t);
+        for (int k0 = 0; k0 < j.kiters; k0 += kSub) {
+          if (!mbar_wait(&empty[slot], phase ^ 1, limit, abort_flag)) {
+            record_error(p.hdr, MOE_ERR_TIMEOUT, kSiteGemmProducer);
+            *abort_flag = 1;
+            break;
+          }
+          const int nsb = min(kSub, j.kiters - k0);
+          if (rank == 0) {
+            uint32_t tx = 0;
+            for (int sb = 0; sb < nsb; ++sb) tx += P::tx_bytes(j, k0 + sb, P::kStageBytes);
+            mbar_arrive_expect_tx(&full[slot], 2 * tx);
+          }
+          uint8_t* st = stages + (size_t)slot * kSlotBytes;
+          for (int sb = 0; sb < nsb; ++sb)
+            P::load(p, j, k0 + sb, st + (size_t)sb * P::kStageBytes, cluster_addr(&full[slot], 0), rank);
+          if (rank == 0 && uses >= kSlots) mbar_arrive_cluster_relaxed(cluster_addr(&empty[slot], 1));
+          ++uses;
+          if (++slot == kSlots) {
+            slot = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      int slot = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      int seq = 0;
+      for (int t = pair; t < ntiles && !*abort_flag; t += npairs) {
+        const Job j = P::job(p, segs, t);
+        if (j.kiters == 0) continue;
+        const uint32_t dt = tmem_base + (uint32_t)(acc * P::kAccCols);
+        // both CTAs' epilogues must have released this accumulator
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, limit, abort_flag)) {
+          record_error(p.hdr, MOE_ERR_TIMEOUT, kSiteGemmMma);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        bool ok = true;
+        for (int k0 = 0; k0 < j.kiters; k0 += kSub) {
+          if (!mbar_wait(&full[slot], phase, limit, abort_flag)) {
+            record_error(p.hdr, MOE_ERR_TIMEOUT, kSiteGemmMma);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const int nsb = min(kSub, j.kiters - k0);
+          const uint32_t sa = smem_u32(stages + (size_t)slot * kSlotBytes);
+          for (int sb = 0; sb < nsb; ++sb) P::mma(j, k0 + sb, sa + sb * P::kStageBytes, dt, seq);
+          umma_commit_pair(smem_u32(&empty[slot]));
+          if (++slot == kSlots) {
+            slot = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair(cluster_addr(&tfull[acc], 0));
+        umma_commit_pair(cluster_addr(&tfull[acc], 1));
+        ++seq;
+        if (++acc == P::kAccBufs) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+    }
+  } else {
+    const int q = warp & 3;            // TMEM lane quarter this warp may access
+    const int part = (warp - 2) >> 2;  // column share when two warps serve one quarter
+    const int row = q * 32 + lane;
+    uint8_t* ebuf = epi + (size_t)(warp - 2) * P::kEpiBoxes * kEpiBox;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    int seq = 0;
+    for (int t = pair; t < ntiles; t += npairs) {
+      Job j = P::job(p, segs, t);
+      j.m0 += kBM * rank;   // this CTA's 128 rows of the pair tile
+      if (j.kiters == 0) {
+        if (part == 0) P::epilogue_zero(p, j, row, part);
+        continue;
+      }
+      if (!mbar_wait(&tfull[acc], acc_phase, limit, abort_flag)) {
+        record_error(p.hdr, MOE_ERR_TIMEOUT, kSiteGemmEpilogue);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after();
+      P::epilogue(p, j, tmem_base + (uint32_t)(acc * P::kAccCols) + ((uint32_t)(q * 32) << 16), row, part,
+                  seq, ebuf);
+      ++seq;
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(cluster_addr(&tempty[acc], 0));
+      if (++acc == P::kAccBufs) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+    if (lane == 0) bulk_wait_all();   // this warp's output stores have landed
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, P::kTmemCols);
+  }
+}
+
 // ---------------------------------------------------------------------------------------------
 // Host side: tensor maps and launches
 // ---------------------------------------------------------------------------------------------
@@ -1129,57 +1383,81 @@ cudaError_t launch(const typename P::Params& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Pairs: as many clusters as fit at once (two CTAs each), one persistent pair per cluster slot.
+template <class P>
+cudaError_t launch_pair(const typename P::Params& p, cudaStream_t s) {
+  constexpr size_t smem = smem_bytes<P>();
+  static_assert(smem <= 232448, "shared memory per block");
+  static int grid = 0;   // per problem type and process (all devices here are alike)
+  cudaError_t e = cudaFuncSetAttribute(gemm_pair_kernel<P>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  if (grid == 0) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (num_sms() / 2), 1, 1);
+    cfg.blockDim = dim3(threads_of<P>(), 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    int nclusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&nclusters, gemm_pair_kernel<P>, &cfg) != cudaSuccess || nclusters <= 0) {
+      (void)cudaGetLastError();
+      nclusters = num_sms() / 2;
+    }
+    grid = 2 * std::min(nclusters, num_sms() / 2);
+  }
+  prof_mark(P::kId, s, true);
+  gemm_pair_kernel<P><<<grid, threads_of<P>(), smem, s>>>(p);
+  prof_mark(P::kId, s, false);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t launch_ffn_fwd(const Cfg& c, const Layout& L, const FfnFwdArgs& a, cudaStream_t s) {
   const uint64_t rows = (uint64_t)L.rows;
   FwdGateUp::Params p1{};
   if (!map_2d(&p1.tmX, a.x_perm, c.d, rows, 64, 128) ||
-      !map_3d(&p1.tmWg, a.Wg, c.d, c.f, c.G, 64, 128) || !map_3d(&p1.tmWu, a.Wu, c.d, c.f, c.G, 64, 128))
+      !map_3d(&p1.tmWg, a.Wg, c.d, c.f, c.G, 64, 128) || !map_3d(&p1.tmWu, a.Wu, c.d, c.f, c.G, 64, 128) ||
+      !map_2d(&p1.tmH, a.h, c.f, rows, 32, 32))
     return cudaErrorInvalidValue;
-  p1.H = a.h;
   p1.f = c.f;
   p1.d = c.d;
   p1.nt = (c.f + 127) / 128;
   p1.hdr = a.hdr;
   p1.tabs = a.tabs;
-  cudaError_t e = launch<FwdGateUp>(p1, s);
+  cudaError_t e = launch_pair<FwdGateUp>(p1, s);
   if (e != cudaSuccess) return e;
   FwdDown::Params p2{};
-  if (!map_2d(&p2.tmH, a.h, c.f, rows, 64, 128) || !map_3d(&p2.tmWd, a.Wd, c.f, c.d, c.G, 64, 256))
+  if (!map_2d(&p2.tmH, a.h, c.f, rows, 64, 128) || !map_3d(&p2.tmWd, a.Wd, c.f, c.d, c.G, 64, 128) ||
+      !map_2d(&p2.tmO, a.o_perm, c.d, rows, 32, 32))
     return cudaErrorInvalidValue;
-  p2.O = a.o_perm;
   p2.f = c.f;
   p2.d = c.d;
   p2.nt = (c.d + 255) / 256;
   p2.hdr = a.hdr;
   p2.tabs = a.tabs;
-  return launch<FwdDown>(p2, s);
+  return launch_pair<FwdDown>(p2, s);
 }
 
 cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, cudaStream_t s) {
   const uint64_t rows = (uint64_t)L.rows;
   BwdDh::Params p2{};
-  if (!map_2d(&p2.tmDY, a.dy_perm, c.d, rows, 64, 128) || !map_3d(&p2.tmWdT, a.Wd, c.f, c.d, c.G, 64, 64))
+  if (!map_2d(&p2.tmDY, a.dy_perm, c.d, rows, 64, 128) || !map_3d(&p2.tmWdT, a.Wd, c.f, c.d, c.G, 64, 64) ||
+      !map_2d(&p2.tmDH, a.dh, c.f, rows, 32, 32))
     return cudaErrorInvalidValue;
-  p2.DH = a.dh;
   p2.f = c.f;
   p2.d = c.d;
   p2.nt = (c.f + 255) / 256;
   p2.hdr = a.hdr;
   p2.tabs = a.tabs;
-  cudaError_t e = launch<BwdDh>(p2, s);
+  cudaError_t e = launch_pair<BwdDh>(p2, s);
   if (e != cudaSuccess) return e;
 
   BwdFused::Params p3{};
   if (!map_2d(&p3.tmX, a.x_perm, c.d, rows, 64, 128) || !map_3d(&p3.tmWg, a.Wg, c.d, c.f, c.G, 64, 128) ||
-      !map_3d(&p3.tmWu, a.Wu, c.d, c.f, c.G, 64, 128))
+      !map_3d(&p3.tmWu, a.Wu, c.d, c.f, c.G, 64, 128) || !map_2d(&p3.tmDA, a.dA, c.f, rows, 32, 32) ||
+      !map_2d(&p3.tmDB, a.dB, c.f, rows, 32, 32) || !map_2d(&p3.tmHg, a.Hg, c.f, rows, 32, 32))
     return cudaErrorInvalidValue;
   p3.DH = a.dh;
   p3.gate_of_prow = a.gate_of_prow;
-  p3.dA = a.dA;
-  p3.dB = a.dB;
-  p3.Hg = a.Hg;
   p3.dg_part = a.dg_part;
   p3.f = c.f;
   p3.d = c.d;
@@ -1187,40 +1465,41 @@ cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, c
   p3.ndg = L.ndg;
   p3.hdr = a.hdr;
   p3.tabs = a.tabs;
-  e = launch<BwdFused>(p3, s);
+  e = launch_pair<BwdFused>(p3, s);
   if (e != cudaSuccess) return e;
 
   Wgrad::Params p4{};
   if (!map_2d(&p4.tmDA, a.dA, c.f, rows, 64, 64) || !map_2d(&p4.tmDB, a.dB, c.f, rows, 64, 64) ||
       !map_2d(&p4.tmX, a.x_perm, c.d, rows, 64, 64) || !map_2d(&p4.tmDY, a.dy_perm, c.d, rows, 64, 64) ||
-      !map_2d(&p4.tmHg, a.Hg, c.f, rows, 64, 64))
+      !map_2d(&p4.tmHg, a.Hg, c.f, rows, 64, 64) || !map_3d(&p4.tmdWg, a.dWg, c.d, c.f, c.G, 32, 32) ||
+      !map_3d(&p4.tmdWu, a.dWu, c.d, c.f, c.G, 32, 32) || !map_3d(&p4.tmdWd, a.dWd, c.f, c.d, c.G, 32, 32))
     return cudaErrorInvalidValue;
   p4.dWg = a.dWg;
   p4.dWu = a.dWu;
   p4.dWd = a.dWd;
   p4.f = c.f;
   p4.d = c.d;
-  p4.mt_f = (c.f + 127) / 128;
+  p4.mt_f = (c.f + kPairM - 1) / kPairM;
   p4.nt_d = (c.d + 255) / 256;
-  p4.mt_d = (c.d + 127) / 128;
+  p4.mt_d = (c.d + kPairM - 1) / kPairM;
   p4.nt_f = (c.f + 255) / 256;
   p4.tps = 2 * p4.mt_f * p4.nt_d + p4.mt_d * p4.nt_f;
   p4.hdr = a.hdr;
   p4.tabs = a.tabs;
-  e = launch<Wgrad>(p4, s);
+  e = launch_pair<Wgrad>(p4, s);
   if (e != cudaSuccess) return e;
 
   DgradX::Params p5{};
   if (!map_2d(&p5.tmDA, a.dA, c.f, rows, 64, 128) || !map_2d(&p5.tmDB, a.dB, c.f, rows, 64, 128) ||
-      !map_3d(&p5.tmWgT, a.Wg, c.d, c.f, c.G, 64, 64) || !map_3d(&p5.tmWuT, a.Wu, c.d, c.f, c.G, 64, 64))
+      !map_3d(&p5.tmWgT, a.Wg, c.d, c.f, c.G, 64, 64) || !map_3d(&p5.tmWuT, a.Wu, c.d, c.f, c.G, 64, 64) ||
+      !map_2d(&p5.tmDX, a.dx_perm, c.d, rows, 32, 32))
     return cudaErrorInvalidValue;
-  p5.dX = a.dx_perm;
   p5.f = c.f;
   p5.d = c.d;
   p5.nt = (c.d + 255) / 256;
   p5.hdr = a.hdr;
   p5.tabs = a.tabs;
-  return launch<DgradX>(p5, s);
+  return launch_pair<DgradX>(p5, s);
 }
 
 cudaError_t launch_router_dwr(const Cfg& c, const Layout& L, const uint16_t* x, const uint16_t* dl_bf16,

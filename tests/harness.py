@@ -42,10 +42,10 @@ def from_dev(t) -> np.ndarray:
 
 
 def padded_starts(kept: np.ndarray) -> np.ndarray:
-    """Segment starts of the documented padded layout: P_0 = 0, P_{g+1} = P_g + roundup(n_g, 128)."""
+    """Segment starts of the documented padded layout: P_0 = 0, P_{g+1} = P_g + roundup(n_g, 256)."""
     P = np.zeros(len(kept) + 1, dtype=np.int64)
     for g, n in enumerate(kept):
-        P[g + 1] = P[g] + (int(n) + 127) // 128 * 128
+        P[g + 1] = P[g] + (int(n) + 255) // 256 * 256
     return P
 
 

@@ -40,8 +40,8 @@ def test_workspace_size_and_rows():
     ws, saved = moe.moe_workspace_size(c)
     assert saved == 8192 * 2 * 8
     rows = moe.moe_perm_rows(c)
-    # routed rows padded per expert to 128, all segment starts multiples of 128
-    assert rows % 128 == 0 and rows >= 8192 * 2 + 127 * 8
+    # routed rows padded per expert to 256, all segment starts multiples of 256
+    assert rows % 256 == 0 and rows >= 8192 * 2 + 255 * 8
     assert ws > 3 * rows * 14336 * 2
     c2 = moe.config(T=16384, d=2048, f=1408, E=64, k=6, S=2, renorm=1)
     assert moe.moe_perm_rows(c2) >= 16384 * 6 + 2 * 16384
