@@ -397,8 +397,8 @@ def main():
                 work = args.steps * ((T + N) * d * 2 + 2 * (T + N) * d * 2 + 3 * 12 * T * k)
             elif name == "combine":
                 work = n * ((N + T) * d * 2 + 8 * T * k)
-            else:
-                work = n * ((N + T) * d * 2 + 4 * T * k + 4 * T * E + 4 * d * E)
+            else:   # expert rows + the router term row in, dx out, slot indices
+                work = n * ((N + 2 * T) * d * 2 + 4 * T * k)
             ent["gbs"] = work / (tot / 1000.0) / 1e9
             ent["frac_of_measured_peak"] = ent["gbs"] / pk["hbm"]
             hbm_bytes += work

@@ -178,7 +178,8 @@ namespace {
 const char* const kKernelNames[kKCount] = {
     "route_fwd", "dispatch_scan", "dispatch_gather", "gemm_gate_up_swiglu", "gemm_down",
     "combine", "gemm_bwd_recompute_swiglu", "gemm_wgrad", "gemm_dgrad_x", "dgates_reduce",
-    "router_dlogits", "router_dwr", "router_reduce", "combine_bwd", "gemm_bwd_dgrad_down"};
+    "router_dlogits", "router_dwr", "router_reduce", "combine_bwd", "gemm_bwd_dgrad_down",
+    "gemm_router_dx"};
 
 struct Profiler {
   std::mutex mu;
@@ -338,21 +339,24 @@ moe_status_t do_route(const Cfg& c, const Ws& w, const uint16_t* x, const float*
   return MOE_OK;
 }
 
-// dx = dlogits W_r^T (when dlogits is given) + the token's expert rows of dx_perm, on the tensor
-// cores with bf16 copies of dlogits and W_r padded to Ep columns.
+// dx = dlogits W_r^T (when dlogits is given) + the token's expert rows of dx_perm.  The router
+// term runs on the tensor cores (bf16 copies of dlogits and W_r padded to Ep columns) into a bf16
+// [T, d] buffer in the workspace's dY_perm region, which the backward no longer needs here; the
+// token-owner gather then adds it to the rows in fp32 with one rounding.
 moe_status_t do_combine_bwd(const Cfg& c, const Ws& w, const uint16_t* dx_perm, const float* dlogits,
                             const float* W_r, uint16_t* dx, cudaStream_t s) {
-  uint16_t* dl_bf16 = w.at<uint16_t>(w.L.dl_bf16);
-  uint16_t* wr_bf16 = w.at<uint16_t>(w.L.wr_bf16);
+  uint16_t* r = nullptr;
   if (dlogits != nullptr) {
+    uint16_t* dl_bf16 = w.at<uint16_t>(w.L.dl_bf16);
+    uint16_t* wr_bf16 = w.at<uint16_t>(w.L.wr_bf16);
+    r = w.at<uint16_t>(w.L.dy_perm);
     MOE_CUDA(launch_to_bf16_rows(dlogits, c.T, c.E, w.L.Ep, dl_bf16, s));
     MOE_CUDA(launch_to_bf16_rows(W_r, c.d, c.E, w.L.Ep, wr_bf16, s));
-  } else {   // no router term: a zero product
-    MOE_CUDA(cudaMemsetAsync(dl_bf16, 0, (size_t)c.T * w.L.Ep * 2, s));
-    MOE_CUDA(cudaMemsetAsync(wr_bf16, 0, (size_t)c.d * w.L.Ep * 2, s));
+    RouterDxArgs ra{dl_bf16, wr_bf16, r, w.hdr(), w.tabs()};
+    MOE_CUDA(launch_router_dx(c, w.L, ra, s));
   }
-  CombineBwdArgs a{dl_bf16, wr_bf16, dx_perm, dx, w.at<int32_t>(w.L.prow_of_slot), w.hdr(), w.tabs()};
-  MOE_CUDA(launch_combine_bwd(c, w.L, a, s));
+  CombineBwdArgs a{dx_perm, r, dx, w.tabs(), w.at<int32_t>(w.L.prow_of_slot)};
+  MOE_CUDA(launch_combine_bwd(c, a, s));
   return MOE_OK;
 }
 

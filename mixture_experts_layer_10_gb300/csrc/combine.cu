@@ -4,8 +4,9 @@
 // its tokens' expert rows with 16-byte loads, in fixed slot order, accumulating in fp32 and
 // rounding once to bf16.  No atomics: the result is bitwise deterministic.  Sources: MoEBlaze
 // (Methodology item 2: scatter/gather around the expert FFN) and the DisagMoE summary (section 2.2:
-// combine after the experts).  The input-gradient combine of the backward runs on the tensor cores
-// (CombineBwd in gemm.cu), where it also adds the router's dlogits W_r^T.
+// combine after the experts).  The input-gradient combine of the backward is the same kernel with
+// unit weights and one more source row per token: the router's dlogits W_r^T, computed on the
+// tensor cores beforehand (RouterDx in gemm.cu).
 #include <algorithm>
 
 #include "common.cuh"
@@ -35,9 +36,11 @@ __device__ __forceinline__ void store_row8(uint16_t* row, const float (&acc)[8])
   *reinterpret_cast<uint4*>(row) = v;
 }
 
-// y[t] = sum_j gates[t,j] * rows[prow(t,j)] + sum_s rows[P_{E+s} + t]
+// y[t] = extra[t] + sum_j gates[t,j] * rows[prow(t,j)] + sum_s rows[P_{E+s} + t], with extra
+// (a [T, d] bf16 row per token) and gates (weight 1 when null) optional.
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ rows,
                                                       const float* __restrict__ gates,
+                                                      const uint16_t* __restrict__ extra,
                                                       uint16_t* __restrict__ out,
                                                       const Tables* __restrict__ tb,
                                                       const int32_t* __restrict__ prow_of_slot,
@@ -54,11 +57,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
     float acc[8];
 #pragma unroll
     for (int m = 0; m < 8; ++m) acc[m] = 0.f;
+    if (extra != nullptr) add_row8(acc, extra + (size_t)t * d + col, 1.f);
     for (int j = 0; j < k; ++j) {
       const size_t slot = (size_t)t * k + j;
       const int p = prow_of_slot[slot];
       if (p < 0) continue;
-      add_row8(acc, rows + (size_t)p * d + col, gates[slot]);
+      add_row8(acc, rows + (size_t)p * d + col, gates != nullptr ? gates[slot] : 1.f);
     }
     for (int s = 0; s < S; ++s) {
       if (t >= tb->kept[E + s]) continue;
@@ -86,8 +90,18 @@ __global__ void dgates_kernel(const float* __restrict__ dg_part, const int32_t* 
 cudaError_t launch_combine(const Cfg& c, const CombineArgs& a, cudaStream_t s) {
   dim3 grid((c.T + kTokTile - 1) / kTokTile, (c.d + kColTile - 1) / kColTile);
   prof_mark(kKCombine, s, true);
-  combine_kernel<<<grid, 256, 0, s>>>(a.o_perm, a.gates, a.y, a.tabs, a.prow_of_slot, c.T, c.d, c.k, c.E, c.S);
+  combine_kernel<<<grid, 256, 0, s>>>(a.o_perm, a.gates, nullptr, a.y, a.tabs, a.prow_of_slot, c.T, c.d, c.k,
+                                      c.E, c.S);
   prof_mark(kKCombine, s, false);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_bwd(const Cfg& c, const CombineBwdArgs& a, cudaStream_t s) {
+  dim3 grid((c.T + kTokTile - 1) / kTokTile, (c.d + kColTile - 1) / kColTile);
+  prof_mark(kKCombineBwd, s, true);
+  combine_kernel<<<grid, 256, 0, s>>>(a.dx_perm, nullptr, a.r, a.dx, a.tabs, a.prow_of_slot, c.T, c.d, c.k,
+                                      c.E, c.S);
+  prof_mark(kKCombineBwd, s, false);
   return cudaGetLastError();
 }
 

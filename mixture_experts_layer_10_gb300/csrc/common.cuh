@@ -120,7 +120,7 @@ moe_status_t cuda_status(cudaError_t e);          // MOE_OK or MOE_ERR_CUDA (cle
 // with prof_mark(id, s, true/false), which records CUDA events on the launching stream.
 enum KernelId : int {
   kKRoute = 0, kKScan, kKGather, kKGateUp, kKDown, kKCombine, kKBwdFused, kKWgrad, kKDgradX,
-  kKDgates, kKRouterDlogits, kKRouterDwr, kKRouterReduce, kKCombineBwd, kKBwdDh, kKCount
+  kKDgates, kKRouterDlogits, kKRouterDwr, kKRouterReduce, kKCombineBwd, kKBwdDh, kKRouterDx, kKCount
 };
 void prof_mark(int id, cudaStream_t s, bool begin);
 
@@ -149,12 +149,17 @@ struct CombineArgs {
 };
 cudaError_t launch_combine(const Cfg& c, const CombineArgs& a, cudaStream_t s);
 
-// dx = dl W_r^T + the token's expert rows of dx_perm (tensor cores; bf16 operands of E padded to Ep)
-struct CombineBwdArgs {
-  const uint16_t* dl_bf16; const uint16_t* wr_bf16; const uint16_t* dx_perm; uint16_t* dx;
-  const int32_t* prow_of_slot; Hdr* hdr; const Tables* tabs;
+// dx = dl W_r^T + the token's expert rows of dx_perm: the router term on the tensor cores (bf16
+// operands of E padded to Ep) into r [T, d] bf16, then a token-owner gather adds the rows.
+struct RouterDxArgs {
+  const uint16_t* dl_bf16; const uint16_t* wr_bf16; uint16_t* r; Hdr* hdr; const Tables* tabs;
 };
-cudaError_t launch_combine_bwd(const Cfg& c, const Layout& L, const CombineBwdArgs& a, cudaStream_t s);
+cudaError_t launch_router_dx(const Cfg& c, const Layout& L, const RouterDxArgs& a, cudaStream_t s);
+struct CombineBwdArgs {
+  const uint16_t* dx_perm; const uint16_t* r; uint16_t* dx;   // r nullable (no router term)
+  const Tables* tabs; const int32_t* prow_of_slot;
+};
+cudaError_t launch_combine_bwd(const Cfg& c, const CombineBwdArgs& a, cudaStream_t s);
 
 struct RouterBwdArgs {
   const uint16_t* x; const float* W_r; const float* b_r; const int32_t* idx; const float* gates;

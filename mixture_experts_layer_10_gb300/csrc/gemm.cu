@@ -30,7 +30,7 @@
 //   DgradX     dX   = dA Wg + dB Wu                        A K-major, B MN-major, K = 2 d_ff
 //   RouterDwr  dW_r partials = x^T dl over token splits    A and B MN-major, N = E padded to 64,
 //              one CTA, M = 128
-//   CombineBwd dx   = dl W_r^T + the token's rows of dX     A and B K-major, K = E padded to 64,
+//   RouterDx   r    = dl W_r^T (the router's share of dx)  A and B K-major, K = E padded to 64,
 //              one CTA, M = 128
 //   RouterLogits  l = x W_r with W_r in three bf16 parts; epilogue: softmax, top-k, or the
 //              router's dlogits                          A and B K-major, N = E padded to 64
@@ -67,7 +67,7 @@ struct PolicyDefaults {
   // a stateful policy keeps per-lane epilogue state across the jobs of one CTA (epilogue_s)
   static constexpr bool kStateful = false;
   struct EpiState {};
-  static constexpr int kEpiBoxes = 0;   // TMA-store staging boxes per epilogue warp (pair kernel)
+  static constexpr uint32_t kEpiWarpBytes = 0;   // shared memory per epilogue warp (boxes, scratch)
 };
 
 struct SegSmem {
@@ -130,7 +130,7 @@ struct PairDefaults : PolicyDefaults {
   static constexpr int kAccBufs = 2;
   static constexpr int kTmemCols = 512;
   static constexpr uint32_t kIdesc = idesc_bf16(kPairM, 256, false, false);
-  static constexpr int kEpiBoxes = 2;
+  static constexpr uint32_t kEpiWarpBytes = 2 * 2048;   // two TMA-store boxes (kEpiBox)
 };
 
 // Epilogue output goes through shared memory and TMA stores: each epilogue warp writes a [32 rows x
@@ -340,12 +340,12 @@ struct BwdDh : PairDefaults {
 // The recompute a | b = X [Wg;Wu]^T (the forward's first GEMM shape, double-buffered TMEM) with the
 // SwiGLU backward in its epilogue, which reads this tile's dh' written by BwdDh:
 //   h = silu(a) b, dg += dh'.h, dh = g dh', dA = dh b silu'(a), dB = dh silu(a), Hg = g h.
-// Eight epilogue warps: two per TMEM lane quarter, each owning 64 of the 128 columns.
+// Four epilogue warps, one per TMEM lane quarter (eight, two per quarter, measured 77% instead of
+// 84% of the MMA rate per SM cycle).  dg is summed per 64-column half of the tile.
 struct BwdFused : PairDefaults {
   static constexpr int kId = kKBwdFused;
-  static constexpr int kEpiWarps = 8;
-  static constexpr int kStages = 5;
-  static constexpr int kEpiBoxes = 3;   // dA, dB, Hg
+  static constexpr int kEpiWarps = 4;
+  static constexpr uint32_t kEpiWarpBytes = 3 * 2048;   // boxes for dA, dB, Hg
   struct Params {
     CUtensorMap tmX, tmWg, tmWu, tmDA, tmDB, tmHg;
     const uint16_t* DH;
@@ -375,57 +375,60 @@ struct BwdFused : PairDefaults {
     const int y = j.m0 + (row & ~31);
     const size_t r = (size_t)(j.m0 + row);
     const float g = p.gate_of_prow[r];
-    float dg = 0.f;
 #pragma unroll 1
-    for (int c = part * 64; c < part * 64 + 64; c += 32) {
-      if (j.n0 + c >= p.f) break;
-      const uint4* dsrc = reinterpret_cast<const uint4*>(p.DH + r * p.f + j.n0 + c);
-      uint4 dv[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) dv[q] = dsrc[q];
-      uint32_t va[32], vb[32];
-      tmem_ld32(ta + c, va);
-      tmem_ld32(ta + 128 + c, vb);
-      tmem_ld_wait();
-      const uint32_t du[16] = {dv[0].x, dv[0].y, dv[0].z, dv[0].w, dv[1].x, dv[1].y, dv[1].z, dv[1].w,
-                               dv[2].x, dv[2].y, dv[2].z, dv[2].w, dv[3].x, dv[3].y, dv[3].z, dv[3].w};
-      uint32_t pa[16], pb[16], ph[16];
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        float o_da[2], o_db[2], o_h[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const float a = __uint_as_float(va[2 * i + h]);
-          const float b = __uint_as_float(vb[2 * i + h]);
-          const float dhp = h ? bf16_hi(du[i]) : bf16_lo(du[i]);
-          const float sg = 1.f / (1.f + __expf(-a));
-          const float sa = a * sg;
-          const float hv = sa * b;
-          dg = fmaf(dhp, hv, dg);
-          const float dh = g * dhp;
-          o_da[h] = dh * b * sg * (1.f + a * (1.f - sg));
-          o_db[h] = dh * sa;
-          o_h[h] = g * hv;
+    for (int half = 0; half < 2; ++half) {
+      float dg = 0.f;
+  #pragma unroll 1
+      for (int c = half * 64; c < half * 64 + 64; c += 32) {
+        if (j.n0 + c >= p.f) break;
+        const uint4* dsrc = reinterpret_cast<const uint4*>(p.DH + r * p.f + j.n0 + c);
+        uint4 dv[4];
+  #pragma unroll
+        for (int q = 0; q < 4; ++q) dv[q] = dsrc[q];
+        uint32_t va[32], vb[32];
+        tmem_ld32(ta + c, va);
+        tmem_ld32(ta + 128 + c, vb);
+        tmem_ld_wait();
+        const uint32_t du[16] = {dv[0].x, dv[0].y, dv[0].z, dv[0].w, dv[1].x, dv[1].y, dv[1].z, dv[1].w,
+                                 dv[2].x, dv[2].y, dv[2].z, dv[2].w, dv[3].x, dv[3].y, dv[3].z, dv[3].w};
+        uint32_t pa[16], pb[16], ph[16];
+  #pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float o_da[2], o_db[2], o_h[2];
+  #pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float a = __uint_as_float(va[2 * i + h]);
+            const float b = __uint_as_float(vb[2 * i + h]);
+            const float dhp = h ? bf16_hi(du[i]) : bf16_lo(du[i]);
+            const float sg = 1.f / (1.f + __expf(-a));
+            const float sa = a * sg;
+            const float hv = sa * b;
+            dg = fmaf(dhp, hv, dg);
+            const float dh = g * dhp;
+            o_da[h] = dh * b * sg * (1.f + a * (1.f - sg));
+            o_db[h] = dh * sa;
+            o_h[h] = g * hv;
+          }
+          pa[i] = pack_bf16(o_da[0], o_da[1]);
+          pb[i] = pack_bf16(o_db[0], o_db[1]);
+          ph[i] = pack_bf16(o_h[0], o_h[1]);
         }
-        pa[i] = pack_bf16(o_da[0], o_da[1]);
-        pb[i] = pack_bf16(o_db[0], o_db[1]);
-        ph[i] = pack_bf16(o_h[0], o_h[1]);
+        if (lane == 0) bulk_wait_read<0>();   // the previous boxes have been read
+        __syncwarp();
+        stage_box(ebuf, lane, pa);
+        stage_box(ebuf + kEpiBox, lane, pb);
+        stage_box(ebuf + 2 * kEpiBox, lane, ph);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&p.tmDA, ebuf, j.n0 + c, y);
+          tma_store_2d(&p.tmDB, ebuf + kEpiBox, j.n0 + c, y);
+          tma_store_2d(&p.tmHg, ebuf + 2 * kEpiBox, j.n0 + c, y);
+          bulk_commit();
+        }
       }
-      if (lane == 0) bulk_wait_read<0>();   // the previous boxes have been read
-      __syncwarp();
-      stage_box(ebuf, lane, pa);
-      stage_box(ebuf + kEpiBox, lane, pb);
-      stage_box(ebuf + 2 * kEpiBox, lane, ph);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_2d(&p.tmDA, ebuf, j.n0 + c, y);
-        tma_store_2d(&p.tmDB, ebuf + kEpiBox, j.n0 + c, y);
-        tma_store_2d(&p.tmHg, ebuf + 2 * kEpiBox, j.n0 + c, y);
-        bulk_commit();
-      }
+      p.dg_part[r * p.ndg + (j.n0 / 128) * 2 + half] = dg;
     }
-    p.dg_part[r * p.ndg + (j.n0 / 128) * 2 + part] = dg;
   }
   __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
 };
@@ -470,10 +473,12 @@ struct DgradX : PairDefaults {
 
 // Weight gradients, K = the expert's rows: dWg = dA^T X and dWu = dB^T X (M = d_ff, N = d_model),
 // dWd = dY^T Hg (M = d_model, N = d_ff).  A and B are row-major activations read MN-major, two
-// 64-wide boxes each per CTA and stage.  Tiles go expert by expert, largest first.
+// 64-wide boxes each per CTA and stage.  Tiles go expert by expert, largest first; inside an
+// expert the d_model-wide operand (X, or dY) is the one cycled through, so the pairs at work keep
+// all of it and a few d_ff-wide column blocks in L2.
 struct Wgrad : PairDefaults {
   static constexpr int kId = kKWgrad;
-  static constexpr int kEpiWarps = 8;
+  static constexpr int kEpiWarps = 4;
   static constexpr uint32_t kIdesc = idesc_bf16(kPairM, 256, true, true);
   struct Params {
     CUtensorMap tmDA, tmDB, tmX, tmDY, tmHg;   // all [rows, width] with 64 x 64 boxes
@@ -498,11 +503,11 @@ struct Wgrad : PairDefaults {
       r -= j.sub * gu;
       j.m0 = (r / p.nt_d) * kPairM;
       j.n0 = (r % p.nt_d) * 256;
-    } else {
+    } else {   // dWd: m fastest, so the pairs at work share a few Hg column blocks (d_ff wide)
       r -= 2 * gu;
       j.sub = 2;
-      j.m0 = (r / p.nt_f) * kPairM;
-      j.n0 = (r % p.nt_f) * 256;
+      j.m0 = (r % p.mt_d) * kPairM;
+      j.n0 = (r / p.mt_d) * 256;
     }
     return j;
   }
@@ -534,9 +539,10 @@ struct Wgrad : PairDefaults {
     uint16_t* W = j.sub == 0 ? p.dWg : (j.sub == 1 ? p.dWu : p.dWd);
     return W + ((size_t)j.seg * M + (ok ? m : 0)) * ncols;
   }
-  // Eight epilogue warps: the two warps of a TMEM lane quarter take 128 columns each.  A warp whose
-  // 32 rows all lie past M (the last pair tile of a d_ff or d_model not a multiple of 256) stores
-  // nothing; boxes that reach past M are clipped by the tensor map.
+  // Four epilogue warps, one per TMEM lane quarter, 256 columns each (eight warps sharing the
+  // quarters measured 3% fewer MMA cycles per SM cycle).  A warp whose 32 rows all lie past M
+  // (the last pair tile of a d_ff or d_model not a multiple of 256) stores nothing; boxes that
+  // reach past M are clipped by the tensor map.
   __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int part, int,
                                   uint8_t* ebuf) {
     const int lane = row & 31;
@@ -547,14 +553,14 @@ struct Wgrad : PairDefaults {
     const CUtensorMap* map = j.sub == 0 ? &p.tmdWg : (j.sub == 1 ? &p.tmdWu : &p.tmdWd);
     epi_begin(lane);
 #pragma unroll 1
-    for (int c = part * 128; c < part * 128 + 128; c += 32) {
+    for (int c = 0; c < 256; c += 32) {
       if (j.n0 + c >= ncols) break;
       uint32_t v[32];
       tmem_ld32(ta + c, v);
       tmem_ld_wait();
       uint32_t pk[16];
       pack32(v, pk);
-      uint8_t* box = claim_box(ebuf, (c - part * 128) / 32, lane);
+      uint8_t* box = claim_box(ebuf, c / 32, lane);
       stage_box(box, lane, pk);
       store_box_3d(map, box, lane, j.n0 + c, y, j.seg);
     }
@@ -641,25 +647,22 @@ struct RouterDwr : PolicyDefaults {
   }
 };
 
-// Input gradient of the layer on the tensor cores: dx[t] = dl[t] W_r^T (M = 128 tokens, N = 256
-// columns of d_model, K = E padded to 64, both operands bf16 K-major), with the epilogue adding, in
-// fixed order and fp32, the token's kept expert rows of dx_perm and its shared-expert rows, then
-// rounding once to bf16.  Token owner, no atomics.  Eight epilogue warps (128 columns each).
-struct CombineBwd : PolicyDefaults {
-  static constexpr int kId = kKCombineBwd;
-  static constexpr int kEpiWarps = 8;
+// The router's share of the input gradient on the tensor cores: r[t] = dl[t] W_r^T (M = 128
+// tokens, N = 256 columns of d_model, K = E padded to 64, both operands bf16 K-major), stored as
+// bf16 [T, d] for the token-owner combine that adds the expert rows.
+struct RouterDx : PolicyDefaults {
+  static constexpr int kId = kKRouterDx;
+  static constexpr int kEpiWarps = 4;
   static constexpr int kStages = 4;
   static constexpr uint32_t kStageBytes = kTileA + 2 * kTileA;   // dl tile + W_r tile (256 rows)
   static constexpr int kAccCols = 256;
   static constexpr int kAccBufs = 2;
   static constexpr int kTmemCols = 512;
   static constexpr uint32_t kIdesc = idesc_bf16(128, 256, false, false);
+  static constexpr uint32_t kEpiWarpBytes = 2 * 2048;   // two TMA-store boxes
   struct Params {
-    CUtensorMap tmDL, tmWR;
-    const uint16_t* dx_perm;
-    uint16_t* dx;
-    const int32_t* prow_of_slot;
-    int T, d, k, E, S, mt, nt, kiters;
+    CUtensorMap tmDL, tmWR, tmR;
+    int T, d, mt, nt, kiters;
     Hdr* hdr;
     const Tables* tabs;
   };
@@ -687,48 +690,10 @@ struct CombineBwd : PolicyDefaults {
       umma_bf16(dt, sdesc_kmajor(sa + kk * 32), sdesc_kmajor(sa + kTileA + kk * 32), kIdesc,
                 (kit | kk) != 0);
   }
-  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int part, int) {
-    const int t = j.m0 + row;
-#pragma unroll 1
-    for (int c = part * 128; c < part * 128 + 128; c += 32) {
-      const int col = j.n0 + c;
-      if (col >= p.d) break;
-      uint32_t v[32];
-      tmem_ld32(ta + c, v);
-      tmem_ld_wait();
-      if (t >= p.T) continue;
-      float acc[32];
-#pragma unroll
-      for (int i = 0; i < 32; ++i) acc[i] = __uint_as_float(v[i]);
-      for (int jj = 0; jj < p.k + p.S; ++jj) {
-        size_t prow;
-        if (jj < p.k) {
-          const int pr = p.prow_of_slot[(size_t)t * p.k + jj];
-          if (pr < 0) continue;
-          prow = (size_t)pr;
-        } else {
-          const int s = p.E + (jj - p.k);
-          if (t >= p.tabs->kept[s]) continue;
-          prow = (size_t)p.tabs->poff[s] + t;
-        }
-        const uint4* src = reinterpret_cast<const uint4*>(p.dx_perm + prow * p.d + col);
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint4 u = src[q];
-          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-#pragma unroll
-          for (int m = 0; m < 4; ++m) {
-            acc[8 * q + 2 * m] += bf16_lo(w[m]);
-            acc[8 * q + 2 * m + 1] += bf16_hi(w[m]);
-          }
-        }
-      }
-      uint4* dst = reinterpret_cast<uint4*>(p.dx + (size_t)t * p.d + col);
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        dst[q] = make_uint4(pack_bf16(acc[8 * q], acc[8 * q + 1]), pack_bf16(acc[8 * q + 2], acc[8 * q + 3]),
-                            pack_bf16(acc[8 * q + 4], acc[8 * q + 5]), pack_bf16(acc[8 * q + 6], acc[8 * q + 7]));
-    }
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int, int, uint8_t* ebuf) {
+    const int y = j.m0 + (row & ~31);
+    if (y >= p.T) return;   // the tile's last warps may lie past the tokens
+    store_acc_boxes(&p.tmR, y, j.n0, p.d, ta, row & 31, ebuf);
   }
   __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
 };
@@ -976,7 +941,8 @@ struct RouterLogits : PolicyDefaults {
 
 template <class P>
 constexpr size_t epi_bytes() {
-  return (size_t)P::kEpiWarps * P::kEpiBoxes * kEpiBox;
+  static_assert(P::kEpiWarpBytes % 1024 == 0, "boxes stay 1024-aligned");
+  return (size_t)P::kEpiWarps * P::kEpiWarpBytes;
 }
 
 template <class P>
@@ -994,13 +960,14 @@ __global__ void __launch_bounds__(threads_of<P>(), 1) gemm_kernel(const __grid_c
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stages = smem;
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + (size_t)P::kStages * P::kStageBytes);
+  uint8_t* epi = smem + (size_t)P::kStages * P::kStageBytes;   // per-warp epilogue shared memory
+  uint64_t* full = reinterpret_cast<uint64_t*>(epi + epi_bytes<P>());
   uint64_t* empty = full + P::kStages;
   uint64_t* tfull = empty + P::kStages;
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  SegSmem& segs = *reinterpret_cast<SegSmem*>(smem + (size_t)P::kStages * P::kStageBytes + 256);
+  SegSmem& segs = *reinterpret_cast<SegSmem*>(epi + epi_bytes<P>() + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   load_segs(segs, p.tabs);
@@ -1109,7 +1076,7 @@ __global__ void __launch_bounds__(threads_of<P>(), 1) gemm_kernel(const __grid_c
         if (part == 0) P::epilogue_zero(p, j, row, part);
         continue;
       }
-      if (!mbar_wait(&tfull[acc], acc_phase, limit, abort_flag)) {
+      if (!mbar_wait_idle(&tfull[acc], acc_phase, limit, abort_flag)) {
         record_error(p.hdr, MOE_ERR_TIMEOUT, kSiteGemmEpilogue);
         *abort_flag = 1;
         break;
@@ -1118,6 +1085,8 @@ __global__ void __launch_bounds__(threads_of<P>(), 1) gemm_kernel(const __grid_c
       const uint32_t ta = tmem_base + (uint32_t)(acc * P::kAccCols) + ((uint32_t)(q * 32) << 16);
       if constexpr (P::kStateful)
         P::epilogue_s(p, j, ta, row, part, seq, es, tmem_base + ((uint32_t)(q * 32) << 16));
+      else if constexpr (P::kEpiWarpBytes > 0)
+        P::epilogue(p, j, ta, row, part, seq, epi + (size_t)(warp - 2) * P::kEpiWarpBytes);
       else
         P::epilogue(p, j, ta, row, part, seq);
       ++seq;
@@ -1129,6 +1098,7 @@ __global__ void __launch_bounds__(threads_of<P>(), 1) gemm_kernel(const __grid_c
         acc_phase ^= 1;
       }
     }
+    if (lane == 0) bulk_wait_all();   // this warp's output stores (if any) have landed
   }
   tc_fence_before();
   __syncthreads();
@@ -1281,7 +1251,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<P>(), 1)
     const int q = warp & 3;            // TMEM lane quarter this warp may access
     const int part = (warp - 2) >> 2;  // column share when two warps serve one quarter
     const int row = q * 32 + lane;
-    uint8_t* ebuf = epi + (size_t)(warp - 2) * P::kEpiBoxes * kEpiBox;
+    uint8_t* ebuf = epi + (size_t)(warp - 2) * P::kEpiWarpBytes;
     int acc = 0;
     uint32_t acc_phase = 0;
     int seq = 0;
@@ -1292,7 +1262,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<P>(), 1)
         if (part == 0) P::epilogue_zero(p, j, row, part);
         continue;
       }
-      if (!mbar_wait(&tfull[acc], acc_phase, limit, abort_flag)) {
+      if (!mbar_wait_idle(&tfull[acc], acc_phase, limit, abort_flag)) {
         record_error(p.hdr, MOE_ERR_TIMEOUT, kSiteGemmEpilogue);
         *abort_flag = 1;
         break;
@@ -1555,24 +1525,19 @@ cudaError_t launch_router_dlogits_tc(const Cfg& c, const Layout& L, const Router
   return launch_router_tc<true>(c, L, a, s);
 }
 
-cudaError_t launch_combine_bwd(const Cfg& c, const Layout& L, const CombineBwdArgs& a, cudaStream_t s) {
-  CombineBwd::Params p{};
-  if (!map_2d(&p.tmDL, a.dl_bf16, L.Ep, c.T, 64, 128) || !map_2d(&p.tmWR, a.wr_bf16, L.Ep, c.d, 64, 256))
+cudaError_t launch_router_dx(const Cfg& c, const Layout& L, const RouterDxArgs& a, cudaStream_t s) {
+  RouterDx::Params p{};
+  if (!map_2d(&p.tmDL, a.dl_bf16, L.Ep, c.T, 64, 128) || !map_2d(&p.tmWR, a.wr_bf16, L.Ep, c.d, 64, 256) ||
+      !map_2d(&p.tmR, a.r, c.d, c.T, 32, 32))
     return cudaErrorInvalidValue;
-  p.dx_perm = a.dx_perm;
-  p.dx = a.dx;
-  p.prow_of_slot = a.prow_of_slot;
   p.T = c.T;
   p.d = c.d;
-  p.k = c.k;
-  p.E = c.E;
-  p.S = c.S;
   p.mt = (c.T + kBM - 1) / kBM;
   p.nt = (c.d + 255) / 256;
   p.kiters = L.Ep / kBK;
   p.hdr = a.hdr;
   p.tabs = a.tabs;
-  return launch<CombineBwd>(p, s);
+  return launch<RouterDx>(p, s);
 }
 
 }  // namespace moe

@@ -68,6 +68,24 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
   }
 }
 
+// The same for a waiter with nothing else to do for a while (an epilogue warp waiting for a whole
+// tile's MMAs): it naps between polls, so its issue slots go to the producer and MMA warps that
+// share its SM sub-partition.
+__device__ __forceinline__ bool mbar_wait_idle(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
+                                               volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  while (true) {
+    __nanosleep(256);
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort) return false;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > limit_ns) return false;
+  }
+}
+
 // ---------------------------------------------------------------------------------------------
 // TMA
 // ---------------------------------------------------------------------------------------------
