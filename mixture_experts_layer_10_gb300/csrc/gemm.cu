@@ -324,9 +324,7 @@ struct BwdDh : PairDefaults {
   __device__ static void prefetch(const Params& p) { tma_prefetch(&p.tmDY); tma_prefetch(&p.tmWdT); }
   __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint32_t cbar, int rank) {
     tma_load_2d_pair(st, &p.tmDY, cbar, kit * kBK, j.m0 + kBM * rank);
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-      tma_load_3d_pair(st + kTileA + i * kBox, &p.tmWdT, cbar, j.n0 + kBM * rank + 64 * i, kit * kBK, j.seg);
+    tma_load_4d_pair(st + kTileA, &p.tmWdT, cbar, 0, kit * kBK, (j.n0 + kBM * rank) / 64, j.seg);
   }
   __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
     mma_kk_bmn(sa, dt, kIdesc, kit);
@@ -457,10 +455,7 @@ struct DgradX : PairDefaults {
     const bool up = kit >= nk;
     const int k0 = (up ? kit - nk : kit) * kBK;
     tma_load_2d_pair(st, up ? &p.tmDB : &p.tmDA, cbar, k0, j.m0 + kBM * rank);
-#pragma unroll
-    for (int i = 0; i < 2; ++i)
-      tma_load_3d_pair(st + kTileA + i * kBox, up ? &p.tmWuT : &p.tmWgT, cbar, j.n0 + kBM * rank + 64 * i, k0,
-                       j.seg);
+    tma_load_4d_pair(st + kTileA, up ? &p.tmWuT : &p.tmWgT, cbar, 0, k0, (j.n0 + kBM * rank) / 64, j.seg);
   }
   __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
     mma_kk_bmn(sa, dt, kIdesc, kit);
@@ -472,8 +467,9 @@ struct DgradX : PairDefaults {
 };
 
 // Weight gradients, K = the expert's rows: dWg = dA^T X and dWu = dB^T X (M = d_ff, N = d_model),
-// dWd = dY^T Hg (M = d_model, N = d_ff).  A and B are row-major activations read MN-major, two
-// 64-wide boxes each per CTA and stage.  Tiles go expert by expert, largest first; inside an
+// dWd = dY^T Hg (M = d_model, N = d_ff).  A and B are row-major activations read MN-major: two
+// 64 x 64 boxes each per CTA and stage, fetched by one copy (map_mn2; two copies per operand held
+// the kernel at 73% of the MMA rate per SM cycle, one copy reaches 86%).  Tiles go expert by expert, largest first; inside an
 // expert the d_model-wide operand (X, or dY) is the one cycled through, so the pairs at work keep
 // all of it and a few d_ff-wide column blocks in L2.
 struct Wgrad : PairDefaults {
@@ -481,7 +477,7 @@ struct Wgrad : PairDefaults {
   static constexpr int kEpiWarps = 4;
   static constexpr uint32_t kIdesc = idesc_bf16(kPairM, 256, true, true);
   struct Params {
-    CUtensorMap tmDA, tmDB, tmX, tmDY, tmHg;   // all [rows, width] with 64 x 64 boxes
+    CUtensorMap tmDA, tmDB, tmX, tmDY, tmHg;   // all [rows, width] as 64-column block pairs (map_mn2)
     CUtensorMap tmdWg, tmdWu, tmdWd;           // [G, M, ncols] with 32 x 32 boxes (stores)
     uint16_t *dWg, *dWu, *dWd;
     int f, d;
@@ -519,11 +515,8 @@ struct Wgrad : PairDefaults {
     const int row = j.kbase + kit * kBK;
     const CUtensorMap* ta = j.sub == 0 ? &p.tmDA : (j.sub == 1 ? &p.tmDB : &p.tmDY);
     const CUtensorMap* tb = j.sub == 2 ? &p.tmHg : &p.tmX;
-#pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      tma_load_2d_pair(st + i * kBox, ta, cbar, j.m0 + kBM * rank + 64 * i, row);
-      tma_load_2d_pair(st + (2 + i) * kBox, tb, cbar, j.n0 + kBM * rank + 64 * i, row);
-    }
+    tma_load_3d_pair(st, ta, cbar, 0, row, (j.m0 + kBM * rank) / 64);
+    tma_load_3d_pair(st + 2 * kBox, tb, cbar, 0, row, (j.n0 + kBM * rank) / 64);
   }
   __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
 #pragma unroll
@@ -1327,6 +1320,34 @@ bool map_2d(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows, uin
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// MN-major operand pairs: [rows, width] bf16 (width a multiple of 64) seen as 64-column blocks,
+// dims {64, rows, width / 64}, box {64, 64, 2}: one copy fills two 64 x 64 boxes back to back,
+// the layout of two 2D boxes of columns c and c + 64.
+bool map_mn2(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {64, rows, width / 64};
+  const cuuint64_t strides[2] = {width * 2, 128};
+  const cuuint32_t box[3] = {64, 64, 2};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The same for [G, rows, width] weights: dims {64, rows, width / 64, G}, box {64, 64, 2, 1}.
+bool map_mn2_g(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows, uint64_t G) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {64, rows, width / 64, G};
+  const cuuint64_t strides[3] = {width * 2, 128, width * rows * 2};
+  const cuuint32_t box[4] = {64, 64, 2, 1};
+  const cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3D bf16 tensor [G, rows, width] with a box of box_w x box_r x 1.
 bool map_3d(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows, uint64_t G,
             uint32_t box_w, uint32_t box_r) {
@@ -1410,7 +1431,7 @@ cudaError_t launch_ffn_fwd(const Cfg& c, const Layout& L, const FfnFwdArgs& a, c
 cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, cudaStream_t s) {
   const uint64_t rows = (uint64_t)L.rows;
   BwdDh::Params p2{};
-  if (!map_2d(&p2.tmDY, a.dy_perm, c.d, rows, 64, 128) || !map_3d(&p2.tmWdT, a.Wd, c.f, c.d, c.G, 64, 64) ||
+  if (!map_2d(&p2.tmDY, a.dy_perm, c.d, rows, 64, 128) || !map_mn2_g(&p2.tmWdT, a.Wd, c.f, c.d, c.G) ||
       !map_2d(&p2.tmDH, a.dh, c.f, rows, 32, 32))
     return cudaErrorInvalidValue;
   p2.f = c.f;
@@ -1439,9 +1460,9 @@ cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, c
   if (e != cudaSuccess) return e;
 
   Wgrad::Params p4{};
-  if (!map_2d(&p4.tmDA, a.dA, c.f, rows, 64, 64) || !map_2d(&p4.tmDB, a.dB, c.f, rows, 64, 64) ||
-      !map_2d(&p4.tmX, a.x_perm, c.d, rows, 64, 64) || !map_2d(&p4.tmDY, a.dy_perm, c.d, rows, 64, 64) ||
-      !map_2d(&p4.tmHg, a.Hg, c.f, rows, 64, 64) || !map_3d(&p4.tmdWg, a.dWg, c.d, c.f, c.G, 32, 32) ||
+  if (!map_mn2(&p4.tmDA, a.dA, c.f, rows) || !map_mn2(&p4.tmDB, a.dB, c.f, rows) ||
+      !map_mn2(&p4.tmX, a.x_perm, c.d, rows) || !map_mn2(&p4.tmDY, a.dy_perm, c.d, rows) ||
+      !map_mn2(&p4.tmHg, a.Hg, c.f, rows) || !map_3d(&p4.tmdWg, a.dWg, c.d, c.f, c.G, 32, 32) ||
       !map_3d(&p4.tmdWu, a.dWu, c.d, c.f, c.G, 32, 32) || !map_3d(&p4.tmdWd, a.dWd, c.f, c.d, c.G, 32, 32))
     return cudaErrorInvalidValue;
   p4.dWg = a.dWg;
@@ -1461,7 +1482,7 @@ cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, c
 
   DgradX::Params p5{};
   if (!map_2d(&p5.tmDA, a.dA, c.f, rows, 64, 128) || !map_2d(&p5.tmDB, a.dB, c.f, rows, 64, 128) ||
-      !map_3d(&p5.tmWgT, a.Wg, c.d, c.f, c.G, 64, 64) || !map_3d(&p5.tmWuT, a.Wu, c.d, c.f, c.G, 64, 64) ||
+      !map_mn2_g(&p5.tmWgT, a.Wg, c.d, c.f, c.G) || !map_mn2_g(&p5.tmWuT, a.Wu, c.d, c.f, c.G) ||
       !map_2d(&p5.tmDX, a.dx_perm, c.d, rows, 32, 32))
     return cudaErrorInvalidValue;
   p5.f = c.f;
