@@ -17,14 +17,17 @@ namespace {
 constexpr int kTokTile = 32;
 constexpr int kColTile = 256;
 
-__device__ __forceinline__ void add_row8(float (&acc)[8], const uint16_t* row, float w) {
-  const uint4 v = *reinterpret_cast<const uint4*>(row);
+__device__ __forceinline__ void add_vec8(float (&acc)[8], const uint4& v, float w) {
   const uint32_t u[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
     acc[2 * m] = fmaf(w, bf16_lo(u[m]), acc[2 * m]);
     acc[2 * m + 1] = fmaf(w, bf16_hi(u[m]), acc[2 * m + 1]);
   }
+}
+
+__device__ __forceinline__ void add_row8(float (&acc)[8], const uint16_t* row, float w) {
+  add_vec8(acc, *reinterpret_cast<const uint4*>(row), w);
 }
 
 __device__ __forceinline__ void store_row8(uint16_t* row, const float (&acc)[8]) {
@@ -58,11 +61,31 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 #pragma unroll
     for (int m = 0; m < 8; ++m) acc[m] = 0.f;
     if (extra != nullptr) add_row8(acc, extra + (size_t)t * d + col, 1.f);
-    for (int j = 0; j < k; ++j) {
-      const size_t slot = (size_t)t * k + j;
-      const int p = prow_of_slot[slot];
-      if (p < 0) continue;
-      add_row8(acc, rows + (size_t)p * d + col, gates != nullptr ? gates[slot] : 1.f);
+    // slots in groups of four: the four rows are loaded before any is added (more bytes in
+    // flight per thread), then added in slot order
+    for (int j0 = 0; j0 < k; j0 += 4) {
+      uint4 v[4];
+      float w[4];
+      bool has[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int j = j0 + u;
+        v[u] = make_uint4(0, 0, 0, 0);
+        w[u] = 0.f;
+        has[u] = false;
+        if (j < k) {
+          const size_t slot = (size_t)t * k + j;
+          const int p = prow_of_slot[slot];
+          if (p >= 0) {
+            v[u] = *reinterpret_cast<const uint4*>(rows + (size_t)p * d + col);
+            w[u] = gates != nullptr ? gates[slot] : 1.f;
+            has[u] = true;
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (has[u]) add_vec8(acc, v[u], w[u]);
     }
     for (int s = 0; s < S; ++s) {
       if (t >= tb->kept[E + s]) continue;

@@ -184,6 +184,8 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(DispatchArg
   }
 }
 
+constexpr int kUnroll = 4;   // 16-byte vectors per lane in flight per source row
+
 template <bool kMeta, bool kX, bool kDy>
 __global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a, int T, int k, int E,
                                                               int S, int d) {
@@ -222,27 +224,42 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a, in
         if (kDy && kept) a.gate_of_prow[prow] = a.gates[slot];
       }
       const int ng = min(32, k - jb);
-      // warp-uniform trip count: every lane takes part in every shuffle, and the vector index is
-      // predicated instead (a row need not be a multiple of 32 vectors, e.g. d = 2880)
-      for (int v0 = 0; v0 < nvec; v0 += 32) {
-        const int v = v0 + lane;
-        const bool live = v < nvec;
-        uint4 vx = make_uint4(0, 0, 0, 0), vd = make_uint4(0, 0, 0, 0);
-        if (kX && live) vx = xs[v];
-        if (kDy && live) vd = dys[v];
+      // kUnroll vectors per lane are loaded before any is stored, so a warp keeps
+      // kUnroll x 512 bytes of each source row in flight.  Warp-uniform trip count: every lane
+      // takes part in every shuffle, and the vector index is predicated instead (a row need not
+      // be a multiple of 32 vectors, e.g. d = 2880).
+      for (int v0 = 0; v0 < nvec; v0 += 32 * kUnroll) {
+        uint4 vx[kUnroll], vd[kUnroll];
+#pragma unroll
+        for (int u = 0; u < kUnroll; ++u) {
+          const int v = v0 + 32 * u + lane;
+          vx[u] = make_uint4(0, 0, 0, 0);
+          vd[u] = make_uint4(0, 0, 0, 0);
+          if (kX && v < nvec) vx[u] = xs[v];
+          if (kDy && v < nvec) vd[u] = dys[v];
+        }
         for (int q = 0; q < ng; ++q) {
           const int p = __shfl_sync(0xffffffffu, prow, q);
-          if (p >= 0 && live) {
-            if (kX) reinterpret_cast<uint4*>(a.x_perm + (size_t)p * d)[v] = vx;
-            if (kDy) reinterpret_cast<uint4*>(a.dy_perm + (size_t)p * d)[v] = vd;
+          if (p < 0) continue;
+#pragma unroll
+          for (int u = 0; u < kUnroll; ++u) {
+            const int v = v0 + 32 * u + lane;
+            if (v >= nvec) continue;
+            if (kX) reinterpret_cast<uint4*>(a.x_perm + (size_t)p * d)[v] = vx[u];
+            if (kDy) reinterpret_cast<uint4*>(a.dy_perm + (size_t)p * d)[v] = vd[u];
           }
         }
-        if (jb == 0 && live) {
+        if (jb == 0) {
           for (int s = 0; s < S; ++s) {
             if (t >= tb->kept[E + s]) continue;
             const size_t p = (size_t)tb->poff[E + s] + t;
-            if (kX) reinterpret_cast<uint4*>(a.x_perm + p * d)[v] = vx;
-            if (kDy) reinterpret_cast<uint4*>(a.dy_perm + p * d)[v] = vd;
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+              const int v = v0 + 32 * u + lane;
+              if (v >= nvec) continue;
+              if (kX) reinterpret_cast<uint4*>(a.x_perm + p * d)[v] = vx[u];
+              if (kDy) reinterpret_cast<uint4*>(a.dy_perm + p * d)[v] = vd[u];
+            }
           }
         }
       }
