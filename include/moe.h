@@ -115,7 +115,7 @@ moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, size_t ws_byt
 
 /* Router: logits, softmax, top-k and gates for every token.  b_r and logits may be NULL.
  * Writes idx [T,k], gates [T,k], and logits [T,E] when non-NULL.  ws is this configuration's
- * workspace (moe_workspace_size).  For 32 <= E <= 128 and k <= 8 the logits run on the tensor
+ * workspace (moe_workspace_size).  For E <= 128 and k <= 8 the logits run on the tensor
  * cores: W_r is split in ws into three bf16 parts whose sum equals it within fp32 rounding, and the
  * products are summed in fp32 over 256-wide slices of d_model; other shapes use an fp32 tile
  * product with warp-per-token selection. */

@@ -174,7 +174,7 @@ cudaError_t launch_router_dwr(const Cfg& c, const Layout& L, const uint16_t* x, 
 // dst [rows, ld] bf16 = src [rows, cols] fp32, zero for cols <= c < ld
 cudaError_t launch_to_bf16_rows(const float* src, int rows, int cols, int ld, uint16_t* dst, cudaStream_t s);
 
-// Router logits on the tensor cores (32 <= E <= 128, k <= 8): W_r [d, E] fp32 is split into
+// Router logits on the tensor cores (E <= 128, k <= 8): W_r [d, E] fp32 is split into
 // hi + mid + lo bf16 parts stored K-major as wr3 [3][Ep][d].
 bool router_on_tensor_cores(const Cfg& c);
 bool router_bwd_on_tensor_cores(const Cfg& c);   // the backward too (gates not renormalised)

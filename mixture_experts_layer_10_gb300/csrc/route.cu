@@ -476,7 +476,7 @@ cudaError_t launch_router_reduce(const Cfg& c, const Layout& L, const RouterBwdA
   return cudaGetLastError();
 }
 
-bool router_on_tensor_cores(const Cfg& c) { return c.E >= 32 && c.E <= 128 && c.k <= 8; }
+bool router_on_tensor_cores(const Cfg& c) { return c.E <= 128 && c.k <= 8; }
 bool router_bwd_on_tensor_cores(const Cfg& c) { return router_on_tensor_cores(c) && !c.renorm; }
 
 cudaError_t launch_split_wr(const float* W_r, int d, int E, int Ep, uint16_t* wr3, cudaStream_t s) {

@@ -25,6 +25,9 @@ CASES = {
     "router_e96_k8": dict(T=333, d=320, E=96, k=8, f=64, S=0, renorm=0, cf=0.0, zipf=True),
     # tensor-core forward with renormalised gates (the backward then needs no logits)
     "router_e64_renorm": dict(T=257, d=256, E=64, k=6, f=128, S=1, renorm=1, cf=0.0, zipf=False),
+    # the fp32 SIMT router: more than 128 experts, and more than 8 experts per token
+    "router_simt_e160": dict(T=300, d=128, E=160, k=4, f=64, S=0, renorm=0, cf=0.0, zipf=True),
+    "router_simt_k10": dict(T=200, d=192, E=24, k=10, f=64, S=0, renorm=1, cf=0.0, zipf=False),
 }
 
 FAST = ["tiny", "ragged_mixtral", "deepseek_small", "qwen_small", "gptoss_small"]
