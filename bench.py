@@ -50,7 +50,8 @@ GEMMS = {  # algorithmic FLOPs per launch in units of N*d*f (N = rows the expert
     "gemm_wgrad": 6, "gemm_dgrad_x": 4,
 }
 HBM_KERNELS = ("dispatch_gather", "combine", "combine_bwd")
-KERNEL_SOURCES = ("gemm.cu", "dispatch.cu", "combine.cu", "route.cu", "ptx.cuh", "common.cuh")
+KERNEL_SOURCES = ("gemm.cu", "dispatch.cu", "combine.cu", "route.cu", "activations.cu", "ptx.cuh", "common.cuh")
+ROW_TILE = 256   # expert segments are padded to multiples of this many rows (include/moe.h)
 
 
 def parse():
@@ -66,6 +67,9 @@ def parse():
     ap.add_argument("--experts", type=int, default=0, help="override E (profiler captures)")
     ap.add_argument("--topk", type=int, default=0, help="override k (profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--keep-rows", type=int, default=0,
+                    help="expert-ordered rows whose gate/up pre-activations the forward keeps instead "
+                         "of the backward recomputing them (0: recompute all, the default; -1: keep all)")
     return ap.parse_args()
 
 
@@ -266,6 +270,10 @@ def main():
     b_r = torch.from_numpy(inp["b_r"]).cuda() if inp["b_r"] is not None else None
     Wg, Wu, Wd = dev_bf16(inp["W_gate"]), dev_bf16(inp["W_up"]), dev_bf16(inp["W_down"])
     mc = moe.config_from(cfg)
+    if args.keep_rows:
+        cfg["keep_rows"] = moe.moe_perm_rows(mc) if args.keep_rows < 0 else args.keep_rows
+        mc = moe.config_from(cfg)
+    keep = min(cfg.get("keep_rows", 0) // ROW_TILE * ROW_TILE, moe.moe_perm_rows(mc))
     buf = moe.Buffers.allocate(mc)
     y = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
     dx = torch.empty_like(y)
@@ -293,6 +301,13 @@ def main():
     counts_h = counts.cpu().numpy()
     n_kept = int(offsets[-1].item())
     N = n_kept + S * T
+    # rows whose a, b the forward keeps (real rows below `keep` in the padded expert order); the
+    # recompute GEMM does the rest
+    seg_rows = list(np.diff(offsets.cpu().numpy())) + [T] * S
+    start, kept_real = 0, 0
+    for n_g in seg_rows:
+        kept_real += max(0, min(start + int(n_g), keep) - start)
+        start += (int(n_g) + ROW_TILE - 1) // ROW_TILE * ROW_TILE
     load_max_over_mean = float(counts_h.max() / counts_h.mean())
     del x_perm, scratch_rows, scratch_tok
 
@@ -387,7 +402,8 @@ def main():
         launches += n
         ent = {"ms_per_step": tot / args.steps, "launches": n}
         if name in GEMMS:
-            work = GEMMS[name] * N * d * f * n     # FLOPs over all launches
+            rows_done = N - kept_real if name == "gemm_bwd_recompute_swiglu" else N
+            work = GEMMS[name] * rows_done * d * f * n     # FLOPs over all launches
             ent["tflops"] = work / (tot / 1000.0) / 1e12
             ent["frac_of_measured_peak"] = ent["tflops"] / tensor_peak
             gemm_flops += work
@@ -428,7 +444,9 @@ def main():
                    "n_shared": S, "global_batch": world * T, "parallelism": f"replicas x{world}",
                    "l2": "no flush: each step streams > L2 (expert weights alone %.2f GB)"
                          % (3 * G * d * f * 2 / 1e9),
-                   "rows_per_step": N, "load_max_over_mean": load_max_over_mean},
+                   "rows_per_step": N, "load_max_over_mean": load_max_over_mean,
+                   "keep_rows": keep, "kept_rows": kept_real,
+                   "kept_activation_bytes": keep * f * 2 * 2},
         "e2e": {"value": world * T / (ms_e2e / 1000.0), "unit": "tokens/s", "ms_per_step": ms_e2e,
                 "h2d_bytes_per_step": 2 * T * d * 2, "d2h_bytes_per_step": 2 * T * d * 2},
         "roofline": roof,

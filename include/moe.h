@@ -54,6 +54,15 @@
  * The exact (unpadded) numbering is reported as well: offsets[e] is the exclusive prefix sum of
  * the kept counts and row_of_slot[t,j] = offsets[e] + q (or -1 when dropped).
  *
+ * Kept activations (MoEBlaze, Methodology item 2: selective checkpointing, here with an adjustable
+ * granularity).  By default the backward recomputes the SwiGLU pre-activations a = x W_gate^T and
+ * b = x W_up^T from x_perm.  With keep_rows > 0, the forward also writes a and b (bf16) of the
+ * first keep_rows expert-ordered rows (rounded down to a multiple of 256, at most all rows) into
+ * the workspace, and the backward takes them from there instead of recomputing those rows:
+ * 2 * d_ff * 2 bytes kept per row buy 4 * d_model * d_ff FLOP per row.  The workspace size does
+ * not change (the kept rows reuse backward buffers); moe_expert_ffn_fwd and moe_layer_fwd must then
+ * be followed by the matching backward on the same workspace before anything else uses it.
+ *
  * Workspace.  Size it with moe_workspace_size(), zero its header once with moe_workspace_init(),
  * and pass the same workspace to every call of one layer instance.  moe_dispatch leaves the
  * routing tables in it that moe_expert_ffn_fwd/bwd, moe_combine and moe_combine_bwd read; the
@@ -97,6 +106,8 @@ typedef struct {
     int32_t n_shared;          /* S always-on shared experts */
     int32_t renorm;            /* 1: gates renormalised over the k selected */
     float capacity_factor;     /* cf > 0: capacity ceil(cf*T*k/E) per expert; <= 0: dropless */
+    int32_t keep_rows;         /* >= 0: expert-ordered rows whose gate/up pre-activations the forward
+                                * keeps for the backward (see "Kept activations"); 0 recomputes all */
 } moe_config_t;
 
 typedef uint16_t moe_bf16;                 /* raw bf16 bit pattern */

@@ -29,7 +29,7 @@ moe_status_t make_cfg(const moe_config_t* in, Cfg* c) {
   if (m.T < 1 || m.T > (1 << 20) || m.E < 1 || m.E > kMaxE || m.k < 1 || m.k > m.E ||
       m.n_shared < 0 || m.n_shared > kMaxS || m.d_model < 64 || m.d_ff < 64 ||
       m.d_model > 16384 || m.d_ff > 16384 || (m.d_model % 64) != 0 || (m.d_ff % 64) != 0 ||
-      (int64_t)m.T * m.k > (int64_t)1 << 24 || !(m.capacity_factor == m.capacity_factor))
+      (int64_t)m.T * m.k > (int64_t)1 << 24 || !(m.capacity_factor == m.capacity_factor) || m.keep_rows < 0)
     return MOE_ERR_INVALID_ARG;
   c->T = m.T;
   c->d = m.d_model;
@@ -39,6 +39,7 @@ moe_status_t make_cfg(const moe_config_t* in, Cfg* c) {
   c->S = m.n_shared;
   c->G = m.E + m.n_shared;
   c->renorm = m.renorm ? 1 : 0;
+  c->keep = m.keep_rows / kRowTile * kRowTile;   // clamped to the row capacity by make_layout users
   if (m.capacity_factor > 0.f) {
     const double cap = std::ceil((double)m.capacity_factor * (double)m.T * (double)m.k / (double)m.E);
     c->C = cap >= (double)INT_MAX ? INT_MAX : (int)cap;
@@ -179,7 +180,7 @@ const char* const kKernelNames[kKCount] = {
     "route_fwd", "dispatch_scan", "dispatch_gather", "gemm_gate_up_swiglu", "gemm_down",
     "combine", "gemm_bwd_recompute_swiglu", "gemm_wgrad", "gemm_dgrad_x", "dgates_reduce",
     "router_dlogits", "router_dwr", "router_reduce", "combine_bwd", "gemm_bwd_dgrad_down",
-    "gemm_router_dx"};
+    "gemm_router_dx", "swiglu_bwd_kept"};
 
 struct Profiler {
   std::mutex mu;
@@ -273,8 +274,8 @@ moe_status_t do_ffn_bwd(const Cfg& c, const Ws& w, const uint16_t* x_perm, const
   b.Wd = Wd;
   b.dh = w.at<uint16_t>(w.L.buf_f3);
   b.dA = w.at<uint16_t>(w.L.buf_f0);
-  b.dB = w.at<uint16_t>(w.L.buf_f1);
-  b.Hg = w.at<uint16_t>(w.L.buf_f2);
+  b.dB = w.at<uint16_t>(w.L.buf_f1);   // holds the kept a of rows [0, c.keep) until the backward
+  b.Hg = w.at<uint16_t>(w.L.buf_f2);   // holds the kept b likewise
   b.dg_part = w.at<float>(w.L.dg_part);
   b.dx_perm = dx_perm;
   b.dWg = dWg;
@@ -441,7 +442,8 @@ moe_status_t moe_expert_ffn_fwd(const moe_config_t* cfg, const moe_bf16* x_perm,
   Ws w;
   MOE_TRY(get_ws(c, ws, ws_bytes, &w));
   MOE_TRY(check_device());
-  FfnFwdArgs a{x_perm, W_gate, W_up, W_down, w.at<uint16_t>(w.L.buf_f0), o_perm, w.hdr(), w.tabs()};
+  FfnFwdArgs a{x_perm, W_gate, W_up, W_down, w.at<uint16_t>(w.L.buf_f0), o_perm, w.hdr(), w.tabs(),
+               w.at<uint16_t>(w.L.buf_f1), w.at<uint16_t>(w.L.buf_f2)};
   MOE_CUDA(launch_ffn_fwd(c, w.L, a, stream));
   return MOE_OK;
 }
@@ -529,7 +531,8 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const moe_bf16* x, const flo
   MOE_TRY(do_dispatch(c, w, idx, x, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, x_perm,
                       nullptr, stream));
   uint16_t* o_perm = w.at<uint16_t>(w.L.buf_d1);
-  FfnFwdArgs fa{x_perm, W_gate, W_up, W_down, w.at<uint16_t>(w.L.buf_f0), o_perm, w.hdr(), w.tabs()};
+  FfnFwdArgs fa{x_perm, W_gate, W_up, W_down, w.at<uint16_t>(w.L.buf_f0), o_perm, w.hdr(), w.tabs(),
+                w.at<uint16_t>(w.L.buf_f1), w.at<uint16_t>(w.L.buf_f2)};
   MOE_CUDA(launch_ffn_fwd(c, w.L, fa, stream));
   CombineArgs ca{o_perm, gates, y, w.tabs(), w.at<int32_t>(w.L.prow_of_slot)};
   MOE_CUDA(launch_combine(c, ca, stream));

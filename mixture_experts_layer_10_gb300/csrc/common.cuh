@@ -78,6 +78,7 @@ struct Layout {
 struct Cfg {               // validated configuration with derived sizes
   int T, d, f, E, k, S, G, renorm;
   int C;                   // capacity (INT32_MAX when dropless)
+  int keep;                // rows with kept a, b: keep_rows rounded down to kRowTile (clamped by the layout)
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -120,7 +121,8 @@ moe_status_t cuda_status(cudaError_t e);          // MOE_OK or MOE_ERR_CUDA (cle
 // with prof_mark(id, s, true/false), which records CUDA events on the launching stream.
 enum KernelId : int {
   kKRoute = 0, kKScan, kKGather, kKGateUp, kKDown, kKCombine, kKBwdFused, kKWgrad, kKDgradX,
-  kKDgates, kKRouterDlogits, kKRouterDwr, kKRouterReduce, kKCombineBwd, kKBwdDh, kKRouterDx, kKCount
+  kKDgates, kKRouterDlogits, kKRouterDwr, kKRouterReduce, kKCombineBwd, kKBwdDh, kKRouterDx, kKSwigluKept,
+  kKCount
 };
 void prof_mark(int id, cudaStream_t s, bool begin);
 
@@ -196,6 +198,7 @@ cudaError_t launch_dgates(const Cfg& c, const Layout& L, const DgatesArgs& a, cu
 struct FfnFwdArgs {
   const uint16_t* x_perm; const uint16_t* Wg; const uint16_t* Wu; const uint16_t* Wd;
   uint16_t* h; uint16_t* o_perm; Hdr* hdr; const Tables* tabs;
+  uint16_t* a_keep; uint16_t* b_keep;   // [rows, d_ff] bf16: a, b of the first c.keep rows
 };
 cudaError_t launch_ffn_fwd(const Cfg& c, const Layout& L, const FfnFwdArgs& a, cudaStream_t s);
 
@@ -206,5 +209,8 @@ struct FfnBwdArgs {
   uint16_t* dWg; uint16_t* dWu; uint16_t* dWd; Hdr* hdr; const Tables* tabs;
 };
 cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, cudaStream_t s);
+// SwiGLU backward of the kept rows [0, c.keep): a is read from a.dB and b from a.Hg (where the
+// forward kept them), dh' from a.dh; writes dA, dB, Hg (in place) and the rows' gate partials.
+cudaError_t launch_swiglu_bwd_kept(const Cfg& c, const Layout& L, const FfnBwdArgs& a, cudaStream_t s);
 
 }  // namespace moe

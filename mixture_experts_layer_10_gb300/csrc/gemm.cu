@@ -206,13 +206,18 @@ __device__ __forceinline__ void mma_kk_bmn(uint32_t sa, uint32_t dt, uint32_t id
 
 // H = silu(X Wg^T) * (X Wu^T).  B = [Wg rows n0..n0+127; Wu rows n0..n0+127]: the even CTA loads
 // the Wg half and the odd CTA the Wu half, so TMEM columns 0-127 hold the gate and 128-255 the up
-// projection of the same 128 hidden units.
-struct FwdGateUp : PairDefaults {
+// projection of the same 128 hidden units.  kKeep: pair tiles below keep_rows also store a and b
+// (bf16) for the backward, from triplets of staging boxes (H, a, b; two triplets per warp, five
+// pipeline stages to make room).
+template <bool kKeep>
+struct FwdGateUpT : PairDefaults {
   static constexpr int kId = kKGateUp;
   static constexpr int kEpiWarps = 4;
+  static constexpr int kStages = kKeep ? 5 : 6;
+  static constexpr uint32_t kEpiWarpBytes = kKeep ? 6 * 2048 : 2 * 2048;
   struct Params {
-    CUtensorMap tmX, tmWg, tmWu, tmH;
-    int f, d, nt;
+    CUtensorMap tmX, tmWg, tmWu, tmH, tmA, tmB;
+    int f, d, nt, keep_rows;
     Hdr* hdr;
     const Tables* tabs;
   };
@@ -233,6 +238,7 @@ struct FwdGateUp : PairDefaults {
   __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int, int, uint8_t* ebuf) {
     const int lane = row & 31;
     const int y = j.m0 + (row & ~31);
+    const bool keep = kKeep && y < p.keep_rows;   // whole pair tiles: keep_rows is a multiple of 256
     epi_begin(lane);
 #pragma unroll 1
     for (int c = 0; c < 128; c += 32) {
@@ -249,13 +255,41 @@ struct FwdGateUp : PairDefaults {
         const float h1 = a1 / (1.f + __expf(-a1)) * __uint_as_float(ub[2 * i + 1]);
         pk[i] = pack_bf16(h0, h1);
       }
-      uint8_t* box = claim_box(ebuf, c / 32, lane);
+      if (!kKeep) {
+        uint8_t* box = claim_box(ebuf, c / 32, lane);
+        stage_box(box, lane, pk);
+        store_box_2d(&p.tmH, box, lane, j.n0 + c, y);
+        continue;
+      }
+      const int i = c / 32;
+      if (i >= 2) {   // the triplet used two pieces ago has been read
+        if (lane == 0) bulk_wait_read<1>();
+        __syncwarp();
+      }
+      uint8_t* box = ebuf + (i & 1) * 3 * kEpiBox;
       stage_box(box, lane, pk);
-      store_box_2d(&p.tmH, box, lane, j.n0 + c, y);
+      if (keep) {
+        uint32_t pa[16], pb[16];
+        pack32(ga, pa);
+        pack32(ub, pb);
+        stage_box(box + kEpiBox, lane, pa);
+        stage_box(box + 2 * kEpiBox, lane, pb);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&p.tmH, box, j.n0 + c, y);
+        if (keep) {
+          tma_store_2d(&p.tmA, box + kEpiBox, j.n0 + c, y);
+          tma_store_2d(&p.tmB, box + 2 * kEpiBox, j.n0 + c, y);
+        }
+        bulk_commit();
+      }
     }
   }
   __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
 };
+using FwdGateUp = FwdGateUpT<false>;
 
 // Shared by FwdDown, BwdDh and DgradX: this warp's 32 rows of the fp32 accumulator [128 x 256] ->
 // bf16 boxes of the output [rows, ncols] at row y (the warp's first row) and columns n0 + c.
@@ -349,13 +383,15 @@ struct BwdFused : PairDefaults {
     const uint16_t* DH;
     const float* gate_of_prow;
     float* dg_part;
-    int f, d, nt, ndg;
+    int f, d, nt, ndg, keep_rows;   // pair tiles below keep_rows come from the kept a, b instead
     Hdr* hdr;
     const Tables* tabs;
   };
   __device__ static int num_tiles(const Params& p, const SegSmem& s) { return s.n_mtiles * p.nt; }
   __device__ static Job job(const Params& p, const SegSmem& s, int t) {
-    return row_job(s, t, p.nt, 128, p.d / kBK);
+    Job j = row_job(s, t, p.nt, 128, p.d / kBK);
+    if (j.m0 < p.keep_rows) j.kiters = 0;
+    return j;
   }
   __device__ static void prefetch(const Params& p) {
     tma_prefetch(&p.tmX); tma_prefetch(&p.tmWg); tma_prefetch(&p.tmWu);
@@ -1402,19 +1438,33 @@ cudaError_t launch_pair(const typename P::Params& p, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_ffn_fwd(const Cfg& c, const Layout& L, const FfnFwdArgs& a, cudaStream_t s) {
+namespace {
+
+template <bool kKeep>
+cudaError_t launch_gate_up(const Cfg& c, const Layout& L, const FfnFwdArgs& a, int keep, cudaStream_t s) {
   const uint64_t rows = (uint64_t)L.rows;
-  FwdGateUp::Params p1{};
+  typename FwdGateUpT<kKeep>::Params p1{};
   if (!map_2d(&p1.tmX, a.x_perm, c.d, rows, 64, 128) ||
       !map_3d(&p1.tmWg, a.Wg, c.d, c.f, c.G, 64, 128) || !map_3d(&p1.tmWu, a.Wu, c.d, c.f, c.G, 64, 128) ||
       !map_2d(&p1.tmH, a.h, c.f, rows, 32, 32))
     return cudaErrorInvalidValue;
+  if (kKeep && (!map_2d(&p1.tmA, a.a_keep, c.f, rows, 32, 32) || !map_2d(&p1.tmB, a.b_keep, c.f, rows, 32, 32)))
+    return cudaErrorInvalidValue;
   p1.f = c.f;
   p1.d = c.d;
   p1.nt = (c.f + 127) / 128;
+  p1.keep_rows = keep;
   p1.hdr = a.hdr;
   p1.tabs = a.tabs;
-  cudaError_t e = launch_pair<FwdGateUp>(p1, s);
+  return launch_pair<FwdGateUpT<kKeep>>(p1, s);
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_fwd(const Cfg& c, const Layout& L, const FfnFwdArgs& a, cudaStream_t s) {
+  const uint64_t rows = (uint64_t)L.rows;
+  const int keep = (int)std::min<int64_t>(c.keep, L.rows);
+  cudaError_t e = keep > 0 ? launch_gate_up<true>(c, L, a, keep, s) : launch_gate_up<false>(c, L, a, 0, s);
   if (e != cudaSuccess) return e;
   FwdDown::Params p2{};
   if (!map_2d(&p2.tmH, a.h, c.f, rows, 64, 128) || !map_3d(&p2.tmWd, a.Wd, c.f, c.d, c.G, 64, 128) ||
@@ -1441,6 +1491,11 @@ cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, c
   p2.tabs = a.tabs;
   cudaError_t e = launch_pair<BwdDh>(p2, s);
   if (e != cudaSuccess) return e;
+  const int keep = (int)std::min<int64_t>(c.keep, L.rows);
+  if (keep > 0) {   // rows whose a, b the forward kept: an element-wise SwiGLU backward
+    e = launch_swiglu_bwd_kept(c, L, a, s);
+    if (e != cudaSuccess) return e;
+  }
 
   BwdFused::Params p3{};
   if (!map_2d(&p3.tmX, a.x_perm, c.d, rows, 64, 128) || !map_3d(&p3.tmWg, a.Wg, c.d, c.f, c.G, 64, 128) ||
@@ -1454,6 +1509,7 @@ cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, c
   p3.d = c.d;
   p3.nt = L.ntf;
   p3.ndg = L.ndg;
+  p3.keep_rows = keep;
   p3.hdr = a.hdr;
   p3.tabs = a.tabs;
   e = launch_pair<BwdFused>(p3, s);

@@ -42,6 +42,23 @@ def run_layer(moe, c, inp, buf=None):
 def test_layer_fwd_bwd(moe, name):
     c, inp, L = case(name)
     out, _ = run_layer(moe, c, inp)
+    check_layer(c, L, out)
+
+
+# Kept activations: the forward stores a, b of the leading expert-ordered rows and the backward
+# uses them instead of recomputing (all rows, or a prefix that ends inside a segment).
+@pytest.mark.parametrize("name,keep", [("ragged_mixtral", -1), ("ragged_mixtral", 256), ("deepseek_small", -1),
+                                       ("deepseek_small", 768), ("gptoss_small", 512), ("qwen_small", -1),
+                                       ("router_e96_k8", 256), ("tiny", 100)])
+def test_layer_kept_activations(moe, name, keep):
+    c, inp, L = case(name)
+    c = dict(c)
+    c["keep_rows"] = moe.moe_perm_rows(moe.config_from(c)) if keep < 0 else keep
+    out, _ = run_layer(moe, c, inp)
+    check_layer(c, L, out)
+
+
+def check_layer(c, L, out):
     R = L.routing()
     same = check_routing(from_dev(out["idx"]), from_dev(out["gates"]), R, c["k"])
     y_ref, _ = L.forward()
