@@ -386,11 +386,45 @@ def main():
     barrier()
     ms_e2e = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
 
+    # The same device-resident step captured once in a CUDA graph and replayed (launch overhead
+    # removed); reported beside the primary, stream-launched number.
+    graph = {"ms_per_step": None}
+    try:
+        g = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            step()
+        stream.wait_stream(side)
+        with torch.cuda.graph(g):
+            step()
+        g.replay()
+        torch.cuda.synchronize()
+        barrier()
+        ev0.record(stream)
+        for _ in range(args.steps):
+            g.replay()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        ms_graph = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
+        graph = {"ms_per_step": ms_graph, "value": world * T / (ms_graph / 1000.0), "unit": "tokens/s"}
+        del g
+    except RuntimeError as err:   # capture unsupported here: say why, keep the stream numbers
+        graph = {"ms_per_step": None, "note": str(err).splitlines()[0][:200]}
+    status = moe.moe_check_error(buf.ws)
+    if status != 0:
+        raise RuntimeError(f"layer failed in the graph replays: {moe.moe_status_string(status)}")
+
     pk = peaks()
     # Denominator for the tensor-bound kernels: the burst cuBLAS figure when the SM clock held at
     # its maximum through the timed region (as during the burst measurement), else the sustained one.
     at_max = clk.get("sm_mhz") and clk.get("sm_max_mhz") and clk["sm_mhz"] >= 0.97 * clk["sm_max_mhz"]
     tensor_peak = pk["tensor_burst"] if at_max else pk["tensor"]
+    # the analytical resource model's roofline prediction for this step (same peaks)
+    from mixture_experts_layer_10_gb300 import resource_model
+    pred = resource_model.predict_ms(cfg, tensor_peak, pk["hbm"], N=n_kept, kept_rows=kept_real)
+    model_line = {"predicted_ms": pred["step_ms"], "measured_over_predicted": ms / pred["step_ms"],
+                  "memory_bytes": resource_model.memory(cfg)}
     tensor_kind = ("bf16_tflops (burst, %s): SM clock held at max in the timed region" if at_max else
                    "bf16_tflops_sustained (%s): SM clock below max in the timed region") % pk["source"]
     kernels = {}
@@ -447,6 +481,8 @@ def main():
                    "rows_per_step": N, "load_max_over_mean": load_max_over_mean,
                    "keep_rows": keep, "kept_rows": kept_real,
                    "kept_activation_bytes": keep * f * 2 * 2},
+        "cuda_graph": graph,
+        "model": model_line,
         "e2e": {"value": world * T / (ms_e2e / 1000.0), "unit": "tokens/s", "ms_per_step": ms_e2e,
                 "h2d_bytes_per_step": 2 * T * d * 2, "d2h_bytes_per_step": 2 * T * d * 2},
         "roofline": roof,

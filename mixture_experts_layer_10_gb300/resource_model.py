@@ -1,0 +1,99 @@
+"""Analytical resource model of one MoE layer step (forward + backward) on one GPU.
+
+Piper's explainer (planner section) predicts each stage's memory and compute from the model shape
+and checks the prediction against measurement; this is the same idea for the single-GPU layer
+built here.  From the configuration alone (and, optionally, the number of routed rows the experts
+really see) it gives:
+
+* memory: the workspace and `saved` bytes the library asks for, the caller's tensors, and the
+  activation bytes kept between forward and backward;
+* work per kernel: FLOPs for the tensor-core kernels, algorithmic HBM bytes for the gather/combine
+  kernels (the same definitions bench.py reports against);
+* a roofline time per kernel, max(FLOPs / tensor rate, bytes / HBM rate) plus a fixed launch cost,
+  summed into a predicted step time that bench.py sets beside the measured one.
+
+Host arithmetic only: nothing here runs on the GPU or calls the library.
+"""
+from __future__ import annotations
+
+import math
+
+ROW_TILE = 256          # expert segments are padded to this many rows (include/moe.h)
+LAUNCH_US = 4.0         # fixed cost per kernel launch on the stream, microseconds
+
+
+def padded_rows(T: int, k: int, E: int, S: int) -> int:
+    """Row capacity of the expert-ordered buffers: every routed segment rounded up to the tile, in
+    the worst case E - 1 extra tiles' worth of padding, plus S shared segments of T rows."""
+    routed = math.ceil((T * k + (ROW_TILE - 1) * E) / ROW_TILE) * ROW_TILE
+    return routed + S * math.ceil(T / ROW_TILE) * ROW_TILE
+
+
+def memory(cfg: dict) -> dict:
+    """Bytes of device memory one layer instance needs, by owner."""
+    T, d, f, E, k, S = cfg["T"], cfg["d"], cfg["f"], cfg["E"], cfg["k"], cfg.get("S", 0)
+    G = E + S
+    Ep = math.ceil(E / 64) * 64
+    rows = padded_rows(T, k, E, S)
+    ndg = 2 * math.ceil(f / 128)
+    per_row = (2 * d + 4 * f + d) * 2 + (4 + 4 + 4 * ndg)   # x/dY/O planes, four d_ff planes, metadata
+    workspace = (rows * per_row + T * k * 12 + T * E * 4 + T * Ep * 2 + 4 * d * Ep * 2
+                 + math.ceil(T * k / 4096) * E * 4)
+    keep = min(cfg.get("keep_rows", 0) // ROW_TILE * ROW_TILE, rows)
+    return {
+        "padded_rows": rows,
+        "workspace": workspace,
+        "saved": 8 * T * k,
+        "weights": 3 * G * d * f * 2 + d * E * 4,
+        "weight_grads": 3 * G * d * f * 2 + d * E * 4,
+        "token_tensors": 4 * T * d * 2,   # x, y, dy, dx
+        "kept_activations": keep * f * 2 * 2,
+    }
+
+
+def work(cfg: dict, N: int | None = None, kept_rows: int = 0) -> dict:
+    """FLOPs and algorithmic HBM bytes per kernel of one forward + backward step.
+
+    N is the number of routed rows the experts see (kept assignments); by default T*k (dropless).
+    kept_rows are rows whose a, b the forward keeps, which the recompute GEMM then skips."""
+    T, d, f, E, k, S = cfg["T"], cfg["d"], cfg["f"], cfg["E"], cfg["k"], cfg.get("S", 0)
+    N = T * k if N is None else N
+    R = N + S * T                                      # rows the experts see
+    Ep = math.ceil(E / 64) * 64
+    tc_router = E <= 128 and k <= 8
+    out = {
+        "route_fwd": {"flops": 2 * T * d * (3 * Ep if tc_router else E), "bytes": T * d * 2},
+        "dispatch_gather": {"flops": 0, "bytes": 3 * (T + R) * d * 2 + 36 * T * k},
+        "gemm_gate_up_swiglu": {"flops": 4 * R * d * f, "bytes": 0},
+        "gemm_down": {"flops": 2 * R * d * f, "bytes": 0},
+        "combine": {"flops": 0, "bytes": (R + T) * d * 2 + 8 * T * k},
+        "gemm_bwd_dgrad_down": {"flops": 2 * R * d * f, "bytes": 0},
+        "gemm_bwd_recompute_swiglu": {"flops": 4 * (R - kept_rows) * d * f, "bytes": 0},
+        "gemm_wgrad": {"flops": 6 * R * d * f, "bytes": 0},
+        "gemm_dgrad_x": {"flops": 4 * R * d * f, "bytes": 0},
+        "router_dlogits": {"flops": 2 * T * d * (3 * Ep if tc_router else E), "bytes": T * d * 2},
+        "router_dwr": {"flops": 2 * T * d * Ep, "bytes": T * d * 2},
+        "gemm_router_dx": {"flops": 2 * T * d * Ep, "bytes": T * d * 2},
+        "combine_bwd": {"flops": 0, "bytes": (R + 2 * T) * d * 2 + 4 * T * k},
+    }
+    if kept_rows:
+        out["swiglu_bwd_kept"] = {"flops": 0, "bytes": 6 * kept_rows * f * 2}
+    return out
+
+
+def gemm_flops(cfg: dict, N: int | None = None, kept_rows: int = 0) -> int:
+    """Expert GEMM FLOPs of one step: 22 (N + S T) d f with full recompute."""
+    return sum(v["flops"] for n, v in work(cfg, N, kept_rows).items() if n.startswith("gemm_")
+               and n != "gemm_router_dx")
+
+
+def predict_ms(cfg: dict, tensor_tflops: float, hbm_gbs: float, N: int | None = None,
+               kept_rows: int = 0, launches: int = 17) -> dict:
+    """Roofline time per kernel and the step total, in milliseconds."""
+    per = {}
+    for name, w in work(cfg, N, kept_rows).items():
+        t_tc = w["flops"] / (tensor_tflops * 1e12)
+        t_hbm = w["bytes"] / (hbm_gbs * 1e9)
+        per[name] = 1e3 * max(t_tc, t_hbm)
+    total = sum(per.values()) + launches * LAUNCH_US / 1e3
+    return {"step_ms": total, "per_kernel_ms": per}
