@@ -28,6 +28,9 @@ CASES = {
     # the fp32 SIMT router: more than 128 experts, and more than 8 experts per token
     "router_simt_e160": dict(T=300, d=128, E=160, k=4, f=64, S=0, renorm=0, cf=0.0, zipf=True),
     "router_simt_k10": dict(T=200, d=192, E=24, k=10, f=64, S=0, renorm=1, cf=0.0, zipf=False),
+    # limits: the most routed experts (256), and the most shared experts (8) at the narrowest widths
+    "max_experts": dict(T=700, d=64, E=256, k=2, f=64, S=0, renorm=0, cf=0.0, zipf=False),
+    "max_shared": dict(T=300, d=64, E=4, k=1, f=64, S=8, renorm=1, cf=0.0, zipf=False),
 }
 
 FAST = ["tiny", "ragged_mixtral", "deepseek_small", "qwen_small", "gptoss_small"]
