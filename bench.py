@@ -341,7 +341,10 @@ def main():
 
     # End to end through the C ABI with host buffers: every step copies its inputs (x, dy) from
     # pinned host memory and its results (y, dx) back.  A copy stream overlaps step i's compute
-    # with step i+1's H2D and step i-1's D2H (double-buffered device inputs and outputs).
+    # with step i+1's H2D and step i-1's D2H (double-buffered device inputs and outputs).  Compute
+    # runs on a stream of its own: work on the legacy default stream would serialise with every
+    # other blocking stream, the copy stream included.
+    cstream = torch.cuda.Stream()
     x_h = torch.empty(T, d, dtype=torch.bfloat16, pin_memory=True).copy_(x.cpu())
     dy_h = torch.empty_like(x_h).copy_(dy.cpu())
     y_h, dx_h = torch.empty_like(x_h), torch.empty_like(x_h)
@@ -354,16 +357,17 @@ def main():
     computed = [torch.cuda.Event(), torch.cuda.Event()]
 
     def e2e_run(n):
-        copy_stream.wait_stream(stream)        # the first copy starts inside the timed region
+        copy_stream.wait_stream(cstream)       # the first copy starts inside the timed region
         with torch.cuda.stream(copy_stream):
             xin[0].copy_(x_h, non_blocking=True)
             dyin[0].copy_(dy_h, non_blocking=True)
             loaded[0].record(copy_stream)
         for i in range(n):
             b = i % 2
-            stream.wait_event(loaded[b])
-            step(xin[b], dyin[b], yout[b], dxout[b])
-            computed[b].record(stream)
+            cstream.wait_event(loaded[b])
+            with torch.cuda.stream(cstream):
+                step(xin[b], dyin[b], yout[b], dxout[b])
+            computed[b].record(cstream)
             with torch.cuda.stream(copy_stream):
                 if i + 1 < n:
                     if i >= 1:
@@ -374,14 +378,15 @@ def main():
                 copy_stream.wait_event(computed[b])
                 y_h.copy_(yout[b], non_blocking=True)
                 dx_h.copy_(dxout[b], non_blocking=True)
-        stream.wait_stream(copy_stream)
+        cstream.wait_stream(copy_stream)
 
+    cstream.wait_stream(stream)
     e2e_run(2)
     barrier()
     torch.cuda.synchronize()
-    ev0.record(stream)
+    ev0.record(cstream)
     e2e_run(args.steps)
-    ev1.record(stream)
+    ev1.record(cstream)
     torch.cuda.synchronize()
     barrier()
     ms_e2e = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
