@@ -203,6 +203,27 @@ moe_status_t moe_router_bwd(const moe_config_t* cfg, const moe_bf16* x, const fl
 moe_status_t moe_combine_bwd(const moe_config_t* cfg, const moe_bf16* dx_perm, const float* dlogits,
                              const float* W_r, moe_bf16* dx, void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* FP8 experts, first step: quantised expert inputs (the MoEBlaze summary names mixed-precision and
+ * quantised experts as future work; the format is this library's reading).  Format: OCP FP8 E4M3
+ * (max 448, no infinities), one fp32 scale per row.
+ *
+ * moe_quantize_rows_e4m3: src [rows, cols] bf16 -> codes [rows, cols] uint8 and scales [rows]
+ * fp32, with scale = amax / 448 over the row (1 for an all-zero row) and code = e4m3(v / scale),
+ * both in fp32, rounded to nearest even and saturated.  cols a multiple of 16; 16-byte-aligned
+ * pointers.  Used for x_perm rows and for the rows (output channels) of W_gate and W_up. */
+moe_status_t moe_quantize_rows_e4m3(const moe_bf16* src, int64_t rows, int32_t cols, uint8_t* codes,
+                                    float* scales, moe_stream_t stream);
+
+/* The gate/up projection and SwiGLU of moe_expert_ffn_fwd with e4m3 operands on the tensor cores
+ * (kind::f8f6f4): h = silu(a) * b, a = s_x s_g (q_x . q_g), b = s_x s_u (q_x . q_u), accumulated in
+ * fp32.  x8 / x_scale: the quantised x_perm rows [moe_perm_rows(), d_model] / [moe_perm_rows()]
+ * (pad rows: zero codes); wg8, wu8 [E+S, d_ff, d_model] codes with wg_scale, wu_scale [E+S, d_ff].
+ * Writes h [moe_perm_rows(), d_ff] bf16.  Uses the tables of moe_dispatch in ws. */
+moe_status_t moe_gate_up_fp8(const moe_config_t* cfg, const uint8_t* x8, const float* x_scale,
+                             const uint8_t* wg8, const float* wg_scale, const uint8_t* wu8,
+                             const float* wu_scale, moe_bf16* h, void* ws, size_t ws_bytes,
+                             moe_stream_t stream);
+
 /* The whole forward: route, dispatch, expert FFN, combine.  Fills `saved` (idx and gates only;
  * activations are recomputed in backward). */
 moe_status_t moe_layer_fwd(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,

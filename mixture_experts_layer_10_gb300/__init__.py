@@ -25,7 +25,8 @@ EXPORTS = ("moe_workspace_size", "moe_perm_rows", "moe_workspace_init", "moe_rou
            "moe_dispatch_noalloc",
            "moe_expert_ffn_fwd", "moe_combine", "moe_expert_ffn_bwd", "moe_router_bwd",
            "moe_combine_bwd", "moe_layer_fwd", "moe_layer_bwd", "moe_check_error",
-           "moe_debug_inject", "moe_profile_enable", "moe_profile_read", "moe_status_string")
+           "moe_debug_inject", "moe_profile_enable", "moe_profile_read", "moe_status_string",
+           "moe_quantize_rows_e4m3", "moe_gate_up_fp8")
 
 
 class moe_config_t(ctypes.Structure):
@@ -68,6 +69,8 @@ def load(path: str | None = None):
         "moe_expert_ffn_bwd": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
         "moe_router_bwd": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
         "moe_combine_bwd": [cfgp, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+        "moe_quantize_rows_e4m3": [_P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P],
+        "moe_gate_up_fp8": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
         "moe_layer_fwd": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
         "moe_layer_bwd": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                           ctypes.c_size_t, _P],
@@ -190,6 +193,18 @@ def moe_router_bwd(cfg, x, W_r, b_r, idx, gates, dgates, dlogits, dW_r, db_r, ws
 def moe_combine_bwd(cfg, dx_perm, dlogits, W_r, dx, ws, stream=None):
     _call("moe_combine_bwd", ctypes.byref(cfg), _ptr(dx_perm), _ptr(dlogits), _ptr(W_r), _ptr(dx),
           _ptr(ws), ws.numel(), _stream(stream))
+
+
+def moe_quantize_rows_e4m3(src, codes, scales, stream=None):
+    """src [rows, cols] bf16 -> codes [rows, cols] uint8, scales [rows] fp32."""
+    rows, cols = src.shape[0], src.shape[-1]
+    _call("moe_quantize_rows_e4m3", _ptr(src), int(src.numel() // cols) if rows else 0, int(cols), _ptr(codes),
+          _ptr(scales), _stream(stream))
+
+
+def moe_gate_up_fp8(cfg, x8, x_scale, wg8, wg_scale, wu8, wu_scale, h, ws, stream=None):
+    _call("moe_gate_up_fp8", ctypes.byref(cfg), _ptr(x8), _ptr(x_scale), _ptr(wg8), _ptr(wg_scale), _ptr(wu8),
+          _ptr(wu_scale), _ptr(h), _ptr(ws), ws.numel(), _stream(stream))
 
 
 def moe_layer_fwd(cfg, x, W_r, b_r, W_gate, W_up, W_down, y, saved, ws, stream=None):

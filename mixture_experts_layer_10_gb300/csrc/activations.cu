@@ -1,3 +1,5 @@
+// Element-wise kernels: the SwiGLU backward of kept rows, and the FP8 row quantiser.
+//
 // SwiGLU backward of the rows whose gate/up pre-activations the forward kept (MoEBlaze,
 // Methodology item 2: the checkpointing choice, here made per row range instead of all-or-nothing).
 //
@@ -10,6 +12,8 @@
 // reduction expects.  dB and Hg overwrite the kept a and b in place: each element is read before
 // it is written, by the same thread.
 #include <algorithm>
+
+#include <cuda_fp8.h>
 
 #include "common.cuh"
 
@@ -68,7 +72,54 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) swiglu_bwd_kept_kernel(
   }
 }
 
+// FP8 rows (the quantisation step of the e4m3 expert GEMMs): per row, amax over the row, scale =
+// amax / 448 in fp32 (1 for an all-zero row), codes = e4m3(v / scale) rounded to nearest even and
+// saturated.  A warp owns a row and reads it twice in 16-byte vectors (eight values).
+__global__ void __launch_bounds__(256) quantize_rows_e4m3_kernel(const uint16_t* __restrict__ src, int64_t rows,
+                                                                 int cols, uint8_t* __restrict__ codes,
+                                                                 float* __restrict__ scales) {
+  const int lane = threadIdx.x & 31;
+  const int nvec = cols / 8;
+  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
+  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
+    const uint4* row = reinterpret_cast<const uint4*>(src + r * cols);
+    float amax = 0.f;
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 u = row[v];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int m = 0; m < 4; ++m) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[m])), fabsf(bf16_hi(w[m]))));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    if (lane == 0) scales[r] = scale;
+    uint2* out = reinterpret_cast<uint2*>(codes + r * cols);
+    for (int v = lane; v < nvec; v += 32) {
+      const uint4 u = row[v];
+      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      uint32_t q[4];
+#pragma unroll
+      for (int m = 0; m < 4; ++m) {
+        const float2 f2 = make_float2(__fdiv_rn(bf16_lo(w[m]), scale), __fdiv_rn(bf16_hi(w[m]), scale));
+        q[m] = (uint32_t)__nv_cvt_float2_to_fp8x2(f2, __NV_SATFINITE, __NV_E4M3);   // .x in the low byte
+      }
+      out[v] = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+    }
+  }
+}
+
 }  // namespace
+
+cudaError_t launch_quantize_rows_e4m3(const uint16_t* src, int64_t rows, int cols, uint8_t* codes, float* scales,
+                                      cudaStream_t s) {
+  if (rows <= 0) return cudaSuccess;
+  const int64_t blocks64 = std::min<int64_t>((rows + 7) / 8, (int64_t)num_sms() * 16);
+  prof_mark(kKQuantE4m3, s, true);
+  quantize_rows_e4m3_kernel<<<(int)std::max<int64_t>(1, blocks64), 256, 0, s>>>(src, rows, cols, codes, scales);
+  prof_mark(kKQuantE4m3, s, false);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_swiglu_bwd_kept(const Cfg& c, const Layout& L, const FfnBwdArgs& a, cudaStream_t s) {
   const int keep = (int)std::min<int64_t>(c.keep, L.rows);

@@ -180,7 +180,7 @@ const char* const kKernelNames[kKCount] = {
     "route_fwd", "dispatch_scan", "dispatch_gather", "gemm_gate_up_swiglu", "gemm_down",
     "combine", "gemm_bwd_recompute_swiglu", "gemm_wgrad", "gemm_dgrad_x", "dgates_reduce",
     "router_dlogits", "router_dwr", "router_reduce", "combine_bwd", "gemm_bwd_dgrad_down",
-    "gemm_router_dx", "swiglu_bwd_kept"};
+    "gemm_router_dx", "swiglu_bwd_kept", "gemm_gate_up_fp8", "quantize_e4m3"};
 
 struct Profiler {
   std::mutex mu;
@@ -511,6 +511,31 @@ moe_status_t moe_combine_bwd(const moe_config_t* cfg, const moe_bf16* dx_perm, c
   MOE_TRY(get_ws(c, ws, ws_bytes, &w));
   MOE_TRY(check_device());
   return do_combine_bwd(c, w, dx_perm, dlogits, W_r, dx, stream);
+}
+
+moe_status_t moe_quantize_rows_e4m3(const moe_bf16* src, int64_t rows, int32_t cols, uint8_t* codes,
+                                    float* scales, moe_stream_t stream) {
+  MOE_NEED(rows >= 0 && cols > 0 && cols % 16 == 0 && rows <= ((int64_t)1 << 31));
+  MOE_NEED(rows == 0 || (src && codes && scales && aligned16(src) && aligned16(codes) && aligned16(scales)));
+  MOE_TRY(check_device());
+  MOE_CUDA(launch_quantize_rows_e4m3(src, rows, cols, codes, scales, stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_gate_up_fp8(const moe_config_t* cfg, const uint8_t* x8, const float* x_scale, const uint8_t* wg8,
+                             const float* wg_scale, const uint8_t* wu8, const float* wu_scale, moe_bf16* h,
+                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+  Cfg c;
+  MOE_TRY(make_cfg(cfg, &c));
+  MOE_NEED(x8 && x_scale && wg8 && wg_scale && wu8 && wu_scale && h);
+  MOE_NEED(aligned16(x8) && aligned16(x_scale) && aligned16(wg8) && aligned16(wg_scale) && aligned16(wu8) &&
+           aligned16(wu_scale) && aligned16(h));
+  Ws w;
+  MOE_TRY(get_ws(c, ws, ws_bytes, &w));
+  MOE_TRY(check_device());
+  GateUpFp8Args a{x8, x_scale, wg8, wg_scale, wu8, wu_scale, h, w.hdr(), w.tabs()};
+  MOE_CUDA(launch_gate_up_fp8(c, w.L, a, stream));
+  return MOE_OK;
 }
 
 moe_status_t moe_layer_fwd(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,

@@ -122,7 +122,7 @@ moe_status_t cuda_status(cudaError_t e);          // MOE_OK or MOE_ERR_CUDA (cle
 enum KernelId : int {
   kKRoute = 0, kKScan, kKGather, kKGateUp, kKDown, kKCombine, kKBwdFused, kKWgrad, kKDgradX,
   kKDgates, kKRouterDlogits, kKRouterDwr, kKRouterReduce, kKCombineBwd, kKBwdDh, kKRouterDx, kKSwigluKept,
-  kKCount
+  kKGateUpFp8, kKQuantE4m3, kKCount
 };
 void prof_mark(int id, cudaStream_t s, bool begin);
 
@@ -212,5 +212,15 @@ cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, c
 // SwiGLU backward of the kept rows [0, c.keep): a is read from a.dB and b from a.Hg (where the
 // forward kept them), dh' from a.dh; writes dA, dB, Hg (in place) and the rows' gate partials.
 cudaError_t launch_swiglu_bwd_kept(const Cfg& c, const Layout& L, const FfnBwdArgs& a, cudaStream_t s);
+
+// FP8 (e4m3) rows: codes [rows, cols] and one fp32 scale per row (amax / 448), from bf16 rows.
+cudaError_t launch_quantize_rows_e4m3(const uint16_t* src, int64_t rows, int cols, uint8_t* codes, float* scales,
+                                      cudaStream_t s);
+// H = silu(a) * b with a, b from e4m3 rows of x_perm and of W_gate / W_up and their row scales.
+struct GateUpFp8Args {
+  const uint8_t* x8; const float* xs; const uint8_t* wg8; const float* gs; const uint8_t* wu8;
+  const float* us; uint16_t* h; Hdr* hdr; const Tables* tabs;
+};
+cudaError_t launch_gate_up_fp8(const Cfg& c, const Layout& L, const GateUpFp8Args& a, cudaStream_t s);
 
 }  // namespace moe

@@ -291,6 +291,70 @@ struct FwdGateUpT : PairDefaults {
 };
 using FwdGateUp = FwdGateUpT<false>;
 
+// The gate/up projection with FP8 operands (tcgen05 kind::f8f6f4, e4m3): x_perm rows and W_gate /
+// W_up rows quantised per row (codes and an fp32 scale each), so a = s_x s_g (q_x . q_g) exactly
+// up to the fp32 accumulation.  Same pair tiling as FwdGateUp: a K block is 128 e4m3 values (the
+// same 128 bytes per row as 64 bf16), four K = 32 MMAs per block; the epilogue applies the row
+// scale and the output channel's scale before SwiGLU.
+struct FwdGateUp8 : PairDefaults {
+  static constexpr int kId = kKGateUpFp8;
+  static constexpr int kEpiWarps = 4;
+  static constexpr int kBK8 = 128;
+  static constexpr uint32_t kIdesc = idesc_e4m3(kPairM, 256);
+  struct Params {
+    CUtensorMap tmX, tmWg, tmWu, tmH;
+    const float *xs, *gs, *us;   // [rows] and [G, f] scales
+    int f, d, nt;
+    Hdr* hdr;
+    const Tables* tabs;
+  };
+  __device__ static int num_tiles(const Params& p, const SegSmem& s) { return s.n_mtiles * p.nt; }
+  __device__ static Job job(const Params& p, const SegSmem& s, int t) {
+    return row_job(s, t, p.nt, 128, (p.d + kBK8 - 1) / kBK8);
+  }
+  __device__ static void prefetch(const Params& p) {
+    tma_prefetch(&p.tmX); tma_prefetch(&p.tmWg); tma_prefetch(&p.tmWu);
+  }
+  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint32_t cbar, int rank) {
+    tma_load_2d_pair(st, &p.tmX, cbar, kit * kBK8, j.m0 + kBM * rank);
+    tma_load_3d_pair(st + kTileA, rank ? &p.tmWu : &p.tmWg, cbar, kit * kBK8, j.n0, j.seg);
+  }
+  __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      umma_f8_pair(dt, sdesc_kmajor(sa + kk * 32), sdesc_kmajor(sa + kTileA + kk * 32), kIdesc, (kit | kk) != 0);
+  }
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int, int, uint8_t* ebuf) {
+    const int lane = row & 31;
+    const int y = j.m0 + (row & ~31);
+    const float sx = p.xs[j.m0 + row];
+    const float* gs = p.gs + (size_t)j.seg * p.f + j.n0;
+    const float* us = p.us + (size_t)j.seg * p.f + j.n0;
+    epi_begin(lane);
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 32) {
+      if (j.n0 + c >= p.f) break;
+      uint32_t ga[32], ub[32];
+      tmem_ld32(ta + c, ga);
+      tmem_ld32(ta + 128 + c, ub);
+      tmem_ld_wait();
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float a0 = __uint_as_float(ga[2 * i]) * sx * gs[c + 2 * i];
+        const float a1 = __uint_as_float(ga[2 * i + 1]) * sx * gs[c + 2 * i + 1];
+        const float h0 = a0 / (1.f + __expf(-a0)) * (__uint_as_float(ub[2 * i]) * sx * us[c + 2 * i]);
+        const float h1 = a1 / (1.f + __expf(-a1)) * (__uint_as_float(ub[2 * i + 1]) * sx * us[c + 2 * i + 1]);
+        pk[i] = pack_bf16(h0, h1);
+      }
+      uint8_t* box = claim_box(ebuf, c / 32, lane);
+      stage_box(box, lane, pk);
+      store_box_2d(&p.tmH, box, lane, j.n0 + c, y);
+    }
+  }
+  __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
+};
+
 // Shared by FwdDown, BwdDh and DgradX: this warp's 32 rows of the fp32 accumulator [128 x 256] ->
 // bf16 boxes of the output [rows, ncols] at row y (the warp's first row) and columns n0 + c.
 __device__ __forceinline__ void store_acc_boxes(const CUtensorMap* map, int y, int n0, int ncols, uint32_t ta,
@@ -1384,6 +1448,32 @@ bool map_mn2_g(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 8-bit tensors (e4m3 codes) [rows, width] and [G, rows, width], boxes of 128 x 128 (x 1): 128-byte
+// rows with the 128-byte swizzle, the layout of a 64-wide bf16 box.
+bool map_u8_2d(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {width, rows};
+  const cuuint64_t strides[1] = {width};
+  const cuuint32_t box[2] = {128, 128};
+  const cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool map_u8_3d(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows, uint64_t G) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {width, rows, G};
+  const cuuint64_t strides[2] = {width, width * rows};
+  const cuuint32_t box[3] = {128, 128, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 3D bf16 tensor [G, rows, width] with a box of box_w x box_r x 1.
 bool map_3d(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows, uint64_t G,
             uint32_t box_w, uint32_t box_r) {
@@ -1547,6 +1637,23 @@ cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, c
   p5.hdr = a.hdr;
   p5.tabs = a.tabs;
   return launch_pair<DgradX>(p5, s);
+}
+
+cudaError_t launch_gate_up_fp8(const Cfg& c, const Layout& L, const GateUpFp8Args& a, cudaStream_t s) {
+  const uint64_t rows = (uint64_t)L.rows;
+  FwdGateUp8::Params p{};
+  if (!map_u8_2d(&p.tmX, a.x8, c.d, rows) || !map_u8_3d(&p.tmWg, a.wg8, c.d, c.f, c.G) ||
+      !map_u8_3d(&p.tmWu, a.wu8, c.d, c.f, c.G) || !map_2d(&p.tmH, a.h, c.f, rows, 32, 32))
+    return cudaErrorInvalidValue;
+  p.xs = a.xs;
+  p.gs = a.gs;
+  p.us = a.us;
+  p.f = c.f;
+  p.d = c.d;
+  p.nt = (c.f + 127) / 128;
+  p.hdr = a.hdr;
+  p.tabs = a.tabs;
+  return launch_pair<FwdGateUp8>(p, s);
 }
 
 cudaError_t launch_router_dwr(const Cfg& c, const Layout& L, const uint16_t* x, const uint16_t* dl_bf16,

@@ -274,6 +274,17 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc,
       : "memory");
 }
 
+// The same pair MMA with 8-bit floating-point operands (kind::f8f6f4, K = 32 per instruction: the
+// same 32 bytes of each K-major row as a bf16 step).
+__device__ __forceinline__ void umma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on the mbarrier at shared::cluster address `cbar` (this CTA's or the peer's) when
 // every pair MMA this thread issued so far has completed.
 __device__ __forceinline__ void umma_commit_pair(uint32_t cbar) {
@@ -382,6 +393,11 @@ __device__ __forceinline__ uint64_t sdesc_mnmajor(uint32_t saddr, uint32_t lbo_b
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) |
          ((b_mn ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// kind::f8f6f4 with E4M3 A and B (format code 0 in bits 7-9 and 10-12), fp32 accumulator, K-major.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 }  // namespace moe
