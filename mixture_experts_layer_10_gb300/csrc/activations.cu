@@ -49,7 +49,7 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) swiglu_bwd_kept_kernel(
           const float a = h ? bf16_hi(ua[m]) : bf16_lo(ua[m]);
           const float b = h ? bf16_hi(ub[m]) : bf16_lo(ub[m]);
           const float dhp = h ? bf16_hi(ud[m]) : bf16_lo(ud[m]);
-          const float sg = 1.f / (1.f + __expf(-a));
+          const float sg = sigmoid_fast(a);
           const float sa = a * sg;
           const float hv = sa * b;
           dg = fmaf(dhp, hv, dg);

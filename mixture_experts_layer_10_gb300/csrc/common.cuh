@@ -107,6 +107,14 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&p);
 }
 
+// Logistic sigmoid 1 / (1 + e^-a) of the SwiGLU epilogues with the approximate reciprocal.  The
+// IEEE fp32 division ends in a range check and a branch to a slow path, which keeps the compiler
+// from overlapping the elements of a row: with one epilogue warp per SM sub-partition nothing else
+// hides that latency.  The approximate reciprocal is within a couple of fp32 ulps, far below the
+// bf16 rounding of every output; for a < -88, e^-a overflows to +inf and the reciprocal gives 0,
+// the limit.
+__device__ __forceinline__ float sigmoid_fast(float a) { return __fdividef(1.f, 1.f + __expf(-a)); }
+
 // ---------------------------------------------------------------------------------------------
 // host-side helpers shared by the launchers
 // ---------------------------------------------------------------------------------------------

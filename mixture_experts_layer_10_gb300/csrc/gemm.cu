@@ -251,8 +251,8 @@ struct FwdGateUpT : PairDefaults {
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
         const float a0 = __uint_as_float(ga[2 * i]), a1 = __uint_as_float(ga[2 * i + 1]);
-        const float h0 = a0 / (1.f + __expf(-a0)) * __uint_as_float(ub[2 * i]);
-        const float h1 = a1 / (1.f + __expf(-a1)) * __uint_as_float(ub[2 * i + 1]);
+        const float h0 = a0 * sigmoid_fast(a0) * __uint_as_float(ub[2 * i]);
+        const float h1 = a1 * sigmoid_fast(a1) * __uint_as_float(ub[2 * i + 1]);
         pk[i] = pack_bf16(h0, h1);
       }
       if (!kKeep) {
@@ -338,14 +338,24 @@ struct FwdGateUp8 : PairDefaults {
       tmem_ld32(ta + c, ga);
       tmem_ld32(ta + 128 + c, ub);
       tmem_ld_wait();
+      float sg[32], su[32];   // the 32 columns' weight scales (the same for every lane)
+#pragma unroll
+      for (int v = 0; v < 8; ++v) {
+        const float4 g4 = __ldg(reinterpret_cast<const float4*>(gs + c) + v);
+        const float4 u4 = __ldg(reinterpret_cast<const float4*>(us + c) + v);
+        sg[4 * v] = g4.x; sg[4 * v + 1] = g4.y; sg[4 * v + 2] = g4.z; sg[4 * v + 3] = g4.w;
+        su[4 * v] = u4.x; su[4 * v + 1] = u4.y; su[4 * v + 2] = u4.z; su[4 * v + 3] = u4.w;
+      }
       uint32_t pk[16];
 #pragma unroll
       for (int i = 0; i < 16; ++i) {
-        const float a0 = __uint_as_float(ga[2 * i]) * sx * gs[c + 2 * i];
-        const float a1 = __uint_as_float(ga[2 * i + 1]) * sx * gs[c + 2 * i + 1];
-        const float h0 = a0 / (1.f + __expf(-a0)) * (__uint_as_float(ub[2 * i]) * sx * us[c + 2 * i]);
-        const float h1 = a1 / (1.f + __expf(-a1)) * (__uint_as_float(ub[2 * i + 1]) * sx * us[c + 2 * i + 1]);
-        pk[i] = pack_bf16(h0, h1);
+        float hv[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const float a = __uint_as_float(ga[2 * i + h]) * sx * sg[2 * i + h];
+          hv[h] = a * sigmoid_fast(a) * (__uint_as_float(ub[2 * i + h]) * sx * su[2 * i + h]);
+        }
+        pk[i] = pack_bf16(hv[0], hv[1]);
       }
       uint8_t* box = claim_box(ebuf, c / 32, lane);
       stage_box(box, lane, pk);
@@ -498,7 +508,7 @@ struct BwdFused : PairDefaults {
             const float a = __uint_as_float(va[2 * i + h]);
             const float b = __uint_as_float(vb[2 * i + h]);
             const float dhp = h ? bf16_hi(du[i]) : bf16_lo(du[i]);
-            const float sg = 1.f / (1.f + __expf(-a));
+            const float sg = sigmoid_fast(a);
             const float sa = a * sg;
             const float hv = sa * b;
             dg = fmaf(dhp, hv, dg);
