@@ -13,6 +13,9 @@ limitations and future work); they fix no format.  The plainest reading taken he
   rounded to the nearest e4m3 value with ties to the even mantissa, and saturated to +-448;
 * an activation row and a weight row (one output channel) are quantised this way, so
   x . w ~= s_x s_w (q_x . q_w), exactly the fp64 product of the decoded codes and the scales.
+* in the forward the SwiGLU output h is held in bf16 between the two projections (the precision
+  of every other intermediate of the layer) and quantised per row like x; W_down is quantised per
+  row, one scale per output channel of d_model; the router stays in fp32.
 
 Both rounding decisions (the fp32 division and the e4m3 rounding) are taken in fp32, as the
 kernels take them.
@@ -20,6 +23,8 @@ kernels take them.
 from __future__ import annotations
 
 import numpy as np
+
+from .moe_oracle import as_f64, combine, f64_to_bf16_value
 
 E4M3_MAX = 448.0
 _MIN_NORMAL_EXP = -6          # smallest normal: 2^-6
@@ -87,3 +92,54 @@ def gate_up_fp8(xq: np.ndarray, xs: np.ndarray, gq: np.ndarray, gs: np.ndarray, 
     a = x @ dequantize_rows(gq, gs).T
     b = x @ dequantize_rows(uq, us).T
     return a / (1.0 + np.exp(-a)) * b
+
+
+def down_fp8(hq: np.ndarray, hs: np.ndarray, dq: np.ndarray, ds: np.ndarray) -> np.ndarray:
+    """o = (s_h q_h)(s_d q_d)^T in float64: hq [n, f] codes with row scales hs [n]; dq [d, f] the
+    codes of one expert's W_down rows (one per output channel) with scales ds [d]."""
+    return dequantize_rows(hq, hs) @ dequantize_rows(dq, ds).T
+
+
+def quantize_expert_rows(W: np.ndarray):
+    """Row quantisation of every expert's matrix: W [G, rows, cols] (exact fp32 values) ->
+    codes [G, rows, cols] uint8 and scales [G, rows] float32."""
+    W = np.asarray(W, dtype=np.float32)
+    codes = np.empty(W.shape, np.uint8)
+    scales = np.empty(W.shape[:2], np.float32)
+    for g in range(W.shape[0]):
+        codes[g], scales[g] = quantize_rows_e4m3(W[g])
+    return codes, scales
+
+
+def expert_forward_fp8(xr: np.ndarray, gq, gs, uq, us, dq, ds) -> np.ndarray:
+    """One expert's output rows with e4m3 GEMMs, in the order the forward takes the steps: the x
+    rows are quantised per row, h = silu(a) * b from gate_up_fp8, h is held in bf16 (rounded once,
+    nearest even) and quantised per row, and o = down_fp8 of those codes.  xr [n, d] exact values."""
+    xq, xsc = quantize_rows_e4m3(np.asarray(xr, np.float32))
+    h = gate_up_fp8(xq, xsc, gq, gs, uq, us)
+    hq, hsc = quantize_rows_e4m3(f64_to_bf16_value(h).astype(np.float32))
+    return down_fp8(hq, hsc, dq, ds)
+
+
+def layer_forward_fp8(L) -> np.ndarray:
+    """y [T, d] (float64) of a Layer whose expert weights are quantised per row (W_gate and W_up
+    rows: channels of d_ff; W_down rows: channels of d_model): routing, dispatch and combine as
+    Layer.forward, every expert's SwiGLU FFN through expert_forward_fp8."""
+    R, D = L.routing(), L.dispatch()
+    T, k, d = L.T, L.k, L.d
+    gq, gs = quantize_expert_rows(as_f64(L.inp["W_gate"]))
+    uq, us = quantize_expert_rows(as_f64(L.inp["W_up"]))
+    dq, ds = quantize_expert_rows(as_f64(L.inp["W_down"]))
+
+    def expert(g, xr):
+        return expert_forward_fp8(xr, gq[g], gs[g], uq[g], us[g], dq[g], ds[g])
+
+    o_slot = np.zeros((T, k, d))
+    for e in range(L.E):
+        rows = np.arange(D.offsets[e], D.offsets[e + 1])
+        if rows.size == 0:
+            continue
+        slots = D.slot_of_row[rows]
+        o_slot[slots // k, slots % k] = expert(e, L.x[slots // k])
+    shared = [expert(L.E + s, L.x) for s in range(L.S)]
+    return combine(o_slot, R.gates, D.row_of_slot >= 0, shared)

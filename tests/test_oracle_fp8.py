@@ -5,6 +5,7 @@ import torch
 
 import oracle
 from oracle import fp8
+import synth
 
 
 def test_decode_landmarks():
@@ -66,3 +67,81 @@ def test_lossless_inputs_reduce_to_the_bf16_expert():
     _, _, h_ref, _ = oracle.expert_forward(x.astype(np.float64), wg.astype(np.float64),
                                            wu.astype(np.float64), np.zeros((1, 32)))
     assert np.allclose(h, h_ref, rtol=1e-12, atol=0)
+
+
+def _grid_rows(rng, n, w, exps):
+    """[n, w] values on the e4m3 grid times 2^exps[i], row i's maximum magnitude 448 * 2^exps[i]:
+    the row quantisation of such rows is exact (scale 2^exps[i])."""
+    grid = fp8.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8))
+    grid = grid[grid >= 2.0 ** -3]
+    r = rng.choice(grid, (n, w)) * rng.choice([-1.0, 1.0], (n, w))
+    r[np.arange(n), rng.integers(0, w, n)] = 448.0
+    return r * np.ldexp(1.0, np.asarray(exps))[:, None]
+
+
+def test_down_lossless_with_per_channel_scales():
+    # rows of W_down with scales 2^-12 .. 2^4 apart: exact only when each output channel gets its
+    # own row's scale
+    rng = np.random.default_rng(3)
+    h = _grid_rows(rng, 7, 64, rng.integers(-4, 4, 7))
+    wd = _grid_rows(rng, 48, 64, rng.integers(-12, 5, 48))
+    hq, hs = fp8.quantize_rows_e4m3(h.astype(np.float32))
+    dq, ds = fp8.quantize_rows_e4m3(wd.astype(np.float32))
+    assert np.array_equal(fp8.down_fp8(hq, hs, dq, ds), h @ wd.T)
+
+
+def _lossless_layer(T=24, d=64, f=64, E=4, k=2, S=1, cf=0.0, renorm=False, seed=5):
+    """Layer inputs on which every step of the e4m3 forward is exact.
+
+    x_t = 2^j_t e_0 + 448 2^j_t e_1 (row scale 2^j_t); W_gate[g][i] has 2^a_i at column 0, 0 at
+    column 1 and its row maximum 448 2^(a_i - 4) elsewhere; W_up[g][i] has its maximum 448 2^b_i
+    at column 0 and 0 at column 1.  So a_ti = 2^(j_t + a_i) >= 64, where silu(a) = a exactly in
+    fp64 (and fp32), b_ti = 448 2^(j_t + b_i), and h_ti = 448 2^(2 j_t + a_i + b_i): on the bf16
+    grid and, per row, on the e4m3 grid times a power of two.  W_down rows are grid rows."""
+    rng = np.random.default_rng(seed)
+    G = E + S
+    j = rng.integers(0, 4, T)
+    x = np.zeros((T, d))
+    x[:, 0] = np.ldexp(1.0, j)
+    x[:, 1] = 448.0 * np.ldexp(1.0, j)
+    Wg = np.empty((G, f, d))
+    Wu = np.empty((G, f, d))
+    Wd = np.empty((G, d, f))
+    for g in range(G):
+        a = rng.integers(6, 11, f)
+        b = rng.integers(-3, 4, f)
+        Wg[g] = _grid_rows(rng, f, d, a - 4) / 2.0   # maxima 224 2^(a-4): below the column-2 entry
+        Wg[g][:, 2] = 448.0 * np.ldexp(1.0, a - 4)
+        Wg[g][:, 0] = np.ldexp(1.0, a)
+        Wg[g][:, 1] = 0.0
+        Wu[g] = _grid_rows(rng, f, d, b) / 2.0
+        Wu[g][:, 0] = 448.0 * np.ldexp(1.0, b)
+        Wu[g][:, 1] = 0.0
+        Wd[g] = _grid_rows(rng, d, f, rng.integers(-8, -2, d))
+    bits = lambda v: synth.f32_to_bf16_bits(v.astype(np.float32))
+    for v in (x, Wg, Wu, Wd):   # every value is exact in bf16
+        assert np.array_equal(oracle.bf16_to_f64(bits(v)), v)
+    inp = {"x": bits(x), "W_r": rng.normal(0, 0.05, (d, E)).astype(np.float32), "b_r": None,
+           "W_gate": bits(Wg), "W_up": bits(Wu), "W_down": bits(Wd), "dy": bits(np.zeros((T, d)))}
+    cfg = {"T": T, "d": d, "E": E, "k": k, "f": f, "S": S, "renorm": renorm, "cf": cf}
+    return oracle.Layer(inp, cfg)
+
+
+@pytest.mark.parametrize("variant", [dict(), dict(S=0, renorm=True, k=3), dict(cf=0.6, S=2)])
+def test_lossless_layer_forward_equals_the_exact_layer(variant):
+    L = _lossless_layer(**variant)
+    y_ref, _ = L.forward()
+    y = fp8.layer_forward_fp8(L)
+    assert np.abs(y_ref).max() > 0
+    assert np.allclose(y, y_ref, rtol=1e-12, atol=0)
+
+
+def test_quantised_layer_forward_error_is_the_e4m3_size():
+    # on ordinary inputs the e4m3 forward is close to, but not the same as, the exact forward:
+    # relative error around the e4m3 step (2^-4 per element, averaging out over the sums)
+    import cases
+    c, inp, L = cases.case("tiny")
+    y_ref, _ = L.forward()
+    y = fp8.layer_forward_fp8(L)
+    rel = np.linalg.norm(y - y_ref) / np.linalg.norm(y_ref)
+    assert 1e-3 < rel < 0.1
