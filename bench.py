@@ -68,7 +68,7 @@ def parse():
     ap.add_argument("--topk", type=int, default=0, help="override k (profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fp8", action="store_true",
-                    help="also time the e4m3 gate/up projection (quantised inputs) on the same rows")
+                    help="also time the forward with e4m3 expert GEMMs beside the bf16 forward")
     ap.add_argument("--keep-rows", type=int, default=0,
                     help="expert-ordered rows whose gate/up pre-activations the forward keeps instead "
                          "of the backward recomputing them (0: recompute all, the default; -1: keep all)")
@@ -83,6 +83,60 @@ def peaks():
                 "source": "measured"}
     except (OSError, KeyError, ValueError):
         return {"hbm": 6800.0, "tensor": 1700.0, "tensor_burst": 1900.0, "source": "fallback"}
+
+
+def fp8_forward(args, mc, cfg, x, W_r, b_r, Wg, Wu, Wd, buf, N, tensor_peak, tensor_kind, pk):
+    """The forward with e4m3 expert GEMMs (weights quantised once, untimed) against the bf16
+    forward on the same inputs, each timed alone over args.steps calls with CUDA events."""
+    import torch
+    import mixture_experts_layer_10_gb300 as moe
+    T, d, f = cfg["T"], cfg["d"], cfg["f"]
+    G = cfg["E"] + cfg["S"]
+
+    def quant(t):
+        codes = torch.empty(t.shape, dtype=torch.uint8, device="cuda")
+        scales = torch.empty(G, t.shape[1], dtype=torch.float32, device="cuda")
+        moe.moe_quantize_rows_e4m3(t, codes, scales)
+        return codes, scales
+    g8, u8, d8 = quant(Wg), quant(Wu), quant(Wd)
+    y8 = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn, profile):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        moe.moe_profile_enable(profile)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            fn()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        prof = moe.moe_profile_read() if profile else {}
+        moe.moe_profile_enable(False)
+        status = moe.moe_check_error(buf.ws)
+        if status != 0:
+            raise RuntimeError(f"forward failed: {moe.moe_status_string(status)}")
+        return ev0.elapsed_time(ev1) / args.steps, prof
+
+    ms16, _ = timed(lambda: moe.moe_layer_fwd(mc, x, W_r, b_r, Wg, Wu, Wd, y8, buf.saved, buf.ws), False)
+    ms8, prof = timed(lambda: moe.moe_layer_fwd_fp8(mc, x, W_r, b_r, *g8, *u8, *d8, y8, buf.saved, buf.ws), True)
+    peak8 = 2 * tensor_peak
+    kern = {}
+    for name, flops in (("gemm_gate_up_fp8", 4 * N * d * f), ("gemm_down_fp8", 2 * N * d * f)):
+        tot, n = prof.get(name, (0.0, 0))
+        if n:
+            tf = flops * n / (tot / 1000.0) / 1e12
+            kern[name] = {"ms_per_step": tot / args.steps, "tflops": tf, "frac": tf / peak8}
+    tot, n = prof.get("quantize_e4m3", (0.0, 0))
+    if n:   # x rows and h rows: bf16 in, codes and a scale out
+        gbs = (N * (d + f) * 3 + 8 * N) * args.steps / (tot / 1000.0) / 1e9
+        kern["quantize_e4m3"] = {"ms_per_step": tot / args.steps, "gbs": gbs, "frac": gbs / pk["hbm"]}
+    return {"metric": "forward tokens/s (e4m3 expert GEMMs)", "value": T / (ms8 / 1000.0), "fwd_ms": ms8,
+            "bf16_fwd_ms": ms16, "speedup_vs_bf16_fwd": ms16 / ms8,
+            "peak_tflops": peak8, "peak_kind": "2 x " + tensor_kind.split(":")[0] + " (nominal fp8:bf16 ratio)",
+            "kernels": kern}
 
 
 def kernel_source_hash() -> str:
@@ -311,14 +365,6 @@ def main():
         kept_real += max(0, min(start + int(n_g), keep) - start)
         start += (int(n_g) + ROW_TILE - 1) // ROW_TILE * ROW_TILE
     load_max_over_mean = float(counts_h.max() / counts_h.mean())
-    fp8_inputs = None
-    if args.fp8:   # quantised copies for the e4m3 gate/up timing below (untimed preparation)
-        def quant(t):
-            codes = torch.empty(t.shape, dtype=torch.uint8, device="cuda")
-            scales = torch.empty(t.numel() // t.shape[-1], dtype=torch.float32, device="cuda")
-            moe.moe_quantize_rows_e4m3(t, codes, scales)
-            return codes, scales
-        fp8_inputs = (*quant(x_perm), *quant(Wg), *quant(Wu))
     del x_perm, scratch_rows, scratch_tok
 
     for _ in range(args.warmup):
@@ -443,31 +489,8 @@ def main():
     tensor_kind = ("bf16_tflops (burst, %s): SM clock held at max in the timed region" if at_max else
                    "bf16_tflops_sustained (%s): SM clock below max in the timed region") % pk["source"]
     fp8_line = None
-    if fp8_inputs is not None:
-        # the e4m3 gate/up projection alone, on the expert rows of the step above: the layer's
-        # forward left the same dispatch tables (same x, same routing) in the workspace
-        x8, xs, g8, gs, u8, us = fp8_inputs
-        h8 = torch.empty(buf.rows, f, dtype=torch.bfloat16, device="cuda")
-        for _ in range(3):
-            moe.moe_gate_up_fp8(mc, x8, xs, g8, gs, u8, us, h8, buf.ws)
-        torch.cuda.synchronize()
-        ev0.record(stream)
-        for _ in range(args.steps):
-            moe.moe_gate_up_fp8(mc, x8, xs, g8, gs, u8, us, h8, buf.ws)
-        ev1.record(stream)
-        torch.cuda.synchronize()
-        ms8 = ev0.elapsed_time(ev1) / args.steps
-        status = moe.moe_check_error(buf.ws)
-        if status != 0:
-            raise RuntimeError(f"fp8 gate/up failed: {moe.moe_status_string(status)}")
-        tf8 = 4 * N * d * f / (ms8 / 1000.0) / 1e12
-        tot16, n16 = prof.get("gemm_gate_up_swiglu", (0.0, 0))
-        bf16_ms = tot16 / n16 if n16 else None
-        fp8_peak = 2 * tensor_peak
-        fp8_line = {"gate_up_ms": ms8, "tflops": tf8, "peak": fp8_peak, "frac": tf8 / fp8_peak,
-                    "peak_kind": "2 x " + tensor_kind.split(":")[0] + " (nominal fp8:bf16 ratio)",
-                    "bf16_gate_up_ms": bf16_ms, "speedup_vs_bf16": bf16_ms / ms8 if bf16_ms else None}
-        del h8
+    if args.fp8:
+        fp8_line = fp8_forward(args, mc, cfg, x, W_r, b_r, Wg, Wu, Wd, buf, N, tensor_peak, tensor_kind, pk)
     kernels = {}
     gemm_flops = gemm_ms = hbm_bytes = hbm_ms = 0.0
     launches = 0
@@ -524,7 +547,7 @@ def main():
                    "kept_activation_bytes": keep * f * 2 * 2},
         "cuda_graph": graph,
         "model": model_line,
-        "fp8_gate_up": fp8_line,
+        "fp8_forward": fp8_line,
         "e2e": {"value": world * T / (ms_e2e / 1000.0), "unit": "tokens/s", "ms_per_step": ms_e2e,
                 "h2d_bytes_per_step": 2 * T * d * 2, "d2h_bytes_per_step": 2 * T * d * 2},
         "roofline": roof,

@@ -209,8 +209,8 @@ moe_status_t moe_combine_bwd(const moe_config_t* cfg, const moe_bf16* dx_perm, c
  *
  * moe_quantize_rows_e4m3: src [rows, cols] bf16 -> codes [rows, cols] uint8 and scales [rows]
  * fp32, with scale = amax / 448 over the row (1 for an all-zero row) and code = e4m3(v / scale),
- * both in fp32, rounded to nearest even and saturated.  cols a multiple of 16; 16-byte-aligned
- * pointers.  Used for x_perm rows and for the rows (output channels) of W_gate and W_up. */
+ * both in fp32, rounded to nearest even and saturated.  cols a multiple of 16, at most 16384;
+ * 16-byte-aligned pointers.  Used for x_perm rows and for the rows (output channels) of W_gate and W_up. */
 moe_status_t moe_quantize_rows_e4m3(const moe_bf16* src, int64_t rows, int32_t cols, uint8_t* codes,
                                     float* scales, moe_stream_t stream);
 
@@ -223,6 +223,25 @@ moe_status_t moe_gate_up_fp8(const moe_config_t* cfg, const uint8_t* x8, const f
                              const uint8_t* wg8, const float* wg_scale, const uint8_t* wu8,
                              const float* wu_scale, moe_bf16* h, void* ws, size_t ws_bytes,
                              moe_stream_t stream);
+
+/* The down projection with e4m3 operands: o = s_h s_d (q_h . q_d) per row and output channel,
+ * accumulated in fp32 and stored bf16.  h8 / h_scale: quantised h rows [moe_perm_rows(), d_ff] /
+ * [moe_perm_rows()] (moe_quantize_rows_e4m3 of h); wd8 [E+S, d_model, d_ff] codes with wd_scale
+ * [E+S, d_model] (one scale per output channel: the rows of W_down).  Writes o_perm
+ * [moe_perm_rows(), d_model] bf16.  Uses the tables of moe_dispatch in ws. */
+moe_status_t moe_down_fp8(const moe_config_t* cfg, const uint8_t* h8, const float* h_scale, const uint8_t* wd8,
+                          const float* wd_scale, moe_bf16* o_perm, void* ws, size_t ws_bytes,
+                          moe_stream_t stream);
+
+/* The whole forward with e4m3 expert GEMMs: route and dispatch as moe_layer_fwd, then per padded
+ * expert row quantise x_perm, moe_gate_up_fp8 (h kept in bf16), quantise h, moe_down_fp8, and the
+ * combine.  The weights come quantised (moe_quantize_rows_e4m3 of every row of W_gate, W_up and
+ * W_down, as above).  The router stays fp32.  Fills `saved` like moe_layer_fwd (idx, gates), so
+ * moe_layer_bwd can follow with the bf16 weights.  Only the rows this step fills are quantised. */
+moe_status_t moe_layer_fwd_fp8(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
+                               const uint8_t* wg8, const float* wg_scale, const uint8_t* wu8,
+                               const float* wu_scale, const uint8_t* wd8, const float* wd_scale, moe_bf16* y,
+                               void* saved, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* The whole forward: route, dispatch, expert FFN, combine.  Fills `saved` (idx and gates only;
  * activations are recomputed in backward). */

@@ -26,7 +26,7 @@ EXPORTS = ("moe_workspace_size", "moe_perm_rows", "moe_workspace_init", "moe_rou
            "moe_expert_ffn_fwd", "moe_combine", "moe_expert_ffn_bwd", "moe_router_bwd",
            "moe_combine_bwd", "moe_layer_fwd", "moe_layer_bwd", "moe_check_error",
            "moe_debug_inject", "moe_profile_enable", "moe_profile_read", "moe_status_string",
-           "moe_quantize_rows_e4m3", "moe_gate_up_fp8")
+           "moe_quantize_rows_e4m3", "moe_gate_up_fp8", "moe_down_fp8", "moe_layer_fwd_fp8")
 
 
 class moe_config_t(ctypes.Structure):
@@ -71,6 +71,8 @@ def load(path: str | None = None):
         "moe_combine_bwd": [cfgp, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
         "moe_quantize_rows_e4m3": [_P, ctypes.c_int64, ctypes.c_int32, _P, _P, _P],
         "moe_gate_up_fp8": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+        "moe_down_fp8": [cfgp, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+        "moe_layer_fwd_fp8": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
         "moe_layer_fwd": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
         "moe_layer_bwd": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                           ctypes.c_size_t, _P],
@@ -205,6 +207,17 @@ def moe_quantize_rows_e4m3(src, codes, scales, stream=None):
 def moe_gate_up_fp8(cfg, x8, x_scale, wg8, wg_scale, wu8, wu_scale, h, ws, stream=None):
     _call("moe_gate_up_fp8", ctypes.byref(cfg), _ptr(x8), _ptr(x_scale), _ptr(wg8), _ptr(wg_scale), _ptr(wu8),
           _ptr(wu_scale), _ptr(h), _ptr(ws), ws.numel(), _stream(stream))
+
+
+def moe_down_fp8(cfg, h8, h_scale, wd8, wd_scale, o_perm, ws, stream=None):
+    _call("moe_down_fp8", ctypes.byref(cfg), _ptr(h8), _ptr(h_scale), _ptr(wd8), _ptr(wd_scale), _ptr(o_perm),
+          _ptr(ws), ws.numel(), _stream(stream))
+
+
+def moe_layer_fwd_fp8(cfg, x, W_r, b_r, wg8, wg_scale, wu8, wu_scale, wd8, wd_scale, y, saved, ws, stream=None):
+    _call("moe_layer_fwd_fp8", ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(b_r), _ptr(wg8), _ptr(wg_scale),
+          _ptr(wu8), _ptr(wu_scale), _ptr(wd8), _ptr(wd_scale), _ptr(y), _ptr(saved), _ptr(ws), ws.numel(),
+          _stream(stream))
 
 
 def moe_layer_fwd(cfg, x, W_r, b_r, W_gate, W_up, W_down, y, saved, ws, stream=None):

@@ -74,49 +74,113 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) swiglu_bwd_kept_kernel(
 
 // FP8 rows (the quantisation step of the e4m3 expert GEMMs): per row, amax over the row, scale =
 // amax / 448 in fp32 (1 for an all-zero row), codes = e4m3(v / scale) rounded to nearest even and
-// saturated.  A warp owns a row and reads it twice in 16-byte vectors (eight values).
-__global__ void __launch_bounds__(256) quantize_rows_e4m3_kernel(const uint16_t* __restrict__ src, int64_t rows,
-                                                                 int cols, uint8_t* __restrict__ codes,
-                                                                 float* __restrict__ scales) {
-  const int lane = threadIdx.x & 31;
-  const int nvec = cols / 8;
-  const int64_t nwarps = (int64_t)gridDim.x * (blockDim.x >> 5);
-  for (int64_t r = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); r < rows; r += nwarps) {
-    const uint4* row = reinterpret_cast<const uint4*>(src + r * cols);
-    float amax = 0.f;
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 u = row[v];
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+// saturated.  A block owns a row at a time and keeps it in registers (up to kQuantV 16-byte vectors
+// of eight values per thread) between the amax and the encode, so each value crosses HBM once in
+// each direction.  With the dispatch tables given, rows past the padded expert rows of this step
+// (tb->total_rows) are skipped.
+constexpr int kQuantV = 8;
+
+// v / scale rounded to nearest in fp32, from the row's reciprocal y = RN(1 / scale): q0 = RN(v y) is
+// within one ulp of the quotient, the residual v - q0 scale is exact in one fma, and RN(q0 + r y) is
+// the correctly rounded quotient (Markstein's theorem on the final correction of a division; it
+// needs no underflow or overflow in the steps, which holds for scales in [2^-80, 2^80] whenever the
+// quotient is large enough to give a nonzero e4m3 code; rows with other scales use the IEEE
+// division).  A zero keeps its sign.
+__device__ __forceinline__ float div_by_scale(float v, float scale, float y) {
+  const float q0 = v * y;
+  const float r = fmaf(-q0, scale, v);
+  return copysignf(fmaf(r, y, q0), v);
+}
+
+template <bool kRecip>
+__device__ __forceinline__ uint2 encode8_e4m3(const uint4& u, float scale, float y) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+  uint32_t c[4];
 #pragma unroll
-      for (int m = 0; m < 4; ++m) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[m])), fabsf(bf16_hi(w[m]))));
+  for (int m = 0; m < 4; ++m) {
+    const float lo = bf16_lo(w[m]), hi = bf16_hi(w[m]);
+    const float2 f2 = kRecip ? make_float2(div_by_scale(lo, scale, y), div_by_scale(hi, scale, y))
+                             : make_float2(__fdiv_rn(lo, scale), __fdiv_rn(hi, scale));
+    c[m] = (uint32_t)__nv_cvt_float2_to_fp8x2(f2, __NV_SATFINITE, __NV_E4M3);   // .x in the low byte
+  }
+  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
+template <int kThreads>
+__global__ void __launch_bounds__(kThreads) quantize_rows_e4m3_kernel(const uint16_t* __restrict__ src, int64_t rows,
+                                                                      int cols, uint8_t* __restrict__ codes,
+                                                                      float* __restrict__ scales,
+                                                                      const Tables* __restrict__ tb) {
+  constexpr int kWarps = kThreads / 32;
+  __shared__ float part[2][kWarps];   // per-warp maxima, double-buffered across rows
+  if (tb != nullptr) rows = min(rows, (int64_t)tb->total_rows);
+  const int nvec = cols / 8;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int buf = 0;
+  for (int64_t r = blockIdx.x; r < rows; r += gridDim.x, buf ^= 1) {
+    const uint4* row = reinterpret_cast<const uint4*>(src + r * cols);
+    uint4 v[kQuantV];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < kQuantV; ++i) {
+      const int q = threadIdx.x + i * kThreads;
+      if (q < nvec) {
+        v[i] = row[q];
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int m = 0; m < 4; ++m) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[m])), fabsf(bf16_hi(w[m]))));
+      }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
-    if (lane == 0) scales[r] = scale;
-    uint2* out = reinterpret_cast<uint2*>(codes + r * cols);
-    for (int v = lane; v < nvec; v += 32) {
-      const uint4 u = row[v];
-      const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-      uint32_t q[4];
+    if (kWarps > 1) {
+      if (lane == 0) part[buf][warp] = amax;
+      __syncthreads();   // also orders the previous row's reads of part[buf ^ 1] before its next writes
 #pragma unroll
-      for (int m = 0; m < 4; ++m) {
-        const float2 f2 = make_float2(__fdiv_rn(bf16_lo(w[m]), scale), __fdiv_rn(bf16_hi(w[m]), scale));
-        q[m] = (uint32_t)__nv_cvt_float2_to_fp8x2(f2, __NV_SATFINITE, __NV_E4M3);   // .x in the low byte
+      for (int w = 0; w < kWarps; ++w) amax = fmaxf(amax, part[buf][w]);
+    }
+    const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    if (threadIdx.x == 0) scales[r] = scale;
+    uint2* out = reinterpret_cast<uint2*>(codes + r * cols);
+    if (scale >= 0x1p-80f && scale <= 0x1p80f) {   // the same branch for the whole block
+      const float y = __frcp_rn(scale);
+#pragma unroll
+      for (int i = 0; i < kQuantV; ++i) {
+        const int q = threadIdx.x + i * kThreads;
+        if (q < nvec) out[q] = encode8_e4m3<true>(v[i], scale, y);
       }
-      out[v] = make_uint2(q[0] | (q[1] << 16), q[2] | (q[3] << 16));
+    } else {
+#pragma unroll
+      for (int i = 0; i < kQuantV; ++i) {
+        const int q = threadIdx.x + i * kThreads;
+        if (q < nvec) out[q] = encode8_e4m3<false>(v[i], scale, 0.f);
+      }
     }
   }
+}
+
+template <int kThreads>
+void launch_quantize(const uint16_t* src, int64_t rows, int cols, uint8_t* codes, float* scales, const Tables* tabs,
+                     cudaStream_t s) {
+  const int per_sm = std::min(32, 2048 / kThreads);
+  const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)num_sms() * per_sm));
+  quantize_rows_e4m3_kernel<kThreads><<<(int)blocks, kThreads, 0, s>>>(src, rows, cols, codes, scales, tabs);
 }
 
 }  // namespace
 
 cudaError_t launch_quantize_rows_e4m3(const uint16_t* src, int64_t rows, int cols, uint8_t* codes, float* scales,
-                                      cudaStream_t s) {
+                                      cudaStream_t s, const Tables* tabs) {
   if (rows <= 0) return cudaSuccess;
-  const int64_t blocks64 = std::min<int64_t>((rows + 7) / 8, (int64_t)num_sms() * 16);
+  // threads per row: about four vectors each, between one warp and 256 threads (eight vectors
+  // each at the widest row, 16384 values)
+  const int nvec = cols / 8;
+  if (nvec > kQuantV * 256) return cudaErrorInvalidValue;
   prof_mark(kKQuantE4m3, s, true);
-  quantize_rows_e4m3_kernel<<<(int)std::max<int64_t>(1, blocks64), 256, 0, s>>>(src, rows, cols, codes, scales);
+  if (nvec <= 4 * 32) launch_quantize<32>(src, rows, cols, codes, scales, tabs, s);
+  else if (nvec <= 4 * 64) launch_quantize<64>(src, rows, cols, codes, scales, tabs, s);
+  else if (nvec <= 4 * 128) launch_quantize<128>(src, rows, cols, codes, scales, tabs, s);
+  else launch_quantize<256>(src, rows, cols, codes, scales, tabs, s);
   prof_mark(kKQuantE4m3, s, false);
   return cudaGetLastError();
 }

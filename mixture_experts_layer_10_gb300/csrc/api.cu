@@ -180,7 +180,7 @@ const char* const kKernelNames[kKCount] = {
     "route_fwd", "dispatch_scan", "dispatch_gather", "gemm_gate_up_swiglu", "gemm_down",
     "combine", "gemm_bwd_recompute_swiglu", "gemm_wgrad", "gemm_dgrad_x", "dgates_reduce",
     "router_dlogits", "router_dwr", "router_reduce", "combine_bwd", "gemm_bwd_dgrad_down",
-    "gemm_router_dx", "swiglu_bwd_kept", "gemm_gate_up_fp8", "quantize_e4m3"};
+    "gemm_router_dx", "swiglu_bwd_kept", "gemm_gate_up_fp8", "quantize_e4m3", "gemm_down_fp8"};
 
 struct Profiler {
   std::mutex mu;
@@ -515,7 +515,7 @@ moe_status_t moe_combine_bwd(const moe_config_t* cfg, const moe_bf16* dx_perm, c
 
 moe_status_t moe_quantize_rows_e4m3(const moe_bf16* src, int64_t rows, int32_t cols, uint8_t* codes,
                                     float* scales, moe_stream_t stream) {
-  MOE_NEED(rows >= 0 && cols > 0 && cols % 16 == 0 && rows <= ((int64_t)1 << 31));
+  MOE_NEED(rows >= 0 && cols > 0 && cols % 16 == 0 && cols <= 16384 && rows <= ((int64_t)1 << 31));
   MOE_NEED(rows == 0 || (src && codes && scales && aligned16(src) && aligned16(codes) && aligned16(scales)));
   MOE_TRY(check_device());
   MOE_CUDA(launch_quantize_rows_e4m3(src, rows, cols, codes, scales, stream));
@@ -535,6 +535,59 @@ moe_status_t moe_gate_up_fp8(const moe_config_t* cfg, const uint8_t* x8, const f
   MOE_TRY(check_device());
   GateUpFp8Args a{x8, x_scale, wg8, wg_scale, wu8, wu_scale, h, w.hdr(), w.tabs()};
   MOE_CUDA(launch_gate_up_fp8(c, w.L, a, stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_down_fp8(const moe_config_t* cfg, const uint8_t* h8, const float* h_scale, const uint8_t* wd8,
+                          const float* wd_scale, moe_bf16* o_perm, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  Cfg c;
+  MOE_TRY(make_cfg(cfg, &c));
+  MOE_NEED(h8 && h_scale && wd8 && wd_scale && o_perm);
+  MOE_NEED(aligned16(h8) && aligned16(h_scale) && aligned16(wd8) && aligned16(wd_scale) && aligned16(o_perm));
+  Ws w;
+  MOE_TRY(get_ws(c, ws, ws_bytes, &w));
+  MOE_TRY(check_device());
+  DownFp8Args a{h8, h_scale, wd8, wd_scale, o_perm, w.hdr(), w.tabs()};
+  MOE_CUDA(launch_down_fp8(c, w.L, a, stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_fwd_fp8(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
+                               const uint8_t* wg8, const float* wg_scale, const uint8_t* wu8,
+                               const float* wu_scale, const uint8_t* wd8, const float* wd_scale, moe_bf16* y,
+                               void* saved, void* ws, size_t ws_bytes, moe_stream_t stream) {
+  Cfg c;
+  MOE_TRY(make_cfg(cfg, &c));
+  MOE_NEED(x && W_r && wg8 && wg_scale && wu8 && wu_scale && wd8 && wd_scale && y && saved);
+  MOE_NEED(aligned16(x) && aligned16(W_r) && (!b_r || aligned16(b_r)) && aligned16(wg8) && aligned16(wg_scale) &&
+           aligned16(wu8) && aligned16(wu_scale) && aligned16(wd8) && aligned16(wd_scale) && aligned16(y) &&
+           aligned16(saved));
+  Ws w;
+  MOE_TRY(get_ws(c, ws, ws_bytes, &w));
+  MOE_TRY(check_device());
+  int32_t* idx = static_cast<int32_t*>(saved);
+  float* gates = reinterpret_cast<float*>(idx + (size_t)c.T * c.k);
+  MOE_TRY(do_route(c, w, x, W_r, b_r, idx, gates, nullptr, stream));
+  uint16_t* x_perm = w.at<uint16_t>(w.L.xperm);
+  MOE_TRY(do_dispatch(c, w, idx, x, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, x_perm,
+                      nullptr, stream));
+  // forward-only scratch in the backward's buffers: e4m3 x_perm rows and their scales in dy_perm
+  // (rows x d bytes + 4 rows <= rows x d x 2), e4m3 h rows and scales in buf_f1 (likewise)
+  const size_t rows = (size_t)w.L.rows;
+  uint8_t* x8 = w.at<uint8_t>(w.L.dy_perm);
+  float* xs = reinterpret_cast<float*>(x8 + rows * c.d);
+  uint8_t* h8 = w.at<uint8_t>(w.L.buf_f1);
+  float* hs = reinterpret_cast<float*>(h8 + rows * c.f);
+  uint16_t* h = w.at<uint16_t>(w.L.buf_f0);
+  uint16_t* o_perm = w.at<uint16_t>(w.L.buf_d1);
+  MOE_CUDA(launch_quantize_rows_e4m3(x_perm, (int64_t)rows, c.d, x8, xs, stream, w.tabs()));
+  GateUpFp8Args ga{x8, xs, wg8, wg_scale, wu8, wu_scale, h, w.hdr(), w.tabs()};
+  MOE_CUDA(launch_gate_up_fp8(c, w.L, ga, stream));
+  MOE_CUDA(launch_quantize_rows_e4m3(h, (int64_t)rows, c.f, h8, hs, stream, w.tabs()));
+  DownFp8Args da{h8, hs, wd8, wd_scale, o_perm, w.hdr(), w.tabs()};
+  MOE_CUDA(launch_down_fp8(c, w.L, da, stream));
+  CombineArgs ca{o_perm, gates, y, w.tabs(), w.at<int32_t>(w.L.prow_of_slot)};
+  MOE_CUDA(launch_combine(c, ca, stream));
   return MOE_OK;
 }
 

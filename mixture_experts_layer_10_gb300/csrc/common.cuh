@@ -130,7 +130,7 @@ moe_status_t cuda_status(cudaError_t e);          // MOE_OK or MOE_ERR_CUDA (cle
 enum KernelId : int {
   kKRoute = 0, kKScan, kKGather, kKGateUp, kKDown, kKCombine, kKBwdFused, kKWgrad, kKDgradX,
   kKDgates, kKRouterDlogits, kKRouterDwr, kKRouterReduce, kKCombineBwd, kKBwdDh, kKRouterDx, kKSwigluKept,
-  kKGateUpFp8, kKQuantE4m3, kKCount
+  kKGateUpFp8, kKQuantE4m3, kKDownFp8, kKCount
 };
 void prof_mark(int id, cudaStream_t s, bool begin);
 
@@ -223,12 +223,18 @@ cudaError_t launch_swiglu_bwd_kept(const Cfg& c, const Layout& L, const FfnBwdAr
 
 // FP8 (e4m3) rows: codes [rows, cols] and one fp32 scale per row (amax / 448), from bf16 rows.
 cudaError_t launch_quantize_rows_e4m3(const uint16_t* src, int64_t rows, int cols, uint8_t* codes, float* scales,
-                                      cudaStream_t s);
+                                      cudaStream_t s, const Tables* tabs = nullptr);
 // H = silu(a) * b with a, b from e4m3 rows of x_perm and of W_gate / W_up and their row scales.
 struct GateUpFp8Args {
   const uint8_t* x8; const float* xs; const uint8_t* wg8; const float* gs; const uint8_t* wu8;
   const float* us; uint16_t* h; Hdr* hdr; const Tables* tabs;
 };
 cudaError_t launch_gate_up_fp8(const Cfg& c, const Layout& L, const GateUpFp8Args& a, cudaStream_t s);
+// O = H W_d^T from e4m3 rows of H and of W_d (one scale per output channel).
+struct DownFp8Args {
+  const uint8_t* h8; const float* hs; const uint8_t* wd8; const float* ds; uint16_t* o; Hdr* hdr;
+  const Tables* tabs;
+};
+cudaError_t launch_down_fp8(const Cfg& c, const Layout& L, const DownFp8Args& a, cudaStream_t s);
 
 }  // namespace moe

@@ -365,6 +365,70 @@ struct FwdGateUp8 : PairDefaults {
   __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
 };
 
+// O = H W_d^T from e4m3 rows of H (one scale per row) and of W_d[g] (one scale per output channel
+// of d_model): N = 256 columns of d_model per pair tile, each CTA loading 128 rows of W_d[g]; 128-wide
+// K blocks of d_ff (the last one zero-filled past d_ff).  The epilogue scales the fp32 accumulator
+// by s_h[row] s_d[g, col] and stores bf16.
+struct FwdDown8 : PairDefaults {
+  static constexpr int kId = kKDownFp8;
+  // two epilogue warps per TMEM lane quarter, 128 columns each: with K blocks twice as deep as
+  // bf16's, a short d_ff (6 to 11 blocks) leaves the main loop shorter than one warp's 256 columns
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kBK8 = 128;
+  static constexpr uint32_t kIdesc = idesc_e4m3(kPairM, 256);
+  struct Params {
+    CUtensorMap tmH, tmWd, tmO;
+    const float *hs, *ds;   // [rows] and [G, d_model] scales
+    int f, d, nt;
+    Hdr* hdr;
+    const Tables* tabs;
+  };
+  __device__ static int num_tiles(const Params& p, const SegSmem& s) { return s.n_mtiles * p.nt; }
+  __device__ static Job job(const Params& p, const SegSmem& s, int t) {
+    return row_job(s, t, p.nt, 256, (p.f + kBK8 - 1) / kBK8);
+  }
+  __device__ static void prefetch(const Params& p) { tma_prefetch(&p.tmH); tma_prefetch(&p.tmWd); }
+  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint32_t cbar, int rank) {
+    tma_load_2d_pair(st, &p.tmH, cbar, kit * kBK8, j.m0 + kBM * rank);
+    tma_load_3d_pair(st + kTileA, &p.tmWd, cbar, kit * kBK8, j.n0 + kBM * rank, j.seg);
+  }
+  __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      umma_f8_pair(dt, sdesc_kmajor(sa + kk * 32), sdesc_kmajor(sa + kTileA + kk * 32), kIdesc, (kit | kk) != 0);
+  }
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int part, int,
+                                  uint8_t* ebuf) {
+    const int lane = row & 31;
+    const int y = j.m0 + (row & ~31);
+    const float sh = p.hs[j.m0 + row];
+    const float* ds = p.ds + (size_t)j.seg * p.d + j.n0;
+    epi_begin(lane);
+#pragma unroll 1
+    for (int c = part * 128; c < part * 128 + 128; c += 32) {
+      if (j.n0 + c >= p.d) break;
+      uint32_t v[32];
+      tmem_ld32(ta + c, v);
+      tmem_ld_wait();
+      float sc[32];   // the 32 columns' weight scales (the same for every lane)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float4 s4 = __ldg(reinterpret_cast<const float4*>(ds + c) + q);
+        sc[4 * q] = s4.x; sc[4 * q + 1] = s4.y; sc[4 * q + 2] = s4.z; sc[4 * q + 3] = s4.w;
+      }
+      uint32_t pk[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i)
+        pk[i] = pack_bf16(__uint_as_float(v[2 * i]) * sh * sc[2 * i],
+                          __uint_as_float(v[2 * i + 1]) * sh * sc[2 * i + 1]);
+      uint8_t* box = claim_box(ebuf, (c / 32) & 3, lane);
+      stage_box(box, lane, pk);
+      store_box_2d(&p.tmO, box, lane, j.n0 + c, y);
+    }
+  }
+  __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
+};
+
 // Shared by FwdDown, BwdDh and DgradX: this warp's 32 rows of the fp32 accumulator [128 x 256] ->
 // bf16 boxes of the output [rows, ncols] at row y (the warp's first row) and columns n0 + c.
 __device__ __forceinline__ void store_acc_boxes(const CUtensorMap* map, int y, int n0, int ncols, uint32_t ta,
@@ -1664,6 +1728,22 @@ cudaError_t launch_gate_up_fp8(const Cfg& c, const Layout& L, const GateUpFp8Arg
   p.hdr = a.hdr;
   p.tabs = a.tabs;
   return launch_pair<FwdGateUp8>(p, s);
+}
+
+cudaError_t launch_down_fp8(const Cfg& c, const Layout& L, const DownFp8Args& a, cudaStream_t s) {
+  const uint64_t rows = (uint64_t)L.rows;
+  FwdDown8::Params p{};
+  if (!map_u8_2d(&p.tmH, a.h8, c.f, rows) || !map_u8_3d(&p.tmWd, a.wd8, c.f, c.d, c.G) ||
+      !map_2d(&p.tmO, a.o, c.d, rows, 32, 32))
+    return cudaErrorInvalidValue;
+  p.hs = a.hs;
+  p.ds = a.ds;
+  p.f = c.f;
+  p.d = c.d;
+  p.nt = (c.d + 255) / 256;
+  p.hdr = a.hdr;
+  p.tabs = a.tabs;
+  return launch_pair<FwdDown8>(p, s);
 }
 
 cudaError_t launch_router_dwr(const Cfg& c, const Layout& L, const uint16_t* x, const uint16_t* dl_bf16,

@@ -76,3 +76,19 @@ def test_small_workspace_rejected(lib):
     assert lib.moe_combine(ctypes.byref(c), 0x10000, 0x20000, 0x30000, 0x100000, ws - 1, None) == 3
     assert lib.moe_dispatch(ctypes.byref(c), 0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000,
                             0x70000, 0x100000, 16, None) == 3
+
+
+def test_fp8_arguments_rejected(lib):
+    # the quantiser: cols a multiple of 16, at most 16384; aligned pointers
+    assert lib.moe_quantize_rows_e4m3(0x10000, 4, 16400, 0x20000, 0x30000, None) == 1
+    assert lib.moe_quantize_rows_e4m3(0x10000, 4, 40, 0x20000, 0x30000, None) == 1
+    assert lib.moe_quantize_rows_e4m3(0x10000, 4, 64, 0x20008, 0x30000, None) == 1
+    assert lib.moe_quantize_rows_e4m3(0x10000, -1, 64, 0x20000, 0x30000, None) == 1
+    c = moe.config(T=64, d=128, f=256, E=8, k=2)
+    ws, _ = moe.moe_workspace_size(c)
+    # null scale, misaligned codes
+    assert lib.moe_down_fp8(ctypes.byref(c), 0x10000, None, 0x20000, 0x30000, 0x40000, 0x100000, ws, None) == 1
+    assert lib.moe_gate_up_fp8(ctypes.byref(c), 0x10004, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000, 0x70000,
+                               0x100000, ws, None) == 1
+    assert lib.moe_layer_fwd_fp8(ctypes.byref(c), 0x10000, 0x20000, None, 0x30000, 0x40000, 0x50000, None,
+                                 0x70000, 0x80000, 0x90000, 0xA0000, 0x100000, ws, None) == 1

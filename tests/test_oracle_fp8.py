@@ -121,7 +121,8 @@ def _lossless_layer(T=24, d=64, f=64, E=4, k=2, S=1, cf=0.0, renorm=False, seed=
     bits = lambda v: synth.f32_to_bf16_bits(v.astype(np.float32))
     for v in (x, Wg, Wu, Wd):   # every value is exact in bf16
         assert np.array_equal(oracle.bf16_to_f64(bits(v)), v)
-    inp = {"x": bits(x), "W_r": rng.normal(0, 0.05, (d, E)).astype(np.float32), "b_r": None,
+    # router logits of a few units (x has entries up to 448 * 8): no saturated gates
+    inp = {"x": bits(x), "W_r": rng.normal(0, 1e-3, (d, E)).astype(np.float32), "b_r": None,
            "W_gate": bits(Wg), "W_up": bits(Wu), "W_down": bits(Wd), "dy": bits(np.zeros((T, d)))}
     cfg = {"T": T, "d": d, "E": E, "k": k, "f": f, "S": S, "renorm": renorm, "cf": cf}
     return oracle.Layer(inp, cfg)
