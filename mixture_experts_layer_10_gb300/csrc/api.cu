@@ -568,19 +568,30 @@ moe_status_t moe_layer_fwd_fp8(const moe_config_t* cfg, const moe_bf16* x, const
   int32_t* idx = static_cast<int32_t*>(saved);
   float* gates = reinterpret_cast<float*>(idx + (size_t)c.T * c.k);
   MOE_TRY(do_route(c, w, x, W_r, b_r, idx, gates, nullptr, stream));
-  uint16_t* x_perm = w.at<uint16_t>(w.L.xperm);
-  MOE_TRY(do_dispatch(c, w, idx, x, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, x_perm,
-                      nullptr, stream));
-  // forward-only scratch in the backward's buffers: e4m3 x_perm rows and their scales in dy_perm
-  // (rows x d bytes + 4 rows <= rows x d x 2), e4m3 h rows and scales in buf_f1 (likewise)
+  // Forward-only scratch in the backward's buffers.  The T token rows are quantised once (codes and
+  // scales in buf_d1, free until the down projection writes o_perm there), and the dispatch gathers
+  // their codes and scales into the padded expert rows (in dy_perm: rows x d bytes + 4 rows <=
+  // rows x d x 2); the e4m3 h rows and scales go to buf_f1 likewise.
   const size_t rows = (size_t)w.L.rows;
+  uint8_t* x8_tok = w.at<uint8_t>(w.L.buf_d1);
+  float* xs_tok = reinterpret_cast<float*>(x8_tok + (size_t)c.T * c.d);
   uint8_t* x8 = w.at<uint8_t>(w.L.dy_perm);
   float* xs = reinterpret_cast<float*>(x8 + rows * c.d);
   uint8_t* h8 = w.at<uint8_t>(w.L.buf_f1);
   float* hs = reinterpret_cast<float*>(h8 + rows * c.f);
   uint16_t* h = w.at<uint16_t>(w.L.buf_f0);
   uint16_t* o_perm = w.at<uint16_t>(w.L.buf_d1);
-  MOE_CUDA(launch_quantize_rows_e4m3(x_perm, (int64_t)rows, c.d, x8, xs, stream, w.tabs()));
+  MOE_CUDA(launch_quantize_rows_e4m3(x, c.T, c.d, x8_tok, xs_tok, stream));
+  DispatchArgs da8 = dispatch_args(w);
+  da8.idx = idx;
+  da8.x = reinterpret_cast<const uint16_t*>(x8_tok);
+  da8.x_perm = reinterpret_cast<uint16_t*>(x8);
+  da8.xs_tok = xs_tok;
+  da8.xs_perm = xs;
+  Cfg c8 = c;
+  c8.d = c.d / 2;   // an e4m3 row of d codes moves as d / 2 two-byte elements
+  MOE_CUDA(launch_dispatch_scan(c, w.L, da8, stream));
+  MOE_CUDA(launch_dispatch_gather(c8, w.L, da8, true, true, false, stream));
   GateUpFp8Args ga{x8, xs, wg8, wg_scale, wu8, wu_scale, h, w.hdr(), w.tabs()};
   MOE_CUDA(launch_gate_up_fp8(c, w.L, ga, stream));
   MOE_CUDA(launch_quantize_rows_e4m3(h, (int64_t)rows, c.f, h8, hs, stream, w.tabs()));

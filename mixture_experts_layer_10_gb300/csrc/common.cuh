@@ -148,6 +148,8 @@ struct DispatchArgs {
   uint16_t* x_perm; uint16_t* dy_perm;
   Hdr* hdr; Tables* tabs; uint32_t* scan_status; int32_t* rank;
   int32_t* prow_of_slot; int32_t* slot_of_prow; float* gate_of_prow;
+  // FP8 forward: per-token row scales carried beside the gathered e4m3 rows (nullable)
+  const float* xs_tok; float* xs_perm;
 };
 cudaError_t launch_dispatch_scan(const Cfg& c, const Layout& L, const DispatchArgs& a, cudaStream_t s);
 cudaError_t launch_dispatch_gather(const Cfg& c, const Layout& L, const DispatchArgs& a,

@@ -10,6 +10,8 @@
 //   starts, pad-row prefix and the segment order by size.
 // dispatch_gather_kernel: token owner.  A warp reads each x (and dy) row once, 16 bytes per lane,
 //   and writes it to every kept slot's row (and every shared expert's row); then zeroes pad rows.
+//   Rows are moved as 16-byte vectors, so the FP8 forward gathers e4m3 token rows (d bytes) through
+//   the same kernel as rows of d/2 two-byte elements, with their row scales beside them.
 #include <mutex>
 
 #include "common.cuh"
@@ -222,6 +224,7 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a, in
           }
         }
         if (kDy && kept) a.gate_of_prow[prow] = a.gates[slot];
+        if (kX && kept && a.xs_perm != nullptr) a.xs_perm[prow] = a.xs_tok[t];
       }
       const int ng = min(32, k - jb);
       // kUnroll vectors per lane are loaded before any is stored, so a warp keeps
@@ -267,6 +270,7 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a, in
     if (lane < S && t < tb->kept[E + lane]) {
       const size_t p = (size_t)tb->poff[E + lane] + t;
       if (kMeta) a.slot_of_prow[p] = -2;
+      if (kX && a.xs_perm != nullptr) a.xs_perm[p] = a.xs_tok[t];
       if (kDy) a.gate_of_prow[p] = 1.f;
     }
   }
@@ -287,6 +291,7 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a, in
     }
     if (lane == 0) {
       if (kMeta) a.slot_of_prow[row] = -1;
+      if (kX && a.xs_perm != nullptr) a.xs_perm[row] = 0.f;
       if (kDy) a.gate_of_prow[row] = 0.f;
     }
   }
