@@ -397,6 +397,8 @@ struct FwdDown8 : PairDefaults {
     for (int kk = 0; kk < 4; ++kk)
       umma_f8_pair(dt, sdesc_kmajor(sa + kk * 32), sdesc_kmajor(sa + kTileA + kk * 32), kIdesc, (kit | kk) != 0);
   }
+  // Two 32-column boxes per round: both TMEM loads and the 64 column scales are in flight together,
+  // and one proxy fence covers both boxes' stores.
   __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int part, int,
                                   uint8_t* ebuf) {
     const int lane = row & 31;
@@ -405,25 +407,37 @@ struct FwdDown8 : PairDefaults {
     const float* ds = p.ds + (size_t)j.seg * p.d + j.n0;
     epi_begin(lane);
 #pragma unroll 1
-    for (int c = part * 128; c < part * 128 + 128; c += 32) {
-      if (j.n0 + c >= p.d) break;
-      uint32_t v[32];
-      tmem_ld32(ta + c, v);
+    for (int c = part * 128; c < part * 128 + 128; c += 64) {
+      if (j.n0 + c >= p.d) break;   // d is a multiple of 64: a round's two boxes both exist
+      uint32_t v[2][32];
+      tmem_ld32(ta + c, v[0]);
+      tmem_ld32(ta + c + 32, v[1]);
+      float4 s4[16];                // the 64 columns' weight scales (the same for every lane)
+#pragma unroll
+      for (int q = 0; q < 16; ++q) s4[q] = __ldg(reinterpret_cast<const float4*>(ds + c) + q);
       tmem_ld_wait();
-      float sc[32];   // the 32 columns' weight scales (the same for every lane)
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float4 s4 = __ldg(reinterpret_cast<const float4*>(ds + c) + q);
-        sc[4 * q] = s4.x; sc[4 * q + 1] = s4.y; sc[4 * q + 2] = s4.z; sc[4 * q + 3] = s4.w;
+      if (c != part * 128) {        // the previous round's boxes have been read by their stores
+        if (lane == 0) bulk_wait_read<0>();
+        __syncwarp();
       }
-      uint32_t pk[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i)
-        pk[i] = pack_bf16(__uint_as_float(v[2 * i]) * sh * sc[2 * i],
-                          __uint_as_float(v[2 * i + 1]) * sh * sc[2 * i + 1]);
-      uint8_t* box = claim_box(ebuf, (c / 32) & 3, lane);
-      stage_box(box, lane, pk);
-      store_box_2d(&p.tmO, box, lane, j.n0 + c, y);
+      for (int bx = 0; bx < 2; ++bx) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float4 sc = s4[bx * 8 + i / 2];
+          const float s0 = (i & 1) ? sc.z : sc.x, s1 = (i & 1) ? sc.w : sc.y;
+          pk[i] = pack_bf16(__uint_as_float(v[bx][2 * i]) * sh * s0, __uint_as_float(v[bx][2 * i + 1]) * sh * s1);
+        }
+        stage_box(ebuf + bx * kEpiBox, lane, pk);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&p.tmO, ebuf, j.n0 + c, y);
+        tma_store_2d(&p.tmO, ebuf + kEpiBox, j.n0 + c + 32, y);
+        bulk_commit();
+      }
     }
   }
   __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
