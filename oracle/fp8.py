@@ -143,3 +143,32 @@ def layer_forward_fp8(L) -> np.ndarray:
         o_slot[slots // k, slots % k] = expert(e, L.x[slots // k])
     shared = [expert(L.E + s, L.x) for s in range(L.S)]
     return combine(o_slot, R.gates, D.row_of_slot >= 0, shared)
+
+
+def token_outputs_fp8(L, tokens: np.ndarray, cols: np.ndarray) -> np.ndarray:
+    """y[tokens][:, cols] of the e4m3 forward, one token at a time (for full-size workloads).
+
+    Routing as Layer.token_outputs (the capacity, when set, needs the queues over all tokens).  Only
+    the experts the tokens visit are quantised, and of W_down only the rows of the requested output
+    channels: each row's quantisation depends on that row alone."""
+    tokens = np.asarray(tokens, np.int64)
+    cols = np.asarray(cols, np.int64)
+    R = L.routing()
+    idx, g = R.idx[tokens], R.gates[tokens]
+    kept = L.dispatch().row_of_slot[tokens] >= 0 if L.C is not None else np.ones(idx.shape, bool)
+    xs = L.x[tokens]
+    y = np.zeros((tokens.size, cols.size))
+    for e in range(L.E + L.S):
+        if e < L.E:
+            sel = np.argwhere((idx == e) & kept)
+            if sel.size == 0:
+                continue
+            ti, gw = sel[:, 0], g[sel[:, 0], sel[:, 1]]
+        else:
+            ti, gw = np.arange(tokens.size), np.ones(tokens.size)
+        gq, gs = quantize_rows_e4m3(as_f64(L.inp["W_gate"][e]).astype(np.float32))
+        uq, us = quantize_rows_e4m3(as_f64(L.inp["W_up"][e]).astype(np.float32))
+        dq, ds = quantize_rows_e4m3(as_f64(L.inp["W_down"][e][cols]).astype(np.float32))
+        o = expert_forward_fp8(xs[ti], gq, gs, uq, us, dq, ds)
+        np.add.at(y, ti, gw[:, None] * o)
+    return y

@@ -1,8 +1,10 @@
-"""FP8 (e4m3) expert inputs on the GPU against the oracle's quantisation step (GPU).
+"""The FP8 (e4m3) forward on the GPU against the oracle's quantised forward (GPU).
 
 * the row quantiser: codes and scales bit-exact (both sides decide in fp32);
-* the e4m3 gate/up projection with SwiGLU: h of every kept row against the fp64 product of the
-  oracle's own codes and scales, under the bf16 output rule.
+* the e4m3 gate/up projection with SwiGLU and the e4m3 down projection: every kept row against the
+  fp64 product of the oracle's own codes and scales, under the bf16 output rule;
+* moe_layer_fwd_fp8: y on the small workloads, on constructed layers where every quantisation step
+  is exact, and on sampled tokens and output channels at the Mixtral- and Qwen3-like full sizes.
 """
 import numpy as np
 import pytest
@@ -11,7 +13,8 @@ import torch
 import oracle
 from oracle import fp8
 from cases import case
-from harness import check_close, check_routing, from_dev, from_dev_bf16, segment_rows, to_dev, to_dev_bf16
+from harness import (check_close, check_routing, decided_tokens, from_dev, from_dev_bf16, segment_rows, to_dev,
+                     to_dev_bf16)
 import synth
 
 pytestmark = pytest.mark.gpu
@@ -155,3 +158,29 @@ def test_layer_fwd_fp8_lossless(moe, variant):
     assert check_routing(idx, gates, L.routing(), c["k"]).all()
     y_ref, _ = L.forward()
     check_close("y (lossless fp8 forward)", y, y_ref)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,n_tok", [("mixtral", 16), ("qwen3", 4)])
+def test_layer_fwd_fp8_full_size(moe, name, n_tok):
+    """The FP8 forward at the workload's full size, as bench.py --fp8 runs it: y of sampled tokens
+    and output channels against the oracle, one token at a time.  The oracle quantises only the
+    experts the sample visits, so the Mixtral-like sample is drawn from the tokens routed to the
+    most common expert pair."""
+    cfg = synth.CONFIGS[name]
+    inp = synth.make_inputs(cfg, seed=0)
+    L = oracle.Layer(inp, cfg)
+    y, idx, gates = _run_fwd_fp8(moe, cfg, inp)
+    R = L.routing()
+    same = check_routing(idx, gates, R, cfg["k"])
+    order_ok, _ = decided_tokens(R.logits, cfg["k"])
+    pool = np.flatnonzero(same & order_ok)
+    if name == "mixtral":
+        pairs = np.sort(R.idx[pool], axis=1)
+        key = pairs[:, 0] * cfg["E"] + pairs[:, 1]
+        pool = pool[key == np.bincount(key).argmax()]
+    rng = np.random.default_rng(9)
+    toks = np.sort(rng.choice(pool, size=n_tok, replace=False))
+    cols = np.sort(rng.choice(cfg["d"], size=64, replace=False))
+    ref = fp8.token_outputs_fp8(L, toks, cols)
+    check_close("y (fp8 forward, full size)", y[toks][:, cols], ref)

@@ -146,3 +146,14 @@ def test_quantised_layer_forward_error_is_the_e4m3_size():
     y = fp8.layer_forward_fp8(L)
     rel = np.linalg.norm(y - y_ref) / np.linalg.norm(y_ref)
     assert 1e-3 < rel < 0.1
+
+
+def test_token_outputs_fp8_equal_the_layer_forward():
+    # the one-token-at-a-time form (sampled output channels) against the whole-layer form
+    import cases
+    for name in ("tiny", "gptoss_small", "deepseek_small"):
+        c, inp, L = cases.case(name)
+        y = fp8.layer_forward_fp8(L)
+        toks = np.array([0, 3, 17, c["T"] - 1])
+        cols = np.array([1, 5, c["d"] - 1])
+        np.testing.assert_allclose(fp8.token_outputs_fp8(L, toks, cols), y[toks][:, cols], rtol=1e-12, atol=1e-300)
