@@ -135,9 +135,27 @@ def _run_fwd_fp8(moe, c, inp):
     return from_dev_bf16(y), from_dev(idx), from_dev(gates)
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged_mixtral", "deepseek_small", "gptoss_small", "qwen_small"])
+@pytest.mark.parametrize("name", ["tiny", "ragged_mixtral", "deepseek_small", "gptoss_small", "qwen_small",
+                                  "single_expert", "k_equals_E", "max_experts", "max_shared", "router_e96_k8",
+                                  "router_simt_e160"])
 def test_layer_fwd_fp8(moe, name):
     c, inp, L = case(name)
+    _check_fwd_fp8(moe, c, inp, L)
+
+
+# widths that are multiples of 64 but not of 128 (the e4m3 K blocks are 128 codes: the last one is
+# half zero-filled), a single token, and a capacity of one row per expert
+@pytest.mark.parametrize("over", [dict(T=160, d=2880, f=192, E=4, k=2), dict(T=150, d=192, f=2880, E=4, k=2),
+                                  dict(T=1, d=64, f=64, E=4, k=2, S=1),
+                                  dict(T=200, d=128, f=128, E=8, k=2, cf=1.0 / 50)])
+def test_layer_fwd_fp8_shapes(moe, over):
+    c = dict(T=0, d=0, f=0, E=0, k=0, S=0, renorm=0, cf=0.0, zipf=False)
+    c.update(over)
+    inp = synth.make_inputs(c, seed=4)
+    _check_fwd_fp8(moe, c, inp, oracle.Layer(inp, c))
+
+
+def _check_fwd_fp8(moe, c, inp, L):
     y, idx, gates = _run_fwd_fp8(moe, c, inp)
     same = check_routing(idx, gates, L.routing(), c["k"])
     if not same.all():
