@@ -401,9 +401,12 @@ def main():
     # runs on a stream of its own: work on the legacy default stream would serialise with every
     # other blocking stream, the copy stream included.
     cstream = torch.cuda.Stream()
-    x_h = torch.empty(T, d, dtype=torch.bfloat16, pin_memory=True).copy_(x.cpu())
-    dy_h = torch.empty_like(x_h).copy_(dy.cpu())
-    y_h, dx_h = torch.empty_like(x_h), torch.empty_like(x_h)
+    # every host buffer pinned (empty_like does not carry pinning over): a copy to or from pageable
+    # memory blocks the host until it completes, which would serialise the next step's launches
+    def pinned():
+        return torch.empty(T, d, dtype=torch.bfloat16, pin_memory=True)
+    x_h, dy_h, y_h, dx_h = pinned().copy_(x.cpu()), pinned().copy_(dy.cpu()), pinned(), pinned()
+    assert all(t.is_pinned() for t in (x_h, dy_h, y_h, dx_h))
     xin = [torch.empty_like(x), torch.empty_like(x)]
     dyin = [torch.empty_like(dy), torch.empty_like(dy)]
     yout = [torch.empty_like(y), torch.empty_like(y)]
