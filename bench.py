@@ -133,8 +133,15 @@ def fp8_forward(args, mc, cfg, x, W_r, b_r, Wg, Wu, Wd, buf, N, tensor_peak, ten
     if n:   # x rows and h rows: bf16 in, codes and a scale out
         gbs = (N * (d + f) * 3 + 8 * N) * args.steps / (tot / 1000.0) / 1e9
         kern["quantize_e4m3"] = {"ms_per_step": tot / args.steps, "gbs": gbs, "frac": gbs / pk["hbm"]}
+    # the resource model's roofline for both forwards, on the same peaks
+    from mixture_experts_layer_10_gb300 import resource_model
+    n_routed = N - cfg["S"] * T
+    p16 = resource_model.predict_forward_ms(cfg, tensor_peak, pk["hbm"], N=n_routed)["step_ms"]
+    p8 = resource_model.predict_forward_ms(cfg, tensor_peak, pk["hbm"], N=n_routed, fp8=True)["step_ms"]
     return {"metric": "forward tokens/s (e4m3 expert GEMMs)", "value": T / (ms8 / 1000.0), "fwd_ms": ms8,
             "bf16_fwd_ms": ms16, "speedup_vs_bf16_fwd": ms16 / ms8,
+            "model": {"fp8_fwd_predicted_ms": p8, "fp8_measured_over_predicted": ms8 / p8,
+                      "bf16_fwd_predicted_ms": p16, "bf16_measured_over_predicted": ms16 / p16},
             "peak_tflops": peak8, "peak_kind": "2 x " + tensor_kind.split(":")[0] + " (nominal fp8:bf16 ratio)",
             "kernels": kern}
 

@@ -97,3 +97,42 @@ def predict_ms(cfg: dict, tensor_tflops: float, hbm_gbs: float, N: int | None = 
         per[name] = 1e3 * max(t_tc, t_hbm)
     total = sum(per.values()) + launches * LAUNCH_US / 1e3
     return {"step_ms": total, "per_kernel_ms": per}
+
+
+def work_forward(cfg: dict, N: int | None = None, fp8: bool = False) -> dict:
+    """FLOPs and algorithmic HBM bytes per kernel of the forward alone, in bf16 (moe_layer_fwd) or
+    with e4m3 expert GEMMs (moe_layer_fwd_fp8: the token rows quantised once, their codes and row
+    scales gathered, h quantised per row between the projections).  FP8 FLOPs are reported under
+    "fp8_flops" so that the prediction can run them at the FP8 tensor rate."""
+    T, d, f, E, k, S = cfg["T"], cfg["d"], cfg["f"], cfg["E"], cfg["k"], cfg.get("S", 0)
+    N = T * k if N is None else N
+    R = N + S * T
+    Ep = math.ceil(E / 64) * 64
+    tc_router = E <= 128 and k <= 8
+    out = {"route_fwd": {"flops": 2 * T * d * (3 * Ep if tc_router else E), "bytes": T * d * 2}}
+    if fp8:
+        out["quantize_e4m3 (x)"] = {"flops": 0, "bytes": T * d * 3 + 4 * T}
+        out["dispatch_gather"] = {"flops": 0, "bytes": (T + R) * d + 8 * R + 12 * T * k}
+        out["gemm_gate_up_fp8"] = {"flops": 0, "fp8_flops": 4 * R * d * f, "bytes": 0}
+        out["quantize_e4m3 (h)"] = {"flops": 0, "bytes": R * f * 3 + 4 * R}
+        out["gemm_down_fp8"] = {"flops": 0, "fp8_flops": 2 * R * d * f, "bytes": 0}
+    else:
+        out["dispatch_gather"] = {"flops": 0, "bytes": (T + R) * d * 2 + 12 * T * k}
+        out["gemm_gate_up_swiglu"] = {"flops": 4 * R * d * f, "bytes": 0}
+        out["gemm_down"] = {"flops": 2 * R * d * f, "bytes": 0}
+    out["combine"] = {"flops": 0, "bytes": (R + T) * d * 2 + 8 * T * k}
+    return out
+
+
+def predict_forward_ms(cfg: dict, tensor_tflops: float, hbm_gbs: float, N: int | None = None,
+                       fp8: bool = False) -> dict:
+    """Roofline time of the forward alone; FP8 GEMMs at twice the bf16 tensor rate (the nominal
+    ratio of the dense FP8 and bf16 peaks)."""
+    per = {}
+    work_ = work_forward(cfg, N, fp8)
+    for name, w in work_.items():
+        t_tc = (w["flops"] + w.get("fp8_flops", 0) / 2) / (tensor_tflops * 1e12)
+        t_hbm = w["bytes"] / (hbm_gbs * 1e9)
+        per[name] = 1e3 * max(t_tc, t_hbm)
+    total = sum(per.values()) + (len(work_) + 1) * LAUNCH_US / 1e3   # + the dispatch scan
+    return {"step_ms": total, "per_kernel_ms": per}

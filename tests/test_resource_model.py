@@ -41,3 +41,30 @@ def test_prediction_is_a_roofline():
     assert p["per_kernel_ms"]["gemm_wgrad"] == pytest.approx(rm.work(cfg)["gemm_wgrad"]["flops"] / 1e12)
     assert p["per_kernel_ms"]["combine"] == pytest.approx(rm.work(cfg)["combine"]["bytes"] / 5e9)
     assert p["step_ms"] > sum(v for v in p["per_kernel_ms"].values())
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+def test_forward_work_closed_forms(name):
+    cfg = synth.CONFIGS[name]
+    T, d, f, k, S = cfg["T"], cfg["d"], cfg["f"], cfg["k"], cfg["S"]
+    R = T * k + S * T
+    bf = rm.work_forward(cfg)
+    q = rm.work_forward(cfg, fp8=True)
+    # the same 6 R d f GEMM FLOPs, in bf16 or in e4m3
+    assert sum(v["flops"] for n, v in bf.items() if n.startswith("gemm_")) == 6 * R * d * f
+    assert sum(v.get("fp8_flops", 0) for v in q.values()) == 6 * R * d * f
+    # the FP8 forward gathers one-byte codes: half the rows' bytes of the bf16 gather, plus scales
+    meta = 12 * T * k
+    assert q["dispatch_gather"]["bytes"] - 8 * R - meta == (bf["dispatch_gather"]["bytes"] - meta) // 2
+    # its quantisation passes read bf16 and write codes once: x over T rows, h over R rows
+    assert q["quantize_e4m3 (x)"]["bytes"] == 3 * T * d + 4 * T
+    assert q["quantize_e4m3 (h)"]["bytes"] == 3 * R * f + 4 * R
+
+
+def test_forward_prediction_runs_fp8_at_twice_the_rate():
+    cfg = synth.CONFIGS["mixtral"]
+    bf = rm.predict_forward_ms(cfg, tensor_tflops=1000.0, hbm_gbs=5000.0)
+    q = rm.predict_forward_ms(cfg, tensor_tflops=1000.0, hbm_gbs=5000.0, fp8=True)
+    assert q["per_kernel_ms"]["gemm_gate_up_fp8"] == pytest.approx(bf["per_kernel_ms"]["gemm_gate_up_swiglu"] / 2)
+    assert q["per_kernel_ms"]["gemm_down_fp8"] == pytest.approx(bf["per_kernel_ms"]["gemm_down"] / 2)
+    assert q["step_ms"] < bf["step_ms"]
