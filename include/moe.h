@@ -203,14 +203,16 @@ moe_status_t moe_router_bwd(const moe_config_t* cfg, const moe_bf16* x, const fl
 moe_status_t moe_combine_bwd(const moe_config_t* cfg, const moe_bf16* dx_perm, const float* dlogits,
                              const float* W_r, moe_bf16* dx, void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* FP8 experts, first step: quantised expert inputs (the MoEBlaze summary names mixed-precision and
- * quantised experts as future work; the format is this library's reading).  Format: OCP FP8 E4M3
- * (max 448, no infinities), one fp32 scale per row.
+/* FP8 expert GEMMs, forward (the MoEBlaze summary names mixed-precision and quantised experts as
+ * future work; the format is this library's reading).  Format: OCP FP8 E4M3 (max 448, no
+ * infinities), one fp32 scale per row.  The steps are exposed one by one (quantise, gate/up, down)
+ * and composed by moe_layer_fwd_fp8 below.
  *
  * moe_quantize_rows_e4m3: src [rows, cols] bf16 -> codes [rows, cols] uint8 and scales [rows]
  * fp32, with scale = amax / 448 over the row (1 for an all-zero row) and code = e4m3(v / scale),
  * both in fp32, rounded to nearest even and saturated.  cols a multiple of 16, at most 16384;
- * 16-byte-aligned pointers.  Used for x_perm rows and for the rows (output channels) of W_gate and W_up. */
+ * 16-byte-aligned pointers.  Used for token or x_perm rows, h rows, and the rows (output channels)
+ * of W_gate, W_up and W_down.  Argument errors are returned before any work is queued. */
 moe_status_t moe_quantize_rows_e4m3(const moe_bf16* src, int64_t rows, int32_t cols, uint8_t* codes,
                                     float* scales, moe_stream_t stream);
 
