@@ -951,13 +951,17 @@ struct RouterLogits : PolicyDefaults {
 #pragma unroll
     for (int q = 0; q < 3; ++q) tma_load_3d(st + (1 + q) * kTileA, &p.tmW, bar, kx, 0, q);
   }
+  // The hi and mid parts sit in adjacent 128-row slots (rows past Ep are TMA zero fill), so one
+  // N = 256 MMA covers both and lands hi in columns [0, Ep) and mid in [128, 128 + Ep); lo then
+  // accumulates onto mid.  Two MMAs per 16-deep step instead of three: the router is bound by MMA
+  // issue, not by the tensor pipe.
+  static constexpr uint32_t kIdescHiMid = idesc_bf16(128, 256, false, false);
   __device__ static void mma(const Job& j, int kit, uint32_t sa, uint32_t dt, int) {
 #pragma unroll
     for (int kk = 0; kk < kBK / 16; ++kk) {
       const uint64_t da = sdesc_kmajor(sa + kk * 32);
       const bool acc = (kit | kk) != 0;
-      umma_bf16(dt, da, sdesc_kmajor(sa + kTileA + kk * 32), j.idesc, acc);
-      umma_bf16(dt + 128, da, sdesc_kmajor(sa + 2 * kTileA + kk * 32), j.idesc, acc);
+      umma_bf16(dt, da, sdesc_kmajor(sa + kTileA + kk * 32), kIdescHiMid, acc);
       umma_bf16(dt + 128, da, sdesc_kmajor(sa + 3 * kTileA + kk * 32), j.idesc, true);
     }
   }
