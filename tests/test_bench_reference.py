@@ -1,0 +1,23 @@
+"""bench.py's reference arm (the oracle on the host cores) keeps the JSON line contract (CPU)."""
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_reference_arm_json_line():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny", "--steps", "2",
+                        "--warmup", "3"], cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    j = json.loads(lines[0])
+    assert j["impl"] == "reference"
+    assert j["value"] > 0 and j["unit"] == "tokens/s" and j["higher_is_better"] is True
+    assert j["steps"] == 2 and j["warmup"] == 3 and j["ms_per_step"] > 0 and j["n_gpus"] == 1
+    assert j["config"]["workload"].startswith("tiny")
+    assert j["e2e"] == {"value": j["value"], "unit": j["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+    cb = j["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == j["value"] and cb["cores"] >= 1 and cb["sample"]
