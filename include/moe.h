@@ -239,7 +239,9 @@ moe_status_t moe_down_fp8(const moe_config_t* cfg, const uint8_t* h8, const floa
  * expert row quantise x_perm, moe_gate_up_fp8 (h kept in bf16), quantise h, moe_down_fp8, and the
  * combine.  The weights come quantised (moe_quantize_rows_e4m3 of every row of W_gate, W_up and
  * W_down, as above).  The router stays fp32.  Fills `saved` like moe_layer_fwd (idx, gates), so
- * moe_layer_bwd can follow with the bf16 weights.  Only the rows this step fills are quantised. */
+ * moe_layer_bwd can follow with the bf16 weights.  Only the rows this step fills are quantised.
+ * keep_rows must be 0 (MOE_ERR_INVALID_ARG otherwise): the call's scratch uses the workspace
+ * buffers that would carry kept activations to the backward. */
 moe_status_t moe_layer_fwd_fp8(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
                                const uint8_t* wg8, const float* wg_scale, const uint8_t* wu8,
                                const float* wu_scale, const uint8_t* wd8, const float* wd_scale, moe_bf16* y,

@@ -558,6 +558,8 @@ moe_status_t moe_layer_fwd_fp8(const moe_config_t* cfg, const moe_bf16* x, const
                                void* saved, void* ws, size_t ws_bytes, moe_stream_t stream) {
   Cfg c;
   MOE_TRY(make_cfg(cfg, &c));
+  // its scratch lives in the backward's buffers, where kept activations would have to survive
+  MOE_NEED(cfg->keep_rows == 0);
   MOE_NEED(x && W_r && wg8 && wg_scale && wu8 && wu_scale && wd8 && wd_scale && y && saved);
   MOE_NEED(aligned16(x) && aligned16(W_r) && (!b_r || aligned16(b_r)) && aligned16(wg8) && aligned16(wg_scale) &&
            aligned16(wu8) && aligned16(wu_scale) && aligned16(wd8) && aligned16(wd_scale) && aligned16(y) &&

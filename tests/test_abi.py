@@ -92,3 +92,8 @@ def test_fp8_arguments_rejected(lib):
                                0x100000, ws, None) == 1
     assert lib.moe_layer_fwd_fp8(ctypes.byref(c), 0x10000, 0x20000, None, 0x30000, 0x40000, 0x50000, None,
                                  0x70000, 0x80000, 0x90000, 0xA0000, 0x100000, ws, None) == 1
+    # kept activations cannot survive the FP8 forward's scratch
+    ck = moe.config(T=64, d=128, f=256, E=8, k=2, keep_rows=256)
+    wsk, _ = moe.moe_workspace_size(ck)
+    assert lib.moe_layer_fwd_fp8(ctypes.byref(ck), 0x10000, 0x20000, None, 0x30000, 0x40000, 0x50000, 0x60000,
+                                 0x70000, 0x80000, 0x90000, 0xA0000, 0x100000, wsk, None) == 1
