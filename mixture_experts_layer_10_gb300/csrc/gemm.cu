@@ -225,6 +225,7 @@ struct FwdGateUpT : PairDefaults {
   __device__ static Job job(const Params& p, const SegSmem& s, int t) {
     return row_job(s, t, p.nt, 128, p.d / kBK);
   }
+  __device__ static int mma_kiters(const Params& p, const SegSmem& s, int t) { (void)s; (void)t; return p.d / kBK; }
   __device__ static void prefetch(const Params& p) {
     tma_prefetch(&p.tmX); tma_prefetch(&p.tmWg); tma_prefetch(&p.tmWu);
   }
@@ -312,6 +313,7 @@ struct FwdGateUp8 : PairDefaults {
   __device__ static Job job(const Params& p, const SegSmem& s, int t) {
     return row_job(s, t, p.nt, 128, (p.d + kBK8 - 1) / kBK8);
   }
+  __device__ static int mma_kiters(const Params& p, const SegSmem& s, int t) { (void)s; (void)t; return (p.d + kBK8 - 1) / kBK8; }
   __device__ static void prefetch(const Params& p) {
     tma_prefetch(&p.tmX); tma_prefetch(&p.tmWg); tma_prefetch(&p.tmWu);
   }
@@ -387,6 +389,7 @@ struct FwdDown8 : PairDefaults {
   __device__ static Job job(const Params& p, const SegSmem& s, int t) {
     return row_job(s, t, p.nt, 256, (p.f + kBK8 - 1) / kBK8);
   }
+  __device__ static int mma_kiters(const Params& p, const SegSmem& s, int t) { (void)s; (void)t; return (p.f + kBK8 - 1) / kBK8; }
   __device__ static void prefetch(const Params& p) { tma_prefetch(&p.tmH); tma_prefetch(&p.tmWd); }
   __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint32_t cbar, int rank) {
     tma_load_2d_pair(st, &p.tmH, cbar, kit * kBK8, j.m0 + kBM * rank);
@@ -476,6 +479,7 @@ struct FwdDown : PairDefaults {
   __device__ static Job job(const Params& p, const SegSmem& s, int t) {
     return row_job(s, t, p.nt, 256, p.f / kBK);
   }
+  __device__ static int mma_kiters(const Params& p, const SegSmem& s, int t) { (void)s; (void)t; return p.f / kBK; }
   __device__ static void prefetch(const Params& p) { tma_prefetch(&p.tmH); tma_prefetch(&p.tmWd); }
   __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint32_t cbar, int rank) {
     tma_load_2d_pair(st, &p.tmH, cbar, kit * kBK, j.m0 + kBM * rank);
@@ -507,6 +511,7 @@ struct BwdDh : PairDefaults {
   __device__ static Job job(const Params& p, const SegSmem& s, int t) {
     return row_job(s, t, p.nt, 256, p.d / kBK);
   }
+  __device__ static int mma_kiters(const Params& p, const SegSmem& s, int t) { (void)s; (void)t; return p.d / kBK; }
   __device__ static void prefetch(const Params& p) { tma_prefetch(&p.tmDY); tma_prefetch(&p.tmWdT); }
   __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint32_t cbar, int rank) {
     tma_load_2d_pair(st, &p.tmDY, cbar, kit * kBK, j.m0 + kBM * rank);
@@ -545,6 +550,7 @@ struct BwdFused : PairDefaults {
     if (j.m0 < p.keep_rows) j.kiters = 0;
     return j;
   }
+  __device__ static int mma_kiters(const Params& p, const SegSmem& s, int t) { return p.keep_rows > 0 ? job(p, s, t).kiters : p.d / kBK; }
   __device__ static void prefetch(const Params& p) {
     tma_prefetch(&p.tmX); tma_prefetch(&p.tmWg); tma_prefetch(&p.tmWu);
   }
@@ -635,6 +641,7 @@ struct DgradX : PairDefaults {
   __device__ static Job job(const Params& p, const SegSmem& s, int t) {
     return row_job(s, t, p.nt, 256, 2 * p.f / kBK);
   }
+  __device__ static int mma_kiters(const Params& p, const SegSmem& s, int t) { (void)s; (void)t; return 2 * p.f / kBK; }
   __device__ static void prefetch(const Params& p) {
     tma_prefetch(&p.tmDA); tma_prefetch(&p.tmDB); tma_prefetch(&p.tmWgT); tma_prefetch(&p.tmWuT);
   }
@@ -674,6 +681,10 @@ struct Wgrad : PairDefaults {
     const Tables* tabs;
   };
   __device__ static int num_tiles(const Params& p, const SegSmem& s) { return s.G * p.tps; }
+  __device__ static int mma_kiters(const Params& p, const SegSmem& s, int t) {
+    const int g = s.seg_order[t / p.tps];
+    return (s.poff[g + 1] - s.poff[g]) / kBK;
+  }
   __device__ static Job job(const Params& p, const SegSmem& s, int t) {
     const int pos = t / p.tps;
     int r = t - pos * p.tps;
@@ -1393,9 +1404,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<P>(), 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       int seq = 0;
+      const Job j{};   // the pair problems' MMAs depend only on the K block
       for (int t = pair; t < ntiles && !*abort_flag; t += npairs) {
-        const Job j = P::job(p, segs, t);
-        if (j.kiters == 0) continue;
+        // the tile's K blocks only: the single issuing thread bounds these kernels, and a full
+        // job (segment search, divisions) between tiles leaves the tensor pipe idle
+        const int kiters = P::mma_kiters(p, segs, t);
+        if (kiters == 0) continue;
         const uint32_t dt = tmem_base + (uint32_t)(acc * P::kAccCols);
         // both CTAs' epilogues must have released this accumulator
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, limit, abort_flag)) {
@@ -1405,7 +1419,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<P>(), 1)
         }
         tc_fence_after();
         bool ok = true;
-        for (int k0 = 0; k0 < j.kiters; k0 += kSub) {
+        for (int k0 = 0; k0 < kiters; k0 += kSub) {
           if (!mbar_wait(&full[slot], phase, limit, abort_flag)) {
             record_error(p.hdr, MOE_ERR_TIMEOUT, kSiteGemmMma);
             *abort_flag = 1;
@@ -1413,7 +1427,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<P>(), 1)
             break;
           }
           tc_fence_after();
-          const int nsb = min(kSub, j.kiters - k0);
+          const int nsb = min(kSub, kiters - k0);
           const uint32_t sa = smem_u32(stages + (size_t)slot * kSlotBytes);
           for (int sb = 0; sb < nsb; ++sb) P::mma(j, k0 + sb, sa + sb * P::kStageBytes, dt, seq);
           umma_commit_pair(smem_u32(&empty[slot]));
