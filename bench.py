@@ -24,6 +24,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -146,11 +147,20 @@ def fp8_forward(args, mc, cfg, x, W_r, b_r, Wg, Wu, Wd, buf, N, tensor_peak, ten
             "kernels": kern}
 
 
+def code_only(src: str) -> str:
+    """CUDA/C++ source without comments and whitespace runs: what the compiler sees of it."""
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", " ", src)
+    return " ".join(src.split())
+
+
 def kernel_source_hash() -> str:
+    """Identifies the kernels' code (comments and layout ignored), so recorded counters stay valid
+    across comment-only edits and lapse with any code change."""
     h = hashlib.sha256()
     for n in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "mixture_experts_layer_10_gb300", "csrc", n), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "mixture_experts_layer_10_gb300", "csrc", n), encoding="utf-8") as fh:
+            h.update(code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -18,7 +18,8 @@
 // SM's shared-memory bandwidth (TMA writes plus tensor-core reads) before the tensor cores.
 // Rows are the dispatch's padded expert segments (multiples of 256), so every 256-row pair tile
 // belongs to one expert and the per-expert tile scheduler is a table walk done identically by
-// the three roles of both CTAs.  Every wait is bounded (MOE_ERR_TIMEOUT instead of a hang).
+// the three roles of both CTAs (the MMA thread needs only each tile's K-block count, which it
+// derives without the walk).  Every wait is bounded (MOE_ERR_TIMEOUT instead of a hang).
 //
 // Problems (BK = 64, operands bf16, accumulators fp32; pair tiles M = 256 unless noted):
 //   FwdGateUp  H    = silu(X Wg^T) * (X Wu^T)              A=X K-major, B=[Wg;Wu] K-major, N=256
@@ -34,6 +35,9 @@
 //              one CTA, M = 128
 //   RouterLogits  l = x W_r with W_r in three bf16 parts; epilogue: softmax, top-k, or the
 //              router's dlogits                          A and B K-major, N = E padded to 64
+//   FwdGateUp8 H    = silu(sx sg (X8 Wg8^T)) * (sx su (X8 Wu8^T)), e4m3 operands (kind::f8f6f4),
+//              K blocks of 128 codes, row / channel scales applied in the epilogue      N=256
+//   FwdDown8   O    = sh sd (H8 Wd8^T), e4m3 operands, eight epilogue warps             N=256
 #include <algorithm>
 #include <mutex>
 
