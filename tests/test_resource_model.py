@@ -68,3 +68,11 @@ def test_forward_prediction_runs_fp8_at_twice_the_rate():
     assert q["per_kernel_ms"]["gemm_gate_up_fp8"] == pytest.approx(bf["per_kernel_ms"]["gemm_gate_up_swiglu"] / 2)
     assert q["per_kernel_ms"]["gemm_down_fp8"] == pytest.approx(bf["per_kernel_ms"]["gemm_down"] / 2)
     assert q["step_ms"] < bf["step_ms"]
+
+
+def test_kernel_source_hash_ignores_comments_only():
+    import bench
+    a = "int f(int x) {  // doubles\n  return 2 * x; /* twice */ }\n"
+    b = "int f(int x) {\n  /* a different\n comment */ return 2 * x; }"
+    assert bench.code_only(a) == bench.code_only(b) == "int f(int x) { return 2 * x; }"
+    assert bench.code_only(a) != bench.code_only(a.replace("2 *", "3 *"))
