@@ -131,8 +131,8 @@ def fp8_forward(args, mc, cfg, x, W_r, b_r, Wg, Wu, Wd, buf, N, tensor_peak, ten
             tf = flops * n / (tot / 1000.0) / 1e12
             kern[name] = {"ms_per_step": tot / args.steps, "tflops": tf, "frac": tf / peak8}
     tot, n = prof.get("quantize_e4m3", (0.0, 0))
-    if n:   # x rows and h rows: bf16 in, codes and a scale out
-        gbs = (N * (d + f) * 3 + 8 * N) * args.steps / (tot / 1000.0) / 1e9
+    if n:   # the T token rows of x and the N rows of h: bf16 in, codes and a scale out
+        gbs = ((T * d + N * f) * 3 + 4 * (T + N)) * args.steps / (tot / 1000.0) / 1e9
         kern["quantize_e4m3"] = {"ms_per_step": tot / args.steps, "gbs": gbs, "frac": gbs / pk["hbm"]}
     # the resource model's roofline for both forwards, on the same peaks
     from mixture_experts_layer_10_gb300 import resource_model
