@@ -90,7 +90,7 @@ extern "C" {
 typedef enum {
     MOE_OK = 0,
     MOE_ERR_INVALID_ARG = 1,   /* a null pointer, a misaligned pointer or a shape out of range */
-    MOE_ERR_UNSUPPORTED = 2,   /* a valid shape this build does not handle (or not an sm_103 device) */
+    MOE_ERR_UNSUPPORTED = 2,   /* a valid shape the library does not handle (or not an sm_103 device) */
     MOE_ERR_WORKSPACE = 3,     /* workspace smaller than moe_workspace_size() */
     MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
     MOE_ERR_BAD_INDEX = 5,     /* (device) an expert id outside [0, E); that slot is dropped */
