@@ -97,3 +97,12 @@ def test_fp8_arguments_rejected(lib):
     wsk, _ = moe.moe_workspace_size(ck)
     assert lib.moe_layer_fwd_fp8(ctypes.byref(ck), 0x10000, 0x20000, None, 0x30000, 0x40000, 0x50000, 0x60000,
                                  0x70000, 0x80000, 0x90000, 0xA0000, 0x100000, wsk, None) == 1
+
+
+def test_a_library_that_does_not_load_raises(tmp_path, monkeypatch):
+    # no fallback: a broken library file is an error, never a silent CPU path
+    bad = tmp_path / "libmoe.so"
+    bad.write_bytes(b"not a shared object")
+    monkeypatch.setattr(moe, "_lib", None)
+    with pytest.raises(OSError):
+        moe.load(str(bad))
