@@ -31,6 +31,9 @@ CASES = {
     # limits: the most routed experts (256), and the most shared experts (8) at the narrowest widths
     "max_experts": dict(T=700, d=64, E=256, k=2, f=64, S=0, renorm=0, cf=0.0, zipf=False),
     "max_shared": dict(T=300, d=64, E=4, k=1, f=64, S=8, renorm=1, cf=0.0, zipf=False),
+    # the widest rows the library accepts: d_model = 16384, and d_ff = 16384
+    "max_d_model": dict(T=96, d=16384, E=4, k=2, f=128, S=1, renorm=0, cf=0.0, zipf=False),
+    "max_d_ff": dict(T=96, d=128, E=4, k=2, f=16384, S=1, renorm=0, cf=0.0, zipf=False),
 }
 
 FAST = ["tiny", "ragged_mixtral", "deepseek_small", "qwen_small", "gptoss_small"]

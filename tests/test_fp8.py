@@ -137,7 +137,7 @@ def _run_fwd_fp8(moe, c, inp):
 
 @pytest.mark.parametrize("name", ["tiny", "ragged_mixtral", "deepseek_small", "gptoss_small", "qwen_small",
                                   "single_expert", "k_equals_E", "max_experts", "max_shared", "router_e96_k8",
-                                  "router_simt_e160"])
+                                  "router_simt_e160", "max_d_model", "max_d_ff"])
 def test_layer_fwd_fp8(moe, name):
     c, inp, L = case(name)
     _check_fwd_fp8(moe, c, inp, L)
