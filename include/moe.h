@@ -235,11 +235,13 @@ moe_status_t moe_down_fp8(const moe_config_t* cfg, const uint8_t* h8, const floa
                           const float* wd_scale, moe_bf16* o_perm, void* ws, size_t ws_bytes,
                           moe_stream_t stream);
 
-/* The whole forward with e4m3 expert GEMMs: route and dispatch as moe_layer_fwd, then per padded
- * expert row quantise x_perm, moe_gate_up_fp8 (h kept in bf16), quantise h, moe_down_fp8, and the
- * combine.  The weights come quantised (moe_quantize_rows_e4m3 of every row of W_gate, W_up and
- * W_down, as above).  The router stays fp32.  Fills `saved` like moe_layer_fwd (idx, gates), so
- * moe_layer_bwd can follow with the bf16 weights.  Only the rows this step fills are quantised.
+/* The whole forward with e4m3 expert GEMMs: route as moe_layer_fwd; quantise the T token rows of
+ * x once (a row's codes are the same in every expert it visits); dispatch, gathering those codes
+ * and row scales into the padded expert rows; moe_gate_up_fp8 (h kept in bf16); quantise the h
+ * rows this step fills; moe_down_fp8; and the combine.  The weights come quantised
+ * (moe_quantize_rows_e4m3 of every row of W_gate, W_up and W_down, as above).  The router stays
+ * fp32.  Fills `saved` like moe_layer_fwd (idx, gates), so moe_layer_bwd can follow with the bf16
+ * weights.
  * keep_rows must be 0 (MOE_ERR_INVALID_ARG otherwise): the call's scratch uses the workspace
  * buffers that would carry kept activations to the backward. */
 moe_status_t moe_layer_fwd_fp8(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
