@@ -179,12 +179,13 @@ def test_layer_fwd_fp8_lossless(moe, variant):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name,n_tok", [("mixtral", 16), ("qwen3", 4)])
+@pytest.mark.parametrize("name,n_tok", [("mixtral", 16), ("qwen3", 4), ("deepseek", 4), ("gptoss", 4)])
 def test_layer_fwd_fp8_full_size(moe, name, n_tok):
     """The FP8 forward at the workload's full size, as bench.py --fp8 runs it: y of sampled tokens
     and output channels against the oracle, one token at a time.  The oracle quantises only the
     experts the sample visits, so the Mixtral-like sample is drawn from the tokens routed to the
-    most common expert pair."""
+    most common expert pair.  With a capacity, a slot's survival depends on every earlier token's
+    routing, so the sample comes from the tokens before the first routing difference."""
     cfg = synth.CONFIGS[name]
     inp = synth.make_inputs(cfg, seed=0)
     L = oracle.Layer(inp, cfg)
@@ -192,7 +193,10 @@ def test_layer_fwd_fp8_full_size(moe, name, n_tok):
     R = L.routing()
     same = check_routing(idx, gates, R, cfg["k"])
     order_ok, _ = decided_tokens(R.logits, cfg["k"])
-    pool = np.flatnonzero(same & order_ok)
+    agree = same & order_ok
+    if cfg["cf"] > 0 and not same.all():
+        agree[int(np.flatnonzero(~same)[0]):] = False
+    pool = np.flatnonzero(agree)
     if name == "mixtral":
         pairs = np.sort(R.idx[pool], axis=1)
         key = pairs[:, 0] * cfg["E"] + pairs[:, 1]
