@@ -24,7 +24,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .moe_oracle import as_f64, combine, f64_to_bf16_value
+from .moe_oracle import as_f64, combine, f64_to_bf16_value, router_backward, router_backward_logits
 
 E4M3_MAX = 448.0
 _MIN_NORMAL_EXP = -6          # smallest normal: 2^-6
@@ -172,3 +172,105 @@ def token_outputs_fp8(L, tokens: np.ndarray, cols: np.ndarray) -> np.ndarray:
         o = expert_forward_fp8(xs[ti], gq, gs, uq, us, dq, ds)
         np.add.at(y, ti, gw[:, None] * o)
     return y
+
+
+# ---------------------------------------------------------------------------------------------
+# e4m3 backward (oracle only: the kernels of this step are not built yet)
+#
+# Reading, continuing the forward's: the two data-gradient products take e4m3 operands,
+#   dh' = dY W_d        left: dY rows, per row;  right: the rows of W_d^T (W_d's columns, one
+#                       scale per d_ff channel)
+#   dX  = dA W_g + dB W_u   left: the row [dA | dB], one scale over both halves; right: the rows of
+#                       [W_g^T | W_u^T] (column i of W_g and of W_u, one scale per d_model channel)
+# a and b come from the forward's codes; dh', dA, dB and Hg are held in bf16 (the precision of
+# those buffers in the bf16 path) and quantised from those bf16 values; the weight gradients stay
+# bf16 GEMMs (their K runs over rows), so they take the rounded dA, dB, Hg exactly.
+# ---------------------------------------------------------------------------------------------
+
+def quantize_cols_e4m3(W: np.ndarray):
+    """Per-column e4m3 codes of a [rows, cols] matrix of exact fp32 values, returned as the codes
+    of W^T ([cols, rows], the K-major operand whose rows are W's columns) and one scale per column."""
+    return quantize_rows_e4m3(np.asarray(W, np.float32).T)
+
+
+def gate_up_pre_fp8(xq, xs, gq, gs, uq, us):
+    """a and b (float64) of quantised rows, before the SwiGLU: the products gate_up_fp8 combines."""
+    x = dequantize_rows(xq, xs)
+    return x @ dequantize_rows(gq, gs).T, x @ dequantize_rows(uq, us).T
+
+
+def dh_fp8(dyq, dys, wdtq, wdts):
+    """dh' = (s_dy q_dy)(s_w q_w)^T: dY rows [n, d] codes with row scales; wdtq [f, d] the codes of
+    W_d^T (W_d's columns) with one scale per d_ff channel."""
+    return dequantize_rows(dyq, dys) @ dequantize_rows(wdtq, wdts).T
+
+
+def dx_fp8(dabq, dabs, wgutq, wguts):
+    """dX = [dA | dB] [W_g ; W_u]: dabq [n, 2f] codes of the joined rows with their scales; wgutq
+    [d, 2f] the codes of [W_g^T | W_u^T] (column i of W_g then of W_u) with one scale per d_model
+    channel."""
+    return dequantize_rows(dabq, dabs) @ dequantize_rows(wgutq, wguts).T
+
+
+def _bf16(v):
+    return f64_to_bf16_value(v)
+
+
+def expert_backward_fp8(xr, dyr, g, Wg, Wu, Wd):
+    """The e4m3 backward of g * expert(xr) for rows xr (exact fp32 values) with upstream dyr and
+    per-row gate g, in the steps and precisions of the reading above.
+
+    Returns dxr, dWg, dWu, dWd, dg as expert_backward does."""
+    f32 = lambda v: np.asarray(v, np.float32)
+    xq, xs = quantize_rows_e4m3(f32(xr))
+    gq, gs = quantize_rows_e4m3(f32(Wg))
+    uq, us = quantize_rows_e4m3(f32(Wu))
+    a, b = gate_up_pre_fp8(xq, xs, gq, gs, uq, us)
+    dyq, dys = quantize_rows_e4m3(f32(dyr))
+    wdtq, wdts = quantize_cols_e4m3(f32(Wd))
+    dhp = _bf16(dh_fp8(dyq, dys, wdtq, wdts))             # dh' held in bf16
+    s = 1.0 / (1.0 + np.exp(-a))
+    h = a * s * b
+    dg = np.sum(dhp * h, axis=1)
+    dh = np.asarray(g, np.float64)[:, None] * dhp
+    dA = _bf16(dh * b * s * (1.0 + a * (1.0 - s)))
+    dB = _bf16(dh * (a * s))
+    Hg = _bf16(np.asarray(g, np.float64)[:, None] * h)
+    dabq, dabs = quantize_rows_e4m3(f32(np.concatenate([dA, dB], axis=1)))
+    wgutq, wguts = quantize_cols_e4m3(f32(np.concatenate([Wg, Wu], axis=0)))
+    dxr = dx_fp8(dabq, dabs, wgutq, wguts)
+    xr64 = np.asarray(xr, np.float64)
+    dWg = dA.T @ xr64
+    dWu = dB.T @ xr64
+    dWd = np.asarray(dyr, np.float64).T @ Hg
+    return dxr, dWg, dWu, dWd, dg
+
+
+def layer_backward_fp8(L) -> dict:
+    """All gradients of sum(dy * y) with the e4m3 backward of every expert (routing, dispatch and the
+    router backward as Layer.backward)."""
+    R, D = L.routing(), L.dispatch()
+    T, k, d, f, E, S = L.T, L.k, L.d, L.f, L.E, L.S
+    dx = np.zeros((T, d))
+    dW_gate, dW_up, dW_down = np.zeros((E + S, f, d)), np.zeros((E + S, f, d)), np.zeros((E + S, d, f))
+    dgates = np.zeros((T, k))
+    for e in range(E + S):
+        Wg, Wu, Wd = L.W(e)
+        if e < E:
+            rows = np.arange(D.offsets[e], D.offsets[e + 1])
+            if rows.size == 0:
+                continue
+            slots = D.slot_of_row[rows]
+            t_of, j_of = slots // k, slots % k
+            gw = R.gates[t_of, j_of]
+        else:
+            t_of, j_of, gw = np.arange(T), None, np.ones(T)
+        dxr, dWg, dWu, dWd, dg = expert_backward_fp8(L.x[t_of], L.dy[t_of], gw, Wg, Wu, Wd)
+        np.add.at(dx, t_of, dxr)
+        dW_gate[e], dW_up[e], dW_down[e] = dWg, dWu, dWd
+        if j_of is not None:
+            dgates[t_of, j_of] = dg
+    dl = router_backward_logits(R.p, R.idx, R.gates, dgates, L.renorm)
+    dW_r, db_r, dx_r = router_backward(L.x, L.inp["W_r"], dl)
+    return dict(dx=dx + dx_r, dW_r=dW_r, db_r=db_r, dW_gate=dW_gate, dW_up=dW_up, dW_down=dW_down,
+                dgates=dgates, dlogits=dl)

@@ -157,3 +157,69 @@ def test_token_outputs_fp8_equal_the_layer_forward():
         toks = np.array([0, 3, 17, c["T"] - 1])
         cols = np.array([1, 5, c["d"] - 1])
         np.testing.assert_allclose(fp8.token_outputs_fp8(L, toks, cols), y[toks][:, cols], rtol=1e-12, atol=1e-300)
+
+
+# ---- the e4m3 backward (oracle only)
+
+def test_column_quantisation_scales_are_column_maxima():
+    rng = np.random.default_rng(11)
+    W = (rng.normal(0, 1, (40, 24)) * np.exp2(rng.integers(-6, 6, 24))[None, :]).astype(np.float32)
+    q, s = fp8.quantize_cols_e4m3(W)
+    assert q.shape == (24, 40) and s.shape == (24,)
+    np.testing.assert_array_equal(s, (np.abs(W).max(axis=0) / np.float32(448.0)).astype(np.float32))
+    assert np.all(np.abs(fp8.e4m3_decode(q)).max(axis=1) == 448.0)
+
+
+def test_data_gradient_products_lossless():
+    # rows of the left operands and columns of the weights on the e4m3 grid (maxima 448 * 2^j):
+    # every quantisation is exact, so the e4m3 products equal the plain ones
+    rng = np.random.default_rng(12)
+    n, d, f = 6, 64, 48
+    dy = _grid_rows(rng, n, d, rng.integers(-5, 3, n))
+    WdT = _grid_rows(rng, f, d, rng.integers(-9, -3, f))        # the columns of W_d
+    dyq, dys = fp8.quantize_rows_e4m3(dy.astype(np.float32))
+    wq, ws = fp8.quantize_cols_e4m3(WdT.T.astype(np.float32))
+    assert np.array_equal(fp8.dh_fp8(dyq, dys, wq, ws), dy @ WdT.T)
+    dab = _grid_rows(rng, n, 2 * f, rng.integers(-7, 0, n))
+    WguT = _grid_rows(rng, d, 2 * f, rng.integers(-10, -4, d))  # column i of W_g, then of W_u
+    aq, as_ = fp8.quantize_rows_e4m3(dab.astype(np.float32))
+    wq, ws = fp8.quantize_cols_e4m3(WguT.T.astype(np.float32))
+    Wg, Wu = WguT[:, :f].T, WguT[:, f:].T
+    assert np.allclose(fp8.dx_fp8(aq, as_, wq, ws), dab[:, :f] @ Wg + dab[:, f:] @ Wu, rtol=1e-13, atol=0)
+
+
+@pytest.mark.parametrize("name", ["tiny", "deepseek_small", "gptoss_small"])
+def test_quantised_backward_error_is_the_e4m3_size(name):
+    # every gradient of the e4m3 backward sits within e4m3-sized relative error of the exact one
+    import cases
+    c, inp, L = cases.case(name)
+    g = L.backward()
+    q = fp8.layer_backward_fp8(L)
+    for key in ("dx", "dW_gate", "dW_up", "dW_down", "dgates", "dW_r"):
+        rel = np.linalg.norm(q[key] - g[key]) / np.linalg.norm(g[key])
+        assert 1e-4 < rel < 0.1, (key, rel)
+
+
+def test_backward_weight_scales_are_per_channel():
+    # channels spread over 2^-20 .. 1, wider than e4m3's range (~2^18): only one scale per channel
+    # keeps every channel's gradient within the e4m3 error; one scale for the whole matrix flushes
+    # the small channels to zero
+    rng = np.random.default_rng(13)
+    n, d, f = 32, 64, 64
+    x = rng.normal(0, 1, (n, d))
+    dy = rng.normal(0, 1, (n, d))
+    g = rng.uniform(0.2, 1.0, n)
+    Wg = rng.normal(0, 0.1, (f, d))
+    Wu = rng.normal(0, 0.1, (f, d))
+    Wd = rng.normal(0, 0.1, (d, f)) * np.exp2(-rng.uniform(0, 20, f))[None, :]   # W_d's columns
+    ref = oracle.expert_backward(x, dy, g, Wg, Wu, Wd)
+    got = fp8.expert_backward_fp8(x.astype(np.float32), dy.astype(np.float32), g, Wg, Wu, Wd)
+    for k, name in ((1, "dW_gate"), (2, "dW_up")):       # rows: the d_ff channels dh' feeds
+        err = np.linalg.norm(got[k] - ref[k], axis=1) / np.linalg.norm(ref[k], axis=1)
+        assert err.max() < 0.2, (name, err.max())
+    sc = np.exp2(-rng.uniform(0, 20, d))[None, :]            # W_g's and W_u's columns
+    Wg2, Wu2 = Wg * sc, Wu * sc
+    ref = oracle.expert_backward(x, dy, g, Wg2, Wu2, Wd)
+    got = fp8.expert_backward_fp8(x.astype(np.float32), dy.astype(np.float32), g, Wg2, Wu2, Wd)
+    err = np.linalg.norm(got[0] - ref[0], axis=0) / np.linalg.norm(ref[0], axis=0)   # dx columns
+    assert err.max() < 0.2, ("dx", err.max())
