@@ -1,4 +1,4 @@
-"""FP8 (e4m3) quantisation step and the quantised gate/up projection, for the oracle.
+"""FP8 (e4m3) quantisation step, the quantised forward and the quantised backward, for the oracle.
 
 TEST INFRASTRUCTURE, like the rest of ``oracle/``: only tests and bench.py's CPU leg use it.
 
