@@ -1,6 +1,7 @@
 """FP8 (e4m3) quantisation step, the quantised forward and the quantised backward, for the oracle.
 
-TEST INFRASTRUCTURE, like the rest of ``oracle/``: only tests and bench.py's CPU leg use it.
+TEST INFRASTRUCTURE, like the rest of ``oracle/``: only tests, ``__graft_entry__.smoke()`` and bench.py's CPU legs
+use it.
 
 The pages name mixed-precision / quantised experts only as a direction ("MoEBlaze" summary,
 limitations and future work); they fix no format.  The plainest reading taken here:
