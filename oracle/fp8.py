@@ -275,3 +275,47 @@ def layer_backward_fp8(L) -> dict:
     dW_r, db_r, dx_r = router_backward(L.x, L.inp["W_r"], dl)
     return dict(dx=dx + dx_r, dW_r=dW_r, db_r=db_r, dW_gate=dW_gate, dW_up=dW_up, dW_down=dW_down,
                 dgates=dgates, dlogits=dl)
+
+
+# ---------------------------------------------------------------------------------------------
+# MXFP8 (oracle only: block-scaled e4m3 as the kind::mxf8f6f4 MMAs consume it; not built yet)
+#
+# Reading (OCP Microscaling Formats v1.0, conversion of a block): every 32 consecutive values
+# along K share one power-of-two scale X = 2^(floor(log2(amax)) - 8), 8 being the exponent of the
+# largest normal E4M3 value (448 = 1.75 * 2^8); each element is RNE(v / X) in E4M3, saturated to
+# +-448 (amax / X lies in [256, 512), so the top of a block can saturate); X is stored as an E8M0
+# byte (exponent + 127).  An all-zero block takes the smallest scale, 2^-127 (byte 0).
+# ---------------------------------------------------------------------------------------------
+
+MX_BLOCK = 32
+_E4M3_EMAX = 8
+
+
+def mx_quantize_e4m3(rows: np.ndarray):
+    """MX E4M3 codes of a [n, width] array of exact fp32 values, width a multiple of 32: returns
+    (codes uint8 [n, width], scale exponents int [n, width / 32]).  The block's scale is
+    2^exponent; the E8M0 byte is exponent + 127."""
+    v = np.asarray(rows, np.float64)
+    n, w = v.shape
+    assert w % MX_BLOCK == 0
+    blocks = v.reshape(n, w // MX_BLOCK, MX_BLOCK)
+    amax = np.abs(blocks).max(axis=2)
+    with np.errstate(divide="ignore"):
+        e = np.where(amax > 0, np.floor(np.log2(np.where(amax > 0, amax, 1.0))) - _E4M3_EMAX, -127)
+    e = np.clip(e, -127, 127).astype(np.int64)
+    scaled = blocks / np.ldexp(1.0, e)[:, :, None]         # exact: a power-of-two division
+    return e4m3_encode_rne(scaled).reshape(n, w), e
+
+
+def mx_dequantize(codes: np.ndarray, exps: np.ndarray) -> np.ndarray:
+    """float64 values of MX E4M3 rows: each code's value times its block's 2^exponent (exact)."""
+    c = np.asarray(codes)
+    n, w = c.shape
+    vals = e4m3_decode(c).reshape(n, w // MX_BLOCK, MX_BLOCK)
+    return (vals * np.ldexp(1.0, np.asarray(exps, np.int64))[:, :, None]).reshape(n, w)
+
+
+def mx_matmul(aq, ae, bq, be) -> np.ndarray:
+    """A B^T in float64 from MX operands both blocked along K: aq [m, K], bq [n, K] codes with their
+    per-block exponents."""
+    return mx_dequantize(aq, ae) @ mx_dequantize(bq, be).T

@@ -223,3 +223,65 @@ def test_backward_weight_scales_are_per_channel():
     got = fp8.expert_backward_fp8(x.astype(np.float32), dy.astype(np.float32), g, Wg2, Wu2, Wd)
     err = np.linalg.norm(got[0] - ref[0], axis=0) / np.linalg.norm(ref[0], axis=0)   # dx columns
     assert err.max() < 0.2, ("dx", err.max())
+
+
+# ---- MXFP8 (oracle only)
+
+def test_mx_scales_are_powers_of_two_from_the_block_maximum():
+    rng = np.random.default_rng(21)
+    v = rng.normal(0, 1, (5, 96)) * np.exp2(rng.integers(-30, 30, (5, 1)))
+    v[2, 32:64] = 0.0                                          # an all-zero block
+    q, e = fp8.mx_quantize_e4m3(v.astype(np.float32))
+    amax = np.abs(v.astype(np.float32).astype(np.float64)).reshape(5, 3, 32).max(axis=2)
+    nz = amax > 0
+    # 256 <= amax / 2^e < 512 for every non-zero block: e = floor(log2 amax) - 8
+    r = amax[nz] / np.ldexp(1.0, e[nz])
+    assert np.all((r >= 256) & (r < 512))
+    assert e[2, 1] == -127 and not q[2, 32:64].any()
+
+
+def test_mx_blocks_are_independent_and_lossless_on_the_grid():
+    # a block whose values are E4M3 grid values times 2^k with its maximum in [256, 448] * 2^k is
+    # exact; changing another block leaves this block's codes and exponent alone
+    rng = np.random.default_rng(22)
+    grid = fp8.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8))
+    grid = grid[grid >= 2.0 ** -3]
+    v = rng.choice(grid, (4, 64)) * rng.choice([-1.0, 1.0], (4, 64))
+    v[:, 0] = 448.0
+    v[:, 32] = 320.0
+    v = v * np.exp2(rng.integers(-20, 20, (4, 1)))
+    q, e = fp8.mx_quantize_e4m3(v.astype(np.float32))
+    assert np.array_equal(fp8.mx_dequantize(q, e), v)
+    w = v.copy()
+    w[:, 32:] *= 2.0 ** 40
+    q2, e2 = fp8.mx_quantize_e4m3(w.astype(np.float32))
+    assert np.array_equal(q2[:, :32], q[:, :32]) and np.array_equal(e2[:, 0], e[:, 0])
+    assert np.array_equal(e2[:, 1], e[:, 1] + 40)
+
+
+def test_mx_block_top_saturates():
+    # amax just below 512 * 2^k: the block maximum saturates to 448 * 2^k (the format's known
+    # clipping), the rest of the block keeps its relative precision
+    v = np.full((1, 32), 3.0)
+    v[0, 0] = 500.0
+    q, e = fp8.mx_quantize_e4m3(v.astype(np.float32))
+    d = fp8.mx_dequantize(q, e)
+    assert e[0, 0] == 0 and d[0, 0] == 448.0 and np.all(d[0, 1:] == 3.0)
+
+
+def test_mx_matmul_is_the_product_of_the_dequantised_blocks():
+    rng = np.random.default_rng(23)
+    a = rng.normal(0, 1, (7, 128))
+    b = rng.normal(0, 1, (9, 128)) * np.exp2(rng.integers(-10, 10, (9, 1)))
+    aq, ae = fp8.mx_quantize_e4m3(a.astype(np.float32))
+    bq, be = fp8.mx_quantize_e4m3(b.astype(np.float32))
+    got = fp8.mx_matmul(aq, ae, bq, be)
+    # the same sum taken block by block, each block's partial product scaled by both exponents
+    ref = np.zeros((7, 9))
+    for blk in range(4):
+        sl = slice(32 * blk, 32 * blk + 32)
+        part = fp8.e4m3_decode(aq[:, sl]) @ fp8.e4m3_decode(bq[:, sl]).T
+        ref += part * np.ldexp(1.0, ae[:, blk])[:, None] * np.ldexp(1.0, be[:, blk])[None, :]
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-300)
+    rel = np.linalg.norm(got - a @ b.T) / np.linalg.norm(a @ b.T)
+    assert 1e-3 < rel < 0.1   # e4m3 rounding of both operands, and block maxima clipped at 448
