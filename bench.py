@@ -100,6 +100,9 @@ def fp8_forward(args, mc, cfg, x, W_r, b_r, Wg, Wu, Wd, buf, N, tensor_peak, ten
         moe.moe_quantize_rows_e4m3(t, codes, scales)
         return codes, scales
     g8, u8, d8 = quant(Wg), quant(Wu), quant(Wd)
+    # both forwards without kept activations: the FP8 call's scratch shares those buffers, and a
+    # forward alone keeps nothing for a backward
+    mc = moe.config_from(dict(cfg, keep_rows=0))
     y8 = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
     stream = torch.cuda.current_stream()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
