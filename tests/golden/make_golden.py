@@ -28,8 +28,21 @@ def summarise():
     for key in ("dx", "dW_r", "dW_gate", "dW_up", "dW_down", "dgates"):
         norms[key] = float(np.sqrt(np.sum(g[key] * g[key])))
     norms["gates"] = float(np.sqrt(np.sum(L.routing().gates ** 2)))
+    # the e4m3 forward and backward, and the MX conversion, on the same workload
+    from oracle import fp8
+    y8 = fp8.layer_forward_fp8(L)
+    g8 = fp8.layer_backward_fp8(L)
+    norms["fp8_y"] = float(np.sqrt(np.sum(y8 * y8)))
+    for key in ("dx", "dW_gate", "dW_up", "dW_down", "dgates"):
+        norms["fp8_" + key] = float(np.sqrt(np.sum(g8[key] * g8[key])))
+    xq, xs = fp8.quantize_rows_e4m3(L.x[:2].astype(np.float32))
+    mq, me = fp8.mx_quantize_e4m3(L.x[:2].astype(np.float32))
     return {"counts": [int(c) for c in D.counts],
             "idx_head": L.routing().idx[:8].tolist(),
+            "fp8_x_codes_head": xq[:, :16].tolist(),
+            "fp8_x_scales_head": [float(v) for v in xs],
+            "mx_x_codes_head": mq[:, :16].tolist(),
+            "mx_x_exps": me.tolist(),
             "norms": norms}
 
 

@@ -336,5 +336,7 @@ def test_stored_summary_of_tiny_workload():
     got = summarise()
     assert got["counts"] == ref["counts"]
     assert got["idx_head"] == ref["idx_head"]
+    for key in ("fp8_x_codes_head", "fp8_x_scales_head", "mx_x_codes_head", "mx_x_exps"):
+        assert got[key] == ref[key], key
     for key in ref["norms"]:
         assert abs(got["norms"][key] - ref["norms"][key]) <= 1e-12 * abs(ref["norms"][key]), key
