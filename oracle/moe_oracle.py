@@ -63,15 +63,28 @@ def as_f64(a) -> np.ndarray:
     return a.astype(np.float64)
 
 
+BF16_MAX = (2.0 - 2.0 ** -7) * 2.0 ** 127     # largest finite bf16
+
+
 def f64_to_bf16_value(v: np.ndarray) -> np.ndarray:
     """The value of ``v`` rounded once to bf16 (nearest, ties to even), returned as float64.
 
-    Used only to state what a bf16 output "is" when a test wants the oracle's rounded result.
+    bf16 keeps 8 significant bits and fp32's exponent range: a value whose leading bit is
+    2^p (p >= -126) is rounded to a multiple of 2^(p-7); below 2^-126 the step stays 2^-133
+    (subnormals).  The rounding is done directly from float64 (no float32 step, which would
+    round twice), with numpy's rint (half to even) on the scaled value.  Magnitudes that round
+    above the largest finite bf16 become infinities; zeros keep their sign; inf and nan pass.
     """
-    f = np.asarray(v, dtype=np.float64).astype(np.float32)
-    u = f.view(np.uint32).astype(np.uint64)
-    r = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    return (r.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    a = np.asarray(v, dtype=np.float64)
+    out = a.copy()
+    fin = np.isfinite(a)
+    mag = np.abs(a[fin])
+    _, e = np.frexp(mag)                                   # mag = m 2^e, m in [0.5, 1)
+    q = np.maximum(e - 1, -126) - 7                        # exponent of the rounding step
+    r = np.ldexp(np.rint(np.ldexp(mag, -q)), q)
+    r = np.where(r > BF16_MAX, np.inf, r)
+    out[fin] = np.copysign(r, a[fin])
+    return out
 
 
 def capacity_of(T: int, k: int, E: int, cf: float) -> int | None:

@@ -327,6 +327,95 @@ def test_sampled_forms_match_full(renorm, cf, S):
         np.testing.assert_allclose(w["dW_down"], full["dW_down"][e][:, cols], rtol=1e-11, atol=1e-12)
 
 
+# ------------------------------------------------------------------------------------------
+# rounding to bf16 (the value a bf16 intermediate holds)
+# ------------------------------------------------------------------------------------------
+
+def _bf16_grid():
+    """Every finite non-negative bf16 value with its bit pattern, plus 2^128 standing for the
+    overflow to infinity (its pattern 0x7F80 is even, as round-to-nearest-even treats it)."""
+    bits = np.arange(0, 0x7F81, dtype=np.uint32)
+    vals = (bits << np.uint32(16)).view(np.float32).astype(np.float64)
+    vals[-1] = 2.0 ** 128
+    return bits, vals
+
+
+def _bf16_brute(v: float) -> float:
+    """Nearest grid value by exact rational distances; a tie takes the even bit pattern."""
+    from fractions import Fraction
+    if v != v or v in (math.inf, -math.inf):
+        return v
+    bits, vals = _bf16_grid()
+    a = abs(v)
+    i = int(np.searchsorted(vals, a))                     # vals[i-1] < a <= vals[i]
+    cands = [j for j in (i - 1, i) if 0 <= j < len(vals)]
+    fa = Fraction(a)
+    dist = [abs(Fraction(vals[j]) - fa) for j in cands]
+    best = min(dist)
+    pick = [j for j, dd in zip(cands, dist) if dd == best]
+    j = pick[0] if len(pick) == 1 else [p for p in pick if bits[p] % 2 == 0][0]
+    r = math.inf if j == len(vals) - 1 else vals[j]
+    return math.copysign(r, v)
+
+
+def test_bf16_rounding_hand_cases():
+    one = 1.0
+    cases = [
+        (one + 2.0 ** -8, 1.0),                            # tie between 1 and 1 + 2^-7: even (1)
+        (one + 3 * 2.0 ** -8, one + 2.0 ** -6),            # tie between odd and even: up to even
+        (one + 2.0 ** -8 + 2.0 ** -40, one + 2.0 ** -7),   # just above a tie (lost by a float32 step)
+        (one + 2.0 ** -8 - 2.0 ** -40, 1.0),               # just below it
+        (2.0 - 2.0 ** -9, 2.0),                            # just below a binade rounds into it
+        (2.0 - 2.0 ** -8 - 2.0 ** -30, 2.0 - 2.0 ** -7),
+        (-(one + 3 * 2.0 ** -8), -(one + 2.0 ** -6)),      # sign symmetric
+        (0.0, 0.0), (-0.0, -0.0),
+        (oracle.moe_oracle.BF16_MAX, oracle.moe_oracle.BF16_MAX),
+        (oracle.moe_oracle.BF16_MAX + 2.0 ** 118, oracle.moe_oracle.BF16_MAX),   # below the halfway point
+        (oracle.moe_oracle.BF16_MAX + 2.0 ** 119, math.inf),                     # halfway: to even = overflow
+        (-1e39, -math.inf), (1e300, math.inf),
+        (2.0 ** -133, 2.0 ** -133),                        # smallest subnormal
+        (2.0 ** -134, 0.0),                                # half of it: tie to even (zero)
+        (3 * 2.0 ** -134, 2.0 ** -132),                    # 1.5 steps: tie to even (2 steps)
+        (-2.0 ** -140, -0.0),
+        (2.0 ** -126 - 2.0 ** -134, 2.0 ** -126),          # top of the subnormals rounds to the min normal
+        (math.inf, math.inf), (-math.inf, -math.inf),
+    ]
+    got = oracle.f64_to_bf16_value(np.array([c[0] for c in cases]))
+    for (v, want), g in zip(cases, got):
+        assert g == want and math.copysign(1, g) == math.copysign(1, want), (v, g, want)
+    assert np.isnan(oracle.f64_to_bf16_value(np.array([math.nan]))[0])
+
+
+def test_bf16_rounding_brute_force():
+    rng = np.random.default_rng(5)
+    v = rng.normal(size=400) * np.exp2(rng.integers(-140, 130, 400))
+    # exact ties of the bf16 grid and one float64 ulp either side of them
+    base = synth.bf16_bits_to_f32(rng.integers(0, 0x7F7F, 100).astype(np.uint16)).astype(np.float64)
+    base = base[base > 2.0 ** -120]
+    _, e = np.frexp(base)
+    tie = base + np.ldexp(1.0, e - 9)                      # half a bf16 step above a grid value
+    v = np.concatenate([v, tie, np.nextafter(tie, 0), np.nextafter(tie, np.inf), -tie])
+    got = oracle.f64_to_bf16_value(v)
+    want = np.array([_bf16_brute(float(a)) for a in v])
+    assert np.array_equal(got, want)
+    assert np.array_equal(np.signbit(got), np.signbit(want))
+
+
+def test_bf16_rounding_matches_torch_on_float32_inputs():
+    """On values that float32 holds exactly, torch's float32 -> bfloat16 conversion (round to
+    nearest even) is one rounding too, so both must agree bit for bit."""
+    import torch
+    rng = np.random.default_rng(6)
+    u = rng.integers(0, 2 ** 32, 20000, dtype=np.uint64).astype(np.uint32)
+    u[:2000] = (u[:2000] & np.uint32(0xFFFF0000)) | np.uint32(0x8000)   # exact ties
+    f = u.view(np.float32)
+    f = f[np.isfinite(f)]
+    want = torch.from_numpy(f.copy()).to(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.f64_to_bf16_value(f.astype(np.float64))
+    assert np.array_equal(got, want)
+    assert np.array_equal(np.signbit(got), np.signbit(want))
+
+
 def test_stored_summary_of_tiny_workload():
     """Regression guard: the oracle's tiny-workload results, written by tests/golden/make_golden.py."""
     import json
