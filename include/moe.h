@@ -93,7 +93,8 @@ typedef enum {
     MOE_ERR_UNSUPPORTED = 2,   /* a valid shape the library does not handle (or not an sm_103 device) */
     MOE_ERR_WORKSPACE = 3,     /* workspace smaller than moe_workspace_size() */
     MOE_ERR_CUDA = 4,          /* a CUDA runtime/driver call failed */
-    MOE_ERR_BAD_INDEX = 5,     /* (device) an expert id outside [0, E); that slot is dropped */
+    MOE_ERR_BAD_INDEX = 5,     /* (device) an expert id outside [0, E): the dispatch that saw it
+                                * publishes no rows (see moe_dispatch) */
     MOE_ERR_TIMEOUT = 6        /* (device) a bounded wait ran out; outputs of that call are invalid */
 } moe_status_t;
 
@@ -140,7 +141,11 @@ moe_status_t moe_route(const moe_config_t* cfg, const moe_bf16* x, const float* 
  * Outputs: counts [E] (raw demand, sums to T*k), offsets [E+1] (exact), row_of_slot [T,k]
  * (exact row or -1), token_of_row [T*k] (entries >= offsets[E] are left untouched),
  * x_perm [moe_perm_rows(), d_model].  Leaves the padded tables in ws for the calls below.
- * An id outside [0,E) in idx drops that slot and records MOE_ERR_BAD_INDEX. */
+ * An id outside [0,E) anywhere in idx records MOE_ERR_BAD_INDEX (read with moe_check_error) and
+ * empties the whole dispatch, since the queue positions of that call cannot be trusted: counts
+ * still hold the demand of the valid ids, but every segment is published with no rows (offsets
+ * all 0, row_of_slot all -1, token_of_row and x_perm not written), so the calls that follow on
+ * this workspace touch no rows.  The next dispatch with valid ids starts afresh. */
 moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* idx, const moe_bf16* x,
                           int32_t* counts, int32_t* offsets, int32_t* row_of_slot, int32_t* token_of_row,
                           moe_bf16* x_perm, void* ws, size_t ws_bytes, moe_stream_t stream);
@@ -157,14 +162,22 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const int32_t* idx, const moe
  * moe_perm_rows() <= 393216 rows; larger configurations return MOE_ERR_UNSUPPORTED and enqueue
  * nothing.  The first call on each device looks up the array's device address
  * (cudaGetSymbolAddress, with that device current); make that first call before any stream
- * capture.  The call allocates nothing: no cudaMalloc, cudaFree or allocating library routine.
+ * capture.  (The address is looked up again on every call, so a device reset or a re-created
+ * primary context between calls is safe.)  The call allocates nothing: no cudaMalloc, cudaFree or
+ * allocating library routine.
  * Every call shares the one array and leaves its contents behind (each call clears what must
  * start at zero), so calls that may overlap on the GPU -- on different streams, or from several
- * host threads -- race and must be serialised by the caller.  Device-side errors (an expert id
- * out of range drops that slot) are not reported by this entry point. */
+ * host threads -- race and must be serialised by the caller.
+ * status: nullable device pointer to one int32 (4-byte aligned).  With no workspace there is no
+ * error word for moe_check_error, so the call's device-side outcome lands here, written on the
+ * stream after the scan: MOE_OK, MOE_ERR_BAD_INDEX (an id outside [0,E); as in moe_dispatch the
+ * whole dispatch is then empty: offsets all 0, row_of_slot all -1, token_of_row and x_perm not
+ * written) or MOE_ERR_TIMEOUT (a bounded wait ran out; outputs invalid).  Read it after the
+ * stream's work completes.  With status NULL a bad id still empties the dispatch, unreported. */
 moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, const int32_t* idx, const moe_bf16* x,
                                   int32_t* counts, int32_t* offsets, int32_t* row_of_slot,
-                                  int32_t* token_of_row, moe_bf16* x_perm, moe_stream_t stream);
+                                  int32_t* token_of_row, moe_bf16* x_perm, int32_t* status,
+                                  moe_stream_t stream);
 
 /* Grouped expert SwiGLU FFN on the rows moe_dispatch laid out in ws: tcgen05/TMEM tiles fed by
  * TMA, a per-expert tile scheduler, SwiGLU fused into the first GEMM's epilogue.

@@ -63,7 +63,7 @@ def load(path: str | None = None):
         "moe_workspace_init": [cfgp, _P, ctypes.c_size_t, _P],
         "moe_route": [cfgp, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
         "moe_dispatch": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
-        "moe_dispatch_noalloc": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P],
+        "moe_dispatch_noalloc": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P],
         "moe_expert_ffn_fwd": [cfgp, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
         "moe_combine": [cfgp, _P, _P, _P, _P, ctypes.c_size_t, _P],
         "moe_expert_ffn_bwd": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
@@ -164,10 +164,12 @@ def moe_dispatch(cfg, idx, x, counts, offsets, row_of_slot, token_of_row, x_perm
           _ptr(row_of_slot), _ptr(token_of_row), _ptr(x_perm), _ptr(ws), ws.numel(), _stream(stream))
 
 
-def moe_dispatch_noalloc(cfg, idx, x, counts, offsets, row_of_slot, token_of_row, x_perm, stream=None):
-    """moe_dispatch without a workspace (scratch in a fixed array inside the library)."""
+def moe_dispatch_noalloc(cfg, idx, x, counts, offsets, row_of_slot, token_of_row, x_perm, status=None,
+                         stream=None):
+    """moe_dispatch without a workspace (scratch in a fixed array inside the library); ``status``
+    (optional int32 device tensor of one element) receives the call's device-side status."""
     _call("moe_dispatch_noalloc", ctypes.byref(cfg), _ptr(idx), _ptr(x), _ptr(counts), _ptr(offsets),
-          _ptr(row_of_slot), _ptr(token_of_row), _ptr(x_perm), _stream(stream))
+          _ptr(row_of_slot), _ptr(token_of_row), _ptr(x_perm), _ptr(status), _stream(stream))
 
 
 def moe_expert_ffn_fwd(cfg, x_perm, W_gate, W_up, W_down, o_perm, ws, stream=None):

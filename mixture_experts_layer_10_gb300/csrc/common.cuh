@@ -150,6 +150,9 @@ struct DispatchArgs {
   int32_t* prow_of_slot; int32_t* slot_of_prow; float* gate_of_prow;
   // FP8 forward: per-token row scales carried beside the gathered e4m3 rows (nullable)
   const float* xs_tok; float* xs_perm;
+  // nullable: receives the header's status (MOE_OK or the first device error of this dispatch)
+  // once the last scan block has built the tables
+  int32_t* status_out;
 };
 cudaError_t launch_dispatch_scan(const Cfg& c, const Layout& L, const DispatchArgs& a, cudaStream_t s);
 cudaError_t launch_dispatch_gather(const Cfg& c, const Layout& L, const DispatchArgs& a,

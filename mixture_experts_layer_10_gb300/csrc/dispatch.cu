@@ -172,6 +172,8 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(DispatchArg
     tb->total_rows = (int)poff;
     tb->n_mtiles = (int)(poff / kRowTile);
     tb->total_pad = (int)pads;
+    // every scan block has recorded its errors before counting itself done
+    if (a.status_out != nullptr) *a.status_out = *((volatile int*)&a.hdr->status);
   }
   __syncthreads();
   if (threadIdx.x < G) {
@@ -339,7 +341,9 @@ cudaError_t launch_dispatch_gather(const Cfg& c, const Layout& L, const Dispatch
 // keeps the dispatch's scratch (header, routing tables, look-back status words, per-slot ranks
 // and rows, per-row slots) in `g_noalloc_scratch`, which every device that loads the library
 // holds until the process exits.  The host side only ever passes the array's device address,
-// taken once per device with cudaGetSymbolAddress while that device is current.
+// taken with cudaGetSymbolAddress while the caller's device is current.  There is no workspace
+// error word to read back, so the device-side status of each call goes to the caller's optional
+// `status` word instead.
 
 namespace moe {
 namespace {
@@ -359,26 +363,17 @@ struct NoAllocScratch {
 
 __device__ __align__(256) unsigned char g_noalloc_scratch[sizeof(NoAllocScratch)];
 
-// Device address of the scratch array on the current device (set up on first use per device).
+// Device address of the scratch array on the current device.  Looked up on every call (a host-side
+// table lookup): an address cached per device ordinal would go stale if the caller reset the
+// device or released and re-created its primary context, which can reload the module elsewhere.
 moe_status_t noalloc_scratch(NoAllocScratch** out) {
-  static std::mutex mu;
-  static void* addr[64] = {nullptr};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+  if (e != cudaSuccess || p == nullptr) {
     (void)cudaGetLastError();
     return MOE_ERR_CUDA;
   }
-  std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
-    void* p = nullptr;
-    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || p == nullptr) {
-      (void)cudaGetLastError();
-      return MOE_ERR_CUDA;
-    }
-    addr[dev] = p;
-  }
-  *out = static_cast<NoAllocScratch*>(addr[dev]);
+  *out = static_cast<NoAllocScratch*>(p);
   return MOE_OK;
 }
 
@@ -388,7 +383,7 @@ moe_status_t noalloc_scratch(NoAllocScratch** out) {
 extern "C" moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, const int32_t* idx,
                                              const moe_bf16* x, int32_t* counts, int32_t* offsets,
                                              int32_t* row_of_slot, int32_t* token_of_row,
-                                             moe_bf16* x_perm, moe_stream_t stream) {
+                                             moe_bf16* x_perm, int32_t* status, moe_stream_t stream) {
   using namespace moe;
   Cfg c;
   moe_status_t st = make_cfg(cfg, &c);
@@ -396,6 +391,7 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, const int3
   const void* ptrs[] = {idx, x, counts, offsets, row_of_slot, token_of_row, x_perm};
   for (const void* p : ptrs)
     if (p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) != 0) return MOE_ERR_INVALID_ARG;
+  if (status != nullptr && (reinterpret_cast<uintptr_t>(status) & 3u) != 0) return MOE_ERR_INVALID_ARG;
   const Layout L = make_layout(c);
   if ((int64_t)c.T * c.k > kNoAllocMaxSlots || L.rows > kNoAllocMaxRows || L.nscan > kNoAllocMaxScanBlocks)
     return MOE_ERR_UNSUPPORTED;
@@ -423,6 +419,7 @@ extern "C" moe_status_t moe_dispatch_noalloc(const moe_config_t* cfg, const int3
   a.rank = sc->rank;
   a.prow_of_slot = sc->prow_of_slot;
   a.slot_of_prow = sc->slot_of_prow;
+  a.status_out = status;
   cudaError_t e = launch_dispatch_scan(c, L, a, s);
   if (e == cudaSuccess) e = launch_dispatch_gather(c, L, a, true, true, false, s);
   if (e != cudaSuccess) {

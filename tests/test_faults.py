@@ -1,7 +1,7 @@
 """Device-side error reporting without faulting the GPU (GPU).
 
-* An expert id outside [0, E) drops that slot and comes back as MOE_ERR_BAD_INDEX through
-  moe_check_error; the next clean call succeeds.
+* An expert id outside [0, E) comes back as MOE_ERR_BAD_INDEX through moe_check_error and empties
+  that dispatch (no rows: offsets all 0, row_of_slot all -1); the next clean call succeeds.
 * A bounded wait that runs out: the test hook makes one dispatch-scan block never publish its
   counts, the look-back of the blocks after it gives up after a short limit, the call reports
   MOE_ERR_TIMEOUT and downstream kernels see empty tables; the next clean call succeeds.
@@ -45,6 +45,10 @@ def test_bad_expert_index_is_reported(moe):
     x = to_dev_bf16(synth.normal_bf16(3, "x", (T, d), 1.0))
     _dispatch(moe, mc, buf, o, to_dev(bad), x)
     assert moe.moe_check_error(buf.ws) == BAD_INDEX
+    valid = bad[(bad >= 0) & (bad < E)]
+    assert np.array_equal(from_dev(o["counts"]), np.bincount(valid, minlength=E))
+    assert np.all(from_dev(o["offsets"]) == 0)
+    assert np.all(from_dev(o["row_of_slot"]) == -1)
     # the error is cleared by the check; a clean call then matches the oracle
     _dispatch(moe, mc, buf, o, to_dev(idx_np), x)
     assert moe.moe_check_error(buf.ws) == 0
