@@ -142,6 +142,11 @@ Layout make_layout(const Cfg& c) {
   L.dl_bf16 = take((size_t)c.T * L.Ep * 2);
   L.wr_bf16 = take((size_t)c.d * L.Ep * 2);
   L.wr3 = take((size_t)3 * L.Ep * c.d * 2);
+  if (router_stream_eligible(c)) {
+    const RouterStreamPlan pl = router_stream_plan(c);
+    L.rt_part = take(pl.maxseg > 1 ? (size_t)pl.ntiles * pl.maxseg * pl.eb * 128 * 4 : 0);
+    L.rt_cnt = take((size_t)pl.ntiles * 4 * 4);
+  }
   L.total = off;
   return L;
 }
@@ -309,7 +314,12 @@ moe_status_t do_router_bwd(const Cfg& c, const Ws& w, const uint16_t* x, const f
   a.dwr_part = w.at<float>(w.L.dwr_part);
   a.db_part = w.at<float>(w.L.db_part);
   uint16_t* dl_bf16 = w.at<uint16_t>(w.L.dl_bf16);
-  if (router_bwd_on_tensor_cores(c)) {   // logits recomputed on the tensor cores; dl in both types
+  if (router_bwd_on_tensor_cores(c) && router_stream_eligible(c)) {   // narrow router, x streamed once
+    RouterStreamArgs t{x, W_r, b_r, w.at<uint16_t>(w.L.wr3), w.at<float>(w.L.rt_part), w.at<uint32_t>(w.L.rt_cnt),
+                       const_cast<int32_t*>(idx), const_cast<float*>(gates), nullptr,
+                       dgates, dlogits, dl_bf16, a.db_part, w.hdr()};
+    MOE_CUDA(launch_router_dlogits_stream(c, w.L, t, s));
+  } else if (router_bwd_on_tensor_cores(c)) {   // logits recomputed on the tensor cores; dl in both types
     uint16_t* wr3 = w.at<uint16_t>(w.L.wr3);
     MOE_CUDA(launch_split_wr(W_r, c.d, c.E, w.L.Ep, wr3, s));
     RouterTcArgs t{x, wr3, b_r, const_cast<int32_t*>(idx), const_cast<float*>(gates), nullptr,
@@ -324,11 +334,16 @@ moe_status_t do_router_bwd(const Cfg& c, const Ws& w, const uint16_t* x, const f
   return MOE_OK;
 }
 
-// Router forward: logits on the tensor cores when the shape allows (W_r split into bf16 parts
-// first), else the fp32 tile product.
+// Router forward: narrow routers (E <= 64, k <= 8) stream x once with K split across CTAs; up to
+// 128 experts the logits run on the tensor cores one 128-token tile per CTA; else the fp32 tile
+// product.  The tensor-core paths split W_r into bf16 parts first.
 moe_status_t do_route(const Cfg& c, const Ws& w, const uint16_t* x, const float* W_r, const float* b_r,
                       int32_t* idx, float* gates, float* logits, cudaStream_t s) {
-  if (router_on_tensor_cores(c)) {
+  if (router_stream_eligible(c)) {
+    RouterStreamArgs t{x, W_r, b_r, w.at<uint16_t>(w.L.wr3), w.at<float>(w.L.rt_part), w.at<uint32_t>(w.L.rt_cnt),
+                       idx, gates, logits, nullptr, nullptr, nullptr, nullptr, w.hdr()};
+    MOE_CUDA(launch_route_stream(c, w.L, t, s));
+  } else if (router_on_tensor_cores(c)) {
     uint16_t* wr3 = w.at<uint16_t>(w.L.wr3);
     MOE_CUDA(launch_split_wr(W_r, c.d, c.E, w.L.Ep, wr3, s));
     RouterTcArgs t{x, wr3, b_r, idx, gates, logits, nullptr, nullptr, nullptr, nullptr, w.hdr(), w.tabs()};

@@ -72,6 +72,7 @@ struct Layout {
   size_t hdr, tabs, scan_status, rank, prow_of_slot, slot_of_prow, gate_of_prow, dg_part,
       dlogits, dwr_part, db_part, dgates, xperm, dy_perm, buf_f0, buf_f1, buf_f2, buf_f3, buf_d1,
       dl_bf16, wr_bf16, wr3;
+  size_t rt_part, rt_cnt;   // streaming router (E <= 64): partial logits and part counters
   size_t total;
 };
 
@@ -202,6 +203,28 @@ struct RouterTcArgs {
 };
 cudaError_t launch_route_tc(const Cfg& c, const Layout& L, const RouterTcArgs& a, cudaStream_t s);
 cudaError_t launch_router_dlogits_tc(const Cfg& c, const Layout& L, const RouterTcArgs& a, cudaStream_t s);
+
+// Router logits for E <= 64 and k <= 8, streaming x once with K split across CTAs
+// (route_tc.cu): W_r's three bf16 parts stacked along N in wstack [Nb][d] (written by the launch
+// into the workspace's wr3 region), partial logits per (tile, part), counters per token quarter.
+struct RouterStreamPlan {
+  int eb;          // E rounded up to 8, 16, 32 or 64
+  int ntiles;      // 128-token tiles
+  int nslice;      // 256-wide K slices
+  int nranges;     // CTAs, each a contiguous run of (tile, slice) pairs
+  int maxseg;      // the most runs one tile is split between
+};
+bool router_stream_eligible(const Cfg& c);
+RouterStreamPlan router_stream_plan(const Cfg& c);
+struct RouterStreamArgs {
+  const uint16_t* x; const float* W_r; const float* b_r; uint16_t* wstack; float* part; uint32_t* cnt;
+  int32_t* idx; float* gates; float* logits;                            // forward (idx, gates read in bwd)
+  const float* dgates; float* dlogits; uint16_t* dl_bf16; float* db_part;   // backward
+  Hdr* hdr;
+};
+cudaError_t launch_route_stream(const Cfg& c, const Layout& L, const RouterStreamArgs& a, cudaStream_t s);
+cudaError_t launch_router_dlogits_stream(const Cfg& c, const Layout& L, const RouterStreamArgs& a,
+                                         cudaStream_t s);
 
 struct DgatesArgs {
   const float* dg_part; const int32_t* prow_of_slot; float* dgates;
