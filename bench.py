@@ -13,6 +13,8 @@ Prints one JSON line (rank 0):
   roofline   the dominant kernel: algorithmic work per launch / its CUDA-event duration, against the
              measured peak (MEASURED_PEAKS.json)
   cpu_baseline  the fp64 oracle on a bounded token sample, on this host's cores (rank 0, N = 1)
+  workloads  (default Mixtral-like run) a compact record of each other workload -- tiny, DeepSeek-,
+             Qwen3- and GPT-OSS-like -- measured the same way over --workload-steps steps
 
 --impl reference times the oracle alone (on the host cores) on the same workload and metric.
 """
@@ -51,7 +53,9 @@ GEMMS = {  # algorithmic FLOPs per launch in units of N*d*f (N = rows the expert
     "gemm_wgrad": 6, "gemm_dgrad_x": 4,
 }
 HBM_KERNELS = ("dispatch_gather", "combine", "combine_bwd")
-KERNEL_SOURCES = ("gemm.cu", "dispatch.cu", "combine.cu", "route.cu", "activations.cu", "ptx.cuh", "common.cuh")
+ROUTER_KERNELS = ("route_fwd", "router_dlogits")   # one HBM pass over x each (logits computed or recomputed)
+KERNEL_SOURCES = ("gemm.cu", "dispatch.cu", "combine.cu", "route.cu", "route_tc.cu", "activations.cu", "ptx.cuh",
+                  "common.cuh", "tmap.cuh")
 ROW_TILE = 256   # expert segments are padded to multiples of this many rows (include/moe.h)
 
 
@@ -73,6 +77,13 @@ def parse():
     ap.add_argument("--keep-rows", type=int, default=0,
                     help="expert-ordered rows whose gate/up pre-activations the forward keeps instead "
                          "of the backward recomputing them (0: recompute all, the default; -1: keep all)")
+    ap.add_argument("--keep-budget", type=float, default=None,
+                    help="bytes of kept activations (a, b) the layer may hold between forward and backward; "
+                         "the library chooses keep_rows from it (moe_keep_rows_for_budget)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="measure the chosen workload only (by default the Mixtral-like line also carries a "
+                         "compact record of every other workload)")
+    ap.add_argument("--workload-steps", type=int, default=10, help="timed steps of each extra workload")
     return ap.parse_args()
 
 
@@ -304,39 +315,32 @@ def reference_arm(args, rank, world):
     print(json.dumps(line), flush=True)
 
 
-def main():
-    args = parse()
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    if args.impl == "reference":
-        reference_arm(args, rank, world)
-        return
-
+def device_experts(cfg, seed=0):
+    """W_gate, W_up ~ N(0, 1/d) and W_down ~ N(0, 1/d_ff) in bf16, drawn on the device from a seeded
+    generator (the extra workloads of the bench line: the routing, which sets every kernel's work,
+    still comes from the seeded x, W_r and bias of synth; drawing billions of weights on the host
+    would take longer than measuring them)."""
     import torch
-    import torch.distributed as dist
+    T, d, f, G = cfg["T"], cfg["d"], cfg["f"], cfg["E"] + cfg["S"]
+    g = torch.Generator(device="cuda").manual_seed(1000 + seed)
+    out = []
+    for shape, std in (((G, f, d), d ** -0.5), ((G, f, d), d ** -0.5), ((G, d, f), f ** -0.5)):
+        w = torch.empty(shape, dtype=torch.bfloat16, device="cuda")
+        for e in range(G):
+            w[e] = (torch.randn(shape[1:], generator=g, device="cuda") * std).to(torch.bfloat16)
+        out.append(w)
+    return out
 
+
+def run_workload(args, name, cfg, steps, warmup, rank, world, local, barrier, extra=False):
+    """One workload's measurement: device-resident steps (CUDA events, per-kernel profile, clocks),
+    end to end through host buffers, and CUDA-graph replay.  Returns the JSON record."""
+    import torch
     import mixture_experts_layer_10_gb300 as moe
 
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    torch.cuda.set_device(local)
-    if world > 1:
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-
-    def barrier():
-        if world > 1:
-            dist.barrier()
-
-    moe.load()
-    cfg = dict(synth.CONFIGS[args.workload])
-    if args.tokens:
-        cfg["T"] = args.tokens
-    if args.experts:
-        cfg["E"] = args.experts
-    if args.topk:
-        cfg["k"] = args.topk
     T, d, f, E, k, S = cfg["T"], cfg["d"], cfg["f"], cfg["E"], cfg["k"], cfg["S"]
     G = E + S
-    inp = synth.make_inputs(cfg, seed=0)
+    inp = synth.make_inputs(cfg, seed=0, parts=("x", "router", "dy") if extra else ("x", "router", "experts", "dy"))
 
     def dev_bf16(a):
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
@@ -344,9 +348,17 @@ def main():
     x, dy = dev_bf16(inp["x"]), dev_bf16(inp["dy"])
     W_r = torch.from_numpy(inp["W_r"]).cuda()
     b_r = torch.from_numpy(inp["b_r"]).cuda() if inp["b_r"] is not None else None
-    Wg, Wu, Wd = dev_bf16(inp["W_gate"]), dev_bf16(inp["W_up"]), dev_bf16(inp["W_down"])
+    if extra:
+        Wg, Wu, Wd = device_experts(cfg)
+    else:
+        Wg, Wu, Wd = dev_bf16(inp["W_gate"]), dev_bf16(inp["W_up"]), dev_bf16(inp["W_down"])
     mc = moe.config_from(cfg)
-    if args.keep_rows:
+    keep_budget = None
+    if not extra and args.keep_budget is not None:
+        keep_budget = int(args.keep_budget)
+        cfg["keep_rows"], _ = moe.moe_keep_rows_for_budget(mc, keep_budget)
+        mc = moe.config_from(cfg)
+    elif not extra and args.keep_rows:
         cfg["keep_rows"] = moe.moe_perm_rows(mc) if args.keep_rows < 0 else args.keep_rows
         mc = moe.config_from(cfg)
     keep = min(cfg.get("keep_rows", 0) // ROW_TILE * ROW_TILE, moe.moe_perm_rows(mc))
@@ -387,7 +399,7 @@ def main():
     load_max_over_mean = float(counts_h.max() / counts_h.mean())
     del x_perm, scratch_rows, scratch_tok
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     status = moe.moe_check_error(buf.ws)
     if status != 0:
@@ -401,7 +413,7 @@ def main():
         moe.moe_profile_enable(True)
         clocks.mark_start()
         ev0.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             step()
         ev1.record(stream)
         torch.cuda.synchronize()
@@ -410,7 +422,7 @@ def main():
     prof = moe.moe_profile_read()
     moe.moe_profile_enable(False)
     clk = clocks.summary()
-    ms = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
+    ms = max_over_ranks(ev0.elapsed_time(ev1) / steps, world)
     status = moe.moe_check_error(buf.ws)
     if status != 0:
         raise RuntimeError(f"layer failed in the timed region: {moe.moe_status_string(status)}")
@@ -464,11 +476,11 @@ def main():
     barrier()
     torch.cuda.synchronize()
     ev0.record(cstream)
-    e2e_run(args.steps)
+    e2e_run(steps)
     ev1.record(cstream)
     torch.cuda.synchronize()
     barrier()
-    ms_e2e = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
+    ms_e2e = max_over_ranks(ev0.elapsed_time(ev1) / steps, world)
 
     # The same device-resident step captured once in a CUDA graph and replayed (launch overhead
     # removed); reported beside the primary, stream-launched number.
@@ -486,11 +498,11 @@ def main():
         torch.cuda.synchronize()
         barrier()
         ev0.record(stream)
-        for _ in range(args.steps):
+        for _ in range(steps):
             g.replay()
         ev1.record(stream)
         torch.cuda.synchronize()
-        ms_graph = max_over_ranks(ev0.elapsed_time(ev1) / args.steps, world)
+        ms_graph = max_over_ranks(ev0.elapsed_time(ev1) / steps, world)
         graph = {"ms_per_step": ms_graph, "value": world * T / (ms_graph / 1000.0), "unit": "tokens/s"}
         del g
     except RuntimeError as err:   # capture unsupported here: say why, keep the stream numbers
@@ -512,62 +524,66 @@ def main():
     tensor_kind = ("bf16_tflops (burst, %s): SM clock held at max in the timed region" if at_max else
                    "bf16_tflops_sustained (%s): SM clock below max in the timed region") % pk["source"]
     fp8_line = None
-    if args.fp8:
+    if args.fp8 and not extra:
         fp8_line = fp8_forward(args, mc, cfg, x, W_r, b_r, Wg, Wu, Wd, buf, N, tensor_peak, tensor_kind, pk)
     kernels = {}
     gemm_flops = gemm_ms = hbm_bytes = hbm_ms = 0.0
     launches = 0
-    for name, (tot, n) in prof.items():
+    for kname, (tot, n) in prof.items():
         if n == 0:
             continue
         launches += n
-        ent = {"ms_per_step": tot / args.steps, "launches": n}
-        if name in GEMMS:
-            rows_done = N - kept_real if name == "gemm_bwd_recompute_swiglu" else N
-            work = GEMMS[name] * rows_done * d * f * n     # FLOPs over all launches
+        ent = {"ms_per_step": tot / steps, "launches": n}
+        if kname in GEMMS:
+            rows_done = N - kept_real if kname == "gemm_bwd_recompute_swiglu" else N
+            work = GEMMS[kname] * rows_done * d * f * n     # FLOPs over all launches
             ent["tflops"] = work / (tot / 1000.0) / 1e12
             ent["frac_of_measured_peak"] = ent["tflops"] / tensor_peak
             gemm_flops += work
             gemm_ms += tot
-        elif name in HBM_KERNELS:
-            if name == "dispatch_gather":   # fwd: x once + N rows; bwd: x and dy once + 2N rows
-                work = args.steps * ((T + N) * d * 2 + 2 * (T + N) * d * 2 + 3 * 12 * T * k)
-            elif name == "combine":
+        elif kname in HBM_KERNELS or kname in ROUTER_KERNELS:
+            if kname == "dispatch_gather":   # fwd: x once + N rows; bwd: x and dy once + 2N rows
+                work = steps * ((T + N) * d * 2 + 2 * (T + N) * d * 2 + 3 * 12 * T * k)
+            elif kname == "combine":
                 work = n * ((N + T) * d * 2 + 8 * T * k)
-            else:   # expert rows + the router term row in, dx out, slot indices
+            elif kname == "combine_bwd":   # expert rows + the router term row in, dx out, slot indices
                 work = n * ((N + 2 * T) * d * 2 + 4 * T * k)
+            else:   # the router's logit passes read x once (and W_r; idx and gates out)
+                work = n * (T * d * 2 + d * E * 4 + T * k * 8)
             ent["gbs"] = work / (tot / 1000.0) / 1e9
             ent["frac_of_measured_peak"] = ent["gbs"] / pk["hbm"]
-            hbm_bytes += work
-            hbm_ms += tot
-        kernels[name] = ent
+            if kname in HBM_KERNELS:
+                hbm_bytes += work
+                hbm_ms += tot
+        kernels[kname] = ent
     dom = max(kernels, key=lambda n: kernels[n]["ms_per_step"])
     dom_n = kernels[dom]["launches"]
     if dom in GEMMS:
         per_launch = GEMMS[dom] * N * d * f
-        achieved = per_launch / (kernels[dom]["ms_per_step"] * args.steps / dom_n / 1000.0) / 1e12
+        achieved = per_launch / (kernels[dom]["ms_per_step"] * steps / dom_n / 1000.0) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tensor_peak,
                 "unit": "TFLOP/s", "frac": achieved / tensor_peak, "peak_kind": tensor_kind,
                 "work_per_launch": per_launch}
     else:
         roof = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom].get("gbs"), "peak": pk["hbm"],
                 "unit": "GB/s", "frac": kernels[dom].get("frac_of_measured_peak")}
-    roof["traffic"] = recorded_traffic(dom, args.workload)
+    roof["traffic"] = recorded_traffic(dom, name)
 
     value = world * T / (ms / 1000.0)
+    over = args.tokens or args.experts or args.topk
     line = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": DESCR[args.workload] + ("" if not (args.tokens or args.experts or args.topk)
-                                                       else f" with T={T}, E={E}, k={k} overridden"),
+        "config": {"workload": DESCR[name] + ("" if not over or extra else f" with T={T}, E={E}, k={k} overridden"),
                    "T": T, "d_model": d, "d_ff": f, "E": E, "k": k,
                    "n_shared": S, "global_batch": world * T, "parallelism": f"replicas x{world}",
                    "l2": "no flush: each step streams > L2 (expert weights alone %.2f GB)"
                          % (3 * G * d * f * 2 / 1e9),
                    "rows_per_step": N, "load_max_over_mean": load_max_over_mean,
                    "keep_rows": keep, "kept_rows": kept_real,
-                   "kept_activation_bytes": keep * f * 2 * 2},
+                   "kept_activation_bytes": keep * f * 2 * 2, "keep_budget_bytes": keep_budget,
+                   "expert_weights": "seeded on the device" if extra else "synth (seeded, host)"},
         "cuda_graph": graph,
         "model": model_line,
         "fp8_forward": fp8_line,
@@ -584,11 +600,78 @@ def main():
         "gpu_launches": launches,
         "clocks": clk,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not extra:
         n, dt = oracle_sample(inp, cfg, args.cpu_tokens)
         line["cpu_baseline"] = {"value": n / dt, "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
                                 "sample": f"{n} seeded tokens of the same workload, fp64 fwd + bwd "
                                           f"(weight-gradient products included), {dt:.1f} s"}
+    del buf, x, dy, Wg, Wu, Wd, dWg, dWu, dWd, xin, dyin, yout, dxout
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return line
+
+
+def compact(line):
+    """The per-workload record carried on the headline line."""
+    k = line["kernels"]
+    router = {n: {"us": 1000 * k[n]["ms_per_step"], "frac_of_hbm": k[n].get("frac_of_measured_peak")}
+              for n in ROUTER_KERNELS if n in k}
+    return {"workload": line["config"]["workload"], "value": line["value"], "unit": line["unit"],
+            "ms_per_step": line["ms_per_step"], "steps": line["steps"], "warmup": line["warmup"],
+            "e2e": {"value": line["e2e"]["value"], "ms_per_step": line["e2e"]["ms_per_step"]},
+            "cuda_graph_ms": line["cuda_graph"].get("ms_per_step"),
+            "roofline": {kk: line["roofline"].get(kk) for kk in ("kernel", "bound", "achieved", "peak", "unit", "frac")},
+            "expert_gemm_frac": line["expert_gemm"]["frac_of_measured_peak"],
+            "dispatch_combine_frac": line["dispatch_combine"]["frac_of_measured_peak"],
+            "gather_frac": k.get("dispatch_gather", {}).get("frac_of_measured_peak"),
+            "combine_frac": k.get("combine", {}).get("frac_of_measured_peak"),
+            "router": router,
+            "model_measured_over_predicted": line["model"]["measured_over_predicted"],
+            "load_max_over_mean": line["config"]["load_max_over_mean"],
+            "gpu_launches": line["gpu_launches"],
+            "clocks": {kk: line["clocks"].get(kk) for kk in ("sm_mhz", "sm_max_mhz", "reasons", "samples")}}
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        reference_arm(args, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+
+    import mixture_experts_layer_10_gb300 as moe
+
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    moe.load()
+    cfg = dict(synth.CONFIGS[args.workload])
+    if args.tokens:
+        cfg["T"] = args.tokens
+    if args.experts:
+        cfg["E"] = args.experts
+    if args.topk:
+        cfg["k"] = args.topk
+    line = run_workload(args, args.workload, cfg, args.steps, args.warmup, rank, world, local, barrier)
+    # every other workload of the pages' families, a few steps each, as a compact record
+    if not args.no_workloads and args.workload == "mixtral" and not (args.tokens or args.experts or args.topk):
+        line["workloads"] = {}
+        for name in synth.CONFIGS:
+            if name == args.workload:
+                continue
+            rec = run_workload(args, name, dict(synth.CONFIGS[name]), args.workload_steps, 3, rank, world, local,
+                               barrier, extra=True)
+            line["workloads"][name] = compact(rec)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -57,11 +57,13 @@
  * Kept activations (MoEBlaze, Methodology item 2: selective checkpointing, here with an adjustable
  * granularity).  By default the backward recomputes the SwiGLU pre-activations a = x W_gate^T and
  * b = x W_up^T from x_perm.  With keep_rows > 0, the forward also writes a and b (bf16) of the
- * first keep_rows expert-ordered rows (rounded down to a multiple of 256, at most all rows) into
- * the workspace, and the backward takes them from there instead of recomputing those rows:
- * 2 * d_ff * 2 bytes kept per row buy 4 * d_model * d_ff FLOP per row.  The workspace size does
- * not change (the kept rows reuse backward buffers); moe_expert_ffn_fwd and moe_layer_fwd must then
- * be followed by the matching backward on the same workspace before anything else uses it.
+ * first keep_rows expert-ordered rows (rounded down to a multiple of 256, at most all rows), and the
+ * backward takes them instead of recomputing those rows: 2 * d_ff * 2 bytes kept per row buy
+ * 4 * d_model * d_ff FLOP per row.  moe_layer_fwd / moe_layer_bwd keep them in `saved` (which grows
+ * by those bytes: moe_workspace_size), so the workspace stays free for other layers between the
+ * forward and the backward; moe_expert_ffn_fwd / moe_expert_ffn_bwd keep them in the workspace,
+ * which must then reach the matching backward untouched.  moe_keep_rows_for_budget chooses
+ * keep_rows from a byte budget (the adaptive granularity of the MoEBlaze summary's future work).
  *
  * Workspace.  Size it with moe_workspace_size(), zero its header once with moe_workspace_init(),
  * and pass the same workspace to every call of one layer instance.  moe_dispatch leaves the
@@ -115,9 +117,26 @@ typedef uint16_t moe_bf16;                 /* raw bf16 bit pattern */
 typedef struct CUstream_st* moe_stream_t;  /* a cudaStream_t; NULL is the legacy default stream */
 
 /* Workspace bytes for any call of this configuration, and bytes of the `saved` buffer that
- * moe_layer_fwd fills and moe_layer_bwd reads (idx int32 [T,k] then gates fp32 [T,k]).
- * Host only; touches no device. */
+ * moe_layer_fwd fills and moe_layer_bwd reads: idx int32 [T,k], then gates fp32 [T,k], then, when
+ * keep_rows > 0, from the next 256-byte boundary the kept a and b [keep, d_ff] bf16 (keep =
+ * keep_rows rounded down to 256, at most moe_perm_rows()).  Host only; touches no device. */
 moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* ws_bytes, size_t* saved_bytes);
+
+/* Checkpoint granularity from a memory budget (MoEBlaze summary, Limitations and future work:
+ * adaptive checkpoint granularity driven by memory pressure at run time; Methodology item 2: keep
+ * a minimum and recompute the rest).  *keep_rows receives the largest keep_rows (a multiple of 256,
+ * at most moe_perm_rows()) whose kept a and b -- 4 * d_ff bytes per expert-ordered row, the bytes
+ * `saved` grows by -- fit in budget_bytes; *kept_bytes (nullable) receives those bytes.  The
+ * cfg's own keep_rows is ignored; set it to the result.  Rows kept cost no recompute GEMM work in
+ * the backward (4 * d_model * d_ff FLOP each).  Host only; touches no device. */
+moe_status_t moe_keep_rows_for_budget(const moe_config_t* cfg, uint64_t budget_bytes, int32_t* keep_rows,
+                                      uint64_t* kept_bytes);
+
+/* The same with the budget taken from the current device's free memory at the time of the call
+ * (cudaMemGetInfo) less reserve_bytes (0 if free memory is below it): the kept share follows the
+ * memory pressure of each step.  MOE_ERR_CUDA if the query fails. */
+moe_status_t moe_keep_rows_for_free_memory(const moe_config_t* cfg, uint64_t reserve_bytes, int32_t* keep_rows,
+                                           uint64_t* kept_bytes);
 
 /* Rows (capacity) of x_perm / o_perm / dx_perm buffers: each is [rows, d_model] bf16.  Host only. */
 moe_status_t moe_perm_rows(const moe_config_t* cfg, int64_t* rows);
@@ -262,15 +281,19 @@ moe_status_t moe_layer_fwd_fp8(const moe_config_t* cfg, const moe_bf16* x, const
                                const float* wu_scale, const uint8_t* wd8, const float* wd_scale, moe_bf16* y,
                                void* saved, void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* The whole forward: route, dispatch, expert FFN, combine.  Fills `saved` (idx and gates only;
- * activations are recomputed in backward). */
+/* The whole forward: route, dispatch, expert FFN, combine (MoEBlaze summary, the training-loop
+ * figure: fused expert kernels forward, then checkpoint).  Fills `saved` with idx and gates, and
+ * with the kept a and b of the first keep_rows expert-ordered rows when keep_rows > 0; every other
+ * activation is recomputed in the backward (Methodology item 2). */
 moe_status_t moe_layer_fwd(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
                            const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down,
                            moe_bf16* y, void* saved, void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* The whole backward from x, the weights, `saved` and dy: rebuilds the dispatch queues from the
- * saved idx, recomputes the expert activations, and writes dx, dW_r, db_r (nullable) and the
- * expert weight gradients. */
+/* The whole backward from x, the weights, `saved` and dy (MoEBlaze summary, the training-loop
+ * figure: fused expert kernels backward, then gradient reduce): rebuilds the dispatch queues from
+ * the saved idx, recomputes the expert activations of the rows not kept (Methodology item 2), and
+ * writes dx, dW_r, db_r (nullable) and the expert weight gradients.  `saved` must come from
+ * moe_layer_fwd of the same configuration (keep_rows included). */
 moe_status_t moe_layer_bwd(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
                            const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down,
                            const void* saved, const moe_bf16* dy,

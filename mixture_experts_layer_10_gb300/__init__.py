@@ -26,7 +26,8 @@ EXPORTS = ("moe_workspace_size", "moe_perm_rows", "moe_workspace_init", "moe_rou
            "moe_expert_ffn_fwd", "moe_combine", "moe_expert_ffn_bwd", "moe_router_bwd",
            "moe_combine_bwd", "moe_layer_fwd", "moe_layer_bwd", "moe_check_error",
            "moe_debug_inject", "moe_profile_enable", "moe_profile_read", "moe_status_string",
-           "moe_quantize_rows_e4m3", "moe_gate_up_fp8", "moe_down_fp8", "moe_layer_fwd_fp8")
+           "moe_quantize_rows_e4m3", "moe_gate_up_fp8", "moe_down_fp8", "moe_layer_fwd_fp8",
+           "moe_keep_rows_for_budget", "moe_keep_rows_for_free_memory")
 
 
 class moe_config_t(ctypes.Structure):
@@ -60,6 +61,10 @@ def load(path: str | None = None):
     sig = {
         "moe_workspace_size": [cfgp, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)],
         "moe_perm_rows": [cfgp, ctypes.POINTER(ctypes.c_int64)],
+        "moe_keep_rows_for_budget": [cfgp, ctypes.c_uint64, ctypes.POINTER(ctypes.c_int32),
+                                     ctypes.POINTER(ctypes.c_uint64)],
+        "moe_keep_rows_for_free_memory": [cfgp, ctypes.c_uint64, ctypes.POINTER(ctypes.c_int32),
+                                          ctypes.POINTER(ctypes.c_uint64)],
         "moe_workspace_init": [cfgp, _P, ctypes.c_size_t, _P],
         "moe_route": [cfgp, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
         "moe_dispatch": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
@@ -148,6 +153,21 @@ def moe_perm_rows(cfg: moe_config_t) -> int:
     r = ctypes.c_int64()
     _call("moe_perm_rows", ctypes.byref(cfg), ctypes.byref(r))
     return r.value
+
+
+def moe_keep_rows_for_budget(cfg: moe_config_t, budget_bytes: int):
+    """(keep_rows, kept bytes) for a byte budget of kept activations."""
+    r, b = ctypes.c_int32(), ctypes.c_uint64()
+    _call("moe_keep_rows_for_budget", ctypes.byref(cfg), int(budget_bytes), ctypes.byref(r), ctypes.byref(b))
+    return r.value, b.value
+
+
+def moe_keep_rows_for_free_memory(cfg: moe_config_t, reserve_bytes: int):
+    """(keep_rows, kept bytes) for the current device's free memory less ``reserve_bytes``."""
+    r, b = ctypes.c_int32(), ctypes.c_uint64()
+    _call("moe_keep_rows_for_free_memory", ctypes.byref(cfg), int(reserve_bytes), ctypes.byref(r),
+          ctypes.byref(b))
+    return r.value, b.value
 
 
 def moe_workspace_init(cfg, ws, stream=None):

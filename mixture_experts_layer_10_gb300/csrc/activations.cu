@@ -9,8 +9,9 @@
 // where silu'(a) = s (1 + a (1 - s)), s = 1/(1 + e^-a) -- the element-wise tail of the recompute
 // GEMM's epilogue.  A warp owns a row and walks it in 16-byte vectors (coalesced), sums dh'.h in
 // fp32 and leaves it in the row's first gate partial (the others zero), the layout the gate
-// reduction expects.  dB and Hg overwrite the kept a and b in place: each element is read before
-// it is written, by the same thread.
+// reduction expects.  The kept a and b come from the caller's `saved` buffer (fused layer calls) or
+// from the workspace buffers that become dB and Hg (granular calls); in the second case dB and Hg
+// overwrite them in place, each element read before it is written, by the same thread.
 #include <algorithm>
 
 #include <cuda_fp8.h>
@@ -24,7 +25,7 @@ constexpr int kRowsPerBlock = 8;   // one warp per row
 
 __global__ void __launch_bounds__(32 * kRowsPerBlock) swiglu_bwd_kept_kernel(
     const uint16_t* __restrict__ dh, const float* __restrict__ gate_of_prow, uint16_t* __restrict__ dA,
-    uint16_t* __restrict__ a_dB, uint16_t* __restrict__ b_Hg, float* __restrict__ dg_part,
+    const uint16_t* a_in, const uint16_t* b_in, uint16_t* dB, uint16_t* Hg, float* __restrict__ dg_part,
     const Tables* __restrict__ tb, int keep, int f, int ndg) {
   const int lane = threadIdx.x & 31;
   const int rows = min(keep, tb->total_rows);
@@ -34,8 +35,8 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) swiglu_bwd_kept_kernel(
     const size_t base = (size_t)r * f;
     float dg = 0.f;
     for (int v = lane; v < nvec; v += 32) {
-      const uint4 va = reinterpret_cast<const uint4*>(a_dB + base)[v];
-      const uint4 vb = reinterpret_cast<const uint4*>(b_Hg + base)[v];
+      const uint4 va = reinterpret_cast<const uint4*>(a_in + base)[v];
+      const uint4 vb = reinterpret_cast<const uint4*>(b_in + base)[v];
       const uint4 vd = reinterpret_cast<const uint4*>(dh + base)[v];
       const uint32_t ua[4] = {va.x, va.y, va.z, va.w};
       const uint32_t ub[4] = {vb.x, vb.y, vb.z, vb.w};
@@ -63,8 +64,8 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) swiglu_bwd_kept_kernel(
         oh[m] = pack_bf16(o_h[0], o_h[1]);
       }
       reinterpret_cast<uint4*>(dA + base)[v] = make_uint4(oa[0], oa[1], oa[2], oa[3]);
-      reinterpret_cast<uint4*>(a_dB + base)[v] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
-      reinterpret_cast<uint4*>(b_Hg + base)[v] = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+      reinterpret_cast<uint4*>(dB + base)[v] = make_uint4(ob[0], ob[1], ob[2], ob[3]);
+      reinterpret_cast<uint4*>(Hg + base)[v] = make_uint4(oh[0], oh[1], oh[2], oh[3]);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) dg += __shfl_xor_sync(0xffffffffu, dg, off);
@@ -190,8 +191,10 @@ cudaError_t launch_swiglu_bwd_kept(const Cfg& c, const Layout& L, const FfnBwdAr
   if (keep <= 0) return cudaSuccess;
   const int blocks = std::max(1, std::min((keep + kRowsPerBlock - 1) / kRowsPerBlock, num_sms() * 8));
   prof_mark(kKSwigluKept, s, true);
-  swiglu_bwd_kept_kernel<<<blocks, 32 * kRowsPerBlock, 0, s>>>(a.dh, a.gate_of_prow, a.dA, a.dB, a.Hg,
-                                                              a.dg_part, a.tabs, keep, c.f, L.ndg);
+  const uint16_t* a_in = a.a_kept != nullptr ? a.a_kept : a.dB;
+  const uint16_t* b_in = a.b_kept != nullptr ? a.b_kept : a.Hg;
+  swiglu_bwd_kept_kernel<<<blocks, 32 * kRowsPerBlock, 0, s>>>(a.dh, a.gate_of_prow, a.dA, a_in, b_in, a.dB,
+                                                              a.Hg, a.dg_part, a.tabs, keep, c.f, L.ndg);
   prof_mark(kKSwigluKept, s, false);
   return cudaGetLastError();
 }

@@ -151,6 +151,20 @@ Layout make_layout(const Cfg& c) {
   return L;
 }
 
+SavedLayout saved_layout(const Cfg& c) {
+  SavedLayout sl{};
+  sl.keep = (int)std::min<int64_t>(c.keep, make_layout(c).rows);
+  const size_t kept = (size_t)sl.keep * c.f * 2;
+  if (sl.keep == 0) {
+    sl.a_off = sl.b_off = sl.total = (size_t)c.T * c.k * 8;
+    return sl;
+  }
+  sl.a_off = align_up((size_t)c.T * c.k * 8, 256);
+  sl.b_off = sl.a_off + kept;
+  sl.total = sl.b_off + kept;
+  return sl;
+}
+
 int num_sms() {
   static int cache[64] = {0};
   int dev = 0;
@@ -269,7 +283,7 @@ moe_status_t do_dispatch(const Cfg& c, const Ws& w, const int32_t* idx, const ui
 moe_status_t do_ffn_bwd(const Cfg& c, const Ws& w, const uint16_t* x_perm, const uint16_t* dy_perm,
                         const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd,
                         uint16_t* dx_perm, float* dgates, uint16_t* dWg, uint16_t* dWu,
-                        uint16_t* dWd, cudaStream_t s) {
+                        uint16_t* dWd, const uint16_t* a_kept, const uint16_t* b_kept, cudaStream_t s) {
   FfnBwdArgs b{};
   b.x_perm = x_perm;
   b.dy_perm = dy_perm;
@@ -279,8 +293,10 @@ moe_status_t do_ffn_bwd(const Cfg& c, const Ws& w, const uint16_t* x_perm, const
   b.Wd = Wd;
   b.dh = w.at<uint16_t>(w.L.buf_f3);
   b.dA = w.at<uint16_t>(w.L.buf_f0);
-  b.dB = w.at<uint16_t>(w.L.buf_f1);   // holds the kept a of rows [0, c.keep) until the backward
-  b.Hg = w.at<uint16_t>(w.L.buf_f2);   // holds the kept b likewise
+  b.dB = w.at<uint16_t>(w.L.buf_f1);   // granular calls: holds the kept a of rows [0, c.keep)
+  b.Hg = w.at<uint16_t>(w.L.buf_f2);   // granular calls: holds the kept b likewise
+  b.a_kept = a_kept;                    // fused calls: the kept a and b in `saved`
+  b.b_kept = b_kept;
   b.dg_part = w.at<float>(w.L.dg_part);
   b.dx_perm = dx_perm;
   b.dWg = dWg;
@@ -398,8 +414,34 @@ moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* ws_bytes, size_
   MOE_TRY(make_cfg(cfg, &c));
   MOE_NEED(ws_bytes != nullptr);
   *ws_bytes = make_layout(c).total;
-  if (saved_bytes) *saved_bytes = (size_t)c.T * c.k * 8;
+  if (saved_bytes) *saved_bytes = saved_layout(c).total;
   return MOE_OK;
+}
+
+// Kept-row count for a byte budget: a and b of one expert-ordered row take 4 d_ff bytes of
+// `saved`; rows go in pair-tile multiples (256) up to the row capacity.
+moe_status_t moe_keep_rows_for_budget(const moe_config_t* cfg, uint64_t budget_bytes, int32_t* keep_rows,
+                                      uint64_t* kept_bytes) {
+  Cfg c;
+  MOE_TRY(make_cfg(cfg, &c));
+  MOE_NEED(keep_rows != nullptr);
+  const uint64_t per_row = (uint64_t)c.f * 4;
+  const int64_t cap = make_layout(c).rows;
+  const int64_t rows = std::min<int64_t>((int64_t)(budget_bytes / per_row) / kRowTile * kRowTile, cap);
+  *keep_rows = (int32_t)rows;
+  if (kept_bytes) *kept_bytes = (uint64_t)rows * per_row;
+  return MOE_OK;
+}
+
+moe_status_t moe_keep_rows_for_free_memory(const moe_config_t* cfg, uint64_t reserve_bytes, int32_t* keep_rows,
+                                           uint64_t* kept_bytes) {
+  Cfg c;
+  MOE_TRY(make_cfg(cfg, &c));
+  MOE_NEED(keep_rows != nullptr);
+  size_t free_b = 0, total_b = 0;
+  MOE_CUDA(cudaMemGetInfo(&free_b, &total_b));
+  const uint64_t budget = free_b > reserve_bytes ? (uint64_t)free_b - reserve_bytes : 0;
+  return moe_keep_rows_for_budget(cfg, budget, keep_rows, kept_bytes);
 }
 
 moe_status_t moe_perm_rows(const moe_config_t* cfg, int64_t* rows) {
@@ -498,7 +540,7 @@ moe_status_t moe_expert_ffn_bwd(const moe_config_t* cfg, const moe_bf16* x_perm,
   a.dy_perm = w.at<uint16_t>(w.L.dy_perm);
   MOE_CUDA(launch_dispatch_gather(c, w.L, a, false, false, true, stream));
   return do_ffn_bwd(c, w, x_perm, a.dy_perm, W_gate, W_up, W_down, dx_perm, dgates, dW_gate, dW_up,
-                    dW_down, stream);
+                    dW_down, nullptr, nullptr, stream);
 }
 
 moe_status_t moe_router_bwd(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
@@ -637,8 +679,12 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const moe_bf16* x, const flo
   MOE_TRY(do_dispatch(c, w, idx, x, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, x_perm,
                       nullptr, stream));
   uint16_t* o_perm = w.at<uint16_t>(w.L.buf_d1);
+  // kept a and b go to `saved`, which lives from this call to the backward; the workspace does not
+  const SavedLayout sv = saved_layout(c);
+  uint16_t* a_keep = reinterpret_cast<uint16_t*>(static_cast<char*>(saved) + sv.a_off);
+  uint16_t* b_keep = reinterpret_cast<uint16_t*>(static_cast<char*>(saved) + sv.b_off);
   FfnFwdArgs fa{x_perm, W_gate, W_up, W_down, w.at<uint16_t>(w.L.buf_f0), o_perm, w.hdr(), w.tabs(),
-                w.at<uint16_t>(w.L.buf_f1), w.at<uint16_t>(w.L.buf_f2)};
+                a_keep, b_keep};
   MOE_CUDA(launch_ffn_fwd(c, w.L, fa, stream));
   CombineArgs ca{o_perm, gates, y, w.tabs(), w.at<int32_t>(w.L.prow_of_slot)};
   MOE_CUDA(launch_combine(c, ca, stream));
@@ -668,8 +714,11 @@ moe_status_t moe_layer_bwd(const moe_config_t* cfg, const moe_bf16* x, const flo
   MOE_TRY(do_dispatch(c, w, idx, x, dy, gates, nullptr, nullptr, nullptr, nullptr, x_perm, dy_perm, stream));
   uint16_t* dx_perm = w.at<uint16_t>(w.L.buf_d1);
   float* dgates = w.at<float>(w.L.dgates);
+  const SavedLayout sv = saved_layout(c);
+  const uint16_t* a_kept = reinterpret_cast<const uint16_t*>(static_cast<const char*>(saved) + sv.a_off);
+  const uint16_t* b_kept = reinterpret_cast<const uint16_t*>(static_cast<const char*>(saved) + sv.b_off);
   MOE_TRY(do_ffn_bwd(c, w, x_perm, dy_perm, W_gate, W_up, W_down, dx_perm, dgates, dW_gate, dW_up,
-                     dW_down, stream));
+                     dW_down, a_kept, b_kept, stream));
   float* dlogits = w.at<float>(w.L.dlogits);
   MOE_TRY(do_router_bwd(c, w, x, W_r, b_r, idx, gates, dgates, dlogits, dW_r, db_r, stream));
   return do_combine_bwd(c, w, dx_perm, dlogits, W_r, dx, stream);

@@ -121,6 +121,10 @@ __device__ __forceinline__ float sigmoid_fast(float a) { return __fdividef(1.f, 
 // ---------------------------------------------------------------------------------------------
 
 Layout make_layout(const Cfg& c);
+// `saved` of the fused layer calls: idx int32 [T,k], gates fp32 [T,k], then (from the 256-byte
+// boundary a_off) the kept a and b [keep_rows, d_ff] bf16 one after the other.
+struct SavedLayout { size_t a_off, b_off, total; int keep; };
+SavedLayout saved_layout(const Cfg& c);
 moe_status_t make_cfg(const moe_config_t* in, Cfg* c);   // validate a configuration
 moe_status_t check_device();                     // MOE_OK on an sm_103 device
 int num_sms();                                   // SMs of the current device (cached)
@@ -243,10 +247,13 @@ struct FfnBwdArgs {
   const uint16_t* Wg; const uint16_t* Wu; const uint16_t* Wd;
   uint16_t* dh; uint16_t* dA; uint16_t* dB; uint16_t* Hg; float* dg_part; uint16_t* dx_perm;
   uint16_t* dWg; uint16_t* dWu; uint16_t* dWd; Hdr* hdr; const Tables* tabs;
+  // kept a, b of rows [0, c.keep) [rows, d_ff] bf16; null: the forward left them in dB and Hg
+  const uint16_t* a_kept; const uint16_t* b_kept;
 };
 cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, cudaStream_t s);
-// SwiGLU backward of the kept rows [0, c.keep): a is read from a.dB and b from a.Hg (where the
-// forward kept them), dh' from a.dh; writes dA, dB, Hg (in place) and the rows' gate partials.
+// SwiGLU backward of the kept rows [0, c.keep): a and b from a.a_kept / a.b_kept (or, when null,
+// from a.dB / a.Hg where a granular forward kept them), dh' from a.dh; writes dA, dB, Hg and the
+// rows' gate partials.
 cudaError_t launch_swiglu_bwd_kept(const Cfg& c, const Layout& L, const FfnBwdArgs& a, cudaStream_t s);
 
 // FP8 (e4m3) rows: codes [rows, cols] and one fp32 scale per row (amax / 448), from bf16 rows.

@@ -1545,7 +1545,9 @@ cudaError_t launch_gate_up(const Cfg& c, const Layout& L, const FfnFwdArgs& a, i
       !map_3d(&p1.tmWg, a.Wg, c.d, c.f, c.G, 64, 128) || !map_3d(&p1.tmWu, a.Wu, c.d, c.f, c.G, 64, 128) ||
       !map_2d(&p1.tmH, a.h, c.f, rows, 32, 32))
     return cudaErrorInvalidValue;
-  if (kKeep && (!map_2d(&p1.tmA, a.a_keep, c.f, rows, 32, 32) || !map_2d(&p1.tmB, a.b_keep, c.f, rows, 32, 32)))
+  // the kept planes hold `keep` rows (in `saved`, or the workspace for granular calls)
+  if (kKeep && (!map_2d(&p1.tmA, a.a_keep, c.f, (uint64_t)keep, 32, 32) ||
+                !map_2d(&p1.tmB, a.b_keep, c.f, (uint64_t)keep, 32, 32)))
     return cudaErrorInvalidValue;
   p1.f = c.f;
   p1.d = c.d;

@@ -29,6 +29,30 @@ def padded_rows(T: int, k: int, E: int, S: int) -> int:
     return routed + S * math.ceil(T / ROW_TILE) * ROW_TILE
 
 
+def router_n(E: int, k: int) -> int:
+    """Columns the router's logit product computes per token: E <= 64 (k <= 8) stacks the three bf16
+    parts of W_r along N (E rounded to 8/16/32/64, times three, rounded to 16); up to 128 experts
+    the parts take E rounded to 64 each; beyond, the fp32 product computes E."""
+    if E <= 64 and k <= 8:
+        eb = 8 if E <= 8 else 16 if E <= 16 else 32 if E <= 32 else 64
+        return math.ceil(3 * eb / 16) * 16
+    if E <= 128 and k <= 8:
+        return 3 * math.ceil(E / 64) * 64
+    return E
+
+
+def kept_rows(cfg: dict) -> int:
+    """keep_rows as the library applies it: rounded down to the pair tile, at most all rows."""
+    T, E, k, S = cfg["T"], cfg["E"], cfg["k"], cfg.get("S", 0)
+    return min(cfg.get("keep_rows", 0) // ROW_TILE * ROW_TILE, padded_rows(T, k, E, S))
+
+
+def keep_rows_for_budget(cfg: dict, budget_bytes: int) -> int:
+    """The largest keep_rows whose kept a and b (4 d_ff bytes a row) fit in the budget."""
+    T, f, E, k, S = cfg["T"], cfg["f"], cfg["E"], cfg["k"], cfg.get("S", 0)
+    return min(budget_bytes // (4 * f) // ROW_TILE * ROW_TILE, padded_rows(T, k, E, S))
+
+
 def memory(cfg: dict) -> dict:
     """Bytes of device memory one layer instance needs, by owner."""
     T, d, f, E, k, S = cfg["T"], cfg["d"], cfg["f"], cfg["E"], cfg["k"], cfg.get("S", 0)
@@ -39,11 +63,12 @@ def memory(cfg: dict) -> dict:
     per_row = (2 * d + 4 * f + d) * 2 + (4 + 4 + 4 * ndg)   # x/dY/O planes, four d_ff planes, metadata
     workspace = (rows * per_row + T * k * 12 + T * E * 4 + T * Ep * 2 + 4 * d * Ep * 2
                  + math.ceil(T * k / 4096) * E * 4)
-    keep = min(cfg.get("keep_rows", 0) // ROW_TILE * ROW_TILE, rows)
+    keep = kept_rows(cfg)
+    saved = 8 * T * k if keep == 0 else math.ceil(8 * T * k / 256) * 256 + keep * f * 2 * 2
     return {
         "padded_rows": rows,
         "workspace": workspace,
-        "saved": 8 * T * k,
+        "saved": saved,                   # idx, gates and the kept a, b: what lives fwd -> bwd
         "weights": 3 * G * d * f * 2 + d * E * 4,
         "weight_grads": 3 * G * d * f * 2 + d * E * 4,
         "token_tensors": 4 * T * d * 2,   # x, y, dy, dx
@@ -60,9 +85,9 @@ def work(cfg: dict, N: int | None = None, kept_rows: int = 0) -> dict:
     N = T * k if N is None else N
     R = N + S * T                                      # rows the experts see
     Ep = math.ceil(E / 64) * 64
-    tc_router = E <= 128 and k <= 8
+    nr = router_n(E, k)
     out = {
-        "route_fwd": {"flops": 2 * T * d * (3 * Ep if tc_router else E), "bytes": T * d * 2},
+        "route_fwd": {"flops": 2 * T * d * nr, "bytes": T * d * 2},
         "dispatch_gather": {"flops": 0, "bytes": 3 * (T + R) * d * 2 + 36 * T * k},
         "gemm_gate_up_swiglu": {"flops": 4 * R * d * f, "bytes": 0},
         "gemm_down": {"flops": 2 * R * d * f, "bytes": 0},
@@ -71,7 +96,7 @@ def work(cfg: dict, N: int | None = None, kept_rows: int = 0) -> dict:
         "gemm_bwd_recompute_swiglu": {"flops": 4 * (R - kept_rows) * d * f, "bytes": 0},
         "gemm_wgrad": {"flops": 6 * R * d * f, "bytes": 0},
         "gemm_dgrad_x": {"flops": 4 * R * d * f, "bytes": 0},
-        "router_dlogits": {"flops": 2 * T * d * (3 * Ep if tc_router else E), "bytes": T * d * 2},
+        "router_dlogits": {"flops": 2 * T * d * nr, "bytes": T * d * 2},
         "router_dwr": {"flops": 2 * T * d * Ep, "bytes": T * d * 2},
         "gemm_router_dx": {"flops": 2 * T * d * Ep, "bytes": T * d * 2},
         "combine_bwd": {"flops": 0, "bytes": (R + 2 * T) * d * 2 + 4 * T * k},
@@ -107,9 +132,7 @@ def work_forward(cfg: dict, N: int | None = None, fp8: bool = False) -> dict:
     T, d, f, E, k, S = cfg["T"], cfg["d"], cfg["f"], cfg["E"], cfg["k"], cfg.get("S", 0)
     N = T * k if N is None else N
     R = N + S * T
-    Ep = math.ceil(E / 64) * 64
-    tc_router = E <= 128 and k <= 8
-    out = {"route_fwd": {"flops": 2 * T * d * (3 * Ep if tc_router else E), "bytes": T * d * 2}}
+    out = {"route_fwd": {"flops": 2 * T * d * router_n(E, k), "bytes": T * d * 2}}
     if fp8:
         out["quantize_e4m3 (x)"] = {"flops": 0, "bytes": T * d * 3 + 4 * T}
         out["dispatch_gather"] = {"flops": 0, "bytes": (T + R) * d + 8 * R + 12 * T * k}

@@ -87,32 +87,43 @@ def check_layer(moe, c, inp, L, out, buf):
 
 
 def backward_on_oracle_assignment(moe, c, inp, R, buf):
-    """moe_layer_bwd from the oracle's idx and gates (gates rounded to fp32) in `saved`.  With kept
-    activations the backward reads a and b of the forward's expert rows, so the expert forward
-    runs first on the oracle's dispatch (moe_dispatch + moe_expert_ffn_fwd on the same workspace),
-    leaving the rows the backward's own dispatch of the same idx will find."""
+    """The GPU backward from the oracle's idx and gates (gates rounded to fp32).  Without kept
+    activations: written into `saved`, then moe_layer_bwd.  With them, the backward needs the
+    forward's kept a and b of the same dispatch, which moe_layer_fwd (its own routing) cannot give:
+    the granular calls run instead on the oracle's assignment -- moe_dispatch, moe_expert_ffn_fwd
+    (keeping a, b in the workspace), moe_expert_ffn_bwd, moe_router_bwd, moe_combine_bwd."""
     mc = moe.config_from(c)
     T, d, f, E, S, k = c["T"], c["d"], c["f"], c["E"], c["S"], c["k"]
     G = E + S
     idx = to_dev(R.idx.astype(np.int32))
-    buf.saved.view(torch.int32)[:T * k].copy_(idx.view(-1))
-    buf.saved.view(torch.float32)[T * k:2 * T * k].copy_(to_dev(R.gates.astype(np.float32)).view(-1))
-    x, Wg, Wu, Wd = (to_dev_bf16(inp[n]) for n in ("x", "W_gate", "W_up", "W_down"))
-    if c.get("keep_rows", 0) > 0:
-        scratch = [torch.empty(n, dtype=torch.int32, device="cuda") for n in (E, E + 1, T * k, T * k)]
-        x_perm = torch.empty(buf.rows, d, dtype=torch.bfloat16, device="cuda")
-        o_perm = torch.empty(buf.rows, d, dtype=torch.bfloat16, device="cuda")
-        moe.moe_dispatch(mc, idx, x, *scratch, x_perm, buf.ws)
-        moe.moe_expert_ffn_fwd(mc, x_perm, Wg, Wu, Wd, o_perm, buf.ws)
+    gates = to_dev(R.gates.astype(np.float32))
+    x, Wg, Wu, Wd, dy = (to_dev_bf16(inp[n]) for n in ("x", "W_gate", "W_up", "W_down", "dy"))
+    W_r = to_dev(inp["W_r"])
+    b_r = to_dev(inp["b_r"]) if inp["b_r"] is not None else None
     out = dict(dx=torch.empty(T, d, dtype=torch.bfloat16, device="cuda"),
                dW_r=torch.empty(d, E, dtype=torch.float32, device="cuda"),
                db_r=torch.empty(E, dtype=torch.float32, device="cuda"),
                dWg=torch.empty(G, f, d, dtype=torch.bfloat16, device="cuda"),
                dWu=torch.empty(G, f, d, dtype=torch.bfloat16, device="cuda"),
                dWd=torch.empty(G, d, f, dtype=torch.bfloat16, device="cuda"))
-    b_r = to_dev(inp["b_r"]) if inp["b_r"] is not None else None
-    moe.moe_layer_bwd(mc, x, to_dev(inp["W_r"]), b_r, Wg, Wu, Wd, buf.saved, to_dev_bf16(inp["dy"]),
-                      out["dx"], out["dW_r"], out["db_r"], out["dWg"], out["dWu"], out["dWd"], buf.ws)
+    if c.get("keep_rows", 0) > 0:
+        scratch = [torch.empty(n, dtype=torch.int32, device="cuda") for n in (E, E + 1, T * k, T * k)]
+        x_perm = torch.empty(buf.rows, d, dtype=torch.bfloat16, device="cuda")
+        o_perm = torch.empty(buf.rows, d, dtype=torch.bfloat16, device="cuda")
+        dx_perm = torch.empty(buf.rows, d, dtype=torch.bfloat16, device="cuda")
+        dgates = torch.empty(T, k, dtype=torch.float32, device="cuda")
+        dlogits = torch.empty(T, E, dtype=torch.float32, device="cuda")
+        moe.moe_dispatch(mc, idx, x, *scratch, x_perm, buf.ws)
+        moe.moe_expert_ffn_fwd(mc, x_perm, Wg, Wu, Wd, o_perm, buf.ws)
+        moe.moe_expert_ffn_bwd(mc, x_perm, dy, gates, Wg, Wu, Wd, dx_perm, dgates, out["dWg"], out["dWu"],
+                               out["dWd"], buf.ws)
+        moe.moe_router_bwd(mc, x, W_r, b_r, idx, gates, dgates, dlogits, out["dW_r"], out["db_r"], buf.ws)
+        moe.moe_combine_bwd(mc, dx_perm, dlogits, W_r, out["dx"], buf.ws)
+    else:
+        buf.saved.view(torch.int32)[:T * k].copy_(idx.view(-1))
+        buf.saved.view(torch.float32)[T * k:2 * T * k].copy_(gates.view(-1))
+        moe.moe_layer_bwd(mc, x, W_r, b_r, Wg, Wu, Wd, buf.saved, dy, out["dx"], out["dW_r"], out["db_r"],
+                          out["dWg"], out["dWu"], out["dWd"], buf.ws)
     status = moe.moe_check_error(buf.ws)
     assert status == 0, moe.moe_status_string(status)
     return out
@@ -135,6 +146,33 @@ def test_backward_on_oracle_assignment(moe, name, keep):
     check_weight_grad("dW_gate", from_dev_bf16(out["dWg"]), g["dW_gate"])
     check_weight_grad("dW_up", from_dev_bf16(out["dWu"]), g["dW_up"])
     check_weight_grad("dW_down", from_dev_bf16(out["dWd"]), g["dW_down"])
+
+
+# The granularity chosen from a byte budget: keep as many rows as the budget holds, and from the
+# device's free memory at the time of the call.
+@pytest.mark.parametrize("name,tiles", [("ragged_mixtral", 3), ("deepseek_small", 2)])
+def test_layer_kept_rows_from_budget(moe, name, tiles):
+    c, inp, L = case(name)
+    mc = moe.config_from(c)
+    budget = tiles * 256 * 4 * c["f"] + 100
+    rows, kept = moe.moe_keep_rows_for_budget(mc, budget)
+    assert rows == tiles * 256 and kept <= budget
+    c = dict(c, keep_rows=rows)
+    out, buf = run_layer(moe, c, inp)
+    assert buf.saved.numel() >= 8 * c["T"] * c["k"] + kept
+    check_layer(moe, c, inp, L, out, buf)
+
+
+def test_keep_rows_follow_free_memory(moe):
+    c, _, _ = case("ragged_mixtral")
+    mc = moe.config_from(c)
+    cap = moe.moe_perm_rows(mc)
+    free, _ = torch.cuda.mem_get_info()
+    assert moe.moe_keep_rows_for_free_memory(mc, 0)[0] == cap           # plenty free: keep all
+    assert moe.moe_keep_rows_for_free_memory(mc, 1 << 62)[0] == 0       # nothing left: recompute all
+    per_tile = 256 * 4 * c["f"]
+    rows, _ = moe.moe_keep_rows_for_free_memory(mc, max(0, free - 2 * per_tile - per_tile // 2))
+    assert rows in (0, 256, 512)    # about two tiles' bytes free above the reserve
 
 
 @pytest.mark.parametrize("name", ["tiny", "deepseek_small", "gptoss_small"])

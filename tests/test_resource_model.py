@@ -33,6 +33,36 @@ def test_gemm_flops_closed_form(name):
 def test_kept_activation_bytes():
     cfg = dict(synth.CONFIGS["mixtral"], keep_rows=1000)
     assert rm.memory(cfg)["kept_activations"] == 768 * 14336 * 4    # rounded down to 256 rows
+    # the fused calls keep them in `saved`, after idx and gates (from a 256-byte boundary)
+    _, saved = moe.moe_workspace_size(moe.config_from(cfg))
+    assert saved == rm.memory(cfg)["saved"] == 8192 * 2 * 8 + 768 * 14336 * 4
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+def test_keep_rows_for_budget(name):
+    """The library's budget rule: whole 256-row tiles of 4 d_ff bytes each, as many as fit, at
+    most every row; `saved` then grows by exactly the kept bytes."""
+    cfg = synth.CONFIGS[name]
+    mc = moe.config_from(cfg)
+    cap = moe.moe_perm_rows(mc)
+    per_tile = 256 * 4 * cfg["f"]
+    _, saved0 = moe.moe_workspace_size(mc)
+    for budget in [0, per_tile - 1, per_tile, 3 * per_tile + 17, 10 ** 9, 1 << 62]:
+        rows, kept = moe.moe_keep_rows_for_budget(mc, budget)
+        assert rows == rm.keep_rows_for_budget(cfg, budget)
+        assert rows % 256 == 0 and 0 <= rows <= cap
+        assert kept == rows * 4 * cfg["f"] <= budget
+        assert rows == cap or kept + per_tile > budget          # one more tile would not fit
+        _, saved = moe.moe_workspace_size(moe.config_from(dict(cfg, keep_rows=rows)))
+        assert saved - (saved0 + 255) // 256 * 256 == kept if rows else saved == saved0
+    assert moe.moe_keep_rows_for_budget(mc, 1 << 62)[0] == cap
+
+
+def test_router_columns():
+    # stacked hi | mid | lo parts for narrow routers, three padded blocks up to 128 experts
+    assert [rm.router_n(E, 2) for E in (1, 8, 9, 16, 24, 32, 64)] == [32, 32, 48, 48, 96, 96, 192]
+    assert rm.router_n(96, 8) == 384 and rm.router_n(128, 4) == 384 and rm.router_n(200, 4) == 200
+    assert rm.router_n(24, 10) == 24
 
 
 def test_prediction_is_a_roofline():
