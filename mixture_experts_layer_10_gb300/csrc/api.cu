@@ -350,7 +350,7 @@ moe_status_t do_router_bwd(const Cfg& c, const Ws& w, const uint16_t* x, const f
   return MOE_OK;
 }
 
-// Router forward: narrow routers (E <= 64, k <= 8) stream x once with K split across CTAs; up to
+// Router forward: narrow routers (E <= 32, k <= 8) stream x once with K split across CTAs; up to
 // 128 experts the logits run on the tensor cores one 128-token tile per CTA; else the fp32 tile
 // product.  The tensor-core paths split W_r into bf16 parts first.
 moe_status_t do_route(const Cfg& c, const Ws& w, const uint16_t* x, const float* W_r, const float* b_r,

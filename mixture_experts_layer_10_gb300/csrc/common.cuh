@@ -72,7 +72,7 @@ struct Layout {
   size_t hdr, tabs, scan_status, rank, prow_of_slot, slot_of_prow, gate_of_prow, dg_part,
       dlogits, dwr_part, db_part, dgates, xperm, dy_perm, buf_f0, buf_f1, buf_f2, buf_f3, buf_d1,
       dl_bf16, wr_bf16, wr3;
-  size_t rt_part, rt_cnt;   // streaming router (E <= 64): partial logits and part counters
+  size_t rt_part, rt_cnt;   // streaming router (E <= 32): partial logits and part counters
   size_t total;
 };
 
@@ -208,11 +208,11 @@ struct RouterTcArgs {
 cudaError_t launch_route_tc(const Cfg& c, const Layout& L, const RouterTcArgs& a, cudaStream_t s);
 cudaError_t launch_router_dlogits_tc(const Cfg& c, const Layout& L, const RouterTcArgs& a, cudaStream_t s);
 
-// Router logits for E <= 64 and k <= 8, streaming x once with K split across CTAs
+// Router logits for E <= 32 and k <= 8, streaming x once with K split across CTAs
 // (route_tc.cu): W_r's three bf16 parts stacked along N in wstack [Nb][d] (written by the launch
 // into the workspace's wr3 region), partial logits per (tile, part), counters per token quarter.
 struct RouterStreamPlan {
-  int eb;          // E rounded up to 8, 16, 32 or 64
+  int eb;          // E rounded up to 8, 16 or 32
   int ntiles;      // 128-token tiles
   int nslice;      // 256-wide K slices
   int nranges;     // CTAs, each a contiguous run of (tile, slice) pairs

@@ -1,4 +1,4 @@
-// Router logits for narrow routers (E <= 64, k <= 8) on the tensor cores, streaming x once at the
+// Router logits for narrow routers (E <= 32, k <= 8) on the tensor cores, streaming x once at the
 // HBM rate: logits = x W_r (+ b), softmax, top-k and gates (forward), or the router's dlogits
 // (backward, gates not renormalised).  Sources: the Piper explainer ("the problem": a router sends
 // each token to a few experts), the MoEBlaze summary (Limitations: static top-k routing); the
@@ -9,7 +9,7 @@
 //   * W_r (fp32) is split into three bf16 parts hi + mid + lo (each difference exact in fp32), so
 //     every partial product with the bf16 x is exact and only the fp32 accumulation rounds.  The
 //     parts are stacked along the MMA's N dimension -- rows [0, EB) hi, [EB, 2EB) mid, [2EB, 3EB)
-//     lo, with EB = E rounded up to 8, 16, 32 or 64 -- so one tcgen05.mma (M = 128 tokens,
+//     lo, with EB = E rounded up to 8, 16 or 32 -- so one tcgen05.mma (M = 128 tokens,
 //     N = 3 EB rounded up to 16, K = 16) covers all three.
 //   * A tensor-core accumulator loses about one fp32 unit of its own size per K step, so K runs in
 //     256-wide slices (16 steps); each slice starts a fresh accumulator, and the epilogue adds
@@ -177,7 +177,7 @@ __device__ __forceinline__ void finish_token(const Params& p, const float (&l)[E
 #pragma unroll
     for (int e = 0; e < EB; ++e)
       if (e < p.E) p.dlogits[(size_t)t * p.E + e] = dl[e];
-    // the bf16 operand row of the dW_r and dx products: 64 columns (E <= 64), zero past E
+    // the bf16 operand row of the dW_r and dx products: 64 columns (E <= 32), zero past E
     uint4* row = reinterpret_cast<uint4*>(p.dl_bf16 + (size_t)t * 64);
 #pragma unroll
     for (int c = 0; c < 64; c += 8) {
@@ -435,13 +435,13 @@ __global__ void split_wr_stack_kernel(const float* __restrict__ W_r, int d, int 
   }
 }
 
-int bucket_eb(int E) { return E <= 8 ? 8 : (E <= 16 ? 16 : (E <= 32 ? 32 : 64)); }
+int bucket_eb(int E) { return E <= 8 ? 8 : (E <= 16 ? 16 : 32); }
 
 template <int EB, bool kBwd>
 cudaError_t launch_eb(const Cfg& c, const Layout& L, const RouterStreamArgs& a, cudaStream_t s) {
   using S = Shape<EB>;
   const RouterStreamPlan pl = router_stream_plan(c);
-  if (L.Ep != 64) return cudaErrorInvalidValue;   // the bf16 dlogits rows are 64 wide for E <= 64
+  if (L.Ep != 64) return cudaErrorInvalidValue;   // the bf16 dlogits rows are 64 wide for E <= 32
   Params p{};
   if (!map_2d(&p.tmX, a.x, c.d, c.T, 64, 128) || !map_2d(&p.tmW, a.wstack, c.d, S::kNb, 64, S::kNb))
     return cudaErrorInvalidValue;
@@ -490,14 +490,17 @@ cudaError_t launch_stream(const Cfg& c, const Layout& L, const RouterStreamArgs&
   switch (EB) {
     case 8: return launch_eb<8, kBwd>(c, L, a, s);
     case 16: return launch_eb<16, kBwd>(c, L, a, s);
-    case 32: return launch_eb<32, kBwd>(c, L, a, s);
-    default: return launch_eb<64, kBwd>(c, L, a, s);
+    default: return launch_eb<32, kBwd>(c, L, a, s);
   }
 }
 
 }  // namespace
 
-bool router_stream_eligible(const Cfg& c) { return c.E <= 64 && c.k <= kTopK; }
+// Up to 32 experts.  Wider routers stay on the tensor-core kernel that gives each 128-token tile
+// one CTA (gemm.cu): at E = 64 the stacked parts (192 rows) make each stage 40 KB for 16 KB of x,
+// and halving the x bytes in flight cost more than the split K gains (measured, T = 16384,
+// d = 2048, L2 cold: 62 against 39 us forward, 95 against 46 us for the dlogits pass).
+bool router_stream_eligible(const Cfg& c) { return c.E <= 32 && c.k <= kTopK; }
 
 // kRanges CTAs (fewer when there are fewer (tile, slice) pairs), each a contiguous run of pairs;
 // maxseg = the most ranges one tile is split between (sizes the partial-logit buffer).  Fixed by

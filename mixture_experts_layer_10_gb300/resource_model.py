@@ -30,11 +30,11 @@ def padded_rows(T: int, k: int, E: int, S: int) -> int:
 
 
 def router_n(E: int, k: int) -> int:
-    """Columns the router's logit product computes per token: E <= 64 (k <= 8) stacks the three bf16
-    parts of W_r along N (E rounded to 8/16/32/64, times three, rounded to 16); up to 128 experts
+    """Columns the router's logit product computes per token: E <= 32 (k <= 8) stacks the three bf16
+    parts of W_r along N (E rounded to 8/16/32, times three, rounded to 16); up to 128 experts
     the parts take E rounded to 64 each; beyond, the fp32 product computes E."""
-    if E <= 64 and k <= 8:
-        eb = 8 if E <= 8 else 16 if E <= 16 else 32 if E <= 32 else 64
+    if E <= 32 and k <= 8:
+        eb = 8 if E <= 8 else 16 if E <= 16 else 32
         return math.ceil(3 * eb / 16) * 16
     if E <= 128 and k <= 8:
         return 3 * math.ceil(E / 64) * 64

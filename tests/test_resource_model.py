@@ -61,6 +61,7 @@ def test_keep_rows_for_budget(name):
 def test_router_columns():
     # stacked hi | mid | lo parts for narrow routers, three padded blocks up to 128 experts
     assert [rm.router_n(E, 2) for E in (1, 8, 9, 16, 24, 32, 64)] == [32, 32, 48, 48, 96, 96, 192]
+    assert rm.router_n(33, 2) == 384 // 2
     assert rm.router_n(96, 8) == 384 and rm.router_n(128, 4) == 384 and rm.router_n(200, 4) == 200
     assert rm.router_n(24, 10) == 24
 
