@@ -73,7 +73,7 @@ def parse():
     ap.add_argument("--topk", type=int, default=0, help="override k (profiler captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--fp8", action="store_true",
-                    help="also time the forward with e4m3 expert GEMMs beside the bf16 forward")
+                    help="also time the layer with e4m3 expert GEMMs (forward, and forward + backward) beside bf16")
     ap.add_argument("--keep-rows", type=int, default=0,
                     help="expert-ordered rows whose gate/up pre-activations the forward keeps instead "
                          "of the backward recomputing them (0: recompute all, the default; -1: keep all)")
@@ -97,9 +97,12 @@ def peaks():
         return {"hbm": 6800.0, "tensor": 1700.0, "tensor_burst": 1900.0, "source": "fallback"}
 
 
-def fp8_forward(args, mc, cfg, x, W_r, b_r, Wg, Wu, Wd, buf, N, tensor_peak, tensor_kind, pk):
-    """The forward with e4m3 expert GEMMs (weights quantised once, untimed) against the bf16
-    forward on the same inputs, each timed alone over args.steps calls with CUDA events."""
+def fp8_forward(args, mc, cfg, x, W_r, b_r, Wg, Wu, Wd, dy, buf, N, tensor_peak, tensor_kind, pk, ms_bf16_step):
+    """The layer with e4m3 expert GEMMs against bf16 on the same inputs, each timed alone over
+    args.steps calls with CUDA events: the forward (moe_layer_fwd_fp8 against moe_layer_fwd) and
+    the whole step (moe_layer_fwd_fp8 + moe_layer_bwd_fp8 against the bf16 step measured above).
+    The weights are quantised once, untimed: row codes of W_gate, W_up, W_down for the forward,
+    column codes of W_down and of W_gate over W_up for the backward."""
     import torch
     import mixture_experts_layer_10_gb300 as moe
     T, d, f = cfg["T"], cfg["d"], cfg["f"]
@@ -111,10 +114,18 @@ def fp8_forward(args, mc, cfg, x, W_r, b_r, Wg, Wu, Wd, buf, N, tensor_peak, ten
         moe.moe_quantize_rows_e4m3(t, codes, scales)
         return codes, scales
     g8, u8, d8 = quant(Wg), quant(Wu), quant(Wd)
-    # both forwards without kept activations: the FP8 call's scratch shares those buffers, and a
-    # forward alone keeps nothing for a backward
+    wdt = (torch.empty(G, f, d, dtype=torch.uint8, device="cuda"), torch.empty(G, f, dtype=torch.float32, device="cuda"))
+    moe.moe_quantize_cols_e4m3(Wd, None, *wdt)
+    wgut = (torch.empty(G, d, 2 * f, dtype=torch.uint8, device="cuda"),
+            torch.empty(G, d, dtype=torch.float32, device="cuda"))
+    moe.moe_quantize_cols_e4m3(Wg, Wu, *wgut)
+    # without kept activations: the FP8 calls recompute every row from the codes
     mc = moe.config_from(dict(cfg, keep_rows=0))
     y8 = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    dx8 = torch.empty(T, d, dtype=torch.bfloat16, device="cuda")
+    dW_r = torch.empty(d, cfg["E"], dtype=torch.float32, device="cuda")
+    db_r = torch.empty(cfg["E"], dtype=torch.float32, device="cuda") if b_r is not None else None
+    dWg, dWu, dWd = torch.empty_like(Wg), torch.empty_like(Wu), torch.empty_like(Wd)
     stream = torch.cuda.current_stream()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
@@ -132,11 +143,20 @@ def fp8_forward(args, mc, cfg, x, W_r, b_r, Wg, Wu, Wd, buf, N, tensor_peak, ten
         moe.moe_profile_enable(False)
         status = moe.moe_check_error(buf.ws)
         if status != 0:
-            raise RuntimeError(f"forward failed: {moe.moe_status_string(status)}")
+            raise RuntimeError(f"fp8 layer failed: {moe.moe_status_string(status)}")
         return ev0.elapsed_time(ev1) / args.steps, prof
 
+    def fwd8():
+        moe.moe_layer_fwd_fp8(mc, x, W_r, b_r, *g8, *u8, *d8, y8, buf.saved, buf.ws)
+
+    def step8():
+        fwd8()
+        moe.moe_layer_bwd_fp8(mc, x, W_r, b_r, *g8, *u8, *wdt, *wgut, buf.saved, dy, dx8, dW_r, db_r, dWg, dWu,
+                              dWd, buf.ws)
+
     ms16, _ = timed(lambda: moe.moe_layer_fwd(mc, x, W_r, b_r, Wg, Wu, Wd, y8, buf.saved, buf.ws), False)
-    ms8, prof = timed(lambda: moe.moe_layer_fwd_fp8(mc, x, W_r, b_r, *g8, *u8, *d8, y8, buf.saved, buf.ws), True)
+    ms8, prof = timed(fwd8, True)
+    ms8_step, prof_step = timed(step8, True)
     peak8 = 2 * tensor_peak
     kern = {}
     for name, flops in (("gemm_gate_up_fp8", 4 * N * d * f), ("gemm_down_fp8", 2 * N * d * f)):
@@ -148,6 +168,17 @@ def fp8_forward(args, mc, cfg, x, W_r, b_r, Wg, Wu, Wd, buf, N, tensor_peak, ten
     if n:   # the T token rows of x and the N rows of h: bf16 in, codes and a scale out
         gbs = ((T * d + N * f) * 3 + 4 * (T + N)) * args.steps / (tot / 1000.0) / 1e9
         kern["quantize_e4m3"] = {"ms_per_step": tot / args.steps, "gbs": gbs, "frac": gbs / pk["hbm"]}
+    step_kern = {}
+    for name, flops in (("gemm_bwd_dgrad_down_fp8", 2 * N * d * f), ("gemm_bwd_recompute_swiglu_fp8", 4 * N * d * f),
+                        ("gemm_dgrad_x_fp8", 4 * N * d * f)):
+        tot, n = prof_step.get(name, (0.0, 0))
+        if n:
+            tf = flops * n / (tot / 1000.0) / 1e12
+            step_kern[name] = {"ms_per_step": tot / args.steps, "tflops": tf, "frac": tf / peak8}
+    for name in ("gemm_wgrad", "quantize_e4m3", "dispatch_gather", "combine_bwd"):
+        tot, n = prof_step.get(name, (0.0, 0))
+        if n:
+            step_kern[name] = {"ms_per_step": tot / args.steps, "launches": n}
     # the resource model's roofline for both forwards, on the same peaks
     from mixture_experts_layer_10_gb300 import resource_model
     n_routed = N - cfg["S"] * T
@@ -155,6 +186,9 @@ def fp8_forward(args, mc, cfg, x, W_r, b_r, Wg, Wu, Wd, buf, N, tensor_peak, ten
     p8 = resource_model.predict_forward_ms(cfg, tensor_peak, pk["hbm"], N=n_routed, fp8=True)["step_ms"]
     return {"metric": "forward tokens/s (e4m3 expert GEMMs)", "value": T / (ms8 / 1000.0), "fwd_ms": ms8,
             "bf16_fwd_ms": ms16, "speedup_vs_bf16_fwd": ms16 / ms8,
+            "step": {"metric": METRIC + " (e4m3 expert GEMMs)", "value": T / (ms8_step / 1000.0),
+                     "ms_per_step": ms8_step, "bf16_ms_per_step": ms_bf16_step,
+                     "speedup_vs_bf16_step": ms_bf16_step / ms8_step, "kernels": step_kern},
             "model": {"fp8_fwd_predicted_ms": p8, "fp8_measured_over_predicted": ms8 / p8,
                       "bf16_fwd_predicted_ms": p16, "bf16_measured_over_predicted": ms16 / p16},
             "peak_tflops": peak8, "peak_kind": "2 x " + tensor_kind.split(":")[0] + " (nominal fp8:bf16 ratio)",
@@ -525,7 +559,7 @@ def run_workload(args, name, cfg, steps, warmup, rank, world, local, barrier, ex
                    "bf16_tflops_sustained (%s): SM clock below max in the timed region") % pk["source"]
     fp8_line = None
     if args.fp8 and not extra:
-        fp8_line = fp8_forward(args, mc, cfg, x, W_r, b_r, Wg, Wu, Wd, buf, N, tensor_peak, tensor_kind, pk)
+        fp8_line = fp8_forward(args, mc, cfg, x, W_r, b_r, Wg, Wu, Wd, dy, buf, N, tensor_peak, tensor_kind, pk, ms)
     kernels = {}
     gemm_flops = gemm_ms = hbm_bytes = hbm_ms = 0.0
     launches = 0

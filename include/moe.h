@@ -281,6 +281,41 @@ moe_status_t moe_layer_fwd_fp8(const moe_config_t* cfg, const moe_bf16* x, const
                                const float* wu_scale, const uint8_t* wd8, const float* wd_scale, moe_bf16* y,
                                void* saved, void* ws, size_t ws_bytes, moe_stream_t stream);
 
+/* Per-column e4m3 codes, written transposed, for the FP8 backward's weights (same format as
+ * moe_quantize_rows_e4m3: scale = amax / 448 over the column, 1 for an all-zero column; code =
+ * e4m3(v / scale) rounded to nearest even and saturated, both in fp32).  For each of G experts the
+ * source is [top[g]; bottom[g]], rows_top + rows_bottom rows of `cols` bf16 values (bottom NULL when
+ * rows_bottom is 0); codes[g] receives its transpose [cols, rows_top + rows_bottom] and scales[g]
+ * one scale per column.  Used as
+ *   W_down [G, d, f]                     -> codes [G, f, d], scales [G, f]   (top = W_down)
+ *   W_gate, W_up [G, f, d] (stacked)     -> codes [G, d, 2f], scales [G, d]  (top = W_gate, bottom = W_up)
+ * rows_top + rows_bottom a multiple of 16, at most 32768; 16-byte-aligned pointers.  The column
+ * maxima are gathered in `scales` before it receives the scales.  Argument errors return before
+ * any work is queued. */
+moe_status_t moe_quantize_cols_e4m3(const moe_bf16* top, const moe_bf16* bottom, int64_t G, int32_t rows_top,
+                                    int32_t rows_bottom, int32_t cols, uint8_t* codes, float* scales,
+                                    moe_stream_t stream);
+
+/* The whole backward with e4m3 expert GEMMs (the MoEBlaze summary names mixed-precision and
+ * quantised experts as future work; the format is this library's reading): as moe_layer_bwd, with
+ *   dh' = (s_dy q_dy) (s_wd q_wd)^T     dY rows quantised per row; W_down's columns per d_ff channel
+ *                                       (wdt8, wdt_scale from moe_quantize_cols_e4m3 of W_down)
+ *   a, b = the forward's e4m3 products, recomputed from the x rows (quantised per row) and the
+ *          forward's row codes of W_gate and W_up (wg8, wg_scale, wu8, wu_scale)
+ *   dA, dB, Hg from the SwiGLU backward in fp32, held in bf16 (dh' too)
+ *   dX = (s_ab q_ab) (s_w q_w)^T        the joined row [dA | dB] quantised per row; column i of
+ *                                       W_gate and W_up quantised together per d_model channel
+ *                                       (wgut8, wgut_scale from moe_quantize_cols_e4m3 of W_gate over W_up)
+ * accumulated in fp32.  The weight gradients stay bf16 products of dA, dB, Hg and the bf16 x and dY
+ * rows; the router stays fp32.  `saved` comes from moe_layer_fwd or moe_layer_fwd_fp8 of the same
+ * configuration; keep_rows must be 0 (MOE_ERR_INVALID_ARG otherwise). */
+moe_status_t moe_layer_bwd_fp8(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
+                               const uint8_t* wg8, const float* wg_scale, const uint8_t* wu8, const float* wu_scale,
+                               const uint8_t* wdt8, const float* wdt_scale, const uint8_t* wgut8,
+                               const float* wgut_scale, const void* saved, const moe_bf16* dy, moe_bf16* dx,
+                               float* dW_r, float* db_r, moe_bf16* dW_gate, moe_bf16* dW_up, moe_bf16* dW_down,
+                               void* ws, size_t ws_bytes, moe_stream_t stream);
+
 /* The whole forward: route, dispatch, expert FFN, combine (MoEBlaze summary, the training-loop
  * figure: fused expert kernels forward, then checkpoint).  Fills `saved` with idx and gates, and
  * with the kept a and b of the first keep_rows expert-ordered rows when keep_rows > 0; every other

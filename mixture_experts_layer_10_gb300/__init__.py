@@ -27,7 +27,8 @@ EXPORTS = ("moe_workspace_size", "moe_perm_rows", "moe_workspace_init", "moe_rou
            "moe_combine_bwd", "moe_layer_fwd", "moe_layer_bwd", "moe_check_error",
            "moe_debug_inject", "moe_profile_enable", "moe_profile_read", "moe_status_string",
            "moe_quantize_rows_e4m3", "moe_gate_up_fp8", "moe_down_fp8", "moe_layer_fwd_fp8",
-           "moe_keep_rows_for_budget", "moe_keep_rows_for_free_memory")
+           "moe_keep_rows_for_budget", "moe_keep_rows_for_free_memory", "moe_quantize_cols_e4m3",
+           "moe_layer_bwd_fp8")
 
 
 class moe_config_t(ctypes.Structure):
@@ -78,6 +79,9 @@ def load(path: str | None = None):
         "moe_gate_up_fp8": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
         "moe_down_fp8": [cfgp, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
         "moe_layer_fwd_fp8": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
+        "moe_quantize_cols_e4m3": [_P, _P, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, _P, _P,
+                                   _P],
+        "moe_layer_bwd_fp8": [cfgp] + [_P] * 20 + [ctypes.c_size_t, _P],
         "moe_layer_fwd": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P],
         "moe_layer_bwd": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                           ctypes.c_size_t, _P],
@@ -240,6 +244,23 @@ def moe_layer_fwd_fp8(cfg, x, W_r, b_r, wg8, wg_scale, wu8, wu_scale, wd8, wd_sc
     _call("moe_layer_fwd_fp8", ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(b_r), _ptr(wg8), _ptr(wg_scale),
           _ptr(wu8), _ptr(wu_scale), _ptr(wd8), _ptr(wd_scale), _ptr(y), _ptr(saved), _ptr(ws), ws.numel(),
           _stream(stream))
+
+
+def moe_quantize_cols_e4m3(top, bottom, codes, scales, stream=None):
+    """top [G, r1, cols] (and bottom [G, r2, cols] or None) bf16 -> codes [G, cols, r1 + r2] uint8 and
+    scales [G, cols] fp32: per-column codes of the stacked source, transposed."""
+    G, r1, cols = top.shape
+    r2 = 0 if bottom is None else bottom.shape[1]
+    _call("moe_quantize_cols_e4m3", _ptr(top), _ptr(bottom), int(G), int(r1), int(r2), int(cols), _ptr(codes),
+          _ptr(scales), _stream(stream))
+
+
+def moe_layer_bwd_fp8(cfg, x, W_r, b_r, wg8, wg_scale, wu8, wu_scale, wdt8, wdt_scale, wgut8, wgut_scale, saved, dy,
+                      dx, dW_r, db_r, dW_gate, dW_up, dW_down, ws, stream=None):
+    _call("moe_layer_bwd_fp8", ctypes.byref(cfg), _ptr(x), _ptr(W_r), _ptr(b_r), _ptr(wg8), _ptr(wg_scale),
+          _ptr(wu8), _ptr(wu_scale), _ptr(wdt8), _ptr(wdt_scale), _ptr(wgut8), _ptr(wgut_scale), _ptr(saved),
+          _ptr(dy), _ptr(dx), _ptr(dW_r), _ptr(db_r), _ptr(dW_gate), _ptr(dW_up), _ptr(dW_down), _ptr(ws),
+          ws.numel(), _stream(stream))
 
 
 def moe_layer_fwd(cfg, x, W_r, b_r, W_gate, W_up, W_down, y, saved, ws, stream=None):

@@ -1,4 +1,4 @@
-// Element-wise kernels: the SwiGLU backward of kept rows, and the FP8 row quantiser.
+// Element-wise kernels: the SwiGLU backward of kept rows, and the FP8 row and column quantisers.
 //
 // SwiGLU backward of the rows whose gate/up pre-activations the forward kept (MoEBlaze,
 // Methodology item 2: the checkpointing choice, here made per row range instead of all-or-nothing).
@@ -108,25 +108,29 @@ __device__ __forceinline__ uint2 encode8_e4m3(const uint4& u, float scale, float
 }
 
 template <int kThreads>
-__global__ void __launch_bounds__(kThreads) quantize_rows_e4m3_kernel(const uint16_t* __restrict__ src, int64_t rows,
-                                                                      int cols, uint8_t* __restrict__ codes,
+__global__ void __launch_bounds__(kThreads) quantize_rows_e4m3_kernel(const uint16_t* __restrict__ src, int cols1,
+                                                                      const uint16_t* __restrict__ src2, int cols2,
+                                                                      int64_t rows, uint8_t* __restrict__ codes,
                                                                       float* __restrict__ scales,
                                                                       const Tables* __restrict__ tb) {
   constexpr int kWarps = kThreads / 32;
   __shared__ float part[2][kWarps];   // per-warp maxima, double-buffered across rows
   if (tb != nullptr) rows = min(rows, (int64_t)tb->total_rows);
-  const int nvec = cols / 8;
+  // a row is src's row (cols1 values) followed by src2's (cols2 values, often none)
+  const int nvec1 = cols1 / 8, nvec = (cols1 + cols2) / 8;
+  const int cols = cols1 + cols2;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int buf = 0;
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x, buf ^= 1) {
-    const uint4* row = reinterpret_cast<const uint4*>(src + r * cols);
+    const uint4* row = reinterpret_cast<const uint4*>(src + r * cols1);
+    const uint4* row2 = reinterpret_cast<const uint4*>(src2 + r * cols2);
     uint4 v[kQuantV];
     float amax = 0.f;
 #pragma unroll
     for (int i = 0; i < kQuantV; ++i) {
       const int q = threadIdx.x + i * kThreads;
       if (q < nvec) {
-        v[i] = row[q];
+        v[i] = q < nvec1 ? row[q] : row2[q - nvec1];
         const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
         for (int m = 0; m < 4; ++m) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[m])), fabsf(bf16_hi(w[m]))));
@@ -161,28 +165,136 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_e4m3_kernel(const uint
 }
 
 template <int kThreads>
-void launch_quantize(const uint16_t* src, int64_t rows, int cols, uint8_t* codes, float* scales, const Tables* tabs,
-                     cudaStream_t s) {
+void launch_quantize(const uint16_t* src, int cols1, const uint16_t* src2, int cols2, int64_t rows, uint8_t* codes,
+                     float* scales, const Tables* tabs, cudaStream_t s) {
   const int per_sm = std::min(32, 2048 / kThreads);
   const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)num_sms() * per_sm));
-  quantize_rows_e4m3_kernel<kThreads><<<(int)blocks, kThreads, 0, s>>>(src, rows, cols, codes, scales, tabs);
+  quantize_rows_e4m3_kernel<kThreads><<<(int)blocks, kThreads, 0, s>>>(src, cols1, src2, cols2, rows, codes, scales,
+                                                                      tabs);
+}
+
+// ---- columns: per-column e4m3 codes written transposed (the K-major operand whose rows are the
+// source's columns), for the backward's weights: W_d's columns (one scale per d_ff channel) and
+// column i of W_gate and W_up together (one scale per d_model channel).  The source of expert g is
+// [top[g] (rows_top rows); bottom[g] (rows_bot rows)], [rows, cols] bf16; codes[g] is [cols, rows].
+// Three passes: column maxima (atomicMax on the bit patterns of non-negative floats, which order
+// like the values, so the result does not depend on the order of the blocks); the encode, 64 rows
+// x 32 columns per block, transposed through shared memory; the scales from the maxima.
+
+constexpr int kColRows = 256;   // rows per block of the column-maximum pass
+
+__device__ __forceinline__ float col_src(const uint16_t* top, const uint16_t* bot, int g, int rt, int rb, int cols,
+                                         int r, int c) {
+  const uint16_t u = r < rt ? top[((size_t)g * rt + r) * cols + c] : bot[((size_t)g * rb + (r - rt)) * cols + c];
+  return __uint_as_float((uint32_t)u << 16);
+}
+
+__global__ void col_amax_kernel(const uint16_t* __restrict__ top, const uint16_t* __restrict__ bot, int rt, int rb,
+                                int cols, uint32_t* __restrict__ amax_bits) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  const int g = blockIdx.z;
+  if (c >= cols) return;
+  const int r0 = blockIdx.y * kColRows, r1 = min(rt + rb, r0 + kColRows);
+  float m = 0.f;
+  for (int r = r0; r < r1; ++r) m = fmaxf(m, fabsf(col_src(top, bot, g, rt, rb, cols, r, c)));
+  atomicMax(&amax_bits[(size_t)g * cols + c], __float_as_uint(m));
+}
+
+// 32 x 8 threads; a block encodes rows [r0, r0 + 64) of columns [c0, c0 + 32) of expert g
+__global__ void col_encode_kernel(const uint16_t* __restrict__ top, const uint16_t* __restrict__ bot, int rt, int rb,
+                                  int cols, const uint32_t* __restrict__ amax_bits, uint8_t* __restrict__ codes) {
+  __shared__ uint8_t tile[32][64 + 16];
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  const int rows = rt + rb;
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 64, g = blockIdx.z;
+  const int c = c0 + tx;
+  float scale = 1.f, y = 1.f;
+  if (c < cols) {
+    const float amax = __uint_as_float(amax_bits[(size_t)g * cols + c]);
+    scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    y = __frcp_rn(scale);
+  }
+  const bool recip = scale >= 0x1p-80f && scale <= 0x1p80f;
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int rr = 2 * ty + 16 * k;   // this thread's row pair within the tile
+    const int r = r0 + rr;
+    float v0 = 0.f, v1 = 0.f;
+    if (c < cols && r < rows) v0 = col_src(top, bot, g, rt, rb, cols, r, c);
+    if (c < cols && r + 1 < rows) v1 = col_src(top, bot, g, rt, rb, cols, r + 1, c);
+    const float2 f2 = recip ? make_float2(div_by_scale(v0, scale, y), div_by_scale(v1, scale, y))
+                            : make_float2(__fdiv_rn(v0, scale), __fdiv_rn(v1, scale));
+    const uint32_t cc = (uint32_t)__nv_cvt_float2_to_fp8x2(f2, __NV_SATFINITE, __NV_E4M3);
+    tile[tx][rr] = (uint8_t)(cc & 0xFFu);
+    tile[tx][rr + 1] = (uint8_t)(cc >> 8);
+  }
+  __syncthreads();
+  // column c0 + j gets codes of rows r0 .. r0 + 63: eight bytes per thread, 256 threads = 32 x 64
+  const int j = threadIdx.x >> 3, part = threadIdx.x & 7;
+  const int cc = c0 + j, rr = r0 + part * 8;
+  if (cc >= cols || rr >= rows) return;
+  uint8_t* dst = codes + ((size_t)g * cols + cc) * rows + rr;
+  if (rr + 8 <= rows) {
+    uint32_t w0 = 0, w1 = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      w0 |= (uint32_t)tile[j][part * 8 + b] << (8 * b);
+      w1 |= (uint32_t)tile[j][part * 8 + 4 + b] << (8 * b);
+    }
+    *reinterpret_cast<uint2*>(dst) = make_uint2(w0, w1);   // rows is a multiple of 16: 8-byte aligned
+  } else {
+    for (int b = 0; rr + b < rows; ++b) dst[b] = tile[j][part * 8 + b];
+  }
+}
+
+__global__ void col_scales_kernel(const uint32_t* __restrict__ amax_bits, float* __restrict__ scales, int64_t n) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const float amax = __uint_as_float(amax_bits[i]);
+    scales[i] = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  }
 }
 
 }  // namespace
 
 cudaError_t launch_quantize_rows_e4m3(const uint16_t* src, int64_t rows, int cols, uint8_t* codes, float* scales,
                                       cudaStream_t s, const Tables* tabs) {
+  return launch_quantize_rows2_e4m3(src, cols, nullptr, 0, rows, codes, scales, s, tabs);
+}
+
+cudaError_t launch_quantize_rows2_e4m3(const uint16_t* src, int cols1, const uint16_t* src2, int cols2, int64_t rows,
+                                       uint8_t* codes, float* scales, cudaStream_t s, const Tables* tabs) {
   if (rows <= 0) return cudaSuccess;
-  // threads per row: about four vectors each, between one warp and 256 threads (eight vectors
-  // each at the widest row, 16384 values)
-  const int nvec = cols / 8;
-  if (nvec > kQuantV * 256) return cudaErrorInvalidValue;
+  // threads per row: about four vectors each, between one warp and 512 threads (eight vectors
+  // each at the widest row, 32768 values)
+  const int nvec = (cols1 + cols2) / 8;
+  if (nvec > kQuantV * 512 || cols1 % 8 != 0 || cols2 % 8 != 0) return cudaErrorInvalidValue;
   prof_mark(kKQuantE4m3, s, true);
-  if (nvec <= 4 * 32) launch_quantize<32>(src, rows, cols, codes, scales, tabs, s);
-  else if (nvec <= 4 * 64) launch_quantize<64>(src, rows, cols, codes, scales, tabs, s);
-  else if (nvec <= 4 * 128) launch_quantize<128>(src, rows, cols, codes, scales, tabs, s);
-  else launch_quantize<256>(src, rows, cols, codes, scales, tabs, s);
+  if (nvec <= 4 * 32) launch_quantize<32>(src, cols1, src2, cols2, rows, codes, scales, tabs, s);
+  else if (nvec <= 4 * 64) launch_quantize<64>(src, cols1, src2, cols2, rows, codes, scales, tabs, s);
+  else if (nvec <= 4 * 128) launch_quantize<128>(src, cols1, src2, cols2, rows, codes, scales, tabs, s);
+  else if (nvec <= kQuantV * 256) launch_quantize<256>(src, cols1, src2, cols2, rows, codes, scales, tabs, s);
+  else launch_quantize<512>(src, cols1, src2, cols2, rows, codes, scales, tabs, s);
   prof_mark(kKQuantE4m3, s, false);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_cols_e4m3(const uint16_t* top, const uint16_t* bottom, int64_t G, int rows_top,
+                                      int rows_bot, int cols, uint8_t* codes, float* scales, cudaStream_t s) {
+  if (G <= 0) return cudaSuccess;
+  const int rows = rows_top + rows_bot;
+  // the maxima are collected in `scales` (as bit patterns), then turned into scales in place
+  uint32_t* amax = reinterpret_cast<uint32_t*>(scales);
+  cudaError_t e = cudaMemsetAsync(amax, 0, (size_t)G * cols * sizeof(uint32_t), s);
+  if (e != cudaSuccess) return e;
+  prof_mark(kKQuantCols, s, true);
+  col_amax_kernel<<<dim3((cols + 255) / 256, (rows + kColRows - 1) / kColRows, (unsigned)G), 256, 0, s>>>(
+      top, bottom, rows_top, rows_bot, cols, amax);
+  col_encode_kernel<<<dim3((cols + 31) / 32, (rows + 63) / 64, (unsigned)G), 256, 0, s>>>(top, bottom, rows_top,
+                                                                                         rows_bot, cols, amax, codes);
+  const int64_t n = G * (int64_t)cols;
+  col_scales_kernel<<<(int)std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, (int64_t)num_sms() * 8)), 256, 0, s>>>(
+      amax, scales, n);
+  prof_mark(kKQuantCols, s, false);
   return cudaGetLastError();
 }
 

@@ -142,6 +142,7 @@ Layout make_layout(const Cfg& c) {
   L.dl_bf16 = take((size_t)c.T * L.Ep * 2);
   L.wr_bf16 = take((size_t)c.d * L.Ep * 2);
   L.wr3 = take((size_t)3 * L.Ep * c.d * 2);
+  L.fp8s = take(rows * 3 * 4);
   if (router_stream_eligible(c)) {
     const RouterStreamPlan pl = router_stream_plan(c);
     L.rt_part = take(pl.maxseg > 1 ? (size_t)pl.ntiles * pl.maxseg * pl.eb * 128 * 4 : 0);
@@ -199,7 +200,8 @@ const char* const kKernelNames[kKCount] = {
     "route_fwd", "dispatch_scan", "dispatch_gather", "gemm_gate_up_swiglu", "gemm_down",
     "combine", "gemm_bwd_recompute_swiglu", "gemm_wgrad", "gemm_dgrad_x", "dgates_reduce",
     "router_dlogits", "router_dwr", "router_reduce", "combine_bwd", "gemm_bwd_dgrad_down",
-    "gemm_router_dx", "swiglu_bwd_kept", "gemm_gate_up_fp8", "quantize_e4m3", "gemm_down_fp8"};
+    "gemm_router_dx", "swiglu_bwd_kept", "gemm_gate_up_fp8", "quantize_e4m3", "gemm_down_fp8",
+    "quantize_cols_e4m3", "gemm_bwd_dgrad_down_fp8", "gemm_bwd_recompute_swiglu_fp8", "gemm_dgrad_x_fp8"};
 
 struct Profiler {
   std::mutex mu;
@@ -305,6 +307,57 @@ moe_status_t do_ffn_bwd(const Cfg& c, const Ws& w, const uint16_t* x_perm, const
   b.hdr = w.hdr();
   b.tabs = w.tabs();
   MOE_CUDA(launch_ffn_bwd(c, w.L, b, s));
+  DgatesArgs g{};
+  g.dg_part = b.dg_part;
+  g.prow_of_slot = w.at<int32_t>(w.L.prow_of_slot);
+  g.dgates = dgates;
+  MOE_CUDA(launch_dgates(c, w.L, g, s));
+  return MOE_OK;
+}
+
+// The FP8 expert-FFN backward on the rows moe_dispatch laid out (x_perm, dy_perm, gates per row).
+// Scratch: the x and dY rows' codes share buf_d1 (free until dgrad x writes dx_perm there), their
+// scales and the [dA | dB] rows' scales go to fp8s, the [dA | dB] codes to buf_f3 once dh' is used.
+moe_status_t do_ffn_bwd_fp8(const Cfg& c, const Ws& w, const uint8_t* wg8, const float* wg_scale,
+                            const uint8_t* wu8, const float* wu_scale, const uint8_t* wdt8,
+                            const float* wdt_scale, const uint8_t* wgut8, const float* wgut_scale,
+                            float* dgates, uint16_t* dWg, uint16_t* dWu, uint16_t* dWd, cudaStream_t s) {
+  const size_t rows = (size_t)w.L.rows;
+  FfnBwd8Args b{};
+  b.x_perm = w.at<uint16_t>(w.L.xperm);
+  b.dy_perm = w.at<uint16_t>(w.L.dy_perm);
+  uint8_t* x8 = w.at<uint8_t>(w.L.buf_d1);
+  uint8_t* dy8 = x8 + rows * c.d;
+  float* sc = w.at<float>(w.L.fp8s);
+  MOE_CUDA(launch_quantize_rows_e4m3(b.x_perm, (int64_t)rows, c.d, x8, sc, s, w.tabs()));
+  MOE_CUDA(launch_quantize_rows_e4m3(b.dy_perm, (int64_t)rows, c.d, dy8, sc + rows, s, w.tabs()));
+  b.x8 = x8;
+  b.xs = sc;
+  b.dy8 = dy8;
+  b.dys = sc + rows;
+  b.wg8 = wg8;
+  b.gs = wg_scale;
+  b.wu8 = wu8;
+  b.us = wu_scale;
+  b.wdt8 = wdt8;
+  b.wdts = wdt_scale;
+  b.wgut8 = wgut8;
+  b.wguts = wgut_scale;
+  b.gate_of_prow = w.at<float>(w.L.gate_of_prow);
+  b.dh = w.at<uint16_t>(w.L.buf_f3);
+  b.dA = w.at<uint16_t>(w.L.buf_f0);
+  b.dB = w.at<uint16_t>(w.L.buf_f1);
+  b.Hg = w.at<uint16_t>(w.L.buf_f2);
+  b.dg_part = w.at<float>(w.L.dg_part);
+  b.dab8 = w.at<uint8_t>(w.L.buf_f3);
+  b.dabs = sc + 2 * rows;
+  b.dx_perm = w.at<uint16_t>(w.L.buf_d1);
+  b.dWg = dWg;
+  b.dWu = dWu;
+  b.dWd = dWd;
+  b.hdr = w.hdr();
+  b.tabs = w.tabs();
+  MOE_CUDA(launch_ffn_bwd_fp8(c, w.L, b, s));
   DgatesArgs g{};
   g.dg_part = b.dg_part;
   g.prow_of_slot = w.at<int32_t>(w.L.prow_of_slot);
@@ -722,6 +775,50 @@ moe_status_t moe_layer_bwd(const moe_config_t* cfg, const moe_bf16* x, const flo
   float* dlogits = w.at<float>(w.L.dlogits);
   MOE_TRY(do_router_bwd(c, w, x, W_r, b_r, idx, gates, dgates, dlogits, dW_r, db_r, stream));
   return do_combine_bwd(c, w, dx_perm, dlogits, W_r, dx, stream);
+}
+
+moe_status_t moe_quantize_cols_e4m3(const moe_bf16* top, const moe_bf16* bottom, int64_t G, int32_t rows_top,
+                                    int32_t rows_bottom, int32_t cols, uint8_t* codes, float* scales,
+                                    moe_stream_t stream) {
+  MOE_NEED(G >= 0 && G <= 65535 && rows_top >= 1 && rows_bottom >= 0 && cols >= 1);
+  const int64_t rows = (int64_t)rows_top + rows_bottom;
+  MOE_NEED(rows % 16 == 0 && rows <= 32768 && (int64_t)cols * G <= ((int64_t)1 << 31));
+  MOE_NEED((rows_bottom == 0) == (bottom == nullptr));
+  MOE_NEED(G == 0 || (top && codes && scales && aligned16(top) && aligned16(codes) && aligned16(scales) &&
+                      (!bottom || aligned16(bottom))));
+  MOE_TRY(check_device());
+  MOE_CUDA(launch_quantize_cols_e4m3(top, bottom, G, rows_top, rows_bottom, cols, codes, scales, stream));
+  return MOE_OK;
+}
+
+moe_status_t moe_layer_bwd_fp8(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
+                               const uint8_t* wg8, const float* wg_scale, const uint8_t* wu8, const float* wu_scale,
+                               const uint8_t* wdt8, const float* wdt_scale, const uint8_t* wgut8,
+                               const float* wgut_scale, const void* saved, const moe_bf16* dy, moe_bf16* dx,
+                               float* dW_r, float* db_r, moe_bf16* dW_gate, moe_bf16* dW_up, moe_bf16* dW_down,
+                               void* ws, size_t ws_bytes, moe_stream_t stream) {
+  Cfg c;
+  MOE_TRY(make_cfg(cfg, &c));
+  MOE_NEED(cfg->keep_rows == 0);   // every row's a, b are recomputed from the codes
+  MOE_NEED(x && W_r && wg8 && wg_scale && wu8 && wu_scale && wdt8 && wdt_scale && wgut8 && wgut_scale && saved &&
+           dy && dx && dW_r && dW_gate && dW_up && dW_down);
+  MOE_NEED(aligned16(x) && aligned16(W_r) && (!b_r || aligned16(b_r)) && aligned16(wg8) && aligned16(wg_scale) &&
+           aligned16(wu8) && aligned16(wu_scale) && aligned16(wdt8) && aligned16(wdt_scale) && aligned16(wgut8) &&
+           aligned16(wgut_scale) && aligned16(saved) && aligned16(dy) && aligned16(dx) && aligned16(dW_r) &&
+           (!db_r || aligned16(db_r)) && aligned16(dW_gate) && aligned16(dW_up) && aligned16(dW_down));
+  Ws w;
+  MOE_TRY(get_ws(c, ws, ws_bytes, &w));
+  MOE_TRY(check_device());
+  const int32_t* idx = static_cast<const int32_t*>(saved);
+  const float* gates = reinterpret_cast<const float*>(idx + (size_t)c.T * c.k);
+  MOE_TRY(do_dispatch(c, w, idx, x, dy, gates, nullptr, nullptr, nullptr, nullptr, w.at<uint16_t>(w.L.xperm),
+                      w.at<uint16_t>(w.L.dy_perm), stream));
+  float* dgates = w.at<float>(w.L.dgates);
+  MOE_TRY(do_ffn_bwd_fp8(c, w, wg8, wg_scale, wu8, wu_scale, wdt8, wdt_scale, wgut8, wgut_scale, dgates, dW_gate,
+                         dW_up, dW_down, stream));
+  float* dlogits = w.at<float>(w.L.dlogits);
+  MOE_TRY(do_router_bwd(c, w, x, W_r, b_r, idx, gates, dgates, dlogits, dW_r, db_r, stream));
+  return do_combine_bwd(c, w, w.at<uint16_t>(w.L.buf_d1), dlogits, W_r, dx, stream);
 }
 
 moe_status_t moe_check_error(void* ws, moe_stream_t stream) {

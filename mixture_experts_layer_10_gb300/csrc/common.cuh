@@ -73,6 +73,7 @@ struct Layout {
       dlogits, dwr_part, db_part, dgates, xperm, dy_perm, buf_f0, buf_f1, buf_f2, buf_f3, buf_d1,
       dl_bf16, wr_bf16, wr3;
   size_t rt_part, rt_cnt;   // streaming router (E <= 32): partial logits and part counters
+  size_t fp8s;              // FP8 backward: row scales of the x, dY and [dA | dB] rows, [3][rows] fp32
   size_t total;
 };
 
@@ -135,7 +136,7 @@ moe_status_t cuda_status(cudaError_t e);          // MOE_OK or MOE_ERR_CUDA (cle
 enum KernelId : int {
   kKRoute = 0, kKScan, kKGather, kKGateUp, kKDown, kKCombine, kKBwdFused, kKWgrad, kKDgradX,
   kKDgates, kKRouterDlogits, kKRouterDwr, kKRouterReduce, kKCombineBwd, kKBwdDh, kKRouterDx, kKSwigluKept,
-  kKGateUpFp8, kKQuantE4m3, kKDownFp8, kKCount
+  kKGateUpFp8, kKQuantE4m3, kKDownFp8, kKQuantCols, kKBwdDhFp8, kKBwdFusedFp8, kKDgradXFp8, kKCount
 };
 void prof_mark(int id, cudaStream_t s, bool begin);
 
@@ -259,12 +260,34 @@ cudaError_t launch_swiglu_bwd_kept(const Cfg& c, const Layout& L, const FfnBwdAr
 // FP8 (e4m3) rows: codes [rows, cols] and one fp32 scale per row (amax / 448), from bf16 rows.
 cudaError_t launch_quantize_rows_e4m3(const uint16_t* src, int64_t rows, int cols, uint8_t* codes, float* scales,
                                       cudaStream_t s, const Tables* tabs = nullptr);
+// The same for joined rows: row r is src's row r (cols1 values) then src2's row r (cols2 values).
+cudaError_t launch_quantize_rows2_e4m3(const uint16_t* src, int cols1, const uint16_t* src2, int cols2, int64_t rows,
+                                       uint8_t* codes, float* scales, cudaStream_t s, const Tables* tabs = nullptr);
+// FP8 columns: for each of G experts, the source [top (rows_top rows); bottom (rows_bot rows)] x cols
+// bf16 gives codes [cols, rows_top + rows_bot] (transposed) and one scale per column.
+cudaError_t launch_quantize_cols_e4m3(const uint16_t* top, const uint16_t* bottom, int64_t G, int rows_top,
+                                      int rows_bot, int cols, uint8_t* codes, float* scales, cudaStream_t s);
 // H = silu(a) * b with a, b from e4m3 rows of x_perm and of W_gate / W_up and their row scales.
 struct GateUpFp8Args {
   const uint8_t* x8; const float* xs; const uint8_t* wg8; const float* gs; const uint8_t* wu8;
   const float* us; uint16_t* h; Hdr* hdr; const Tables* tabs;
 };
 cudaError_t launch_gate_up_fp8(const Cfg& c, const Layout& L, const GateUpFp8Args& a, cudaStream_t s);
+// The FP8 backward of the expert FFN: e4m3 codes of the x and dY rows (per row), the forward's
+// weight codes (recompute), W_d's columns [G, f, d] (one scale per d_ff channel) and the joined
+// columns of W_gate and W_up [G, d, 2f] (one scale per d_model channel); bf16 dh', dA, dB, Hg,
+// the joined [dA | dB] rows' codes and scales, dx_perm and the weight gradients.
+struct FfnBwd8Args {
+  const uint16_t* x_perm; const uint16_t* dy_perm;
+  const uint8_t* x8; const float* xs; const uint8_t* dy8; const float* dys;
+  const uint8_t* wg8; const float* gs; const uint8_t* wu8; const float* us;
+  const uint8_t* wdt8; const float* wdts; const uint8_t* wgut8; const float* wguts;
+  const float* gate_of_prow;
+  uint16_t* dh; uint16_t* dA; uint16_t* dB; uint16_t* Hg; float* dg_part;
+  uint8_t* dab8; float* dabs; uint16_t* dx_perm;
+  uint16_t* dWg; uint16_t* dWu; uint16_t* dWd; Hdr* hdr; const Tables* tabs;
+};
+cudaError_t launch_ffn_bwd_fp8(const Cfg& c, const Layout& L, const FfnBwd8Args& a, cudaStream_t s);
 // O = H W_d^T from e4m3 rows of H and of W_d (one scale per output channel).
 struct DownFp8Args {
   const uint8_t* h8; const float* hs; const uint8_t* wd8; const float* ds; uint16_t* o; Hdr* hdr;

@@ -369,33 +369,39 @@ struct FwdGateUp8 : PairDefaults {
   __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
 };
 
-// O = H W_d^T from e4m3 rows of H (one scale per row) and of W_d[g] (one scale per output channel
-// of d_model): N = 256 columns of d_model per pair tile, each CTA loading 128 rows of W_d[g]; 128-wide
-// K blocks of d_ff (the last one zero-filled past d_ff).  The epilogue scales the fp32 accumulator
-// by s_h[row] s_d[g, col] and stores bf16.
-struct FwdDown8 : PairDefaults {
-  static constexpr int kId = kKDownFp8;
+// Out = (s_a A8)(s_b B8[g])^T with e4m3 operands, both K-major: A [rows, K] codes with one scale
+// per row, B[g] [N, K] codes with one scale per output channel; N = 256 columns per pair tile, each
+// CTA loading 128 rows of B[g]; 128-wide K blocks (the last one zero-filled past K).  The epilogue
+// scales the fp32 accumulator by s_a[row] s_b[g, col] and stores bf16.  Three problems have this
+// shape (one kernel each, by kId_):
+//   FwdDown8   O   = H8 Wd8^T         A = h rows (K = d_ff),       B = W_down rows (N = d_model)
+//   BwdDh8     dh' = dY8 WdT8^T       A = dY rows (K = d_model),   B = W_down's columns (N = d_ff)
+//   DgradX8    dX  = dAB8 WguT8^T     A = [dA | dB] rows (K = 2 d_ff), B = column i of W_gate and W_up
+//                                     together (N = d_model)
+template <int kId_>
+struct RowChan8 : PairDefaults {
+  static constexpr int kId = kId_;
   // two epilogue warps per TMEM lane quarter, 128 columns each: with K blocks twice as deep as
-  // bf16's, a short d_ff (6 to 11 blocks) leaves the main loop shorter than one warp's 256 columns
+  // bf16's, a short K (6 to 11 blocks) leaves the main loop shorter than one warp's 256 columns
   static constexpr int kEpiWarps = 8;
   static constexpr int kBK8 = 128;
   static constexpr uint32_t kIdesc = idesc_e4m3(kPairM, 256);
   struct Params {
-    CUtensorMap tmH, tmWd, tmO;
-    const float *hs, *ds;   // [rows] and [G, d_model] scales
-    int f, d, nt;
+    CUtensorMap tmA, tmB, tmO;
+    const float *as, *bs;   // [rows] and [G, N] scales
+    int K, N, nt;
     Hdr* hdr;
     const Tables* tabs;
   };
   __device__ static int num_tiles(const Params& p, const SegSmem& s) { return s.n_mtiles * p.nt; }
   __device__ static Job job(const Params& p, const SegSmem& s, int t) {
-    return row_job(s, t, p.nt, 256, (p.f + kBK8 - 1) / kBK8);
+    return row_job(s, t, p.nt, 256, (p.K + kBK8 - 1) / kBK8);
   }
-  __device__ static int mma_kiters(const Params& p, const SegSmem& s, int t) { (void)s; (void)t; return (p.f + kBK8 - 1) / kBK8; }
-  __device__ static void prefetch(const Params& p) { tma_prefetch(&p.tmH); tma_prefetch(&p.tmWd); }
+  __device__ static int mma_kiters(const Params& p, const SegSmem& s, int t) { (void)s; (void)t; return (p.K + kBK8 - 1) / kBK8; }
+  __device__ static void prefetch(const Params& p) { tma_prefetch(&p.tmA); tma_prefetch(&p.tmB); }
   __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint32_t cbar, int rank) {
-    tma_load_2d_pair(st, &p.tmH, cbar, kit * kBK8, j.m0 + kBM * rank);
-    tma_load_3d_pair(st + kTileA, &p.tmWd, cbar, kit * kBK8, j.n0 + kBM * rank, j.seg);
+    tma_load_2d_pair(st, &p.tmA, cbar, kit * kBK8, j.m0 + kBM * rank);
+    tma_load_3d_pair(st + kTileA, &p.tmB, cbar, kit * kBK8, j.n0 + kBM * rank, j.seg);
   }
   __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
 #pragma unroll
@@ -408,12 +414,12 @@ struct FwdDown8 : PairDefaults {
                                   uint8_t* ebuf) {
     const int lane = row & 31;
     const int y = j.m0 + (row & ~31);
-    const float sh = p.hs[j.m0 + row];
-    const float* ds = p.ds + (size_t)j.seg * p.d + j.n0;
+    const float sh = p.as[j.m0 + row];
+    const float* ds = p.bs + (size_t)j.seg * p.N + j.n0;
     epi_begin(lane);
 #pragma unroll 1
     for (int c = part * 128; c < part * 128 + 128; c += 64) {
-      if (j.n0 + c >= p.d) break;   // d is a multiple of 64: a round's two boxes both exist
+      if (j.n0 + c >= p.N) break;   // N is a multiple of 64: a round's two boxes both exist
       uint32_t v[2][32];
       tmem_ld32(ta + c, v[0]);
       tmem_ld32(ta + c + 32, v[1]);
@@ -447,6 +453,9 @@ struct FwdDown8 : PairDefaults {
   }
   __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
 };
+using FwdDown8 = RowChan8<kKDownFp8>;
+using BwdDh8 = RowChan8<kKBwdDhFp8>;
+using DgradX8 = RowChan8<kKDgradXFp8>;
 
 // Shared by FwdDown, BwdDh and DgradX: this warp's 32 rows of the fp32 accumulator [128 x 256] ->
 // bf16 boxes of the output [rows, ncols] at row y (the warp's first row) and columns n0 + c.
@@ -600,6 +609,117 @@ struct BwdFused : PairDefaults {
             dg = fmaf(dhp, hv, dg);
             const float dh = g * dhp;
             o_da[h] = dh * b * sg * (1.f + a * (1.f - sg));
+            o_db[h] = dh * sa;
+            o_h[h] = g * hv;
+          }
+          pa[i] = pack_bf16(o_da[0], o_da[1]);
+          pb[i] = pack_bf16(o_db[0], o_db[1]);
+          ph[i] = pack_bf16(o_h[0], o_h[1]);
+        }
+        if (lane == 0) bulk_wait_read<0>();   // the previous boxes have been read
+        __syncwarp();
+        stage_box(ebuf, lane, pa);
+        stage_box(ebuf + kEpiBox, lane, pb);
+        stage_box(ebuf + 2 * kEpiBox, lane, ph);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_2d(&p.tmDA, ebuf, j.n0 + c, y);
+          tma_store_2d(&p.tmDB, ebuf + kEpiBox, j.n0 + c, y);
+          tma_store_2d(&p.tmHg, ebuf + 2 * kEpiBox, j.n0 + c, y);
+          bulk_commit();
+        }
+      }
+      p.dg_part[r * p.ndg + (j.n0 / 128) * 2 + half] = dg;
+    }
+  }
+  __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
+};
+
+// The FP8 backward's recompute: a | b = s_x s_g (X8 Wg8^T) | s_x s_u (X8 Wu8^T) from the forward's
+// e4m3 codes (FwdGateUp8's main loop), with BwdFused's SwiGLU backward in the epilogue reading this
+// tile's dh' (written by BwdDh8):
+//   h = silu(a) b, dg += dh'.h, dh = g dh', dA = dh b silu'(a), dB = dh silu(a), Hg = g h.
+struct BwdFused8 : PairDefaults {
+  static constexpr int kId = kKBwdFusedFp8;
+  static constexpr int kEpiWarps = 4;
+  static constexpr int kBK8 = 128;
+  static constexpr uint32_t kIdesc = idesc_e4m3(kPairM, 256);
+  static constexpr uint32_t kEpiWarpBytes = 3 * 2048;   // boxes for dA, dB, Hg
+  struct Params {
+    CUtensorMap tmX, tmWg, tmWu, tmDA, tmDB, tmHg;
+    const float *xs, *gs, *us;   // [rows] and [G, f] scales
+    const uint16_t* DH;
+    const float* gate_of_prow;
+    float* dg_part;
+    int f, d, nt, ndg;
+    Hdr* hdr;
+    const Tables* tabs;
+  };
+  __device__ static int num_tiles(const Params& p, const SegSmem& s) { return s.n_mtiles * p.nt; }
+  __device__ static Job job(const Params& p, const SegSmem& s, int t) {
+    return row_job(s, t, p.nt, 128, (p.d + kBK8 - 1) / kBK8);
+  }
+  __device__ static int mma_kiters(const Params& p, const SegSmem& s, int t) { (void)s; (void)t; return (p.d + kBK8 - 1) / kBK8; }
+  __device__ static void prefetch(const Params& p) {
+    tma_prefetch(&p.tmX); tma_prefetch(&p.tmWg); tma_prefetch(&p.tmWu);
+  }
+  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint32_t cbar, int rank) {
+    tma_load_2d_pair(st, &p.tmX, cbar, kit * kBK8, j.m0 + kBM * rank);
+    tma_load_3d_pair(st + kTileA, rank ? &p.tmWu : &p.tmWg, cbar, kit * kBK8, j.n0, j.seg);
+  }
+  __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk)
+      umma_f8_pair(dt, sdesc_kmajor(sa + kk * 32), sdesc_kmajor(sa + kTileA + kk * 32), kIdesc, (kit | kk) != 0);
+  }
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int, int, uint8_t* ebuf) {
+    const int lane = row & 31;
+    const int y = j.m0 + (row & ~31);
+    const size_t r = (size_t)(j.m0 + row);
+    const float g = p.gate_of_prow[r];
+    const float sx = p.xs[r];
+    const float* gsp = p.gs + (size_t)j.seg * p.f + j.n0;
+    const float* usp = p.us + (size_t)j.seg * p.f + j.n0;
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+      float dg = 0.f;
+#pragma unroll 1
+      for (int c = half * 64; c < half * 64 + 64; c += 32) {
+        if (j.n0 + c >= p.f) break;
+        const uint4* dsrc = reinterpret_cast<const uint4*>(p.DH + r * p.f + j.n0 + c);
+        uint4 dv[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) dv[q] = dsrc[q];
+        uint32_t va[32], vb[32];
+        tmem_ld32(ta + c, va);
+        tmem_ld32(ta + 128 + c, vb);
+        float sg[32], su[32];   // the 32 columns' weight scales (the same for every lane)
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          const float4 g4 = __ldg(reinterpret_cast<const float4*>(gsp + c) + v);
+          const float4 u4 = __ldg(reinterpret_cast<const float4*>(usp + c) + v);
+          sg[4 * v] = g4.x; sg[4 * v + 1] = g4.y; sg[4 * v + 2] = g4.z; sg[4 * v + 3] = g4.w;
+          su[4 * v] = u4.x; su[4 * v + 1] = u4.y; su[4 * v + 2] = u4.z; su[4 * v + 3] = u4.w;
+        }
+        tmem_ld_wait();
+        const uint32_t du[16] = {dv[0].x, dv[0].y, dv[0].z, dv[0].w, dv[1].x, dv[1].y, dv[1].z, dv[1].w,
+                                 dv[2].x, dv[2].y, dv[2].z, dv[2].w, dv[3].x, dv[3].y, dv[3].z, dv[3].w};
+        uint32_t pa[16], pb[16], ph[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          float o_da[2], o_db[2], o_h[2];
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float a = __uint_as_float(va[2 * i + h]) * sx * sg[2 * i + h];
+            const float b = __uint_as_float(vb[2 * i + h]) * sx * su[2 * i + h];
+            const float dhp = h ? bf16_hi(du[i]) : bf16_lo(du[i]);
+            const float sgm = sigmoid_fast(a);
+            const float sa = a * sgm;
+            const float hv = sa * b;
+            dg = fmaf(dhp, hv, dg);
+            const float dh = g * dhp;
+            o_da[h] = dh * b * sgm * (1.f + a * (1.f - sgm));
             o_db[h] = dh * sa;
             o_h[h] = g * hv;
           }
@@ -1558,6 +1678,33 @@ cudaError_t launch_gate_up(const Cfg& c, const Layout& L, const FfnFwdArgs& a, i
   return launch_pair<FwdGateUpT<kKeep>>(p1, s);
 }
 
+// Weight gradients (bf16 operands in both the bf16 and the FP8 backward): dWg = dA^T X, dWu = dB^T X,
+// dWd = dY^T Hg per expert.
+cudaError_t launch_wgrad(const Cfg& c, const Layout& L, const uint16_t* dA, const uint16_t* dB, const uint16_t* Hg,
+                         const uint16_t* x_perm, const uint16_t* dy_perm, uint16_t* dWg, uint16_t* dWu,
+                         uint16_t* dWd, Hdr* hdr, const Tables* tabs, cudaStream_t s) {
+  const uint64_t rows = (uint64_t)L.rows;
+  Wgrad::Params p4{};
+  if (!map_mn2(&p4.tmDA, dA, c.f, rows) || !map_mn2(&p4.tmDB, dB, c.f, rows) ||
+      !map_mn2(&p4.tmX, x_perm, c.d, rows) || !map_mn2(&p4.tmDY, dy_perm, c.d, rows) ||
+      !map_mn2(&p4.tmHg, Hg, c.f, rows) || !map_3d(&p4.tmdWg, dWg, c.d, c.f, c.G, 32, 32) ||
+      !map_3d(&p4.tmdWu, dWu, c.d, c.f, c.G, 32, 32) || !map_3d(&p4.tmdWd, dWd, c.f, c.d, c.G, 32, 32))
+    return cudaErrorInvalidValue;
+  p4.dWg = dWg;
+  p4.dWu = dWu;
+  p4.dWd = dWd;
+  p4.f = c.f;
+  p4.d = c.d;
+  p4.mt_f = (c.f + kPairM - 1) / kPairM;
+  p4.nt_d = (c.d + 255) / 256;
+  p4.mt_d = (c.d + kPairM - 1) / kPairM;
+  p4.nt_f = (c.f + 255) / 256;
+  p4.tps = 2 * p4.mt_f * p4.nt_d + p4.mt_d * p4.nt_f;
+  p4.hdr = hdr;
+  p4.tabs = tabs;
+  return launch_pair<Wgrad>(p4, s);
+}
+
 }  // namespace
 
 cudaError_t launch_ffn_fwd(const Cfg& c, const Layout& L, const FfnFwdArgs& a, cudaStream_t s) {
@@ -1614,25 +1761,7 @@ cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, c
   e = launch_pair<BwdFused>(p3, s);
   if (e != cudaSuccess) return e;
 
-  Wgrad::Params p4{};
-  if (!map_mn2(&p4.tmDA, a.dA, c.f, rows) || !map_mn2(&p4.tmDB, a.dB, c.f, rows) ||
-      !map_mn2(&p4.tmX, a.x_perm, c.d, rows) || !map_mn2(&p4.tmDY, a.dy_perm, c.d, rows) ||
-      !map_mn2(&p4.tmHg, a.Hg, c.f, rows) || !map_3d(&p4.tmdWg, a.dWg, c.d, c.f, c.G, 32, 32) ||
-      !map_3d(&p4.tmdWu, a.dWu, c.d, c.f, c.G, 32, 32) || !map_3d(&p4.tmdWd, a.dWd, c.f, c.d, c.G, 32, 32))
-    return cudaErrorInvalidValue;
-  p4.dWg = a.dWg;
-  p4.dWu = a.dWu;
-  p4.dWd = a.dWd;
-  p4.f = c.f;
-  p4.d = c.d;
-  p4.mt_f = (c.f + kPairM - 1) / kPairM;
-  p4.nt_d = (c.d + 255) / 256;
-  p4.mt_d = (c.d + kPairM - 1) / kPairM;
-  p4.nt_f = (c.f + 255) / 256;
-  p4.tps = 2 * p4.mt_f * p4.nt_d + p4.mt_d * p4.nt_f;
-  p4.hdr = a.hdr;
-  p4.tabs = a.tabs;
-  e = launch_pair<Wgrad>(p4, s);
+  e = launch_wgrad(c, L, a.dA, a.dB, a.Hg, a.x_perm, a.dy_perm, a.dWg, a.dWu, a.dWd, a.hdr, a.tabs, s);
   if (e != cudaSuccess) return e;
 
   DgradX::Params p5{};
@@ -1668,17 +1797,75 @@ cudaError_t launch_gate_up_fp8(const Cfg& c, const Layout& L, const GateUpFp8Arg
 cudaError_t launch_down_fp8(const Cfg& c, const Layout& L, const DownFp8Args& a, cudaStream_t s) {
   const uint64_t rows = (uint64_t)L.rows;
   FwdDown8::Params p{};
-  if (!map_u8_2d(&p.tmH, a.h8, c.f, rows) || !map_u8_3d(&p.tmWd, a.wd8, c.f, c.d, c.G) ||
+  if (!map_u8_2d(&p.tmA, a.h8, c.f, rows) || !map_u8_3d(&p.tmB, a.wd8, c.f, c.d, c.G) ||
       !map_2d(&p.tmO, a.o, c.d, rows, 32, 32))
     return cudaErrorInvalidValue;
-  p.hs = a.hs;
-  p.ds = a.ds;
-  p.f = c.f;
-  p.d = c.d;
+  p.as = a.hs;
+  p.bs = a.ds;
+  p.K = c.f;
+  p.N = c.d;
   p.nt = (c.d + 255) / 256;
   p.hdr = a.hdr;
   p.tabs = a.tabs;
   return launch_pair<FwdDown8>(p, s);
+}
+
+// The FP8 backward of the expert FFN (reading in moe.h): dh' = dY8 WdT8^T (e4m3, bf16 out); the
+// recompute of a, b from the forward's codes with the SwiGLU backward (dA, dB, Hg bf16); the bf16
+// weight gradients; the joined [dA | dB] rows quantised per row; dX = dAB8 WguT8^T (e4m3).
+cudaError_t launch_ffn_bwd_fp8(const Cfg& c, const Layout& L, const FfnBwd8Args& a, cudaStream_t s) {
+  const uint64_t rows = (uint64_t)L.rows;
+  BwdDh8::Params p1{};
+  if (!map_u8_2d(&p1.tmA, a.dy8, c.d, rows) || !map_u8_3d(&p1.tmB, a.wdt8, c.d, c.f, c.G) ||
+      !map_2d(&p1.tmO, a.dh, c.f, rows, 32, 32))
+    return cudaErrorInvalidValue;
+  p1.as = a.dys;
+  p1.bs = a.wdts;
+  p1.K = c.d;
+  p1.N = c.f;
+  p1.nt = (c.f + 255) / 256;
+  p1.hdr = a.hdr;
+  p1.tabs = a.tabs;
+  cudaError_t e = launch_pair<BwdDh8>(p1, s);
+  if (e != cudaSuccess) return e;
+
+  BwdFused8::Params p2{};
+  if (!map_u8_2d(&p2.tmX, a.x8, c.d, rows) || !map_u8_3d(&p2.tmWg, a.wg8, c.d, c.f, c.G) ||
+      !map_u8_3d(&p2.tmWu, a.wu8, c.d, c.f, c.G) || !map_2d(&p2.tmDA, a.dA, c.f, rows, 32, 32) ||
+      !map_2d(&p2.tmDB, a.dB, c.f, rows, 32, 32) || !map_2d(&p2.tmHg, a.Hg, c.f, rows, 32, 32))
+    return cudaErrorInvalidValue;
+  p2.xs = a.xs;
+  p2.gs = a.gs;
+  p2.us = a.us;
+  p2.DH = a.dh;
+  p2.gate_of_prow = a.gate_of_prow;
+  p2.dg_part = a.dg_part;
+  p2.f = c.f;
+  p2.d = c.d;
+  p2.nt = L.ntf;
+  p2.ndg = L.ndg;
+  p2.hdr = a.hdr;
+  p2.tabs = a.tabs;
+  e = launch_pair<BwdFused8>(p2, s);
+  if (e != cudaSuccess) return e;
+
+  e = launch_wgrad(c, L, a.dA, a.dB, a.Hg, a.x_perm, a.dy_perm, a.dWg, a.dWu, a.dWd, a.hdr, a.tabs, s);
+  if (e != cudaSuccess) return e;
+  e = launch_quantize_rows2_e4m3(a.dA, c.f, a.dB, c.f, (int64_t)rows, a.dab8, a.dabs, s, a.tabs);
+  if (e != cudaSuccess) return e;
+
+  DgradX8::Params p3{};
+  if (!map_u8_2d(&p3.tmA, a.dab8, 2 * c.f, rows) || !map_u8_3d(&p3.tmB, a.wgut8, 2 * c.f, c.d, c.G) ||
+      !map_2d(&p3.tmO, a.dx_perm, c.d, rows, 32, 32))
+    return cudaErrorInvalidValue;
+  p3.as = a.dabs;
+  p3.bs = a.wguts;
+  p3.K = 2 * c.f;
+  p3.N = c.d;
+  p3.nt = (c.d + 255) / 256;
+  p3.hdr = a.hdr;
+  p3.tabs = a.tabs;
+  return launch_pair<DgradX8>(p3, s);
 }
 
 cudaError_t launch_router_dwr(const Cfg& c, const Layout& L, const uint16_t* x, const uint16_t* dl_bf16,

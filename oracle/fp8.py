@@ -176,7 +176,7 @@ def token_outputs_fp8(L, tokens: np.ndarray, cols: np.ndarray) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------------------------
-# e4m3 backward (oracle only: the kernels of this step are not built yet)
+# e4m3 backward (moe_layer_bwd_fp8 computes it)
 #
 # Reading, continuing the forward's: the two data-gradient products take e4m3 operands,
 #   dh' = dY W_d        left: dY rows, per row;  right: the rows of W_d^T (W_d's columns, one
@@ -275,6 +275,85 @@ def layer_backward_fp8(L) -> dict:
     dW_r, db_r, dx_r = router_backward(L.x, L.inp["W_r"], dl)
     return dict(dx=dx + dx_r, dW_r=dW_r, db_r=db_r, dW_gate=dW_gate, dW_up=dW_up, dW_down=dW_down,
                 dgates=dgates, dlogits=dl)
+
+
+def token_grads_fp8(L, tokens: np.ndarray) -> dict:
+    """dx[tokens] and dgates[tokens] of the e4m3 backward, token by token (for full-size workloads).
+
+    A token's rows go through expert_backward_fp8 on their own: the quantisation of an x, dY or
+    [dA | dB] row depends on that row alone, and each expert's weights are quantised whole (their
+    column scales span the expert).  The router term follows from the token's own routing and gate
+    gradients.  Routing as Layer.token_outputs (a capacity needs the queues over all tokens)."""
+    from .moe_oracle import gates_of, router_logits, softmax, topk_by_rank
+    tokens = np.asarray(tokens, np.int64)
+    k = L.k
+    if L.C is not None:
+        R = L.routing()
+        p, idx, g = R.p[tokens], R.idx[tokens], R.gates[tokens]
+        kept = L.dispatch().row_of_slot[tokens] >= 0
+    else:
+        lg = router_logits(L.x[tokens], L.inp["W_r"], L.inp.get("b_r"))
+        p = softmax(lg)
+        idx = topk_by_rank(lg, k)
+        g = gates_of(p, idx, L.renorm)
+        kept = np.ones(idx.shape, dtype=bool)
+    n = tokens.size
+    xs, dys = L.x[tokens], L.dy[tokens]
+    dx = np.zeros((n, L.d))
+    dgates = np.zeros((n, k))
+    for e in range(L.E + L.S):
+        if e < L.E:
+            sel = np.argwhere((idx == e) & kept)
+            if sel.size == 0:
+                continue
+            ti, jj = sel[:, 0], sel[:, 1]
+            gw = g[ti, jj]
+        else:
+            ti, jj, gw = np.arange(n), None, np.ones(n)
+        Wg, Wu, Wd = L.W(e)
+        dxr, _, _, _, dg = expert_backward_fp8(xs[ti], dys[ti], gw, Wg, Wu, Wd)
+        np.add.at(dx, ti, dxr)
+        if jj is not None:
+            dgates[ti, jj] = dg
+    dl = router_backward_logits(p, idx, g, dgates, L.renorm)
+    dx += dl @ np.asarray(L.inp["W_r"], np.float64).T
+    return dict(dx=dx, dgates=dgates)
+
+
+def weight_grad_columns_fp8(L, e: int, cols: np.ndarray) -> dict:
+    """dW_gate[e][cols, :], dW_up[e][cols, :] and dW_down[e][:, cols] of the e4m3 backward.
+
+    Hidden unit c needs only column c of a, b and dh' over the expert's rows: a and b from row c of
+    W_gate and W_up (each quantised with its own scale), dh' from column c of W_down (its own
+    scale), the x and dY rows quantised per row -- expert_backward_fp8's steps, for these units."""
+    cols = np.asarray(cols, np.int64)
+    k = L.k
+    if e < L.E:
+        D, R = L.dispatch(), L.routing()
+        rows = np.arange(D.offsets[e], D.offsets[e + 1])
+        slots = D.slot_of_row[rows]
+        t_of, j_of = slots // k, slots % k
+        gw = R.gates[t_of, j_of]
+    else:
+        t_of = np.arange(L.T)
+        gw = np.ones(L.T)
+    f32 = lambda v: np.asarray(v, np.float32)
+    Wg, Wu, Wd = L.W(e)
+    xr, dyr = L.x[t_of], L.dy[t_of]
+    xq, xs = quantize_rows_e4m3(f32(xr))
+    gq, gs = quantize_rows_e4m3(f32(Wg[cols]))
+    uq, us = quantize_rows_e4m3(f32(Wu[cols]))
+    a, b = gate_up_pre_fp8(xq, xs, gq, gs, uq, us)
+    dyq, dys = quantize_rows_e4m3(f32(dyr))
+    wdtq, wdts = quantize_cols_e4m3(f32(Wd[:, cols]))
+    dhp = _bf16(dh_fp8(dyq, dys, wdtq, wdts))
+    s = 1.0 / (1.0 + np.exp(-a))
+    h = a * s * b
+    dh = gw[:, None] * dhp
+    dA = _bf16(dh * b * s * (1.0 + a * (1.0 - s)))
+    dB = _bf16(dh * (a * s))
+    Hg = _bf16(gw[:, None] * h)
+    return dict(dW_gate=dA.T @ xr, dW_up=dB.T @ xr, dW_down=dyr.T @ Hg)
 
 
 # ---------------------------------------------------------------------------------------------

@@ -99,6 +99,26 @@ def test_fp8_arguments_rejected(lib):
                                  0x70000, 0x80000, 0x90000, 0xA0000, 0x100000, wsk, None) == 1
 
 
+def test_fp8_backward_arguments_rejected(lib):
+    # the column quantiser: rows (top + bottom) a multiple of 16, a bottom exactly when it has rows
+    assert lib.moe_quantize_cols_e4m3(0x10000, None, 2, 40, 0, 64, 0x20000, 0x30000, None) == 1
+    assert lib.moe_quantize_cols_e4m3(0x10000, None, 2, 64, 64, 64, 0x20000, 0x30000, None) == 1
+    assert lib.moe_quantize_cols_e4m3(0x10000, 0x18000, 2, 64, 0, 64, 0x20000, 0x30000, None) == 1
+    assert lib.moe_quantize_cols_e4m3(0x10000, None, 2, 16384, 16400, 64, 0x20000, 0x30000, None) == 1
+    assert lib.moe_quantize_cols_e4m3(0x10008, None, 2, 64, 0, 64, 0x20000, 0x30000, None) == 1
+    c = moe.config(T=64, d=128, f=256, E=8, k=2)
+    ws, _ = moe.moe_workspace_size(c)
+    p = [0x10000 * (i + 1) for i in range(19)]
+    # a null scale
+    q = list(p)
+    q[4] = None
+    assert lib.moe_layer_bwd_fp8(ctypes.byref(c), *q, 0x1000000, ws, None) == 1
+    # every row's a, b come from the codes: no kept activations
+    ck = moe.config(T=64, d=128, f=256, E=8, k=2, keep_rows=256)
+    wsk, _ = moe.moe_workspace_size(ck)
+    assert lib.moe_layer_bwd_fp8(ctypes.byref(ck), *p, 0x1000000, wsk, None) == 1
+
+
 def test_a_library_that_does_not_load_raises(tmp_path, monkeypatch):
     # no fallback: a broken library file is an error, never a silent CPU path
     bad = tmp_path / "libmoe.so"

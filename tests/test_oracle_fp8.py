@@ -159,7 +159,7 @@ def test_token_outputs_fp8_equal_the_layer_forward():
         np.testing.assert_allclose(fp8.token_outputs_fp8(L, toks, cols), y[toks][:, cols], rtol=1e-12, atol=1e-300)
 
 
-# ---- the e4m3 backward (oracle only)
+# ---- the e4m3 backward
 
 def test_column_quantisation_scales_are_column_maxima():
     rng = np.random.default_rng(11)
@@ -223,6 +223,25 @@ def test_backward_weight_scales_are_per_channel():
     got = fp8.expert_backward_fp8(x.astype(np.float32), dy.astype(np.float32), g, Wg2, Wu2, Wd)
     err = np.linalg.norm(got[0] - ref[0], axis=0) / np.linalg.norm(ref[0], axis=0)   # dx columns
     assert err.max() < 0.2, ("dx", err.max())
+
+
+def test_sampled_backward_forms_equal_the_layer_backward():
+    # token by token (dx, dgates) and hidden unit by unit (weight-gradient rows and columns)
+    # against the whole-layer e4m3 backward: capacity drops, shared experts, renormalised gates
+    import cases
+    for name in ("tiny", "gptoss_small", "deepseek_small"):
+        c, inp, L = cases.case(name)
+        full = fp8.layer_backward_fp8(L)
+        toks = np.array([0, 3, 17, c["T"] - 1])
+        s = fp8.token_grads_fp8(L, toks)
+        np.testing.assert_allclose(s["dx"], full["dx"][toks], rtol=1e-11, atol=1e-12)
+        np.testing.assert_allclose(s["dgates"], full["dgates"][toks], rtol=1e-11, atol=1e-13)
+        cols = np.array([0, 5, c["f"] - 1])
+        for e in (0, 3, c["E"] + c["S"] - 1):
+            w = fp8.weight_grad_columns_fp8(L, e, cols)
+            np.testing.assert_allclose(w["dW_gate"], full["dW_gate"][e][cols], rtol=1e-11, atol=1e-12)
+            np.testing.assert_allclose(w["dW_up"], full["dW_up"][e][cols], rtol=1e-11, atol=1e-12)
+            np.testing.assert_allclose(w["dW_down"], full["dW_down"][e][:, cols], rtol=1e-11, atol=1e-12)
 
 
 # ---- MXFP8 (oracle only)
