@@ -144,12 +144,14 @@ moe_status_t moe_perm_rows(const moe_config_t* cfg, int64_t* rows);
 /* Zero the workspace header (error word and device counters).  Call once after allocating. */
 moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* Router: logits, softmax, top-k and gates for every token.  b_r and logits may be NULL.
- * Writes idx [T,k], gates [T,k], and logits [T,E] when non-NULL.  ws is this configuration's
- * workspace (moe_workspace_size).  For E <= 128 and k <= 8 the logits run on the tensor
- * cores: W_r is split in ws into three bf16 parts whose sum equals it within fp32 rounding, and the
- * products are summed in fp32 over 256-wide slices of d_model; other shapes use an fp32 tile
- * product with warp-per-token selection. */
+/* Router (Piper explainer, "the problem": a router sends each token to a few experts; MoEBlaze
+ * summary, Limitations: a static top-k routing policy): logits, softmax, top-k and gates for every
+ * token, by the readings above.  b_r and logits may be NULL.  Writes idx [T,k], gates [T,k], and
+ * logits [T,E] when non-NULL.  ws is this configuration's workspace (moe_workspace_size).  For
+ * E <= 128 and k <= 8 the logits run on the tensor cores: W_r is split in ws into three bf16 parts
+ * whose sum equals it within fp32 rounding, and the products are summed in fp32 over 256-wide
+ * slices of d_model (E <= 32: the parts stacked in one MMA and d_model split across CTAs, so that
+ * the whole GPU streams x); other shapes use an fp32 tile product with warp-per-token selection. */
 moe_status_t moe_route(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
                        int32_t* idx, float* gates, float* logits, void* ws, size_t ws_bytes,
                        moe_stream_t stream);
@@ -205,8 +207,11 @@ moe_status_t moe_expert_ffn_fwd(const moe_config_t* cfg, const moe_bf16* x_perm,
                                 const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down,
                                 moe_bf16* o_perm, void* ws, size_t ws_bytes, moe_stream_t stream);
 
-/* Weighted combine back to token order, by token owner (no atomics, fixed slot order, fp32 sums,
- * one rounding): y[t] = sum_kept gates[t,j] o_perm[row(t,j)] + sum_s o_perm[P_{E+s}+t]. */
+/* Weighted combine back to token order (MoEBlaze summary, Methodology item 2: the reverse
+ * dispatch after the expert FFN; DisagMoE technical summary, section 2.2: combine), by token owner
+ * (no atomics, fixed slot order, fp32 sums, one rounding):
+ * y[t] = sum_kept gates[t,j] o_perm[row(t,j)] + sum_s o_perm[P_{E+s}+t].  Reads the row tables
+ * moe_dispatch left in ws. */
 moe_status_t moe_combine(const moe_config_t* cfg, const moe_bf16* o_perm, const float* gates,
                          moe_bf16* y, void* ws, size_t ws_bytes, moe_stream_t stream);
 
@@ -340,10 +345,16 @@ moe_status_t moe_layer_bwd(const moe_config_t* cfg, const moe_bf16* x, const flo
  * (MOE_OK if none) and clear it.  Returns MOE_ERR_CUDA if the stream itself reports an error. */
 moe_status_t moe_check_error(void* ws, moe_stream_t stream);
 
-/* Test hook: make dispatch scan block `stall_block` never publish its counts (-1: off) and bound
+/* Test hook: make dispatch scan block `stall_block` never publish its counts (-1: off), make the
+ * first CTA pair of every expert GEMM skip its fill number `stall_fill` of the operand ring -- no
+ * loads, no expected bytes, so the MMA's wait for that stage never completes (-1: off) -- and bound
  * every device wait of later calls by `timeout_ns` (0: the default, 2 s).  Used to check that a
- * wait that runs out returns MOE_ERR_TIMEOUT through moe_check_error instead of hanging. */
-moe_status_t moe_debug_inject(void* ws, int32_t stall_block, uint64_t timeout_ns, moe_stream_t stream);
+ * wait that runs out returns MOE_ERR_TIMEOUT through moe_check_error instead of hanging: the kernel
+ * that gives up still waits, with the same bound, for the copies and MMAs it has in flight before
+ * it frees its shared memory and TMEM, so the next call runs normally.  Outputs of the stalled call
+ * are invalid. */
+moe_status_t moe_debug_inject(void* ws, int32_t stall_block, int32_t stall_fill, uint64_t timeout_ns,
+                              moe_stream_t stream);
 
 /* Kernel timing.  While enabled, every kernel launch of the library is bracketed by two CUDA
  * events recorded on its launching stream.  moe_profile_enable(on) also clears the totals.

@@ -86,7 +86,7 @@ def load(path: str | None = None):
         "moe_layer_bwd": [cfgp, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P,
                           ctypes.c_size_t, _P],
         "moe_check_error": [_P, _P],
-        "moe_debug_inject": [_P, ctypes.c_int32, ctypes.c_uint64, _P],
+        "moe_debug_inject": [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_uint64, _P],
         "moe_profile_enable": [ctypes.c_int32],
         "moe_profile_read": [ctypes.c_int32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),
                              ctypes.POINTER(ctypes.c_int32)],
@@ -280,8 +280,8 @@ def moe_check_error(ws, stream=None) -> int:
     return load().moe_check_error(_ptr(ws), _stream(stream))
 
 
-def moe_debug_inject(ws, stall_block: int, timeout_ns: int, stream=None):
-    _call("moe_debug_inject", _ptr(ws), int(stall_block), int(timeout_ns), _stream(stream))
+def moe_debug_inject(ws, stall_block: int, timeout_ns: int, stream=None, stall_fill: int = -1):
+    _call("moe_debug_inject", _ptr(ws), int(stall_block), int(stall_fill), int(timeout_ns), _stream(stream))
 
 
 def moe_profile_enable(on: bool):

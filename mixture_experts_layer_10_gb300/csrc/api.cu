@@ -872,11 +872,14 @@ moe_status_t moe_profile_read(int32_t kernel, const char** name, double* total_m
   return MOE_OK;
 }
 
-moe_status_t moe_debug_inject(void* ws, int32_t stall_block, uint64_t timeout_ns, moe_stream_t stream) {
+moe_status_t moe_debug_inject(void* ws, int32_t stall_block, int32_t stall_fill, uint64_t timeout_ns,
+                              moe_stream_t stream) {
   if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MOE_ERR_INVALID_ARG;
   Hdr* h = static_cast<Hdr*>(ws);
   const int32_t stall_p1 = stall_block < 0 ? 0 : stall_block + 1;
+  const int32_t fill_p1 = stall_fill < 0 ? 0 : stall_fill + 1;
   MOE_CUDA(cudaMemcpyAsync(&h->stall_block_p1, &stall_p1, sizeof(stall_p1), cudaMemcpyHostToDevice, stream));
+  MOE_CUDA(cudaMemcpyAsync(&h->stall_fill_p1, &fill_p1, sizeof(fill_p1), cudaMemcpyHostToDevice, stream));
   MOE_CUDA(cudaMemcpyAsync(&h->timeout_ns, &timeout_ns, sizeof(timeout_ns), cudaMemcpyHostToDevice, stream));
   MOE_CUDA(cudaStreamSynchronize(stream));
   return MOE_OK;

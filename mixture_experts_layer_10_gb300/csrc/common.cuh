@@ -36,7 +36,7 @@ struct Hdr {
   int32_t status;
   int32_t site;
   int32_t stall_block_p1;   // test hook: scan block (value - 1) never publishes (0 off)
-  int32_t reserved0;
+  int32_t stall_fill_p1;    // test hook: the expert GEMMs' first CTA pair skips fill (value - 1) (0 off)
   uint64_t timeout_ns;      // 0 = kDefaultTimeoutNs
   uint32_t scan_ticket;     // dynamic block index of the dispatch scan
   uint32_t scan_done;       // scan blocks finished; the last one builds the tables

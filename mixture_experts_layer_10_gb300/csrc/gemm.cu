@@ -1265,6 +1265,7 @@ constexpr size_t epi_bytes() {
 
 template <class P>
 constexpr size_t smem_bytes() {
+  static_assert(8 * (2 * P::kStages + 5) + 8 <= 256, "barriers fit their 256 bytes");
   return 1024 + (size_t)P::kStages * P::kStageBytes + epi_bytes<P>() + 256 + sizeof(SegSmem);
 }
 
@@ -1283,7 +1284,8 @@ __global__ void __launch_bounds__(threads_of<P>(), 1) gemm_kernel(const __grid_c
   uint64_t* empty = full + P::kStages;
   uint64_t* tfull = empty + P::kStages;
   uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* drain = tempty + 2;   // the MMA thread's last commit, waited for before TMEM is freed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   SegSmem& segs = *reinterpret_cast<SegSmem*>(epi + epi_bytes<P>() + 256);
 
@@ -1298,6 +1300,7 @@ __global__ void __launch_bounds__(threads_of<P>(), 1) gemm_kernel(const __grid_c
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], P::kEpiWarps);
     }
+    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
     P::prefetch(p);
@@ -1317,6 +1320,7 @@ __global__ void __launch_bounds__(threads_of<P>(), 1) gemm_kernel(const __grid_c
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
+      int uses = 0;
       for (int t = blockIdx.x; t < ntiles && !*abort_flag; t += gridDim.x) {
         const Job j = P::job(p, segs, t);
         for (int kit = 0; kit < j.kiters; ++kit) {
@@ -1327,12 +1331,15 @@ __global__ void __launch_bounds__(threads_of<P>(), 1) gemm_kernel(const __grid_c
           }
           mbar_arrive_expect_tx(&full[stage], P::tx_bytes(j, kit, P::kStageBytes));
           P::load(p, j, kit, stages + (size_t)stage * P::kStageBytes, &full[stage]);
+          ++uses;
           if (++stage == P::kStages) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
+      // every load this CTA issued lands before its shared memory is released (bounded)
+      drain_fills(full, P::kStages, stage, phase, uses, limit);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -1379,6 +1386,9 @@ __global__ void __launch_bounds__(threads_of<P>(), 1) gemm_kernel(const __grid_c
           acc_phase ^= 1;
         }
       }
+      // every MMA this thread issued has completed before TMEM is freed (bounded)
+      umma_commit(drain);
+      mbar_wait_drain(drain, 0, limit);
     }
   } else {
     const int q = warp & 3;            // TMEM lane quarter this warp may access
@@ -1451,7 +1461,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<P>(), 1)
   uint64_t* empty = full + P::kStages;
   uint64_t* tfull = empty + P::kStages;
   uint64_t* tempty = tfull + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  uint64_t* drain = tempty + 2;   // the MMA thread's last commit, waited for before TMEM is freed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   SegSmem& segs = *reinterpret_cast<SegSmem*>(epi + epi_bytes<P>() + 256);
 
@@ -1472,6 +1483,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<P>(), 1)
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], 2 * P::kEpiWarps);
     }
+    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
     P::prefetch(p);
@@ -1493,6 +1505,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<P>(), 1)
       int slot = 0;
       uint32_t phase = 0;
       int uses = 0;   // slots filled so far; from kSlots on, every fill follows a completed use
+      // test hook: the first pair skips one fill (no loads, no expected bytes), so that the MMA
+      // thread's wait for it runs out
+      const int skip = pair == 0 ? *((volatile const int32_t*)&p.hdr->stall_fill_p1) - 1 : -1;
       for (int t = pair; t < ntiles && !*abort_flag; t += npairs) {
         const Job j = P::job(p, segs, t);
         for (int k0 = 0; k0 < j.kiters; k0 += kSub) {
@@ -1502,14 +1517,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<P>(), 1)
             break;
           }
           const int nsb = min(kSub, j.kiters - k0);
-          if (rank == 0) {
-            uint32_t tx = 0;
-            for (int sb = 0; sb < nsb; ++sb) tx += P::tx_bytes(j, k0 + sb, P::kStageBytes);
-            mbar_arrive_expect_tx(&full[slot], 2 * tx);
+          if (uses != skip) {
+            if (rank == 0) {
+              uint32_t tx = 0;
+              for (int sb = 0; sb < nsb; ++sb) tx += P::tx_bytes(j, k0 + sb, P::kStageBytes);
+              mbar_arrive_expect_tx(&full[slot], 2 * tx);
+            }
+            uint8_t* st = stages + (size_t)slot * kSlotBytes;
+            for (int sb = 0; sb < nsb; ++sb)
+              P::load(p, j, k0 + sb, st + (size_t)sb * P::kStageBytes, cluster_addr(&full[slot], 0), rank);
           }
-          uint8_t* st = stages + (size_t)slot * kSlotBytes;
-          for (int sb = 0; sb < nsb; ++sb)
-            P::load(p, j, k0 + sb, st + (size_t)sb * P::kStageBytes, cluster_addr(&full[slot], 0), rank);
           if (rank == 0 && uses >= kSlots) mbar_arrive_cluster_relaxed(cluster_addr(&empty[slot], 1));
           ++uses;
           if (++slot == kSlots) {
@@ -1518,6 +1535,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<P>(), 1)
           }
         }
       }
+      // every load of the pair lands before either CTA's shared memory is released: the even CTA's
+      // full barriers count both CTAs' bytes, and the odd CTA waits at the final cluster barrier
+      // (bounded; a skipped fill never completes and ends this wait at its limit)
+      if (rank == 0) drain_fills(full, kSlots, slot, phase, uses, limit);
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
@@ -1567,6 +1588,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<P>(), 1)
           acc_phase ^= 1;
         }
       }
+      // every pair MMA issued has completed before either CTA frees its TMEM (bounded)
+      umma_commit_pair(cluster_addr(drain, 0));
+      mbar_wait_drain(drain, 0, limit);
     }
   } else {
     const int q = warp & 3;            // TMEM lane quarter this warp may access

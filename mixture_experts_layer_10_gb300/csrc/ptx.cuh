@@ -86,6 +86,33 @@ __device__ __forceinline__ bool mbar_wait_idle(uint64_t* bar, uint32_t parity, u
   }
 }
 
+// Bounded wait that ignores the abort flag: the drain before a CTA exits, when its own copies and
+// MMAs in flight must land before the shared memory and TMEM they write are released.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  uint64_t t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > limit_ns) return false;
+  }
+}
+
+// A producer's drain: the last fill of every stage of its ring has landed.  Fills go through the
+// stages in order, so after `uses` fills with the cursor at (slot, phase) -- the next fill's stage
+// and phase -- stage s < slot was last filled in phase `phase` and stage s >= slot in phase ^ 1
+// (if it was filled at all).  Waiting on the last fill's phase is enough: nothing fills it after.
+__device__ __forceinline__ bool drain_fills(uint64_t* full, int nslots, int slot, uint32_t phase, int uses,
+                                            uint64_t limit_ns) {
+  bool ok = true;
+  for (int s = 0; s < nslots && s < uses; ++s) ok = mbar_wait_drain(&full[s], s < slot ? phase : phase ^ 1u, limit_ns) && ok;
+  return ok;
+}
+
 // ---------------------------------------------------------------------------------------------
 // TMA
 // ---------------------------------------------------------------------------------------------

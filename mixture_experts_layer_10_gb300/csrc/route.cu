@@ -1,10 +1,15 @@
 // Router: logits = x W_r (+ b), softmax over the E routed experts, top-k by logit (ties to the
 // lower expert index), gates; and its backward with the selection held fixed.
 //
-// The logits are an fp32 SIMT tile product (x is bf16, W_r fp32, E <= 256 columns); selection,
-// softmax and the gate gradient run warp-per-token with shuffle reductions.  Sources: the Piper
-// explainer ("the problem": a router sends each token to a few experts) and the MoEBlaze summary
-// (Limitations: static top-k routing); the formulas are the plain softmax-then-top-k reading.
+// This file holds the SIMT router, used where the tensor-core routers do not apply (more than 128
+// experts, or more than 8 per token): the logits are an fp32 tile product (x is bf16, W_r fp32,
+// E <= 256 columns); selection, softmax and the gate gradient run warp-per-token with shuffle
+// reductions.  Up to 32 experts (k <= 8) route_tc.cu streams x on the tensor cores with K split
+// across CTAs, and up to 128 experts gemm.cu's RouterLogits gives each 128-token tile a CTA; the
+// W_r split kernels of both, the router-backward reductions and the bf16 row conversion are here
+// too.  Sources: the Piper explainer ("the problem": a router sends each token to a few experts)
+// and the MoEBlaze summary (Limitations: static top-k routing); the formulas are the plain
+// softmax-then-top-k reading.
 #include <algorithm>
 #include <cfloat>
 

@@ -71,7 +71,7 @@ struct Shape {
   static constexpr int kSegBatch = EB <= 8 ? 4 : (EB <= 16 ? 2 : 1);   // segments loaded at once
   static constexpr size_t kSmem = 1024 + (size_t)kStages * kStageBytes + 256;
   static_assert(kStageBytes % 1024 == 0, "stages stay 1024-aligned");
-  static_assert(8 * (2 * kStages + 2 * kAccBufs) + 8 <= 256, "barriers fit their 256 bytes");
+  static_assert(8 * (2 * kStages + 2 * kAccBufs + 1) + 8 <= 256, "barriers fit their 256 bytes");
   static_assert(kSmem <= 232448, "shared memory per block");
 };
 
@@ -207,7 +207,8 @@ __global__ void __launch_bounds__(kThreads, 1) route_stream_kernel(const __grid_
   uint64_t* empty = full + S::kStages;
   uint64_t* tfull = empty + S::kStages;
   uint64_t* tempty = tfull + S::kAccBufs;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + S::kAccBufs);
+  uint64_t* drain = tempty + S::kAccBufs;   // the MMA thread's last commit, waited for before TMEM is freed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -220,6 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1) route_stream_kernel(const __grid_
       mbar_init(&tfull[a], 1);
       mbar_init(&tempty[a], 4);
     }
+    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch(&p.tmX);
@@ -242,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 1) route_stream_kernel(const __grid_
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
+      int uses = 0;
       for (long long sp = sl0; sp < sl1 && !*abort_flag; ++sp) {
         const int tile = (int)(sp / p.nslice), sl = (int)(sp - (long long)tile * p.nslice);
         const int kb1 = min(p.nkb, (sl + 1) * kSliceKB);
@@ -255,12 +258,15 @@ __global__ void __launch_bounds__(kThreads, 1) route_stream_kernel(const __grid_
           mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
           tma_load_2d(st, &p.tmX, &full[stage], kb * kKB, tile * kTok);
           tma_load_2d(st + kXBytes, &p.tmW, &full[stage], kb * kKB, 0);
+          ++uses;
           if (++stage == S::kStages) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
+      // every load this CTA issued lands before its shared memory is released (bounded)
+      drain_fills(full, S::kStages, stage, phase, uses, limit);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -307,6 +313,9 @@ __global__ void __launch_bounds__(kThreads, 1) route_stream_kernel(const __grid_
         record_error(p.hdr, MOE_ERR_TIMEOUT, kSiteGemmMma);
         *abort_flag = 1;
       }
+      // every MMA this thread issued has completed before TMEM is freed (bounded)
+      umma_commit(drain);
+      mbar_wait_drain(drain, 0, limit);
     }
   } else {
     const int q = warp & 3;              // TMEM lane quarter of this warp

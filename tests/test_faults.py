@@ -5,6 +5,8 @@
 * A bounded wait that runs out: the test hook makes one dispatch-scan block never publish its
   counts, the look-back of the blocks after it gives up after a short limit, the call reports
   MOE_ERR_TIMEOUT and downstream kernels see empty tables; the next clean call succeeds.
+* The same in an expert GEMM: one operand stage never arrives, the MMA's wait gives up, the kernel
+  drains what it has in flight, and the next call matches a call made before the stall.
 """
 import numpy as np
 import pytest
@@ -72,6 +74,36 @@ def test_stalled_scan_block_times_out(moe):
     assert np.array_equal(from_dev(o["counts"]), D.counts)
     assert np.array_equal(from_dev(o["offsets"]), D.offsets)
     assert np.array_equal(from_dev(o["row_of_slot"]).reshape(T, k), D.row_of_slot)
+
+
+def test_stalled_gemm_times_out_and_drains(moe):
+    """An expert GEMM whose operand stage never arrives (the test hook makes the first CTA pair
+    skip one fill): the MMA thread's bounded wait runs out and the call reports MOE_ERR_TIMEOUT.
+    The kernel waits for the loads and MMAs it has in flight before it frees shared memory and
+    TMEM, so the next call runs normally and gives bit for bit what a call before the stall gave."""
+    from cases import case
+    c, inp, L = case("ragged_mixtral")
+    T, d, k, E = c["T"], c["d"], c["k"], c["E"]
+    mc = moe.config_from(c)
+    buf = moe.Buffers.allocate(mc)
+    scratch = [torch.empty(n, dtype=torch.int32, device="cuda") for n in (E, E + 1, T * k, T * k)]
+    x_perm = torch.empty(buf.rows, d, dtype=torch.bfloat16, device="cuda")
+    moe.moe_dispatch(mc, to_dev(L.routing().idx.astype(np.int32)), to_dev_bf16(inp["x"]), *scratch, x_perm, buf.ws)
+    Wg, Wu, Wd = (to_dev_bf16(inp[n]) for n in ("W_gate", "W_up", "W_down"))
+
+    def ffn():
+        o = torch.zeros(buf.rows, d, dtype=torch.bfloat16, device="cuda")
+        moe.moe_expert_ffn_fwd(mc, x_perm, Wg, Wu, Wd, o, buf.ws)
+        return o
+    ref = ffn()
+    assert moe.moe_check_error(buf.ws) == 0
+    moe.moe_debug_inject(buf.ws, -1, 20_000_000, stall_fill=2)       # 20 ms bound
+    ffn()
+    assert moe.moe_check_error(buf.ws) == TIMEOUT
+    moe.moe_debug_inject(buf.ws, -1, 0)
+    again = ffn()
+    assert moe.moe_check_error(buf.ws) == 0
+    assert torch.equal(again.view(torch.int16), ref.view(torch.int16))
 
 
 def test_invalid_arguments_enqueue_nothing(moe):
