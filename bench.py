@@ -14,7 +14,8 @@ Prints one JSON line (rank 0):
              measured peak (MEASURED_PEAKS.json)
   cpu_baseline  the fp64 oracle on a bounded token sample, on this host's cores (rank 0, N = 1)
   workloads  (default Mixtral-like run) a compact record of each other workload -- tiny, DeepSeek-,
-             Qwen3- and GPT-OSS-like -- measured the same way over --workload-steps steps
+             Qwen3- and GPT-OSS-like -- measured the same way over --workload-steps steps, and of
+             the Mixtral-, DeepSeek- and Qwen3-like layers with gather_in_gemm = 1 ("+gather_in_gemm")
 
 --impl reference times the oracle alone (on the host cores) on the same workload and metric.
 """
@@ -84,6 +85,9 @@ def parse():
                     help="measure the chosen workload only (by default the Mixtral-like line also carries a "
                          "compact record of every other workload)")
     ap.add_argument("--workload-steps", type=int, default=10, help="timed steps of each extra workload")
+    ap.add_argument("--gather-in-gemm", action="store_true",
+                    help="the expert GEMMs gather x and dy rows from token order (gather_in_gemm = 1) instead of "
+                         "reading x_perm / dY_perm written by the dispatch gather")
     return ap.parse_args()
 
 
@@ -576,7 +580,9 @@ def run_workload(args, name, cfg, steps, warmup, rank, world, local, barrier, ex
             gemm_flops += work
             gemm_ms += tot
         elif kname in HBM_KERNELS or kname in ROUTER_KERNELS:
-            if kname == "dispatch_gather":   # fwd: x once + N rows; bwd: x and dy once + 2N rows
+            if kname == "dispatch_gather" and cfg.get("gather_in_gemm"):   # tables, row tokens, row gates
+                work = steps * (3 * 12 * T * k + 12 * N)
+            elif kname == "dispatch_gather":   # fwd: x once + N rows; bwd: x and dy once + 2N rows
                 work = steps * ((T + N) * d * 2 + 2 * (T + N) * d * 2 + 3 * 12 * T * k)
             elif kname == "combine":
                 work = n * ((N + T) * d * 2 + 8 * T * k)
@@ -615,7 +621,7 @@ def run_workload(args, name, cfg, steps, warmup, rank, world, local, barrier, ex
                    "l2": "no flush: each step streams > L2 (expert weights alone %.2f GB)"
                          % (3 * G * d * f * 2 / 1e9),
                    "rows_per_step": N, "load_max_over_mean": load_max_over_mean,
-                   "keep_rows": keep, "kept_rows": kept_real,
+                   "keep_rows": keep, "kept_rows": kept_real, "gather_in_gemm": cfg.get("gather_in_gemm", 0),
                    "kept_activation_bytes": keep * f * 2 * 2, "keep_budget_bytes": keep_budget,
                    "expert_weights": "seeded on the device" if extra else "synth (seeded, host)"},
         "cuda_graph": graph,
@@ -696,6 +702,8 @@ def main():
         cfg["E"] = args.experts
     if args.topk:
         cfg["k"] = args.topk
+    if args.gather_in_gemm:
+        cfg["gather_in_gemm"] = 1
     line = run_workload(args, args.workload, cfg, args.steps, args.warmup, rank, world, local, barrier)
     # every other workload of the pages' families, a few steps each, as a compact record
     if not args.no_workloads and args.workload == "mixtral" and not (args.tokens or args.experts or args.topk):
@@ -706,6 +714,11 @@ def main():
             rec = run_workload(args, name, dict(synth.CONFIGS[name]), args.workload_steps, 3, rank, world, local,
                                barrier, extra=True)
             line["workloads"][name] = compact(rec)
+        # the dispatch gather fused into the expert GEMMs' operand loads, beside the default path
+        for name in ("mixtral", "deepseek", "qwen3"):
+            rec = run_workload(args, name, dict(synth.CONFIGS[name], gather_in_gemm=1), args.workload_steps, 3, rank,
+                               world, local, barrier, extra=True)
+            line["workloads"][name + "+gather_in_gemm"] = compact(rec)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -65,6 +65,19 @@
  * which must then reach the matching backward untouched.  moe_keep_rows_for_budget chooses
  * keep_rows from a byte budget (the adaptive granularity of the MoEBlaze summary's future work).
  *
+ * Gathered operand loads (MoEBlaze summary, Methodology item 2, first bullet: the dispatch gather
+ * fused with the expert feed-forward).  With gather_in_gemm = 1, moe_layer_fwd and moe_layer_bwd
+ * write no x_perm or dY_perm: the dispatch builds its tables and the token of every padded row, and
+ * the GEMMs that read those rows (gate/up, dh', the recompute, the weight gradients) fetch them from
+ * x and dy in token order, four rows per TMA tile::gather4 copy, from four producer warps.  For
+ * finite x and dy the results are those of gather_in_gemm = 0 bit for bit (a pad row reads token 0's
+ * row instead of zeros, and its zero gate zeroes every gradient term it feeds).  It is the slower
+ * choice on GB300: a stage's
+ * 32 gather copies take about twice as long as the tensor cores' work on it, where one TMA box of a
+ * contiguous x_perm tile keeps up, so the GEMMs that gather run at about half their speed while the
+ * separate gather they save costs 0.1 to 0.5 ms per step.  It saves the x_perm and dY_perm traffic
+ * (2 (T + N) d bytes each way) for a workload where that matters more than GEMM time.
+ *
  * Workspace.  Size it with moe_workspace_size(), zero its header once with moe_workspace_init(),
  * and pass the same workspace to every call of one layer instance.  moe_dispatch leaves the
  * routing tables in it that moe_expert_ffn_fwd/bwd, moe_combine and moe_combine_bwd read; the
@@ -111,6 +124,10 @@ typedef struct {
     float capacity_factor;     /* cf > 0: capacity ceil(cf*T*k/E) per expert; <= 0: dropless */
     int32_t keep_rows;         /* >= 0: expert-ordered rows whose gate/up pre-activations the forward
                                 * keeps for the backward (see "Kept activations"); 0 recomputes all */
+    int32_t gather_in_gemm;    /* 0 or 1, moe_layer_fwd / moe_layer_bwd only: 1 gathers the x and dy
+                                * rows inside the expert GEMMs' operand loads (TMA tile::gather4 from
+                                * token order) instead of copying them to x_perm / dY_perm first;
+                                * same results, slower on GB300 (see "Gathered operand loads") */
 } moe_config_t;
 
 typedef uint16_t moe_bf16;                 /* raw bf16 bit pattern */

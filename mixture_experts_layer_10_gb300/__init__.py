@@ -35,7 +35,7 @@ class moe_config_t(ctypes.Structure):
     _fields_ = [("T", ctypes.c_int32), ("d_model", ctypes.c_int32), ("d_ff", ctypes.c_int32),
                 ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("n_shared", ctypes.c_int32),
                 ("renorm", ctypes.c_int32), ("capacity_factor", ctypes.c_float),
-                ("keep_rows", ctypes.c_int32)]
+                ("keep_rows", ctypes.c_int32), ("gather_in_gemm", ctypes.c_int32)]
 
 
 class MoEError(RuntimeError):
@@ -105,14 +105,16 @@ def load(path: str | None = None):
 # ------------------------------------------------------------------------------------------------
 
 def config(T: int, d: int, f: int, E: int, k: int, S: int = 0, renorm: int = 0, cf: float = 0.0,
-           keep_rows: int = 0):
-    return moe_config_t(int(T), int(d), int(f), int(E), int(k), int(S), int(renorm), float(cf), int(keep_rows))
+           keep_rows: int = 0, gather_in_gemm: int = 0):
+    return moe_config_t(int(T), int(d), int(f), int(E), int(k), int(S), int(renorm), float(cf), int(keep_rows),
+                        int(gather_in_gemm))
 
 
 def config_from(c: dict) -> moe_config_t:
-    """From a workload dict with keys T, d, f, E, k, S, renorm, cf (and keep_rows, default 0)."""
+    """From a workload dict with keys T, d, f, E, k, S, renorm, cf (and keep_rows, gather_in_gemm,
+    default 0)."""
     return config(c["T"], c["d"], c["f"], c["E"], c["k"], c.get("S", 0), c.get("renorm", 0), c.get("cf", 0.0),
-                  c.get("keep_rows", 0))
+                  c.get("keep_rows", 0), c.get("gather_in_gemm", 0))
 
 
 def _ptr(t):

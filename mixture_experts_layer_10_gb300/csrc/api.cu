@@ -29,7 +29,8 @@ moe_status_t make_cfg(const moe_config_t* in, Cfg* c) {
   if (m.T < 1 || m.T > (1 << 20) || m.E < 1 || m.E > kMaxE || m.k < 1 || m.k > m.E ||
       m.n_shared < 0 || m.n_shared > kMaxS || m.d_model < 64 || m.d_ff < 64 ||
       m.d_model > 16384 || m.d_ff > 16384 || (m.d_model % 64) != 0 || (m.d_ff % 64) != 0 ||
-      (int64_t)m.T * m.k > (int64_t)1 << 24 || !(m.capacity_factor == m.capacity_factor) || m.keep_rows < 0)
+      (int64_t)m.T * m.k > (int64_t)1 << 24 || !(m.capacity_factor == m.capacity_factor) || m.keep_rows < 0 ||
+      (m.gather_in_gemm != 0 && m.gather_in_gemm != 1))
     return MOE_ERR_INVALID_ARG;
   c->T = m.T;
   c->d = m.d_model;
@@ -40,6 +41,7 @@ moe_status_t make_cfg(const moe_config_t* in, Cfg* c) {
   c->G = m.E + m.n_shared;
   c->renorm = m.renorm ? 1 : 0;
   c->keep = m.keep_rows / kRowTile * kRowTile;   // clamped to the row capacity by make_layout users
+  c->gather_in_gemm = m.gather_in_gemm;
   if (m.capacity_factor > 0.f) {
     const double cap = std::ceil((double)m.capacity_factor * (double)m.T * (double)m.k / (double)m.E);
     c->C = cap >= (double)INT_MAX ? INT_MAX : (int)cap;
@@ -143,6 +145,7 @@ Layout make_layout(const Cfg& c) {
   L.wr_bf16 = take((size_t)c.d * L.Ep * 2);
   L.wr3 = take((size_t)3 * L.Ep * c.d * 2);
   L.fp8s = take(rows * 3 * 4);
+  L.tok_of_prow = take(rows * 4);
   if (router_stream_eligible(c)) {
     const RouterStreamPlan pl = router_stream_plan(c);
     L.rt_part = take(pl.maxseg > 1 ? (size_t)pl.ntiles * pl.maxseg * pl.eb * 128 * 4 : 0);
@@ -282,11 +285,29 @@ moe_status_t do_dispatch(const Cfg& c, const Ws& w, const int32_t* idx, const ui
   return MOE_OK;
 }
 
+// The dispatch of the fused calls: the queues and tables only, the token of every padded row (the
+// expert GEMMs gather their rows from token order), and for the backward the gate of every row.
+moe_status_t do_dispatch_tables(const Cfg& c, const Ws& w, const int32_t* idx, const float* gates, cudaStream_t s) {
+  DispatchArgs a = dispatch_args(w);
+  a.idx = idx;
+  a.gates = gates;
+  a.tok_of_prow = w.at<int32_t>(w.L.tok_of_prow);
+  MOE_CUDA(launch_dispatch_scan(c, w.L, a, s));
+  MOE_CUDA(launch_dispatch_gather(c, w.L, a, true, false, false, s, gates != nullptr));
+  return MOE_OK;
+}
+
+// x_perm / dy_perm, or (tok non-null) x and dy in token order with the token of every padded row.
 moe_status_t do_ffn_bwd(const Cfg& c, const Ws& w, const uint16_t* x_perm, const uint16_t* dy_perm,
                         const uint16_t* Wg, const uint16_t* Wu, const uint16_t* Wd,
                         uint16_t* dx_perm, float* dgates, uint16_t* dWg, uint16_t* dWu,
-                        uint16_t* dWd, const uint16_t* a_kept, const uint16_t* b_kept, cudaStream_t s) {
+                        uint16_t* dWd, const uint16_t* a_kept, const uint16_t* b_kept, cudaStream_t s,
+                        const uint16_t* x_tok = nullptr, const uint16_t* dy_tok = nullptr,
+                        const int32_t* tok = nullptr) {
   FfnBwdArgs b{};
+  b.x_tok = x_tok;
+  b.dy_tok = dy_tok;
+  b.tok = tok;
   b.x_perm = x_perm;
   b.dy_perm = dy_perm;
   b.gate_of_prow = w.at<float>(w.L.gate_of_prow);
@@ -728,16 +749,26 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const moe_bf16* x, const flo
   int32_t* idx = static_cast<int32_t*>(saved);
   float* gates = reinterpret_cast<float*>(idx + (size_t)c.T * c.k);
   MOE_TRY(do_route(c, w, x, W_r, b_r, idx, gates, nullptr, stream));
+  // x rows to x_perm, or (gather_in_gemm) the tables only: the gate/up GEMM then gathers the x rows
+  // itself from token order (MoEBlaze summary, Methodology item 2: dispatch fused with the FFN)
   uint16_t* x_perm = w.at<uint16_t>(w.L.xperm);
-  MOE_TRY(do_dispatch(c, w, idx, x, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, x_perm,
-                      nullptr, stream));
+  if (c.gather_in_gemm)
+    MOE_TRY(do_dispatch_tables(c, w, idx, nullptr, stream));
+  else
+    MOE_TRY(do_dispatch(c, w, idx, x, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, x_perm, nullptr,
+                        stream));
   uint16_t* o_perm = w.at<uint16_t>(w.L.buf_d1);
   // kept a and b go to `saved`, which lives from this call to the backward; the workspace does not
   const SavedLayout sv = saved_layout(c);
   uint16_t* a_keep = reinterpret_cast<uint16_t*>(static_cast<char*>(saved) + sv.a_off);
   uint16_t* b_keep = reinterpret_cast<uint16_t*>(static_cast<char*>(saved) + sv.b_off);
   FfnFwdArgs fa{x_perm, W_gate, W_up, W_down, w.at<uint16_t>(w.L.buf_f0), o_perm, w.hdr(), w.tabs(),
-                a_keep, b_keep};
+                a_keep, b_keep, nullptr, nullptr};
+  if (c.gather_in_gemm) {
+    fa.x_perm = nullptr;
+    fa.x_tok = x;
+    fa.tok = w.at<int32_t>(w.L.tok_of_prow);
+  }
   MOE_CUDA(launch_ffn_fwd(c, w.L, fa, stream));
   CombineArgs ca{o_perm, gates, y, w.tabs(), w.at<int32_t>(w.L.prow_of_slot)};
   MOE_CUDA(launch_combine(c, ca, stream));
@@ -762,16 +793,25 @@ moe_status_t moe_layer_bwd(const moe_config_t* cfg, const moe_bf16* x, const flo
   MOE_TRY(check_device());
   const int32_t* idx = static_cast<const int32_t*>(saved);
   const float* gates = reinterpret_cast<const float*>(idx + (size_t)c.T * c.k);
+  // the queues again from the saved idx, the rows' gates, and the x and dy rows -- or (gather_in_gemm)
+  // no rows: the GEMMs that read them (dh', the recompute, the weight gradients) gather them
   uint16_t* x_perm = w.at<uint16_t>(w.L.xperm);
   uint16_t* dy_perm = w.at<uint16_t>(w.L.dy_perm);
-  MOE_TRY(do_dispatch(c, w, idx, x, dy, gates, nullptr, nullptr, nullptr, nullptr, x_perm, dy_perm, stream));
+  if (c.gather_in_gemm)
+    MOE_TRY(do_dispatch_tables(c, w, idx, gates, stream));
+  else
+    MOE_TRY(do_dispatch(c, w, idx, x, dy, gates, nullptr, nullptr, nullptr, nullptr, x_perm, dy_perm, stream));
   uint16_t* dx_perm = w.at<uint16_t>(w.L.buf_d1);
   float* dgates = w.at<float>(w.L.dgates);
   const SavedLayout sv = saved_layout(c);
   const uint16_t* a_kept = reinterpret_cast<const uint16_t*>(static_cast<const char*>(saved) + sv.a_off);
   const uint16_t* b_kept = reinterpret_cast<const uint16_t*>(static_cast<const char*>(saved) + sv.b_off);
-  MOE_TRY(do_ffn_bwd(c, w, x_perm, dy_perm, W_gate, W_up, W_down, dx_perm, dgates, dW_gate, dW_up,
-                     dW_down, a_kept, b_kept, stream));
+  if (c.gather_in_gemm)
+    MOE_TRY(do_ffn_bwd(c, w, nullptr, nullptr, W_gate, W_up, W_down, dx_perm, dgates, dW_gate, dW_up, dW_down,
+                       a_kept, b_kept, stream, x, dy, w.at<int32_t>(w.L.tok_of_prow)));
+  else
+    MOE_TRY(do_ffn_bwd(c, w, x_perm, dy_perm, W_gate, W_up, W_down, dx_perm, dgates, dW_gate, dW_up, dW_down,
+                       a_kept, b_kept, stream));
   float* dlogits = w.at<float>(w.L.dlogits);
   MOE_TRY(do_router_bwd(c, w, x, W_r, b_r, idx, gates, dgates, dlogits, dW_r, db_r, stream));
   return do_combine_bwd(c, w, dx_perm, dlogits, W_r, dx, stream);

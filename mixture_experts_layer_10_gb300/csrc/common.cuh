@@ -72,6 +72,7 @@ struct Layout {
   size_t hdr, tabs, scan_status, rank, prow_of_slot, slot_of_prow, gate_of_prow, dg_part,
       dlogits, dwr_part, db_part, dgates, xperm, dy_perm, buf_f0, buf_f1, buf_f2, buf_f3, buf_d1,
       dl_bf16, wr_bf16, wr3;
+  size_t tok_of_prow;       // token of every padded expert row (pad rows: token 0), for gathered loads
   size_t rt_part, rt_cnt;   // streaming router (E <= 32): partial logits and part counters
   size_t fp8s;              // FP8 backward: row scales of the x, dY and [dA | dB] rows, [3][rows] fp32
   size_t total;
@@ -81,6 +82,7 @@ struct Cfg {               // validated configuration with derived sizes
   int T, d, f, E, k, S, G, renorm;
   int C;                   // capacity (INT32_MAX when dropless)
   int keep;                // rows with kept a, b: keep_rows rounded down to kRowTile (clamped by the layout)
+  int gather_in_gemm;      // fused layer calls: x, dy rows gathered by the GEMMs from token order
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -159,10 +161,16 @@ struct DispatchArgs {
   // nullable: receives the header's status (MOE_OK or the first device error of this dispatch)
   // once the last scan block has built the tables
   int32_t* status_out;
+  // nullable: the token of every padded expert row (pad rows: token 0), for GEMMs that gather their
+  // operand rows from token order instead of reading x_perm / dY_perm
+  int32_t* tok_of_prow;
 };
 cudaError_t launch_dispatch_scan(const Cfg& c, const Layout& L, const DispatchArgs& a, cudaStream_t s);
+// write_meta: the slot/row tables (and tok_of_prow when given); gather_x / gather_dy: copy the rows;
+// gates: the gate of every padded row (implied by gather_dy)
 cudaError_t launch_dispatch_gather(const Cfg& c, const Layout& L, const DispatchArgs& a,
-                                   bool write_meta, bool gather_x, bool gather_dy, cudaStream_t s);
+                                   bool write_meta, bool gather_x, bool gather_dy, cudaStream_t s,
+                                   bool gates = false);
 
 struct CombineArgs {
   const uint16_t* o_perm; const float* gates; uint16_t* y;
@@ -240,6 +248,9 @@ struct FfnFwdArgs {
   const uint16_t* x_perm; const uint16_t* Wg; const uint16_t* Wu; const uint16_t* Wd;
   uint16_t* h; uint16_t* o_perm; Hdr* hdr; const Tables* tabs;
   uint16_t* a_keep; uint16_t* b_keep;   // [rows, d_ff] bf16: a, b of the first c.keep rows
+  // gathered A rows (both non-null): x [T, d] in token order and the token of every padded row;
+  // x_perm is then not read
+  const uint16_t* x_tok; const int32_t* tok;
 };
 cudaError_t launch_ffn_fwd(const Cfg& c, const Layout& L, const FfnFwdArgs& a, cudaStream_t s);
 
@@ -250,6 +261,9 @@ struct FfnBwdArgs {
   uint16_t* dWg; uint16_t* dWu; uint16_t* dWd; Hdr* hdr; const Tables* tabs;
   // kept a, b of rows [0, c.keep) [rows, d_ff] bf16; null: the forward left them in dB and Hg
   const uint16_t* a_kept; const uint16_t* b_kept;
+  // gathered rows (all non-null): x and dy [T, d] in token order and the token of every padded row;
+  // x_perm and dy_perm are then not read
+  const uint16_t* x_tok; const uint16_t* dy_tok; const int32_t* tok;
 };
 cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, cudaStream_t s);
 // SwiGLU backward of the kept rows [0, c.keep): a and b from a.a_kept / a.b_kept (or, when null,

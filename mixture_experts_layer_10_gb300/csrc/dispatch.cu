@@ -11,7 +11,9 @@
 // dispatch_gather_kernel: token owner.  A warp reads each x (and dy) row once, 16 bytes per lane,
 //   and writes it to every kept slot's row (and every shared expert's row); then zeroes pad rows.
 //   Rows are moved as 16-byte vectors, so the FP8 forward gathers e4m3 token rows (d bytes) through
-//   the same kernel as rows of d/2 two-byte elements, with their row scales beside them.
+//   the same kernel as rows of d/2 two-byte elements, with their row scales beside them.  For GEMMs
+//   that gather their operand rows themselves (tile::gather4 from token order) the kernel moves no
+//   data and writes only the tables, the token of every padded row and, for the backward, its gate.
 #include <mutex>
 
 #include "common.cuh"
@@ -190,9 +192,10 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(DispatchArg
 
 constexpr int kUnroll = 4;   // 16-byte vectors per lane in flight per source row
 
-template <bool kMeta, bool kX, bool kDy>
+template <bool kMeta, bool kX, bool kDy, bool kGate>
 __global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a, int T, int k, int E,
                                                               int S, int d) {
+  constexpr bool kGates = kDy || kGate;   // the gate of every padded row
   const Tables* tb = a.tabs;
   const int lane = threadIdx.x & 31;
   const int gw = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
@@ -225,9 +228,11 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a, in
             a.slot_of_prow[prow] = (int)slot;
           }
         }
-        if (kDy && kept) a.gate_of_prow[prow] = a.gates[slot];
+        if (kGates && kept) a.gate_of_prow[prow] = a.gates[slot];
+        if (kept && a.tok_of_prow != nullptr) a.tok_of_prow[prow] = t;
         if (kX && kept && a.xs_perm != nullptr) a.xs_perm[prow] = a.xs_tok[t];
       }
+      if (!kX && !kDy) continue;   // tables only
       const int ng = min(32, k - jb);
       // kUnroll vectors per lane are loaded before any is stored, so a warp keeps
       // kUnroll x 512 bytes of each source row in flight.  Warp-uniform trip count: every lane
@@ -272,8 +277,9 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a, in
     if (lane < S && t < tb->kept[E + lane]) {
       const size_t p = (size_t)tb->poff[E + lane] + t;
       if (kMeta) a.slot_of_prow[p] = -2;
+      if (kMeta && a.tok_of_prow != nullptr) a.tok_of_prow[p] = t;
       if (kX && a.xs_perm != nullptr) a.xs_perm[p] = a.xs_tok[t];
-      if (kDy) a.gate_of_prow[p] = 1.f;
+      if (kGates) a.gate_of_prow[p] = 1.f;
     }
   }
   // zero the pad rows of every segment
@@ -287,14 +293,16 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a, in
     }
     const size_t row = (size_t)tb->poff[lo] + tb->kept[lo] + (p - tb->pad_start[lo]);
     const uint4 z = make_uint4(0, 0, 0, 0);
-    for (int v = lane; v < nvec; v += 32) {
+    for (int v = lane; (kX || kDy) && v < nvec; v += 32) {
       if (kX) reinterpret_cast<uint4*>(a.x_perm + row * d)[v] = z;
       if (kDy) reinterpret_cast<uint4*>(a.dy_perm + row * d)[v] = z;
     }
     if (lane == 0) {
       if (kMeta) a.slot_of_prow[row] = -1;
+      // a pad row gathers token 0: with a zero gate its dA, dB and Hg are exactly zero
+      if (kMeta && a.tok_of_prow != nullptr) a.tok_of_prow[row] = 0;
       if (kX && a.xs_perm != nullptr) a.xs_perm[row] = 0.f;
-      if (kDy) a.gate_of_prow[row] = 0.f;
+      if (kGates) a.gate_of_prow[row] = 0.f;
     }
   }
 }
@@ -314,17 +322,24 @@ cudaError_t launch_dispatch_scan(const Cfg& c, const Layout& L, const DispatchAr
 }
 
 cudaError_t launch_dispatch_gather(const Cfg& c, const Layout& L, const DispatchArgs& a,
-                                   bool write_meta, bool gather_x, bool gather_dy, cudaStream_t s) {
+                                   bool write_meta, bool gather_x, bool gather_dy, cudaStream_t s, bool gates) {
   (void)L;
   const int blocks = num_sms() * 8;
-  if (!(write_meta && gather_x) && !(!write_meta && gather_dy && !gather_x)) return cudaErrorInvalidValue;
   prof_mark(kKGather, s, true);
   if (write_meta && gather_x && gather_dy)
-    dispatch_gather_kernel<true, true, true><<<blocks, 256, 0, s>>>(a, c.T, c.k, c.E, c.S, c.d);
+    dispatch_gather_kernel<true, true, true, false><<<blocks, 256, 0, s>>>(a, c.T, c.k, c.E, c.S, c.d);
   else if (write_meta && gather_x)
-    dispatch_gather_kernel<true, true, false><<<blocks, 256, 0, s>>>(a, c.T, c.k, c.E, c.S, c.d);
-  else
-    dispatch_gather_kernel<false, false, true><<<blocks, 256, 0, s>>>(a, c.T, c.k, c.E, c.S, c.d);
+    dispatch_gather_kernel<true, true, false, false><<<blocks, 256, 0, s>>>(a, c.T, c.k, c.E, c.S, c.d);
+  else if (write_meta && !gather_x && !gather_dy && gates)
+    dispatch_gather_kernel<true, false, false, true><<<blocks, 256, 0, s>>>(a, c.T, c.k, c.E, c.S, c.d);
+  else if (write_meta && !gather_x && !gather_dy)
+    dispatch_gather_kernel<true, false, false, false><<<blocks, 256, 0, s>>>(a, c.T, c.k, c.E, c.S, c.d);
+  else if (!write_meta && gather_dy && !gather_x)
+    dispatch_gather_kernel<false, false, true, false><<<blocks, 256, 0, s>>>(a, c.T, c.k, c.E, c.S, c.d);
+  else {
+    prof_mark(kKGather, s, false);
+    return cudaErrorInvalidValue;
+  }
   prof_mark(kKGather, s, false);
   return cudaGetLastError();
 }

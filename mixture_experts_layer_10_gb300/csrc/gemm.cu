@@ -64,6 +64,12 @@ struct Job {
 struct PolicyDefaults {
   // k-iteration before which the MMA waits for the epilogue to release the accumulator
   __device__ static int acc_wait_kit(const Job&) { return 0; }
+  // Gathered operand rows (the dispatch gather fused into the operand load; CTA-pair problems): 0
+  // none; 1 the K-major A tile's 128 rows come from token order (x or dY) through the token of every
+  // padded row; 2 the weight gradient's token-side operand (x or dY, MN-major) takes its 64 K rows per
+  // stage the same way, as two 64-column boxes.  Either way a CTA's stage takes 32 tile::gather4
+  // copies (four 128-byte lines each) from kGatherWarps warps, and one TMA box for the other operand.
+  static constexpr int kGather = 0;
   // TMA bytes that complete one stage at k-iteration kit
   __device__ static uint32_t tx_bytes(const Job&, int, uint32_t stage_bytes) { return stage_bytes; }
   // a stateful policy keeps per-lane epilogue state across the jobs of one CTA (epilogue_s)
@@ -133,6 +139,16 @@ struct PairDefaults : PolicyDefaults {
   static constexpr int kTmemCols = 512;
   static constexpr uint32_t kIdesc = idesc_bf16(kPairM, 256, false, false);
   static constexpr uint32_t kEpiWarpBytes = 2 * 2048;   // two TMA-store boxes (kEpiBox)
+};
+
+// A stage's gathered operand: 128 lines of 128 bytes (64 bf16) from `dst` within the stage, in the
+// 128-byte-swizzled layout a TMA box of 128 rows would leave.  Line L is row tok[L] (kGather 1) or
+// tok[L % 64] (kGather 2) of the token-order tensor behind `map` (one-row boxes), from column col0
+// (L < 64) or col1.
+struct GatherOp {
+  const CUtensorMap* map;
+  int col0, col1;
+  uint32_t dst;
 };
 
 // Epilogue output goes through shared memory and TMA stores: each epilogue warp writes a [32 rows x
@@ -211,14 +227,16 @@ __device__ __forceinline__ void mma_kk_bmn(uint32_t sa, uint32_t dt, uint32_t id
 // projection of the same 128 hidden units.  kKeep: pair tiles below keep_rows also store a and b
 // (bf16) for the backward, from triplets of staging boxes (H, a, b; two triplets per warp, five
 // pipeline stages to make room).
-template <bool kKeep>
+template <bool kKeep, bool kG = false>
 struct FwdGateUpT : PairDefaults {
   static constexpr int kId = kKGateUp;
   static constexpr int kEpiWarps = 4;
   static constexpr int kStages = kKeep ? 5 : 6;
   static constexpr uint32_t kEpiWarpBytes = kKeep ? 6 * 2048 : 2 * 2048;
+  static constexpr int kGather = kG ? 1 : 0;
   struct Params {
-    CUtensorMap tmX, tmWg, tmWu, tmH, tmA, tmB;
+    CUtensorMap tmX, tmWg, tmWu, tmH, tmA, tmB;   // tmX: x_perm, or x in token order (gathered)
+    const int32_t* tok;                           // gathered: token of every padded row
     int f, d, nt, keep_rows;
     Hdr* hdr;
     const Tables* tabs;
@@ -232,8 +250,15 @@ struct FwdGateUpT : PairDefaults {
     tma_prefetch(&p.tmX); tma_prefetch(&p.tmWg); tma_prefetch(&p.tmWu);
   }
   __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint32_t cbar, int rank) {
-    tma_load_2d_pair(st, &p.tmX, cbar, kit * kBK, j.m0 + kBM * rank);
+    if constexpr (!kG) tma_load_2d_pair(st, &p.tmX, cbar, kit * kBK, j.m0 + kBM * rank);
     tma_load_3d_pair(st + kTileA, rank ? &p.tmWu : &p.tmWg, cbar, kit * kBK, j.n0, j.seg);
+  }
+  // gathered: this CTA's 128 rows of the tile, K block kit
+  __device__ static const int32_t* gather_tok(const Params& p, const Job& j, int, int rank) {
+    return p.tok + j.m0 + kBM * rank;
+  }
+  __device__ static GatherOp gather_op(const Params& p, const Job&, int kit, int) {
+    return GatherOp{&p.tmX, kit * kBK, kit * kBK, 0u};
   }
   __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
     mma_kk_kmajor(sa, dt, kIdesc, kit);
@@ -293,6 +318,7 @@ struct FwdGateUpT : PairDefaults {
   __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
 };
 using FwdGateUp = FwdGateUpT<false>;
+using FwdGateUpG = FwdGateUpT<false, true>;
 
 // The gate/up projection with FP8 operands (tcgen05 kind::f8f6f4, e4m3): x_perm rows and W_gate /
 // W_up rows quantised per row (codes and an fp32 scale each), so a = s_x s_g (q_x . q_g) exactly
@@ -508,12 +534,15 @@ struct FwdDown : PairDefaults {
 // dh' = dY W_d for every row tile: N = 256 columns of d_ff, K = d_model.  W_d[e] is
 // [d_model, d_ff], so it is the MN-major B operand (two 64-wide boxes per CTA and stage).  dh' is
 // stored in bf16 for the SwiGLU backward below.
-struct BwdDh : PairDefaults {
+template <bool kG>
+struct BwdDhT : PairDefaults {
   static constexpr int kId = kKBwdDh;
   static constexpr int kEpiWarps = 4;
   static constexpr uint32_t kIdesc = idesc_bf16(kPairM, 256, false, true);
+  static constexpr int kGather = kG ? 1 : 0;
   struct Params {
-    CUtensorMap tmDY, tmWdT, tmDH;
+    CUtensorMap tmDY, tmWdT, tmDH;   // tmDY: dY_perm, or dy in token order (gathered)
+    const int32_t* tok;              // gathered: token of every padded row
     int f, d, nt;
     Hdr* hdr;
     const Tables* tabs;
@@ -525,8 +554,15 @@ struct BwdDh : PairDefaults {
   __device__ static int mma_kiters(const Params& p, const SegSmem& s, int t) { (void)s; (void)t; return p.d / kBK; }
   __device__ static void prefetch(const Params& p) { tma_prefetch(&p.tmDY); tma_prefetch(&p.tmWdT); }
   __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint32_t cbar, int rank) {
-    tma_load_2d_pair(st, &p.tmDY, cbar, kit * kBK, j.m0 + kBM * rank);
+    if constexpr (!kG) tma_load_2d_pair(st, &p.tmDY, cbar, kit * kBK, j.m0 + kBM * rank);
     tma_load_4d_pair(st + kTileA, &p.tmWdT, cbar, 0, kit * kBK, (j.n0 + kBM * rank) / 64, j.seg);
+  }
+  // gathered: this CTA's 128 rows of the tile, K block kit
+  __device__ static const int32_t* gather_tok(const Params& p, const Job& j, int, int rank) {
+    return p.tok + j.m0 + kBM * rank;
+  }
+  __device__ static GatherOp gather_op(const Params& p, const Job&, int kit, int) {
+    return GatherOp{&p.tmDY, kit * kBK, kit * kBK, 0u};
   }
   __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
     mma_kk_bmn(sa, dt, kIdesc, kit);
@@ -536,18 +572,23 @@ struct BwdDh : PairDefaults {
   }
   __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
 };
+using BwdDh = BwdDhT<false>;
+using BwdDhG = BwdDhT<true>;
 
 // The recompute a | b = X [Wg;Wu]^T (the forward's first GEMM shape, double-buffered TMEM) with the
 // SwiGLU backward in its epilogue, which reads this tile's dh' written by BwdDh:
 //   h = silu(a) b, dg += dh'.h, dh = g dh', dA = dh b silu'(a), dB = dh silu(a), Hg = g h.
 // Four epilogue warps, one per TMEM lane quarter (eight, two per quarter, measured 77% instead of
 // 84% of the MMA rate per SM cycle).  dg is summed per 64-column half of the tile.
-struct BwdFused : PairDefaults {
+template <bool kG>
+struct BwdFusedT : PairDefaults {
   static constexpr int kId = kKBwdFused;
   static constexpr int kEpiWarps = 4;
   static constexpr uint32_t kEpiWarpBytes = 3 * 2048;   // boxes for dA, dB, Hg
+  static constexpr int kGather = kG ? 1 : 0;
   struct Params {
-    CUtensorMap tmX, tmWg, tmWu, tmDA, tmDB, tmHg;
+    CUtensorMap tmX, tmWg, tmWu, tmDA, tmDB, tmHg;   // tmX: x_perm, or x in token order (gathered)
+    const int32_t* tok;                              // gathered: token of every padded row
     const uint16_t* DH;
     const float* gate_of_prow;
     float* dg_part;
@@ -566,8 +607,15 @@ struct BwdFused : PairDefaults {
     tma_prefetch(&p.tmX); tma_prefetch(&p.tmWg); tma_prefetch(&p.tmWu);
   }
   __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint32_t cbar, int rank) {
-    tma_load_2d_pair(st, &p.tmX, cbar, kit * kBK, j.m0 + kBM * rank);
+    if constexpr (!kG) tma_load_2d_pair(st, &p.tmX, cbar, kit * kBK, j.m0 + kBM * rank);
     tma_load_3d_pair(st + kTileA, rank ? &p.tmWu : &p.tmWg, cbar, kit * kBK, j.n0, j.seg);
+  }
+  // gathered: this CTA's 128 rows of the tile, K block kit
+  __device__ static const int32_t* gather_tok(const Params& p, const Job& j, int, int rank) {
+    return p.tok + j.m0 + kBM * rank;
+  }
+  __device__ static GatherOp gather_op(const Params& p, const Job&, int kit, int) {
+    return GatherOp{&p.tmX, kit * kBK, kit * kBK, 0u};
   }
   __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
     mma_kk_kmajor(sa, dt, kIdesc, kit);
@@ -635,6 +683,8 @@ struct BwdFused : PairDefaults {
   }
   __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
 };
+using BwdFused = BwdFusedT<false>;
+using BwdFusedG = BwdFusedT<true>;
 
 // The FP8 backward's recompute: a | b = s_x s_g (X8 Wg8^T) | s_x s_u (X8 Wu8^T) from the forward's
 // e4m3 codes (FwdGateUp8's main loop), with BwdFused's SwiGLU backward in the epilogue reading this
@@ -789,13 +839,17 @@ struct DgradX : PairDefaults {
 // the kernel at 73% of the MMA rate per SM cycle, one copy reaches 86%).  Tiles go expert by expert, largest first; inside an
 // expert the d_model-wide operand (X, or dY) is the one cycled through, so the pairs at work keep
 // all of it and a few d_ff-wide column blocks in L2.
-struct Wgrad : PairDefaults {
+template <bool kG>
+struct WgradT : PairDefaults {
   static constexpr int kId = kKWgrad;
   static constexpr int kEpiWarps = 4;
   static constexpr uint32_t kIdesc = idesc_bf16(kPairM, 256, true, true);
+  static constexpr int kGather = kG ? 2 : 0;
   struct Params {
-    CUtensorMap tmDA, tmDB, tmX, tmDY, tmHg;   // all [rows, width] as 64-column block pairs (map_mn2)
+    CUtensorMap tmDA, tmDB, tmX, tmDY, tmHg;   // all [rows, width] as 64-column block pairs (map_mn2);
+                                               // gathered: tmX, tmDY are x, dy in token order, one-row boxes
     CUtensorMap tmdWg, tmdWu, tmdWd;           // [G, M, ncols] with 32 x 32 boxes (stores)
+    const int32_t* tok;                        // gathered: token of every padded row
     uint16_t *dWg, *dWu, *dWd;
     int f, d;
     int mt_f, nt_d, mt_d, nt_f, tps;           // pair tiles: dWg/dWu (mt_f x nt_d), dWd (mt_d x nt_f)
@@ -834,10 +888,27 @@ struct Wgrad : PairDefaults {
   }
   __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint32_t cbar, int rank) {
     const int row = j.kbase + kit * kBK;
+    if constexpr (kG) {   // the operand of the other side only; the token-side one is gathered
+      if (j.sub == 2) tma_load_3d_pair(st + 2 * kBox, &p.tmHg, cbar, 0, row, (j.n0 + kBM * rank) / 64);
+      else tma_load_3d_pair(st, j.sub == 0 ? &p.tmDA : &p.tmDB, cbar, 0, row, (j.m0 + kBM * rank) / 64);
+      return;
+    }
     const CUtensorMap* ta = j.sub == 0 ? &p.tmDA : (j.sub == 1 ? &p.tmDB : &p.tmDY);
     const CUtensorMap* tb = j.sub == 2 ? &p.tmHg : &p.tmX;
     tma_load_3d_pair(st, ta, cbar, 0, row, (j.m0 + kBM * rank) / 64);
     tma_load_3d_pair(st + 2 * kBox, tb, cbar, 0, row, (j.n0 + kBM * rank) / 64);
+  }
+  // The token-side operand, MN-major: its 64 K rows (this stage's padded rows) x this CTA's 128
+  // columns, as two 64-column boxes (dY for dWd in the A place, x for dWg / dWu in the B place).  A
+  // column block past d_model (the last tile of a width not a multiple of 256) is clamped onto the
+  // last block: those accumulator rows or columns are never stored.
+  __device__ static const int32_t* gather_tok(const Params& p, const Job& j, int kit, int) {
+    return p.tok + j.kbase + kit * kBK;
+  }
+  __device__ static GatherOp gather_op(const Params& p, const Job& j, int, int rank) {
+    const int c = (j.sub == 2 ? j.m0 : j.n0) + kBM * rank;
+    return GatherOp{j.sub == 2 ? &p.tmDY : &p.tmX, min(c, p.d - 64), min(c + 64, p.d - 64),
+                    j.sub == 2 ? 0u : 2 * kBox};
   }
   __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
 #pragma unroll
@@ -889,6 +960,8 @@ struct Wgrad : PairDefaults {
       *reinterpret_cast<uint4*>(base + j.n0 + c) = make_uint4(0, 0, 0, 0);
   }
 };
+using Wgrad = WgradT<false>;
+using WgradG = WgradT<true>;
 
 // Router weight gradient on the tensor cores: partial[split][i][e] = sum over the split's tokens of
 // x[t][i] dl[t][e].  M = d_model in 128-row tiles (A = x, MN-major), N = E padded to 64 (B = the
@@ -1269,9 +1342,13 @@ constexpr size_t smem_bytes() {
   return 1024 + (size_t)P::kStages * P::kStageBytes + epi_bytes<P>() + 256 + sizeof(SegSmem);
 }
 
+// Warps that copy gathered operand rows: warp 0 and, after the epilogue warps, three more.
+constexpr int kGatherWarps = 4;
+
+// producer, MMA, epilogue warps (+ the extra gather warps)
 template <class P>
 constexpr int threads_of() {
-  return 64 + 32 * P::kEpiWarps;
+  return 64 + 32 * P::kEpiWarps + (P::kGather != 0 ? 32 * (kGatherWarps - 1) : 0);
 }
 
 template <class P>
@@ -1500,7 +1577,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<P>(), 1)
   const int ntiles = P::num_tiles(p, segs);
   const uint64_t limit = wait_limit_ns(p.hdr);
 
-  if (warp == 0) {
+  if (warp == 0 && P::kGather == 0) {
     if (lane == 0) {
       int slot = 0;
       uint32_t phase = 0;
@@ -1539,6 +1616,104 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<P>(), 1)
       // full barriers count both CTAs' bytes, and the odd CTA waits at the final cluster barrier
       // (bounded; a skipped fill never completes and ends this wait at its limit)
       if (rank == 0) drain_fills(full, kSlots, slot, phase, uses, limit);
+    }
+  } else if (warp == 0 || warp >= 2 + P::kEpiWarps) {
+    if constexpr (P::kGather != 0) {
+      // Gathered operand rows: four warps copy them, each 32 of the stage's 128 lines of 128 bytes,
+      // with eight tile::gather4 copies of four lines (lanes 0..7).  A single warp issuing all 32
+      // copies of a stage left the tensor pipe idle most of the time, and so did 16-byte cp.async
+      // copies from one or four warps; four warps of gather4 copies halve that loss.  Warp 0 also
+      // announces the pair's bytes, loads the other operand by TMA and forwards the slot's release
+      // to the odd CTA.  Each lane holds the token of one line, fetched one tile (kGather 1) or
+      // kAhead stages (kGather 2) ahead, and hands it round by shuffle.
+      static_assert(kSub == 1, "gathered loads fill one K block per slot");
+      constexpr int kAhead = 8;
+      const bool lead = warp == 0;
+      const int gw = lead ? 0 : warp - (1 + P::kEpiWarps);   // lines 32 gw .. 32 gw + 31
+      int slot = 0;
+      uint32_t phase = 0;
+      int uses = 0;
+      const int skip = pair == 0 ? *((volatile const int32_t*)&p.hdr->stall_fill_p1) - 1 : -1;
+      bool ok = true;
+      auto fill = [&](const Job& j, int kit, int tokv) {
+        int w = 1;
+        if (lane == 0) w = (*abort_flag == 0 && mbar_wait(&empty[slot], phase ^ 1, limit, abort_flag)) ? 1 : 0;
+        if (__shfl_sync(0xffffffffu, w, 0) == 0) {
+          if (lane == 0) {
+            record_error(p.hdr, MOE_ERR_TIMEOUT, kSiteGemmProducer);
+            *abort_flag = 1;
+          }
+          ok = false;
+          return;
+        }
+        if (uses != skip) {
+          uint8_t* st = stages + (size_t)slot * kSlotBytes;
+          if (lead && lane == 0) {
+            if (rank == 0) mbar_arrive_expect_tx(&full[slot], 2 * P::tx_bytes(j, kit, P::kStageBytes));
+            P::load(p, j, kit, st, cluster_addr(&full[slot], 0), rank);
+          }
+          // lane l < 8: lines 32 gw + 4 l .. + 3, whose tokens lanes 4 l .. 4 l + 3 hold
+          const GatherOp op = P::gather_op(p, j, kit, rank);
+          int4 r;
+          r.x = __shfl_sync(0xffffffffu, tokv, (4 * lane + 0) & 31);
+          r.y = __shfl_sync(0xffffffffu, tokv, (4 * lane + 1) & 31);
+          r.z = __shfl_sync(0xffffffffu, tokv, (4 * lane + 2) & 31);
+          r.w = __shfl_sync(0xffffffffu, tokv, (4 * lane + 3) & 31);
+          if (lane < 8)
+            tma_gather4_pair(smem_u32(st) + op.dst + (uint32_t)(32 * gw + 4 * lane) * 128u, op.map,
+                             cluster_addr(&full[slot], 0), gw < 2 ? op.col0 : op.col1, r);
+        }
+        if (lead && lane == 0 && rank == 0 && uses >= kSlots) mbar_arrive_cluster_relaxed(cluster_addr(&empty[slot], 1));
+        ++uses;
+        if (++slot == kSlots) {
+          slot = 0;
+          phase ^= 1;
+        }
+      };
+      if constexpr (P::kGather == 1) {
+        // a tile's rows are the same for all its K blocks: fetch the next tile's with this one
+        auto tile_tok = [&](int t) { return __ldg(P::gather_tok(p, P::job(p, segs, t), 0, rank) + 32 * gw + lane); };
+        int next = 0;
+        if (pair < ntiles) next = tile_tok(pair);
+        for (int t = pair; t < ntiles && ok; t += npairs) {
+          const Job j = P::job(p, segs, t);
+          const int tokv = next;
+          if (t + npairs < ntiles) next = tile_tok(t + npairs);
+          for (int kit = 0; kit < j.kiters && ok; ++kit) fill(j, kit, tokv);
+        }
+      } else {
+        // the K rows change every stage: a cursor over this pair's stages, in the order they are
+        // filled, keeps kAhead stages' tokens in flight (the two 64-column boxes share the rows)
+        int pt = pair, pkit = 0;
+        Job pj{};
+        if (pt < ntiles) pj = P::job(p, segs, pt);
+        auto ahead = [&]() {
+          while (pt < ntiles && pkit >= pj.kiters) {
+            pt += npairs;
+            pkit = 0;
+            if (pt < ntiles) pj = P::job(p, segs, pt);
+          }
+          if (pt >= ntiles) return 0;
+          const int v = __ldg(P::gather_tok(p, pj, pkit, rank) + 32 * (gw & 1) + lane);
+          ++pkit;
+          return v;
+        };
+        int ring[kAhead];
+#pragma unroll
+        for (int i = 0; i < kAhead; ++i) ring[i] = ahead();
+        for (int t = pair; t < ntiles && ok; t += npairs) {
+          const Job j = P::job(p, segs, t);
+          for (int kit = 0; kit < j.kiters && ok; ++kit) {
+            const int tokv = ring[0];
+#pragma unroll
+            for (int i = 0; i + 1 < kAhead; ++i) ring[i] = ring[i + 1];
+            ring[kAhead - 1] = ahead();
+            fill(j, kit, tokv);
+          }
+        }
+      }
+      // every load of the pair lands before either CTA's shared memory is released (as above)
+      if (lead && lane == 0 && rank == 0) drain_fills(full, kSlots, slot, phase, uses, limit);
     }
   } else if (warp == 1) {
     if (lane == 0 && rank == 0) {
@@ -1681,11 +1856,13 @@ cudaError_t launch_pair(const typename P::Params& p, cudaStream_t s) {
 
 namespace {
 
-template <bool kKeep>
+template <bool kKeep, bool kG>
 cudaError_t launch_gate_up(const Cfg& c, const Layout& L, const FfnFwdArgs& a, int keep, cudaStream_t s) {
   const uint64_t rows = (uint64_t)L.rows;
-  typename FwdGateUpT<kKeep>::Params p1{};
-  if (!map_2d(&p1.tmX, a.x_perm, c.d, rows, 64, 128) ||
+  typename FwdGateUpT<kKeep, kG>::Params p1{};
+  const bool mx = kG ? map_gather_rows(&p1.tmX, a.x_tok, c.d, c.T) : map_2d(&p1.tmX, a.x_perm, c.d, rows, 64, 128);
+  p1.tok = a.tok;
+  if (!mx ||
       !map_3d(&p1.tmWg, a.Wg, c.d, c.f, c.G, 64, 128) || !map_3d(&p1.tmWu, a.Wu, c.d, c.f, c.G, 64, 128) ||
       !map_2d(&p1.tmH, a.h, c.f, rows, 32, 32))
     return cudaErrorInvalidValue;
@@ -1699,21 +1876,25 @@ cudaError_t launch_gate_up(const Cfg& c, const Layout& L, const FfnFwdArgs& a, i
   p1.keep_rows = keep;
   p1.hdr = a.hdr;
   p1.tabs = a.tabs;
-  return launch_pair<FwdGateUpT<kKeep>>(p1, s);
+  return launch_pair<FwdGateUpT<kKeep, kG>>(p1, s);
 }
 
 // Weight gradients (bf16 operands in both the bf16 and the FP8 backward): dWg = dA^T X, dWu = dB^T X,
 // dWd = dY^T Hg per expert.
-cudaError_t launch_wgrad(const Cfg& c, const Layout& L, const uint16_t* dA, const uint16_t* dB, const uint16_t* Hg,
-                         const uint16_t* x_perm, const uint16_t* dy_perm, uint16_t* dWg, uint16_t* dWu,
-                         uint16_t* dWd, Hdr* hdr, const Tables* tabs, cudaStream_t s) {
+// x and dY rows from x_perm / dy_perm, or (tok non-null) gathered from x / dy in token order.
+template <bool kG>
+cudaError_t launch_wgrad_t(const Cfg& c, const Layout& L, const uint16_t* dA, const uint16_t* dB, const uint16_t* Hg,
+                           const uint16_t* x_rows, const uint16_t* dy_rows, const int32_t* tok, uint16_t* dWg,
+                           uint16_t* dWu, uint16_t* dWd, Hdr* hdr, const Tables* tabs, cudaStream_t s) {
   const uint64_t rows = (uint64_t)L.rows;
-  Wgrad::Params p4{};
-  if (!map_mn2(&p4.tmDA, dA, c.f, rows) || !map_mn2(&p4.tmDB, dB, c.f, rows) ||
-      !map_mn2(&p4.tmX, x_perm, c.d, rows) || !map_mn2(&p4.tmDY, dy_perm, c.d, rows) ||
+  typename WgradT<kG>::Params p4{};
+  const bool tok_side = kG ? map_gather_rows(&p4.tmX, x_rows, c.d, c.T) && map_gather_rows(&p4.tmDY, dy_rows, c.d, c.T)
+                           : map_mn2(&p4.tmX, x_rows, c.d, rows) && map_mn2(&p4.tmDY, dy_rows, c.d, rows);
+  if (!tok_side || !map_mn2(&p4.tmDA, dA, c.f, rows) || !map_mn2(&p4.tmDB, dB, c.f, rows) ||
       !map_mn2(&p4.tmHg, Hg, c.f, rows) || !map_3d(&p4.tmdWg, dWg, c.d, c.f, c.G, 32, 32) ||
       !map_3d(&p4.tmdWu, dWu, c.d, c.f, c.G, 32, 32) || !map_3d(&p4.tmdWd, dWd, c.f, c.d, c.G, 32, 32))
     return cudaErrorInvalidValue;
+  p4.tok = tok;
   p4.dWg = dWg;
   p4.dWu = dWu;
   p4.dWd = dWd;
@@ -1726,7 +1907,14 @@ cudaError_t launch_wgrad(const Cfg& c, const Layout& L, const uint16_t* dA, cons
   p4.tps = 2 * p4.mt_f * p4.nt_d + p4.mt_d * p4.nt_f;
   p4.hdr = hdr;
   p4.tabs = tabs;
-  return launch_pair<Wgrad>(p4, s);
+  return launch_pair<WgradT<kG>>(p4, s);
+}
+
+cudaError_t launch_wgrad(const Cfg& c, const Layout& L, const uint16_t* dA, const uint16_t* dB, const uint16_t* Hg,
+                         const uint16_t* x_rows, const uint16_t* dy_rows, const int32_t* tok, uint16_t* dWg,
+                         uint16_t* dWu, uint16_t* dWd, Hdr* hdr, const Tables* tabs, cudaStream_t s) {
+  return tok != nullptr ? launch_wgrad_t<true>(c, L, dA, dB, Hg, x_rows, dy_rows, tok, dWg, dWu, dWd, hdr, tabs, s)
+                        : launch_wgrad_t<false>(c, L, dA, dB, Hg, x_rows, dy_rows, tok, dWg, dWu, dWd, hdr, tabs, s);
 }
 
 }  // namespace
@@ -1734,7 +1922,9 @@ cudaError_t launch_wgrad(const Cfg& c, const Layout& L, const uint16_t* dA, cons
 cudaError_t launch_ffn_fwd(const Cfg& c, const Layout& L, const FfnFwdArgs& a, cudaStream_t s) {
   const uint64_t rows = (uint64_t)L.rows;
   const int keep = (int)std::min<int64_t>(c.keep, L.rows);
-  cudaError_t e = keep > 0 ? launch_gate_up<true>(c, L, a, keep, s) : launch_gate_up<false>(c, L, a, 0, s);
+  const bool g = a.tok != nullptr;   // x rows gathered from token order
+  cudaError_t e = keep > 0 ? (g ? launch_gate_up<true, true>(c, L, a, keep, s) : launch_gate_up<true, false>(c, L, a, keep, s))
+                           : (g ? launch_gate_up<false, true>(c, L, a, 0, s) : launch_gate_up<false, false>(c, L, a, 0, s));
   if (e != cudaSuccess) return e;
   FwdDown::Params p2{};
   if (!map_2d(&p2.tmH, a.h, c.f, rows, 64, 128) || !map_3d(&p2.tmWd, a.Wd, c.f, c.d, c.G, 64, 128) ||
@@ -1748,18 +1938,23 @@ cudaError_t launch_ffn_fwd(const Cfg& c, const Layout& L, const FfnFwdArgs& a, c
   return launch_pair<FwdDown>(p2, s);
 }
 
-cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, cudaStream_t s) {
+namespace {
+
+// dY and x rows from dy_perm / x_perm, or (kG) gathered from dy / x in token order through a.tok.
+template <bool kG>
+cudaError_t launch_ffn_bwd_t(const Cfg& c, const Layout& L, const FfnBwdArgs& a, cudaStream_t s) {
   const uint64_t rows = (uint64_t)L.rows;
-  BwdDh::Params p2{};
-  if (!map_2d(&p2.tmDY, a.dy_perm, c.d, rows, 64, 128) || !map_mn2_g(&p2.tmWdT, a.Wd, c.f, c.d, c.G) ||
-      !map_2d(&p2.tmDH, a.dh, c.f, rows, 32, 32))
+  typename BwdDhT<kG>::Params p2{};
+  const bool mdy = kG ? map_gather_rows(&p2.tmDY, a.dy_tok, c.d, c.T) : map_2d(&p2.tmDY, a.dy_perm, c.d, rows, 64, 128);
+  if (!mdy || !map_mn2_g(&p2.tmWdT, a.Wd, c.f, c.d, c.G) || !map_2d(&p2.tmDH, a.dh, c.f, rows, 32, 32))
     return cudaErrorInvalidValue;
+  p2.tok = a.tok;
   p2.f = c.f;
   p2.d = c.d;
   p2.nt = (c.f + 255) / 256;
   p2.hdr = a.hdr;
   p2.tabs = a.tabs;
-  cudaError_t e = launch_pair<BwdDh>(p2, s);
+  cudaError_t e = launch_pair<BwdDhT<kG>>(p2, s);
   if (e != cudaSuccess) return e;
   const int keep = (int)std::min<int64_t>(c.keep, L.rows);
   if (keep > 0) {   // rows whose a, b the forward kept: an element-wise SwiGLU backward
@@ -1767,11 +1962,13 @@ cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, c
     if (e != cudaSuccess) return e;
   }
 
-  BwdFused::Params p3{};
-  if (!map_2d(&p3.tmX, a.x_perm, c.d, rows, 64, 128) || !map_3d(&p3.tmWg, a.Wg, c.d, c.f, c.G, 64, 128) ||
+  typename BwdFusedT<kG>::Params p3{};
+  const bool mx = kG ? map_gather_rows(&p3.tmX, a.x_tok, c.d, c.T) : map_2d(&p3.tmX, a.x_perm, c.d, rows, 64, 128);
+  if (!mx || !map_3d(&p3.tmWg, a.Wg, c.d, c.f, c.G, 64, 128) ||
       !map_3d(&p3.tmWu, a.Wu, c.d, c.f, c.G, 64, 128) || !map_2d(&p3.tmDA, a.dA, c.f, rows, 32, 32) ||
       !map_2d(&p3.tmDB, a.dB, c.f, rows, 32, 32) || !map_2d(&p3.tmHg, a.Hg, c.f, rows, 32, 32))
     return cudaErrorInvalidValue;
+  p3.tok = a.tok;
   p3.DH = a.dh;
   p3.gate_of_prow = a.gate_of_prow;
   p3.dg_part = a.dg_part;
@@ -1782,10 +1979,11 @@ cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, c
   p3.keep_rows = keep;
   p3.hdr = a.hdr;
   p3.tabs = a.tabs;
-  e = launch_pair<BwdFused>(p3, s);
+  e = launch_pair<BwdFusedT<kG>>(p3, s);
   if (e != cudaSuccess) return e;
 
-  e = launch_wgrad(c, L, a.dA, a.dB, a.Hg, a.x_perm, a.dy_perm, a.dWg, a.dWu, a.dWd, a.hdr, a.tabs, s);
+  e = launch_wgrad(c, L, a.dA, a.dB, a.Hg, kG ? a.x_tok : a.x_perm, kG ? a.dy_tok : a.dy_perm, kG ? a.tok : nullptr,
+                   a.dWg, a.dWu, a.dWd, a.hdr, a.tabs, s);
   if (e != cudaSuccess) return e;
 
   DgradX::Params p5{};
@@ -1799,6 +1997,12 @@ cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, c
   p5.hdr = a.hdr;
   p5.tabs = a.tabs;
   return launch_pair<DgradX>(p5, s);
+}
+
+}  // namespace
+
+cudaError_t launch_ffn_bwd(const Cfg& c, const Layout& L, const FfnBwdArgs& a, cudaStream_t s) {
+  return a.tok != nullptr ? launch_ffn_bwd_t<true>(c, L, a, s) : launch_ffn_bwd_t<false>(c, L, a, s);
 }
 
 cudaError_t launch_gate_up_fp8(const Cfg& c, const Layout& L, const GateUpFp8Args& a, cudaStream_t s) {
@@ -1873,7 +2077,7 @@ cudaError_t launch_ffn_bwd_fp8(const Cfg& c, const Layout& L, const FfnBwd8Args&
   e = launch_pair<BwdFused8>(p2, s);
   if (e != cudaSuccess) return e;
 
-  e = launch_wgrad(c, L, a.dA, a.dB, a.Hg, a.x_perm, a.dy_perm, a.dWg, a.dWu, a.dWd, a.hdr, a.tabs, s);
+  e = launch_wgrad(c, L, a.dA, a.dB, a.Hg, a.x_perm, a.dy_perm, nullptr, a.dWg, a.dWu, a.dWd, a.hdr, a.tabs, s);
   if (e != cudaSuccess) return e;
   e = launch_quantize_rows2_e4m3(a.dA, c.f, a.dB, c.f, (int64_t)rows, a.dab8, a.dabs, s, a.tabs);
   if (e != cudaSuccess) return e;

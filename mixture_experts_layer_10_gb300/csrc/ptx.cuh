@@ -233,6 +233,19 @@ __device__ __forceinline__ void tma_load_4d_pair(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// TMA gather of four rows (tile::gather4, 2D): rows r.x .. r.w of the tensor, one box width of
+// columns from c0, landing as four consecutive 128-byte box rows at dst (the layout -- swizzle
+// included -- of a box of four rows there).  The tensor map's box is one row high.  Completion is
+// counted on the mbarrier at shared::cluster address `cbar`, which may be the peer CTA's.
+__device__ __forceinline__ void tma_gather4_pair(uint32_t dst, const CUtensorMap* map, uint32_t cbar, int32_t c0,
+                                                 int4 r) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(cbar), "r"(c0), "r"(r.x), "r"(r.y), "r"(r.z), "r"(r.w)
+      : "memory");
+}
+
 // ---------------------------------------------------------------------------------------------
 // tcgen05: TMEM, MMA, commit, loads
 // ---------------------------------------------------------------------------------------------

@@ -112,4 +112,10 @@ inline bool map_3d(CUtensorMap* m, const void* base, uint64_t width, uint64_t ro
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Rows gathered by tile::gather4 from [rows, width] bf16 (token order): a box one row high and 64
+// columns wide, 128-byte swizzle, so four gathered rows land like four rows of a 64-wide box.
+inline bool map_gather_rows(CUtensorMap* m, const void* base, uint64_t width, uint64_t rows) {
+  return map_2d(m, base, width, rows, 64, 1);
+}
+
 }  // namespace moe

@@ -52,6 +52,7 @@ def test_workspace_size_and_rows():
     dict(T=16, d=128, f=96, E=8, k=2), dict(T=16, d=128, f=256, E=8, k=9),
     dict(T=16, d=128, f=256, E=300, k=2), dict(T=16, d=128, f=256, E=8, k=2, S=9),
     dict(T=16, d=128, f=256, E=8, k=0), dict(T=16, d=128, f=256, E=8, k=2, keep_rows=-1),
+    dict(T=16, d=128, f=256, E=8, k=2, gather_in_gemm=2), dict(T=16, d=128, f=256, E=8, k=2, gather_in_gemm=-1),
 ])
 def test_invalid_config_rejected(lib, bad):
     c = moe.config(**bad)

@@ -167,3 +167,40 @@ def test_router_backward_all_tokens(full, moe):
     check_close("dlogits", from_dev(dlogits), dl_ref)
     check_close("dW_r", from_dev(dW_r), dWr_ref)
     check_close("db_r", from_dev(db_r), db_ref)
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+def test_gather_in_gemm_bitwise_full_size(moe, name):
+    """Gathered operand loads at full size, in the bench's launch configuration: every output of
+    moe_layer_fwd / moe_layer_bwd equals the default path's bit for bit (finite inputs)."""
+    cfg = synth.CONFIGS[name]
+    inp = synth.make_inputs(cfg, seed=0)
+    T, d, f, E, S = cfg["T"], cfg["d"], cfg["f"], cfg["E"], cfg["S"]
+    G = E + S
+    dev = dict(x=to_dev_bf16(inp["x"]), W_r=to_dev(inp["W_r"]),
+               b_r=to_dev(inp["b_r"]) if inp["b_r"] is not None else None,
+               Wg=to_dev_bf16(inp["W_gate"]), Wu=to_dev_bf16(inp["W_up"]), Wd=to_dev_bf16(inp["W_down"]),
+               dy=to_dev_bf16(inp["dy"]))
+    res = []
+    for gig in (0, 1):
+        mc = moe.config_from(dict(cfg, gather_in_gemm=gig))
+        buf = moe.Buffers.allocate(mc)
+        out = dict(y=torch.empty(T, d, dtype=torch.bfloat16, device="cuda"),
+                   dx=torch.empty(T, d, dtype=torch.bfloat16, device="cuda"),
+                   dW_r=torch.empty(d, E, dtype=torch.float32, device="cuda"),
+                   db_r=torch.empty(E, dtype=torch.float32, device="cuda"),
+                   dWg=torch.empty(G, f, d, dtype=torch.bfloat16, device="cuda"),
+                   dWu=torch.empty(G, f, d, dtype=torch.bfloat16, device="cuda"),
+                   dWd=torch.empty(G, d, f, dtype=torch.bfloat16, device="cuda"))
+        moe.moe_layer_fwd(mc, dev["x"], dev["W_r"], dev["b_r"], dev["Wg"], dev["Wu"], dev["Wd"], out["y"], buf.saved,
+                          buf.ws)
+        moe.moe_layer_bwd(mc, dev["x"], dev["W_r"], dev["b_r"], dev["Wg"], dev["Wu"], dev["Wd"], buf.saved, dev["dy"],
+                          out["dx"], out["dW_r"], out["db_r"], out["dWg"], out["dWu"], out["dWd"], buf.ws)
+        assert moe.moe_check_error(buf.ws) == 0
+        out["saved"] = buf.saved
+        res.append(out)
+        del buf
+    for key in res[0]:
+        assert torch.equal(res[0][key].view(torch.uint8), res[1][key].view(torch.uint8)), key
+    del res, dev
+    torch.cuda.empty_cache()

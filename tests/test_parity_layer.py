@@ -182,3 +182,26 @@ def test_layer_is_deterministic(moe, name):
     b, _ = run_layer(moe, c, inp, buf)
     for key in a:
         assert torch.equal(a[key].view(torch.uint8), b[key].view(torch.uint8)), key
+
+
+# Gathered operand loads (gather_in_gemm = 1): the GEMMs gather x and dy from token order instead of
+# reading x_perm / dY_perm.  For finite inputs every output equals the default path's bit for bit: a
+# pad row reads token 0's row instead of zeros, and its zero gate zeroes every term it feeds.
+@pytest.mark.parametrize("name,keep", [(n, 0) for n in CASES] + [("ragged_mixtral", 256), ("deepseek_small", -1),
+                                                                 ("gptoss_small", 512)])
+def test_gather_in_gemm_bitwise(moe, name, keep):
+    c, inp, _ = case(name)
+    c = dict(c)
+    c["keep_rows"] = moe.moe_perm_rows(moe.config_from(c)) if keep < 0 else keep
+    a, buf = run_layer(moe, c, inp)
+    b, _ = run_layer(moe, dict(c, gather_in_gemm=1), inp)
+    for key in a:
+        assert torch.equal(a[key].view(torch.uint8), b[key].view(torch.uint8)), key
+
+
+@pytest.mark.parametrize("name", ["ragged_mixtral", "deepseek_small", "gptoss_small"])
+def test_gather_in_gemm_against_oracle(moe, name):
+    c, inp, L = case(name)
+    c = dict(c, gather_in_gemm=1)
+    out, buf = run_layer(moe, c, inp)
+    check_layer(moe, c, inp, L, out, buf)
