@@ -70,6 +70,9 @@ struct PolicyDefaults {
   // stage the same way, as two 64-column boxes.  Either way a CTA's stage takes 32 tile::gather4
   // copies (four 128-byte lines each) from kGatherWarps warps, and one TMA box for the other operand.
   static constexpr int kGather = 0;
+  // Tiles numbered from num_tiles on, zero_tiles() of them, that only the epilogue stores (CTA-pair
+  // problems): epilogue_zero of each, by the pair's epilogue warps while they wait for an MMA tile.
+  static constexpr bool kZeroTiles = false;
   // TMA bytes that complete one stage at k-iteration kit
   __device__ static uint32_t tx_bytes(const Job&, int, uint32_t stage_bytes) { return stage_bytes; }
   // a stateful policy keeps per-lane epilogue state across the jobs of one CTA (epilogue_s)
@@ -836,15 +839,17 @@ struct DgradX : PairDefaults {
 // Weight gradients, K = the expert's rows: dWg = dA^T X and dWu = dB^T X (M = d_ff, N = d_model),
 // dWd = dY^T Hg (M = d_model, N = d_ff).  A and B are row-major activations read MN-major: two
 // 64 x 64 boxes each per CTA and stage, fetched by one copy (map_mn2; two copies per operand held
-// the kernel at 73% of the MMA rate per SM cycle, one copy reaches 86%).  Tiles go expert by expert, largest first; inside an
-// expert the d_model-wide operand (X, or dY) is the one cycled through, so the pairs at work keep
-// all of it and a few d_ff-wide column blocks in L2.
+// the kernel at 73% of the MMA rate per SM cycle, one copy reaches 86%).  Tiles go expert by
+// expert, largest first (experts with no rows spread among them, tile_of); inside an expert the
+// d_model-wide operand (X, or dY) is the one cycled through, so the pairs at work keep all of it
+// and a few d_ff-wide column blocks in L2.
 template <bool kG>
 struct WgradT : PairDefaults {
   static constexpr int kId = kKWgrad;
   static constexpr int kEpiWarps = 4;
   static constexpr uint32_t kIdesc = idesc_bf16(kPairM, 256, true, true);
   static constexpr int kGather = kG ? 2 : 0;
+  static constexpr bool kZeroTiles = true;
   struct Params {
     CUtensorMap tmDA, tmDB, tmX, tmDY, tmHg;   // all [rows, width] as 64-column block pairs (map_mn2);
                                                // gathered: tmX, tmDY are x, dy in token order, one-row boxes
@@ -856,7 +861,20 @@ struct WgradT : PairDefaults {
     Hdr* hdr;
     const Tables* tabs;
   };
-  __device__ static int num_tiles(const Params& p, const SegSmem& s) { return s.G * p.tps; }
+  // The MMA tiles are those of experts with rows, largest first (seg_order).  The tiles of experts
+  // with none -- a zero gradient each, no MMA -- come after them in the same numbering; the
+  // epilogue warps store them in between their MMA tiles (zero_tiles).
+  __device__ static int nonempty(const SegSmem& s) {
+    int lo = 0, hi = s.G;   // first position of seg_order whose segment is empty
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      const int g = s.seg_order[mid];
+      if (s.poff[g + 1] > s.poff[g]) lo = mid + 1; else hi = mid;
+    }
+    return lo;
+  }
+  __device__ static int num_tiles(const Params& p, const SegSmem& s) { return nonempty(s) * p.tps; }
+  __device__ static int zero_tiles(const Params& p, const SegSmem& s) { return (s.G - nonempty(s)) * p.tps; }
   __device__ static int mma_kiters(const Params& p, const SegSmem& s, int t) {
     const int g = s.seg_order[t / p.tps];
     return (s.poff[g + 1] - s.poff[g]) / kBK;
@@ -916,14 +934,6 @@ struct WgradT : PairDefaults {
       umma_bf16_pair(dt, sdesc_mnmajor(sa + kk * 2048, kBox), sdesc_mnmajor(sa + 2 * kBox + kk * 2048, kBox),
                      kIdesc, (kit | kk) != 0);
   }
-  __device__ static uint16_t* out_row(const Params& p, const Job& j, int row, int& ncols, bool& ok) {
-    const int M = j.sub == 2 ? p.d : p.f;
-    ncols = j.sub == 2 ? p.f : p.d;
-    const int m = j.m0 + row;
-    ok = m < M;
-    uint16_t* W = j.sub == 0 ? p.dWg : (j.sub == 1 ? p.dWu : p.dWd);
-    return W + ((size_t)j.seg * M + (ok ? m : 0)) * ncols;
-  }
   // Four epilogue warps, one per TMEM lane quarter, 256 columns each (eight warps sharing the
   // quarters measured 3% fewer MMA cycles per SM cycle).  A warp whose 32 rows all lie past M
   // (the last pair tile of a d_ff or d_model not a multiple of 256) stores nothing; boxes that
@@ -950,14 +960,19 @@ struct WgradT : PairDefaults {
       store_box_3d(map, box, lane, j.n0 + c, y, j.seg);
     }
   }
-  // An expert that received no rows has a zero gradient.
+  // An expert that received no rows has a zero gradient.  The warp stores its 32 rows of the tile
+  // one row at a time, 16 bytes a lane: 256 columns, whole lines per instruction.
   __device__ static void epilogue_zero(const Params& p, const Job& j, int row, int) {
-    int ncols;
-    bool ok;
-    uint16_t* base = out_row(p, j, row, ncols, ok);
-    if (!ok) return;
-    for (int c = 0; c < 256 && j.n0 + c < ncols; c += 8)
-      *reinterpret_cast<uint4*>(base + j.n0 + c) = make_uint4(0, 0, 0, 0);
+    const int lane = row & 31;
+    const int M = j.sub == 2 ? p.d : p.f;
+    const int ncols = j.sub == 2 ? p.f : p.d;
+    uint16_t* W = j.sub == 0 ? p.dWg : (j.sub == 1 ? p.dWu : p.dWd);
+    const int c = j.n0 + 8 * lane;
+    for (int i = 0; i < 32; ++i) {
+      const int m = j.m0 + (row & ~31) + i;
+      if (m >= M) break;
+      if (c < ncols) *reinterpret_cast<uint4*>(W + ((size_t)j.seg * M + m) * ncols + c) = make_uint4(0, 0, 0, 0);
+    }
   }
 };
 using Wgrad = WgradT<false>;
@@ -1775,12 +1790,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<P>(), 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     int seq = 0;
+    // epilogue-only tiles of this pair (pair, pair + npairs, ...), stored while an MMA tile is pending
+    int zt = pair;
+    int nzt = 0;
+    if constexpr (P::kZeroTiles) nzt = P::zero_tiles(p, segs);
+    auto zero_tile = [&]() {
+      Job j = P::job(p, segs, ntiles + zt);
+      j.m0 += kBM * rank;
+      if (part == 0) P::epilogue_zero(p, j, row, part);
+      zt += npairs;
+    };
     for (int t = pair; t < ntiles; t += npairs) {
       Job j = P::job(p, segs, t);
       j.m0 += kBM * rank;   // this CTA's 128 rows of the pair tile
       if (j.kiters == 0) {
         if (part == 0) P::epilogue_zero(p, j, row, part);
         continue;
+      }
+      if constexpr (P::kZeroTiles) {   // one decision per warp: its tcgen05 loads below are warp-wide
+        while (zt < nzt) {
+          const int ready = lane == 0 ? (int)mbar_try_wait(&tfull[acc], acc_phase) : 0;
+          if (__shfl_sync(0xffffffffu, ready, 0)) break;
+          zero_tile();
+        }
       }
       if (!mbar_wait_idle(&tfull[acc], acc_phase, limit, abort_flag)) {
         record_error(p.hdr, MOE_ERR_TIMEOUT, kSiteGemmEpilogue);
@@ -1798,6 +1830,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<P>(), 1)
         acc = 0;
         acc_phase ^= 1;
       }
+    }
+    if constexpr (P::kZeroTiles) {
+      while (zt < nzt && !*abort_flag) zero_tile();
     }
     if (lane == 0) bulk_wait_all();   // this warp's output stores have landed
   }

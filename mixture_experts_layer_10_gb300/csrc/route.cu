@@ -346,22 +346,28 @@ __global__ void __launch_bounds__(kThreads) router_dlogits_kernel(RouterBwdArgs 
   }
 }
 
-// Router backward, part 3: fixed-order sums of the dW_r and db partials.
-__global__ void router_reduce_kernel(RouterBwdArgs a, int d, int E, int nsplit, int nblk) {
-  const size_t n = (size_t)d * E;
-  for (size_t p = blockIdx.x * (size_t)blockDim.x + threadIdx.x; p < n + E;
-       p += (size_t)gridDim.x * blockDim.x) {
-    if (p < n) {
+// Router backward, part 3: fixed-order sums of the dW_r and db partials.  The first dw_blocks
+// blocks sum dW_r element by element over the splits; then one warp per expert sums its db
+// partials, lane l taking blocks l, l + 32, ... and a shuffle tree of fixed shape joining the lanes
+// (the partials of the bias run to thousands of blocks: a single thread's chain would dominate).
+__global__ void router_reduce_kernel(RouterBwdArgs a, int d, int E, int nsplit, int nblk, int dw_blocks) {
+  if ((int)blockIdx.x < dw_blocks) {
+    const size_t n = (size_t)d * E;
+    for (size_t p = blockIdx.x * (size_t)blockDim.x + threadIdx.x; p < n; p += (size_t)dw_blocks * blockDim.x) {
       float v = 0.f;
       for (int s = 0; s < nsplit; ++s) v += a.dwr_part[(size_t)s * n + p];
       a.dW_r[p] = v;
-    } else if (a.db_r != nullptr) {
-      const int e = (int)(p - n);
-      float v = 0.f;
-      for (int b = 0; b < nblk; ++b) v += a.db_part[(size_t)b * E + e];
-      a.db_r[e] = v;
     }
+    return;
   }
+  const int e = ((int)blockIdx.x - dw_blocks) * (int)(blockDim.x >> 5) + (int)(threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (a.db_r == nullptr || e >= E) return;
+  float v = 0.f;
+  for (int b = lane; b < nblk; b += 32) v += a.db_part[(size_t)b * E + e];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_down_sync(0xffffffffu, v, o);
+  if (lane == 0) a.db_r[e] = v;
 }
 
 int bucket_of(int E) {
@@ -473,10 +479,11 @@ cudaError_t launch_router_dlogits(const Cfg& c, const Layout& L, const RouterBwd
 }
 
 cudaError_t launch_router_reduce(const Cfg& c, const Layout& L, const RouterBwdArgs& a, cudaStream_t s) {
-  const size_t n = (size_t)c.d * c.E + c.E;
-  const int blocks = (int)std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 4);
+  const size_t n = (size_t)c.d * c.E;
+  const int dw_blocks = (int)std::max<size_t>(1, std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 4));
+  const int db_blocks = a.db_r != nullptr ? (c.E + 7) / 8 : 0;   // 8 warps, one expert each
   prof_mark(kKRouterReduce, s, true);
-  router_reduce_kernel<<<blocks, 256, 0, s>>>(a, c.d, c.E, L.nsplit_dwr, L.nblk_router);
+  router_reduce_kernel<<<dw_blocks + db_blocks, 256, 0, s>>>(a, c.d, c.E, L.nsplit_dwr, L.nblk_router, dw_blocks);
   prof_mark(kKRouterReduce, s, false);
   return cudaGetLastError();
 }
