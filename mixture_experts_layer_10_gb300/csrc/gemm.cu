@@ -1107,14 +1107,8 @@ struct RouterDx : PolicyDefaults {
 // over all 3 d_model / 16 steps drifts by ~1e-5 of the logit at d_model = 2048.  K is therefore cut
 // into chunks of kChunkKits 64-wide blocks; each chunk starts two fresh accumulators, one for the hi
 // products (16 MMA steps) and one for the mid + lo products (2^8 smaller, so their rounding is
-// negligible), and the epilogue adds both into fp32 registers.  A job is one (256-token pair tile,
-// K chunk); the chunks of a tile run on one CTA pair, in order.  M = 256 tokens (128 per CTA), and
-// the pair splits B: the even CTA holds the hi part, the odd the mid part (one N = 256 MMA), and
-// each holds 64 rows of the lo part (N = 128).  A CTA's stage is then 40 KB (x 16, W 24) against
-// 64 KB when one CTA held all three parts, and each W_r row read from L2 serves 256 tokens
-// (10-17% faster than one CTA per 128-token tile at E = 128).  A chunk's MMAs run at the tensor-core
-// rate; at E = 128 the kernel is bound by the epilogue of a tile's last chunk (softmax and top-k over
-// 128 experts, one token per lane: about 16 us a tile, measured), which holds its accumulator.
+// negligible), and the epilogue adds both into fp32 registers.  A job is one (128-token tile, K
+// chunk); the chunks of a tile run on one CTA, in order.  M = 128 tokens, N = Ep (64 or 128).
 // After the last chunk the epilogue stores each lane's sums into the hi columns of the accumulator
 // it still holds, then reads its logits back in 32-column pieces:
 //   forward (kBwd = false): online softmax (running max and rescaled sum of exp) and the top-k
@@ -1127,19 +1121,18 @@ struct RouterDx : PolicyDefaults {
 constexpr int kRouterTopK = 8;
 
 template <bool kBwd>
-struct RouterLogits : PairDefaults {
+struct RouterLogits : PolicyDefaults {
   static constexpr int kId = kBwd ? kKRouterDlogits : kKRoute;
   static constexpr int kEpiWarps = 4;
-  static constexpr int kStages = 5;
-  static constexpr uint32_t kStageBytes = 2 * kTileA + kTileA / 2;   // x tile, hi or mid part, half of lo
-  static constexpr uint32_t kEpiWarpBytes = 0;
+  static constexpr int kStages = 3;
+  static constexpr uint32_t kStageBytes = 4 * kTileA;   // x tile + three W_r parts (128 rows each)
   static constexpr int kAccCols = 256;                   // hi products, then mid + lo at +128
   static constexpr int kAccBufs = 2;
   static constexpr int kTmemCols = 512;
   static constexpr int kChunkKits = 4;                   // 256 of K per chunk
   static constexpr bool kStateful = true;
   struct Params {
-    CUtensorMap tmX, tmW, tmWlo;   // tmW: 128-row boxes of a part; tmWlo: 64-row boxes
+    CUtensorMap tmX, tmW;
     const float* b_r;
     int T, d, E, Ep, k, renorm, mt, nch;
     int32_t* idx;            // forward output / backward input
@@ -1152,55 +1145,50 @@ struct RouterLogits : PairDefaults {
     Hdr* hdr;
     const Tables* tabs;
   };
-  // pair q runs pair tiles q, q + npairs, ... and each tile's nch chunks back to back
+  // CTA b runs tiles b, b + grid, ... and each tile's nch chunks back to back
   __device__ static int num_tiles(const Params& p, const SegSmem&) {
-    const int g = (int)(gridDim.x >> 1);
-    const int mt2 = (p.mt + 1) >> 1;
-    return g * ((mt2 + g - 1) / g) * p.nch;
+    const int g = (int)gridDim.x;
+    return g * ((p.mt + g - 1) / g) * p.nch;
   }
   __device__ static Job job(const Params& p, const SegSmem&, int t) {
-    const int g = (int)(gridDim.x >> 1);
+    const int g = (int)gridDim.x;
     const int i = t / g;
     const int tile = (t - i * g) + (i / p.nch) * g;
     const int ch = i % p.nch;
     Job j;
-    j.m0 = tile * kPairM;
+    j.m0 = tile * kBM;
     j.n0 = 0;
     j.seg = 0;
     j.sub = ch;
     j.kbase = ch * kChunkKits;
-    j.kiters = tile < (p.mt + 1) >> 1 ? min(kChunkKits, p.d / kBK - j.kbase) : 0;
+    j.kiters = tile < p.mt ? min(kChunkKits, p.d / kBK - j.kbase) : 0;
+    j.idesc = idesc_bf16(128, p.Ep, false, false);
     return j;
   }
-  __device__ static int mma_kiters(const Params& p, const SegSmem& s, int t) { return job(p, s, t).kiters; }
-  __device__ static void prefetch(const Params& p) {
-    tma_prefetch(&p.tmX); tma_prefetch(&p.tmW); tma_prefetch(&p.tmWlo);
-  }
-  // this CTA's 128 tokens, its part of hi | mid (hi on the even CTA), its 64 rows of lo; rows past
-  // Ep (and past T) are TMA zero fill
-  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint32_t cbar, int rank) {
+  __device__ static void prefetch(const Params& p) { tma_prefetch(&p.tmX); tma_prefetch(&p.tmW); }
+  __device__ static void load(const Params& p, const Job& j, int kit, uint8_t* st, uint64_t* bar) {
     const int kx = (j.kbase + kit) * kBK;
-    tma_load_2d_pair(st, &p.tmX, cbar, kx, j.m0 + kBM * rank);
-    tma_load_3d_pair(st + kTileA, &p.tmW, cbar, kx, 0, rank);
-    tma_load_3d_pair(st + 2 * kTileA, &p.tmWlo, cbar, kx, 64 * rank, 2);
+    tma_load_2d(st, &p.tmX, bar, kx, j.m0);
+#pragma unroll
+    for (int q = 0; q < 3; ++q) tma_load_3d(st + (1 + q) * kTileA, &p.tmW, bar, kx, 0, q);
   }
-  // One N = 256 MMA over hi | mid lands hi in columns [0, Ep) and mid in [128, 128 + Ep); an
-  // N = 128 MMA over lo then accumulates onto mid.  Two MMAs per 16-deep step instead of three.
-  static constexpr uint32_t kIdescHiMid = idesc_bf16(kPairM, 256, false, false);
-  static constexpr uint32_t kIdescLo = idesc_bf16(kPairM, 128, false, false);
-  __device__ static void mma(const Job&, int kit, uint32_t sa, uint32_t dt, int) {
+  // The hi and mid parts sit in adjacent 128-row slots (rows past Ep are TMA zero fill), so one
+  // N = 256 MMA covers both and lands hi in columns [0, Ep) and mid in [128, 128 + Ep); lo then
+  // accumulates onto mid.  Two MMAs per 16-deep step instead of three: the router is bound by MMA
+  // issue, not by the tensor pipe.
+  static constexpr uint32_t kIdescHiMid = idesc_bf16(128, 256, false, false);
+  __device__ static void mma(const Job& j, int kit, uint32_t sa, uint32_t dt, int) {
 #pragma unroll
     for (int kk = 0; kk < kBK / 16; ++kk) {
       const uint64_t da = sdesc_kmajor(sa + kk * 32);
       const bool acc = (kit | kk) != 0;
-      umma_bf16_pair(dt, da, sdesc_kmajor(sa + kTileA + kk * 32), kIdescHiMid, acc);
-      umma_bf16_pair(dt + 128, da, sdesc_kmajor(sa + 2 * kTileA + kk * 32), kIdescLo, true);
+      umma_bf16(dt, da, sdesc_kmajor(sa + kTileA + kk * 32), kIdescHiMid, acc);
+      umma_bf16(dt + 128, da, sdesc_kmajor(sa + 3 * kTileA + kk * 32), j.idesc, true);
     }
   }
   struct EpiState { float l[128]; };   // this lane's running sums over the chunks so far
   __device__ static void epilogue_s(const Params& p, const Job& j, uint32_t ta, int row, int, int,
                                     EpiState& st, uint32_t) {
-    if (j.m0 >= p.T) return;   // the odd CTA's half of a last pair tile past T: nothing to do
     const bool first = j.sub == 0;
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
@@ -1799,7 +1787,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<P>(), 1)
     const int part = (warp - 2) >> 2;  // column share when two warps serve one quarter
     const int row = q * 32 + lane;
     uint8_t* ebuf = epi + (size_t)(warp - 2) * P::kEpiWarpBytes;
-    typename P::EpiState es;   // stateful problems: per-lane state across this CTA's jobs
     int acc = 0;
     uint32_t acc_phase = 0;
     int seq = 0;
@@ -1833,12 +1820,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<P>(), 1)
         break;
       }
       tc_fence_after();
-      if constexpr (P::kStateful)
-        P::epilogue_s(p, j, tmem_base + (uint32_t)(acc * P::kAccCols) + ((uint32_t)(q * 32) << 16), row, part,
-                      seq, es, tmem_base + ((uint32_t)(q * 32) << 16));
-      else
-        P::epilogue(p, j, tmem_base + (uint32_t)(acc * P::kAccCols) + ((uint32_t)(q * 32) << 16), row, part,
-                    seq, ebuf);
+      P::epilogue(p, j, tmem_base + (uint32_t)(acc * P::kAccCols) + ((uint32_t)(q * 32) << 16), row, part,
+                  seq, ebuf);
       ++seq;
       tc_fence_before();
       __syncwarp();
@@ -2170,8 +2153,7 @@ template <bool kBwd>
 cudaError_t launch_router_tc(const Cfg& c, const Layout& L, const RouterTcArgs& a, cudaStream_t s) {
   using P = RouterLogits<kBwd>;
   typename P::Params p{};
-  if (!map_2d(&p.tmX, a.x, c.d, c.T, 64, 128) || !map_3d(&p.tmW, a.wr3, c.d, L.Ep, 3, 64, 128) ||
-      !map_3d(&p.tmWlo, a.wr3, c.d, L.Ep, 3, 64, 64))
+  if (!map_2d(&p.tmX, a.x, c.d, c.T, 64, 128) || !map_3d(&p.tmW, a.wr3, c.d, L.Ep, 3, 64, 128))
     return cudaErrorInvalidValue;
   p.b_r = a.b_r;
   p.T = c.T;
@@ -2191,7 +2173,7 @@ cudaError_t launch_router_tc(const Cfg& c, const Layout& L, const RouterTcArgs& 
   p.db_part = a.db_part;
   p.hdr = a.hdr;
   p.tabs = a.tabs;
-  return launch_pair<P>(p, s);
+  return launch<P>(p, s);
 }
 
 cudaError_t launch_route_tc(const Cfg& c, const Layout& L, const RouterTcArgs& a, cudaStream_t s) {
