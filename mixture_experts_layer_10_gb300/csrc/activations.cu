@@ -17,6 +17,7 @@
 #include <cuda_fp8.h>
 
 #include "common.cuh"
+#include "e4m3.cuh"
 
 namespace moe {
 namespace {
@@ -81,32 +82,6 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) swiglu_bwd_kept_kernel(
 // (tb->total_rows) are skipped.
 constexpr int kQuantV = 8;
 
-// v / scale rounded to nearest in fp32, from the row's reciprocal y = RN(1 / scale): q0 = RN(v y) is
-// within one ulp of the quotient, the residual v - q0 scale is exact in one fma, and RN(q0 + r y) is
-// the correctly rounded quotient (Markstein's theorem on the final correction of a division; it
-// needs no underflow or overflow in the steps, which holds for scales in [2^-80, 2^80] whenever the
-// quotient is large enough to give a nonzero e4m3 code; rows with other scales use the IEEE
-// division).  A zero keeps its sign.
-__device__ __forceinline__ float div_by_scale(float v, float scale, float y) {
-  const float q0 = v * y;
-  const float r = fmaf(-q0, scale, v);
-  return copysignf(fmaf(r, y, q0), v);
-}
-
-template <bool kRecip>
-__device__ __forceinline__ uint2 encode8_e4m3(const uint4& u, float scale, float y) {
-  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
-  uint32_t c[4];
-#pragma unroll
-  for (int m = 0; m < 4; ++m) {
-    const float lo = bf16_lo(w[m]), hi = bf16_hi(w[m]);
-    const float2 f2 = kRecip ? make_float2(div_by_scale(lo, scale, y), div_by_scale(hi, scale, y))
-                             : make_float2(__fdiv_rn(lo, scale), __fdiv_rn(hi, scale));
-    c[m] = (uint32_t)__nv_cvt_float2_to_fp8x2(f2, __NV_SATFINITE, __NV_E4M3);   // .x in the low byte
-  }
-  return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-}
-
 template <int kThreads>
 __global__ void __launch_bounds__(kThreads) quantize_rows_e4m3_kernel(const uint16_t* __restrict__ src, int cols1,
                                                                       const uint16_t* __restrict__ src2, int cols2,
@@ -131,9 +106,7 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_e4m3_kernel(const uint
       const int q = threadIdx.x + i * kThreads;
       if (q < nvec) {
         v[i] = q < nvec1 ? row[q] : row2[q - nvec1];
-        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-        for (int m = 0; m < 4; ++m) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[m])), fabsf(bf16_hi(w[m]))));
+        amax = fmaxf(amax, amax8_bf16(v[i]));
       }
     }
 #pragma unroll
@@ -144,10 +117,10 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_e4m3_kernel(const uint
 #pragma unroll
       for (int w = 0; w < kWarps; ++w) amax = fmaxf(amax, part[buf][w]);
     }
-    const float scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    const float scale = e4m3_row_scale(amax);
     if (threadIdx.x == 0) scales[r] = scale;
     uint2* out = reinterpret_cast<uint2*>(codes + r * cols);
-    if (scale >= 0x1p-80f && scale <= 0x1p80f) {   // the same branch for the whole block
+    if (e4m3_recip_ok(scale)) {   // the same branch for the whole block
       const float y = __frcp_rn(scale);
 #pragma unroll
       for (int i = 0; i < kQuantV; ++i) {
@@ -211,10 +184,10 @@ __global__ void col_encode_kernel(const uint16_t* __restrict__ top, const uint16
   float scale = 1.f, y = 1.f;
   if (c < cols) {
     const float amax = __uint_as_float(amax_bits[(size_t)g * cols + c]);
-    scale = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    scale = e4m3_row_scale(amax);
     y = __frcp_rn(scale);
   }
-  const bool recip = scale >= 0x1p-80f && scale <= 0x1p80f;
+  const bool recip = e4m3_recip_ok(scale);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int rr = 2 * ty + 16 * k;   // this thread's row pair within the tile
@@ -250,7 +223,7 @@ __global__ void col_encode_kernel(const uint16_t* __restrict__ top, const uint16
 __global__ void col_scales_kernel(const uint32_t* __restrict__ amax_bits, float* __restrict__ scales, int64_t n) {
   for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
     const float amax = __uint_as_float(amax_bits[i]);
-    scales[i] = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+    scales[i] = e4m3_row_scale(amax);
   }
 }
 

@@ -339,10 +339,33 @@ moe_status_t do_ffn_bwd(const Cfg& c, const Ws& w, const uint16_t* x_perm, const
 // The FP8 expert-FFN backward on the rows moe_dispatch laid out (x_perm, dy_perm, gates per row).
 // Scratch: the x and dY rows' codes share buf_d1 (free until dgrad x writes dx_perm there), their
 // scales and the [dA | dB] rows' scales go to fp8s, the [dA | dB] codes to buf_f3 once dh' is used.
+// The FP8 backward's dispatch: the queues from the saved idx, the bf16 x and dY rows (the weight
+// gradients' operands) and, from the same pass over each token's rows, their e4m3 codes and row
+// scales (the dh' and recompute GEMMs' operands): into O/dX's buffer and the FP8 scale planes.
+moe_status_t do_dispatch_fp8_bwd(const Cfg& c, const Ws& w, const int32_t* idx, const uint16_t* x,
+                                 const uint16_t* dy, const float* gates, cudaStream_t s) {
+  const size_t rows = (size_t)w.L.rows;
+  DispatchArgs a = dispatch_args(w);
+  a.idx = idx;
+  a.x = x;
+  a.dy = dy;
+  a.gates = gates;
+  a.x_perm = w.at<uint16_t>(w.L.xperm);
+  a.dy_perm = w.at<uint16_t>(w.L.dy_perm);
+  a.x8 = w.at<uint8_t>(w.L.buf_d1);
+  a.dy8 = a.x8 + rows * c.d;
+  a.x8s = w.at<float>(w.L.fp8s);
+  a.dy8s = a.x8s + rows;
+  MOE_CUDA(launch_dispatch_scan(c, w.L, a, s));
+  MOE_CUDA(launch_dispatch_gather(c, w.L, a, true, true, true, s, false, true));
+  return MOE_OK;
+}
+
 moe_status_t do_ffn_bwd_fp8(const Cfg& c, const Ws& w, const uint8_t* wg8, const float* wg_scale,
                             const uint8_t* wu8, const float* wu_scale, const uint8_t* wdt8,
                             const float* wdt_scale, const uint8_t* wgut8, const float* wgut_scale,
                             float* dgates, uint16_t* dWg, uint16_t* dWu, uint16_t* dWd, cudaStream_t s) {
+  // the x and dY rows' codes and scales were written by the dispatch (do_dispatch_fp8_bwd)
   const size_t rows = (size_t)w.L.rows;
   FfnBwd8Args b{};
   b.x_perm = w.at<uint16_t>(w.L.xperm);
@@ -350,8 +373,6 @@ moe_status_t do_ffn_bwd_fp8(const Cfg& c, const Ws& w, const uint8_t* wg8, const
   uint8_t* x8 = w.at<uint8_t>(w.L.buf_d1);
   uint8_t* dy8 = x8 + rows * c.d;
   float* sc = w.at<float>(w.L.fp8s);
-  MOE_CUDA(launch_quantize_rows_e4m3(b.x_perm, (int64_t)rows, c.d, x8, sc, s, w.tabs()));
-  MOE_CUDA(launch_quantize_rows_e4m3(b.dy_perm, (int64_t)rows, c.d, dy8, sc + rows, s, w.tabs()));
   b.x8 = x8;
   b.xs = sc;
   b.dy8 = dy8;
@@ -851,8 +872,7 @@ moe_status_t moe_layer_bwd_fp8(const moe_config_t* cfg, const moe_bf16* x, const
   MOE_TRY(check_device());
   const int32_t* idx = static_cast<const int32_t*>(saved);
   const float* gates = reinterpret_cast<const float*>(idx + (size_t)c.T * c.k);
-  MOE_TRY(do_dispatch(c, w, idx, x, dy, gates, nullptr, nullptr, nullptr, nullptr, w.at<uint16_t>(w.L.xperm),
-                      w.at<uint16_t>(w.L.dy_perm), stream));
+  MOE_TRY(do_dispatch_fp8_bwd(c, w, idx, x, dy, gates, stream));
   float* dgates = w.at<float>(w.L.dgates);
   MOE_TRY(do_ffn_bwd_fp8(c, w, wg8, wg_scale, wu8, wu_scale, wdt8, wdt_scale, wgut8, wgut_scale, dgates, dW_gate,
                          dW_up, dW_down, stream));

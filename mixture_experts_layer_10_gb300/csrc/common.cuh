@@ -164,13 +164,17 @@ struct DispatchArgs {
   // nullable: the token of every padded expert row (pad rows: token 0), for GEMMs that gather their
   // operand rows from token order instead of reading x_perm / dY_perm
   int32_t* tok_of_prow;
+  // FP8 backward (quant): e4m3 codes [rows, d] and row scales of every padded x and dY row, written
+  // beside the bf16 rows (pad rows: zero codes, scale 1)
+  uint8_t* x8; uint8_t* dy8; float* x8s; float* dy8s;
 };
 cudaError_t launch_dispatch_scan(const Cfg& c, const Layout& L, const DispatchArgs& a, cudaStream_t s);
 // write_meta: the slot/row tables (and tok_of_prow when given); gather_x / gather_dy: copy the rows;
-// gates: the gate of every padded row (implied by gather_dy)
+// gates: the gate of every padded row (implied by gather_dy); quant (with all three): also the
+// rows' e4m3 codes and scales (a.x8, a.dy8, a.x8s, a.dy8s)
 cudaError_t launch_dispatch_gather(const Cfg& c, const Layout& L, const DispatchArgs& a,
                                    bool write_meta, bool gather_x, bool gather_dy, cudaStream_t s,
-                                   bool gates = false);
+                                   bool gates = false, bool quant = false);
 
 struct CombineArgs {
   const uint16_t* o_perm; const float* gates; uint16_t* y;

@@ -14,9 +14,13 @@
 //   the same kernel as rows of d/2 two-byte elements, with their row scales beside them.  For GEMMs
 //   that gather their operand rows themselves (tile::gather4 from token order) the kernel moves no
 //   data and writes only the tables, the token of every padded row and, for the backward, its gate.
+//   For the FP8 backward it also quantises: a token's x and dy rows get their e4m3 row scales from
+//   one amax pass, and each vector's codes are written beside its bf16 copy to every expert row,
+//   so no pass re-reads the k-fold expert rows to quantise them.
 #include <mutex>
 
 #include "common.cuh"
+#include "e4m3.cuh"
 
 namespace moe {
 namespace {
@@ -192,9 +196,10 @@ __global__ void __launch_bounds__(kScanThreads) dispatch_scan_kernel(DispatchArg
 
 constexpr int kUnroll = 4;   // 16-byte vectors per lane in flight per source row
 
-template <bool kMeta, bool kX, bool kDy, bool kGate>
+template <bool kMeta, bool kX, bool kDy, bool kGate, bool kQ = false>
 __global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a, int T, int k, int E,
                                                               int S, int d) {
+  static_assert(!kQ || (kX && kDy), "the quantising gather moves x and dy");
   constexpr bool kGates = kDy || kGate;   // the gate of every padded row
   const Tables* tb = a.tabs;
   const int lane = threadIdx.x & 31;
@@ -204,6 +209,28 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a, in
   for (int t = gw; t < T; t += nw) {
     const uint4* xs = kX ? reinterpret_cast<const uint4*>(a.x + (size_t)t * d) : nullptr;
     const uint4* dys = kDy ? reinterpret_cast<const uint4*>(a.dy + (size_t)t * d) : nullptr;
+    // quant: the token's row scales (amax over the whole row first; the copy pass below re-reads the
+    // row from L2) and their reciprocals, warp-uniform
+    float sx = 1.f, sd = 1.f, yx = 0.f, yd = 0.f;
+    bool rx = true, rd = true;
+    if constexpr (kQ) {
+      float ax = 0.f, ad = 0.f;
+      for (int v = lane; v < nvec; v += 32) {
+        ax = fmaxf(ax, amax8_bf16(xs[v]));
+        ad = fmaxf(ad, amax8_bf16(dys[v]));
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        ax = fmaxf(ax, __shfl_xor_sync(0xffffffffu, ax, off));
+        ad = fmaxf(ad, __shfl_xor_sync(0xffffffffu, ad, off));
+      }
+      sx = e4m3_row_scale(ax);
+      sd = e4m3_row_scale(ad);
+      rx = e4m3_recip_ok(sx);
+      rd = e4m3_recip_ok(sd);
+      yx = rx ? __frcp_rn(sx) : 0.f;
+      yd = rd ? __frcp_rn(sd) : 0.f;
+    }
     for (int jb = 0; jb < k; jb += 32) {
       const int j = jb + lane;
       int prow = -1;
@@ -248,6 +275,14 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a, in
           if (kX && v < nvec) vx[u] = xs[v];
           if (kDy && v < nvec) vd[u] = dys[v];
         }
+        uint2 cx[kUnroll], cd[kUnroll];   // quant: the vectors' codes, stored to every destination
+        if constexpr (kQ) {
+#pragma unroll
+          for (int u = 0; u < kUnroll; ++u) {
+            cx[u] = rx ? encode8_e4m3<true>(vx[u], sx, yx) : encode8_e4m3<false>(vx[u], sx, 0.f);
+            cd[u] = rd ? encode8_e4m3<true>(vd[u], sd, yd) : encode8_e4m3<false>(vd[u], sd, 0.f);
+          }
+        }
         for (int q = 0; q < ng; ++q) {
           const int p = __shfl_sync(0xffffffffu, prow, q);
           if (p < 0) continue;
@@ -257,6 +292,14 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a, in
             if (v >= nvec) continue;
             if (kX) reinterpret_cast<uint4*>(a.x_perm + (size_t)p * d)[v] = vx[u];
             if (kDy) reinterpret_cast<uint4*>(a.dy_perm + (size_t)p * d)[v] = vd[u];
+            if constexpr (kQ) {
+              reinterpret_cast<uint2*>(a.x8 + (size_t)p * d)[v] = cx[u];
+              reinterpret_cast<uint2*>(a.dy8 + (size_t)p * d)[v] = cd[u];
+            }
+          }
+          if (kQ && v0 == 0 && lane == 0) {
+            a.x8s[p] = sx;
+            a.dy8s[p] = sd;
           }
         }
         if (jb == 0) {
@@ -269,6 +312,14 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a, in
               if (v >= nvec) continue;
               if (kX) reinterpret_cast<uint4*>(a.x_perm + p * d)[v] = vx[u];
               if (kDy) reinterpret_cast<uint4*>(a.dy_perm + p * d)[v] = vd[u];
+              if constexpr (kQ) {
+                reinterpret_cast<uint2*>(a.x8 + p * d)[v] = cx[u];
+                reinterpret_cast<uint2*>(a.dy8 + p * d)[v] = cd[u];
+              }
+            }
+            if (kQ && v0 == 0 && lane == 0) {
+              a.x8s[p] = sx;
+              a.dy8s[p] = sd;
             }
           }
         }
@@ -297,6 +348,16 @@ __global__ void __launch_bounds__(256) dispatch_gather_kernel(DispatchArgs a, in
       if (kX) reinterpret_cast<uint4*>(a.x_perm + row * d)[v] = z;
       if (kDy) reinterpret_cast<uint4*>(a.dy_perm + row * d)[v] = z;
     }
+    if constexpr (kQ) {   // a zero row's codes and scale, as the row quantiser gives them
+      for (int v = lane; v < d / 16; v += 32) {
+        reinterpret_cast<uint4*>(a.x8 + row * d)[v] = z;
+        reinterpret_cast<uint4*>(a.dy8 + row * d)[v] = z;
+      }
+      if (lane == 0) {
+        a.x8s[row] = 1.f;
+        a.dy8s[row] = 1.f;
+      }
+    }
     if (lane == 0) {
       if (kMeta) a.slot_of_prow[row] = -1;
       // a pad row gathers token 0: with a zero gate its dA, dB and Hg are exactly zero
@@ -322,11 +383,17 @@ cudaError_t launch_dispatch_scan(const Cfg& c, const Layout& L, const DispatchAr
 }
 
 cudaError_t launch_dispatch_gather(const Cfg& c, const Layout& L, const DispatchArgs& a,
-                                   bool write_meta, bool gather_x, bool gather_dy, cudaStream_t s, bool gates) {
+                                   bool write_meta, bool gather_x, bool gather_dy, cudaStream_t s, bool gates,
+                                   bool quant) {
   (void)L;
   const int blocks = num_sms() * 8;
   prof_mark(kKGather, s, true);
-  if (write_meta && gather_x && gather_dy)
+  if (quant && write_meta && gather_x && gather_dy && a.x8 && a.dy8 && a.x8s && a.dy8s)
+    dispatch_gather_kernel<true, true, true, false, true><<<blocks, 256, 0, s>>>(a, c.T, c.k, c.E, c.S, c.d);
+  else if (quant) {
+    prof_mark(kKGather, s, false);
+    return cudaErrorInvalidValue;
+  } else if (write_meta && gather_x && gather_dy)
     dispatch_gather_kernel<true, true, true, false><<<blocks, 256, 0, s>>>(a, c.T, c.k, c.E, c.S, c.d);
   else if (write_meta && gather_x)
     dispatch_gather_kernel<true, true, false, false><<<blocks, 256, 0, s>>>(a, c.T, c.k, c.E, c.S, c.d);
