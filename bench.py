@@ -56,7 +56,7 @@ GEMMS = {  # algorithmic FLOPs per launch in units of N*d*f (N = rows the expert
 HBM_KERNELS = ("dispatch_gather", "combine", "combine_bwd")
 ROUTER_KERNELS = ("route_fwd", "router_dlogits")   # one HBM pass over x each (logits computed or recomputed)
 KERNEL_SOURCES = ("gemm.cu", "dispatch.cu", "combine.cu", "route.cu", "route_tc.cu", "activations.cu", "ptx.cuh",
-                  "common.cuh", "tmap.cuh")
+                  "common.cuh", "tmap.cuh", "e4m3.cuh")
 ROW_TILE = 256   # expert segments are padded to multiples of this many rows (include/moe.h)
 
 
