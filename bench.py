@@ -557,7 +557,10 @@ def run_workload(args, name, cfg, steps, warmup, rank, world, local, barrier, ex
     # the analytical resource model's roofline prediction for this step (same peaks)
     from mixture_experts_layer_10_gb300 import resource_model
     pred = resource_model.predict_ms(cfg, tensor_peak, pk["hbm"], N=n_kept, kept_rows=kept_real)
+    cal = resource_model.predict_ms_calibrated(cfg, tensor_peak, pk["hbm"], N=n_kept, kept_rows=kept_real,
+                                               counts=[int(c) for c in counts_h])
     model_line = {"predicted_ms": pred["step_ms"], "measured_over_predicted": ms / pred["step_ms"],
+                  "calibrated_ms": cal["step_ms"], "measured_over_calibrated": ms / cal["step_ms"],
                   "memory_bytes": resource_model.memory(cfg)}
     tensor_kind = ("bf16_tflops (burst, %s): SM clock held at max in the timed region" if at_max else
                    "bf16_tflops_sustained (%s): SM clock below max in the timed region") % pk["source"]
@@ -667,6 +670,7 @@ def compact(line):
             "combine_frac": k.get("combine", {}).get("frac_of_measured_peak"),
             "router": router,
             "model_measured_over_predicted": line["model"]["measured_over_predicted"],
+            "model_measured_over_calibrated": line["model"]["measured_over_calibrated"],
             "load_max_over_mean": line["config"]["load_max_over_mean"],
             "gpu_launches": line["gpu_launches"],
             "clocks": {kk: line["clocks"].get(kk) for kk in ("sm_mhz", "sm_max_mhz", "reasons", "samples")}}

@@ -124,6 +124,66 @@ def predict_ms(cfg: dict, tensor_tflops: float, hbm_gbs: float, N: int | None = 
     return {"step_ms": total, "per_kernel_ms": per}
 
 
+# Calibration of the step-time model on GB300 (one GPU, kernels timed inside the bench's step).  The
+# roofline above leaves out what the kernels cannot avoid or have not removed: the expert GEMMs run
+# over padded rows at a fraction of the peak, the HBM kernels at a fraction of the copy bandwidth,
+# the dispatch scan is latency (a decoupled look-back), and the routers have fixed costs.  The GEMM
+# and HBM fractions are the Mixtral-like step's live figures; the router and scan constants come
+# from the routers' and the scan's own timings at several shapes.  Other workloads are predictions.
+EFF_GEMM = 0.92          # expert pair GEMMs, of the tensor peak passed in, over padded rows
+EFF_HBM = 0.85           # gather / combine kernels, of the copy bandwidth passed in
+SCAN_US = 30.0           # one dispatch scan (two per step)
+ROUTER_FIXED_US = 12.0   # streaming router (E <= 32): setup, first loads, cross-CTA finish, per pass
+ROUTER_TILE_US = 16.0    # per-tile router (32 < E <= 128): softmax / top-k epilogue of a 128-token tile
+SMALL_US = 10.0          # the small reductions (gate partials, router partials) per launch
+NUM_SMS = 152
+
+
+def padded_routed_rows(counts, row_tile: int = ROW_TILE) -> int:
+    """Rows the expert GEMMs run over for per-expert row counts: each expert's rows rounded up to the
+    tile (an expert with none takes no rows)."""
+    return int(sum(math.ceil(int(c) / row_tile) * row_tile for c in counts))
+
+
+def predict_ms_calibrated(cfg: dict, tensor_tflops: float, hbm_gbs: float, N: int | None = None,
+                          kept_rows: int = 0, counts=None) -> dict:
+    """Step time from the calibrated model: per kernel, its work at the efficiency the kernel class
+    reaches on GB300, plus its fixed costs.  counts: the routed rows of each expert (the padded
+    rows then follow them); without them every expert gets an equal share."""
+    T, d, f, E, k, S = cfg["T"], cfg["d"], cfg["f"], cfg["E"], cfg["k"], cfg.get("S", 0)
+    N = T * k if N is None else N
+    if counts is None:
+        counts = [N // E + (1 if e < N % E else 0) for e in range(E)]
+    R = N + S * T
+    Rpad = padded_routed_rows(counts) + S * math.ceil(T / ROW_TILE) * ROW_TILE
+    w = work(cfg, N, kept_rows)
+    tc, bw = tensor_tflops * 1e12, hbm_gbs * 1e9
+    per = {}
+    for name, v in w.items():
+        if name.startswith("gemm_") and name != "gemm_router_dx":
+            per[name] = 1e3 * v["flops"] * (Rpad / max(R, 1)) / (EFF_GEMM * tc)
+        elif name in ("dispatch_gather", "combine", "combine_bwd", "swiglu_bwd_kept"):
+            per[name] = 1e3 * v["bytes"] / (EFF_HBM * bw)
+    Ep = math.ceil(E / 64) * 64
+    for name in ("route_fwd", "router_dlogits"):
+        if E <= 32 and k <= 8:
+            t = T * d * 2 / (EFF_HBM * bw) + ROUTER_FIXED_US * 1e-6
+        elif E <= 128 and k <= 8:
+            tiles = math.ceil(T / 128)
+            waves = math.ceil(tiles / NUM_SMS)
+            mma = 2 * 128 * 3 * Ep * d / (tc / NUM_SMS)
+            t = waves * (mma + ROUTER_TILE_US * 1e-6)
+        else:   # the SIMT fp32 kernels
+            t = 2 * T * d * E / (tc / 16) + T * d * 2 / bw
+        per[name] = 1e3 * t
+    for name in ("router_dwr", "gemm_router_dx"):   # small GEMMs over T (K or M) and Ep
+        per[name] = 1e3 * max(2 * T * d * Ep / (0.5 * tc), T * d * 2 / (0.5 * bw))
+    per["dispatch_scan"] = 2 * SCAN_US * 1e-3
+    per["small_reductions"] = 2 * SMALL_US * 1e-3
+    total = sum(per.values()) + len(per) * LAUNCH_US * 1e-3 / 2
+    return {"step_ms": total, "per_kernel_ms": per, "padded_rows": Rpad}
+
+
 def work_forward(cfg: dict, N: int | None = None, fp8: bool = False) -> dict:
     """FLOPs and algorithmic HBM bytes per kernel of the forward alone, in bf16 (moe_layer_fwd) or
     with e4m3 expert GEMMs (moe_layer_fwd_fp8: the token rows quantised once, their codes and row

@@ -107,3 +107,32 @@ def test_kernel_source_hash_ignores_comments_only():
     b = "int f(int x) {\n  /* a different\n comment */ return 2 * x; }"
     assert bench.code_only(a) == bench.code_only(b) == "int f(int x) { return 2 * x; }"
     assert bench.code_only(a) != bench.code_only(a.replace("2 *", "3 *"))
+
+
+def test_padded_routed_rows():
+    assert rm.padded_routed_rows([0, 1, 256, 257, 512]) == 0 + 256 + 256 + 512 + 512
+    assert rm.padded_routed_rows([]) == 0
+
+
+@pytest.mark.parametrize("name", WORKLOADS)
+def test_calibrated_model_is_above_the_roofline(name):
+    """The calibrated prediction adds padded rows, efficiencies below 1 and fixed costs to the same
+    work: never faster than the roofline, and its GEMM share is the roofline's over EFF_GEMM (equal
+    loads, rows a multiple of the tile)."""
+    cfg = synth.CONFIGS[name]
+    r = rm.predict_ms(cfg, tensor_tflops=1800.0, hbm_gbs=6800.0)
+    c = rm.predict_ms_calibrated(cfg, tensor_tflops=1800.0, hbm_gbs=6800.0)
+    assert c["step_ms"] > r["step_ms"]
+    for n, t in r["per_kernel_ms"].items():
+        if n.startswith("gemm_") and n != "gemm_router_dx":
+            assert c["per_kernel_ms"][n] >= t / rm.EFF_GEMM * (1 - 1e-12)
+
+
+def test_calibrated_model_charges_padding():
+    cfg = synth.CONFIGS["qwen3"]
+    N = cfg["T"] * cfg["k"]
+    even = rm.predict_ms_calibrated(cfg, 1800.0, 6800.0)
+    skew = [N - 127 * 10] + [10] * 127            # one large expert, 127 with 10 rows each
+    c = rm.predict_ms_calibrated(cfg, 1800.0, 6800.0, counts=skew)
+    assert c["padded_rows"] == rm.padded_routed_rows(skew)
+    assert c["per_kernel_ms"]["gemm_wgrad"] > even["per_kernel_ms"]["gemm_wgrad"]
