@@ -1120,10 +1120,11 @@ struct RouterDx : PolicyDefaults {
 //     tokens (summed in a fixed order afterwards).
 constexpr int kRouterTopK = 8;
 
-template <bool kBwd>
+template <bool kBwd, bool kSplit>
 struct RouterLogits : PolicyDefaults {
   static constexpr int kId = kBwd ? kKRouterDlogits : kKRoute;
-  static constexpr int kEpiWarps = 4;
+  static constexpr int kEpiWarps = kSplit ? 8 : 4;       // kSplit: two per TMEM lane quarter
+  static constexpr uint32_t kEpiWarpBytes = kSplit ? 3072 : 0;   // each warp's exchange buffer
   static constexpr int kStages = 3;
   static constexpr uint32_t kStageBytes = 4 * kTileA;   // x tile + three W_r parts (128 rows each)
   static constexpr int kAccCols = 256;                   // hi products, then mid + lo at +128
@@ -1186,35 +1187,52 @@ struct RouterLogits : PolicyDefaults {
       umma_bf16(dt + 128, da, sdesc_kmajor(sa + 3 * kTileA + kk * 32), j.idesc, true);
     }
   }
-  struct EpiState { float l[128]; };   // this lane's running sums over the chunks so far
-  __device__ static void epilogue_s(const Params& p, const Job& j, uint32_t ta, int row, int, int,
-                                    EpiState& st, uint32_t) {
+  // kSplit (Ep = 128): eight epilogue warps, two per TMEM lane quarter; part h of a quarter sums and
+  // finishes experts [64 h, 64 h + 64) of its 32 tokens, and the two parts meet in shared memory
+  // (row maxima, sums of exp, top-k lists) before the outputs.  With one warp per quarter the last
+  // slice's softmax and top-k over 128 experts took ~16 us a tile, one token per lane, while its
+  // accumulator was held (split: 10-16% off the E = 128 routers; at Ep = 64 the second part would
+  // have no experts, so those routers keep one warp per quarter).
+  static constexpr int kPartCols = kSplit ? 64 : 128;
+  struct EpiState {
+    float l[kPartCols];   // this lane's running sums over the slices so far (its part)
+    uint32_t xphase = 0;  // phase of the quarter's exchange barrier
+  };
+  static constexpr uint32_t kBarOff = 2560;   // the exchange barrier, in the part-0 warp's buffer
+  // thread 0, before the kernel's first barrier fence: one two-arrival barrier per quarter
+  __device__ static void init_epi(uint8_t* epi) {
+    if constexpr (kSplit)
+      for (int w = 0; w < 4; ++w) mbar_init(reinterpret_cast<uint64_t*>(epi + w * kEpiWarpBytes + kBarOff), 2);
+  }
+  __device__ static void epilogue_s(const Params& p, const Job& j, uint32_t ta, int row, int part, int,
+                                    EpiState& st, uint8_t* ebuf) {
     const bool first = j.sub == 0;
+    const int cb = part * kPartCols;
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      if (c * 32 < p.Ep) {   // warp-uniform: tcgen05.ld is warp-wide
+    for (int c = 0; c < kPartCols; c += 32) {
+      if (cb + c < p.Ep) {   // warp-uniform: tcgen05.ld is warp-wide
         uint32_t h[32], r[32];
-        tmem_ld32(ta + c * 32, h);
-        tmem_ld32(ta + 128 + c * 32, r);
+        tmem_ld32(ta + cb + c, h);
+        tmem_ld32(ta + 128 + cb + c, r);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 32; ++i)
-          st.l[c * 32 + i] = (first ? 0.f : st.l[c * 32 + i]) + (__uint_as_float(h[i]) + __uint_as_float(r[i]));
+          st.l[c + i] = (first ? 0.f : st.l[c + i]) + (__uint_as_float(h[i]) + __uint_as_float(r[i]));
       }
     }
     if (j.sub != p.nch - 1) return;
-    // last chunk: the sums go back into this accumulator's hi columns for the rolled passes below
+    // last slice: the sums go back into this accumulator's hi columns for the rolled passes below
 #pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      if (c * 32 < p.Ep) {
+    for (int c = 0; c < kPartCols; c += 32) {
+      if (cb + c < p.Ep) {
         uint32_t v[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(st.l[c * 32 + i]);
-        tmem_st32(ta + c * 32, v);
+        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(st.l[c + i]);
+        tmem_st32(ta + cb + c, v);
       }
     }
     tmem_st_wait();
-    finish(p, j, ta, row);
+    finish(p, j, ta, row, part, ebuf, st.xphase);
   }
   // logits of columns [c, c + 32) for this lane's token from S (bias added, -inf past E)
   __device__ static void chunk(const Params& p, uint32_t sum, int c, float (&l)[32]) {
@@ -1227,10 +1245,25 @@ struct RouterLogits : PolicyDefaults {
       l[i] = e < p.E ? __uint_as_float(v[i]) + (p.b_r != nullptr ? p.b_r[e] : 0.f) : -INFINITY;
     }
   }
-  __device__ static void finish(const Params& p, const Job& j, uint32_t sum, int row) {
+  // The two parts of a quarter (warps 4 apart) meet on a barrier of two arrivals, one per warp,
+  // after each warp's shared-memory writes; the wait is bounded, so a partner that gave up leaves
+  // an error instead of a hang.
+  __device__ static void pair_sync(const Params& p, uint8_t* ebuf, int part, uint32_t& phase) {
+    uint64_t* bar = reinterpret_cast<uint64_t*>((part == 0 ? ebuf : ebuf - 4 * kEpiWarpBytes) + kBarOff);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+    const bool ok = mbar_wait_drain(bar, phase, wait_limit_ns(p.hdr));
+    phase ^= 1u;
+    if (!ok && (threadIdx.x & 31) == 0) record_error(p.hdr, MOE_ERR_TIMEOUT, kSiteGemmEpilogue);
+  }
+  __device__ static void finish(const Params& p, const Job& j, uint32_t sum, int row, int part, uint8_t* ebuf,
+                                uint32_t& xphase) {
     const int t = j.m0 + row;
     const bool live = t < p.T;
-    // pass 1: running max and rescaled sum of exp (every lane loads: tcgen05.ld is warp-wide)
+    const int lane = threadIdx.x & 31;
+    const int cb = part * kPartCols;
+    // pass 1 over this part's experts: running max and rescaled sum of exp, and (forward) the top-k
+    // kept sorted, larger logit first and a tie keeping the lower expert index
     float m = -INFINITY, z = 0.f;
     float tv[kRouterTopK];
     int ti[kRouterTopK];
@@ -1240,7 +1273,7 @@ struct RouterLogits : PolicyDefaults {
       ti[s] = 0x7fffffff;
     }
 #pragma unroll 1
-    for (int c = 0; c < p.Ep; c += 32) {
+    for (int c = cb; c < cb + kPartCols && c < p.Ep; c += 32) {
       float l[32];
       chunk(p, sum, c, l);
       float cm = -INFINITY;
@@ -1271,8 +1304,70 @@ struct RouterLogits : PolicyDefaults {
         }
       }
     }
+    if constexpr (kSplit) {
+      // exchange with the other part of this quarter: word w of lane l at word w * 32 + l (the two
+      // warps' buffers are 4 warps apart)
+      constexpr int kWords = 2 + 2 * kRouterTopK;
+      float* mine = reinterpret_cast<float*>(ebuf);
+      const float* other = reinterpret_cast<const float*>(part == 0 ? ebuf + 4 * kEpiWarpBytes : ebuf - 4 * kEpiWarpBytes);
+      mine[0 * 32 + lane] = m;
+      mine[1 * 32 + lane] = z;
+      if (!kBwd) {
+#pragma unroll
+        for (int s = 0; s < kRouterTopK; ++s) {
+          mine[(2 + s) * 32 + lane] = tv[s];
+          mine[(2 + kRouterTopK + s) * 32 + lane] = __int_as_float(ti[s]);
+        }
+      }
+      pair_sync(p, ebuf, part, xphase);
+      const float mo = other[0 * 32 + lane], zo = other[1 * 32 + lane];
+      float ov[kRouterTopK];
+      int oi[kRouterTopK];
+      if (!kBwd) {
+#pragma unroll
+        for (int s = 0; s < kRouterTopK; ++s) {
+          ov[s] = other[(2 + s) * 32 + lane];
+          oi[s] = __float_as_int(other[(2 + kRouterTopK + s) * 32 + lane]);
+        }
+      }
+      pair_sync(p, ebuf, part, xphase);   // both have read before either buffer is written again
+      static_assert(kWords * 32 * 4 <= kBarOff && kBarOff + 8 <= kEpiWarpBytes, "exchange fits the warp's buffer");
+      // the token's max and sum of exp over all experts
+      const float M = fmaxf(m, mo);
+      z = (m == -INFINITY ? 0.f : z * expf(m - M)) + (mo == -INFINITY ? 0.f : zo * expf(mo - M));
+      m = M;
+      if (!kBwd) {
+        // part 0's list (the lower expert indices) with part 1's entries inserted after equal ones
+        if (part == 1) {
+#pragma unroll
+          for (int s = 0; s < kRouterTopK; ++s) {
+            const float fv = tv[s];
+            const int fi = ti[s];
+            tv[s] = ov[s];
+            ti[s] = oi[s];
+            ov[s] = fv;
+            oi[s] = fi;
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kRouterTopK; ++q) {
+          float cv = ov[q];
+          int ci = oi[q];
+#pragma unroll
+          for (int s = 0; s < kRouterTopK; ++s)
+            if (cv > tv[s]) {
+              const float fv = tv[s];
+              const int fi = ti[s];
+              tv[s] = cv;
+              ti[s] = ci;
+              cv = fv;
+              ci = fi;
+            }
+        }
+      }
+    }
     if (!kBwd) {
-      if (!live) return;
+      if (!live || part != 0) return;
       float zsel = 0.f;
 #pragma unroll
       for (int s = 0; s < kRouterTopK; ++s)
@@ -1286,7 +1381,7 @@ struct RouterLogits : PolicyDefaults {
         }
       return;
     }
-    // backward pass 2: dl for every expert of this token
+    // backward pass 2: dl for every expert of this part
     float sdg = 0.f;
     int sid[kRouterTopK];
     float sgd[kRouterTopK];
@@ -1300,10 +1395,9 @@ struct RouterLogits : PolicyDefaults {
         sdg += sgd[s] * p.gates[(size_t)t * p.k + s];
       }
     }
-    const int lane = threadIdx.x & 31;
     const int wq = row >> 5;   // TMEM lane quarter: one db partial per 32 tokens
 #pragma unroll 1
-    for (int c = 0; c < p.Ep; c += 32) {
+    for (int c = cb; c < cb + kPartCols && c < p.Ep; c += 32) {
       float l[32];
       chunk(p, sum, c, l);
       float dl[32];
@@ -1327,15 +1421,15 @@ struct RouterLogits : PolicyDefaults {
           if (c + i < p.E) p.dlogits[(size_t)t * p.E + c + i] = dl[i];
       }
       // db partial of these 32 tokens: a warp sum per expert, lane i keeps expert c + i
-      float mine = 0.f;
+      float mine_db = 0.f;
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         float v = dl[i];
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        if (lane == i) mine = v;
+        if (lane == i) mine_db = v;
       }
-      if (c + lane < p.E) p.db_part[((size_t)(j.m0 / kBM) * 4 + wq) * p.E + c + lane] = mine;
+      if (c + lane < p.E) p.db_part[((size_t)(j.m0 / kBM) * 4 + wq) * p.E + c + lane] = mine_db;
     }
   }
   __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
@@ -1393,6 +1487,7 @@ __global__ void __launch_bounds__(threads_of<P>(), 1) gemm_kernel(const __grid_c
       mbar_init(&tempty[a], P::kEpiWarps);
     }
     mbar_init(drain, 1);
+    if constexpr (P::kStateful) P::init_epi(epi);
     *abort_flag = 0;
     fence_mbar_init();
     P::prefetch(p);
@@ -1504,7 +1599,7 @@ __global__ void __launch_bounds__(threads_of<P>(), 1) gemm_kernel(const __grid_c
       tc_fence_after();
       const uint32_t ta = tmem_base + (uint32_t)(acc * P::kAccCols) + ((uint32_t)(q * 32) << 16);
       if constexpr (P::kStateful)
-        P::epilogue_s(p, j, ta, row, part, seq, es, tmem_base + ((uint32_t)(q * 32) << 16));
+        P::epilogue_s(p, j, ta, row, part, seq, es, epi + (size_t)(warp - 2) * P::kEpiWarpBytes);
       else if constexpr (P::kEpiWarpBytes > 0)
         P::epilogue(p, j, ta, row, part, seq, epi + (size_t)(warp - 2) * P::kEpiWarpBytes);
       else
@@ -2149,9 +2244,9 @@ cudaError_t launch_router_dwr(const Cfg& c, const Layout& L, const uint16_t* x, 
   return launch<RouterDwr>(p, s);
 }
 
-template <bool kBwd>
-cudaError_t launch_router_tc(const Cfg& c, const Layout& L, const RouterTcArgs& a, cudaStream_t s) {
-  using P = RouterLogits<kBwd>;
+template <bool kBwd, bool kSplit>
+cudaError_t launch_router_tc_t(const Cfg& c, const Layout& L, const RouterTcArgs& a, cudaStream_t s) {
+  using P = RouterLogits<kBwd, kSplit>;
   typename P::Params p{};
   if (!map_2d(&p.tmX, a.x, c.d, c.T, 64, 128) || !map_3d(&p.tmW, a.wr3, c.d, L.Ep, 3, 64, 128))
     return cudaErrorInvalidValue;
@@ -2174,6 +2269,11 @@ cudaError_t launch_router_tc(const Cfg& c, const Layout& L, const RouterTcArgs& 
   p.hdr = a.hdr;
   p.tabs = a.tabs;
   return launch<P>(p, s);
+}
+
+template <bool kBwd>
+cudaError_t launch_router_tc(const Cfg& c, const Layout& L, const RouterTcArgs& a, cudaStream_t s) {
+  return L.Ep > 64 ? launch_router_tc_t<kBwd, true>(c, L, a, s) : launch_router_tc_t<kBwd, false>(c, L, a, s);
 }
 
 cudaError_t launch_route_tc(const Cfg& c, const Layout& L, const RouterTcArgs& a, cudaStream_t s) {
