@@ -130,6 +130,7 @@ def predict_ms(cfg: dict, tensor_tflops: float, hbm_gbs: float, N: int | None = 
 # the dispatch scan is latency (a decoupled look-back), and the routers have fixed costs.  The GEMM
 # and HBM fractions are the Mixtral-like step's live figures; the router and scan constants come
 # from the routers' and the scan's own timings at several shapes.  Other workloads are predictions.
+# The GEMM fraction counts the pad rows' MMAs: 0.95 over padded rows is ~0.90 over routed rows.
 EFF_GEMM = 0.95          # expert pair GEMMs, of the tensor peak passed in, over padded rows
 EFF_HBM = 0.85           # gather / combine kernels, of the copy bandwidth passed in
 SCAN_US = 30.0           # one dispatch scan (two per step)
