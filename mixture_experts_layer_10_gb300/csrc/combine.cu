@@ -96,15 +96,26 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 }
 
 // dgates[t,j] = sum over the d_ff tiles of the per-row partials dy.o written by the backward
-// GEMM's epilogue (0 for dropped slots).
+// GEMM's epilogue (0 for dropped slots).  kG lanes own a slot: lane i of the group reads partials
+// i, i + kG, ... of the row (coalesced, several loads in flight per lane), and a shuffle tree of
+// fixed shape joins the group; the order is fixed, so the result is deterministic.
+template <int kG>
 __global__ void dgates_kernel(const float* __restrict__ dg_part, const int32_t* __restrict__ prow_of_slot,
                               float* __restrict__ dgates, int n, int ntf) {
-  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
-    const int p = prow_of_slot[i];
+  const int sub = threadIdx.x & (kG - 1);
+  const int g0 = (int)((blockIdx.x * blockDim.x + threadIdx.x) / kG);
+  const int ng = (int)((gridDim.x * blockDim.x) / kG);
+  for (int i0 = g0 - (g0 % (32 / kG)); i0 < n; i0 += ng) {   // whole warps iterate together
+    const int i = i0 + (g0 % (32 / kG));
+    const int p = i < n ? prow_of_slot[i] : -1;
     float v = 0.f;
-    if (p >= 0)
-      for (int q = 0; q < ntf; ++q) v += dg_part[(size_t)p * ntf + q];
-    dgates[i] = v;
+    if (p >= 0) {
+#pragma unroll 4
+      for (int q = sub; q < ntf; q += kG) v += dg_part[(size_t)p * ntf + q];
+    }
+#pragma unroll
+    for (int off = kG / 2; off > 0; off >>= 1) v += __shfl_down_sync(0xffffffffu, v, off, kG);
+    if (sub == 0 && i < n) dgates[i] = v;
   }
 }
 
@@ -130,9 +141,21 @@ cudaError_t launch_combine_bwd(const Cfg& c, const CombineBwdArgs& a, cudaStream
 
 cudaError_t launch_dgates(const Cfg& c, const Layout& L, const DgatesArgs& a, cudaStream_t s) {
   const int n = c.T * c.k;
-  const int blocks = std::max(1, std::min((n + 255) / 256, num_sms() * 4));
+  // lanes per slot: the largest power of two that leaves each lane about six of the row's partials
+  // (memory-level parallelism), at most a warp
+  int g = 1;
+  while (g < 32 && 2 * g * 6 <= L.ndg) g *= 2;
+  const long long threads = (long long)n * g;
+  const int blocks = (int)std::max<long long>(1, std::min<long long>((threads + 255) / 256, (long long)num_sms() * 16));
   prof_mark(kKDgates, s, true);
-  dgates_kernel<<<blocks, 256, 0, s>>>(a.dg_part, a.prow_of_slot, a.dgates, n, L.ndg);
+  switch (g) {
+    case 32: dgates_kernel<32><<<blocks, 256, 0, s>>>(a.dg_part, a.prow_of_slot, a.dgates, n, L.ndg); break;
+    case 16: dgates_kernel<16><<<blocks, 256, 0, s>>>(a.dg_part, a.prow_of_slot, a.dgates, n, L.ndg); break;
+    case 8: dgates_kernel<8><<<blocks, 256, 0, s>>>(a.dg_part, a.prow_of_slot, a.dgates, n, L.ndg); break;
+    case 4: dgates_kernel<4><<<blocks, 256, 0, s>>>(a.dg_part, a.prow_of_slot, a.dgates, n, L.ndg); break;
+    case 2: dgates_kernel<2><<<blocks, 256, 0, s>>>(a.dg_part, a.prow_of_slot, a.dgates, n, L.ndg); break;
+    default: dgates_kernel<1><<<blocks, 256, 0, s>>>(a.dg_part, a.prow_of_slot, a.dgates, n, L.ndg); break;
+  }
   prof_mark(kKDgates, s, false);
   return cudaGetLastError();
 }
