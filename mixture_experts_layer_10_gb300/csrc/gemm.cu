@@ -1199,6 +1199,8 @@ struct RouterLogits : PolicyDefaults {
     uint32_t xphase = 0;  // phase of the quarter's exchange barrier
   };
   static constexpr uint32_t kBarOff = 2560;   // the exchange barrier, in the part-0 warp's buffer
+  static_assert(!kSplit || ((2 + 2 * kRouterTopK) * 32 * 4 <= kBarOff && kBarOff + 8 <= kEpiWarpBytes),
+                "the exchange and its barrier fit the warp's buffer");
   // thread 0, before the kernel's first barrier fence: one two-arrival barrier per quarter
   __device__ static void init_epi(uint8_t* epi) {
     if constexpr (kSplit)
@@ -1307,7 +1309,6 @@ struct RouterLogits : PolicyDefaults {
     if constexpr (kSplit) {
       // exchange with the other part of this quarter: word w of lane l at word w * 32 + l (the two
       // warps' buffers are 4 warps apart)
-      constexpr int kWords = 2 + 2 * kRouterTopK;
       float* mine = reinterpret_cast<float*>(ebuf);
       const float* other = reinterpret_cast<const float*>(part == 0 ? ebuf + 4 * kEpiWarpBytes : ebuf - 4 * kEpiWarpBytes);
       mine[0 * 32 + lane] = m;
@@ -1331,7 +1332,6 @@ struct RouterLogits : PolicyDefaults {
         }
       }
       pair_sync(p, ebuf, part, xphase);   // both have read before either buffer is written again
-      static_assert(kWords * 32 * 4 <= kBarOff && kBarOff + 8 <= kEpiWarpBytes, "exchange fits the warp's buffer");
       // the token's max and sum of exp over all experts
       const float M = fmaxf(m, mo);
       z = (m == -INFINITY ? 0.f : z * expf(m - M)) + (mo == -INFINITY ? 0.f : zo * expf(mo - M));
