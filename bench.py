@@ -54,7 +54,7 @@ GEMMS = {  # algorithmic FLOPs per launch in units of N*d*f (N = rows the expert
     "gemm_wgrad": 6, "gemm_dgrad_x": 4,
 }
 HBM_KERNELS = ("dispatch_gather", "combine", "combine_bwd")
-ROUTER_KERNELS = ("route_fwd", "router_dlogits")   # one HBM pass over x each (logits computed or recomputed)
+ROUTER_KERNELS = ("route_fwd", "router_dlogits")   # the logit pass over x; dl from the kept logits
 KERNEL_SOURCES = ("gemm.cu", "dispatch.cu", "combine.cu", "route.cu", "route_tc.cu", "activations.cu", "ptx.cuh",
                   "common.cuh", "tmap.cuh", "e4m3.cuh")
 ROW_TILE = 256   # expert segments are padded to multiples of this many rows (include/moe.h)
@@ -591,8 +591,11 @@ def run_workload(args, name, cfg, steps, warmup, rank, world, local, barrier, ex
                 work = n * ((N + T) * d * 2 + 8 * T * k)
             elif kname == "combine_bwd":   # expert rows + the router term row in, dx out, slot indices
                 work = n * ((N + 2 * T) * d * 2 + 4 * T * k)
-            else:   # the router's logit passes read x once (and W_r; idx and gates out)
-                work = n * (T * d * 2 + d * E * 4 + T * k * 8)
+            elif kname == "route_fwd":   # x once and W_r in; idx, gates and (kept for the backward) logits out
+                work = n * (T * d * 2 + d * E * 4 + T * k * 8 + (0 if cfg.get("renorm") else T * E * 4))
+            else:   # router_dlogits: idx, gates, dgates (and the kept logits) in; dl fp32 and bf16 rows out
+                Ep = (E + 63) // 64 * 64
+                work = n * (T * k * 12 + (0 if cfg.get("renorm") else T * E * 4) + T * E * 4 + T * Ep * 2)
             ent["gbs"] = work / (tot / 1000.0) / 1e9
             ent["frac_of_measured_peak"] = ent["gbs"] / pk["hbm"]
             if kname in HBM_KERNELS:

@@ -135,9 +135,18 @@ typedef struct CUstream_st* moe_stream_t;  /* a cudaStream_t; NULL is the legacy
 
 /* Workspace bytes for any call of this configuration, and bytes of the `saved` buffer that
  * moe_layer_fwd fills and moe_layer_bwd reads: idx int32 [T,k], then gates fp32 [T,k], then, when
+ * the gates are not renormalised, from the next 256-byte boundary the router logits fp32 [T,E]
+ * (bias included: the backward's softmax reads them instead of recomputing x W_r), then, when
  * keep_rows > 0, from the next 256-byte boundary the kept a and b [keep, d_ff] bf16 (keep =
  * keep_rows rounded down to 256, at most moe_perm_rows()).  Host only; touches no device. */
 moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* ws_bytes, size_t* saved_bytes);
+
+/* Where the parts of `saved` after idx and gates sit (the layout above): the logits' byte offset
+ * and size (both 0 with renormalised gates, which keep none), and the kept a, b block's offset and
+ * size (a first, b right after it; size 0 when keep_rows is 0).  Every pointer is nullable.  Host
+ * only; touches no device. */
+moe_status_t moe_saved_layout(const moe_config_t* cfg, size_t* logits_off, size_t* logits_bytes, size_t* kept_off,
+                              size_t* kept_bytes);
 
 /* Checkpoint granularity from a memory budget (MoEBlaze summary, Limitations and future work:
  * adaptive checkpoint granularity driven by memory pressure at run time; Methodology item 2: keep
@@ -294,8 +303,8 @@ moe_status_t moe_down_fp8(const moe_config_t* cfg, const uint8_t* h8, const floa
  * and row scales into the padded expert rows; moe_gate_up_fp8 (h kept in bf16); quantise the h
  * rows this step fills; moe_down_fp8; and the combine.  The weights come quantised
  * (moe_quantize_rows_e4m3 of every row of W_gate, W_up and W_down, as above).  The router stays
- * fp32.  Fills `saved` like moe_layer_fwd (idx, gates), so moe_layer_bwd can follow with the bf16
- * weights.
+ * fp32.  Fills `saved` like moe_layer_fwd (idx, gates, logits), so moe_layer_bwd can follow with
+ * the bf16 weights.
  * keep_rows must be 0 (MOE_ERR_INVALID_ARG otherwise): the call's scratch uses the workspace
  * buffers that would carry kept activations to the backward. */
 moe_status_t moe_layer_fwd_fp8(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
@@ -339,18 +348,20 @@ moe_status_t moe_layer_bwd_fp8(const moe_config_t* cfg, const moe_bf16* x, const
                                void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* The whole forward: route, dispatch, expert FFN, combine (MoEBlaze summary, the training-loop
- * figure: fused expert kernels forward, then checkpoint).  Fills `saved` with idx and gates, and
- * with the kept a and b of the first keep_rows expert-ordered rows when keep_rows > 0; every other
- * activation is recomputed in the backward (Methodology item 2). */
+ * figure: fused expert kernels forward, then checkpoint).  Fills `saved` with idx and gates, the
+ * router logits (gates not renormalised; T * E fp32, small beside x), and the kept a and b of the
+ * first keep_rows expert-ordered rows when keep_rows > 0; every other activation is recomputed in
+ * the backward (Methodology item 2). */
 moe_status_t moe_layer_fwd(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
                            const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down,
                            moe_bf16* y, void* saved, void* ws, size_t ws_bytes, moe_stream_t stream);
 
 /* The whole backward from x, the weights, `saved` and dy (MoEBlaze summary, the training-loop
  * figure: fused expert kernels backward, then gradient reduce): rebuilds the dispatch queues from
- * the saved idx, recomputes the expert activations of the rows not kept (Methodology item 2), and
- * writes dx, dW_r, db_r (nullable) and the expert weight gradients.  `saved` must come from
- * moe_layer_fwd of the same configuration (keep_rows included). */
+ * the saved idx, recomputes the expert activations of the rows not kept (Methodology item 2), takes
+ * the router's softmax from the saved logits, and writes dx, dW_r, db_r (nullable) and the expert
+ * weight gradients.  `saved` must come from moe_layer_fwd of the same configuration (keep_rows
+ * included); a caller that writes idx and gates into it by hand writes the logits too. */
 moe_status_t moe_layer_bwd(const moe_config_t* cfg, const moe_bf16* x, const float* W_r, const float* b_r,
                            const moe_bf16* W_gate, const moe_bf16* W_up, const moe_bf16* W_down,
                            const void* saved, const moe_bf16* dy,

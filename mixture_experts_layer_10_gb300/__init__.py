@@ -28,7 +28,7 @@ EXPORTS = ("moe_workspace_size", "moe_perm_rows", "moe_workspace_init", "moe_rou
            "moe_debug_inject", "moe_profile_enable", "moe_profile_read", "moe_status_string",
            "moe_quantize_rows_e4m3", "moe_gate_up_fp8", "moe_down_fp8", "moe_layer_fwd_fp8",
            "moe_keep_rows_for_budget", "moe_keep_rows_for_free_memory", "moe_quantize_cols_e4m3",
-           "moe_layer_bwd_fp8")
+           "moe_layer_bwd_fp8", "moe_saved_layout")
 
 
 class moe_config_t(ctypes.Structure):
@@ -62,6 +62,7 @@ def load(path: str | None = None):
     sig = {
         "moe_workspace_size": [cfgp, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_size_t)],
         "moe_perm_rows": [cfgp, ctypes.POINTER(ctypes.c_int64)],
+        "moe_saved_layout": [cfgp] + [ctypes.POINTER(ctypes.c_size_t)] * 4,
         "moe_keep_rows_for_budget": [cfgp, ctypes.c_uint64, ctypes.POINTER(ctypes.c_int32),
                                      ctypes.POINTER(ctypes.c_uint64)],
         "moe_keep_rows_for_free_memory": [cfgp, ctypes.c_uint64, ctypes.POINTER(ctypes.c_int32),
@@ -153,6 +154,13 @@ def moe_workspace_size(cfg: moe_config_t):
     ws, saved = ctypes.c_size_t(), ctypes.c_size_t()
     _call("moe_workspace_size", ctypes.byref(cfg), ctypes.byref(ws), ctypes.byref(saved))
     return ws.value, saved.value
+
+
+def moe_saved_layout(cfg: moe_config_t):
+    """(logits_off, logits_bytes, kept_off, kept_bytes) of the `saved` buffer."""
+    v = [ctypes.c_size_t() for _ in range(4)]
+    _call("moe_saved_layout", ctypes.byref(cfg), *(ctypes.byref(x) for x in v))
+    return tuple(x.value for x in v)
 
 
 def moe_perm_rows(cfg: moe_config_t) -> int:
@@ -327,3 +335,14 @@ class Buffers:
         saved = torch.empty(saved_bytes, dtype=torch.uint8, device=device)
         moe_workspace_init(cfg, ws, stream)
         return cls(cfg, ws, saved, moe_perm_rows(cfg))
+
+    def saved_views(self):
+        """Views of `saved`: idx int32 [T,k], gates fp32 [T,k], logits fp32 [T,E] (None with
+        renormalised gates, which keep none)."""
+        import torch
+        T, k, E = self.cfg.T, self.cfg.k, self.cfg.E
+        idx = self.saved[:4 * T * k].view(torch.int32).view(T, k)
+        gates = self.saved[4 * T * k:8 * T * k].view(torch.float32).view(T, k)
+        off, nbytes, _, _ = moe_saved_layout(self.cfg)
+        logits = self.saved[off:off + nbytes].view(torch.float32).view(T, E) if nbytes else None
+        return idx, gates, logits

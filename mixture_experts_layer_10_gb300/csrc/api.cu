@@ -100,6 +100,29 @@ DispatchArgs dispatch_args(const Ws& w) {
 
 }  // namespace
 
+// Token splits of the dW_r product (x^T dl, one read of x): the persistent kernel deals its
+// (d_model tile, split) jobs round-robin to 152 CTAs, so take the split count whose busiest CTA
+// streams the fewest tokens (plus a small fixed cost a job), among counts whose fp32 partials
+// (splits x d_model x E x 4 bytes) stay within about a fifth of x.  Fixed by the configuration, not the
+// device, so the order of the fixed-order sum of the partials is too.
+int router_dwr_splits(const Cfg& c) {
+  constexpr int kCtas = 152;
+  constexpr long long kJobCost = 32;   // tokens' worth of fixed cost per job
+  const int mt = (c.d + 127) / 128;
+  const int nmax = std::max(1, std::min(c.T / (10 * c.E), 256));
+  int best = 1;
+  long long best_cost = -1;
+  for (int n = 1; n <= nmax; ++n) {
+    const long long waves = ((long long)mt * n + kCtas - 1) / kCtas;
+    const long long cost = waves * (router_dwr_ksplit(c.T, n) + kJobCost);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = n;
+    }
+  }
+  return best;
+}
+
 Layout make_layout(const Cfg& c) {
   Layout L{};
   const int64_t routed = ((int64_t)c.T * c.k + (int64_t)(kRowTile - 1) * c.E + kRowTile - 1) / kRowTile * kRowTile;
@@ -111,9 +134,7 @@ Layout make_layout(const Cfg& c) {
   // db partials: one per 32 tokens from the tensor-core backward, else one per SIMT router block
   L.nblk_router = router_bwd_on_tensor_cores(c) ? 4 * ((c.T + kRouterTile - 1) / kRouterTile)
                                                 : (c.T + route_block_tokens(c.E) - 1) / route_block_tokens(c.E);
-  // token splits of the dW_r tensor-core GEMM: about two tiles per SM, at least 512 tokens each
-  const int mtiles = (c.d + 127) / 128;
-  L.nsplit_dwr = std::max(1, std::min((304 + mtiles - 1) / mtiles, (c.T + 511) / 512));
+  L.nsplit_dwr = router_dwr_splits(c);
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -131,7 +152,7 @@ Layout make_layout(const Cfg& c) {
   L.dg_part = take(rows * L.ndg * 4);
   L.dlogits = take((size_t)c.T * c.E * 4);
   L.dwr_part = take((size_t)L.nsplit_dwr * c.d * c.E * 4);
-  L.db_part = take((size_t)L.nblk_router * c.E * 4);
+  L.db_part = take((size_t)std::max(L.nblk_router, router_saved_blocks(c)) * c.E * 4);
   L.dgates = take((size_t)c.T * c.k * 4);
   L.xperm = take(rows * c.d * 2);
   L.dy_perm = take(rows * c.d * 2);
@@ -155,15 +176,23 @@ Layout make_layout(const Cfg& c) {
   return L;
 }
 
+// idx [T, k], gates [T, k]; the logits [T, E] fp32 when the gates are not renormalised (the
+// router backward's softmax reads them instead of a second pass over x); the kept a and b.
 SavedLayout saved_layout(const Cfg& c) {
   SavedLayout sl{};
   sl.keep = (int)std::min<int64_t>(c.keep, make_layout(c).rows);
+  size_t off = (size_t)c.T * c.k * 8;
+  sl.logits_bytes = c.renorm ? 0 : (size_t)c.T * c.E * 4;
+  if (sl.logits_bytes != 0) {
+    sl.logits_off = align_up(off, 256);
+    off = sl.logits_off + sl.logits_bytes;
+  }
   const size_t kept = (size_t)sl.keep * c.f * 2;
   if (sl.keep == 0) {
-    sl.a_off = sl.b_off = sl.total = (size_t)c.T * c.k * 8;
+    sl.a_off = sl.b_off = sl.total = off;
     return sl;
   }
-  sl.a_off = align_up((size_t)c.T * c.k * 8, 256);
+  sl.a_off = align_up(off, 256);
   sl.b_off = sl.a_off + kept;
   sl.total = sl.b_off + kept;
   return sl;
@@ -441,7 +470,30 @@ moe_status_t do_router_bwd(const Cfg& c, const Ws& w, const uint16_t* x, const f
     MOE_CUDA(launch_to_bf16_rows(dlogits, c.T, c.E, w.L.Ep, dl_bf16, s));
   }
   MOE_CUDA(launch_router_dwr(c, w.L, x, dl_bf16, a.dwr_part, w.hdr(), w.tabs(), s));
-  MOE_CUDA(launch_router_reduce(c, w.L, a, s));
+  MOE_CUDA(launch_router_reduce(c, w.L, a, w.L.nblk_router, s));
+  return MOE_OK;
+}
+
+// The layer backward's router gradient: dl from the logits the forward kept in `saved` (the
+// softmax needs them only when the gates are not renormalised), so x is read once here, by the
+// dW_r product, instead of twice.  Leaves dl's bf16 rows in the workspace for the dx term.
+moe_status_t do_router_bwd_saved(const Cfg& c, const Ws& w, const uint16_t* x, const float* logits,
+                                 const int32_t* idx, const float* gates, const float* dgates, float* dlogits,
+                                 float* dW_r, float* db_r, cudaStream_t s) {
+  RouterBwdArgs a{};
+  a.x = x;
+  a.idx = idx;
+  a.gates = gates;
+  a.dgates = dgates;
+  a.dlogits = dlogits;
+  a.dW_r = dW_r;
+  a.db_r = db_r;
+  a.dwr_part = w.at<float>(w.L.dwr_part);
+  a.db_part = w.at<float>(w.L.db_part);
+  uint16_t* dl_bf16 = w.at<uint16_t>(w.L.dl_bf16);
+  MOE_CUDA(launch_router_dlogits_saved(c, w.L, a, logits, dl_bf16, s));
+  MOE_CUDA(launch_router_dwr(c, w.L, x, dl_bf16, a.dwr_part, w.hdr(), w.tabs(), s));
+  MOE_CUDA(launch_router_reduce(c, w.L, a, router_saved_blocks(c), s));
   return MOE_OK;
 }
 
@@ -470,14 +522,15 @@ moe_status_t do_route(const Cfg& c, const Ws& w, const uint16_t* x, const float*
 // term runs on the tensor cores (bf16 copies of dlogits and W_r padded to Ep columns) into a bf16
 // [T, d] buffer in the workspace's dY_perm region, which the backward no longer needs here; the
 // token-owner gather then adds it to the rows in fp32 with one rounding.
+// dl_ready: the workspace already holds dl's bf16 rows (the layer backward's router gradient).
 moe_status_t do_combine_bwd(const Cfg& c, const Ws& w, const uint16_t* dx_perm, const float* dlogits,
-                            const float* W_r, uint16_t* dx, cudaStream_t s) {
+                            const float* W_r, uint16_t* dx, cudaStream_t s, bool dl_ready = false) {
   uint16_t* r = nullptr;
   if (dlogits != nullptr) {
     uint16_t* dl_bf16 = w.at<uint16_t>(w.L.dl_bf16);
     uint16_t* wr_bf16 = w.at<uint16_t>(w.L.wr_bf16);
     r = w.at<uint16_t>(w.L.dy_perm);
-    MOE_CUDA(launch_to_bf16_rows(dlogits, c.T, c.E, w.L.Ep, dl_bf16, s));
+    if (!dl_ready) MOE_CUDA(launch_to_bf16_rows(dlogits, c.T, c.E, w.L.Ep, dl_bf16, s));
     MOE_CUDA(launch_to_bf16_rows(W_r, c.d, c.E, w.L.Ep, wr_bf16, s));
     RouterDxArgs ra{dl_bf16, wr_bf16, r, w.hdr(), w.tabs()};
     MOE_CUDA(launch_router_dx(c, w.L, ra, s));
@@ -510,6 +563,18 @@ moe_status_t moe_workspace_size(const moe_config_t* cfg, size_t* ws_bytes, size_
   MOE_NEED(ws_bytes != nullptr);
   *ws_bytes = make_layout(c).total;
   if (saved_bytes) *saved_bytes = saved_layout(c).total;
+  return MOE_OK;
+}
+
+moe_status_t moe_saved_layout(const moe_config_t* cfg, size_t* logits_off, size_t* logits_bytes, size_t* kept_off,
+                              size_t* kept_bytes) {
+  Cfg c;
+  MOE_TRY(make_cfg(cfg, &c));
+  const SavedLayout sl = saved_layout(c);
+  if (logits_off) *logits_off = sl.logits_off;
+  if (logits_bytes) *logits_bytes = sl.logits_bytes;
+  if (kept_off) *kept_off = sl.a_off;
+  if (kept_bytes) *kept_bytes = sl.total - sl.a_off;
   return MOE_OK;
 }
 
@@ -721,7 +786,9 @@ moe_status_t moe_layer_fwd_fp8(const moe_config_t* cfg, const moe_bf16* x, const
   MOE_TRY(check_device());
   int32_t* idx = static_cast<int32_t*>(saved);
   float* gates = reinterpret_cast<float*>(idx + (size_t)c.T * c.k);
-  MOE_TRY(do_route(c, w, x, W_r, b_r, idx, gates, nullptr, stream));
+  const SavedLayout sv = saved_layout(c);
+  float* logits = sv.logits_bytes ? reinterpret_cast<float*>(static_cast<char*>(saved) + sv.logits_off) : nullptr;
+  MOE_TRY(do_route(c, w, x, W_r, b_r, idx, gates, logits, stream));
   // Forward-only scratch in the backward's buffers.  The T token rows are quantised once (codes and
   // scales in buf_d1, free until the down projection writes o_perm there), and the dispatch gathers
   // their codes and scales into the padded expert rows (in dy_perm: rows x d bytes + 4 rows <=
@@ -769,7 +836,9 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const moe_bf16* x, const flo
   MOE_TRY(check_device());
   int32_t* idx = static_cast<int32_t*>(saved);
   float* gates = reinterpret_cast<float*>(idx + (size_t)c.T * c.k);
-  MOE_TRY(do_route(c, w, x, W_r, b_r, idx, gates, nullptr, stream));
+  const SavedLayout sv = saved_layout(c);
+  float* logits = sv.logits_bytes ? reinterpret_cast<float*>(static_cast<char*>(saved) + sv.logits_off) : nullptr;
+  MOE_TRY(do_route(c, w, x, W_r, b_r, idx, gates, logits, stream));
   // x rows to x_perm, or (gather_in_gemm) the tables only: the gate/up GEMM then gathers the x rows
   // itself from token order (MoEBlaze summary, Methodology item 2: dispatch fused with the FFN)
   uint16_t* x_perm = w.at<uint16_t>(w.L.xperm);
@@ -780,7 +849,6 @@ moe_status_t moe_layer_fwd(const moe_config_t* cfg, const moe_bf16* x, const flo
                         stream));
   uint16_t* o_perm = w.at<uint16_t>(w.L.buf_d1);
   // kept a and b go to `saved`, which lives from this call to the backward; the workspace does not
-  const SavedLayout sv = saved_layout(c);
   uint16_t* a_keep = reinterpret_cast<uint16_t*>(static_cast<char*>(saved) + sv.a_off);
   uint16_t* b_keep = reinterpret_cast<uint16_t*>(static_cast<char*>(saved) + sv.b_off);
   FfnFwdArgs fa{x_perm, W_gate, W_up, W_down, w.at<uint16_t>(w.L.buf_f0), o_perm, w.hdr(), w.tabs(),
@@ -834,8 +902,10 @@ moe_status_t moe_layer_bwd(const moe_config_t* cfg, const moe_bf16* x, const flo
     MOE_TRY(do_ffn_bwd(c, w, x_perm, dy_perm, W_gate, W_up, W_down, dx_perm, dgates, dW_gate, dW_up, dW_down,
                        a_kept, b_kept, stream));
   float* dlogits = w.at<float>(w.L.dlogits);
-  MOE_TRY(do_router_bwd(c, w, x, W_r, b_r, idx, gates, dgates, dlogits, dW_r, db_r, stream));
-  return do_combine_bwd(c, w, dx_perm, dlogits, W_r, dx, stream);
+  const float* logits =
+      sv.logits_bytes ? reinterpret_cast<const float*>(static_cast<const char*>(saved) + sv.logits_off) : nullptr;
+  MOE_TRY(do_router_bwd_saved(c, w, x, logits, idx, gates, dgates, dlogits, dW_r, db_r, stream));
+  return do_combine_bwd(c, w, dx_perm, dlogits, W_r, dx, stream, true);
 }
 
 moe_status_t moe_quantize_cols_e4m3(const moe_bf16* top, const moe_bf16* bottom, int64_t G, int32_t rows_top,
@@ -877,8 +947,11 @@ moe_status_t moe_layer_bwd_fp8(const moe_config_t* cfg, const moe_bf16* x, const
   MOE_TRY(do_ffn_bwd_fp8(c, w, wg8, wg_scale, wu8, wu_scale, wdt8, wdt_scale, wgut8, wgut_scale, dgates, dW_gate,
                          dW_up, dW_down, stream));
   float* dlogits = w.at<float>(w.L.dlogits);
-  MOE_TRY(do_router_bwd(c, w, x, W_r, b_r, idx, gates, dgates, dlogits, dW_r, db_r, stream));
-  return do_combine_bwd(c, w, w.at<uint16_t>(w.L.buf_d1), dlogits, W_r, dx, stream);
+  const SavedLayout sv = saved_layout(c);
+  const float* logits =
+      sv.logits_bytes ? reinterpret_cast<const float*>(static_cast<const char*>(saved) + sv.logits_off) : nullptr;
+  MOE_TRY(do_router_bwd_saved(c, w, x, logits, idx, gates, dgates, dlogits, dW_r, db_r, stream));
+  return do_combine_bwd(c, w, w.at<uint16_t>(w.L.buf_d1), dlogits, W_r, dx, stream, true);
 }
 
 moe_status_t moe_check_error(void* ws, moe_stream_t stream) {

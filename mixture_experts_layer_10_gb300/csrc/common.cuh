@@ -66,7 +66,7 @@ struct Layout {
   int nscan;             // dispatch-scan blocks
   int ntf;               // 128-wide tiles over d_ff
   int ndg;               // per-row gate-gradient partials (two 64-column halves per d_ff tile)
-  int nsplit_dwr;        // token splits of dW_r = x^T dlogits
+  int nsplit_dwr;        // token splits of dW_r = x^T dlogits (router_dwr_splits)
   int nblk_router;       // router backward blocks (db partials)
   int Ep;                // E rounded up to 64: row length of the bf16 router operands
   size_t hdr, tabs, scan_status, rank, prow_of_slot, slot_of_prow, gate_of_prow, dg_part,
@@ -126,8 +126,11 @@ __device__ __forceinline__ float sigmoid_fast(float a) { return __fdividef(1.f, 
 Layout make_layout(const Cfg& c);
 // `saved` of the fused layer calls: idx int32 [T,k], gates fp32 [T,k], then (from the 256-byte
 // boundary a_off) the kept a and b [keep_rows, d_ff] bf16 one after the other.
-struct SavedLayout { size_t a_off, b_off, total; int keep; };
+struct SavedLayout { size_t logits_off, logits_bytes, a_off, b_off, total; int keep; };
 SavedLayout saved_layout(const Cfg& c);
+int router_dwr_splits(const Cfg& c);
+// tokens of each dW_r split: T / n rounded up to whole 64-token K blocks (the last split is shorter)
+inline int router_dwr_ksplit(int T, int n) { return ((T + n - 1) / n + 63) / 64 * 64; }
 moe_status_t make_cfg(const moe_config_t* in, Cfg* c);   // validate a configuration
 moe_status_t check_device();                     // MOE_OK on an sm_103 device
 int num_sms();                                   // SMs of the current device (cached)
@@ -200,7 +203,13 @@ struct RouterBwdArgs {
   float* dwr_part; float* db_part;
 };
 cudaError_t launch_router_dlogits(const Cfg& c, const Layout& L, const RouterBwdArgs& a, cudaStream_t s);
-cudaError_t launch_router_reduce(const Cfg& c, const Layout& L, const RouterBwdArgs& a, cudaStream_t s);
+// the same from the logits the layer forward kept (not read with renormalised gates): dl in fp32,
+// the bf16 rows [T, Ep] and router_saved_blocks(c) db partials
+cudaError_t launch_router_dlogits_saved(const Cfg& c, const Layout& L, const RouterBwdArgs& a, const float* logits,
+                                        uint16_t* dl_bf16, cudaStream_t s);
+int router_saved_blocks(const Cfg& c);
+// dW_r and db from their partials (nblk db partials)
+cudaError_t launch_router_reduce(const Cfg& c, const Layout& L, const RouterBwdArgs& a, int nblk, cudaStream_t s);
 // dW_r partials over token splits on the tensor cores (x and the bf16 dlogits, both MN-major)
 cudaError_t launch_router_dwr(const Cfg& c, const Layout& L, const uint16_t* x, const uint16_t* dl_bf16,
                               float* dwr_part, Hdr* hdr, const Tables* tabs, cudaStream_t s);

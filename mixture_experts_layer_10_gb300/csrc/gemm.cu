@@ -489,17 +489,17 @@ using DgradX8 = RowChan8<kKDgradXFp8>;
 // Shared by FwdDown, BwdDh and DgradX: this warp's 32 rows of the fp32 accumulator [128 x 256] ->
 // bf16 boxes of the output [rows, ncols] at row y (the warp's first row) and columns n0 + c.
 __device__ __forceinline__ void store_acc_boxes(const CUtensorMap* map, int y, int n0, int ncols, uint32_t ta,
-                                                int lane, uint8_t* ebuf) {
+                                                int lane, uint8_t* ebuf, int cbeg = 0, int cend = 256) {
   epi_begin(lane);
 #pragma unroll 1
-  for (int c = 0; c < 256; c += 32) {
+  for (int c = cbeg; c < cend; c += 32) {
     if (n0 + c >= ncols) break;
     uint32_t v[32];
     tmem_ld32(ta + c, v);
     tmem_ld_wait();
     uint32_t pk[16];
     pack32(v, pk);
-    uint8_t* box = claim_box(ebuf, c / 32, lane);
+    uint8_t* box = claim_box(ebuf, (c - cbeg) / 32, lane);
     stage_box(box, lane, pk);
     store_box_2d(map, box, lane, n0 + c, y);
   }
@@ -980,14 +980,15 @@ using WgradG = WgradT<true>;
 
 // Router weight gradient on the tensor cores: partial[split][i][e] = sum over the split's tokens of
 // x[t][i] dl[t][e].  M = d_model in 128-row tiles (A = x, MN-major), N = E padded to 64 (B = the
-// bf16 dlogits [T, Ep], MN-major), K = the split's tokens (tensor maps zero-fill past T).  Four B
-// boxes are always loaded; boxes past Ep are zero-filled and never read by the MMA.  The splits are
-// summed in a fixed order afterwards, so the result is deterministic.
-struct RouterDwr : PolicyDefaults {
+// bf16 dlogits [T, Ep], MN-major, NB = Ep / 64 boxes), K = the split's tokens (tensor maps zero-fill
+// past T).  The product is one read of x, so the stages are sized by NB: as many as fit, to keep
+// x in flight.  The splits are summed in a fixed order afterwards, so the result is deterministic.
+template <int NB>
+struct RouterDwrT : PolicyDefaults {
   static constexpr int kId = kKRouterDwr;
   static constexpr int kEpiWarps = 4;
-  static constexpr int kStages = 4;
-  static constexpr uint32_t kStageBytes = 2 * kBox + 4 * kBox;
+  static constexpr uint32_t kStageBytes = (2 + NB) * kBox;
+  static constexpr int kStages = (int)(196u * 1024u / kStageBytes) < 8 ? (int)(196u * 1024u / kStageBytes) : 8;
   static constexpr int kAccCols = 256;
   static constexpr int kAccBufs = 2;
   static constexpr int kTmemCols = 512;
@@ -1018,7 +1019,7 @@ struct RouterDwr : PolicyDefaults {
     tma_load_2d(st, &p.tmX, bar, j.m0, row);
     tma_load_2d(st + kBox, &p.tmX, bar, j.m0 + 64, row);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) tma_load_2d(st + (2 + i) * kBox, &p.tmDL, bar, 64 * i, row);
+    for (int i = 0; i < NB; ++i) tma_load_2d(st + (2 + i) * kBox, &p.tmDL, bar, 64 * i, row);
   }
   __device__ static void mma(const Job& j, int kit, uint32_t sa, uint32_t dt, int) {
 #pragma unroll
@@ -1051,11 +1052,12 @@ struct RouterDwr : PolicyDefaults {
 
 // The router's share of the input gradient on the tensor cores: r[t] = dl[t] W_r^T (M = 128
 // tokens, N = 256 columns of d_model, K = E padded to 64, both operands bf16 K-major), stored as
-// bf16 [T, d] for the token-owner combine that adds the expert rows.
+// bf16 [T, d] for the token-owner combine that adds the expert rows.  With K this short the kernel
+// is its output stores: two epilogue warps per TMEM lane quarter each store half of the columns.
 struct RouterDx : PolicyDefaults {
   static constexpr int kId = kKRouterDx;
-  static constexpr int kEpiWarps = 4;
-  static constexpr int kStages = 4;
+  static constexpr int kEpiWarps = 8;
+  static constexpr int kStages = 3;
   static constexpr uint32_t kStageBytes = kTileA + 2 * kTileA;   // dl tile + W_r tile (256 rows)
   static constexpr int kAccCols = 256;
   static constexpr int kAccBufs = 2;
@@ -1092,10 +1094,11 @@ struct RouterDx : PolicyDefaults {
       umma_bf16(dt, sdesc_kmajor(sa + kk * 32), sdesc_kmajor(sa + kTileA + kk * 32), kIdesc,
                 (kit | kk) != 0);
   }
-  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int, int, uint8_t* ebuf) {
+  __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int part, int,
+                                  uint8_t* ebuf) {
     const int y = j.m0 + (row & ~31);
     if (y >= p.T) return;   // the tile's last warps may lie past the tokens
-    store_acc_boxes(&p.tmR, y, j.n0, p.d, ta, row & 31, ebuf);
+    store_acc_boxes(&p.tmR, y, j.n0, p.d, ta, row & 31, ebuf, 128 * part, 128 * part + 128);
   }
   __device__ static void epilogue_zero(const Params&, const Job&, int, int) {}
 };
@@ -1247,6 +1250,21 @@ struct RouterLogits : PolicyDefaults {
       l[i] = e < p.E ? __uint_as_float(v[i]) + (p.b_r != nullptr ? p.b_r[e] : 0.f) : -INFINITY;
     }
   }
+  // Logits [c, c + 32) of token t: 16-byte stores when the rows are 16-byte aligned (E a multiple
+  // of 4, so a group of four is wholly below E or wholly past it), else one value at a time.
+  __device__ static void store_logits(const Params& p, int t, int c, const float (&l)[32]) {
+    float* row = p.logits + (size_t)t * p.E;
+    if ((p.E & 3) == 0) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        if (c + 4 * q < p.E)
+          *reinterpret_cast<float4*>(row + c + 4 * q) = make_float4(l[4 * q], l[4 * q + 1], l[4 * q + 2], l[4 * q + 3]);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 32; ++i)
+        if (c + i < p.E) row[c + i] = l[i];
+    }
+  }
   // The two parts of a quarter (warps 4 apart) meet on a barrier of two arrivals, one per warp,
   // after each warp's shared-memory writes; the wait is bounded, so a partner that gave up leaves
   // an error instead of a hang.
@@ -1288,9 +1306,9 @@ struct RouterLogits : PolicyDefaults {
 #pragma unroll
       for (int i = 0; i < 32; ++i) z += (c + i < p.E) ? expf(l[i] - m) : 0.f;
       if (!kBwd) {
+        if (live && p.logits != nullptr) store_logits(p, t, c, l);
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          if (live && p.logits != nullptr && c + i < p.E) p.logits[(size_t)t * p.E + c + i] = l[i];
           float cv = l[i];
           int ci = c + i;
 #pragma unroll
@@ -2226,9 +2244,10 @@ cudaError_t launch_ffn_bwd_fp8(const Cfg& c, const Layout& L, const FfnBwd8Args&
   return launch_pair<DgradX8>(p3, s);
 }
 
-cudaError_t launch_router_dwr(const Cfg& c, const Layout& L, const uint16_t* x, const uint16_t* dl_bf16,
-                              float* dwr_part, Hdr* hdr, const Tables* tabs, cudaStream_t s) {
-  RouterDwr::Params p{};
+template <int NB>
+cudaError_t launch_router_dwr_nb(const Cfg& c, const Layout& L, const uint16_t* x, const uint16_t* dl_bf16,
+                                 float* dwr_part, Hdr* hdr, const Tables* tabs, cudaStream_t s) {
+  typename RouterDwrT<NB>::Params p{};
   if (!map_2d(&p.tmX, x, c.d, c.T, 64, 64) || !map_2d(&p.tmDL, dl_bf16, L.Ep, c.T, 64, 64))
     return cudaErrorInvalidValue;
   p.part = dwr_part;
@@ -2238,10 +2257,20 @@ cudaError_t launch_router_dwr(const Cfg& c, const Layout& L, const uint16_t* x, 
   p.T = c.T;
   p.mt = (c.d + kBM - 1) / kBM;
   p.nsplit = L.nsplit_dwr;
-  p.ksplit = ((c.T + L.nsplit_dwr - 1) / L.nsplit_dwr + kBK - 1) / kBK * kBK;
+  p.ksplit = router_dwr_ksplit(c.T, L.nsplit_dwr);
   p.hdr = hdr;
   p.tabs = tabs;
-  return launch<RouterDwr>(p, s);
+  return launch<RouterDwrT<NB>>(p, s);
+}
+
+cudaError_t launch_router_dwr(const Cfg& c, const Layout& L, const uint16_t* x, const uint16_t* dl_bf16,
+                              float* dwr_part, Hdr* hdr, const Tables* tabs, cudaStream_t s) {
+  switch (L.Ep / 64) {
+    case 1: return launch_router_dwr_nb<1>(c, L, x, dl_bf16, dwr_part, hdr, tabs, s);
+    case 2: return launch_router_dwr_nb<2>(c, L, x, dl_bf16, dwr_part, hdr, tabs, s);
+    case 3: return launch_router_dwr_nb<3>(c, L, x, dl_bf16, dwr_part, hdr, tabs, s);
+    default: return launch_router_dwr_nb<4>(c, L, x, dl_bf16, dwr_part, hdr, tabs, s);
+  }
 }
 
 template <bool kBwd, bool kSplit>

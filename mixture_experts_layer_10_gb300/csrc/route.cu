@@ -346,6 +346,131 @@ __global__ void __launch_bounds__(kThreads) router_dlogits_kernel(RouterBwdArgs 
   }
 }
 
+// Router backward, part 1, from the logits the layer forward kept: no second pass over x.  Per
+// token, with s = sum_j dg_j g_j (in slot order):
+//   gates not renormalised: p = softmax(logits), dl_e = p_e (dg_slot(e) [e selected] - s);
+//   renormalised:           dl_{idx_j} = g_j (dg_j - s), 0 elsewhere (the logits are not read).
+// Outputs: dl in fp32 [T, E], as the bf16 operand row [T, Ep] of the dW_r and dx products (zero
+// past E), and one db partial per 32 tokens.  A block takes 32 tokens, four per warp; G = min(32,
+// EB) lanes share a token, lane i of a group holding experts i, i + G, ... and (k <= G) slot i of
+// the token; the group's max and sum are xor shuffles within it.  Every load of a warp's four
+// tokens is issued before the arithmetic of the first (the kernel is bound by memory latency).
+// db: each lane adds its tokens in order, then one thread per expert adds the groups in
+// (warp, group) order -- a fixed order.
+template <int EB>
+__global__ void __launch_bounds__(kThreads) router_dlogits_saved_kernel(RouterBwdArgs a, const float* __restrict__ logits,
+                                                                        uint16_t* __restrict__ dl_bf16, int T, int E,
+                                                                        int Ep, int k, int renorm) {
+  constexpr int G = EB < 32 ? EB : 32;   // lanes per token
+  constexpr int TPW = 32 / G;            // tokens per warp pass
+  constexpr int NV = EB / G;             // experts per lane
+  constexpr int kTokens = 32;            // tokens per block (one db partial)
+  constexpr int kWarps = kThreads / 32;
+  constexpr int kPerWarp = kTokens / kWarps;
+  constexpr int P = kPerWarp / TPW;      // passes per warp
+  static_assert(kPerWarp % TPW == 0, "whole passes per warp");
+  __shared__ float red[kWarps * TPW * EB];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int grp = lane / G, li = lane % G, g0 = lane - li;
+  const bool slots_in_lanes = k <= G;    // else each lane walks the token's slots itself
+  // every pass's loads first (rows past T load nothing; every lane runs every pass, since the
+  // shuffles below take the whole warp)
+  int sid[P];
+  float sg[P], sdg[P], lv[P][NV];
+#pragma unroll
+  for (int ps = 0; ps < P; ++ps) {
+    const int t = blockIdx.x * kTokens + warp * kPerWarp + ps * TPW + grp;
+    const bool live = t < T;
+    sid[ps] = -1;
+    sg[ps] = sdg[ps] = 0.f;
+    if (live && slots_in_lanes && li < k) {
+      sid[ps] = a.idx[(size_t)t * k + li];
+      sg[ps] = a.gates[(size_t)t * k + li];
+      sdg[ps] = a.dgates[(size_t)t * k + li];
+    }
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int e = li + G * i;
+      lv[ps][i] = (!renorm && live && e < E) ? logits[(size_t)t * E + e] : -INFINITY;
+    }
+  }
+  float dbacc[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) dbacc[i] = 0.f;
+#pragma unroll
+  for (int ps = 0; ps < P; ++ps) {
+    const int t = blockIdx.x * kTokens + warp * kPerWarp + ps * TPW + grp;
+    const bool live = t < T;
+    const int tl = live ? t : 0;
+    float s = 0.f;
+    float dsel[NV];
+#pragma unroll
+    for (int i = 0; i < NV; ++i) dsel[i] = 0.f;
+    if (slots_in_lanes) {
+      for (int j = 0; j < k; ++j) s += __shfl_sync(0xffffffffu, sdg[ps] * sg[ps], g0 + j);
+      for (int j = 0; j < k; ++j) {
+        const int e = __shfl_sync(0xffffffffu, sid[ps], g0 + j);
+        const float dg = __shfl_sync(0xffffffffu, sdg[ps], g0 + j);
+        const float g = __shfl_sync(0xffffffffu, sg[ps], g0 + j);
+        const float v = renorm ? g * (dg - s) : dg;
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+          if (e == li + G * i) dsel[i] += v;
+      }
+    } else {
+      for (int j = 0; j < k; ++j) s += a.dgates[(size_t)tl * k + j] * a.gates[(size_t)tl * k + j];
+      for (int j = 0; j < k; ++j) {
+        const int e = a.idx[(size_t)tl * k + j];
+        const float dg = a.dgates[(size_t)tl * k + j];
+        const float v = renorm ? a.gates[(size_t)tl * k + j] * (dg - s) : dg;
+#pragma unroll
+        for (int i = 0; i < NV; ++i)
+          if (e == li + G * i) dsel[i] += v;
+      }
+    }
+    float dl[NV];
+    if (renorm) {
+#pragma unroll
+      for (int i = 0; i < NV; ++i) dl[i] = li + G * i < E ? dsel[i] : 0.f;
+    } else {
+      float m = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) m = fmaxf(m, lv[ps][i]);
+#pragma unroll
+      for (int off = G / 2; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      float ex[NV], z = 0.f;
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        ex[i] = li + G * i < E ? expf(lv[ps][i] - m) : 0.f;
+        z += ex[i];
+      }
+#pragma unroll
+      for (int off = G / 2; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+#pragma unroll
+      for (int i = 0; i < NV; ++i) dl[i] = li + G * i < E ? ex[i] / z * (dsel[i] - s) : 0.f;
+    }
+    if (!live) continue;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int e = li + G * i;
+      if (e < E) a.dlogits[(size_t)t * E + e] = dl[i];
+      if (e < Ep) dl_bf16[(size_t)t * Ep + e] = (uint16_t)(pack_bf16(dl[i], 0.f) & 0xFFFFu);
+      dbacc[i] += dl[i];
+    }
+    // columns [EB, Ep) of the bf16 row are zero (EB < Ep only for E <= 32: 16-byte pieces)
+    for (int c = EB + 8 * li; c < Ep; c += 8 * G)
+      *reinterpret_cast<uint4*>(dl_bf16 + (size_t)t * Ep + c) = make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int i = 0; i < NV; ++i) red[(warp * TPW + grp) * EB + li + G * i] = dbacc[i];
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kThreads) {
+    float v = 0.f;
+    for (int r = 0; r < kWarps * TPW; ++r) v += red[r * EB + e];
+    a.db_part[(size_t)blockIdx.x * E + e] = v;
+  }
+}
+
 // Router backward, part 3: fixed-order sums of the dW_r and db partials.  The first dw_blocks
 // blocks sum dW_r element by element over the splits; then one warp per expert sums its db
 // partials, lane l taking blocks l, l + 32, ... and a shuffle tree of fixed shape joining the lanes
@@ -445,6 +570,9 @@ __global__ void to_bf16_rows_kernel(const float* __restrict__ src, int rows, int
 
 }  // namespace
 
+// blocks (and db partials) of router_dlogits_saved_kernel: 32 tokens each
+int router_saved_blocks(const Cfg& c) { return (c.T + 31) / 32; }
+
 int route_block_tokens(int E) {
   switch (bucket_of(E)) {
     case 8: return RouteShape<8>::BT;
@@ -478,12 +606,35 @@ cudaError_t launch_router_dlogits(const Cfg& c, const Layout& L, const RouterBwd
   }
 }
 
-cudaError_t launch_router_reduce(const Cfg& c, const Layout& L, const RouterBwdArgs& a, cudaStream_t s) {
+template <int EB>
+cudaError_t router_dlogits_saved_eb(const Cfg& c, const Layout& L, const RouterBwdArgs& a, const float* logits,
+                                    uint16_t* dl_bf16, cudaStream_t s) {
+  prof_mark(kKRouterDlogits, s, true);
+  router_dlogits_saved_kernel<EB><<<router_saved_blocks(c), kThreads, 0, s>>>(a, logits, dl_bf16, c.T, c.E, L.Ep, c.k,
+                                                                              c.renorm);
+  prof_mark(kKRouterDlogits, s, false);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_dlogits_saved(const Cfg& c, const Layout& L, const RouterBwdArgs& a, const float* logits,
+                                        uint16_t* dl_bf16, cudaStream_t s) {
+  if (!c.renorm && logits == nullptr) return cudaErrorInvalidValue;
+  switch (bucket_of(c.E)) {
+    case 8: return router_dlogits_saved_eb<8>(c, L, a, logits, dl_bf16, s);
+    case 16: return router_dlogits_saved_eb<16>(c, L, a, logits, dl_bf16, s);
+    case 32: return router_dlogits_saved_eb<32>(c, L, a, logits, dl_bf16, s);
+    case 64: return router_dlogits_saved_eb<64>(c, L, a, logits, dl_bf16, s);
+    case 128: return router_dlogits_saved_eb<128>(c, L, a, logits, dl_bf16, s);
+    default: return router_dlogits_saved_eb<256>(c, L, a, logits, dl_bf16, s);
+  }
+}
+
+cudaError_t launch_router_reduce(const Cfg& c, const Layout& L, const RouterBwdArgs& a, int nblk, cudaStream_t s) {
   const size_t n = (size_t)c.d * c.E;
   const int dw_blocks = (int)std::max<size_t>(1, std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 4));
   const int db_blocks = a.db_r != nullptr ? (c.E + 7) / 8 : 0;   // 8 warps, one expert each
   prof_mark(kKRouterReduce, s, true);
-  router_reduce_kernel<<<dw_blocks + db_blocks, 256, 0, s>>>(a, c.d, c.E, L.nsplit_dwr, L.nblk_router, dw_blocks);
+  router_reduce_kernel<<<dw_blocks + db_blocks, 256, 0, s>>>(a, c.d, c.E, L.nsplit_dwr, nblk, dw_blocks);
   prof_mark(kKRouterReduce, s, false);
   return cudaGetLastError();
 }

@@ -121,10 +121,21 @@ __device__ __forceinline__ void finish_token(const Params& p, const float (&l)[E
       tv[s] = -INFINITY;
       ti[s] = 0x7fffffff;
     }
+    if (p.logits != nullptr) {   // 16-byte stores when the rows are 16-byte aligned (E a multiple of 4)
+      float* row = p.logits + (size_t)t * p.E;
+      if ((p.E & 3) == 0) {
+#pragma unroll
+        for (int q = 0; q < EB / 4; ++q)
+          if (4 * q < p.E) *reinterpret_cast<float4*>(row + 4 * q) = make_float4(l[4 * q], l[4 * q + 1], l[4 * q + 2], l[4 * q + 3]);
+      } else {
+#pragma unroll
+        for (int e = 0; e < EB; ++e)
+          if (e < p.E) row[e] = l[e];
+      }
+    }
 #pragma unroll
     for (int e = 0; e < EB; ++e) {
       if (e >= p.E) continue;
-      if (p.logits != nullptr) p.logits[(size_t)t * p.E + e] = l[e];
       float cv = l[e];
       int ci = e;
 #pragma unroll
@@ -212,6 +223,30 @@ __global__ void __launch_bounds__(kThreads, 1) route_stream_kernel(const __grid_
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // this CTA's (tile, slice) pairs, tiles outer
+  const long long sl0 = range_first(blockIdx.x, p.nsl, p.nranges);
+  const long long sl1 = range_first(blockIdx.x + 1, p.nsl, p.nranges);
+  // the producer's position (thread 0): the next (tile, slice) pair, its next K block and stage
+  long long lsp = sl0;
+  int lkb = (int)(sl0 % p.nslice) * kSliceKB;
+  int stage = 0, uses = 0;
+  uint32_t phase = 0;
+  auto issue = [&]() {   // one stage's loads at the producer's position, then step past it
+    const int tile = (int)(lsp / p.nslice), sl = (int)(lsp - (long long)tile * p.nslice);
+    uint8_t* st = stages + (size_t)stage * S::kStageBytes;
+    mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
+    tma_load_2d(st, &p.tmX, &full[stage], lkb * kKB, tile * kTok);
+    tma_load_2d(st + kXBytes, &p.tmW, &full[stage], lkb * kKB, 0);
+    ++uses;
+    if (++stage == S::kStages) {
+      stage = 0;
+      phase ^= 1;
+    }
+    if (++lkb >= min(p.nkb, (sl + 1) * kSliceKB)) {
+      ++lsp;
+      lkb = (int)(lsp % p.nslice) * kSliceKB;
+    }
+  };
   if (threadIdx.x == 0) {
     for (int s = 0; s < S::kStages; ++s) {
       mbar_init(&full[s], 1);
@@ -226,6 +261,9 @@ __global__ void __launch_bounds__(kThreads, 1) route_stream_kernel(const __grid_
     fence_mbar_init();
     tma_prefetch(&p.tmX);
     tma_prefetch(&p.tmW);
+    // a fresh ring needs no wait: the first stages' loads leave before the block's setup (TMEM
+    // allocation, the barrier), so that the setup overlaps their trip to memory
+    while (uses < S::kStages && lsp < sl1) issue();
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -236,34 +274,16 @@ __global__ void __launch_bounds__(kThreads, 1) route_stream_kernel(const __grid_
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   const uint64_t limit = wait_limit_ns(p.hdr);
-  // this CTA's (tile, slice) pairs, tiles outer
-  const long long sl0 = range_first(blockIdx.x, p.nsl, p.nranges);
-  const long long sl1 = range_first(blockIdx.x + 1, p.nsl, p.nranges);
 
   if (warp == 0) {
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int uses = 0;
-      for (long long sp = sl0; sp < sl1 && !*abort_flag; ++sp) {
-        const int tile = (int)(sp / p.nslice), sl = (int)(sp - (long long)tile * p.nslice);
-        const int kb1 = min(p.nkb, (sl + 1) * kSliceKB);
-        for (int kb = sl * kSliceKB; kb < kb1; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, limit, abort_flag)) {
-            record_error(p.hdr, MOE_ERR_TIMEOUT, kSiteGemmProducer);
-            *abort_flag = 1;
-            break;
-          }
-          uint8_t* st = stages + (size_t)stage * S::kStageBytes;
-          mbar_arrive_expect_tx(&full[stage], S::kStageBytes);
-          tma_load_2d(st, &p.tmX, &full[stage], kb * kKB, tile * kTok);
-          tma_load_2d(st + kXBytes, &p.tmW, &full[stage], kb * kKB, 0);
-          ++uses;
-          if (++stage == S::kStages) {
-            stage = 0;
-            phase ^= 1;
-          }
+      while (lsp < sl1 && !*abort_flag) {
+        if (!mbar_wait(&empty[stage], phase ^ 1, limit, abort_flag)) {
+          record_error(p.hdr, MOE_ERR_TIMEOUT, kSiteGemmProducer);
+          *abort_flag = 1;
+          break;
         }
+        issue();
       }
       // every load this CTA issued lands before its shared memory is released (bounded)
       drain_fills(full, S::kStages, stage, phase, uses, limit);

@@ -64,11 +64,15 @@ def memory(cfg: dict) -> dict:
     workspace = (rows * per_row + T * k * 12 + T * E * 4 + T * Ep * 2 + 4 * d * Ep * 2
                  + math.ceil(T * k / 4096) * E * 4)
     keep = kept_rows(cfg)
-    saved = 8 * T * k if keep == 0 else math.ceil(8 * T * k / 256) * 256 + keep * f * 2 * 2
+    saved = 8 * T * k                  # idx, gates
+    if not cfg.get("renorm", 0):       # the logits, for the backward's softmax
+        saved = math.ceil(saved / 256) * 256 + T * E * 4
+    if keep:
+        saved = math.ceil(saved / 256) * 256 + keep * f * 2 * 2
     return {
         "padded_rows": rows,
         "workspace": workspace,
-        "saved": saved,                   # idx, gates and the kept a, b: what lives fwd -> bwd
+        "saved": saved,                   # idx, gates, logits and the kept a, b: what lives fwd -> bwd
         "weights": 3 * G * d * f * 2 + d * E * 4,
         "weight_grads": 3 * G * d * f * 2 + d * E * 4,
         "token_tensors": 4 * T * d * 2,   # x, y, dy, dx
@@ -86,8 +90,9 @@ def work(cfg: dict, N: int | None = None, kept_rows: int = 0) -> dict:
     R = N + S * T                                      # rows the experts see
     Ep = math.ceil(E / 64) * 64
     nr = router_n(E, k)
+    logits = 0 if cfg.get("renorm", 0) else T * E * 4   # kept by the forward for the backward
     out = {
-        "route_fwd": {"flops": 2 * T * d * nr, "bytes": T * d * 2},
+        "route_fwd": {"flops": 2 * T * d * nr, "bytes": T * d * 2 + logits},
         "dispatch_gather": {"flops": 0, "bytes": 3 * (T + R) * d * 2 + 36 * T * k},
         "gemm_gate_up_swiglu": {"flops": 4 * R * d * f, "bytes": 0},
         "gemm_down": {"flops": 2 * R * d * f, "bytes": 0},
@@ -96,7 +101,7 @@ def work(cfg: dict, N: int | None = None, kept_rows: int = 0) -> dict:
         "gemm_bwd_recompute_swiglu": {"flops": 4 * (R - kept_rows) * d * f, "bytes": 0},
         "gemm_wgrad": {"flops": 6 * R * d * f, "bytes": 0},
         "gemm_dgrad_x": {"flops": 4 * R * d * f, "bytes": 0},
-        "router_dlogits": {"flops": 2 * T * d * nr, "bytes": T * d * 2},
+        "router_dlogits": {"flops": 0, "bytes": 12 * T * k + logits + T * E * 4 + T * Ep * 2},
         "router_dwr": {"flops": 2 * T * d * Ep, "bytes": T * d * 2},
         "gemm_router_dx": {"flops": 2 * T * d * Ep, "bytes": T * d * 2},
         "combine_bwd": {"flops": 0, "bytes": (R + 2 * T) * d * 2 + 4 * T * k},
@@ -166,7 +171,8 @@ def predict_ms_calibrated(cfg: dict, tensor_tflops: float, hbm_gbs: float, N: in
         elif name in ("dispatch_gather", "combine", "combine_bwd", "swiglu_bwd_kept"):
             per[name] = 1e3 * v["bytes"] / (EFF_HBM * bw)
     Ep = math.ceil(E / 64) * 64
-    for name in ("route_fwd", "router_dlogits"):
+    per["router_dlogits"] = 1e3 * (w["router_dlogits"]["bytes"] / (EFF_HBM * bw) + SMALL_US * 1e-6)
+    for name in ("route_fwd",):
         if E <= 32 and k <= 8:
             t = T * d * 2 / (EFF_HBM * bw) + ROUTER_FIXED_US * 1e-6
         elif E <= 128 and k <= 8:
@@ -193,7 +199,8 @@ def work_forward(cfg: dict, N: int | None = None, fp8: bool = False) -> dict:
     T, d, f, E, k, S = cfg["T"], cfg["d"], cfg["f"], cfg["E"], cfg["k"], cfg.get("S", 0)
     N = T * k if N is None else N
     R = N + S * T
-    out = {"route_fwd": {"flops": 2 * T * d * router_n(E, k), "bytes": T * d * 2}}
+    logits = 0 if cfg.get("renorm", 0) else T * E * 4   # kept for the backward
+    out = {"route_fwd": {"flops": 2 * T * d * router_n(E, k), "bytes": T * d * 2 + logits}}
     if fp8:
         out["quantize_e4m3 (x)"] = {"flops": 0, "bytes": T * d * 3 + 4 * T}
         out["dispatch_gather"] = {"flops": 0, "bytes": (T + R) * d + 8 * R + 12 * T * k}

@@ -38,13 +38,20 @@ def test_status_strings(lib):
 def test_workspace_size_and_rows():
     c = moe.config(T=8192, d=4096, f=14336, E=8, k=2)
     ws, saved = moe.moe_workspace_size(c)
-    assert saved == 8192 * 2 * 8
+    assert saved == 8192 * 2 * 8 + 8192 * 8 * 4          # idx, gates; the logits (256-aligned here)
+    assert moe.moe_saved_layout(c) == (8192 * 2 * 8, 8192 * 8 * 4, saved, 0)
     rows = moe.moe_perm_rows(c)
     # routed rows padded per expert to 256, all segment starts multiples of 256
     assert rows % 256 == 0 and rows >= 8192 * 2 + 255 * 8
     assert ws > 3 * rows * 14336 * 2
     c2 = moe.config(T=16384, d=2048, f=1408, E=64, k=6, S=2, renorm=1)
     assert moe.moe_perm_rows(c2) >= 16384 * 6 + 2 * 16384
+    # renormalised gates keep no logits; odd sizes start the logits and kept rows on 256 bytes
+    assert moe.moe_saved_layout(c2)[:2] == (0, 0) and moe.moe_workspace_size(c2)[1] == 16384 * 6 * 8
+    c3 = moe.config(T=100, d=64, f=64, E=3, k=1, keep_rows=256)
+    lo, lb, ko, kb = moe.moe_saved_layout(c3)
+    assert (lo, lb) == (1024, 1200) and ko == 2304 and kb == 2 * 256 * 64 * 2
+    assert moe.moe_workspace_size(c3)[1] == ko + kb
 
 
 @pytest.mark.parametrize("bad", [

@@ -4,7 +4,7 @@
   bit-exact, both sides deciding in fp32;
 * moe_layer_bwd_fp8 on the small workloads: dx, dW_r, db_r and the expert weight gradients against
   oracle.fp8.layer_backward_fp8 under the bf16 output rule, given identical assignments (the
-  oracle's idx and gates are written into `saved`, so the backward differentiates the oracle's
+  oracle's idx, gates and logits are written into `saved`, so the backward differentiates the oracle's
   routed layer; nothing flows from the GPU into the oracle);
 * the same at the four large workloads' full sizes on sampled tokens (dx, dgates) and sampled
   hidden units (whole weight-gradient rows and columns).
@@ -73,13 +73,17 @@ def _weight_codes(moe, Wg, Wu, Wd, G, f, d):
 
 
 def run_bwd_fp8(moe, c, inp, R):
-    """moe_layer_bwd_fp8 from the oracle's assignment R (idx, gates rounded to fp32) in `saved`."""
+    """moe_layer_bwd_fp8 from the oracle's assignment R (idx; gates and logits rounded to fp32) in
+    `saved`."""
     mc = moe.config_from(c)
     buf = moe.Buffers.allocate(mc)
     T, d, f, E, S, k = c["T"], c["d"], c["f"], c["E"], c["S"], c["k"]
     G = E + S
-    buf.saved.view(torch.int32)[:T * k].copy_(to_dev(R.idx.astype(np.int32)).view(-1))
-    buf.saved.view(torch.float32)[T * k:2 * T * k].copy_(to_dev(R.gates.astype(np.float32)).view(-1))
+    idx_v, gates_v, logits_v = buf.saved_views()
+    idx_v.copy_(to_dev(R.idx.astype(np.int32)))
+    gates_v.copy_(to_dev(R.gates.astype(np.float32)))
+    if logits_v is not None:
+        logits_v.copy_(to_dev(R.logits.astype(np.float32)))
     x, Wg, Wu, Wd, dy = (to_dev_bf16(inp[n]) for n in ("x", "W_gate", "W_up", "W_down", "dy"))
     codes = _weight_codes(moe, Wg, Wu, Wd, G, f, d)
     out = dict(dx=torch.full((T, d), float("nan"), dtype=torch.bfloat16, device="cuda"),

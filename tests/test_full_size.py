@@ -50,12 +50,15 @@ def full(request, moe):
     idx_fwd = from_dev(buf.saved.view(torch.int32)[:T * k].view(T, k))
     gates_fwd = from_dev(buf.saved.view(torch.float32)[T * k:2 * T * k].view(T, k))
     # The gradients depend on every token's assignment.  Where a near-tie went the other way on the
-    # GPU, the backward runs from the oracle's assignment (idx and fp32 gates written into `saved`),
+    # GPU, the backward runs from the oracle's assignment (idx, fp32 gates and logits in `saved`),
     # so the gradient checks below compare the same routed layer; nothing flows into the oracle.
     R = L.routing()
     if not np.array_equal(idx_fwd, R.idx):
-        buf.saved.view(torch.int32)[:T * k].copy_(to_dev(R.idx.astype(np.int32)).view(-1))
-        buf.saved.view(torch.float32)[T * k:2 * T * k].copy_(to_dev(R.gates.astype(np.float32)).view(-1))
+        idx_v, gates_v, logits_v = buf.saved_views()
+        idx_v.copy_(to_dev(R.idx.astype(np.int32)))
+        gates_v.copy_(to_dev(R.gates.astype(np.float32)))
+        if logits_v is not None:
+            logits_v.copy_(to_dev(R.logits.astype(np.float32)))
     moe.moe_layer_bwd(mc, dev["x"], dev["W_r"], dev["b_r"], dev["Wg"], dev["Wu"], dev["Wd"], buf.saved, dev["dy"],
                       dx, dW_r, db_r, dWg, dWu, dWd, buf.ws)
     assert moe.moe_check_error(buf.ws) == 0

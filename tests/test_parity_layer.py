@@ -65,11 +65,17 @@ def check_layer(moe, c, inp, L, out, buf):
     before it (its own, and with a capacity those of earlier tokens), so it is compared on the
     tokens whose routing agrees (with a capacity: before the first difference).  The gradients
     depend on every token's assignment: when a near-tie went the other way on the GPU, the
-    oracle's assignment is fed to the GPU backward (its idx and gates written into `saved`) and
+    oracle's assignment is fed to the GPU backward (its idx, gates and logits written into `saved`) and
     the backward runs again, so that both sides differentiate the same routed layer.  Nothing
     flows from the GPU into the oracle."""
     R = L.routing()
     same = check_routing(from_dev(out["idx"]), from_dev(out["gates"]), R, c["k"])
+    _, _, lg = buf.saved_views()
+    if lg is not None:   # the logits the forward keeps for the backward's softmax (bias included)
+        lgv = from_dev(lg).astype(np.float64)
+        assert np.max(np.abs(lgv - R.logits) / (1.0 + np.abs(R.logits))) < 2e-5
+    else:
+        assert c["renorm"]
     y_ref, _ = L.forward()
     g = L.backward()
     rows = np.flatnonzero(same)
@@ -88,7 +94,8 @@ def check_layer(moe, c, inp, L, out, buf):
 
 def backward_on_oracle_assignment(moe, c, inp, R, buf):
     """The GPU backward from the oracle's idx and gates (gates rounded to fp32).  Without kept
-    activations: written into `saved`, then moe_layer_bwd.  With them, the backward needs the
+    activations: written into `saved` with the oracle's logits (rounded to fp32; gates not
+    renormalised), then moe_layer_bwd.  With them, the backward needs the
     forward's kept a and b of the same dispatch, which moe_layer_fwd (its own routing) cannot give:
     the granular calls run instead on the oracle's assignment -- moe_dispatch, moe_expert_ffn_fwd
     (keeping a, b in the workspace), moe_expert_ffn_bwd, moe_router_bwd, moe_combine_bwd."""
@@ -120,8 +127,11 @@ def backward_on_oracle_assignment(moe, c, inp, R, buf):
         moe.moe_router_bwd(mc, x, W_r, b_r, idx, gates, dgates, dlogits, out["dW_r"], out["db_r"], buf.ws)
         moe.moe_combine_bwd(mc, dx_perm, dlogits, W_r, out["dx"], buf.ws)
     else:
-        buf.saved.view(torch.int32)[:T * k].copy_(idx.view(-1))
-        buf.saved.view(torch.float32)[T * k:2 * T * k].copy_(gates.view(-1))
+        idx_v, gates_v, logits_v = buf.saved_views()
+        idx_v.copy_(idx)
+        gates_v.copy_(gates)
+        if logits_v is not None:   # the backward's softmax reads the oracle's logits as well
+            logits_v.copy_(to_dev(R.logits.astype(np.float32)))
         moe.moe_layer_bwd(mc, x, W_r, b_r, Wg, Wu, Wd, buf.saved, dy, out["dx"], out["dW_r"], out["db_r"],
                           out["dWg"], out["dWu"], out["dWd"], buf.ws)
     status = moe.moe_check_error(buf.ws)

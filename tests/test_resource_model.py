@@ -33,9 +33,10 @@ def test_gemm_flops_closed_form(name):
 def test_kept_activation_bytes():
     cfg = dict(synth.CONFIGS["mixtral"], keep_rows=1000)
     assert rm.memory(cfg)["kept_activations"] == 768 * 14336 * 4    # rounded down to 256 rows
-    # the fused calls keep them in `saved`, after idx and gates (from a 256-byte boundary)
+    # the fused calls keep them in `saved`, after idx, gates and the logits (each from a 256-byte
+    # boundary)
     _, saved = moe.moe_workspace_size(moe.config_from(cfg))
-    assert saved == rm.memory(cfg)["saved"] == 8192 * 2 * 8 + 768 * 14336 * 4
+    assert saved == rm.memory(cfg)["saved"] == 8192 * 2 * 8 + 8192 * 8 * 4 + 768 * 14336 * 4
 
 
 @pytest.mark.parametrize("name", WORKLOADS)
