@@ -1027,18 +1027,30 @@ struct RouterDwrT : PolicyDefaults {
       umma_bf16(dt, sdesc_mnmajor(sa + kk * 2048, kBox), sdesc_mnmajor(sa + 2 * kBox + kk * 2048, kBox),
                 j.idesc, (kit | kk) != 0);
   }
+  // Row m of the partial, E floats from part + (split d + m) E: 16-byte stores when the rows are
+  // 16-byte aligned (E a multiple of 4; a group of four is then wholly below E or wholly past it).
   __device__ static void epilogue(const Params& p, const Job& j, uint32_t ta, int row, int, int) {
     const int m = j.m0 + row;
     float* out = p.part + ((size_t)j.sub * p.d + (m < p.d ? m : 0)) * p.E;
+    const bool vec = (p.E & 3) == 0;
 #pragma unroll 1
     for (int c = 0; c < p.Ep; c += 32) {
       uint32_t v[32];
       tmem_ld32(ta + c, v);
       tmem_ld_wait();
       if (m >= p.d) continue;
+      if (vec) {
 #pragma unroll
-      for (int i = 0; i < 32; ++i)
-        if (c + i < p.E) out[c + i] = __uint_as_float(v[i]);
+        for (int q = 0; q < 8; ++q)
+          if (c + 4 * q < p.E)
+            *reinterpret_cast<float4*>(out + c + 4 * q) =
+                make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]), __uint_as_float(v[4 * q + 2]),
+                            __uint_as_float(v[4 * q + 3]));
+      } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i)
+          if (c + i < p.E) out[c + i] = __uint_as_float(v[i]);
+      }
     }
   }
   // a split with no tokens contributes zeros
