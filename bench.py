@@ -458,6 +458,7 @@ def run_workload(args, name, cfg, steps, warmup, rank, world, local, barrier, ex
         clocks.mark_end()
         barrier()
     prof = moe.moe_profile_read()
+    sm_in = moe.moe_profile_sm_clock()   # the SM clock each GEMM kernel ran at (in-kernel cycles / ns)
     moe.moe_profile_enable(False)
     clk = clocks.summary()
     ms = max_over_ranks(ev0.elapsed_time(ev1) / steps, world)
@@ -550,9 +551,17 @@ def run_workload(args, name, cfg, steps, warmup, rank, world, local, barrier, ex
         raise RuntimeError(f"layer failed in the graph replays: {moe.moe_status_string(status)}")
 
     pk = peaks()
-    # Denominator for the tensor-bound kernels: the burst cuBLAS figure when the SM clock held at
-    # its maximum through the timed region (as during the burst measurement), else the sustained one.
-    at_max = clk.get("sm_mhz") and clk.get("sm_max_mhz") and clk["sm_mhz"] >= 0.97 * clk["sm_max_mhz"]
+    # Denominator for the tensor-bound kernels: the burst cuBLAS figure when the SM clock held at its
+    # maximum (as during the burst measurement), else the sustained one (the power cap lowered it, as
+    # in the sustained cuBLAS loop).  The clock is the one the GEMM kernels ran at -- their CTAs' SM
+    # cycles over nanoseconds, time-weighted over the expert GEMMs -- since nvidia-smi's 50 ms samples
+    # of a 13 ms step miss the cap; without it, nvidia-smi's median.
+    gemm_clk = [(sm_in[n], prof[n][0]) for n in GEMMS if n in sm_in and n in prof and prof[n][0] > 0]
+    gemm_mhz = sum(m * t for m, t in gemm_clk) / sum(t for _, t in gemm_clk) if gemm_clk else None
+    clk["gemm_sm_mhz"] = gemm_mhz
+    clk["sm_mhz_in_kernels"] = {n: round(v, 1) for n, v in sm_in.items()}
+    ref_mhz = gemm_mhz if gemm_mhz else clk.get("sm_mhz")
+    at_max = bool(ref_mhz and clk.get("sm_max_mhz") and ref_mhz >= 0.97 * clk["sm_max_mhz"])
     tensor_peak = pk["tensor_burst"] if at_max else pk["tensor"]
     # the analytical resource model's roofline prediction for this step (same peaks)
     from mixture_experts_layer_10_gb300 import resource_model
@@ -562,8 +571,9 @@ def run_workload(args, name, cfg, steps, warmup, rank, world, local, barrier, ex
     model_line = {"predicted_ms": pred["step_ms"], "measured_over_predicted": ms / pred["step_ms"],
                   "calibrated_ms": cal["step_ms"], "measured_over_calibrated": ms / cal["step_ms"],
                   "memory_bytes": resource_model.memory(cfg)}
-    tensor_kind = ("bf16_tflops (burst, %s): SM clock held at max in the timed region" if at_max else
-                   "bf16_tflops_sustained (%s): SM clock below max in the timed region") % pk["source"]
+    tensor_kind = ("bf16_tflops (burst, %s): the GEMMs' SM clock held at max in the timed region" if at_max else
+                   "bf16_tflops_sustained (%s): the GEMMs' SM clock below max (power cap) in the timed region"
+                   ) % pk["source"]
     fp8_line = None
     if args.fp8 and not extra:
         fp8_line = fp8_forward(args, mc, cfg, x, W_r, b_r, Wg, Wu, Wd, dy, buf, N, tensor_peak, tensor_kind, pk, ms)
@@ -609,7 +619,8 @@ def run_workload(args, name, cfg, steps, warmup, rank, world, local, barrier, ex
         achieved = per_launch / (kernels[dom]["ms_per_step"] * steps / dom_n / 1000.0) / 1e12
         roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": tensor_peak,
                 "unit": "TFLOP/s", "frac": achieved / tensor_peak, "peak_kind": tensor_kind,
-                "work_per_launch": per_launch}
+                "frac_of_burst": achieved / pk["tensor_burst"], "frac_of_sustained": achieved / pk["tensor"],
+                "sm_mhz_in_kernel": sm_in.get(dom), "work_per_launch": per_launch}
     else:
         roof = {"kernel": dom, "bound": "hbm", "achieved": kernels[dom].get("gbs"), "peak": pk["hbm"],
                 "unit": "GB/s", "frac": kernels[dom].get("frac_of_measured_peak")}
@@ -666,7 +677,8 @@ def compact(line):
             "ms_per_step": line["ms_per_step"], "steps": line["steps"], "warmup": line["warmup"],
             "e2e": {"value": line["e2e"]["value"], "ms_per_step": line["e2e"]["ms_per_step"]},
             "cuda_graph_ms": line["cuda_graph"].get("ms_per_step"),
-            "roofline": {kk: line["roofline"].get(kk) for kk in ("kernel", "bound", "achieved", "peak", "unit", "frac")},
+            "roofline": {kk: line["roofline"].get(kk) for kk in ("kernel", "bound", "achieved", "peak", "unit", "frac",
+                                                                 "frac_of_burst", "sm_mhz_in_kernel")},
             "expert_gemm_frac": line["expert_gemm"]["frac_of_measured_peak"],
             "dispatch_combine_frac": line["dispatch_combine"]["frac_of_measured_peak"],
             "gather_frac": k.get("dispatch_gather", {}).get("frac_of_measured_peak"),
@@ -676,7 +688,8 @@ def compact(line):
             "model_measured_over_calibrated": line["model"]["measured_over_calibrated"],
             "load_max_over_mean": line["config"]["load_max_over_mean"],
             "gpu_launches": line["gpu_launches"],
-            "clocks": {kk: line["clocks"].get(kk) for kk in ("sm_mhz", "sm_max_mhz", "reasons", "samples")}}
+            "clocks": {kk: line["clocks"].get(kk) for kk in ("sm_mhz", "sm_max_mhz", "reasons", "samples",
+                                                             "gemm_sm_mhz")}}
 
 
 def main():

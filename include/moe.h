@@ -392,6 +392,15 @@ moe_status_t moe_debug_inject(void* ws, int32_t stall_block, int32_t stall_fill,
 moe_status_t moe_profile_enable(int32_t on);
 moe_status_t moe_profile_read(int32_t kernel, const char** name, double* total_ms, int32_t* launches);
 
+/* The SM clock a tensor-core GEMM kernel actually ran at: while profiling is enabled, one thread of
+ * each of its CTAs adds the SM cycles (clock64) and nanoseconds (globaltimer) from its entry to its
+ * exit on the current device; *mhz receives cycles / ns x 1000 over all its CTAs since
+ * moe_profile_enable (0 when none ran; same kernel ids as moe_profile_read).  Under the GPU's
+ * power cap this is the clock the kernel's work ran at, which nvidia-smi's periodic samples miss.
+ * moe_profile_enable touches the current device for this (MOE_ERR_CUDA if it cannot);
+ * moe_profile_sm_clock synchronises with it.  The other kernels record nothing here. */
+moe_status_t moe_profile_sm_clock(int32_t kernel, double* mhz);
+
 /* Static text for a status code. */
 const char* moe_status_string(moe_status_t status);
 

@@ -28,7 +28,7 @@ EXPORTS = ("moe_workspace_size", "moe_perm_rows", "moe_workspace_init", "moe_rou
            "moe_debug_inject", "moe_profile_enable", "moe_profile_read", "moe_status_string",
            "moe_quantize_rows_e4m3", "moe_gate_up_fp8", "moe_down_fp8", "moe_layer_fwd_fp8",
            "moe_keep_rows_for_budget", "moe_keep_rows_for_free_memory", "moe_quantize_cols_e4m3",
-           "moe_layer_bwd_fp8", "moe_saved_layout")
+           "moe_layer_bwd_fp8", "moe_saved_layout", "moe_profile_sm_clock")
 
 
 class moe_config_t(ctypes.Structure):
@@ -89,6 +89,7 @@ def load(path: str | None = None):
         "moe_check_error": [_P, _P],
         "moe_debug_inject": [_P, ctypes.c_int32, ctypes.c_int32, ctypes.c_uint64, _P],
         "moe_profile_enable": [ctypes.c_int32],
+        "moe_profile_sm_clock": [ctypes.c_int32, ctypes.POINTER(ctypes.c_double)],
         "moe_profile_read": [ctypes.c_int32, ctypes.POINTER(ctypes.c_char_p), ctypes.POINTER(ctypes.c_double),
                              ctypes.POINTER(ctypes.c_int32)],
         "moe_status_string": [ctypes.c_int],
@@ -309,6 +310,19 @@ def moe_profile_read() -> dict:
         _check(code, "moe_profile_read")
         out[name.value.decode()] = (ms.value, n.value)
         i += 1
+
+
+def moe_profile_sm_clock() -> dict:
+    """{kernel name: mean SM MHz} of the tensor-core GEMM kernels that ran since
+    moe_profile_enable (in-kernel clock64 over globaltimer; synchronises the device)."""
+    names = moe_profile_read()
+    out = {}
+    mhz = ctypes.c_double()
+    for i, name in enumerate(names):
+        _call("moe_profile_sm_clock", i, ctypes.byref(mhz))
+        if mhz.value > 0:
+            out[name] = mhz.value
+    return out
 
 
 def moe_status_string(code: int) -> str:

@@ -977,6 +977,14 @@ moe_status_t moe_profile_enable(int32_t on) {
     p.total_ms[i] = 0.0;
     p.launches[i] = 0;
   }
+  return cuda_status(clock_profile_set(p.on));
+}
+
+moe_status_t moe_profile_sm_clock(int32_t kernel, double* mhz) {
+  if (kernel < 0 || kernel >= kKCount || mhz == nullptr) return MOE_ERR_INVALID_ARG;
+  unsigned long long acc[kKCount][2];
+  MOE_CUDA(clock_profile_read(acc));
+  *mhz = acc[kernel][1] ? 1000.0 * (double)acc[kernel][0] / (double)acc[kernel][1] : 0.0;
   return MOE_OK;
 }
 

@@ -144,6 +144,10 @@ enum KernelId : int {
   kKGateUpFp8, kKQuantE4m3, kKDownFp8, kKQuantCols, kKBwdDhFp8, kKBwdFusedFp8, kKDgradXFp8, kKCount
 };
 void prof_mark(int id, cudaStream_t s, bool begin);
+// In-kernel SM clock of the GEMM kernels (gemm.cu): per kernel id, summed clock64 cycles and
+// globaltimer nanoseconds of their CTAs while enabled.
+cudaError_t clock_profile_set(bool on);
+cudaError_t clock_profile_read(unsigned long long (*acc)[2]);
 
 // Launchers implemented in the kernel translation units.  All enqueue on `s` and return the
 // launch status.

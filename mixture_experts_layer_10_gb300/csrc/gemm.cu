@@ -45,7 +45,35 @@
 #include "tmap.cuh"
 
 namespace moe {
+
+// In-kernel SM clock (profiling only): while g_clock_on is set, one thread of every CTA of the GEMM
+// kernels (lane 0 of its last warp, idle at entry) adds its clock64 cycles and globaltimer nanoseconds from entry to exit to the kernel's
+// pair of sums, so cycles / ns is the mean SM clock over the CTAs' lifetimes -- the clock the
+// kernel actually ran at, which a power cap lowers well below what a 50 ms nvidia-smi sample sees.
+__device__ int g_clock_on;
+__device__ unsigned long long g_clock_acc[kKCount][2];
+
 namespace {
+
+struct ClockSpan {
+  unsigned long long c0 = 0, n0 = 0;
+  bool on = false;
+  __device__ void start() {
+    on = g_clock_on != 0;
+    if (on) {
+      asm volatile("mov.u64 %0, %%clock64;" : "=l"(c0));
+      n0 = global_ns();
+    }
+  }
+  __device__ void stop(int id) {
+    if (!on) return;
+    unsigned long long c1;
+    asm volatile("mov.u64 %0, %%clock64;" : "=l"(c1));
+    const unsigned long long n1 = global_ns();
+    atomicAdd(&g_clock_acc[id][0], c1 - c0);
+    atomicAdd(&g_clock_acc[id][1], n1 - n0);
+  }
+};
 
 constexpr int kBM = 128;
 constexpr int kBK = 64;
@@ -1506,6 +1534,8 @@ __global__ void __launch_bounds__(threads_of<P>(), 1) gemm_kernel(const __grid_c
   SegSmem& segs = *reinterpret_cast<SegSmem*>(epi + epi_bytes<P>() + 256);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  ClockSpan span;
+  if (threadIdx.x == blockDim.x - 32) span.start();   // an epilogue warp: off the setup's path
   load_segs(segs, p.tabs);
   if (threadIdx.x == 0) {
     for (int s = 0; s < P::kStages; ++s) {
@@ -1647,6 +1677,7 @@ __global__ void __launch_bounds__(threads_of<P>(), 1) gemm_kernel(const __grid_c
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == blockDim.x - 32) span.stop(P::kId);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, P::kTmemCols);
@@ -1690,6 +1721,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<P>(), 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = (int)cluster_rank();
   const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
+  ClockSpan span;
+  if (threadIdx.x == blockDim.x - 32) span.start();   // an epilogue warp: off the setup's path
   load_segs(segs, p.tabs);
   if (threadIdx.x == 0) {
     for (int s = 0; s < P::kStages; ++s) {
@@ -1963,6 +1996,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<P>(), 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (threadIdx.x == blockDim.x - 32) span.stop(P::kId);
   cluster_sync();
   if (warp == 1) {
     tc_fence_after();
@@ -2338,6 +2372,20 @@ cudaError_t launch_router_dx(const Cfg& c, const Layout& L, const RouterDxArgs& 
   p.hdr = a.hdr;
   p.tabs = a.tabs;
   return launch<RouterDx>(p, s);
+}
+
+// In-kernel clock sums: set or clear the switch and zero the sums (on the current device), and
+// read them back; both synchronise with the device.
+cudaError_t clock_profile_set(bool on) {
+  const int v = on ? 1 : 0;
+  static const unsigned long long zero[kKCount][2] = {};
+  cudaError_t e = cudaMemcpyToSymbol(g_clock_acc, zero, sizeof(zero));
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_clock_on, &v, sizeof(v));
+  return e;
+}
+
+cudaError_t clock_profile_read(unsigned long long (*acc)[2]) {
+  return cudaMemcpyFromSymbol(acc, g_clock_acc, sizeof(unsigned long long) * 2 * kKCount);
 }
 
 }  // namespace moe
