@@ -186,8 +186,8 @@ def fp8_forward(args, mc, cfg, x, W_r, b_r, Wg, Wu, Wd, dy, buf, N, tensor_peak,
     # the resource model's roofline for both forwards, on the same peaks
     from mixture_experts_layer_10_gb300 import resource_model
     n_routed = N - cfg["S"] * T
-    p16 = resource_model.predict_forward_ms(cfg, tensor_peak, pk["hbm"], N=n_routed)["step_ms"]
-    p8 = resource_model.predict_forward_ms(cfg, tensor_peak, pk["hbm"], N=n_routed, fp8=True)["step_ms"]
+    p16 = resource_model.predict_forward_ms(cfg, pk["tensor_burst"], pk["hbm"], N=n_routed)["step_ms"]
+    p8 = resource_model.predict_forward_ms(cfg, pk["tensor_burst"], pk["hbm"], N=n_routed, fp8=True)["step_ms"]
     return {"metric": "forward tokens/s (e4m3 expert GEMMs)", "value": T / (ms8 / 1000.0), "fwd_ms": ms8,
             "bf16_fwd_ms": ms16, "speedup_vs_bf16_fwd": ms16 / ms8,
             "step": {"metric": METRIC + " (e4m3 expert GEMMs)", "value": T / (ms8_step / 1000.0),
@@ -563,10 +563,11 @@ def run_workload(args, name, cfg, steps, warmup, rank, world, local, barrier, ex
     ref_mhz = gemm_mhz if gemm_mhz else clk.get("sm_mhz")
     at_max = bool(ref_mhz and clk.get("sm_max_mhz") and ref_mhz >= 0.97 * clk["sm_max_mhz"])
     tensor_peak = pk["tensor_burst"] if at_max else pk["tensor"]
-    # the analytical resource model's roofline prediction for this step (same peaks)
+    # the analytical resource model's roofline prediction for this step; the model's tensor rate is
+    # the burst figure whatever the regime (its GEMM efficiency was calibrated against it)
     from mixture_experts_layer_10_gb300 import resource_model
-    pred = resource_model.predict_ms(cfg, tensor_peak, pk["hbm"], N=n_kept, kept_rows=kept_real)
-    cal = resource_model.predict_ms_calibrated(cfg, tensor_peak, pk["hbm"], N=n_kept, kept_rows=kept_real,
+    pred = resource_model.predict_ms(cfg, pk["tensor_burst"], pk["hbm"], N=n_kept, kept_rows=kept_real)
+    cal = resource_model.predict_ms_calibrated(cfg, pk["tensor_burst"], pk["hbm"], N=n_kept, kept_rows=kept_real,
                                                counts=[int(c) for c in counts_h])
     model_line = {"predicted_ms": pred["step_ms"], "measured_over_predicted": ms / pred["step_ms"],
                   "calibrated_ms": cal["step_ms"], "measured_over_calibrated": ms / cal["step_ms"],
