@@ -28,6 +28,9 @@ CASES = {
     # the fp32 SIMT router: more than 128 experts, and more than 8 experts per token
     "router_simt_e160": dict(T=300, d=128, E=160, k=4, f=64, S=0, renorm=0, cf=0.0, zipf=True),
     "router_simt_k10": dict(T=200, d=192, E=24, k=10, f=64, S=0, renorm=1, cf=0.0, zipf=False),
+    # more slots per token than a warp has lanes (k = 40): the layer backward's dlogits then walks
+    # each token's slots in every lane instead of holding one slot per lane
+    "router_simt_k40": dict(T=70, d=128, E=64, k=40, f=64, S=0, renorm=0, cf=0.0, zipf=False),
     # limits: the most routed experts (256), and the most shared experts (8) at the narrowest widths
     "max_experts": dict(T=700, d=64, E=256, k=2, f=64, S=0, renorm=0, cf=0.0, zipf=False),
     "max_shared": dict(T=300, d=64, E=4, k=1, f=64, S=8, renorm=1, cf=0.0, zipf=False),
