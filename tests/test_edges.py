@@ -67,7 +67,6 @@ def run_steps(moe, T, d, f, E, k, S, idx, gates, cf=0.0, seed=0):
     ref_W = [np.zeros((G, f, d)), np.zeros((G, f, d)), np.zeros((G, d, f))]
     ref_dg = np.zeros((T, k))
     ref_dxp, got_dxp = [], []
-    dxp = from_dev_bf16(dx_perm)
     for g in range(G):
         W = tuple(oracle.bf16_to_f64(inp[n][g]) for n in ("W_gate", "W_up", "W_down"))
         if g < E:
@@ -82,7 +81,7 @@ def run_steps(moe, T, d, f, E, k, S, idx, gates, cf=0.0, seed=0):
         dxr, a, b, c, dg = oracle.expert_backward(x[toks], dy[toks], gw, *W)
         ref_W[0][g], ref_W[1][g], ref_W[2][g] = a, b, c
         ref_dxp.append(dxr)
-        got_dxp.append(dxp[P[g]:P[g] + kept[g]])
+        got_dxp.append(from_dev_bf16(dx_perm[P[g]:P[g] + kept[g]]))   # rows past kept hold no values
         if g < E:
             o_slot[toks, js] = o
             ref_dg[toks, js] = dg
