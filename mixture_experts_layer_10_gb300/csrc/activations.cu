@@ -76,13 +76,28 @@ __global__ void __launch_bounds__(32 * kRowsPerBlock) swiglu_bwd_kept_kernel(
 
 // FP8 rows (the quantisation step of the e4m3 expert GEMMs): per row, amax over the row, scale =
 // amax / 448 in fp32 (1 for an all-zero row), codes = e4m3(v / scale) rounded to nearest even and
-// saturated.  A block owns a row at a time and keeps it in registers (up to kQuantV 16-byte vectors
-// of eight values per thread) between the amax and the encode, so each value crosses HBM once in
-// each direction.  With the dispatch tables given, rows past the padded expert rows of this step
-// (tb->total_rows) are skipped.
-constexpr int kQuantV = 8;
+// saturated.  A block owns a row at a time and keeps it in registers (NV 16-byte vectors of eight
+// values per thread) between the amax and the encode, so each value crosses HBM once in each
+// direction; the block's next row is loaded while the current one is reduced and encoded, so two
+// rows a block are in flight (one row a block left the kernel at about half the copy bandwidth).
+// With the dispatch tables given, rows past the padded expert rows of this step (tb->total_rows)
+// are skipped.
+constexpr int kQuantV = 8;   // the most vectors a thread holds (512 threads: 32768 values a row)
 
-template <int kThreads>
+template <int NV>
+__device__ __forceinline__ void load_row(const uint16_t* __restrict__ src, int cols1, const uint16_t* __restrict__ src2,
+                                         int cols2, int64_t r, int nvec1, int nvec, int nthreads, uint4 (&v)[NV]) {
+  const uint4* row = reinterpret_cast<const uint4*>(src + r * cols1);
+  const uint4* row2 = reinterpret_cast<const uint4*>(src2 + r * cols2);
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int q = threadIdx.x + i * nthreads;
+    v[i] = make_uint4(0u, 0u, 0u, 0u);
+    if (q < nvec) v[i] = q < nvec1 ? row[q] : row2[q - nvec1];
+  }
+}
+
+template <int kThreads, int NV>
 __global__ void __launch_bounds__(kThreads) quantize_rows_e4m3_kernel(const uint16_t* __restrict__ src, int cols1,
                                                                       const uint16_t* __restrict__ src2, int cols2,
                                                                       int64_t rows, uint8_t* __restrict__ codes,
@@ -96,19 +111,16 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_e4m3_kernel(const uint
   const int cols = cols1 + cols2;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   int buf = 0;
+  uint4 v[NV], nx[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) nx[i] = make_uint4(0u, 0u, 0u, 0u);
+  if ((int64_t)blockIdx.x < rows) load_row<NV>(src, cols1, src2, cols2, blockIdx.x, nvec1, nvec, kThreads, v);
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x, buf ^= 1) {
-    const uint4* row = reinterpret_cast<const uint4*>(src + r * cols1);
-    const uint4* row2 = reinterpret_cast<const uint4*>(src2 + r * cols2);
-    uint4 v[kQuantV];
+    const int64_t rn = r + gridDim.x;
+    if (rn < rows) load_row<NV>(src, cols1, src2, cols2, rn, nvec1, nvec, kThreads, nx);   // the next row, early
     float amax = 0.f;
 #pragma unroll
-    for (int i = 0; i < kQuantV; ++i) {
-      const int q = threadIdx.x + i * kThreads;
-      if (q < nvec) {
-        v[i] = q < nvec1 ? row[q] : row2[q - nvec1];
-        amax = fmaxf(amax, amax8_bf16(v[i]));
-      }
-    }
+    for (int i = 0; i < NV; ++i) amax = fmaxf(amax, amax8_bf16(v[i]));   // zero vectors past the row
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     if (kWarps > 1) {
@@ -123,27 +135,40 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_e4m3_kernel(const uint
     if (e4m3_recip_ok(scale)) {   // the same branch for the whole block
       const float y = __frcp_rn(scale);
 #pragma unroll
-      for (int i = 0; i < kQuantV; ++i) {
+      for (int i = 0; i < NV; ++i) {
         const int q = threadIdx.x + i * kThreads;
         if (q < nvec) out[q] = encode8_e4m3<true>(v[i], scale, y);
       }
     } else {
 #pragma unroll
-      for (int i = 0; i < kQuantV; ++i) {
+      for (int i = 0; i < NV; ++i) {
         const int q = threadIdx.x + i * kThreads;
         if (q < nvec) out[q] = encode8_e4m3<false>(v[i], scale, 0.f);
       }
     }
+#pragma unroll
+    for (int i = 0; i < NV; ++i) v[i] = nx[i];
   }
 }
 
+template <int kThreads, int NV>
+void launch_quantize_nv(const uint16_t* src, int cols1, const uint16_t* src2, int cols2, int64_t rows, uint8_t* codes,
+                        float* scales, const Tables* tabs, cudaStream_t s) {
+  const int per_sm = std::min(32, 2048 / kThreads);
+  const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)num_sms() * per_sm));
+  quantize_rows_e4m3_kernel<kThreads, NV><<<(int)blocks, kThreads, 0, s>>>(src, cols1, src2, cols2, rows, codes,
+                                                                          scales, tabs);
+}
+
+// vectors a thread holds: the row's vectors over the block's threads, rounded up to 1, 2, 4 or 8
 template <int kThreads>
 void launch_quantize(const uint16_t* src, int cols1, const uint16_t* src2, int cols2, int64_t rows, uint8_t* codes,
                      float* scales, const Tables* tabs, cudaStream_t s) {
-  const int per_sm = std::min(32, 2048 / kThreads);
-  const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>(rows, (int64_t)num_sms() * per_sm));
-  quantize_rows_e4m3_kernel<kThreads><<<(int)blocks, kThreads, 0, s>>>(src, cols1, src2, cols2, rows, codes, scales,
-                                                                      tabs);
+  const int nv = ((cols1 + cols2) / 8 + kThreads - 1) / kThreads;
+  if (nv <= 1) launch_quantize_nv<kThreads, 1>(src, cols1, src2, cols2, rows, codes, scales, tabs, s);
+  else if (nv <= 2) launch_quantize_nv<kThreads, 2>(src, cols1, src2, cols2, rows, codes, scales, tabs, s);
+  else if (nv <= 4) launch_quantize_nv<kThreads, 4>(src, cols1, src2, cols2, rows, codes, scales, tabs, s);
+  else launch_quantize_nv<kThreads, kQuantV>(src, cols1, src2, cols2, rows, codes, scales, tabs, s);
 }
 
 // ---- columns: per-column e4m3 codes written transposed (the K-major operand whose rows are the
