@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kThreads) router_dlogits_kernel(RouterBwdArgs 
 }
 
 // Router backward, part 1, from the logits the layer forward kept: no second pass over x.  Per
-// token, with s = sum_j dg_j g_j (in slot order):
+// token, with s = sum_j dg_j g_j:
 //   gates not renormalised: p = softmax(logits), dl_e = p_e (dg_slot(e) [e selected] - s);
 //   renormalised:           dl_{idx_j} = g_j (dg_j - s), 0 elsewhere (the logits are not read).
 // Outputs: dl in fp32 [T, E], as the bf16 operand row [T, Ep] of the dW_r and dx products (zero
@@ -407,12 +407,15 @@ __global__ void __launch_bounds__(kThreads) router_dlogits_saved_kernel(RouterBw
 #pragma unroll
     for (int i = 0; i < NV; ++i) dsel[i] = 0.f;
     if (slots_in_lanes) {
-      for (int j = 0; j < k; ++j) s += __shfl_sync(0xffffffffu, sdg[ps] * sg[ps], g0 + j);
+      // s by an xor tree inside the group (lanes past k hold zeros); then each slot's share of dl,
+      // formed by the lane that holds it, goes to every lane of the group with its expert
+      s = sdg[ps] * sg[ps];
+#pragma unroll
+      for (int off = G / 2; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+      const float vmine = renorm ? sg[ps] * (sdg[ps] - s) : sdg[ps];
       for (int j = 0; j < k; ++j) {
         const int e = __shfl_sync(0xffffffffu, sid[ps], g0 + j);
-        const float dg = __shfl_sync(0xffffffffu, sdg[ps], g0 + j);
-        const float g = __shfl_sync(0xffffffffu, sg[ps], g0 + j);
-        const float v = renorm ? g * (dg - s) : dg;
+        const float v = __shfl_sync(0xffffffffu, vmine, g0 + j);
 #pragma unroll
         for (int i = 0; i < NV; ++i)
           if (e == li + G * i) dsel[i] += v;
@@ -438,16 +441,19 @@ __global__ void __launch_bounds__(kThreads) router_dlogits_saved_kernel(RouterBw
       for (int i = 0; i < NV; ++i) m = fmaxf(m, lv[ps][i]);
 #pragma unroll
       for (int off = G / 2; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      // the fast exponential and one reciprocal a token: the kernel is bound by instruction issue,
+      // and dl feeds bf16 products and fp32 sums held to the bf16 gradient rule
       float ex[NV], z = 0.f;
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
-        ex[i] = li + G * i < E ? expf(lv[ps][i] - m) : 0.f;
+        ex[i] = li + G * i < E ? __expf(lv[ps][i] - m) : 0.f;
         z += ex[i];
       }
 #pragma unroll
       for (int off = G / 2; off > 0; off >>= 1) z += __shfl_xor_sync(0xffffffffu, z, off);
+      const float rz = 1.f / z;
 #pragma unroll
-      for (int i = 0; i < NV; ++i) dl[i] = li + G * i < E ? ex[i] / z * (dsel[i] - s) : 0.f;
+      for (int i = 0; i < NV; ++i) dl[i] = li + G * i < E ? ex[i] * rz * (dsel[i] - s) : 0.f;
     }
     if (!live) continue;
 #pragma unroll
