@@ -228,12 +228,14 @@ moe_status_t cuda_status(cudaError_t e) {
 
 namespace {
 
-const char* const kKernelNames[kKCount] = {
+const char* const kKernelNames[] = {
     "route_fwd", "dispatch_scan", "dispatch_gather", "gemm_gate_up_swiglu", "gemm_down",
     "combine", "gemm_bwd_recompute_swiglu", "gemm_wgrad", "gemm_dgrad_x", "dgates_reduce",
     "router_dlogits", "router_dwr", "router_reduce", "combine_bwd", "gemm_bwd_dgrad_down",
     "gemm_router_dx", "swiglu_bwd_kept", "gemm_gate_up_fp8", "quantize_e4m3", "gemm_down_fp8",
-    "quantize_cols_e4m3", "gemm_bwd_dgrad_down_fp8", "gemm_bwd_recompute_swiglu_fp8", "gemm_dgrad_x_fp8"};
+    "quantize_cols_e4m3", "gemm_bwd_dgrad_down_fp8", "gemm_bwd_recompute_swiglu_fp8", "gemm_dgrad_x_fp8",
+    "router_split_wr", "to_bf16_rows"};
+static_assert(sizeof(kKernelNames) / sizeof(kKernelNames[0]) == kKCount, "a name for every kernel id");
 
 struct Profiler {
   std::mutex mu;

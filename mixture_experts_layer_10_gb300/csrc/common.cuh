@@ -141,7 +141,8 @@ moe_status_t cuda_status(cudaError_t e);          // MOE_OK or MOE_ERR_CUDA (cle
 enum KernelId : int {
   kKRoute = 0, kKScan, kKGather, kKGateUp, kKDown, kKCombine, kKBwdFused, kKWgrad, kKDgradX,
   kKDgates, kKRouterDlogits, kKRouterDwr, kKRouterReduce, kKCombineBwd, kKBwdDh, kKRouterDx, kKSwigluKept,
-  kKGateUpFp8, kKQuantE4m3, kKDownFp8, kKQuantCols, kKBwdDhFp8, kKBwdFusedFp8, kKDgradXFp8, kKCount
+  kKGateUpFp8, kKQuantE4m3, kKDownFp8, kKQuantCols, kKBwdDhFp8, kKBwdFusedFp8, kKDgradXFp8, kKSplitWr,
+  kKToBf16, kKCount
 };
 void prof_mark(int id, cudaStream_t s, bool begin);
 // In-kernel SM clock of the GEMM kernels (gemm.cu): per kernel id, summed clock64 cycles and

@@ -650,14 +650,18 @@ bool router_bwd_on_tensor_cores(const Cfg& c) { return router_on_tensor_cores(c)
 
 cudaError_t launch_split_wr(const float* W_r, int d, int E, int Ep, uint16_t* wr3, cudaStream_t s) {
   const dim3 grid((d + 31) / 32, (Ep + 31) / 32);
+  prof_mark(kKSplitWr, s, true);
   split_wr_kernel<<<grid, 256, 0, s>>>(W_r, d, E, Ep, wr3);
+  prof_mark(kKSplitWr, s, false);
   return cudaGetLastError();
 }
 
 cudaError_t launch_to_bf16_rows(const float* src, int rows, int cols, int ld, uint16_t* dst, cudaStream_t s) {
   const size_t n = (size_t)rows * ld;
   const int blocks = (int)std::max<size_t>(1, std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 8));
+  prof_mark(kKToBf16, s, true);
   to_bf16_rows_kernel<<<blocks, 256, 0, s>>>(src, rows, cols, ld, dst);
+  prof_mark(kKToBf16, s, false);
   return cudaGetLastError();
 }
 

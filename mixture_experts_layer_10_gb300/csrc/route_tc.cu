@@ -513,7 +513,9 @@ cudaError_t launch_stream(const Cfg& c, const Layout& L, const RouterStreamArgs&
   const int ncnt = pl.ntiles * 4;
   const size_t n = (size_t)Nb * c.d + ncnt;
   const int blocks = (int)std::max<size_t>(1, std::min<size_t>((n + 255) / 256, (size_t)num_sms() * 4));
+  prof_mark(kKSplitWr, s, true);
   split_wr_stack_kernel<<<blocks, 256, 0, s>>>(a.W_r, c.d, c.E, EB, Nb, a.wstack, a.cnt, ncnt);
+  prof_mark(kKSplitWr, s, false);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   switch (EB) {
