@@ -354,9 +354,9 @@ __global__ void __launch_bounds__(kThreads) router_dlogits_kernel(RouterBwdArgs 
 // past E), and one db partial per 32 tokens.  A block takes 32 tokens, four per warp; G = min(32,
 // EB) lanes share a token, lane i of a group holding experts i, i + G, ... and (k <= G) slot i of
 // the token; the group's max and sum are xor shuffles within it.  Every load of a warp's four
-// tokens is issued before the arithmetic of the first (the kernel is bound by memory latency).
-// db: each lane adds its tokens in order, then one thread per expert adds the groups in
-// (warp, group) order -- a fixed order.
+// tokens is issued before the arithmetic of the first, so their latencies overlap; what remains
+// bounds the kernel by instruction issue.  db: each lane adds its tokens in order, then one thread
+// per expert adds the groups in (warp, group) order -- a fixed order.
 template <int EB>
 __global__ void __launch_bounds__(kThreads) router_dlogits_saved_kernel(RouterBwdArgs a, const float* __restrict__ logits,
                                                                         uint16_t* __restrict__ dl_bf16, int T, int E,
