@@ -47,9 +47,10 @@
 namespace moe {
 
 // In-kernel SM clock (profiling only): while g_clock_on is set, one thread of every CTA of the GEMM
-// kernels (lane 0 of its last warp, idle at entry) adds its clock64 cycles and globaltimer nanoseconds from entry to exit to the kernel's
-// pair of sums, so cycles / ns is the mean SM clock over the CTAs' lifetimes -- the clock the
-// kernel actually ran at, which a power cap lowers well below what a 50 ms nvidia-smi sample sees.
+// kernels (lane 0 of its last warp, not the thread that sets the kernel up) adds its clock64 cycles
+// and globaltimer nanoseconds from entry to exit to the kernel's pair of sums, so cycles / ns is the
+// mean SM clock over the CTAs' lifetimes -- the clock the kernel actually ran at, which a power cap
+// lowers well below what a 50 ms nvidia-smi sample sees.
 __device__ int g_clock_on;
 __device__ unsigned long long g_clock_acc[kKCount][2];
 
@@ -1535,7 +1536,7 @@ __global__ void __launch_bounds__(threads_of<P>(), 1) gemm_kernel(const __grid_c
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   ClockSpan span;
-  if (threadIdx.x == blockDim.x - 32) span.start();   // an epilogue warp: off the setup's path
+  if (threadIdx.x == blockDim.x - 32) span.start();   // the last warp: off thread 0's setup path
   load_segs(segs, p.tabs);
   if (threadIdx.x == 0) {
     for (int s = 0; s < P::kStages; ++s) {
@@ -1722,7 +1723,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(threads_of<P>(), 1)
   const int rank = (int)cluster_rank();
   const int pair = (int)(blockIdx.x >> 1), npairs = (int)(gridDim.x >> 1);
   ClockSpan span;
-  if (threadIdx.x == blockDim.x - 32) span.start();   // an epilogue warp: off the setup's path
+  if (threadIdx.x == blockDim.x - 32) span.start();   // the last warp: off thread 0's setup path
   load_segs(segs, p.tabs);
   if (threadIdx.x == 0) {
     for (int s = 0; s < P::kStages; ++s) {
