@@ -1299,7 +1299,8 @@ struct RouterLogits : PolicyDefaults {
 #pragma unroll
       for (int q = 0; q < 8; ++q)
         if (c + 4 * q < p.E)
-          *reinterpret_cast<float4*>(row + c + 4 * q) = make_float4(l[4 * q], l[4 * q + 1], l[4 * q + 2], l[4 * q + 3]);
+          *reinterpret_cast<float4*>(row + c + 4 * q) =
+              make_float4(l[4 * q], l[4 * q + 1], l[4 * q + 2], l[4 * q + 3]);
     } else {
 #pragma unroll
       for (int i = 0; i < 32; ++i)

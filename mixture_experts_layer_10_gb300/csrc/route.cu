@@ -358,9 +358,9 @@ __global__ void __launch_bounds__(kThreads) router_dlogits_kernel(RouterBwdArgs 
 // bounds the kernel by instruction issue.  db: each lane adds its tokens in order, then one thread
 // per expert adds the groups in (warp, group) order -- a fixed order.
 template <int EB>
-__global__ void __launch_bounds__(kThreads) router_dlogits_saved_kernel(RouterBwdArgs a, const float* __restrict__ logits,
-                                                                        uint16_t* __restrict__ dl_bf16, int T, int E,
-                                                                        int Ep, int k, int renorm) {
+__global__ void __launch_bounds__(kThreads)
+    router_dlogits_saved_kernel(RouterBwdArgs a, const float* __restrict__ logits, uint16_t* __restrict__ dl_bf16,
+                                int T, int E, int Ep, int k, int renorm) {
   constexpr int G = EB < 32 ? EB : 32;   // lanes per token
   constexpr int TPW = 32 / G;            // tokens per warp pass
   constexpr int NV = EB / G;             // experts per lane
