@@ -134,3 +134,18 @@ def test_a_library_that_does_not_load_raises(tmp_path, monkeypatch):
     monkeypatch.setattr(moe, "_lib", None)
     with pytest.raises(OSError):
         moe.load(str(bad))
+
+
+def test_saved_layout_and_clock_query_arguments(lib):
+    """The saved-layout query takes nullable outputs and rejects a bad configuration; the in-kernel
+    clock query rejects a kernel id out of range or a missing output before touching a device."""
+    c = moe.config(T=64, d=128, f=128, E=8, k=2)
+    assert lib.moe_saved_layout(ctypes.byref(c), None, None, None, None) == 0
+    bad = moe.config(T=16, d=100, f=256, E=8, k=2)
+    out = ctypes.c_size_t()
+    assert lib.moe_saved_layout(ctypes.byref(bad), ctypes.byref(out), None, None, None) == 1
+    mhz = ctypes.c_double()
+    n = len(moe.moe_profile_read())
+    assert lib.moe_profile_sm_clock(-1, ctypes.byref(mhz)) == 1
+    assert lib.moe_profile_sm_clock(n, ctypes.byref(mhz)) == 1
+    assert lib.moe_profile_sm_clock(0, None) == 1
