@@ -215,3 +215,44 @@ def test_gather_in_gemm_against_oracle(moe, name):
     c = dict(c, gather_in_gemm=1)
     out, buf = run_layer(moe, c, inp)
     check_layer(moe, c, inp, L, out, buf)
+
+
+# The layer backward takes the router's softmax from the logits the forward kept in `saved`: a
+# constant added to them changes nothing (softmax is shift-invariant), and equal logits give the
+# gradients of a uniform p.  Both runs start from the oracle's assignment written into `saved`.
+def test_backward_reads_the_kept_logits(moe):
+    import oracle
+    c, inp, L = case("ragged_mixtral")
+    mc = moe.config_from(c)
+    buf = moe.Buffers.allocate(mc)
+    T, d, f, E, k = c["T"], c["d"], c["f"], c["E"], c["k"]
+    R = L.routing()
+    g = L.backward()
+    x, Wg, Wu, Wd, dy = (to_dev_bf16(inp[n]) for n in ("x", "W_gate", "W_up", "W_down", "dy"))
+    W_r = to_dev(inp["W_r"])
+    idx_v, gates_v, logits_v = buf.saved_views()
+    gates32 = R.gates.astype(np.float32)
+
+    def backward(logits):
+        idx_v.copy_(to_dev(R.idx.astype(np.int32)))
+        gates_v.copy_(to_dev(gates32))
+        logits_v.copy_(to_dev(logits.astype(np.float32)))
+        out = [torch.empty(d, E, dtype=torch.float32, device="cuda"), torch.empty(T, d, dtype=torch.bfloat16,
+                                                                                  device="cuda")]
+        dW = [torch.empty(E, f, d, dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+        dWd = torch.empty(E, d, f, dtype=torch.bfloat16, device="cuda")
+        moe.moe_layer_bwd(mc, x, W_r, None, Wg, Wu, Wd, buf.saved, dy, out[1], out[0], None, dW[0], dW[1], dWd,
+                          buf.ws)
+        assert moe.moe_check_error(buf.ws) == 0
+        return from_dev(out[0]).astype(np.float64)
+
+    dw_kept = backward(R.logits)
+    check_close("dW_r", dw_kept, g["dW_r"])
+    dw_shift = backward(R.logits + 5.0)
+    assert np.max(np.abs(dw_shift - dw_kept)) <= 1e-3 * np.max(np.abs(dw_kept))
+    dw_flat = backward(np.zeros((T, E)))
+    dl = oracle.router_backward_logits(np.full((T, E), 1.0 / E), R.idx, gates32.astype(np.float64), g["dgates"],
+                                       False)
+    ref = oracle.bf16_to_f64(inp["x"]).T @ dl
+    check_close("dW_r (uniform p)", dw_flat, ref)
+    assert np.max(np.abs(dw_flat - dw_kept)) > 0.1 * np.max(np.abs(dw_kept))
